@@ -1,0 +1,331 @@
+// Prepare kernel (Gated DeltaNet, scalar gate): everything of a chunk that does not depend
+// on the carried state, for two chunks per CTA.
+//
+// Per chunk (the eager reference `torch_chunk_gated_delta_rule`, hyper-parallel GDN Diff
+// Coverage page, steps before its chunk loop):
+//   r_q, r_k   = rsqrt(|q|^2 + 1e-6), rsqrt(|k|^2 + 1e-6)            (`_l2norm`)
+//   G          = chunk-local cumulative gate                          (`g.cumsum(-1)`)
+//   L_ij       = beta_i r_i r_j (k_i . k_j) exp(G_i - G_j), i > j     (`attn`, strictly lower)
+//   A          = (I + L)^-1                                           (row loop + identity)
+//   W          = A diag(beta exp(G) r_k) k                            (`k_cumdecay`)
+//   U          = A diag(beta) v                                       (`value`)
+//   Aqk_ij     = scale r_q,i r_k,j (q_i . k_j) exp(G_i - G_j), i >= j (chunk-loop `attn`)
+//   Qt         = scale r_q exp(G) q ;  KtT = (r_k exp(G_last - G) k)^T ; gam = exp(G_last)
+//
+// GB300 mapping. The two chunks of a CTA are stacked into one 128-row tile so every
+// tensor-core product is a 128-lane tcgen05 MMA: the Gram products K K^T and Q K^T
+// (raw bf16 tiles straight from TMA, so the operands are exact) land in TMEM and only their
+// two diagonal 64x64 blocks are used; W and U are block-diagonal (A) times the raw k / v tile
+// (MN-major B operand). L2-norm factors and decays are applied to the fp32 MMA results, never
+// to the bf16 operands. The unit-lower-triangular inverse runs in fp32 registers, one column
+// per thread (forward substitution, the same recurrence as the page's row loop).
+#include "common.cuh"
+#include "umma.cuh"
+
+namespace gdn {
+
+namespace {
+
+constexpr int kThreads = 128;
+constexpr uint32_t kPanel = 16384;  // 128 rows x 128 B
+constexpr uint32_t kOffQ = 0, kOffK = 32768, kOffV = 65536, kOffA1 = 98304, kOffA2 = 131072,
+                   kOffL = 163840, kSmemBytes = 196608 + 1024;
+
+__device__ __forceinline__ uint8_t* align1k(uint8_t* p) {
+  return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
+}
+
+__device__ __forceinline__ void bf16x8_to_f32(const uint4& u, float* f) {
+  const __nv_bfloat162* b = reinterpret_cast<const __nv_bfloat162*>(&u);
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    const float2 t = __bfloat1622float2(b[e]);
+    f[2 * e] = t.x;
+    f[2 * e + 1] = t.y;
+  }
+}
+
+// Column `c` of (I + L)^-1 for a 64x64 strictly lower L (row-major fp32 in shared memory):
+// x_c = 1, x_r = -sum_{c <= j < r} L[r][j] x_j for r > c, x_r = 0 for r < c.
+__device__ __forceinline__ void unit_lower_inverse_column(const float* __restrict__ L, int c, float* x) {
+#pragma unroll
+  for (int r = 0; r < kC; ++r) {
+    float acc = 0.f;
+    const float4* row4 = reinterpret_cast<const float4*>(L + r * kC);
+#pragma unroll
+    for (int j4 = 0; j4 < (r + 3) / 4; ++j4) {
+      const float4 l = row4[j4];
+      acc = fmaf(l.x, x[4 * j4], acc);
+      if (4 * j4 + 1 < r) acc = fmaf(l.y, x[4 * j4 + 1], acc);
+      if (4 * j4 + 2 < r) acc = fmaf(l.z, x[4 * j4 + 2], acc);
+      if (4 * j4 + 3 < r) acc = fmaf(l.w, x[4 * j4 + 3], acc);
+    }
+    x[r] = (r < c) ? 0.f : ((r == c) ? 1.f : -acc);
+  }
+}
+
+}  // namespace
+
+__global__ void __launch_bounds__(kThreads, 1)
+    k_prep_gdn(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
+               const __grid_constant__ CUtensorMap mv, const PrepParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = align1k(smem_raw);
+  uint8_t* sQ = sm + kOffQ;
+  uint8_t* sK = sm + kOffK;
+  uint8_t* sV = sm + kOffV;
+  uint8_t* sA1 = sm + kOffA1;
+  uint8_t* sA2 = sm + kOffA2;
+  float* sL = reinterpret_cast<float*>(sm + kOffL);
+  __shared__ uint64_t bar_tma, bar_mma;
+  __shared__ uint32_t tslot;
+  __shared__ int abort_flag;
+  __shared__ float s_g[kThreads], s_b[kThreads], s_rk[kThreads], s_G[kThreads];
+  __shared__ int4 s_chunk[2];
+
+  const int tid = threadIdx.x, warp = tid >> 5;
+  const int h = blockIdx.y, pair = blockIdx.x, H = p.H;
+  const int blk = tid >> 6, il = tid & 63;
+
+  if (tid < 2) {
+    const int c = 2 * pair + tid;
+    s_chunk[tid] = c < p.NC ? p.chunks[c] : make_int4(0, 0, 0, 0);
+  }
+  if (warp == 0) tmem_alloc(&tslot, 256);
+  if (tid == 0) {
+    abort_flag = 0;
+    mbar_init(&bar_tma, 1);
+    mbar_init(&bar_mma, 1);
+    fence_mbar_init();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tb = tslot;
+  const uint32_t lane_base = tmem_lane_base(warp);
+  const int4 ch = s_chunk[blk];
+  const int len = ch.y;
+  const int c_idx = 2 * pair + blk;
+  const bool valid = il < len;
+  const int row = ch.x + il;
+
+  if (tid == 0) {
+    const int nexist = (s_chunk[0].y > 0) + (s_chunk[1].y > 0);
+    mbar_expect_tx(&bar_tma, uint32_t(nexist) * 6u * 8192u);
+    for (int b = 0; b < 2; ++b) {
+      if (s_chunk[b].y <= 0) continue;
+      for (int pp = 0; pp < 2; ++pp) {
+        const int x = h * kD + 64 * pp, y = s_chunk[b].x;
+        tma_load_2d(sQ + pp * kPanel + b * 8192, &mq, x, y, &bar_tma);
+        tma_load_2d(sK + pp * kPanel + b * 8192, &mk, x, y, &bar_tma);
+        tma_load_2d(sV + pp * kPanel + b * 8192, &mv, x, y, &bar_tma);
+      }
+    }
+  }
+  // A missing second chunk leaves its tile rows unloaded: zero them so that the products
+  // with zero coefficients stay exactly zero.
+  if (len == 0) {
+#pragma unroll
+    for (int c16 = 0; c16 < 16; ++c16) {
+      const uint32_t off = sw128_offset(tid, c16 * 8, 128, 2);
+      *reinterpret_cast<uint4*>(sQ + off) = make_uint4(0, 0, 0, 0);
+      *reinterpret_cast<uint4*>(sK + off) = make_uint4(0, 0, 0, 0);
+      *reinterpret_cast<uint4*>(sV + off) = make_uint4(0, 0, 0, 0);
+    }
+    fence_async_smem();
+  }
+  float gi = 0.f, bi = 0.f;
+  if (valid) {
+    gi = p.g[size_t(row) * H + h];
+    bi = __bfloat162float(p.beta[size_t(row) * H + h]);
+    if (p.beta_sigmoid) bi = 1.f / (1.f + expf(-bi));
+  }
+  s_g[tid] = gi;
+  s_b[tid] = bi;
+  mbar_wait(&bar_tma, 0, &abort_flag, p.status, kDevTimeoutTma);
+
+  // L2-norm factors from the staged rows.
+  float ssq = 0.f, ssk = 0.f;
+#pragma unroll
+  for (int c16 = 0; c16 < 16; ++c16) {
+    const uint32_t off = sw128_offset(tid, c16 * 8, 128, 2);
+    float f[8];
+    bf16x8_to_f32(*reinterpret_cast<const uint4*>(sQ + off), f);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) ssq = fmaf(f[e], f[e], ssq);
+    bf16x8_to_f32(*reinterpret_cast<const uint4*>(sK + off), f);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) ssk = fmaf(f[e], f[e], ssk);
+  }
+  const float rq = p.l2norm ? 1.f / sqrtf(ssq + 1e-6f) : 1.f;
+  const float rk = p.l2norm ? 1.f / sqrtf(ssk + 1e-6f) : 1.f;
+  s_rk[tid] = rk;
+  __syncthreads();
+  float G = 0.f;
+  for (int j = 0; j <= il; ++j) G += s_g[blk * kC + j];
+  s_G[tid] = G;
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const float Glast = len > 0 ? s_G[blk * kC + len - 1] : 0.f;
+
+  // Gram products: TMEM cols [0,128) = K K^T, [128,256) = Q K^T (pair-stacked).
+  if (tid == 0 && !abort_flag) {
+    const uint32_t id = idesc_bf16(128, 128);
+    const uint32_t q0 = smem_u32(sQ), k0 = smem_u32(sK);
+    for (int s = 0; s < 8; ++s) mma_bf16_ss(tb, desc_kmajor(k0, kPanel, s), desc_kmajor(k0, kPanel, s), id, s > 0);
+    for (int s = 0; s < 8; ++s)
+      mma_bf16_ss(tb + 128, desc_kmajor(q0, kPanel, s), desc_kmajor(k0, kPanel, s), id, s > 0);
+    mma_commit(&bar_mma);
+  }
+
+  // Gated queries and end-decayed keys (state-independent operands of the chunk loop).
+  const size_t tile = size_t(c_idx) * H + h;
+  if (len > 0) {
+    const float fq = valid ? p.scale * rq * expf(G) : 0.f;
+    const float fk = valid ? rk * expf(Glast - G) : 0.f;
+    float* qt = p.Qt + tile * kTileW + size_t(il) * kD;
+    float* ktt = p.KtT + tile * kTileKtT + il;
+#pragma unroll
+    for (int c16 = 0; c16 < 16; ++c16) {
+      const uint32_t off = sw128_offset(tid, c16 * 8, 128, 2);
+      float f[8];
+      bf16x8_to_f32(*reinterpret_cast<const uint4*>(sQ + off), f);
+      float4* dst = reinterpret_cast<float4*>(qt + c16 * 8);
+      dst[0] = make_float4(to_tf32(f[0] * fq), to_tf32(f[1] * fq), to_tf32(f[2] * fq), to_tf32(f[3] * fq));
+      dst[1] = make_float4(to_tf32(f[4] * fq), to_tf32(f[5] * fq), to_tf32(f[6] * fq), to_tf32(f[7] * fq));
+      bf16x8_to_f32(*reinterpret_cast<const uint4*>(sK + off), f);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) ktt[size_t(c16 * 8 + e) * kC] = to_tf32(f[e] * fk);
+    }
+    if (il == 0) p.gam[tile * kD] = expf(Glast);
+    if (p.Gc) p.Gc[tile * kC + il] = G;
+    if (p.rq) p.rq[tile * kC + il] = rq;
+    if (p.rk) p.rk[tile * kC + il] = rk;
+    if (p.beff) p.beff[tile * kC + il] = bi;
+  }
+
+  const bool ok1 = mbar_wait(&bar_mma, 0, &abort_flag, p.status, kDevTimeoutMma);
+  tc_fence_after();
+  if (ok1) {
+    float* Lrow = sL + blk * (kC * kC) + il * kC;
+    float* aqk = p.Aqk + tile * kTileAqk + size_t(il) * kC;
+#pragma unroll
+    for (int cc = 0; cc < 4; ++cc) {
+      float r[16];
+      tmem_ld16(tb + lane_base + blk * kC + cc * 16, r);
+      tmem_wait_ld();
+#pragma unroll
+      for (int e = 0; e < 16; ++e) {
+        const int j = cc * 16 + e;
+        const int pj = blk * kC + j;
+        Lrow[j] = (j < il) ? bi * rk * s_rk[pj] * r[e] * expf(G - s_G[pj]) : 0.f;
+      }
+      tmem_ld16(tb + lane_base + 128 + blk * kC + cc * 16, r);
+      tmem_wait_ld();
+      float a[16];
+#pragma unroll
+      for (int e = 0; e < 16; ++e) {
+        const int j = cc * 16 + e;
+        const int pj = blk * kC + j;
+        a[e] = (j <= il && valid) ? to_tf32(p.scale * rq * s_rk[pj] * r[e] * expf(G - s_G[pj])) : 0.f;
+      }
+      if (len > 0) {
+        float4* dst = reinterpret_cast<float4*>(aqk + cc * 16);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) dst[e] = make_float4(a[4 * e], a[4 * e + 1], a[4 * e + 2], a[4 * e + 3]);
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+
+  // Column il of A = (I + L)^-1 for this thread's chunk; then the scaled block-diagonal
+  // operands A1 = A diag(beta exp(G) r_k) and A2 = A diag(beta), bf16, K-major, 128x128.
+  {
+    float x[kC];
+    unit_lower_inverse_column(sL + blk * (kC * kC), il, x);
+    const float s1 = bi * expf(G) * rk, s2 = bi;
+    const int col = tid;
+    const __nv_bfloat16 z = __float2bfloat16_rn(0.f);
+#pragma unroll
+    for (int r = 0; r < 128; ++r) {
+      const int rb = r >> 6;
+      const uint32_t off = sw128_offset(r, col, 128, 2);
+      if (rb == blk) {
+        // the unit diagonal is applied in fp32 after the MMA (see below)
+        const float xr = (r & 63) == il ? 0.f : x[r & 63];
+        *reinterpret_cast<__nv_bfloat16*>(sA1 + off) = __float2bfloat16_rn(xr * s1);
+        *reinterpret_cast<__nv_bfloat16*>(sA2 + off) = __float2bfloat16_rn(xr * s2);
+      } else {
+        *reinterpret_cast<__nv_bfloat16*>(sA1 + off) = z;
+        *reinterpret_cast<__nv_bfloat16*>(sA2 + off) = z;
+      }
+    }
+  }
+  fence_async_smem();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+
+  // W = A1 k (TMEM cols [0,128)), U = A2 v (cols [128,256)); k, v as MN-major B operands.
+  // A1, A2 carry only the strictly lower part of A (bf16); the identity part, which dominates
+  // W and U, is added in fp32 from the exact inputs: W_i += beta_i exp(G_i) r_i k_i,
+  // U_i += beta_i v_i. This keeps the bf16 rounding confined to the small off-diagonal terms.
+  if (tid == 0 && !abort_flag) {
+    const uint32_t id = idesc_bf16(128, 128, false, true);
+    const uint32_t a1 = smem_u32(sA1), a2 = smem_u32(sA2), k0 = smem_u32(sK), v0 = smem_u32(sV);
+    for (int s = 0; s < 8; ++s) mma_bf16_ss(tb, desc_kmajor(a1, kPanel, s), desc_mnmajor_bf16(k0, kPanel, s), id, s > 0);
+    for (int s = 0; s < 8; ++s)
+      mma_bf16_ss(tb + 128, desc_kmajor(a2, kPanel, s), desc_mnmajor_bf16(v0, kPanel, s), id, s > 0);
+    mma_commit(&bar_mma);
+  }
+  const bool ok2 = mbar_wait(&bar_mma, 1, &abort_flag, p.status, kDevTimeoutMma);
+  tc_fence_after();
+  if (ok2 && len > 0) {
+    float* w = p.W + tile * kTileW + size_t(il) * kD;
+    float* u = p.U + tile * kTileW + size_t(il) * kD;
+    const float dw_scale = bi * expf(G) * rk, du_scale = bi;
+#pragma unroll
+    for (int cc = 0; cc < 8; ++cc) {
+      float r[16], kr[16], vr[16];
+      bf16x8_to_f32(*reinterpret_cast<const uint4*>(sK + sw128_offset(tid, cc * 16, 128, 2)), kr);
+      bf16x8_to_f32(*reinterpret_cast<const uint4*>(sK + sw128_offset(tid, cc * 16 + 8, 128, 2)), kr + 8);
+      bf16x8_to_f32(*reinterpret_cast<const uint4*>(sV + sw128_offset(tid, cc * 16, 128, 2)), vr);
+      bf16x8_to_f32(*reinterpret_cast<const uint4*>(sV + sw128_offset(tid, cc * 16 + 8, 128, 2)), vr + 8);
+      tmem_ld16(tb + lane_base + cc * 16, r);
+      tmem_wait_ld();
+#pragma unroll
+      for (int e = 0; e < 16; ++e) r[e] = fmaf(dw_scale, kr[e], r[e]);
+      float4* dw = reinterpret_cast<float4*>(w + cc * 16);
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+        dw[e] = make_float4(to_tf32(r[4 * e]), to_tf32(r[4 * e + 1]), to_tf32(r[4 * e + 2]), to_tf32(r[4 * e + 3]));
+      tmem_ld16(tb + lane_base + 128 + cc * 16, r);
+      tmem_wait_ld();
+#pragma unroll
+      for (int e = 0; e < 16; ++e) r[e] = fmaf(du_scale, vr[e], r[e]);
+      float4* du = reinterpret_cast<float4*>(u + cc * 16);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) du[e] = make_float4(r[4 * e], r[4 * e + 1], r[4 * e + 2], r[4 * e + 3]);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) tmem_dealloc(tb, 256);
+}
+
+cudaError_t launch_prep_gdn(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
+                            const PrepParams& p, cudaStream_t s) {
+  static bool attr = false;
+  if (!attr) {
+    cudaError_t e = cudaFuncSetAttribute(k_prep_gdn, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    if (e != cudaSuccess) return e;
+    attr = true;
+  }
+  dim3 grid((p.NC + 1) / 2, p.H);
+  k_prep_gdn<<<grid, kThreads, kSmemBytes, s>>>(mq, mk, mv, p);
+  return cudaGetLastError();
+}
+
+}  // namespace gdn

@@ -1,0 +1,201 @@
+"""PyTorch-facing wrappers of libgdn. Argument marshalling only: torch allocates device memory
+and provides the stream; every step of the computation runs in the library's CUDA kernels.
+There is no fallback path: without the built library or a GB300 these functions raise."""
+from __future__ import annotations
+
+import ctypes
+from typing import Optional, Sequence
+
+import torch
+
+from . import _lib
+
+K_DIM = 128
+CHUNK = 64
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _check_tensor(name, t, dtype, shape, device):
+    if not isinstance(t, torch.Tensor):
+        raise ValueError(f"{name} must be a tensor")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+    if t.device != device:
+        raise ValueError(f"{name} must be on {device}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def _offsets(cu_seqlens, T):
+    """Host int32 copy of packed document offsets (CPU tensor or sequence of ints)."""
+    if cu_seqlens is None:
+        return None
+    if isinstance(cu_seqlens, torch.Tensor):
+        if cu_seqlens.device.type != "cpu" or cu_seqlens.dim() != 1 or \
+                cu_seqlens.dtype not in (torch.int32, torch.int64):
+            raise ValueError("cu_seqlens must be a one-dimensional CPU int32/int64 tensor or a sequence")
+        vals = [int(x) for x in cu_seqlens.tolist()]
+    else:
+        if any(isinstance(x, bool) or not isinstance(x, int) for x in cu_seqlens):
+            raise ValueError("cu_seqlens entries must be ints")
+        vals = [int(x) for x in cu_seqlens]
+    if len(vals) < 2:
+        raise ValueError("cu_seqlens needs at least two entries")
+    return (ctypes.c_int32 * len(vals))(*vals), len(vals) - 1
+
+
+def _desc(B, T, H, scale, l2, sig, final, offsets):
+    d = _lib.Desc()
+    d.B, d.T, d.H, d.K, d.V, d.chunk_size = B, T, H, K_DIM, K_DIM, CHUNK
+    if offsets is not None:
+        arr, n = offsets
+        d.cu_seqlens = ctypes.cast(arr, ctypes.POINTER(ctypes.c_int32))
+        d.num_seqs = n
+    else:
+        d.num_seqs = B
+    d.scale = 0.0 if scale is None else float(scale)
+    d.use_qk_l2norm, d.use_beta_sigmoid, d.output_final_state = int(bool(l2)), int(bool(sig)), int(bool(final))
+    return d
+
+
+def _common_checks(q, k, v, g, beta, per_channel, offsets):
+    if q.dim() != 4:
+        raise ValueError("q must have shape [B,T,H,K]")
+    B, T, H, K = q.shape
+    dev = q.device
+    if dev.type != "cuda":
+        raise ValueError("inputs must be CUDA tensors")
+    _check_tensor("q", q, torch.bfloat16, (B, T, H, K), dev)
+    _check_tensor("k", k, torch.bfloat16, (B, T, H, K), dev)
+    _check_tensor("v", v, torch.bfloat16, (B, T, H, v.shape[-1] if v.dim() == 4 else -1), dev)
+    gshape = (B, T, H, K) if per_channel else (B, T, H)
+    _check_tensor("g", g, torch.float32, gshape, dev)
+    _check_tensor("beta", beta, torch.bfloat16, (B, T, H), dev)
+    N = B if offsets is None else offsets[1]
+    return B, T, H, N, dev
+
+
+def _fwd(per_channel, q, k, v, g, beta, initial_state, output_final_state, use_qk_l2norm,
+         use_beta_sigmoid, cu_seqlens, scale, status):
+    lib = _lib.load()
+    offsets = _offsets(cu_seqlens, q.shape[1] if q.dim() == 4 else 0)
+    B, T, H, N, dev = _common_checks(q, k, v, g, beta, per_channel, offsets)
+    if initial_state is not None:
+        _check_tensor("initial_state", initial_state, torch.float32, (N, H, K_DIM, K_DIM), dev)
+    desc = _desc(B, T, H, scale, use_qk_l2norm, use_beta_sigmoid, output_final_state, offsets)
+    size_fn = lib.kda_fwd_workspace_size if per_channel else lib.gdn_fwd_workspace_size
+    ws_bytes = size_fn(ctypes.byref(desc))
+    if ws_bytes == 0:
+        _lib.check(_lib.GDN_EINVAL)
+    o = torch.empty((B, T, H, K_DIM), dtype=torch.bfloat16, device=dev)
+    final = torch.empty((N, H, K_DIM, K_DIM), dtype=torch.float32, device=dev) if output_final_state else None
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    if status is None:
+        status = torch.empty(1, dtype=torch.int32, device=dev)
+    a = _lib.FwdArgs(q=_ptr(q), k=_ptr(k), v=_ptr(v), g=_ptr(g), beta=_ptr(beta),
+                     initial_state=_ptr(initial_state), o=_ptr(o), final_state=_ptr(final),
+                     workspace=_ptr(ws), workspace_bytes=ws_bytes, status=_ptr(status))
+    stream = ctypes.c_void_p(torch.cuda.current_stream(dev).cuda_stream)
+    fn = lib.kda_fwd if per_channel else lib.gdn_fwd
+    _lib.check(fn(ctypes.byref(desc), ctypes.byref(a), stream))
+    return o, final
+
+
+def _bwd(per_channel, q, k, v, g, beta, dO, dht, initial_state, use_qk_l2norm, use_beta_sigmoid,
+         cu_seqlens, scale, status):
+    lib = _lib.load()
+    offsets = _offsets(cu_seqlens, q.shape[1] if q.dim() == 4 else 0)
+    B, T, H, N, dev = _common_checks(q, k, v, g, beta, per_channel, offsets)
+    _check_tensor("dO", dO, torch.bfloat16, (B, T, H, K_DIM), dev)
+    if initial_state is not None:
+        _check_tensor("initial_state", initial_state, torch.float32, (N, H, K_DIM, K_DIM), dev)
+    if dht is not None:
+        _check_tensor("dht", dht, torch.float32, (N, H, K_DIM, K_DIM), dev)
+    desc = _desc(B, T, H, scale, use_qk_l2norm, use_beta_sigmoid, False, offsets)
+    size_fn = lib.kda_bwd_workspace_size if per_channel else lib.gdn_bwd_workspace_size
+    ws_bytes = size_fn(ctypes.byref(desc))
+    if ws_bytes == 0:
+        _lib.check(_lib.GDN_EINVAL)
+    dq = torch.empty_like(q)
+    dk = torch.empty_like(k)
+    dv = torch.empty_like(v)
+    dbeta = torch.empty_like(beta)
+    dg = torch.empty_like(g)
+    dh0 = torch.empty((N, H, K_DIM, K_DIM), dtype=torch.float32, device=dev) if initial_state is not None else None
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    if status is None:
+        status = torch.empty(1, dtype=torch.int32, device=dev)
+    a = _lib.BwdArgs(q=_ptr(q), k=_ptr(k), v=_ptr(v), g=_ptr(g), beta=_ptr(beta),
+                     initial_state=_ptr(initial_state), dO=_ptr(dO), dht=_ptr(dht), dq=_ptr(dq),
+                     dk=_ptr(dk), dv=_ptr(dv), dbeta=_ptr(dbeta), dg=_ptr(dg), dh0=_ptr(dh0),
+                     workspace=_ptr(ws), workspace_bytes=ws_bytes, status=_ptr(status))
+    stream = ctypes.c_void_p(torch.cuda.current_stream(dev).cuda_stream)
+    fn = lib.kda_bwd if per_channel else lib.gdn_bwd
+    _lib.check(fn(ctypes.byref(desc), ctypes.byref(a), stream))
+    return dq, dk, dv, dbeta, dg, dh0
+
+
+def gdn_fwd(q, k, v, g, beta, *, initial_state=None, output_final_state=False, use_qk_l2norm=True,
+            use_beta_sigmoid=False, cu_seqlens: Optional[Sequence[int]] = None, scale=None, status=None):
+    """Gated DeltaNet forward. Returns ``(o [B,T,H,128] bf16, final_state [N,H,128,128] fp32 or None)``."""
+    return _fwd(False, q, k, v, g, beta, initial_state, output_final_state, use_qk_l2norm,
+                use_beta_sigmoid, cu_seqlens, scale, status)
+
+
+def kda_fwd(q, k, v, g, beta, *, initial_state=None, output_final_state=False, use_qk_l2norm=True,
+            use_beta_sigmoid=True, cu_seqlens: Optional[Sequence[int]] = None, scale=None, status=None):
+    """Kimi Delta Attention forward (per-channel gate g [B,T,H,128])."""
+    return _fwd(True, q, k, v, g, beta, initial_state, output_final_state, use_qk_l2norm,
+                use_beta_sigmoid, cu_seqlens, scale, status)
+
+
+def gdn_bwd(q, k, v, g, beta, dO, *, dht=None, initial_state=None, use_qk_l2norm=True,
+            use_beta_sigmoid=False, cu_seqlens=None, scale=None, status=None):
+    """Gated DeltaNet backward. Returns ``(dq, dk, dv, dbeta, dg, dh0 or None)``."""
+    return _bwd(False, q, k, v, g, beta, dO, dht, initial_state, use_qk_l2norm, use_beta_sigmoid,
+                cu_seqlens, scale, status)
+
+
+def kda_bwd(q, k, v, g, beta, dO, *, dht=None, initial_state=None, use_qk_l2norm=True,
+            use_beta_sigmoid=True, cu_seqlens=None, scale=None, status=None):
+    """Kimi Delta Attention backward. Returns ``(dq, dk, dv, dbeta, dg, dh0 or None)``."""
+    return _bwd(True, q, k, v, g, beta, dO, dht, initial_state, use_qk_l2norm, use_beta_sigmoid,
+                cu_seqlens, scale, status)
+
+
+class ChunkGatedDeltaRule(torch.autograd.Function):
+    """Autograd wrapper: forward through gdn_fwd/kda_fwd, backward through gdn_bwd/kda_bwd
+    (the backward recomputes the forward's intermediates from the saved inputs)."""
+
+    @staticmethod
+    def forward(ctx, q, k, v, g, beta, initial_state, per_channel, use_qk_l2norm, use_beta_sigmoid,
+                cu_seqlens, scale, output_final_state):
+        o, final = _fwd(per_channel, q, k, v, g, beta, initial_state, output_final_state, use_qk_l2norm,
+                        use_beta_sigmoid, cu_seqlens, scale, None)
+        ctx.save_for_backward(q, k, v, g, beta, initial_state)
+        ctx.cfg = (per_channel, use_qk_l2norm, use_beta_sigmoid, cu_seqlens, scale)
+        return o, final
+
+    @staticmethod
+    def backward(ctx, dO, dfinal):
+        q, k, v, g, beta, h0 = ctx.saved_tensors
+        per_channel, l2, sig, cu, scale = ctx.cfg
+        dq, dk, dv, dbeta, dg, dh0 = _bwd(per_channel, q, k, v, g, beta, dO.contiguous(),
+                                          None if dfinal is None else dfinal.contiguous(), h0, l2, sig,
+                                          cu, scale, None)
+        return dq, dk, dv, dg, dbeta, dh0, None, None, None, None, None, None
+
+
+def chunk_gated_delta_rule(q, k, v, g, beta, *, initial_state=None, output_final_state=False,
+                           use_qk_l2norm=True, use_beta_sigmoid=None, cu_seqlens=None, scale=None):
+    """Differentiable entry point; the gate's rank selects GDN ([B,T,H]) or KDA ([B,T,H,K])."""
+    per_channel = g.dim() == 4
+    if use_beta_sigmoid is None:
+        use_beta_sigmoid = per_channel
+    return ChunkGatedDeltaRule.apply(q, k, v, g, beta, initial_state, per_channel, use_qk_l2norm,
+                                     use_beta_sigmoid, cu_seqlens, scale, output_final_state)

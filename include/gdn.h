@@ -1,0 +1,135 @@
+/* C ABI of libgdn: the chunkwise gated delta rule on one NVIDIA GB300 (sm_103a).
+ *
+ * Operations (forward and backward of one layer's recurrence):
+ *   gdn_fwd / gdn_bwd : Gated DeltaNet, one scalar log-decay g per token and head.
+ *   kda_fwd / kda_bwd : Kimi Delta Attention, one log-decay per token, head and key channel.
+ *
+ * What is computed. For every independent sequence (a dense batch row, or one document of a
+ * packed row) and head, starting from S = initial_state (or 0), with K x V state S:
+ *   qh = q / sqrt(|q|^2 + 1e-6), kh likewise        (when use_qk_l2norm; else qh = q, kh = k)
+ *   b  = sigmoid(beta) when use_beta_sigmoid, else beta
+ *   S' = exp(g_t) S           (GDN)   |   S' = diag(exp(g_t[:])) S   (KDA, per key channel)
+ *   S  = S' + kh (b (v_t - S'^T kh))^T
+ *   o_t = scale * S^T qh
+ * This is the recurrence carried by the chunk loop of the eager reference
+ * `torch_chunk_gated_delta_rule` (hyper-parallel GDN module, Diff Coverage page: `_l2norm`
+ * with eps 1e-6 inside the square root, the cumulative-gate decay mask, the KK^T strictly
+ * lower matrix and its forward-substitution inverse, the WY terms `value`/`k_cumdecay`, and
+ * the per-chunk state update); the KDA form is the same rule with the per-channel
+ * cumulative gate of the KDA staged native interface (`_KDAPrepared.gk`,
+ * kimi_delta_attention_ascendc.py coverage page). The library evaluates it chunkwise with
+ * 64-token chunks; results equal the recurrence up to rounding.
+ *
+ * Layout. Token-major BSND, contiguous: q, k [B,T,H,K]; v, o [B,T,H,V]; beta [B,T,H]; GDN g
+ * [B,T,H]; KDA g [B,T,H,K]. States are [N,H,K,V] fp32 with N = B (dense) or the number of
+ * documents (packed). K == V == 128. Packed documents use B == 1 and a HOST array
+ * cu_seqlens of N+1 int32 offsets, 0 = c_0 < c_1 < ... < c_N = T; each document starts from
+ * its own initial state and yields its own final state.
+ *
+ * Dtypes. q, k, v, o, beta, dq, dk, dv, dbeta, dO: bf16 (passed as uint16 bit patterns).
+ * g, dg, states, dht, dh0: fp32. Arithmetic: fp32 accumulation; tensor-core operands bf16
+ * where they are exact input values, tf32 (round-to-nearest) elsewhere.
+ *
+ * Ownership. Every pointer in the argument structs is a DEVICE pointer owned by the caller,
+ * except cu_seqlens (HOST). The library never allocates or frees memory: the caller passes a
+ * device workspace of at least *_workspace_size() bytes (256-byte aligned). No output may
+ * alias an input. cu_seqlens is read during the call only.
+ *
+ * Asynchrony and errors. Validation is host-side and synchronous; on success the work is
+ * enqueued on `stream` (a cudaStream_t, NULL = legacy default stream) and the call returns
+ * GDN_OK without synchronising. A contract violation returns GDN_EINVAL before anything is
+ * enqueued (gdn_last_error() gives the reason); a device other than compute capability 10.3
+ * gives GDN_EUNSUPPORTED; a CUDA launch failure gives GDN_ECUDA. Device kernels never trap:
+ * every wait inside a kernel is bounded and, when it runs out, records a nonzero code in the
+ * caller's `status` word (an int in device memory, or NULL), which the caller may read after
+ * synchronising (GDN_ETIMEOUT semantics).
+ */
+#ifndef GDN_GB300_H
+#define GDN_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define GDN_OK 0
+#define GDN_EINVAL 1        /* contract violation: shapes, flags, offsets, pointers, workspace */
+#define GDN_EUNSUPPORTED 2  /* not a compute-capability 10.3 device, or no device */
+#define GDN_ECUDA 3         /* a CUDA runtime call or kernel launch failed */
+#define GDN_ETIMEOUT 4      /* a bounded in-kernel wait ran out (reported via the status word) */
+
+/* Problem description shared by every entry point. */
+typedef struct {
+  int B, T, H, K, V;         /* dense: B >= 1; packed (cu_seqlens != NULL): B == 1. K == V == 128 */
+  int chunk_size;            /* must be 64 */
+  const int32_t* cu_seqlens; /* HOST, num_seqs + 1 offsets, or NULL for dense */
+  int num_seqs;              /* documents when packed; ignored (== B) when dense */
+  float scale;               /* output scale; <= 0 selects 1/sqrt(K) */
+  int use_qk_l2norm;         /* L2-normalise q and k per token and head (eps 1e-6) */
+  int use_beta_sigmoid;      /* beta holds logits; the kernel applies sigmoid */
+  int output_final_state;    /* write final_state */
+} gdn_desc_t;
+
+typedef struct {
+  const void* q;             /* bf16 [B,T,H,K] */
+  const void* k;             /* bf16 [B,T,H,K] */
+  const void* v;             /* bf16 [B,T,H,V] */
+  const float* g;            /* GDN [B,T,H], KDA [B,T,H,K]: natural-log decay, <= 0 expected */
+  const void* beta;          /* bf16 [B,T,H] */
+  const float* initial_state;/* [N,H,K,V] or NULL (zeros) */
+  void* o;                   /* bf16 [B,T,H,V], written */
+  float* final_state;        /* [N,H,K,V], written when output_final_state (else may be NULL) */
+  void* workspace;           /* device, >= *_fwd_workspace_size() bytes, 256-byte aligned */
+  size_t workspace_bytes;
+  int* status;               /* device int or NULL: nonzero after a bounded wait ran out */
+} gdn_fwd_args_t;
+
+typedef struct {
+  const void* q;             /* forward inputs, as passed to the forward */
+  const void* k;
+  const void* v;
+  const float* g;
+  const void* beta;
+  const float* initial_state;/* [N,H,K,V] or NULL */
+  const void* dO;            /* bf16 [B,T,H,V]: gradient of the output */
+  const float* dht;          /* [N,H,K,V] gradient of the final state, or NULL */
+  void* dq;                  /* bf16 [B,T,H,K] */
+  void* dk;                  /* bf16 [B,T,H,K] */
+  void* dv;                  /* bf16 [B,T,H,V] */
+  void* dbeta;               /* bf16 [B,T,H]: w.r.t. beta as passed (the logit when use_beta_sigmoid) */
+  float* dg;                 /* fp32, same shape as g: w.r.t. the raw per-token gate */
+  float* dh0;                /* [N,H,K,V] or NULL */
+  void* workspace;
+  size_t workspace_bytes;
+  int* status;
+} gdn_bwd_args_t;
+
+/* Human-readable name of an error code. */
+const char* gdn_strerror(int code);
+/* Reason for the last GDN_EINVAL / GDN_ECUDA returned on the calling thread ("" if none). */
+const char* gdn_last_error(void);
+/* GDN_OK if `device` is a compute-capability 10.3 GPU this library was built for. */
+int gdn_device_supported(int device);
+
+/* Workspace sizes in bytes for a valid description; 0 when the description is invalid. */
+size_t gdn_fwd_workspace_size(const gdn_desc_t* desc);
+size_t gdn_bwd_workspace_size(const gdn_desc_t* desc);
+size_t kda_fwd_workspace_size(const gdn_desc_t* desc);
+size_t kda_bwd_workspace_size(const gdn_desc_t* desc);
+
+/* Gated DeltaNet forward: o (and final_state). */
+int gdn_fwd(const gdn_desc_t* desc, const gdn_fwd_args_t* args, void* stream);
+/* Gated DeltaNet backward: gradients of <dO, o> + <dht, final_state> w.r.t. q, k, v, beta,
+ * g and initial_state (dh0). The forward is recomputed from the inputs. */
+int gdn_bwd(const gdn_desc_t* desc, const gdn_bwd_args_t* args, void* stream);
+/* Kimi Delta Attention forward / backward: as above with the per-channel gate g [B,T,H,K]. */
+int kda_fwd(const gdn_desc_t* desc, const gdn_fwd_args_t* args, void* stream);
+int kda_bwd(const gdn_desc_t* desc, const gdn_bwd_args_t* args, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GDN_GB300_H */

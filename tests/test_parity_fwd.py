@@ -1,0 +1,70 @@
+"""GPU forward parity: the CUDA path against the fp64 oracle on the same seeded inputs."""
+import numpy as np
+import pytest
+import torch
+
+from chunked_gated_delta_05_gb300 import gdn_fwd, synth
+from tests._util import assert_output, assert_state, oracle_fwd, to_cuda
+
+pytestmark = pytest.mark.gpu
+
+
+def run_gdn(d, **kw):
+    dc = to_cuda(d)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    o, hT = gdn_fwd(dc["q"], dc["k"], dc["v"], dc["g"], dc["beta"], initial_state=dc["h0"],
+                    output_final_state=True, cu_seqlens=d["cu_seqlens"], status=status, **kw)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    return o.float().cpu().numpy(), hT.cpu().numpy()
+
+
+def check(d, **kw):
+    o, hT = run_gdn(d, **kw)
+    ref_kw = {k: v for k, v in kw.items() if k in ("use_qk_l2norm", "use_beta_sigmoid", "scale")}
+    ro, rT = oracle_fwd(d, **ref_kw)
+    r_o = assert_output("o", o, ro)
+    r_s = assert_state("final_state", hT, rT)
+    print(f"parity o rel-L2 {r_o[0]:.2e} max-abs {r_o[1]:.2e}; state rel-L2 {r_s:.2e}")
+
+
+def test_smoke_workload():
+    w = synth.WORKLOADS["gdn_smoke_b1_t256_h2"]
+    check(synth.make_inputs(w))
+
+
+@pytest.mark.parametrize("T", [1, 63, 64, 65, 127, 200])
+def test_ragged_lengths(T):
+    check(synth.custom(2, T, 2, h0_std=0.02, seed=T))
+
+
+def test_no_l2norm_and_custom_scale():
+    d = synth.custom(1, 130, 2, seed=3)
+    # unnormalised keys make the delta rule unstable; shrink them so the state stays bounded
+    d["k"] = (d["k"].float() * 0.08).to(torch.bfloat16)
+    d["q"] = (d["q"].float() * 0.08).to(torch.bfloat16)
+    check(d, use_qk_l2norm=False, scale=0.3)
+
+
+def test_beta_logits_with_sigmoid():
+    d = synth.custom(1, 150, 3, beta_logits=True, seed=4)
+    check(d, use_beta_sigmoid=True)
+
+
+def test_packed_documents():
+    lens = [1, 63, 64, 65, 130, 7, 200]
+    d = synth.custom(1, sum(lens), 2, h0_std=0.02, lengths=lens, seed=5)
+    check(d)
+
+
+def test_strong_decay():
+    d = synth.custom(1, 256, 2, seed=6, g_scale=4.0)
+    check(d)
+
+
+def test_two_calls_identical():
+    d = synth.custom(1, 192, 2, seed=7)
+    o1, h1 = run_gdn(d)
+    o2, h2 = run_gdn(d)
+    np.testing.assert_array_equal(o1, o2)
+    np.testing.assert_array_equal(h1, h2)
