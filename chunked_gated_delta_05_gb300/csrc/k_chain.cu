@@ -4,39 +4,97 @@
 // `torch_chunk_gated_delta_rule`, hyper-parallel GDN Diff Coverage page):
 //   v_new = U - W S
 //   o     = Qt S + Aqk v_new
-//   S     = gam (.) S + KtT^T-applied: S <- diag(gam) S + (k decayed to chunk end)^T v_new
+//   S     = diag(gam) S + k~^T v_new,     k~ = keys decayed to the chunk end (KtT = k~^T)
 // (gam is exp(G_last): a scalar for GDN, one value per key row for KDA.)
 //
-// GB300 mapping: one CTA per (sequence, head). The state is held transposed, S^T (V x K),
-// one row per thread of warps 0-3 (thread v owns column v of S, 128 fp32 registers), so
-// every product is a 128-lane tcgen05 MMA with S^T or v_new^T as the TMEM-resident A
-// operand (kind::tf32; operands rounded to nearest tf32 when written) and the chunk tiles
-// from the prepare kernel as TMA-loaded SW128 B operands:
-//   P   = S^T  W^T    (v_new^T = U^T - P)        -> TMEM
-//   O   = S^T  Qt^T + v_new^T Aqk^T              -> TMEM (double-buffered by chunk parity)
-//   D   = v_new^T KtT^T  (= (k~^T v_new)^T)      -> TMEM; S^T <- gam S^T + D in registers
-// Warp 4 streams the tiles with TMA (three buffer groups, each refilled as soon as its
-// consumers finish) and issues the MMAs from one thread. All waits are bounded.
+// GB300 mapping: one CTA per (sequence, head). The state lives in TMEM, transposed: S^T
+// (V x K), lane v = column v of S, as an fp32 master copy plus a round-to-nearest tf32 copy
+// that the MMAs read as their TMEM-resident A operand (kind::tf32). The chunk tiles from the
+// prepare kernel are TMA-loaded SW128 B operands:
+//   P    = S^T W^T           (v_new^T = U^T - P)           -- on the serial chain
+//   S^T += v_new^T KtT^T     (master pre-decayed by gam)   -- on the serial chain
+//   O    = S^T Qt^T + v_new^T Aqk^T                        -- off the chain, issued after
+// The MMAs on the chain are issued first and committed on their own barriers, so the output
+// products run on the tensor pipe while the chain threads work. Eight chain warps share the
+// TMEM lanes (two threads per lane, each on half of the columns); warp 8 streams the tiles
+// with TMA (KtT/Aqk double-buffered) and issues the MMAs from one thread. All waits bounded.
 #include "common.cuh"
 #include "umma.cuh"
 
 namespace gdn {
 
+#ifdef GDN_TRACE
+// Optional timeline of the first CTA (compiled only with -DGDN_TRACE; never in the library).
+__device__ unsigned long long g_trace[64 * 8];
+#define TRACE(j, slot)                                                                          \
+  do {                                                                                          \
+    if (blockIdx.x == 0 && blockIdx.y == 0 && (j) < 64) g_trace[(j) * 8 + (slot)] = globaltimer(); \
+  } while (0)
+#else
+#define TRACE(j, slot) \
+  do {                 \
+  } while (0)
+#endif
+
 namespace {
 
-constexpr int kThreads = 160;
+constexpr int kChainThreads = 256;            // 8 warps: lane v = tid % 128, half = tid / 128
+constexpr int kThreads = kChainThreads + 32;  // + producer warp
 // shared memory tile offsets (bytes, 1024-aligned)
 constexpr uint32_t kOffW = 0;          // 4 panels x 64 rows x 128 B   (W   [t][k], K-major)
 constexpr uint32_t kOffQt = 32768;     // 4 panels x 64 rows x 128 B   (Qt  [t][k])
-constexpr uint32_t kOffKtT = 65536;    // 2 panels x 128 rows x 128 B  (KtT [k][t])
-constexpr uint32_t kOffAqk = 98304;    // 2 panels x 64 rows x 128 B   (Aqk [i][j])
-constexpr uint32_t kOffU = 114688;     // 4 panels x [64][32] fp32, no swizzle
-constexpr uint32_t kSmemBytes = 147456 + 1024;
+constexpr uint32_t kOffU = 65536;      // 4 panels x [64][32] fp32, no swizzle
+constexpr uint32_t kOffG3 = 98304;     // 2 stages x {KtT 32 KB (2 panels x 128 rows), Aqk 16 KB}
+constexpr uint32_t kG3Stage = 49152;
+constexpr uint32_t kSmemBytes = kOffG3 + 2 * kG3Stage + 1024;
 // TMEM columns
-constexpr uint32_t kTS = 0, kTP = 128, kTVN = 192, kTD = 256, kTO = 384;
+constexpr uint32_t kTSM = 0, kTST = 128, kTP = 256, kTVN = 320, kTO = 384;
 
 __device__ __forceinline__ uint8_t* align1k(uint8_t* p) {
   return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
+}
+
+// S pass for chunk c (one thread: lane v, state columns [k0, k0+64)): record the entry state,
+// write its tf32 copy (the MMA operand) and pre-apply the chunk's end decay to the fp32 master
+// copy (the MMA then adds k~^T v_new in place).
+__device__ __forceinline__ void chain_state_pass(const ChainParams& p, int c, int h, int v, int k0,
+                                                 uint32_t tl, uint64_t* sready) {
+  const size_t tile = size_t(c) * p.H + h;
+  float s[64];
+  tmem_ld64(tl + kTSM + k0, s);
+  tmem_wait_ld_regs(s);
+  if (p.h_save) {
+    float* hs = p.h_save + tile * kD * kD + size_t(k0) * kD + v;
+#pragma unroll
+    for (int e = 0; e < 64; ++e) hs[size_t(e) * kD] = s[e];
+  }
+#pragma unroll
+  for (int half = 0; half < 2; ++half) {
+    float t[32];
+#pragma unroll
+    for (int e = 0; e < 32; ++e) t[e] = to_tf32(s[32 * half + e]);
+    tmem_st32(tl + kTST + k0 + 32 * half, t);
+  }
+  if (p.kda) {
+    const float4* gam = reinterpret_cast<const float4*>(p.gam + tile * kD + k0);
+#pragma unroll
+    for (int e = 0; e < 16; ++e) {
+      const float4 g4 = gam[e];
+      s[4 * e] *= g4.x;
+      s[4 * e + 1] *= g4.y;
+      s[4 * e + 2] *= g4.z;
+      s[4 * e + 3] *= g4.w;
+    }
+  } else {
+    const float g0 = p.gam[tile * kD];
+#pragma unroll
+    for (int e = 0; e < 64; ++e) s[e] *= g0;
+  }
+  tmem_st32(tl + kTSM + k0, s);
+  tmem_st32(tl + kTSM + k0 + 32, s + 32);
+  tmem_wait_st();
+  tc_fence_before();
+  mbar_arrive(sready);
 }
 
 }  // namespace
@@ -47,7 +105,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const __grid_constant__ CUtensorMap mU, const ChainParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = align1k(smem_raw);
-  __shared__ uint64_t full1, full2, full3, mma1, mma2, sready, vready;
+  __shared__ uint64_t full1, full2, full3[2], mma1, mma1b, mma2, mma3, sready, vready;
   __shared__ uint32_t tslot;
   __shared__ int abort_flag;
 
@@ -61,11 +119,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     abort_flag = 0;
     mbar_init(&full1, 1);
     mbar_init(&full2, 1);
-    mbar_init(&full3, 1);
+    mbar_init(&full3[0], 1);
+    mbar_init(&full3[1], 1);
     mbar_init(&mma1, 1);
+    mbar_init(&mma1b, 1);
     mbar_init(&mma2, 1);
-    mbar_init(&sready, 128);
-    mbar_init(&vready, 128);
+    mbar_init(&mma3, 1);
+    mbar_init(&sready, kChainThreads);
+    mbar_init(&vready, kChainThreads);
     fence_mbar_init();
   }
   tc_fence_before();
@@ -73,11 +134,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tb = tslot;
 
-  if (warp == 4) {
+  if (warp == kChainThreads / 32) {
     if (lane == 0) {
       // ---------------- producer + MMA issuer ----------------
-      const uint32_t sW = smem_u32(sm + kOffW), sQt = smem_u32(sm + kOffQt), sKtT = smem_u32(sm + kOffKtT),
-                     sAqk = smem_u32(sm + kOffAqk);
+      const uint32_t sW = smem_u32(sm + kOffW), sQt = smem_u32(sm + kOffQt);
       auto load_g1 = [&](int c) {
         const int y = (c * H + h) * kC;
         mbar_expect_tx(&full1, 65536u);
@@ -91,149 +151,133 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_expect_tx(&full2, 32768u);
         for (int pp = 0; pp < 4; ++pp) tma_load_2d(sm + kOffU + pp * 8192, &mU, pp * 32, y, &full2);
       };
-      auto load_g3 = [&](int c) {
-        mbar_expect_tx(&full3, 49152u);
+      auto load_g3 = [&](int c, int st) {
+        uint8_t* base = sm + kOffG3 + st * kG3Stage;
+        mbar_expect_tx(&full3[st], 49152u);
         for (int pp = 0; pp < 2; ++pp) {
-          tma_load_2d(sm + kOffKtT + pp * 16384, &mKtT, pp * 32, (c * H + h) * kD, &full3);
-          tma_load_2d(sm + kOffAqk + pp * 8192, &mAqk, pp * 32, (c * H + h) * kC, &full3);
+          tma_load_2d(base + pp * 16384, &mKtT, pp * 32, (c * H + h) * kD, &full3[st]);
+          tma_load_2d(base + 32768 + pp * 8192, &mAqk, pp * 32, (c * H + h) * kC, &full3[st]);
         }
       };
       load_g1(first);
       load_g2(first);
-      load_g3(first);
+      load_g3(first, 0);
+      if (nc > 1) load_g3(first + 1, 1);
       const uint32_t id64 = idesc_tf32(128, 64), id128 = idesc_tf32(128, 128);
       for (int j = 0; j < nc; ++j) {
         const uint32_t par = j & 1;
-        const int c = first + j;
+        const int c = first + j, st = j & 1;
         const uint32_t tO = tb + kTO + (j & 1) * 64;
+        const uint32_t sKtT = smem_u32(sm + kOffG3 + st * kG3Stage), sAqk = sKtT + 32768;
+        TRACE(j, 0);
         if (!mbar_wait(&full1, par, &abort_flag, p.status, kDevTimeoutTma)) break;
         if (!mbar_wait(&sready, par, &abort_flag, p.status, kDevTimeoutSync)) break;
+        TRACE(j, 1);
         tc_fence_after();
-        for (int s = 0; s < 16; ++s) mma_tf32_ts(tb + kTP, tb + kTS + s * 8, desc_kmajor(sW, 8192, s), id64, s > 0);
-        for (int s = 0; s < 16; ++s) mma_tf32_ts(tO, tb + kTS + s * 8, desc_kmajor(sQt, 8192, s), id64, s > 0);
+        for (int s = 0; s < 16; ++s) mma_tf32_ts(tb + kTP, tb + kTST + s * 8, desc_kmajor(sW, 8192, s), id64, s > 0);
         mma_commit(&mma1);
-        if (!mbar_wait(&mma1, par, &abort_flag, p.status, kDevTimeoutMma)) break;
+        for (int s = 0; s < 16; ++s) mma_tf32_ts(tO, tb + kTST + s * 8, desc_kmajor(sQt, 8192, s), id64, s > 0);
+        mma_commit(&mma1b);
+        if (!mbar_wait(&mma1b, par, &abort_flag, p.status, kDevTimeoutMma)) break;
+        TRACE(j, 2);
         if (j + 1 < nc) load_g1(c + 1);
         if (!mbar_wait(&vready, par, &abort_flag, p.status, kDevTimeoutSync)) break;
+        TRACE(j, 3);
         if (j + 1 < nc) load_g2(c + 1);
-        if (!mbar_wait(&full3, par, &abort_flag, p.status, kDevTimeoutTma)) break;
+        if (!mbar_wait(&full3[st], (j >> 1) & 1, &abort_flag, p.status, kDevTimeoutTma)) break;
+        TRACE(j, 4);
         tc_fence_after();
-        for (int s = 0; s < 8; ++s) mma_tf32_ts(tO, tb + kTVN + s * 8, desc_kmajor(sAqk, 8192, s), id64, true);
-        for (int s = 0; s < 8; ++s) mma_tf32_ts(tb + kTD, tb + kTVN + s * 8, desc_kmajor(sKtT, 16384, s), id128, s > 0);
+        for (int s = 0; s < 8; ++s) mma_tf32_ts(tb + kTSM, tb + kTVN + s * 8, desc_kmajor(sKtT, 16384, s), id128, true);
         mma_commit(&mma2);
-        if (!mbar_wait(&mma2, par, &abort_flag, p.status, kDevTimeoutMma)) break;
-        if (j + 1 < nc) load_g3(c + 1);
+        for (int s = 0; s < 8; ++s) mma_tf32_ts(tO, tb + kTVN + s * 8, desc_kmajor(sAqk, 8192, s), id64, true);
+        mma_commit(&mma3);
+        if (!mbar_wait(&mma3, par, &abort_flag, p.status, kDevTimeoutMma)) break;
+        TRACE(j, 5);
+        if (j + 2 < nc) load_g3(c + 2, st);
       }
-      // Drain: make sure no TMA write is still landing in shared memory before exit.
-      // Loads are only issued for chunks that the loop then waits on, except on abort.
     }
-  } else {
-    // ---------------- chain warps: thread v owns row v of S^T ----------------
-    const int v = tid;
+  } else if (warp < kChainThreads / 32) {
+    // ---------------- chain warps: lane v of S^T, column half `half` ----------------
+    const int v = tid & 127, half = tid >> 7;
     const uint32_t lb = tmem_lane_base(warp);
     const float* sU = reinterpret_cast<const float*>(sm + kOffU);
-    float S[kD];
-    if (p.h0) {
-      const float* src = p.h0 + (size_t(n) * H + h) * kD * kD + v;
+    const int k0 = 64 * half;  // state columns handled by this thread
+    const int t0 = 32 * half;  // token columns handled by this thread
+    {
+      float buf[64];
+      const float* src = p.h0 ? p.h0 + (size_t(n) * H + h) * kD * kD + size_t(k0) * kD + v : nullptr;
 #pragma unroll
-      for (int k = 0; k < kD; ++k) S[k] = src[size_t(k) * kD];
-    } else {
-#pragma unroll
-      for (int k = 0; k < kD; ++k) S[k] = 0.f;
-    }
-    auto store_state = [&]() {
-#pragma unroll
-      for (int c0 = 0; c0 < kD; c0 += 16) {
-        float r[16];
-#pragma unroll
-        for (int e = 0; e < 16; ++e) r[e] = to_tf32(S[c0 + e]);
-        tmem_st16(tb + lb + kTS + c0, r);
-      }
+      for (int e = 0; e < 64; ++e) buf[e] = src ? src[size_t(e) * kD] : 0.f;
+      tmem_st32(tb + lb + kTSM + k0, buf);
+      tmem_st32(tb + lb + kTSM + k0 + 32, buf + 32);
       tmem_wait_st();
-      tc_fence_before();
-      mbar_arrive(&sready);
-    };
-    store_state();
+    }
+    chain_state_pass(p, first, h, v, k0, tb + lb, &sready);
     bool alive = true;
-    for (int j = 0; j < nc && alive; ++j) {
+    for (int j = 0; j < nc; ++j) {
       const uint32_t par = j & 1;
       const int c = first + j;
       const ChunkEntry ch = p.chunks[c];
       const size_t tile = size_t(c) * H + h;
-      if (p.h_save) {
-        float* dst = p.h_save + tile * kD * kD + v;
+      if (!mbar_wait(&full2, par, &abort_flag, p.status, kDevTimeoutTma)) { alive = false; break; }
+      float u[32];
 #pragma unroll
-        for (int k = 0; k < kD; ++k) dst[size_t(k) * kD] = S[k];
-      }
+      for (int t = 0; t < 32; ++t) u[t] = sU[(v >> 5) * 2048 + (t0 + t) * 32 + (v & 31)];
       if (!mbar_wait(&mma1, par, &abort_flag, p.status, kDevTimeoutMma)) { alive = false; break; }
       tc_fence_after();
-      if (!mbar_wait(&full2, par, &abort_flag, p.status, kDevTimeoutTma)) { alive = false; break; }
-      // v_new^T row v = U[:, v] - P[v, :]
-      float* vsave = p.vnew_save ? p.vnew_save + tile * kTileW + v : nullptr;
+      {
+        float r[32];
+        tmem_ld32(tb + lb + kTP + t0, r);
+        tmem_wait_ld_regs(r);
+        float* vsave = p.vnew_save ? p.vnew_save + tile * kTileW + size_t(t0) * kD + v : nullptr;
 #pragma unroll
-      for (int t0 = 0; t0 < kC; t0 += 16) {
-        float r[16];
-        tmem_ld16(tb + lb + kTP + t0, r);
-        tmem_wait_ld();
-#pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          const int t = t0 + e;
-          const float u = sU[(v >> 5) * 2048 + t * 32 + (v & 31)];
-          const float vn = u - r[e];
+        for (int t = 0; t < 32; ++t) {
+          const float vn = u[t] - r[t];
           if (vsave) vsave[size_t(t) * kD] = vn;
-          r[e] = to_tf32(vn);
+          r[t] = to_tf32(vn);
         }
-        tmem_st16(tb + lb + kTVN + t0, r);
+        tmem_st32(tb + lb + kTVN + t0, r);
       }
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(&vready);
-      const float* gam = p.gam + tile * kD;  // end-of-chunk decay: entry 0 (GDN) or per key row (KDA)
-      const float gsc = gam[0];
       if (!mbar_wait(&mma2, par, &abort_flag, p.status, kDevTimeoutMma)) { alive = false; break; }
       tc_fence_after();
-#pragma unroll
-      for (int k0 = 0; k0 < kD; k0 += 16) {
-        float r[16];
-        tmem_ld16(tb + lb + kTD + k0, r);
-        tmem_wait_ld();
-#pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          const float gk = p.kda ? gam[k0 + e] : gsc;
-          S[k0 + e] = fmaf(gk, S[k0 + e], r[e]);
-        }
-      }
-      // output rows of this chunk (read before the state is released for the next chunk's
-      // MMAs, which may reuse this parity's O buffer two chunks later)
+      if (j + 1 < nc) chain_state_pass(p, c + 1, h, v, k0, tb + lb, &sready);
+      if (!mbar_wait(&mma3, par, &abort_flag, p.status, kDevTimeoutMma)) { alive = false; break; }
+      tc_fence_after();
       {
         const uint32_t tO = tb + kTO + (j & 1) * 64;
-        __nv_bfloat16* op = p.o ? p.o + (size_t(ch.x) * H + h) * kD + v : nullptr;
+        float r[32];
+        tmem_ld32(tO + lb + t0, r);
+        tmem_wait_ld_regs(r);
+        if (p.o) {
+          __nv_bfloat16* op = p.o + (size_t(ch.x + t0) * H + h) * kD + v;
 #pragma unroll
-        for (int t0 = 0; t0 < kC; t0 += 16) {
-          float r[16];
-          tmem_ld16(tO + lb + t0, r);
-          tmem_wait_ld();
-          if (op) {
-#pragma unroll
-            for (int e = 0; e < 16; ++e) {
-              const int t = t0 + e;
-              if (t < ch.y) op[size_t(t) * H * kD] = __float2bfloat16_rn(r[e]);
-            }
-          }
+          for (int t = 0; t < 32; ++t)
+            if (t0 + t < ch.y) op[size_t(t) * H * kD] = __float2bfloat16_rn(r[t]);
         }
       }
-      store_state();
     }
     if (alive && p.hT) {
-      float* dst = p.hT + (size_t(n) * H + h) * kD * kD + v;
+      float s[64];
+      tmem_ld64(tb + lb + kTSM + k0, s);
+      tmem_wait_ld_regs(s);
+      float* dst = p.hT + (size_t(n) * H + h) * kD * kD + size_t(k0) * kD + v;
 #pragma unroll
-      for (int k = 0; k < kD; ++k) dst[size_t(k) * kD] = S[k];
+      for (int e = 0; e < 64; ++e) dst[size_t(e) * kD] = s[e];
     }
   }
   tc_fence_before();
   __syncthreads();
   if (warp == 0) tmem_dealloc(tb, 512);
 }
+
+#ifdef GDN_TRACE
+extern "C" int gdn_trace_read(unsigned long long* host) {
+  return cudaMemcpyFromSymbol(host, g_trace, sizeof(g_trace)) == cudaSuccess ? 0 : -1;
+}
+#endif
 
 cudaError_t launch_chain_fwd(const CUtensorMap& mW, const CUtensorMap& mQt, const CUtensorMap& mKtT,
                              const CUtensorMap& mAqk, const CUtensorMap& mU, const ChainParams& p,

@@ -45,22 +45,45 @@ __device__ __forceinline__ void bf16x8_to_f32(const uint4& u, float* f) {
   }
 }
 
-// Column `c` of (I + L)^-1 for a 64x64 strictly lower L (row-major fp32 in shared memory):
-// x_c = 1, x_r = -sum_{c <= j < r} L[r][j] x_j for r > c, x_r = 0 for r < c.
-__device__ __forceinline__ void unit_lower_inverse_column(const float* __restrict__ L, int c, float* x) {
+// Column `c` of X = (I + L)^-1 for a 64x64 strictly lower L, written to column c of sX
+// (row-major [64][64] fp32). LT is L transposed (LT[j][i] = L[i][j]) so that the 16 rows of a
+// tile read one column of L as four broadcast float4 loads. Forward substitution by 16-row
+// tiles: y = -L[tile, :16b] X[:16b, c], then the 16x16 diagonal block is solved in registers
+// (x_c = 1, x_r = 0 above the diagonal, x_r = y_r - sum_j L[r][j] x_j below it).
+__device__ __forceinline__ void unit_lower_inverse_column(const float* __restrict__ LT, float* sX, int c) {
+  for (int b = 0; b < 4; ++b) {
+    const int r0 = 16 * b;
+    float x[16];
+    if (r0 + 15 < c) {
 #pragma unroll
-  for (int r = 0; r < kC; ++r) {
-    float acc = 0.f;
-    const float4* row4 = reinterpret_cast<const float4*>(L + r * kC);
+      for (int e = 0; e < 16; ++e) x[e] = 0.f;
+    } else {
+      float y[16];
 #pragma unroll
-    for (int j4 = 0; j4 < (r + 3) / 4; ++j4) {
-      const float4 l = row4[j4];
-      acc = fmaf(l.x, x[4 * j4], acc);
-      if (4 * j4 + 1 < r) acc = fmaf(l.y, x[4 * j4 + 1], acc);
-      if (4 * j4 + 2 < r) acc = fmaf(l.z, x[4 * j4 + 2], acc);
-      if (4 * j4 + 3 < r) acc = fmaf(l.w, x[4 * j4 + 3], acc);
+      for (int e = 0; e < 16; ++e) y[e] = 0.f;
+      for (int j = c; j < r0; ++j) {
+        const float xj = sX[j * kC + c];
+        const float4* l4 = reinterpret_cast<const float4*>(LT + j * kC + r0);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const float4 l = l4[q];
+          y[4 * q] = fmaf(-l.x, xj, y[4 * q]);
+          y[4 * q + 1] = fmaf(-l.y, xj, y[4 * q + 1]);
+          y[4 * q + 2] = fmaf(-l.z, xj, y[4 * q + 2]);
+          y[4 * q + 3] = fmaf(-l.w, xj, y[4 * q + 3]);
+        }
+      }
+#pragma unroll
+      for (int r = 0; r < 16; ++r) {
+        float acc = y[r];
+#pragma unroll
+        for (int j = 0; j < r; ++j) acc = fmaf(-LT[(r0 + j) * kC + r0 + r], x[j], acc);
+        const int R = r0 + r;
+        x[r] = (R < c) ? 0.f : ((R == c) ? 1.f : acc);
+      }
     }
-    x[r] = (r < c) ? 0.f : ((r == c) ? 1.f : -acc);
+#pragma unroll
+    for (int e = 0; e < 16; ++e) sX[(r0 + e) * kC + c] = x[e];
   }
 }
 
@@ -208,59 +231,49 @@ __global__ void __launch_bounds__(kThreads, 1)
   const bool ok1 = mbar_wait(&bar_mma, 0, &abort_flag, p.status, kDevTimeoutMma);
   tc_fence_after();
   if (ok1) {
-    float* Lrow = sL + blk * (kC * kC) + il * kC;
+    float* LT = sL + blk * (kC * kC) + il;  // column il of L^T
     float* aqk = p.Aqk + tile * kTileAqk + size_t(il) * kC;
+    float kk[kC], qk[kC];
+    tmem_ld64(tb + lane_base + blk * kC, kk);
+    tmem_ld64(tb + lane_base + 128 + blk * kC, qk);
+    tmem_wait_ld_regs(kk);
+    tmem_wait_ld_regs(qk);
 #pragma unroll
-    for (int cc = 0; cc < 4; ++cc) {
-      float r[16];
-      tmem_ld16(tb + lane_base + blk * kC + cc * 16, r);
-      tmem_wait_ld();
+    for (int j = 0; j < kC; ++j) {
+      const int pj = blk * kC + j;
+      const float dec = expf(G - s_G[pj]) * s_rk[pj];
+      LT[j * kC] = (j < il) ? bi * rk * kk[j] * dec : 0.f;
+      qk[j] = (j <= il && valid) ? to_tf32(p.scale * rq * qk[j] * dec) : 0.f;
+    }
+    if (len > 0) {
+      float4* dst = reinterpret_cast<float4*>(aqk);
 #pragma unroll
-      for (int e = 0; e < 16; ++e) {
-        const int j = cc * 16 + e;
-        const int pj = blk * kC + j;
-        Lrow[j] = (j < il) ? bi * rk * s_rk[pj] * r[e] * expf(G - s_G[pj]) : 0.f;
-      }
-      tmem_ld16(tb + lane_base + 128 + blk * kC + cc * 16, r);
-      tmem_wait_ld();
-      float a[16];
-#pragma unroll
-      for (int e = 0; e < 16; ++e) {
-        const int j = cc * 16 + e;
-        const int pj = blk * kC + j;
-        a[e] = (j <= il && valid) ? to_tf32(p.scale * rq * s_rk[pj] * r[e] * expf(G - s_G[pj])) : 0.f;
-      }
-      if (len > 0) {
-        float4* dst = reinterpret_cast<float4*>(aqk + cc * 16);
-#pragma unroll
-        for (int e = 0; e < 4; ++e) dst[e] = make_float4(a[4 * e], a[4 * e + 1], a[4 * e + 2], a[4 * e + 3]);
-      }
+      for (int e = 0; e < kC / 4; ++e) dst[e] = make_float4(qk[4 * e], qk[4 * e + 1], qk[4 * e + 2], qk[4 * e + 3]);
     }
   }
   tc_fence_before();
   __syncthreads();
 
-  // Column il of A = (I + L)^-1 for this thread's chunk; then the scaled block-diagonal
-  // operands A1 = A diag(beta exp(G) r_k) and A2 = A diag(beta), bf16, K-major, 128x128.
+  // Column il of A = (I + L)^-1 for this thread's chunk (into sX, which reuses the q tile:
+  // q is no longer needed once Qt and the Q K^T product are done); then the scaled
+  // block-diagonal operands A1 = A diag(beta exp(G) r_k) and A2 = A diag(beta), bf16,
+  // K-major, 128x128, with the unit diagonal left out (added in fp32 after the MMA).
+  float* sX = reinterpret_cast<float*>(sQ) + blk * (kC * kC);
+  unit_lower_inverse_column(sL + blk * (kC * kC), sX, il);
   {
-    float x[kC];
-    unit_lower_inverse_column(sL + blk * (kC * kC), il, x);
     const float s1 = bi * expf(G) * rk, s2 = bi;
     const int col = tid;
     const __nv_bfloat16 z = __float2bfloat16_rn(0.f);
-#pragma unroll
-    for (int r = 0; r < 128; ++r) {
-      const int rb = r >> 6;
-      const uint32_t off = sw128_offset(r, col, 128, 2);
-      if (rb == blk) {
-        // the unit diagonal is applied in fp32 after the MMA (see below)
-        const float xr = (r & 63) == il ? 0.f : x[r & 63];
-        *reinterpret_cast<__nv_bfloat16*>(sA1 + off) = __float2bfloat16_rn(xr * s1);
-        *reinterpret_cast<__nv_bfloat16*>(sA2 + off) = __float2bfloat16_rn(xr * s2);
-      } else {
-        *reinterpret_cast<__nv_bfloat16*>(sA1 + off) = z;
-        *reinterpret_cast<__nv_bfloat16*>(sA2 + off) = z;
-      }
+    const int other = (blk ^ 1) * kC;
+#pragma unroll 4
+    for (int r = 0; r < kC; ++r) {
+      const float xr = r == il ? 0.f : sX[r * kC + il];
+      const uint32_t own = sw128_offset(blk * kC + r, col, 128, 2);
+      *reinterpret_cast<__nv_bfloat16*>(sA1 + own) = __float2bfloat16_rn(xr * s1);
+      *reinterpret_cast<__nv_bfloat16*>(sA2 + own) = __float2bfloat16_rn(xr * s2);
+      const uint32_t off = sw128_offset(other + r, col, 128, 2);
+      *reinterpret_cast<__nv_bfloat16*>(sA1 + off) = z;
+      *reinterpret_cast<__nv_bfloat16*>(sA2 + off) = z;
     }
   }
   fence_async_smem();
@@ -283,31 +296,29 @@ __global__ void __launch_bounds__(kThreads, 1)
   const bool ok2 = mbar_wait(&bar_mma, 1, &abort_flag, p.status, kDevTimeoutMma);
   tc_fence_after();
   if (ok2 && len > 0) {
-    float* w = p.W + tile * kTileW + size_t(il) * kD;
-    float* u = p.U + tile * kTileW + size_t(il) * kD;
     const float dw_scale = bi * expf(G) * rk, du_scale = bi;
+    for (int which = 0; which < 2; ++which) {
+      float* dst = (which == 0 ? p.W : p.U) + tile * kTileW + size_t(il) * kD;
+      const uint8_t* src = which == 0 ? sK : sV;
+      const float sc = which == 0 ? dw_scale : du_scale;
+      for (int half = 0; half < 2; ++half) {
+        float r[64];
+        tmem_ld64(tb + lane_base + which * 128 + half * 64, r);
+        tmem_wait_ld_regs(r);
 #pragma unroll
-    for (int cc = 0; cc < 8; ++cc) {
-      float r[16], kr[16], vr[16];
-      bf16x8_to_f32(*reinterpret_cast<const uint4*>(sK + sw128_offset(tid, cc * 16, 128, 2)), kr);
-      bf16x8_to_f32(*reinterpret_cast<const uint4*>(sK + sw128_offset(tid, cc * 16 + 8, 128, 2)), kr + 8);
-      bf16x8_to_f32(*reinterpret_cast<const uint4*>(sV + sw128_offset(tid, cc * 16, 128, 2)), vr);
-      bf16x8_to_f32(*reinterpret_cast<const uint4*>(sV + sw128_offset(tid, cc * 16 + 8, 128, 2)), vr + 8);
-      tmem_ld16(tb + lane_base + cc * 16, r);
-      tmem_wait_ld();
+        for (int c8 = 0; c8 < 8; ++c8) {
+          float in[8];
+          bf16x8_to_f32(*reinterpret_cast<const uint4*>(src + sw128_offset(tid, half * 64 + c8 * 8, 128, 2)), in);
 #pragma unroll
-      for (int e = 0; e < 16; ++e) r[e] = fmaf(dw_scale, kr[e], r[e]);
-      float4* dw = reinterpret_cast<float4*>(w + cc * 16);
+          for (int e = 0; e < 8; ++e) {
+            const float val = fmaf(sc, in[e], r[c8 * 8 + e]);
+            r[c8 * 8 + e] = which == 0 ? to_tf32(val) : val;
+          }
+        }
+        float4* d4 = reinterpret_cast<float4*>(dst + half * 64);
 #pragma unroll
-      for (int e = 0; e < 4; ++e)
-        dw[e] = make_float4(to_tf32(r[4 * e]), to_tf32(r[4 * e + 1]), to_tf32(r[4 * e + 2]), to_tf32(r[4 * e + 3]));
-      tmem_ld16(tb + lane_base + 128 + cc * 16, r);
-      tmem_wait_ld();
-#pragma unroll
-      for (int e = 0; e < 16; ++e) r[e] = fmaf(du_scale, vr[e], r[e]);
-      float4* du = reinterpret_cast<float4*>(u + cc * 16);
-#pragma unroll
-      for (int e = 0; e < 4; ++e) du[e] = make_float4(r[4 * e], r[4 * e + 1], r[4 * e + 2], r[4 * e + 3]);
+        for (int e = 0; e < 16; ++e) d4[e] = make_float4(r[4 * e], r[4 * e + 1], r[4 * e + 2], r[4 * e + 3]);
+      }
     }
   }
   tc_fence_before();
