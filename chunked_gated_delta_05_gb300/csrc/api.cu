@@ -100,12 +100,19 @@ int validate_desc(const gdn_desc_t* d, Problem* P) {
   return GDN_OK;
 }
 
-struct FwdLayout {
-  size_t cu, seqs, chunks, W, U, Qt, KtT, Aqk, gam, total;
+// Workspace carve-up. Forward: tables + the prepare tiles the chain reads. Backward adds
+// the transposed tiles of the reverse chain, the per-chunk saves of both chains and the
+// outputs of the feature-major backward kernel. Every region is 256-byte aligned.
+struct Layout {
+  size_t cu, seqs, chunks, W, U, Qt, KtT, Aqk, gam;               // forward
+  size_t Kt, QtT, AqkT, WT, A, Gc, rq, rk, beff;                  // prepare, backward mode
+  size_t hs, vns, dhs, dvns;                                       // chain saves
+  size_t dQt, dKt, dW, dK1, dV1, dgam;                             // feature-major backward
+  size_t total;
 };
 
-FwdLayout fwd_layout(const Problem& P) {
-  FwdLayout L{};
+Layout make_layout(const Problem& P, bool backward) {
+  Layout L{};
   size_t off = 0;
   auto take = [&](size_t bytes) {
     size_t o = off;
@@ -122,6 +129,27 @@ FwdLayout fwd_layout(const Problem& P) {
   L.KtT = take(4 * tiles * kTileKtT);
   L.Aqk = take(4 * tiles * kTileAqk);
   L.gam = take(4 * tiles * kD);
+  if (backward) {
+    L.Kt = take(4 * tiles * kTileW);
+    L.QtT = take(4 * tiles * kTileKtT);
+    L.AqkT = take(4 * tiles * kTileAqk);
+    L.WT = take(4 * tiles * kTileKtT);
+    L.A = take(4 * tiles * kTileAqk);
+    L.Gc = take(4 * tiles * kC);
+    L.rq = take(4 * tiles * kC);
+    L.rk = take(4 * tiles * kC);
+    L.beff = take(4 * tiles * kC);
+    L.hs = take(4 * tiles * kD * kD);
+    L.vns = take(4 * tiles * kTileW);
+    L.dhs = take(4 * tiles * kD * kD);
+    L.dvns = take(4 * tiles * kTileW);
+    L.dQt = take(4 * tiles * kTileW);
+    L.dKt = take(4 * tiles * kTileW);
+    L.dW = take(4 * tiles * kTileW);
+    L.dK1 = take(4 * tiles * kTileW);
+    L.dV1 = take(4 * tiles * kTileW);
+    L.dgam = take(4 * tiles * kD);
+  }
   L.total = off;
   return L;
 }
@@ -150,9 +178,39 @@ int check_cuda(cudaError_t e, const char* what) {
   return GDN_OK;
 }
 
+struct Maps {
+  CUtensorMap q, k, v, W, Qt, KtT, Aqk, U;           // forward
+  CUtensorMap Kt, AqkT, QtT, WT, VN, DVN, DW;         // backward
+};
+
+// Row-major fp32 workspace tiles as TMA sources: `cols` per row, boxes of 32 columns.
+bool tile_map(CUtensorMap* m, const char* base, uint64_t cols, uint64_t rows, uint32_t box_rows, bool swz) {
+  return make_map(m, base, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, cols, rows, cols * 4, 32, box_rows,
+                  swz ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE);
+}
+
+bool fwd_maps(const Problem& P, const void* q, const void* k, const void* v, const char* ws, const Layout& L, Maps* M) {
+  const uint64_t HD = uint64_t(P.H) * kD;
+  const uint64_t r64 = uint64_t(P.NC) * P.H * kC, r128 = uint64_t(P.NC) * P.H * kD;
+  return make_map(&M->q, q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, HD, P.R, HD * 2, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B) &&
+         make_map(&M->k, k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, HD, P.R, HD * 2, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B) &&
+         make_map(&M->v, v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, HD, P.R, HD * 2, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B) &&
+         tile_map(&M->W, ws + L.W, kD, r64, 64, true) && tile_map(&M->Qt, ws + L.Qt, kD, r64, 64, true) &&
+         tile_map(&M->U, ws + L.U, kD, r64, 64, false) && tile_map(&M->KtT, ws + L.KtT, kC, r128, 128, true) &&
+         tile_map(&M->Aqk, ws + L.Aqk, kC, r64, 64, true);
+}
+
+bool bwd_maps(const Problem& P, const char* ws, const Layout& L, Maps* M) {
+  const uint64_t r64 = uint64_t(P.NC) * P.H * kC, r128 = uint64_t(P.NC) * P.H * kD;
+  return tile_map(&M->Kt, ws + L.Kt, kD, r64, 64, true) && tile_map(&M->AqkT, ws + L.AqkT, kC, r64, 64, true) &&
+         tile_map(&M->QtT, ws + L.QtT, kC, r128, 128, true) && tile_map(&M->WT, ws + L.WT, kC, r128, 128, true) &&
+         tile_map(&M->VN, ws + L.vns, kD, r64, 64, true) && tile_map(&M->DVN, ws + L.dvns, kD, r64, 64, true) &&
+         tile_map(&M->DW, ws + L.dW, kD, r64, 64, true);
+}
+
 // Copy the packed offsets into the workspace through kernel parameters (no host staging
 // buffer outlives the call), then build the chunk and sequence tables on the device.
-int build_tables(const Problem& P, void* ws, const FwdLayout& L, int* status, cudaStream_t s) {
+int build_tables(const Problem& P, void* ws, const Layout& L, int* status, cudaStream_t s) {
   char* base = static_cast<char*>(ws);
   int* dcu = nullptr;
   if (P.packed) {
@@ -190,7 +248,7 @@ int run_fwd(const gdn_desc_t* d, const gdn_fwd_args_t* a, void* stream, bool kda
   const size_t nqk = size_t(P.R) * P.H * kD * 2;
   if (overlaps(a->o, nqk, a->q, nqk) || overlaps(a->o, nqk, a->k, nqk) || overlaps(a->o, nqk, a->v, nqk))
     return fail(GDN_EINVAL, "o must not alias q, k or v");
-  const FwdLayout L = fwd_layout(P);
+  const Layout L = make_layout(P, false);
   if (!a->workspace || a->workspace_bytes < L.total)
     return fail(GDN_EINVAL, "workspace missing or smaller than the required size");
   if (reinterpret_cast<uintptr_t>(a->workspace) & 255) return fail(GDN_EINVAL, "workspace must be 256-byte aligned");
@@ -203,18 +261,8 @@ int run_fwd(const gdn_desc_t* d, const gdn_fwd_args_t* a, void* stream, bool kda
   rc = build_tables(P, ws, L, a->status, s);
   if (rc) return rc;
 
-  CUtensorMap mq, mk, mv, mW, mQt, mKtT, mAqk, mU;
-  const uint64_t HD = uint64_t(P.H) * kD;
-  const uint64_t rows64 = uint64_t(P.NC) * P.H * kC, rows128 = uint64_t(P.NC) * P.H * kD;
-  bool ok = make_map(&mq, a->q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, HD, P.R, HD * 2, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B) &&
-            make_map(&mk, a->k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, HD, P.R, HD * 2, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B) &&
-            make_map(&mv, a->v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, HD, P.R, HD * 2, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B) &&
-            make_map(&mW, ws + L.W, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, kD, rows64, kD * 4, 32, 64, CU_TENSOR_MAP_SWIZZLE_128B) &&
-            make_map(&mQt, ws + L.Qt, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, kD, rows64, kD * 4, 32, 64, CU_TENSOR_MAP_SWIZZLE_128B) &&
-            make_map(&mU, ws + L.U, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, kD, rows64, kD * 4, 32, 64, CU_TENSOR_MAP_SWIZZLE_NONE) &&
-            make_map(&mKtT, ws + L.KtT, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, kC, rows128, kC * 4, 32, 128, CU_TENSOR_MAP_SWIZZLE_128B) &&
-            make_map(&mAqk, ws + L.Aqk, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, kC, rows64, kC * 4, 32, 64, CU_TENSOR_MAP_SWIZZLE_128B);
-  if (!ok) return fail(GDN_ECUDA, "cuTensorMapEncodeTiled failed");
+  Maps M;
+  if (!fwd_maps(P, a->q, a->k, a->v, ws, L, &M)) return fail(GDN_ECUDA, "cuTensorMapEncodeTiled failed");
 
   PrepParams pp{};
   pp.chunks = reinterpret_cast<const ChunkEntry*>(ws + L.chunks);
@@ -232,7 +280,7 @@ int run_fwd(const gdn_desc_t* d, const gdn_fwd_args_t* a, void* stream, bool kda
   pp.Aqk = reinterpret_cast<float*>(ws + L.Aqk);
   pp.gam = reinterpret_cast<float*>(ws + L.gam);
   pp.status = a->status;
-  rc = check_cuda(launch_prep_gdn(mq, mk, mv, pp, s), "prepare kernel");
+  rc = check_cuda(launch_prep_gdn(M.q, M.k, M.v, pp, s), "prepare kernel");
   if (rc) return rc;
 
   ChainParams cp{};
@@ -246,7 +294,118 @@ int run_fwd(const gdn_desc_t* d, const gdn_fwd_args_t* a, void* stream, bool kda
   cp.hT = d->output_final_state ? a->final_state : nullptr;
   cp.o = static_cast<__nv_bfloat16*>(a->o);
   cp.status = a->status;
-  return check_cuda(launch_chain_fwd(mW, mQt, mKtT, mAqk, mU, cp, s), "chain kernel");
+  return check_cuda(launch_chain_fwd(M.W, M.Qt, M.KtT, M.Aqk, M.U, cp, s), "chain kernel");
+}
+
+int run_bwd(const gdn_desc_t* d, const gdn_bwd_args_t* a, void* stream, bool kda) {
+  Problem P;
+  int rc = validate_desc(d, &P);
+  if (rc) return rc;
+  if (!a) return fail(GDN_EINVAL, "args is NULL");
+  if (!a->q || !a->k || !a->v || !a->g || !a->beta || !a->dO || !a->dq || !a->dk || !a->dv || !a->dbeta || !a->dg)
+    return fail(GDN_EINVAL, "q, k, v, g, beta, dO and every gradient output except dh0 must be non-NULL");
+  if (!aligned16(a->q) || !aligned16(a->k) || !aligned16(a->v))
+    return fail(GDN_EINVAL, "q, k and v must be 16-byte aligned");
+  const size_t nqk = size_t(P.R) * P.H * kD * 2;
+  const void* ins[] = {a->q, a->k, a->v, a->dO};
+  const void* outs[] = {a->dq, a->dk, a->dv};
+  for (const void* o : outs)
+    for (const void* i : ins)
+      if (overlaps(o, nqk, i, nqk)) return fail(GDN_EINVAL, "gradient outputs must not alias the inputs");
+  const Layout L = make_layout(P, true);
+  if (!a->workspace || a->workspace_bytes < L.total)
+    return fail(GDN_EINVAL, "workspace missing or smaller than the required size");
+  if (reinterpret_cast<uintptr_t>(a->workspace) & 255) return fail(GDN_EINVAL, "workspace must be 256-byte aligned");
+  if (kda) return fail(GDN_EUNSUPPORTED, "per-channel gate backward is not built yet");
+  rc = device_check();
+  if (rc) return rc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  char* ws = static_cast<char*>(a->workspace);
+  rc = build_tables(P, ws, L, a->status, s);
+  if (rc) return rc;
+  Maps M;
+  if (!fwd_maps(P, a->q, a->k, a->v, ws, L, &M) || !bwd_maps(P, ws, L, &M))
+    return fail(GDN_ECUDA, "cuTensorMapEncodeTiled failed");
+  auto F = [&](size_t off) { return reinterpret_cast<float*>(ws + off); };
+  const ChunkEntry* chunks = reinterpret_cast<const ChunkEntry*>(ws + L.chunks);
+
+  PrepParams pp{};
+  pp.chunks = chunks;
+  pp.NC = P.NC;
+  pp.H = P.H;
+  pp.g = a->g;
+  pp.beta = static_cast<const __nv_bfloat16*>(a->beta);
+  pp.scale = P.scale;
+  pp.l2norm = d->use_qk_l2norm;
+  pp.beta_sigmoid = d->use_beta_sigmoid;
+  pp.W = F(L.W); pp.U = F(L.U); pp.Qt = F(L.Qt); pp.KtT = F(L.KtT); pp.Aqk = F(L.Aqk); pp.gam = F(L.gam);
+  pp.Gc = F(L.Gc); pp.rq = F(L.rq); pp.rk = F(L.rk); pp.beff = F(L.beff);
+  pp.Kt = F(L.Kt); pp.QtT = F(L.QtT); pp.AqkT = F(L.AqkT); pp.WT = F(L.WT); pp.A = F(L.A);
+  pp.status = a->status;
+  rc = check_cuda(launch_prep_gdn(M.q, M.k, M.v, pp, s), "prepare kernel");
+  if (rc) return rc;
+
+  ChainParams cp{};
+  cp.seqs = reinterpret_cast<const SeqEntry*>(ws + L.seqs);
+  cp.chunks = chunks;
+  cp.N = P.N;
+  cp.H = P.H;
+  cp.gam = F(L.gam);
+  cp.h0 = a->initial_state;
+  cp.h_save = F(L.hs);
+  cp.vnew_save = F(L.vns);
+  cp.status = a->status;
+  rc = check_cuda(launch_chain_fwd(M.W, M.Qt, M.KtT, M.Aqk, M.U, cp, s), "chain kernel");
+  if (rc) return rc;
+
+  RevChainParams rp{};
+  rp.seqs = cp.seqs;
+  rp.chunks = chunks;
+  rp.N = P.N;
+  rp.H = P.H;
+  rp.gam = F(L.gam);
+  rp.dO = static_cast<const __nv_bfloat16*>(a->dO);
+  rp.dht = a->dht;
+  rp.dh0 = a->dh0;
+  rp.dh_save = F(L.dhs);
+  rp.dvn_save = F(L.dvns);
+  rp.status = a->status;
+  rc = check_cuda(launch_chain_bwd(M.Kt, M.AqkT, M.QtT, M.WT, rp, s), "reverse chain kernel");
+  if (rc) return rc;
+
+  BwdFeatParams fp{};
+  fp.chunks = chunks;
+  fp.NC = P.NC;
+  fp.H = P.H;
+  fp.h = F(L.hs);
+  fp.dh = F(L.dhs);
+  fp.dO = rp.dO;
+  fp.A = F(L.A);
+  fp.dvn = F(L.dvns);
+  fp.dQt = F(L.dQt); fp.dKt = F(L.dKt); fp.dW = F(L.dW); fp.dK1 = F(L.dK1); fp.dV1 = F(L.dV1);
+  fp.dgam = F(L.dgam);
+  fp.status = a->status;
+  rc = check_cuda(launch_bwd_feat(M.VN, M.DVN, fp, s), "feature-major backward kernel");
+  if (rc) return rc;
+
+  BwdTokParams tp{};
+  tp.chunks = chunks;
+  tp.NC = P.NC;
+  tp.H = P.H;
+  tp.scale = P.scale;
+  tp.beta_sigmoid = d->use_beta_sigmoid;
+  tp.dO = rp.dO;
+  tp.A = F(L.A);
+  tp.Gc = F(L.Gc); tp.rq = F(L.rq); tp.rk = F(L.rk); tp.beff = F(L.beff);
+  tp.dQt = F(L.dQt); tp.dKt = F(L.dKt); tp.dK1 = F(L.dK1); tp.dV1 = F(L.dV1);
+  tp.gam = F(L.gam); tp.dgam = F(L.dgam);
+  tp.dq = static_cast<__nv_bfloat16*>(a->dq);
+  tp.dk = static_cast<__nv_bfloat16*>(a->dk);
+  tp.dv = static_cast<__nv_bfloat16*>(a->dv);
+  tp.dbeta = static_cast<__nv_bfloat16*>(a->dbeta);
+  tp.dg = a->dg;
+  tp.status = a->status;
+  return check_cuda(launch_bwd_tok(M.q, M.k, M.v, M.VN, M.DW, M.DVN, tp, s), "token-major backward kernel");
 }
 
 }  // namespace
@@ -280,7 +439,7 @@ int gdn_device_supported(int device) {
 size_t gdn_fwd_workspace_size(const gdn_desc_t* desc) {
   Problem P;
   if (validate_desc(desc, &P)) return 0;
-  return fwd_layout(P).total;
+  return make_layout(P, false).total;
 }
 
 size_t kda_fwd_workspace_size(const gdn_desc_t* desc) { return gdn_fwd_workspace_size(desc); }
@@ -288,7 +447,7 @@ size_t kda_fwd_workspace_size(const gdn_desc_t* desc) { return gdn_fwd_workspace
 size_t gdn_bwd_workspace_size(const gdn_desc_t* desc) {
   Problem P;
   if (validate_desc(desc, &P)) return 0;
-  return 0;
+  return make_layout(P, true).total;
 }
 
 size_t kda_bwd_workspace_size(const gdn_desc_t* desc) { return gdn_bwd_workspace_size(desc); }
@@ -304,13 +463,13 @@ int kda_fwd(const gdn_desc_t* desc, const gdn_fwd_args_t* args, void* stream) {
 }
 
 int gdn_bwd(const gdn_desc_t* desc, const gdn_bwd_args_t* args, void* stream) {
-  (void)desc; (void)args; (void)stream;
-  return fail(GDN_EUNSUPPORTED, "backward is not built yet");
+  g_err.clear();
+  return run_bwd(desc, args, stream, false);
 }
 
 int kda_bwd(const gdn_desc_t* desc, const gdn_bwd_args_t* args, void* stream) {
-  (void)desc; (void)args; (void)stream;
-  return fail(GDN_EUNSUPPORTED, "backward is not built yet");
+  g_err.clear();
+  return run_bwd(desc, args, stream, true);
 }
 
 }  // extern "C"

@@ -39,6 +39,26 @@ struct PrepParams {
   int l2norm, beta_sigmoid;
   float *W, *U, *Qt, *KtT, *Aqk, *gam;
   float *Gc, *rq, *rk, *beff;  // optional per-token saves [NC*H*64] (KDA Gc: [NC*H*64*128]); may be null
+  // Backward-only tiles (all null in the forward):
+  float* Kt;                   // [64][128]  r_k exp(G_last - G) k   (row-major KtT^T)
+  float* QtT;                  // [128][64]  Qt^T
+  float* AqkT;                 // [64][64]   Aqk^T
+  float* WT;                   // [128][64]  W^T
+  float* A;                    // [64][64]   (I + L)^-1
+  int* status;
+};
+
+struct RevChainParams {
+  const SeqEntry* seqs;
+  const ChunkEntry* chunks;
+  int N, H;
+  int kda;
+  const float* gam;            // [NC,H,128]
+  const __nv_bfloat16* dO;     // [R,H,V]
+  const float* dht;            // [N,H,K,V] or null
+  float* dh0;                  // [N,H,K,V] or null
+  float* dh_save;              // [NC,H,K,V] gradient w.r.t. the state leaving each chunk
+  float* dvn_save;             // [NC,H,64,V] gradient w.r.t. v_new
   int* status;
 };
 
@@ -69,11 +89,44 @@ struct UploadParams {
   int vals[kMaxUploadInts];
 };
 
+struct BwdFeatParams {
+  const ChunkEntry* chunks;
+  int NC, H, kda;
+  const float* h;              // [NC,H,K,V] state entering each chunk
+  const float* dh;             // [NC,H,K,V] gradient w.r.t. the state leaving each chunk
+  const __nv_bfloat16* dO;     // [R,H,V]
+  const float* A;              // [NC,H,64,64]
+  const float* dvn;            // [NC,H,64,V]
+  float *dQt, *dKt, *dW, *dK1, *dV1;  // [NC,H,64,128] token-major
+  float* dgam;                 // [NC,H,128] (GDN: entry 0)
+  int* status;
+};
+
+struct BwdTokParams {
+  const ChunkEntry* chunks;
+  int NC, H, kda;
+  float scale;
+  int beta_sigmoid;
+  const __nv_bfloat16* dO;     // [R,H,V]
+  const float* A;              // [NC,H,64,64]
+  const float *Gc, *rq, *rk, *beff;   // per token [NC,H,64]
+  const float *dQt, *dKt, *dK1, *dV1; // [NC,H,64,128]
+  const float *gam, *dgam;     // [NC,H,128]
+  __nv_bfloat16 *dq, *dk, *dv, *dbeta;
+  float* dg;
+  int* status;
+};
+
 // Launchers (defined next to their kernels). Return the cudaError_t of the launch.
 cudaError_t launch_upload(const UploadParams& p, int* dst, cudaStream_t s);
 cudaError_t launch_tables(const TableParams& p, cudaStream_t s);
 cudaError_t launch_prep_gdn(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
                             const PrepParams& p, cudaStream_t s);
+cudaError_t launch_chain_bwd(const CUtensorMap& mKt, const CUtensorMap& mAqkT, const CUtensorMap& mQtT,
+                             const CUtensorMap& mWT, const RevChainParams& p, cudaStream_t s);
+cudaError_t launch_bwd_feat(const CUtensorMap& mVN, const CUtensorMap& mDVN, const BwdFeatParams& p, cudaStream_t s);
+cudaError_t launch_bwd_tok(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, const CUtensorMap& mVN,
+                           const CUtensorMap& mDW, const CUtensorMap& mDVN, const BwdTokParams& p, cudaStream_t s);
 cudaError_t launch_chain_fwd(const CUtensorMap& mW, const CUtensorMap& mQt, const CUtensorMap& mKtT,
                              const CUtensorMap& mAqk, const CUtensorMap& mU, const ChainParams& p,
                              cudaStream_t s);

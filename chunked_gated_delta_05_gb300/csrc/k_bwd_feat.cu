@@ -1,0 +1,215 @@
+// Backward, feature-major part: per chunk, the products contracted over the value dimension
+// that involve the carried state, computed with the key/value feature on the 128 TMEM lanes.
+//
+// With h the state entering the chunk (K x V), dh' the gradient w.r.t. the state leaving it,
+// v_new / dv_new the chunk's corrected values and their gradient, dO the output gradient and
+// A = (I + L)^-1, the chunk map's adjoint gives (see the forward chain kernel for the map):
+//   dQt  = dO h^T            (gradient of the gated, scaled queries)
+//   dW   = -dv_new h^T       (gradient of k_cumdecay = W)
+//   dKt  = v_new dh'^T       (gradient of the end-decayed keys)
+//   dK1  = A^T dW            (gradient of beta exp(G) k^, the right factor of W = A K1)
+//   dV1  = A^T dv_new        (gradient of beta v,        the right factor of U = A V1)
+//   dgam = sum over v of h (.) dh'   (per key row; summed over keys for the scalar gate)
+// GB300 mapping: one CTA per chunk and head, 128 threads, thread f = feature f = TMEM lane f.
+// h and dh' rows are loaded by their lane owner and stored to TMEM (tf32) as A operands of
+// kind::tf32 MMAs; dO^T, v_new, dv_new and A^T are SW128 K-major B operands in shared memory
+// (v_new, dv_new by TMA). Results leave as token-major fp32 rows [t][f] (coalesced: the 128
+// threads of one token row write 512 contiguous bytes).
+#include "common.cuh"
+#include "umma.cuh"
+
+namespace gdn {
+
+namespace {
+
+constexpr int kThreads = 128;
+constexpr uint32_t kOffDO = 0;        // dO   [t][v] tf32, 4 panels x 64 rows (32 KB)
+constexpr uint32_t kOffVN = 32768;    // v_new [t][v] (TMA)
+constexpr uint32_t kOffDVN = 65536;   // dv_new [t][v] (TMA)
+constexpr uint32_t kOffAT = 98304;    // A^T  [j][i] tf32, 2 panels x 64 rows (16 KB)
+constexpr uint32_t kSmemBytes = 114688 + 1024;
+constexpr uint32_t kTH = 0, kTDH = 128, kTP1 = 256, kTP2 = 320, kTP3 = 384, kTP5 = 448;
+
+__device__ __forceinline__ uint8_t* align1k(uint8_t* p) {
+  return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
+}
+
+}  // namespace
+
+__global__ void __launch_bounds__(kThreads, 1)
+    k_bwd_feat(const __grid_constant__ CUtensorMap mVN, const __grid_constant__ CUtensorMap mDVN,
+               const BwdFeatParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = align1k(smem_raw);
+  __shared__ uint64_t bar_tma, bar_mma;
+  __shared__ uint32_t tslot;
+  __shared__ int abort_flag;
+  __shared__ float s_red[4];
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int c = blockIdx.x, h = blockIdx.y, H = p.H;
+  const size_t tile = size_t(c) * H + h;
+  const ChunkEntry ch = p.chunks[c];
+  const int f = tid;
+
+  if (warp == 0) tmem_alloc(&tslot, 512);
+  if (tid == 0) {
+    abort_flag = 0;
+    mbar_init(&bar_tma, 1);
+    mbar_init(&bar_mma, 1);
+    fence_mbar_init();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tb = tslot;
+  const uint32_t tl = tb + tmem_lane_base(warp);
+  if (tid == 0) {
+    mbar_expect_tx(&bar_tma, 65536u);
+    for (int pp = 0; pp < 4; ++pp) {
+      tma_load_2d(sm + kOffVN + pp * 8192, &mVN, pp * 32, int(tile) * kC, &bar_tma);
+      tma_load_2d(sm + kOffDVN + pp * 8192, &mDVN, pp * 32, int(tile) * kC, &bar_tma);
+    }
+  }
+  // h and dh' rows -> TMEM (tf32 A operands); dgam partial sums in fp32.
+  float dg = 0.f;
+  {
+    const float4* hr = reinterpret_cast<const float4*>(p.h + tile * kD * kD + size_t(f) * kD);
+    const float4* dr = reinterpret_cast<const float4*>(p.dh + tile * kD * kD + size_t(f) * kD);
+    for (int g4 = 0; g4 < 4; ++g4) {
+      float a[32], b[32];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const float4 x = hr[g4 * 8 + e], y = dr[g4 * 8 + e];
+        a[4 * e] = x.x; a[4 * e + 1] = x.y; a[4 * e + 2] = x.z; a[4 * e + 3] = x.w;
+        b[4 * e] = y.x; b[4 * e + 1] = y.y; b[4 * e + 2] = y.z; b[4 * e + 3] = y.w;
+      }
+#pragma unroll
+      for (int e = 0; e < 32; ++e) {
+        dg = fmaf(a[e], b[e], dg);
+        a[e] = to_tf32(a[e]);
+        b[e] = to_tf32(b[e]);
+      }
+      tmem_st32(tl + kTH + 32 * g4, a);
+      tmem_st32(tl + kTDH + 32 * g4, b);
+    }
+  }
+  // dO^T operand: element (t, v=f) of the K-major [t][v] tile; rows past the chunk are zero.
+  {
+    const __nv_bfloat16* src = p.dO + (size_t(ch.x) * H + h) * kD + f;
+    for (int t = 0; t < kC; ++t) {
+      const float x = t < ch.y ? __bfloat162float(src[size_t(t) * H * kD]) : 0.f;
+      *reinterpret_cast<float*>(sm + kOffDO + sw128_offset(t, f, kC, 4)) = x;
+    }
+  }
+  // A^T operand: element (j, i) = A[i][j], threads 0..63 own column j of A.
+  if (f < kC) {
+    const float* a = p.A + tile * kTileAqk + f;
+    for (int i = 0; i < kC; ++i) *reinterpret_cast<float*>(sm + kOffAT + sw128_offset(f, i, kC, 4)) = to_tf32(a[size_t(i) * kC]);
+  }
+  tmem_wait_st();
+  fence_async_smem();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+
+  if (tid == 0) {
+    if (mbar_wait(&bar_tma, 0, &abort_flag, p.status, kDevTimeoutTma)) {
+      tc_fence_after();
+      const uint32_t id64 = idesc_tf32(128, 64);
+      const uint32_t sDO = smem_u32(sm + kOffDO), sVN = smem_u32(sm + kOffVN), sDVN = smem_u32(sm + kOffDVN);
+      for (int s = 0; s < 16; ++s) mma_tf32_ts(tb + kTP1, tb + kTH + s * 8, desc_kmajor(sDO, 8192, s), id64, s > 0);
+      for (int s = 0; s < 16; ++s) mma_tf32_ts(tb + kTP2, tb + kTH + s * 8, desc_kmajor(sDVN, 8192, s), id64, s > 0);
+      for (int s = 0; s < 16; ++s) mma_tf32_ts(tb + kTP3, tb + kTDH + s * 8, desc_kmajor(sVN, 8192, s), id64, s > 0);
+      mma_commit(&bar_mma);
+    }
+  }
+  __syncwarp();
+  const bool ok = mbar_wait(&bar_mma, 0, &abort_flag, p.status, kDevTimeoutMma);
+  tc_fence_after();
+  if (ok) {
+    float r[64];
+    // dQt and dKt: token-major rows
+    tmem_ld64(tl + kTP1, r);
+    tmem_wait_ld_regs(r);
+    float* dq = p.dQt + tile * kTileW + f;
+#pragma unroll
+    for (int t = 0; t < kC; ++t) dq[size_t(t) * kD] = r[t];
+    tmem_ld64(tl + kTP3, r);
+    tmem_wait_ld_regs(r);
+    float* dk = p.dKt + tile * kTileW + f;
+#pragma unroll
+    for (int t = 0; t < kC; ++t) dk[size_t(t) * kD] = r[t];
+    // dW^T = -(h dv_new^T): saved token-major (tf32, an MMA operand later) and written back
+    // to TMEM as the A operand of A^T dW.
+    tmem_ld64(tl + kTP2, r);
+    tmem_wait_ld_regs(r);
+    float* dw = p.dW + tile * kTileW + f;
+#pragma unroll
+    for (int t = 0; t < kC; ++t) {
+      r[t] = to_tf32(-r[t]);
+      dw[size_t(t) * kD] = r[t];
+    }
+    tmem_st32(tl + kTP2, r);
+    tmem_st32(tl + kTP2 + 32, r + 32);
+    // dv_new^T row f (lane f = value column f) as the A operand of A^T dv_new (reuses h's columns).
+    const float* dvn = p.dvn + tile * kTileW + f;
+#pragma unroll
+    for (int t = 0; t < kC; ++t) r[t] = to_tf32(dvn[size_t(t) * kD]);
+    tmem_st32(tl + kTH, r);
+    tmem_st32(tl + kTH + 32, r + 32);
+    tmem_wait_st();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (tid == 0 && ok && !abort_flag) {
+    const uint32_t id64 = idesc_tf32(128, 64);
+    const uint32_t sAT = smem_u32(sm + kOffAT);
+    for (int s = 0; s < 8; ++s) mma_tf32_ts(tb + kTP5, tb + kTP2 + s * 8, desc_kmajor(sAT, 8192, s), id64, s > 0);
+    for (int s = 0; s < 8; ++s) mma_tf32_ts(tb + kTDH, tb + kTH + s * 8, desc_kmajor(sAT, 8192, s), id64, s > 0);
+    mma_commit(&bar_mma);
+  }
+  __syncwarp();
+  const bool ok2 = ok && mbar_wait(&bar_mma, 1, &abort_flag, p.status, kDevTimeoutMma);
+  tc_fence_after();
+  if (ok2) {
+    float r[64];
+    tmem_ld64(tl + kTP5, r);
+    tmem_wait_ld_regs(r);
+    float* k1 = p.dK1 + tile * kTileW + f;
+#pragma unroll
+    for (int t = 0; t < kC; ++t) k1[size_t(t) * kD] = r[t];
+    tmem_ld64(tl + kTDH, r);
+    tmem_wait_ld_regs(r);
+    float* v1 = p.dV1 + tile * kTileW + f;
+#pragma unroll
+    for (int t = 0; t < kC; ++t) v1[size_t(t) * kD] = r[t];
+  }
+  // dgam: per key row (KDA) or summed over the block (GDN).
+  if (p.kda) {
+    p.dgam[tile * kD + f] = dg;
+  } else {
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) dg += __shfl_xor_sync(0xffffffffu, dg, off);
+    if (lane == 0) s_red[warp] = dg;
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (!p.kda && tid == 0) p.dgam[tile * kD] = s_red[0] + s_red[1] + s_red[2] + s_red[3];
+  if (warp == 0) tmem_dealloc(tb, 512);
+}
+
+cudaError_t launch_bwd_feat(const CUtensorMap& mVN, const CUtensorMap& mDVN, const BwdFeatParams& p, cudaStream_t s) {
+  static bool attr = false;
+  if (!attr) {
+    cudaError_t e = cudaFuncSetAttribute(k_bwd_feat, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    if (e != cudaSuccess) return e;
+    attr = true;
+  }
+  dim3 grid(p.NC, p.H);
+  k_bwd_feat<<<grid, kThreads, kSmemBytes, s>>>(mVN, mDVN, p);
+  return cudaGetLastError();
+}
+
+}  // namespace gdn

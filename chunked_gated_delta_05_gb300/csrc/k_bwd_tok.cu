@@ -1,0 +1,437 @@
+// Backward, token-major part (scalar gate): the chunk-local adjoint of the prepare step and
+// the assembly of the input gradients, one CTA per chunk and head.
+//
+// Chunk quantities (see the prepare kernel): G = chunk-local cumulative gate, Gam_ij =
+// exp(G_i - G_j); k^ = r_k k, q^ = r_q q (L2 norm, r = rsqrt(|x|^2 + 1e-6));
+//   L    = strictly_lower(beta_i Gam_ij (k^_i . k^_j)),  A = (I + L)^-1,
+//   W    = A K1, K1 = diag(beta exp(G)) k^;   U = A V1, V1 = diag(beta) v;
+//   Aqk  = lower(scale Gam_ij (q^_i . k^_j));  Qt = scale diag(exp(G)) q^;
+//   Kt   = diag(exp(G_last - G)) k^;           gam = exp(G_last).
+// Given dAqk = dO v_new^T, dW, dU = dv_new (feature-major kernel, reverse chain), the
+// chain rule through these definitions is:
+//   dA   = dW K1^T + dU V1^T,            dL = strictly_lower(-A^T dA A^T)
+//   dq^  = (scale dAqk (.) Gam) k^ + scale exp(G) dQt
+//   dk^  = (dL beta (.) Gam) k^ + (dL beta (.) Gam)^T k^ + (scale dAqk (.) Gam)^T q^
+//          + diag(beta exp(G)) dK1 + diag(exp(G_last - G)) dKt
+//   dbeta_i = sum_j dL_ij Gam_ij (k^_i . k^_j) + exp(G_i) (dK1_i . k^_i) + (dV1_i . v_i)
+//   dG_i = row_i(P) - col_i(P) + scale exp(G_i)(dQt_i . q^_i) + beta_i exp(G_i)(dK1_i . k^_i)
+//          - (dKt_i . Kt_i),   P = dL (.) L + dAqk (.) Aqk,
+//   dG_last += sum_i (dKt_i . Kt_i) + gam dgam
+//   dg  = reverse cumulative sum of dG within the chunk (g -> G is a cumulative sum)
+//   dq  = r_q (dq^ - q^ (q^ . dq^)),  dk likewise   (L2-norm backward)
+//   dv  = diag(beta) dV1;  dbeta_logit = dbeta sigmoid'(.) when beta was a logit.
+// GB300 mapping: all token x token products are 64-row tcgen05 MMAs (kind::tf32; the raw
+// Gram products K K^T and Q K^T are recomputed exactly with kind::f16 on the bf16 tiles), so
+// row r of a result sits in TMEM lane 32*(r/16) + r%16 and the 64 threads with lane < 16
+// own one token row each. dA is one K=256 product over [dW | dU] and [K1 | V1].
+#include "common.cuh"
+#include "umma.cuh"
+
+namespace gdn {
+
+namespace {
+
+constexpr int kThreads = 128;
+constexpr uint32_t kOffQ = 0, kOffK = 16384, kOffV = 32768;   // bf16 [64][128], 2 panels of 8 KB
+constexpr uint32_t kR1 = 49152, kR2 = 81920, kR3 = 114688, kR4 = 147456;  // 32 KB regions
+constexpr uint32_t kSmemBytes = 180224 + 1024;
+// TMEM columns (64-row results)
+constexpr uint32_t kTAqk = 0, kTKK = 64, kTQK = 128, kTdA = 192, kTX = 256, kTdL = 320;
+constexpr uint32_t kTRq = 0, kTRk = 128;  // reuse after the first products are consumed
+
+__device__ __forceinline__ uint8_t* align1k(uint8_t* p) {
+  return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
+}
+
+__device__ __forceinline__ float bf16_at(const uint8_t* tile, int row, int col) {
+  return __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(tile + sw128_offset(row, col, kC, 2)));
+}
+__device__ __forceinline__ void put32(uint8_t* tile, int rows, int row, int col, float x) {
+  *reinterpret_cast<float*>(tile + sw128_offset(row, col, rows, 4)) = x;
+}
+
+}  // namespace
+
+__global__ void __launch_bounds__(kThreads, 1)
+    k_bwd_tok(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
+              const __grid_constant__ CUtensorMap mv, const __grid_constant__ CUtensorMap mVN,
+              const __grid_constant__ CUtensorMap mDW, const __grid_constant__ CUtensorMap mDVN,
+              const BwdTokParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = align1k(smem_raw);
+  __shared__ uint64_t bar_tma, bar_mma;
+  __shared__ uint32_t tslot;
+  __shared__ int abort_flag;
+  __shared__ float s_G[kC], s_rq[kC], s_rk[kC], s_b[kC], s_dG[kC], s_db[kC], s_P[kC][kC + 1];
+  __shared__ float s_glast;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int c = blockIdx.x, h = blockIdx.y, H = p.H;
+  const size_t tile = size_t(c) * H + h;
+  const ChunkEntry ch = p.chunks[c];
+  const int len = ch.y;
+  const bool owner = lane < 16;          // owns token row rr of every 64-row MMA result
+  const int rr = 16 * warp + (lane & 15);
+  const float scale = p.scale;
+  uint8_t* sQ = sm + kOffQ;
+  uint8_t* sK = sm + kOffK;
+  uint8_t* sV = sm + kOffV;
+
+  if (warp == 0) tmem_alloc(&tslot, 512);
+  if (tid == 0) {
+    abort_flag = 0;
+    s_glast = 0.f;
+    mbar_init(&bar_tma, 1);
+    mbar_init(&bar_mma, 1);
+    fence_mbar_init();
+  }
+  if (tid < kC) {
+    const bool ok = tid < len;
+    s_G[tid] = p.Gc[tile * kC + tid];
+    s_rq[tid] = ok ? p.rq[tile * kC + tid] : 0.f;
+    s_rk[tid] = ok ? p.rk[tile * kC + tid] : 0.f;
+    s_b[tid] = ok ? p.beff[tile * kC + tid] : 0.f;
+    s_dG[tid] = 0.f;
+    s_db[tid] = 0.f;
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tb = tslot;
+  const uint32_t tl = tb + tmem_lane_base(warp);
+  const float Glast = s_G[len - 1];
+  if (tid == 0) {
+    mbar_expect_tx(&bar_tma, 3u * 16384u + 3u * 32768u);
+    for (int pp = 0; pp < 2; ++pp) {
+      const int x = h * kD + 64 * pp;
+      tma_load_2d(sQ + pp * 8192, &mq, x, ch.x, &bar_tma);
+      tma_load_2d(sK + pp * 8192, &mk, x, ch.x, &bar_tma);
+      tma_load_2d(sV + pp * 8192, &mv, x, ch.x, &bar_tma);
+    }
+    for (int pp = 0; pp < 4; ++pp) {
+      tma_load_2d(sm + kR2 + pp * 8192, &mVN, pp * 32, int(tile) * kC, &bar_tma);
+      tma_load_2d(sm + kR3 + pp * 8192, &mDW, pp * 32, int(tile) * kC, &bar_tma);
+      tma_load_2d(sm + kR4 + pp * 8192, &mDVN, pp * 32, int(tile) * kC, &bar_tma);
+    }
+  }
+  // dO as a 64-row tf32 operand [i][v] (rows past the chunk are zero).
+  {
+    const __nv_bfloat16* src = p.dO + (size_t(ch.x) * H + h) * kD + tid;
+    for (int t = 0; t < kC; ++t) put32(sm + kR1, kC, t, tid, t < len ? __bfloat162float(src[size_t(t) * H * kD]) : 0.f);
+  }
+  fence_async_smem();
+  __syncthreads();
+  const bool tma_ok = mbar_wait(&bar_tma, 0, &abort_flag, p.status, kDevTimeoutTma);
+  // Rows of q, k, v past the chunk belong to the next document (or are zero): clear them so
+  // the exact Gram products below see zeros there.
+  if (tid >= len && tid < kC) {
+    for (int c16 = 0; c16 < 16; ++c16) {
+      const uint32_t off = sw128_offset(tid, c16 * 8, kC, 2);
+      *reinterpret_cast<uint4*>(sQ + off) = make_uint4(0, 0, 0, 0);
+      *reinterpret_cast<uint4*>(sK + off) = make_uint4(0, 0, 0, 0);
+      *reinterpret_cast<uint4*>(sV + off) = make_uint4(0, 0, 0, 0);
+    }
+  }
+  fence_async_smem();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+
+  // ---- products 1: dAqk = dO v_new^T, K K^T, Q K^T
+  if (tid == 0 && tma_ok) {
+    const uint32_t id_tf = idesc_tf32(64, 64), id_bf = idesc_bf16(64, 64);
+    const uint32_t r1 = smem_u32(sm + kR1), r2 = smem_u32(sm + kR2);
+    const uint32_t q0 = smem_u32(sQ), k0 = smem_u32(sK);
+    for (int s = 0; s < 16; ++s) mma_tf32_ss(tb + kTAqk, desc_kmajor(r1, 8192, s), desc_kmajor(r2, 8192, s), id_tf, s > 0);
+    for (int s = 0; s < 8; ++s) mma_bf16_ss(tb + kTKK, desc_kmajor(k0, 8192, s), desc_kmajor(k0, 8192, s), id_bf, s > 0);
+    for (int s = 0; s < 8; ++s) mma_bf16_ss(tb + kTQK, desc_kmajor(q0, 8192, s), desc_kmajor(k0, 8192, s), id_bf, s > 0);
+    mma_commit(&bar_mma);
+  }
+  __syncwarp();
+  bool ok = tma_ok && mbar_wait(&bar_mma, 0, &abort_flag, p.status, kDevTimeoutMma);
+  tc_fence_after();
+  // ---- K1 = diag(beta exp(G) r_k) k and V1 = diag(beta) v as 64-row operands [j][d]
+  {
+    const int f = tid;
+    for (int j = 0; j < kC; ++j) {
+      const float s1 = s_b[j] * expf(s_G[j]) * s_rk[j];
+      put32(sm + kR1, kC, j, f, to_tf32(s1 * bf16_at(sK, j, f)));
+      put32(sm + kR2, kC, j, f, to_tf32(s_b[j] * bf16_at(sV, j, f)));
+    }
+  }
+  fence_async_smem();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  // ---- product 2: dA = [dW | dU] [K1 | V1]^T  (K = 256)
+  if (tid == 0 && ok) {
+    const uint32_t id_tf = idesc_tf32(64, 64);
+    const uint32_t r1 = smem_u32(sm + kR1), r2 = smem_u32(sm + kR2), r3 = smem_u32(sm + kR3), r4 = smem_u32(sm + kR4);
+    for (int s = 0; s < 16; ++s) mma_tf32_ss(tb + kTdA, desc_kmajor(r3, 8192, s), desc_kmajor(r1, 8192, s), id_tf, s > 0);
+    for (int s = 0; s < 16; ++s) mma_tf32_ss(tb + kTdA, desc_kmajor(r4, 8192, s), desc_kmajor(r2, 8192, s), id_tf, true);
+    mma_commit(&bar_mma);
+  }
+  __syncwarp();
+  ok = ok && mbar_wait(&bar_mma, 1, &abort_flag, p.status, kDevTimeoutMma);
+  tc_fence_after();
+  // ---- dL = -A^T dA A^T: X = A^T dA, then X A^T.
+  // Operands (64x64 tf32, 16 KB each): AT [j][i] (A op), dAT [m][i] (B op), A [l][m] (B op), X.
+  uint8_t* sAT = sm + kR3;
+  uint8_t* sdAT = sm + kR3 + 16384;
+  uint8_t* sA = sm + kR4;
+  uint8_t* sX = sm + kR4 + 16384;
+  {
+    float r[64];
+    tmem_ld64(tl + kTdA, r);
+    tmem_wait_ld_regs(r);
+    if (owner) {
+#pragma unroll
+      for (int m = 0; m < kC; ++m) put32(sdAT, kC, m, rr, to_tf32(r[m]));
+    }
+    if (tid < kC) {
+      const float* a = p.A + tile * kTileAqk;
+      for (int i = 0; i < kC; ++i) {
+        put32(sAT, kC, tid, i, to_tf32(a[size_t(i) * kC + tid]));   // (j = tid, i) = A[i][j]
+        put32(sA, kC, tid, i, to_tf32(a[size_t(tid) * kC + i]));    // (l = tid, m = i) = A[l][m]
+      }
+    }
+  }
+  fence_async_smem();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (tid == 0 && ok) {
+    const uint32_t id_tf = idesc_tf32(64, 64);
+    for (int s = 0; s < 8; ++s)
+      mma_tf32_ss(tb + kTX, desc_kmajor(smem_u32(sAT), 8192, s), desc_kmajor(smem_u32(sdAT), 8192, s), id_tf, s > 0);
+    mma_commit(&bar_mma);
+  }
+  __syncwarp();
+  ok = ok && mbar_wait(&bar_mma, 0, &abort_flag, p.status, kDevTimeoutMma);
+  tc_fence_after();
+  {
+    float r[64];
+    tmem_ld64(tl + kTX, r);
+    tmem_wait_ld_regs(r);
+    if (owner) {
+#pragma unroll
+      for (int m = 0; m < kC; ++m) put32(sX, kC, rr, m, to_tf32(r[m]));
+    }
+  }
+  fence_async_smem();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (tid == 0 && ok) {
+    const uint32_t id_tf = idesc_tf32(64, 64);
+    for (int s = 0; s < 8; ++s)
+      mma_tf32_ss(tb + kTdL, desc_kmajor(smem_u32(sX), 8192, s), desc_kmajor(smem_u32(sA), 8192, s), id_tf, s > 0);
+    mma_commit(&bar_mma);
+  }
+  __syncwarp();
+  ok = ok && mbar_wait(&bar_mma, 1, &abort_flag, p.status, kDevTimeoutMma);
+  tc_fence_after();
+
+  // ---- elementwise on token pairs: row owner i holds row i of dL', dAqk, KK, QK.
+  // A operands for the last products: E1 [i][j], E2^T [j][i], Nq [i][j], Nk^T [j][i];
+  // B operands: k^T [d][j], q^T [d][i] (raw tiles, tf32).
+  uint8_t* sE1 = sm + kR1;
+  uint8_t* sE2T = sm + kR1 + 16384;
+  uint8_t* sNq = sm + kR2;
+  uint8_t* sNkT = sm + kR2 + 16384;
+  uint8_t* sKT = sm + kR3;   // [128][64]: 2 panels x 128 rows
+  uint8_t* sQT = sm + kR4;
+  {
+    const int i = rr;
+    const bool vi = i < len;
+    const float Gi = s_G[i], bi = s_b[i], rki = s_rk[i], rqi = s_rq[i];
+    float rowP = 0.f, dbi = 0.f;
+    for (int half = 0; half < 2; ++half) {
+      float dl[32], nn[32], kk[32], qk[32];
+      tmem_ld32(tl + kTdL + 32 * half, dl);
+      tmem_ld32(tl + kTAqk + 32 * half, nn);
+      tmem_ld32(tl + kTKK + 32 * half, kk);
+      tmem_ld32(tl + kTQK + 32 * half, qk);
+      tmem_wait_ld_regs(dl);
+      tmem_wait_ld_regs(nn);
+      tmem_wait_ld_regs(kk);
+      tmem_wait_ld_regs(qk);
+      if (owner) {
+#pragma unroll 8
+        for (int jj = 0; jj < 32; ++jj) {
+          const int j = 32 * half + jj;
+          const float gam = (j <= i && vi) ? expf(Gi - s_G[j]) : 0.f;
+          const float D = (j < i && vi) ? -dl[jj] : 0.f;                 // dL_ij
+          const float N = (j <= i && vi) ? nn[jj] : 0.f;                 // dAqk_ij
+          const float Lij = bi * rki * s_rk[j] * kk[jj] * gam;
+          const float Aij = scale * rqi * s_rk[j] * qk[jj] * gam;
+          const float P = D * Lij + N * Aij;
+          rowP += P;
+          s_P[i][j] = P;
+          dbi = fmaf(D * rki * s_rk[j] * kk[jj], gam, dbi);
+          const float e = D * bi * gam;
+          put32(sE1, kC, i, j, to_tf32(e * s_rk[j]));
+          put32(sE2T, kC, j, i, to_tf32(e * rki));
+          const float nq = scale * N * gam;
+          put32(sNq, kC, i, j, to_tf32(nq * s_rk[j]));
+          put32(sNkT, kC, j, i, to_tf32(nq * rqi));
+        }
+      }
+    }
+    if (owner) {
+      s_dG[i] += rowP;
+      s_db[i] += dbi;
+    }
+  }
+  // transposed raw tiles k^T [d][j], q^T [d][i] (zero past the chunk: cleared above)
+  {
+    const int d = tid;
+    for (int j = 0; j < kC; ++j) {
+      put32(sKT, kD, d, j, to_tf32(bf16_at(sK, j, d)));
+      put32(sQT, kD, d, j, to_tf32(bf16_at(sQ, j, d)));
+    }
+  }
+  fence_async_smem();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  // column sums of P
+  if (tid < kC) {
+    float col = 0.f;
+    for (int i = 0; i < kC; ++i) col += s_P[i][tid];
+    s_dG[tid] -= col;
+  }
+  // ---- products 4: dq^ part = Nq k^T^T (rows i); dk^ part = E1 k + E2^T k + Nk^T q (rows)
+  if (tid == 0 && ok) {
+    const uint32_t id = idesc_tf32(64, 128);
+    const uint32_t kt = smem_u32(sKT), qt = smem_u32(sQT);
+    for (int s = 0; s < 8; ++s) mma_tf32_ss(tb + kTRq, desc_kmajor(smem_u32(sNq), 8192, s), desc_kmajor(kt, 16384, s), id, s > 0);
+    for (int s = 0; s < 8; ++s) mma_tf32_ss(tb + kTRk, desc_kmajor(smem_u32(sE1), 8192, s), desc_kmajor(kt, 16384, s), id, s > 0);
+    for (int s = 0; s < 8; ++s) mma_tf32_ss(tb + kTRk, desc_kmajor(smem_u32(sE2T), 8192, s), desc_kmajor(kt, 16384, s), id, true);
+    for (int s = 0; s < 8; ++s) mma_tf32_ss(tb + kTRk, desc_kmajor(smem_u32(sNkT), 8192, s), desc_kmajor(qt, 16384, s), id, true);
+    mma_commit(&bar_mma);
+  }
+  __syncwarp();
+  ok = ok && mbar_wait(&bar_mma, 0, &abort_flag, p.status, kDevTimeoutMma);
+  tc_fence_after();
+
+  // ---- per-token assembly (row owner t)
+  const size_t rowbase = tile * kTileW;
+  float dG_extra = 0.f, dGlast_part = 0.f, db_extra = 0.f;
+  if (ok) {
+    const int t = rr;
+    const bool vt = t < len && owner;
+    const float Gt = s_G[t], rqt = s_rq[t], rkt = s_rk[t], bt = s_b[t];
+    const float eG = expf(Gt), eL = expf(Glast - Gt);
+    // dq^ = Rq + scale exp(G) dQt, then the L2-norm backward
+    {
+      float r[128];
+      tmem_ld64(tl + kTRq, r);
+      tmem_ld64(tl + kTRq + 64, r + 64);
+      tmem_wait_ld_regs(r);
+      if (vt) {
+        const float* dqt = p.dQt + rowbase + size_t(t) * kD;
+        float dot = 0.f, qdq = 0.f;
+#pragma unroll
+        for (int d = 0; d < kD; ++d) {
+          const float qh = rqt * bf16_at(sQ, t, d);
+          const float x = dqt[d];
+          qdq = fmaf(x, qh, qdq);
+          r[d] = fmaf(scale * eG, x, r[d]);
+          dot = fmaf(r[d], qh, dot);
+        }
+        dG_extra += scale * eG * qdq;
+        __nv_bfloat16* dq = p.dq + (size_t(ch.x + t) * H + h) * kD;
+#pragma unroll
+        for (int d = 0; d < kD; ++d) {
+          const float qh = rqt * bf16_at(sQ, t, d);
+          dq[d] = __float2bfloat16_rn(rqt * (r[d] - qh * dot));
+        }
+      }
+    }
+    // dk^ = Rk + beta exp(G) dK1 + exp(G_last - G) dKt, then the L2-norm backward
+    {
+      float r[128];
+      tmem_ld64(tl + kTRk, r);
+      tmem_ld64(tl + kTRk + 64, r + 64);
+      tmem_wait_ld_regs(r);
+      if (vt) {
+        const float* dk1 = p.dK1 + rowbase + size_t(t) * kD;
+        const float* dkt = p.dKt + rowbase + size_t(t) * kD;
+        float dot = 0.f, k1k = 0.f, ktk = 0.f;
+#pragma unroll
+        for (int d = 0; d < kD; ++d) {
+          const float kh = rkt * bf16_at(sK, t, d);
+          const float a = dk1[d], b = dkt[d];
+          k1k = fmaf(a, kh, k1k);
+          ktk = fmaf(b, kh, ktk);
+          r[d] += bt * eG * a + eL * b;
+          dot = fmaf(r[d], kh, dot);
+        }
+        dG_extra += bt * eG * k1k - eL * ktk;
+        dGlast_part = eL * ktk;
+        db_extra += eG * k1k;
+        __nv_bfloat16* dk = p.dk + (size_t(ch.x + t) * H + h) * kD;
+#pragma unroll
+        for (int d = 0; d < kD; ++d) {
+          const float kh = rkt * bf16_at(sK, t, d);
+          dk[d] = __float2bfloat16_rn(rkt * (r[d] - kh * dot));
+        }
+      }
+    }
+    // dv = diag(beta) dV1; dbeta gets dV1 . v
+    if (vt) {
+      const float* dv1 = p.dV1 + rowbase + size_t(t) * kD;
+      __nv_bfloat16* dv = p.dv + (size_t(ch.x + t) * H + h) * kD;
+      float vv = 0.f;
+#pragma unroll 8
+      for (int d = 0; d < kD; ++d) {
+        const float x = dv1[d];
+        vv = fmaf(x, bf16_at(sV, t, d), vv);
+        dv[d] = __float2bfloat16_rn(bt * x);
+      }
+      db_extra += vv;
+    }
+    if (vt) {
+      s_dG[t] += dG_extra;
+      s_db[t] += db_extra;
+      atomicAdd(&s_glast, dGlast_part);
+    }
+  }
+  __syncthreads();
+  if (tid == 0 && ok) {
+    // gate: G_last collects the end-decay terms; reverse cumulative sum gives dg.
+    const float dgam = p.dgam[tile * kD];
+    float acc = s_glast + expf(Glast) * dgam;
+    for (int t = len - 1; t >= 0; --t) {
+      acc += s_dG[t];
+      s_dG[t] = acc;
+    }
+  }
+  __syncthreads();
+  if (tid < len && ok) {
+    const size_t o = size_t(ch.x + tid) * H + h;
+    p.dg[o] = s_dG[tid];
+    float db = s_db[tid];
+    if (p.beta_sigmoid) db *= s_b[tid] * (1.f - s_b[tid]);
+    p.dbeta[o] = __float2bfloat16_rn(db);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) tmem_dealloc(tb, 512);
+}
+
+cudaError_t launch_bwd_tok(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, const CUtensorMap& mVN,
+                           const CUtensorMap& mDW, const CUtensorMap& mDVN, const BwdTokParams& p, cudaStream_t s) {
+  static bool attr = false;
+  if (!attr) {
+    cudaError_t e = cudaFuncSetAttribute(k_bwd_tok, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    if (e != cudaSuccess) return e;
+    attr = true;
+  }
+  dim3 grid(p.NC, p.H);
+  k_bwd_tok<<<grid, kThreads, kSmemBytes, s>>>(mq, mk, mv, mVN, mDW, mDVN, p);
+  return cudaGetLastError();
+}
+
+}  // namespace gdn

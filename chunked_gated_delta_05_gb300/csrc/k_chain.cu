@@ -232,9 +232,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         float* vsave = p.vnew_save ? p.vnew_save + tile * kTileW + size_t(t0) * kD + v : nullptr;
 #pragma unroll
         for (int t = 0; t < 32; ++t) {
-          const float vn = u[t] - r[t];
-          if (vsave) vsave[size_t(t) * kD] = vn;
-          r[t] = to_tf32(vn);
+          r[t] = to_tf32(u[t] - r[t]);
+          if (vsave) vsave[size_t(t) * kD] = r[t];
         }
         tmem_st32(tb + lb + kTVN + t0, r);
       }

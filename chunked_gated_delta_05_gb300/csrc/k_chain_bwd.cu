@@ -1,0 +1,231 @@
+// Reverse chain kernel: the serial backward recurrence of the state gradient.
+//
+// For the forward chunk map  v_new = U - W S,  o = Qt S + Aqk v_new,
+// S' = diag(gam) S + k~^T v_new  (k~ = Kt, keys decayed to the chunk end), the adjoint,
+// with dS' the gradient w.r.t. the state leaving the chunk and dO the output gradient, is
+//   dv_new = Aqk^T dO + Kt dS'
+//   dS     = diag(gam) dS' + Qt^T dO - W^T dv_new
+// run from the last chunk of a sequence to the first, seeded by dht (or 0); the result
+// after the first chunk is dh0. The pages' backward adapters hand this reverse-order pass to
+// a native `chunk_gated_delta_rule_bwd_dhu` stage (KDA coverage page, `_AscendCKDAStages`
+// backward); the recurrence above is the exact adjoint of the forward chunk loop.
+//
+// GB300 mapping mirrors the forward chain: one CTA per (sequence, head); dS is held
+// transposed in TMEM (lane v = column v of dS) as an fp32 master copy and a tf32 copy;
+// dO^T and -dv_new^T are TMEM-resident A operands; the chunk tiles (Kt, Aqk^T, Qt^T, W^T,
+// double-buffered) are TMA-loaded SW128 B operands; every product is a 128-lane tf32 MMA.
+// The products that do not depend on dS (Aqk^T dO, Qt^T dO) are issued alongside the chain
+// ones. Eight chain warps, one producer warp; all waits bounded.
+#include "common.cuh"
+#include "umma.cuh"
+
+namespace gdn {
+
+namespace {
+
+constexpr int kChainThreads = 256;
+constexpr int kThreads = kChainThreads + 32;
+constexpr uint32_t kStage = 114688;                  // one chunk's tiles
+constexpr uint32_t kOffKt = 0;                       // [t][k]  4 panels x 64 rows   (32 KB)
+constexpr uint32_t kOffAqkT = 32768;                 // [t][i]  2 panels x 64 rows   (16 KB)
+constexpr uint32_t kOffQtT = 49152;                  // [k][i]  2 panels x 128 rows  (32 KB)
+constexpr uint32_t kOffWT = 81920;                   // [k][t]  2 panels x 128 rows  (32 KB)
+constexpr uint32_t kSmemBytes = 2 * kStage + 1024;
+constexpr uint32_t kTDM = 0, kTDT = 128, kTDV = 256, kTDN = 320, kTDO = 384;
+
+__device__ __forceinline__ uint8_t* align1k(uint8_t* p) {
+  return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
+}
+
+// dS pass for chunk c (lane v, state columns [k0, k0+64); token columns [t0, t0+32)):
+// save dS' (the gradient w.r.t. the state leaving chunk c), write its tf32 copy, pre-apply
+// the chunk decay to the master copy, and stage dO^T for this chunk as an A operand.
+__device__ __forceinline__ void rev_pass(const RevChainParams& p, int c, int h, int v, int k0, int t0,
+                                         uint32_t tl, uint64_t* ready) {
+  const size_t tile = size_t(c) * p.H + h;
+  const ChunkEntry ch = p.chunks[c];
+  float s[64];
+  tmem_ld64(tl + kTDM + k0, s);
+  tmem_wait_ld_regs(s);
+  {
+    float* ds = p.dh_save + tile * kD * kD + size_t(k0) * kD + v;
+#pragma unroll
+    for (int e = 0; e < 64; ++e) ds[size_t(e) * kD] = s[e];
+  }
+#pragma unroll
+  for (int half = 0; half < 2; ++half) {
+    float t[32];
+#pragma unroll
+    for (int e = 0; e < 32; ++e) t[e] = to_tf32(s[32 * half + e]);
+    tmem_st32(tl + kTDT + k0 + 32 * half, t);
+  }
+  if (p.kda) {
+    const float4* gam = reinterpret_cast<const float4*>(p.gam + tile * kD + k0);
+#pragma unroll
+    for (int e = 0; e < 16; ++e) {
+      const float4 g4 = gam[e];
+      s[4 * e] *= g4.x;
+      s[4 * e + 1] *= g4.y;
+      s[4 * e + 2] *= g4.z;
+      s[4 * e + 3] *= g4.w;
+    }
+  } else {
+    const float g0 = p.gam[tile * kD];
+#pragma unroll
+    for (int e = 0; e < 64; ++e) s[e] *= g0;
+  }
+  tmem_st32(tl + kTDM + k0, s);
+  tmem_st32(tl + kTDM + k0 + 32, s + 32);
+  {
+    float d[32];
+    const __nv_bfloat16* src = p.dO + (size_t(ch.x + t0) * p.H + h) * kD + v;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) d[i] = (t0 + i < ch.y) ? __bfloat162float(src[size_t(i) * p.H * kD]) : 0.f;
+    tmem_st32(tl + kTDO + t0, d);
+  }
+  tmem_wait_st();
+  tc_fence_before();
+  mbar_arrive(ready);
+}
+
+}  // namespace
+
+__global__ void __launch_bounds__(kThreads, 1)
+    k_chain_bwd(const __grid_constant__ CUtensorMap mKt, const __grid_constant__ CUtensorMap mAqkT,
+                const __grid_constant__ CUtensorMap mQtT, const __grid_constant__ CUtensorMap mWT,
+                const RevChainParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = align1k(smem_raw);
+  __shared__ uint64_t full[2], mma1, mma2, dready, vready;
+  __shared__ uint32_t tslot;
+  __shared__ int abort_flag;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int n = blockIdx.x, h = blockIdx.y, H = p.H;
+  const SeqEntry seq = p.seqs[n];
+  const int first = seq.x, nc = seq.y;
+  const int last = first + nc - 1;
+
+  if (warp == 0) tmem_alloc(&tslot, 512);
+  if (tid == 0) {
+    abort_flag = 0;
+    mbar_init(&full[0], 1);
+    mbar_init(&full[1], 1);
+    mbar_init(&mma1, 1);
+    mbar_init(&mma2, 1);
+    mbar_init(&dready, kChainThreads);
+    mbar_init(&vready, kChainThreads);
+    fence_mbar_init();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tb = tslot;
+
+  if (warp == kChainThreads / 32) {
+    if (lane == 0) {
+      auto load = [&](int c, int st) {
+        uint8_t* base = sm + st * kStage;
+        const int y64 = (c * H + h) * kC, y128 = (c * H + h) * kD;
+        mbar_expect_tx(&full[st], kStage);
+        for (int pp = 0; pp < 4; ++pp) tma_load_2d(base + kOffKt + pp * 8192, &mKt, pp * 32, y64, &full[st]);
+        for (int pp = 0; pp < 2; ++pp) {
+          tma_load_2d(base + kOffAqkT + pp * 8192, &mAqkT, pp * 32, y64, &full[st]);
+          tma_load_2d(base + kOffQtT + pp * 16384, &mQtT, pp * 32, y128, &full[st]);
+          tma_load_2d(base + kOffWT + pp * 16384, &mWT, pp * 32, y128, &full[st]);
+        }
+      };
+      load(last, 0);
+      if (nc > 1) load(last - 1, 1);
+      const uint32_t id64 = idesc_tf32(128, 64), id128 = idesc_tf32(128, 128);
+      for (int j = 0; j < nc; ++j) {
+        const int c = last - j, st = j & 1;
+        const uint32_t par = j & 1;
+        const uint32_t base = smem_u32(sm + st * kStage);
+        if (!mbar_wait(&full[st], (j >> 1) & 1, &abort_flag, p.status, kDevTimeoutTma)) break;
+        if (!mbar_wait(&dready, par, &abort_flag, p.status, kDevTimeoutSync)) break;
+        tc_fence_after();
+        // dv_new^T = dO^T Aqk + dS'^T Kt^T
+        for (int s = 0; s < 8; ++s) mma_tf32_ts(tb + kTDV, tb + kTDO + s * 8, desc_kmajor(base + kOffAqkT, 8192, s), id64, s > 0);
+        for (int s = 0; s < 16; ++s) mma_tf32_ts(tb + kTDV, tb + kTDT + s * 8, desc_kmajor(base + kOffKt, 8192, s), id64, true);
+        mma_commit(&mma1);
+        // dS^T += dO^T Qt   (master copy already holds gam dS'^T)
+        for (int s = 0; s < 8; ++s) mma_tf32_ts(tb + kTDM, tb + kTDO + s * 8, desc_kmajor(base + kOffQtT, 16384, s), id128, true);
+        if (!mbar_wait(&vready, par, &abort_flag, p.status, kDevTimeoutSync)) break;
+        tc_fence_after();
+        // dS^T += (-dv_new^T) W
+        for (int s = 0; s < 8; ++s) mma_tf32_ts(tb + kTDM, tb + kTDN + s * 8, desc_kmajor(base + kOffWT, 16384, s), id128, true);
+        mma_commit(&mma2);
+        if (!mbar_wait(&mma2, par, &abort_flag, p.status, kDevTimeoutMma)) break;
+        if (j + 2 < nc) load(c - 2, st);
+      }
+    }
+  } else if (warp < kChainThreads / 32) {
+    const int v = tid & 127, half = tid >> 7;
+    const uint32_t tl = tb + tmem_lane_base(warp);
+    const int k0 = 64 * half, t0 = 32 * half;
+    {
+      float buf[64];
+      const float* src = p.dht ? p.dht + (size_t(n) * H + h) * kD * kD + size_t(k0) * kD + v : nullptr;
+#pragma unroll
+      for (int e = 0; e < 64; ++e) buf[e] = src ? src[size_t(e) * kD] : 0.f;
+      tmem_st32(tl + kTDM + k0, buf);
+      tmem_st32(tl + kTDM + k0 + 32, buf + 32);
+      tmem_wait_st();
+    }
+    rev_pass(p, last, h, v, k0, t0, tl, &dready);
+    bool alive = true;
+    for (int j = 0; j < nc; ++j) {
+      const int c = last - j;
+      const uint32_t par = j & 1;
+      const size_t tile = size_t(c) * H + h;
+      if (!mbar_wait(&mma1, par, &abort_flag, p.status, kDevTimeoutMma)) { alive = false; break; }
+      tc_fence_after();
+      {
+        float r[32];
+        tmem_ld32(tl + kTDV + t0, r);
+        tmem_wait_ld_regs(r);
+        float* dv = p.dvn_save + tile * kTileW + size_t(t0) * kD + v;
+#pragma unroll
+        for (int t = 0; t < 32; ++t) {
+          r[t] = to_tf32(r[t]);
+          dv[size_t(t) * kD] = r[t];
+          r[t] = -r[t];
+        }
+        tmem_st32(tl + kTDN + t0, r);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(&vready);
+      if (!mbar_wait(&mma2, par, &abort_flag, p.status, kDevTimeoutMma)) { alive = false; break; }
+      tc_fence_after();
+      if (j + 1 < nc) rev_pass(p, c - 1, h, v, k0, t0, tl, &dready);
+    }
+    if (alive && p.dh0) {
+      float s[64];
+      tmem_ld64(tl + kTDM + k0, s);
+      tmem_wait_ld_regs(s);
+      float* dst = p.dh0 + (size_t(n) * H + h) * kD * kD + size_t(k0) * kD + v;
+#pragma unroll
+      for (int e = 0; e < 64; ++e) dst[size_t(e) * kD] = s[e];
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) tmem_dealloc(tb, 512);
+}
+
+cudaError_t launch_chain_bwd(const CUtensorMap& mKt, const CUtensorMap& mAqkT, const CUtensorMap& mQtT,
+                             const CUtensorMap& mWT, const RevChainParams& p, cudaStream_t s) {
+  static bool attr = false;
+  if (!attr) {
+    cudaError_t e = cudaFuncSetAttribute(k_chain_bwd, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    if (e != cudaSuccess) return e;
+    attr = true;
+  }
+  dim3 grid(p.N, p.H);
+  k_chain_bwd<<<grid, kThreads, kSmemBytes, s>>>(mKt, mAqkT, mQtT, mWT, p);
+  return cudaGetLastError();
+}
+
+}  // namespace gdn

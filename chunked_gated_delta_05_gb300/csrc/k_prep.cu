@@ -217,9 +217,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       float4* dst = reinterpret_cast<float4*>(qt + c16 * 8);
       dst[0] = make_float4(to_tf32(f[0] * fq), to_tf32(f[1] * fq), to_tf32(f[2] * fq), to_tf32(f[3] * fq));
       dst[1] = make_float4(to_tf32(f[4] * fq), to_tf32(f[5] * fq), to_tf32(f[6] * fq), to_tf32(f[7] * fq));
+      if (p.QtT) {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) p.QtT[tile * kTileKtT + size_t(c16 * 8 + e) * kC + il] = to_tf32(f[e] * fq);
+      }
       bf16x8_to_f32(*reinterpret_cast<const uint4*>(sK + off), f);
 #pragma unroll
       for (int e = 0; e < 8; ++e) ktt[size_t(c16 * 8 + e) * kC] = to_tf32(f[e] * fk);
+      if (p.Kt) {
+        float4* kt = reinterpret_cast<float4*>(p.Kt + tile * kTileW + size_t(il) * kD + c16 * 8);
+        kt[0] = make_float4(to_tf32(f[0] * fk), to_tf32(f[1] * fk), to_tf32(f[2] * fk), to_tf32(f[3] * fk));
+        kt[1] = make_float4(to_tf32(f[4] * fk), to_tf32(f[5] * fk), to_tf32(f[6] * fk), to_tf32(f[7] * fk));
+      }
     }
     if (il == 0) p.gam[tile * kD] = expf(Glast);
     if (p.Gc) p.Gc[tile * kC + il] = G;
@@ -249,6 +258,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       float4* dst = reinterpret_cast<float4*>(aqk);
 #pragma unroll
       for (int e = 0; e < kC / 4; ++e) dst[e] = make_float4(qk[4 * e], qk[4 * e + 1], qk[4 * e + 2], qk[4 * e + 3]);
+      if (p.AqkT) {
+        float* at = p.AqkT + tile * kTileAqk + il;
+#pragma unroll
+        for (int j = 0; j < kC; ++j) at[size_t(j) * kC] = qk[j];
+      }
     }
   }
   tc_fence_before();
@@ -260,6 +274,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   // K-major, 128x128, with the unit diagonal left out (added in fp32 after the MMA).
   float* sX = reinterpret_cast<float*>(sQ) + blk * (kC * kC);
   unit_lower_inverse_column(sL + blk * (kC * kC), sX, il);
+  if (p.A && len > 0) {
+    float* a = p.A + tile * kTileAqk + il;
+    for (int r = 0; r < kC; ++r) a[size_t(r) * kC] = sX[r * kC + il];
+  }
   {
     const float s1 = bi * expf(G) * rk, s2 = bi;
     const int col = tid;
@@ -318,6 +336,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         float4* d4 = reinterpret_cast<float4*>(dst + half * 64);
 #pragma unroll
         for (int e = 0; e < 16; ++e) d4[e] = make_float4(r[4 * e], r[4 * e + 1], r[4 * e + 2], r[4 * e + 3]);
+        if (which == 0 && p.WT) {
+          float* wt = p.WT + tile * kTileKtT + size_t(half * 64) * kC + il;
+#pragma unroll
+          for (int e = 0; e < 64; ++e) wt[size_t(e) * kC] = r[e];
+        }
       }
     }
   }
