@@ -47,6 +47,10 @@ SIGNATURES = {
     "gdn_bwd": ([ctypes.POINTER(Desc), ctypes.POINTER(BwdArgs), c_void_p], c_int),
     "kda_fwd": ([ctypes.POINTER(Desc), ctypes.POINTER(FwdArgs), c_void_p], c_int),
     "kda_bwd": ([ctypes.POINTER(Desc), ctypes.POINTER(BwdArgs), c_void_p], c_int),
+    "gdn_timing_enable": ([c_int], c_int),
+    "gdn_timing_kinds": ([], c_int),
+    "gdn_timing_name": ([c_int], ctypes.c_char_p),
+    "gdn_timing_read": ([c_int, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(c_int)], c_int),
 }
 
 _lock = threading.Lock()
@@ -87,3 +91,20 @@ def check(code: int) -> None:
     if code == GDN_EINVAL:
         raise ValueError(detail)
     raise GdnError(code, f"{lib.gdn_strerror(code).decode()}: {detail}")
+
+
+def timing_enable(on: bool = True) -> None:
+    """Bracket every library kernel launch with CUDA events (profiling aid)."""
+    check(load().gdn_timing_enable(int(bool(on))))
+
+
+def timing_read() -> dict:
+    """Per-kernel {name: (total_ms, launches)} since the last read; synchronizes the events."""
+    lib = load()
+    out = {}
+    for kind in range(lib.gdn_timing_kinds()):
+        ms = ctypes.c_double()
+        n = c_int()
+        check(lib.gdn_timing_read(kind, ctypes.byref(ms), ctypes.byref(n)))
+        out[lib.gdn_timing_name(kind).decode()] = (ms.value, n.value)
+    return out

@@ -178,6 +178,38 @@ int check_cuda(cudaError_t e, const char* what) {
   return GDN_OK;
 }
 
+// Optional per-kernel timing (CUDA events recorded on the launching stream around every
+// launch while enabled). Process-global and not thread-safe: a profiling aid.
+enum KernelKind { kKTables = 0, kKPrep, kKChainFwd, kKChainBwd, kKBwdFeat, kKBwdTok, kKinds };
+const char* const kKindNames[kKinds] = {"tables", "prepare", "chain_fwd", "chain_bwd", "bwd_feat", "bwd_tok"};
+struct Timing {
+  bool on = false;
+  std::vector<std::pair<cudaEvent_t, cudaEvent_t>> ev[kKinds];
+  size_t used[kKinds] = {};
+} g_tim;
+
+struct TimedLaunch {
+  int kind;
+  cudaStream_t s;
+  bool active;
+  TimedLaunch(int k, cudaStream_t st) : kind(k), s(st), active(g_tim.on) {
+    if (!active) return;
+    auto& v = g_tim.ev[kind];
+    if (g_tim.used[kind] == v.size()) {
+      cudaEvent_t a, b;
+      cudaEventCreate(&a);
+      cudaEventCreate(&b);
+      v.push_back({a, b});
+    }
+    cudaEventRecord(v[g_tim.used[kind]].first, s);
+  }
+  ~TimedLaunch() {
+    if (!active) return;
+    cudaEventRecord(g_tim.ev[kind][g_tim.used[kind]].second, s);
+    ++g_tim.used[kind];
+  }
+};
+
 struct Maps {
   CUtensorMap q, k, v, W, Qt, KtT, Aqk, U;           // forward
   CUtensorMap Kt, AqkT, QtT, WT, VN, DVN, DW;         // backward
@@ -232,6 +264,7 @@ int build_tables(const Problem& P, void* ws, const Layout& L, int* status, cudaS
   tp.seqs = reinterpret_cast<SeqEntry*>(base + L.seqs);
   tp.chunks = reinterpret_cast<ChunkEntry*>(base + L.chunks);
   tp.status = status;
+  TimedLaunch tl_(kKTables, s);
   return check_cuda(launch_tables(tp, s), "chunk tables");
 }
 
@@ -280,7 +313,10 @@ int run_fwd(const gdn_desc_t* d, const gdn_fwd_args_t* a, void* stream, bool kda
   pp.Aqk = reinterpret_cast<float*>(ws + L.Aqk);
   pp.gam = reinterpret_cast<float*>(ws + L.gam);
   pp.status = a->status;
-  rc = check_cuda(launch_prep_gdn(M.q, M.k, M.v, pp, s), "prepare kernel");
+  {
+    TimedLaunch tl_(kKPrep, s);
+    rc = check_cuda(launch_prep_gdn(M.q, M.k, M.v, pp, s), "prepare kernel");
+  }
   if (rc) return rc;
 
   ChainParams cp{};
@@ -294,6 +330,7 @@ int run_fwd(const gdn_desc_t* d, const gdn_fwd_args_t* a, void* stream, bool kda
   cp.hT = d->output_final_state ? a->final_state : nullptr;
   cp.o = static_cast<__nv_bfloat16*>(a->o);
   cp.status = a->status;
+  TimedLaunch tl_(kKChainFwd, s);
   return check_cuda(launch_chain_fwd(M.W, M.Qt, M.KtT, M.Aqk, M.U, cp, s), "chain kernel");
 }
 
@@ -342,7 +379,10 @@ int run_bwd(const gdn_desc_t* d, const gdn_bwd_args_t* a, void* stream, bool kda
   pp.Gc = F(L.Gc); pp.rq = F(L.rq); pp.rk = F(L.rk); pp.beff = F(L.beff);
   pp.Kt = F(L.Kt); pp.QtT = F(L.QtT); pp.AqkT = F(L.AqkT); pp.WT = F(L.WT); pp.A = F(L.A);
   pp.status = a->status;
-  rc = check_cuda(launch_prep_gdn(M.q, M.k, M.v, pp, s), "prepare kernel");
+  {
+    TimedLaunch tl_(kKPrep, s);
+    rc = check_cuda(launch_prep_gdn(M.q, M.k, M.v, pp, s), "prepare kernel");
+  }
   if (rc) return rc;
 
   ChainParams cp{};
@@ -355,7 +395,10 @@ int run_bwd(const gdn_desc_t* d, const gdn_bwd_args_t* a, void* stream, bool kda
   cp.h_save = F(L.hs);
   cp.vnew_save = F(L.vns);
   cp.status = a->status;
-  rc = check_cuda(launch_chain_fwd(M.W, M.Qt, M.KtT, M.Aqk, M.U, cp, s), "chain kernel");
+  {
+    TimedLaunch tl_(kKChainFwd, s);
+    rc = check_cuda(launch_chain_fwd(M.W, M.Qt, M.KtT, M.Aqk, M.U, cp, s), "chain kernel");
+  }
   if (rc) return rc;
 
   RevChainParams rp{};
@@ -370,7 +413,10 @@ int run_bwd(const gdn_desc_t* d, const gdn_bwd_args_t* a, void* stream, bool kda
   rp.dh_save = F(L.dhs);
   rp.dvn_save = F(L.dvns);
   rp.status = a->status;
-  rc = check_cuda(launch_chain_bwd(M.Kt, M.AqkT, M.QtT, M.WT, rp, s), "reverse chain kernel");
+  {
+    TimedLaunch tl_(kKChainBwd, s);
+    rc = check_cuda(launch_chain_bwd(M.Kt, M.AqkT, M.QtT, M.WT, rp, s), "reverse chain kernel");
+  }
   if (rc) return rc;
 
   BwdFeatParams fp{};
@@ -385,7 +431,10 @@ int run_bwd(const gdn_desc_t* d, const gdn_bwd_args_t* a, void* stream, bool kda
   fp.dQt = F(L.dQt); fp.dKt = F(L.dKt); fp.dW = F(L.dW); fp.dK1 = F(L.dK1); fp.dV1 = F(L.dV1);
   fp.dgam = F(L.dgam);
   fp.status = a->status;
-  rc = check_cuda(launch_bwd_feat(M.VN, M.DVN, fp, s), "feature-major backward kernel");
+  {
+    TimedLaunch tl_(kKBwdFeat, s);
+    rc = check_cuda(launch_bwd_feat(M.VN, M.DVN, fp, s), "feature-major backward kernel");
+  }
   if (rc) return rc;
 
   BwdTokParams tp{};
@@ -394,6 +443,7 @@ int run_bwd(const gdn_desc_t* d, const gdn_bwd_args_t* a, void* stream, bool kda
   tp.H = P.H;
   tp.scale = P.scale;
   tp.beta_sigmoid = d->use_beta_sigmoid;
+  tp.l2norm = d->use_qk_l2norm;
   tp.dO = rp.dO;
   tp.A = F(L.A);
   tp.Gc = F(L.Gc); tp.rq = F(L.rq); tp.rk = F(L.rk); tp.beff = F(L.beff);
@@ -405,6 +455,7 @@ int run_bwd(const gdn_desc_t* d, const gdn_bwd_args_t* a, void* stream, bool kda
   tp.dbeta = static_cast<__nv_bfloat16*>(a->dbeta);
   tp.dg = a->dg;
   tp.status = a->status;
+  TimedLaunch tl_(kKBwdTok, s);
   return check_cuda(launch_bwd_tok(M.q, M.k, M.v, M.VN, M.DW, M.DVN, tp, s), "token-major backward kernel");
 }
 
@@ -451,6 +502,32 @@ size_t gdn_bwd_workspace_size(const gdn_desc_t* desc) {
 }
 
 size_t kda_bwd_workspace_size(const gdn_desc_t* desc) { return gdn_bwd_workspace_size(desc); }
+
+int gdn_timing_enable(int enable) {
+  g_tim.on = enable != 0;
+  for (int k = 0; k < kKinds; ++k) g_tim.used[k] = 0;
+  return GDN_OK;
+}
+
+int gdn_timing_kinds(void) { return kKinds; }
+
+const char* gdn_timing_name(int kind) { return (kind >= 0 && kind < kKinds) ? kKindNames[kind] : ""; }
+
+int gdn_timing_read(int kind, double* total_ms, int* launches) {
+  if (kind < 0 || kind >= kKinds || !total_ms || !launches) return fail(GDN_EINVAL, "bad timing query");
+  double tot = 0.0;
+  for (size_t i = 0; i < g_tim.used[kind]; ++i) {
+    float ms = 0.f;
+    if (cudaEventSynchronize(g_tim.ev[kind][i].second) != cudaSuccess ||
+        cudaEventElapsedTime(&ms, g_tim.ev[kind][i].first, g_tim.ev[kind][i].second) != cudaSuccess)
+      return fail(GDN_ECUDA, "timing event query failed");
+    tot += ms;
+  }
+  *total_ms = tot;
+  *launches = int(g_tim.used[kind]);
+  g_tim.used[kind] = 0;
+  return GDN_OK;
+}
 
 int gdn_fwd(const gdn_desc_t* desc, const gdn_fwd_args_t* args, void* stream) {
   g_err.clear();

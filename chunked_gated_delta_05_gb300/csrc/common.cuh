@@ -106,7 +106,7 @@ struct BwdTokParams {
   const ChunkEntry* chunks;
   int NC, H, kda;
   float scale;
-  int beta_sigmoid;
+  int beta_sigmoid, l2norm;
   const __nv_bfloat16* dO;     // [R,H,V]
   const float* A;              // [NC,H,64,64]
   const float *Gc, *rq, *rk, *beff;   // per token [NC,H,64]

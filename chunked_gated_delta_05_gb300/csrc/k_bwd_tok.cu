@@ -341,6 +341,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           dot = fmaf(r[d], qh, dot);
         }
         dG_extra += scale * eG * qdq;
+        if (!p.l2norm) dot = 0.f;
         __nv_bfloat16* dq = p.dq + (size_t(ch.x + t) * H + h) * kD;
 #pragma unroll
         for (int d = 0; d < kD; ++d) {
@@ -371,6 +372,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         dG_extra += bt * eG * k1k - eL * ktk;
         dGlast_part = eL * ktk;
         db_extra += eG * k1k;
+        if (!p.l2norm) dot = 0.f;
         __nv_bfloat16* dk = p.dk + (size_t(ch.x + t) * H + h) * kD;
 #pragma unroll
         for (int d = 0; d < kD; ++d) {

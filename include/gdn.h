@@ -128,6 +128,16 @@ int gdn_bwd(const gdn_desc_t* desc, const gdn_bwd_args_t* args, void* stream);
 int kda_fwd(const gdn_desc_t* desc, const gdn_fwd_args_t* args, void* stream);
 int kda_bwd(const gdn_desc_t* desc, const gdn_bwd_args_t* args, void* stream);
 
+/* Profiling hooks (not part of the computation). While enabled, every kernel launch of the
+ * calls above is bracketed by CUDA events on its stream. gdn_timing_read() synchronizes the
+ * recorded events of one kernel kind (0 .. gdn_timing_kinds()-1, named by gdn_timing_name()),
+ * returns their summed device time in milliseconds and the number of launches, and clears
+ * them. Process-global state, not thread-safe; enabling resets all counters. */
+int gdn_timing_enable(int enable);
+int gdn_timing_kinds(void);
+const char* gdn_timing_name(int kind);
+int gdn_timing_read(int kind, double* total_ms, int* launches);
+
 #ifdef __cplusplus
 }
 #endif
