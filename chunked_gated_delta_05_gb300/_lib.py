@@ -47,6 +47,8 @@ SIGNATURES = {
     "gdn_bwd": ([ctypes.POINTER(Desc), ctypes.POINTER(BwdArgs), c_void_p], c_int),
     "kda_fwd": ([ctypes.POINTER(Desc), ctypes.POINTER(FwdArgs), c_void_p], c_int),
     "kda_bwd": ([ctypes.POINTER(Desc), ctypes.POINTER(BwdArgs), c_void_p], c_int),
+    "gdn_fwd_noalloc": ([ctypes.POINTER(Desc), ctypes.POINTER(FwdArgs), c_void_p], c_int),
+    "gdn_fwd_noalloc_capacity": ([], c_size_t),
     "gdn_timing_enable": ([c_int], c_int),
     "gdn_timing_kinds": ([], c_int),
     "gdn_timing_name": ([c_int], ctypes.c_char_p),

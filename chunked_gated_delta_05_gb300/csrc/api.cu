@@ -460,6 +460,10 @@ int run_bwd(const gdn_desc_t* d, const gdn_bwd_args_t* a, void* stream, bool kda
 }
 
 }  // namespace
+
+// Records `msg` as the calling thread's last error (for entry points defined in other files).
+int set_last_error(int code, const char* msg) { return fail(code, msg); }
+
 }  // namespace gdn
 
 using namespace gdn;

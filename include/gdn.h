@@ -128,6 +128,20 @@ int gdn_bwd(const gdn_desc_t* desc, const gdn_bwd_args_t* args, void* stream);
 int kda_fwd(const gdn_desc_t* desc, const gdn_fwd_args_t* args, void* stream);
 int kda_bwd(const gdn_desc_t* desc, const gdn_bwd_args_t* args, void* stream);
 
+/* Allocation-free forward (no counterpart in the paper: an interface addition for callers
+ * that cannot allocate device memory when they run the layer, such as code inside a CUDA
+ * graph capture, embedders bound to a framework allocator, or latency-critical paths).
+ * Same computation and arguments as gdn_fwd, except that args->workspace must be NULL and
+ * args->workspace_bytes 0: the workspace is a fixed static device array of
+ * gdn_fwd_noalloc_capacity() bytes (32 MiB) inside this library, held by every GPU that loads
+ * it until exit. Problems whose gdn_fwd_workspace_size() exceeds it return GDN_EINVAL. The call
+ * itself allocates nothing. All calls on a device share that array (it keeps the last call's
+ * contents; nothing needs clearing), so calls that overlap on the GPU race and must not be
+ * issued. The first call on each device, with that device current, looks the array's device
+ * address up once; make it before any stream capture. */
+int gdn_fwd_noalloc(const gdn_desc_t* desc, const gdn_fwd_args_t* args, void* stream);
+size_t gdn_fwd_noalloc_capacity(void);
+
 /* Profiling hooks (not part of the computation). While enabled, every kernel launch of the
  * calls above is bracketed by CUDA events on its stream. gdn_timing_read() synchronizes the
  * recorded events of one kernel kind (0 .. gdn_timing_kinds()-1, named by gdn_timing_name()),
