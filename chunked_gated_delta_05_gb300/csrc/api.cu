@@ -111,7 +111,7 @@ struct Layout {
   size_t total;
 };
 
-Layout make_layout(const Problem& P, bool backward) {
+Layout make_layout(const Problem& P, bool backward, bool kda = false) {
   Layout L{};
   size_t off = 0;
   auto take = [&](size_t bytes) {
@@ -135,7 +135,7 @@ Layout make_layout(const Problem& P, bool backward) {
     L.AqkT = take(4 * tiles * kTileAqk);
     L.WT = take(4 * tiles * kTileKtT);
     L.A = take(4 * tiles * kTileAqk);
-    L.Gc = take(4 * tiles * kC);
+    L.Gc = take(4 * tiles * kC * (kda ? kD : 1));
     L.rq = take(4 * tiles * kC);
     L.rk = take(4 * tiles * kC);
     L.beff = take(4 * tiles * kC);
@@ -285,7 +285,6 @@ int run_fwd(const gdn_desc_t* d, const gdn_fwd_args_t* a, void* stream, bool kda
   if (!a->workspace || a->workspace_bytes < L.total)
     return fail(GDN_EINVAL, "workspace missing or smaller than the required size");
   if (reinterpret_cast<uintptr_t>(a->workspace) & 255) return fail(GDN_EINVAL, "workspace must be 256-byte aligned");
-  if (kda) return fail(GDN_EUNSUPPORTED, "per-channel gate forward is not built yet");
   rc = device_check();
   if (rc) return rc;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -315,7 +314,8 @@ int run_fwd(const gdn_desc_t* d, const gdn_fwd_args_t* a, void* stream, bool kda
   pp.status = a->status;
   {
     TimedLaunch tl_(kKPrep, s);
-    rc = check_cuda(launch_prep_gdn(M.q, M.k, M.v, pp, s), "prepare kernel");
+    rc = check_cuda(kda ? launch_prep_kda(M.q, M.k, M.v, pp, s) : launch_prep_gdn(M.q, M.k, M.v, pp, s),
+                    "prepare kernel");
   }
   if (rc) return rc;
 
@@ -324,7 +324,7 @@ int run_fwd(const gdn_desc_t* d, const gdn_fwd_args_t* a, void* stream, bool kda
   cp.chunks = pp.chunks;
   cp.N = P.N;
   cp.H = P.H;
-  cp.kda = 0;
+  cp.kda = kda ? 1 : 0;
   cp.gam = pp.gam;
   cp.h0 = a->initial_state;
   cp.hT = d->output_final_state ? a->final_state : nullptr;

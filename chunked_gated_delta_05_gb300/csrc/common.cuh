@@ -122,6 +122,8 @@ cudaError_t launch_upload(const UploadParams& p, int* dst, cudaStream_t s);
 cudaError_t launch_tables(const TableParams& p, cudaStream_t s);
 cudaError_t launch_prep_gdn(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
                             const PrepParams& p, cudaStream_t s);
+cudaError_t launch_prep_kda(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
+                            const PrepParams& p, cudaStream_t s);
 cudaError_t launch_chain_bwd(const CUtensorMap& mKt, const CUtensorMap& mAqkT, const CUtensorMap& mQtT,
                              const CUtensorMap& mWT, const RevChainParams& p, cudaStream_t s);
 cudaError_t launch_bwd_feat(const CUtensorMap& mVN, const CUtensorMap& mDVN, const BwdFeatParams& p, cudaStream_t s);

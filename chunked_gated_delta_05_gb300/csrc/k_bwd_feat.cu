@@ -11,8 +11,8 @@
 //   dV1  = A^T dv_new        (gradient of beta v,        the right factor of U = A V1)
 //   dgam = sum over v of h (.) dh'   (per key row; summed over keys for the scalar gate)
 // GB300 mapping: one CTA per chunk and head, 128 threads, thread f = feature f = TMEM lane f.
-// h and dh' rows are loaded by their lane owner and stored to TMEM (tf32) as A operands of
-// kind::tf32 MMAs; dO^T, v_new, dv_new and A^T are SW128 K-major B operands in shared memory
+// h and dh' rows are staged through shared memory (coalesced) and stored to TMEM (tf32) by
+// their lane owner as A operands of kind::tf32 MMAs; dO^T, v_new, dv_new and A^T are SW128 K-major B operands in shared memory
 // (v_new, dv_new by TMA). Results leave as token-major fp32 rows [t][f] (coalesced: the 128
 // threads of one token row write 512 contiguous bytes).
 #include "common.cuh"
@@ -45,6 +45,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __shared__ uint32_t tslot;
   __shared__ int abort_flag;
   __shared__ float s_red[4];
+  __shared__ float s_stage[4 * 2 * 32 * 33];
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int c = blockIdx.x, h = blockIdx.y, H = p.H;
@@ -71,25 +72,38 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_load_2d(sm + kOffDVN + pp * 8192, &mDVN, pp * 32, int(tile) * kC, &bar_tma);
     }
   }
-  // h and dh' rows -> TMEM (tf32 A operands); dgam partial sums in fp32.
+  // h and dh' rows -> TMEM (tf32 A operands); dgam partial sums in fp32. Each warp stages its
+  // 32 rows in 32-column groups through shared memory so the global reads are coalesced
+  // (a lane reads 16 B of a row, 8 lanes cover 128 contiguous bytes), then every thread
+  // picks up its own row from the padded staging tile.
   float dg = 0.f;
   {
-    const float4* hr = reinterpret_cast<const float4*>(p.h + tile * kD * kD + size_t(f) * kD);
-    const float4* dr = reinterpret_cast<const float4*>(p.dh + tile * kD * kD + size_t(f) * kD);
+    float* stg_h = s_stage + warp * (2 * 32 * 33);
+    float* stg_d = stg_h + 32 * 33;
+    const float* hb = p.h + tile * kD * kD + size_t(32 * warp) * kD;
+    const float* db = p.dh + tile * kD * kD + size_t(32 * warp) * kD;
     for (int g4 = 0; g4 < 4; ++g4) {
+#pragma unroll
+      for (int it = 0; it < 8; ++it) {
+        const int row = 4 * it + (lane >> 3), col = 4 * (lane & 7);
+        const float4 x = *reinterpret_cast<const float4*>(hb + size_t(row) * kD + 32 * g4 + col);
+        const float4 y = *reinterpret_cast<const float4*>(db + size_t(row) * kD + 32 * g4 + col);
+        float* sh = stg_h + row * 33 + col;
+        float* sd = stg_d + row * 33 + col;
+        sh[0] = x.x; sh[1] = x.y; sh[2] = x.z; sh[3] = x.w;
+        sd[0] = y.x; sd[1] = y.y; sd[2] = y.z; sd[3] = y.w;
+      }
+      __syncwarp();
       float a[32], b[32];
 #pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        const float4 x = hr[g4 * 8 + e], y = dr[g4 * 8 + e];
-        a[4 * e] = x.x; a[4 * e + 1] = x.y; a[4 * e + 2] = x.z; a[4 * e + 3] = x.w;
-        b[4 * e] = y.x; b[4 * e + 1] = y.y; b[4 * e + 2] = y.z; b[4 * e + 3] = y.w;
-      }
-#pragma unroll
       for (int e = 0; e < 32; ++e) {
+        a[e] = stg_h[lane * 33 + e];
+        b[e] = stg_d[lane * 33 + e];
         dg = fmaf(a[e], b[e], dg);
         a[e] = to_tf32(a[e]);
         b[e] = to_tf32(b[e]);
       }
+      __syncwarp();
       tmem_st32(tl + kTH + 32 * g4, a);
       tmem_st32(tl + kTDH + 32 * g4, b);
     }
@@ -97,15 +111,23 @@ __global__ void __launch_bounds__(kThreads, 1)
   // dO^T operand: element (t, v=f) of the K-major [t][v] tile; rows past the chunk are zero.
   {
     const __nv_bfloat16* src = p.dO + (size_t(ch.x) * H + h) * kD + f;
-    for (int t = 0; t < kC; ++t) {
-      const float x = t < ch.y ? __bfloat162float(src[size_t(t) * H * kD]) : 0.f;
-      *reinterpret_cast<float*>(sm + kOffDO + sw128_offset(t, f, kC, 4)) = x;
+    for (int t0 = 0; t0 < kC; t0 += 32) {
+      float buf[32];
+#pragma unroll
+      for (int e = 0; e < 32; ++e) buf[e] = (t0 + e < ch.y) ? __bfloat162float(src[size_t(t0 + e) * H * kD]) : 0.f;
+#pragma unroll
+      for (int e = 0; e < 32; ++e) *reinterpret_cast<float*>(sm + kOffDO + sw128_offset(t0 + e, f, kC, 4)) = buf[e];
     }
   }
-  // A^T operand: element (j, i) = A[i][j], threads 0..63 own column j of A.
-  if (f < kC) {
-    const float* a = p.A + tile * kTileAqk + f;
-    for (int i = 0; i < kC; ++i) *reinterpret_cast<float*>(sm + kOffAT + sw128_offset(f, i, kC, 4)) = to_tf32(a[size_t(i) * kC]);
+  // A^T operand: element (j, i) = A[i][j]; thread pairs split the 64 rows i of column j = f % 64.
+  {
+    const int j = f & 63, i0 = (f >> 6) * 32;
+    const float* a = p.A + tile * kTileAqk + j;
+    float buf[32];
+#pragma unroll
+    for (int e = 0; e < 32; ++e) buf[e] = a[size_t(i0 + e) * kC];
+#pragma unroll
+    for (int e = 0; e < 32; ++e) *reinterpret_cast<float*>(sm + kOffAT + sw128_offset(j, i0 + e, kC, 4)) = to_tf32(buf[e]);
   }
   tmem_wait_st();
   fence_async_smem();

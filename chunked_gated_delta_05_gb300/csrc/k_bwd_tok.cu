@@ -29,14 +29,25 @@
 
 namespace gdn {
 
+#ifdef GDN_TRACE
+__device__ unsigned long long g_trace_tok[16];
+#define TTRACE(slot) \
+  do { if (blockIdx.x == 5 && blockIdx.y == 0 && threadIdx.x == 0) g_trace_tok[slot] = globaltimer(); } while (0)
+extern "C" int gdn_trace_tok_read(unsigned long long* host) {
+  return cudaMemcpyFromSymbol(host, g_trace_tok, sizeof(g_trace_tok)) == cudaSuccess ? 0 : -1;
+}
+#else
+#define TTRACE(slot) do {} while (0)
+#endif
+
 namespace {
 
-constexpr int kThreads = 128;
+constexpr int kThreads = 256;   // 8 warps; two threads per TMEM lane (halves of the columns)
 constexpr uint32_t kOffQ = 0, kOffK = 16384, kOffV = 32768;   // bf16 [64][128], 2 panels of 8 KB
 constexpr uint32_t kR1 = 49152, kR2 = 81920, kR3 = 114688, kR4 = 147456;  // 32 KB regions
 constexpr uint32_t kSmemBytes = 180224 + 1024;
 // TMEM columns (64-row results)
-constexpr uint32_t kTAqk = 0, kTKK = 64, kTQK = 128, kTdA = 192, kTX = 256, kTdL = 320;
+constexpr uint32_t kTAqk = 0, kTKK = 64, kTQK = 128, kTdA = 192, kTX = 192, kTdL = 192;
 constexpr uint32_t kTRq = 0, kTRk = 128;  // reuse after the first products are consumed
 
 __device__ __forceinline__ uint8_t* align1k(uint8_t* p) {
@@ -63,24 +74,24 @@ __global__ void __launch_bounds__(kThreads, 1)
   __shared__ uint32_t tslot;
   __shared__ int abort_flag;
   __shared__ float s_G[kC], s_rq[kC], s_rk[kC], s_b[kC], s_dG[kC], s_db[kC], s_P[kC][kC + 1];
-  __shared__ float s_glast;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int c = blockIdx.x, h = blockIdx.y, H = p.H;
   const size_t tile = size_t(c) * H + h;
   const ChunkEntry ch = p.chunks[c];
   const int len = ch.y;
-  const bool owner = lane < 16;          // owns token row rr of every 64-row MMA result
-  const int rr = 16 * warp + (lane & 15);
+  const int wq = warp & 3, half = warp >> 2;   // TMEM lane quadrant; which half of the columns
+  const bool owner = lane < 16;                // owns token row rr of every 64-row MMA result
+  const int rr = 16 * wq + (lane & 15);
   const float scale = p.scale;
   uint8_t* sQ = sm + kOffQ;
   uint8_t* sK = sm + kOffK;
   uint8_t* sV = sm + kOffV;
 
-  if (warp == 0) tmem_alloc(&tslot, 512);
+  TTRACE(0);
+  if (warp == 0) tmem_alloc(&tslot, 256);
   if (tid == 0) {
     abort_flag = 0;
-    s_glast = 0.f;
     mbar_init(&bar_tma, 1);
     mbar_init(&bar_mma, 1);
     fence_mbar_init();
@@ -116,12 +127,19 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   // dO as a 64-row tf32 operand [i][v] (rows past the chunk are zero).
   {
-    const __nv_bfloat16* src = p.dO + (size_t(ch.x) * H + h) * kD + tid;
-    for (int t = 0; t < kC; ++t) put32(sm + kR1, kC, t, tid, t < len ? __bfloat162float(src[size_t(t) * H * kD]) : 0.f);
+    const int v = tid & 127, t0 = 32 * half;
+    const __nv_bfloat16* src = p.dO + (size_t(ch.x) * H + h) * kD + v;
+    float buf[32];
+#pragma unroll
+    for (int e = 0; e < 32; ++e) buf[e] = (t0 + e < len) ? __bfloat162float(src[size_t(t0 + e) * H * kD]) : 0.f;
+#pragma unroll
+    for (int e = 0; e < 32; ++e) put32(sm + kR1, kC, t0 + e, v, buf[e]);
   }
   fence_async_smem();
   __syncthreads();
+  TTRACE(1);
   const bool tma_ok = mbar_wait(&bar_tma, 0, &abort_flag, p.status, kDevTimeoutTma);
+  TTRACE(2);
   // Rows of q, k, v past the chunk belong to the next document (or are zero): clear them so
   // the exact Gram products below see zeros there.
   if (tid >= len && tid < kC) {
@@ -149,11 +167,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   __syncwarp();
   bool ok = tma_ok && mbar_wait(&bar_mma, 0, &abort_flag, p.status, kDevTimeoutMma);
+  TTRACE(3);
   tc_fence_after();
   // ---- K1 = diag(beta exp(G) r_k) k and V1 = diag(beta) v as 64-row operands [j][d]
   {
-    const int f = tid;
-    for (int j = 0; j < kC; ++j) {
+    const int f = tid & 127;
+    for (int j = 32 * half; j < 32 * half + 32; ++j) {
       const float s1 = s_b[j] * expf(s_G[j]) * s_rk[j];
       put32(sm + kR1, kC, j, f, to_tf32(s1 * bf16_at(sK, j, f)));
       put32(sm + kR2, kC, j, f, to_tf32(s_b[j] * bf16_at(sV, j, f)));
@@ -163,6 +182,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  TTRACE(4);
   // ---- product 2: dA = [dW | dU] [K1 | V1]^T  (K = 256)
   if (tid == 0 && ok) {
     const uint32_t id_tf = idesc_tf32(64, 64);
@@ -173,6 +193,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   __syncwarp();
   ok = ok && mbar_wait(&bar_mma, 1, &abort_flag, p.status, kDevTimeoutMma);
+  TTRACE(5);
   tc_fence_after();
   // ---- dL = -A^T dA A^T: X = A^T dA, then X A^T.
   // Operands (64x64 tf32, 16 KB each): AT [j][i] (A op), dAT [m][i] (B op), A [l][m] (B op), X.
@@ -181,18 +202,36 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* sA = sm + kR4;
   uint8_t* sX = sm + kR4 + 16384;
   {
-    float r[64];
-    tmem_ld64(tl + kTdA, r);
+    float r[32];
+    tmem_ld32(tl + kTdA + 32 * half, r);
     tmem_wait_ld_regs(r);
     if (owner) {
 #pragma unroll
-      for (int m = 0; m < kC; ++m) put32(sdAT, kC, m, rr, to_tf32(r[m]));
+      for (int m = 0; m < 32; ++m) put32(sdAT, kC, 32 * half + m, rr, to_tf32(r[m]));
     }
-    if (tid < kC) {
+    {
+      // thread groups of 64: 0,1 write A^T (j, i) = A[i][j] for i in their half; 2,3 write
+      // A (l = j, m) = A[l][m] for m in their half.
       const float* a = p.A + tile * kTileAqk;
-      for (int i = 0; i < kC; ++i) {
-        put32(sAT, kC, tid, i, to_tf32(a[size_t(i) * kC + tid]));   // (j = tid, i) = A[i][j]
-        put32(sA, kC, tid, i, to_tf32(a[size_t(tid) * kC + i]));    // (l = tid, m = i) = A[l][m]
+      const int j = tid & 63, grp = tid >> 6;
+      {
+        const int i0 = 32 * (grp & 1);
+        float buf[32];
+        if (grp < 2) {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) buf[e] = a[size_t(i0 + e) * kC + j];
+#pragma unroll
+          for (int e = 0; e < 32; ++e) put32(sAT, kC, j, i0 + e, to_tf32(buf[e]));
+        } else {
+          const float4* row = reinterpret_cast<const float4*>(a + size_t(j) * kC + i0);
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            const float4 x = row[e];
+            buf[4 * e] = x.x; buf[4 * e + 1] = x.y; buf[4 * e + 2] = x.z; buf[4 * e + 3] = x.w;
+          }
+#pragma unroll
+          for (int e = 0; e < 32; ++e) put32(sA, kC, j, i0 + e, to_tf32(buf[e]));
+        }
       }
     }
   }
@@ -210,12 +249,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   ok = ok && mbar_wait(&bar_mma, 0, &abort_flag, p.status, kDevTimeoutMma);
   tc_fence_after();
   {
-    float r[64];
-    tmem_ld64(tl + kTX, r);
+    float r[32];
+    tmem_ld32(tl + kTX + 32 * half, r);
     tmem_wait_ld_regs(r);
     if (owner) {
 #pragma unroll
-      for (int m = 0; m < kC; ++m) put32(sX, kC, rr, m, to_tf32(r[m]));
+      for (int m = 0; m < 32; ++m) put32(sX, kC, rr, 32 * half + m, to_tf32(r[m]));
     }
   }
   fence_async_smem();
@@ -232,6 +271,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   ok = ok && mbar_wait(&bar_mma, 1, &abort_flag, p.status, kDevTimeoutMma);
   tc_fence_after();
 
+  TTRACE(6);
   // ---- elementwise on token pairs: row owner i holds row i of dL', dAqk, KK, QK.
   // A operands for the last products: E1 [i][j], E2^T [j][i], Nq [i][j], Nk^T [j][i];
   // B operands: k^T [d][j], q^T [d][i] (raw tiles, tf32).
@@ -246,7 +286,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool vi = i < len;
     const float Gi = s_G[i], bi = s_b[i], rki = s_rk[i], rqi = s_rq[i];
     float rowP = 0.f, dbi = 0.f;
-    for (int half = 0; half < 2; ++half) {
+    {
       float dl[32], nn[32], kk[32], qk[32];
       tmem_ld32(tl + kTdL + 32 * half, dl);
       tmem_ld32(tl + kTAqk + 32 * half, nn);
@@ -257,7 +297,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_wait_ld_regs(kk);
       tmem_wait_ld_regs(qk);
       if (owner) {
-#pragma unroll 8
+#pragma unroll
         for (int jj = 0; jj < 32; ++jj) {
           const int j = 32 * half + jj;
           const float gam = (j <= i && vi) ? expf(Gi - s_G[j]) : 0.f;
@@ -279,14 +319,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     if (owner) {
-      s_dG[i] += rowP;
-      s_db[i] += dbi;
+      atomicAdd(&s_dG[i], rowP);
+      atomicAdd(&s_db[i], dbi);
     }
   }
   // transposed raw tiles k^T [d][j], q^T [d][i] (zero past the chunk: cleared above)
   {
-    const int d = tid;
-    for (int j = 0; j < kC; ++j) {
+    const int d = tid & 127;
+    for (int j = 32 * half; j < 32 * half + 32; ++j) {
       put32(sKT, kD, d, j, to_tf32(bf16_at(sK, j, d)));
       put32(sQT, kD, d, j, to_tf32(bf16_at(sQ, j, d)));
     }
@@ -295,6 +335,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  TTRACE(7);
   // column sums of P
   if (tid < kC) {
     float col = 0.f;
@@ -315,96 +356,128 @@ __global__ void __launch_bounds__(kThreads, 1)
   ok = ok && mbar_wait(&bar_mma, 0, &abort_flag, p.status, kDevTimeoutMma);
   tc_fence_after();
 
-  // ---- per-token assembly (row owner t)
-  const size_t rowbase = tile * kTileW;
-  float dG_extra = 0.f, dGlast_part = 0.f, db_extra = 0.f;
+  TTRACE(8);
+  // ---- per-token assembly. Owner threads stage their rows of the two last products from
+  // TMEM into padded shared rows; then each warp takes whole token rows (lane l: columns
+  // 4l..4l+3) with coalesced float4 loads of the fp32 intermediates and shuffle-reduced dots.
+  constexpr int kPad = 132;                                  // padded row stride (floats)
+  float* sRq = reinterpret_cast<float*>(sm + kR1);           // [64][132]
+  float* sRk = sRq + kC * kPad;                              // [64][132]
   if (ok) {
-    const int t = rr;
-    const bool vt = t < len && owner;
-    const float Gt = s_G[t], rqt = s_rq[t], rkt = s_rk[t], bt = s_b[t];
-    const float eG = expf(Gt), eL = expf(Glast - Gt);
-    // dq^ = Rq + scale exp(G) dQt, then the L2-norm backward
     {
-      float r[128];
-      tmem_ld64(tl + kTRq, r);
-      tmem_ld64(tl + kTRq + 64, r + 64);
-      tmem_wait_ld_regs(r);
-      if (vt) {
-        const float* dqt = p.dQt + rowbase + size_t(t) * kD;
-        float dot = 0.f, qdq = 0.f;
+      const int which = half;
+      float* dst = (which == 0 ? sRq : sRk) + rr * kPad;
+      const uint32_t col = which == 0 ? kTRq : kTRk;
+      for (int g4 = 0; g4 < 4; ++g4) {
+        float r[32];
+        tmem_ld32(tl + col + 32 * g4, r);
+        tmem_wait_ld_regs(r);
+        if (owner) {
+          float4* d4 = reinterpret_cast<float4*>(dst + 32 * g4);
 #pragma unroll
-        for (int d = 0; d < kD; ++d) {
-          const float qh = rqt * bf16_at(sQ, t, d);
-          const float x = dqt[d];
-          qdq = fmaf(x, qh, qdq);
-          r[d] = fmaf(scale * eG, x, r[d]);
-          dot = fmaf(r[d], qh, dot);
-        }
-        dG_extra += scale * eG * qdq;
-        if (!p.l2norm) dot = 0.f;
-        __nv_bfloat16* dq = p.dq + (size_t(ch.x + t) * H + h) * kD;
-#pragma unroll
-        for (int d = 0; d < kD; ++d) {
-          const float qh = rqt * bf16_at(sQ, t, d);
-          dq[d] = __float2bfloat16_rn(rqt * (r[d] - qh * dot));
+          for (int e = 0; e < 8; ++e) d4[e] = make_float4(r[4 * e], r[4 * e + 1], r[4 * e + 2], r[4 * e + 3]);
         }
       }
-    }
-    // dk^ = Rk + beta exp(G) dK1 + exp(G_last - G) dKt, then the L2-norm backward
-    {
-      float r[128];
-      tmem_ld64(tl + kTRk, r);
-      tmem_ld64(tl + kTRk + 64, r + 64);
-      tmem_wait_ld_regs(r);
-      if (vt) {
-        const float* dk1 = p.dK1 + rowbase + size_t(t) * kD;
-        const float* dkt = p.dKt + rowbase + size_t(t) * kD;
-        float dot = 0.f, k1k = 0.f, ktk = 0.f;
-#pragma unroll
-        for (int d = 0; d < kD; ++d) {
-          const float kh = rkt * bf16_at(sK, t, d);
-          const float a = dk1[d], b = dkt[d];
-          k1k = fmaf(a, kh, k1k);
-          ktk = fmaf(b, kh, ktk);
-          r[d] += bt * eG * a + eL * b;
-          dot = fmaf(r[d], kh, dot);
-        }
-        dG_extra += bt * eG * k1k - eL * ktk;
-        dGlast_part = eL * ktk;
-        db_extra += eG * k1k;
-        if (!p.l2norm) dot = 0.f;
-        __nv_bfloat16* dk = p.dk + (size_t(ch.x + t) * H + h) * kD;
-#pragma unroll
-        for (int d = 0; d < kD; ++d) {
-          const float kh = rkt * bf16_at(sK, t, d);
-          dk[d] = __float2bfloat16_rn(rkt * (r[d] - kh * dot));
-        }
-      }
-    }
-    // dv = diag(beta) dV1; dbeta gets dV1 . v
-    if (vt) {
-      const float* dv1 = p.dV1 + rowbase + size_t(t) * kD;
-      __nv_bfloat16* dv = p.dv + (size_t(ch.x + t) * H + h) * kD;
-      float vv = 0.f;
-#pragma unroll 8
-      for (int d = 0; d < kD; ++d) {
-        const float x = dv1[d];
-        vv = fmaf(x, bf16_at(sV, t, d), vv);
-        dv[d] = __float2bfloat16_rn(bt * x);
-      }
-      db_extra += vv;
-    }
-    if (vt) {
-      s_dG[t] += dG_extra;
-      s_db[t] += db_extra;
-      atomicAdd(&s_glast, dGlast_part);
     }
   }
   __syncthreads();
+  if (ok) {
+    const size_t rowbase = tile * kTileW;
+    const int d0 = 4 * lane;
+    auto bf4 = [&](const uint8_t* tl16, int t, float* f) {
+      const uint2 u = *reinterpret_cast<const uint2*>(tl16 + sw128_offset(t, d0, kC, 2));
+      const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.x));
+      const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.y));
+      f[0] = a.x; f[1] = a.y; f[2] = b.x; f[3] = b.y;
+    };
+    auto store4 = [&](__nv_bfloat16* dst, const float* x) {
+      __nv_bfloat162 a = __floats2bfloat162_rn(x[0], x[1]), b = __floats2bfloat162_rn(x[2], x[3]);
+      uint2 u;
+      u.x = *reinterpret_cast<uint32_t*>(&a);
+      u.y = *reinterpret_cast<uint32_t*>(&b);
+      *reinterpret_cast<uint2*>(dst) = u;
+    };
+    auto allsum = [](float x) {
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) x += __shfl_xor_sync(0xffffffffu, x, off);
+      return x;
+    };
+#pragma unroll 2
+    for (int t = warp; t < len; t += 8) {
+      const float Gt = s_G[t], rqt = s_rq[t], rkt = s_rk[t], bt = s_b[t];
+      const float eG = expf(Gt), eL = expf(Glast - Gt);
+      const size_t orow = (size_t(ch.x + t) * H + h) * kD + d0;
+      // dq
+      float qv[4], a[4], x[4];
+      bf4(sQ, t, qv);
+      const float4 dqt = *reinterpret_cast<const float4*>(p.dQt + rowbase + size_t(t) * kD + d0);
+      const float4 rq4 = *reinterpret_cast<const float4*>(sRq + t * kPad + d0);
+      const float dqtv[4] = {dqt.x, dqt.y, dqt.z, dqt.w}, rqv[4] = {rq4.x, rq4.y, rq4.z, rq4.w};
+      float dot = 0.f, qdq = 0.f;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float qh = rqt * qv[e];
+        a[e] = fmaf(scale * eG, dqtv[e], rqv[e]);
+        dot = fmaf(a[e], qh, dot);
+        qdq = fmaf(dqtv[e], qh, qdq);
+      }
+      dot = allsum(dot);
+      qdq = allsum(qdq);
+      if (!p.l2norm) dot = 0.f;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) x[e] = rqt * (a[e] - rqt * qv[e] * dot);
+      store4(p.dq + orow, x);
+      // dk
+      float kv[4];
+      bf4(sK, t, kv);
+      const float4 k1 = *reinterpret_cast<const float4*>(p.dK1 + rowbase + size_t(t) * kD + d0);
+      const float4 kt = *reinterpret_cast<const float4*>(p.dKt + rowbase + size_t(t) * kD + d0);
+      const float4 rk4 = *reinterpret_cast<const float4*>(sRk + t * kPad + d0);
+      const float k1v[4] = {k1.x, k1.y, k1.z, k1.w}, ktv[4] = {kt.x, kt.y, kt.z, kt.w};
+      const float rkv[4] = {rk4.x, rk4.y, rk4.z, rk4.w};
+      float kdot = 0.f, k1k = 0.f, ktk = 0.f;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float kh = rkt * kv[e];
+        a[e] = rkv[e] + bt * eG * k1v[e] + eL * ktv[e];
+        kdot = fmaf(a[e], kh, kdot);
+        k1k = fmaf(k1v[e], kh, k1k);
+        ktk = fmaf(ktv[e], kh, ktk);
+      }
+      kdot = allsum(kdot);
+      k1k = allsum(k1k);
+      ktk = allsum(ktk);
+      if (!p.l2norm) kdot = 0.f;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) x[e] = rkt * (a[e] - rkt * kv[e] * kdot);
+      store4(p.dk + orow, x);
+      // dv and the v part of dbeta
+      float vv4[4];
+      bf4(sV, t, vv4);
+      const float4 v1 = *reinterpret_cast<const float4*>(p.dV1 + rowbase + size_t(t) * kD + d0);
+      const float v1v[4] = {v1.x, v1.y, v1.z, v1.w};
+      float vv = 0.f;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        vv = fmaf(v1v[e], vv4[e], vv);
+        x[e] = bt * v1v[e];
+      }
+      vv = allsum(vv);
+      store4(p.dv + orow, x);
+      if (lane == 0) {
+        s_dG[t] += scale * eG * qdq + bt * eG * k1k - eL * ktk;
+        s_db[t] += eG * k1k + vv;
+        s_P[t][0] = eL * ktk;   // this row's share of dG_last (column 0 of P is free now)
+      }
+    }
+  }
+  __syncthreads();
+  TTRACE(9);
   if (tid == 0 && ok) {
     // gate: G_last collects the end-decay terms; reverse cumulative sum gives dg.
     const float dgam = p.dgam[tile * kD];
-    float acc = s_glast + expf(Glast) * dgam;
+    float acc = expf(Glast) * dgam;
+    for (int t = 0; t < len; ++t) acc += s_P[t][0];
     for (int t = len - 1; t >= 0; --t) {
       acc += s_dG[t];
       s_dG[t] = acc;
@@ -420,7 +493,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == 0) tmem_dealloc(tb, 512);
+  TTRACE(10);
+  if (warp == 0) tmem_dealloc(tb, 256);
 }
 
 cudaError_t launch_bwd_tok(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, const CUtensorMap& mVN,

@@ -1,0 +1,381 @@
+// Prepare kernel for Kimi Delta Attention (per-channel gate), one chunk per CTA.
+//
+// With G[t][c] the chunk-local cumulative gate of key channel c (the `gk` slot of the KDA
+// staged native interface, `_KDAPrepared.gk`, kimi_delta_attention_ascendc.py coverage page)
+// and k^, q^ the L2-normalised rows, the chunk quantities are those of the scalar-gate
+// prepare kernel with every decay taken per channel:
+//   L_ij   = beta_i sum_c k^_ic k^_jc exp(G_ic - G_jc), i > j;      A = (I + L)^-1
+//   Aqk_ij = scale sum_c q^_ic k^_jc exp(G_ic - G_jc), i >= j
+//   W      = A K1,  K1_jc = beta_j exp(G_jc) k^_jc;                 U = A diag(beta) v
+//   Qt_ic  = scale exp(G_ic) q^_ic;  KtT_ci = exp(G_last,c - G_ic) k^_ic;  gam_c = exp(G_last,c)
+//
+// GB300 mapping. exp(G_ic - G_jc) does not factor into bounded row and column terms over a
+// whole chunk (G spans tens of units), so each 16-row block I of the chunk gets its own
+// reference row r_I = 16 I: exp(G_ic - G_jc) = exp(G_ic - G_{r_I,c}) exp(G_{r_I,c} - G_jc).
+// For i in block I the first factor is <= 1, and for j < r_I the second one is too; for j in
+// block I it is at most the decay across 15 tokens. One stacked 128-row tf32 operand (keys
+// then queries, each row scaled by its block's reference) times B_I = k^ exp(G_{r_I} - G)
+// (rows j <= 16 I + 15) gives, in four 128-lane MMAs, every row block of both L and Aqk.
+// The unit-lower inverse and the WY products follow the scalar-gate kernel: W's right factor
+// carries the per-channel decay (tf32, thread-written); U uses the raw v tile (bf16); the
+// unit diagonal of A is applied in fp32 from the exact inputs.
+#include "common.cuh"
+#include "umma.cuh"
+
+namespace gdn {
+
+namespace {
+
+constexpr int kThreads = 128;
+constexpr int kGP = kD + 1;                                // padded row stride of G (floats)
+constexpr uint32_t kOffQ = 0, kOffK = 16384, kOffV = 32768;  // bf16 [64][128] tiles
+constexpr uint32_t kOffG = 49152;                          // fp32 [64][129]
+constexpr uint32_t kOffAS = 83968;                         // stacked A operand, tf32 [128][128] (64 KB)
+constexpr uint32_t kOffB = 149504;                         // two B_I operands, tf32 [64][128] (2 x 32 KB)
+constexpr uint32_t kSmemBytes = kOffB + 65536 + 1024;
+// Later phases reuse the operand region [kOffAS, kOffB + 64 KB):
+constexpr uint32_t kOffLT = kOffAS;                        // L^T fp32 [64][64]
+constexpr uint32_t kOffX = kOffAS + 16384;                 // inverse columns fp32 [64][64]
+constexpr uint32_t kOffA1 = kOffAS + 32768;                // (A - I) diag(beta r_k), tf32 [64][64]
+constexpr uint32_t kOffA2 = kOffAS + 49152;                // (A - I) diag(beta), bf16 [64][64]
+constexpr uint32_t kOffK1T = kOffB;                        // (k (.) exp(G))^T, tf32 [128][64]
+
+__device__ __forceinline__ uint8_t* align1k(uint8_t* p) {
+  return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
+}
+__device__ __forceinline__ float bf16_at(const uint8_t* tile, int row, int col) {
+  return __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(tile + sw128_offset(row, col, kC, 2)));
+}
+__device__ __forceinline__ void put32(uint8_t* tile, int rows, int row, int col, float x) {
+  *reinterpret_cast<float*>(tile + sw128_offset(row, col, rows, 4)) = x;
+}
+
+// Column c of (I + L)^-1 from L^T in shared memory (see the scalar-gate prepare kernel).
+__device__ __forceinline__ void inverse_column(const float* __restrict__ LT, float* sX, int c) {
+  for (int b = 0; b < 4; ++b) {
+    const int r0 = 16 * b;
+    float x[16];
+    if (r0 + 15 < c) {
+#pragma unroll
+      for (int e = 0; e < 16; ++e) x[e] = 0.f;
+    } else {
+      float y[16];
+#pragma unroll
+      for (int e = 0; e < 16; ++e) y[e] = 0.f;
+      for (int j = c; j < r0; ++j) {
+        const float xj = sX[j * kC + c];
+        const float4* l4 = reinterpret_cast<const float4*>(LT + j * kC + r0);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const float4 l = l4[q];
+          y[4 * q] = fmaf(-l.x, xj, y[4 * q]);
+          y[4 * q + 1] = fmaf(-l.y, xj, y[4 * q + 1]);
+          y[4 * q + 2] = fmaf(-l.z, xj, y[4 * q + 2]);
+          y[4 * q + 3] = fmaf(-l.w, xj, y[4 * q + 3]);
+        }
+      }
+#pragma unroll
+      for (int r = 0; r < 16; ++r) {
+        float acc = y[r];
+#pragma unroll
+        for (int j = 0; j < r; ++j) acc = fmaf(-LT[(r0 + j) * kC + r0 + r], x[j], acc);
+        const int R = r0 + r;
+        x[r] = (R < c) ? 0.f : ((R == c) ? 1.f : acc);
+      }
+    }
+#pragma unroll
+    for (int e = 0; e < 16; ++e) sX[(r0 + e) * kC + c] = x[e];
+  }
+}
+
+}  // namespace
+
+__global__ void __launch_bounds__(kThreads, 1)
+    k_prep_kda(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
+               const __grid_constant__ CUtensorMap mv, const PrepParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = align1k(smem_raw);
+  uint8_t* sQ = sm + kOffQ;
+  uint8_t* sK = sm + kOffK;
+  uint8_t* sV = sm + kOffV;
+  float* sG = reinterpret_cast<float*>(sm + kOffG);
+  __shared__ uint64_t bar_tma, bar_mma;
+  __shared__ uint32_t tslot;
+  __shared__ int abort_flag;
+  __shared__ float s_rq[kC], s_rk[kC], s_b[kC], s_gl[kD];
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int c_idx = blockIdx.x, h = blockIdx.y, H = p.H;
+  const size_t tile = size_t(c_idx) * H + h;
+  const ChunkEntry ch = p.chunks[c_idx];
+  const int len = ch.y;
+
+  if (warp == 0) tmem_alloc(&tslot, 256);
+  if (tid == 0) {
+    abort_flag = 0;
+    mbar_init(&bar_tma, 1);
+    mbar_init(&bar_mma, 1);
+    fence_mbar_init();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tb = tslot;
+  const uint32_t tl = tb + tmem_lane_base(warp);
+  if (tid == 0) {
+    mbar_expect_tx(&bar_tma, 3u * 16384u);
+    for (int pp = 0; pp < 2; ++pp) {
+      const int x = h * kD + 64 * pp;
+      tma_load_2d(sQ + pp * 8192, &mq, x, ch.x, &bar_tma);
+      tma_load_2d(sK + pp * 8192, &mk, x, ch.x, &bar_tma);
+      tma_load_2d(sV + pp * 8192, &mv, x, ch.x, &bar_tma);
+    }
+  }
+  // Cumulative gate of channel c = tid (rows past the chunk repeat the last value).
+  {
+    const int c = tid;
+    const float* src = p.g + (size_t(ch.x) * H + h) * kD + c;
+    float run = 0.f;
+    for (int t0 = 0; t0 < kC; t0 += 32) {
+      float buf[32];
+#pragma unroll
+      for (int e = 0; e < 32; ++e) buf[e] = (t0 + e < len) ? src[size_t(t0 + e) * H * kD] : 0.f;
+#pragma unroll
+      for (int e = 0; e < 32; ++e) {
+        run += buf[e];
+        sG[(t0 + e) * kGP + c] = run;
+      }
+    }
+  }
+  if (tid < kC) {
+    float b = 0.f;
+    if (tid < len) {
+      b = __bfloat162float(p.beta[size_t(ch.x + tid) * H + h]);
+      if (p.beta_sigmoid) b = 1.f / (1.f + expf(-b));
+    }
+    s_b[tid] = b;
+  }
+  mbar_wait(&bar_tma, 0, &abort_flag, p.status, kDevTimeoutTma);
+  // rows past the chunk belong to the next document (or are zero): clear them
+  if (tid >= len && tid < kC) {
+    for (int c16 = 0; c16 < 16; ++c16) {
+      const uint32_t off = sw128_offset(tid, c16 * 8, kC, 2);
+      *reinterpret_cast<uint4*>(sQ + off) = make_uint4(0, 0, 0, 0);
+      *reinterpret_cast<uint4*>(sK + off) = make_uint4(0, 0, 0, 0);
+      *reinterpret_cast<uint4*>(sV + off) = make_uint4(0, 0, 0, 0);
+    }
+  }
+  __syncthreads();
+  // L2-norm factors: threads 0..63 for q rows, 64..127 for k rows.
+  {
+    const int t = tid & 63;
+    const uint8_t* src = tid < kC ? sQ : sK;
+    float ss = 0.f;
+    for (int d = 0; d < kD; ++d) {
+      const float x = bf16_at(src, t, d);
+      ss = fmaf(x, x, ss);
+    }
+    const float r = p.l2norm ? 1.f / sqrtf(ss + 1e-6f) : 1.f;
+    if (tid < kC) s_rq[t] = r; else s_rk[t] = r;
+  }
+  s_gl[tid] = sG[(len - 1) * kGP + tid];
+  __syncthreads();
+
+  // Stacked operand: rows 0..63 k^_i, rows 64..127 q^_i, each times exp(G_i - G_{r(i)}).
+  uint8_t* sAS = sm + kOffAS;
+  {
+    const int i = tid & 63;
+    const bool isq = tid >= kC;
+    const int rref = i & ~15;
+    const float rs = isq ? s_rq[i] : s_rk[i];
+    const uint8_t* src = isq ? sQ : sK;
+    const bool vi = i < len;
+    for (int c = 0; c < kD; ++c) {
+      const float val = vi ? rs * bf16_at(src, i, c) * expf(sG[i * kGP + c] - sG[rref * kGP + c]) : 0.f;
+      put32(sAS, 128, tid, c, to_tf32(val));
+    }
+  }
+  // B_I = k^_j exp(G_{r_I} - G_j) for j <= 16 I + 15 (zero elsewhere), two blocks at a time.
+  auto build_b = [&](int I0) {
+    const int j = tid & 63, I = I0 + (tid >> 6);
+    const int rref = 16 * I;
+    uint8_t* dst = sm + kOffB + (tid >> 6) * 32768;
+    const bool vj = j < len && j <= 16 * I + 15;
+    const float rs = s_rk[j];
+    for (int c = 0; c < kD; ++c) {
+      const float val = vj ? rs * bf16_at(sK, j, c) * expf(sG[rref * kGP + c] - sG[j * kGP + c]) : 0.f;
+      put32(dst, kC, j, c, to_tf32(val));
+    }
+  };
+  const uint32_t id_g = idesc_tf32(128, 64);
+  uint32_t mma_phase = 0;
+  bool ok = true;
+  for (int I0 = 0; I0 < 4; I0 += 2) {
+    build_b(I0);
+    fence_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (tid == 0 && ok) {
+      const uint32_t as = smem_u32(sAS);
+      for (int q = 0; q < 2; ++q) {
+        const uint32_t bs = smem_u32(sm + kOffB + q * 32768);
+        for (int s = 0; s < 16; ++s)
+          mma_tf32_ss(tb + (I0 + q) * 64, desc_kmajor(as, 16384, s), desc_kmajor(bs, 8192, s), id_g, s > 0);
+      }
+      mma_commit(&bar_mma);
+    }
+    __syncwarp();
+    ok = ok && mbar_wait(&bar_mma, mma_phase, &abort_flag, p.status, kDevTimeoutMma);
+    mma_phase ^= 1;
+    tc_fence_after();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+
+  // Row blocks of L (lanes 0..63) and Aqk (lanes 64..127) from D_I, I = block of the row.
+  float* sLT = reinterpret_cast<float*>(sm + kOffLT);
+  if (ok) {
+    const int i = tid & 63;
+    const bool isq = tid >= kC;
+    // The lanes of one warp cover two row blocks (I0, I0 + 1); the TMEM load address must be
+    // warp-uniform, so load both and select per lane.
+    const int I0 = 2 * (warp & 1);
+    const bool second = ((i >> 4) & 1) != 0;
+    float r0[64], r1[64];
+    tmem_ld64(tl + I0 * 64, r0);
+    tmem_ld64(tl + (I0 + 1) * 64, r1);
+    tmem_wait_ld_regs(r0);
+    tmem_wait_ld_regs(r1);
+    const bool vi = i < len;
+    if (!isq) {
+#pragma unroll
+      for (int j = 0; j < kC; ++j) sLT[j * kC + i] = (j < i && vi) ? s_b[i] * (second ? r1[j] : r0[j]) : 0.f;
+    } else {
+      float a[kC];
+#pragma unroll
+      for (int j = 0; j < kC; ++j) a[j] = (j <= i && vi) ? to_tf32(p.scale * (second ? r1[j] : r0[j])) : 0.f;
+      float4* dst = reinterpret_cast<float4*>(p.Aqk + tile * kTileAqk + size_t(i) * kC);
+#pragma unroll
+      for (int e = 0; e < kC / 4; ++e) dst[e] = make_float4(a[4 * e], a[4 * e + 1], a[4 * e + 2], a[4 * e + 3]);
+      if (p.AqkT) {
+        float* at = p.AqkT + tile * kTileAqk + i;
+#pragma unroll
+        for (int j = 0; j < kC; ++j) at[size_t(j) * kC] = a[j];
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  float* sX = reinterpret_cast<float*>(sm + kOffX);
+  if (tid < kC) inverse_column(sLT, sX, tid);
+  __syncthreads();
+  // WY operands: A1 = (A - I) diag(beta r_k) (tf32), A2 = (A - I) diag(beta) (bf16), both
+  // K-major [i][j]; K1T = (k (.) exp(G))^T (tf32, K-major [c][j]).
+  {
+    const int j = tid & 63;
+    if (tid < kC) {
+      const float s1 = s_b[j] * s_rk[j], s2 = s_b[j];
+      for (int i = 0; i < kC; ++i) {
+        const float x = i == j ? 0.f : sX[i * kC + j];
+        put32(sm + kOffA1, kC, i, j, to_tf32(x * s1));
+        *reinterpret_cast<__nv_bfloat16*>(sm + kOffA2 + sw128_offset(i, j, kC, 2)) = __float2bfloat16_rn(x * s2);
+      }
+      if (p.A) {
+        float* a = p.A + tile * kTileAqk + j;
+        for (int i = 0; i < kC; ++i) a[size_t(i) * kC] = sX[i * kC + j];
+      }
+    }
+    const int c = tid;
+    for (int jj = 0; jj < kC; ++jj) {
+      const float val = jj < len ? bf16_at(sK, jj, c) * expf(sG[jj * kGP + c]) : 0.f;
+      put32(sm + kOffK1T, kD, c, jj, to_tf32(val));
+    }
+  }
+  fence_async_smem();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (tid == 0 && ok) {
+    const uint32_t a1 = smem_u32(sm + kOffA1), a2 = smem_u32(sm + kOffA2), k1t = smem_u32(sm + kOffK1T);
+    const uint32_t v0 = smem_u32(sV);
+    const uint32_t idw = idesc_tf32(64, 128), idu = idesc_bf16(64, 128, false, true);
+    for (int s = 0; s < 8; ++s) mma_tf32_ss(tb, desc_kmajor(a1, 8192, s), desc_kmajor(k1t, 16384, s), idw, s > 0);
+    for (int s = 0; s < 4; ++s) mma_bf16_ss(tb + 128, desc_kmajor(a2, 8192, s), desc_mnmajor_bf16(v0, 8192, s), idu, s > 0);
+    mma_commit(&bar_mma);
+  }
+  __syncwarp();
+  ok = ok && mbar_wait(&bar_mma, mma_phase, &abort_flag, p.status, kDevTimeoutMma);
+  tc_fence_after();
+  // W and U rows (64-row MMA results: lane 32*(r/16) + r%16 holds row r).
+  if (ok) {
+    const bool owner = lane < 16;
+    const int r = 16 * warp + (lane & 15);
+    const bool vr = owner && r < len;
+    const float dw = s_b[r] * s_rk[r], du = s_b[r];
+    for (int which = 0; which < 2; ++which) {
+      for (int half = 0; half < 2; ++half) {
+        float x[64];
+        tmem_ld64(tl + which * 128 + half * 64, x);
+        tmem_wait_ld_regs(x);
+        if (vr) {
+          float* dst = (which == 0 ? p.W : p.U) + tile * kTileW + size_t(r) * kD + half * 64;
+#pragma unroll
+          for (int e = 0; e < 64; ++e) {
+            const int c = half * 64 + e;
+            float val;
+            if (which == 0) {
+              val = to_tf32(fmaf(dw * expf(sG[r * kGP + c]), bf16_at(sK, r, c), x[e]));
+              if (p.WT) p.WT[tile * kTileKtT + size_t(c) * kC + r] = val;
+            } else {
+              val = fmaf(du, bf16_at(sV, r, c), x[e]);
+            }
+            dst[e] = val;
+          }
+        }
+      }
+    }
+  }
+  // Per-element outputs: thread c writes channel c of every row.
+  {
+    const int c = tid;
+    const float glc = s_gl[c];
+    p.gam[tile * kD + c] = expf(glc);
+    for (int t = 0; t < kC; ++t) {
+      const bool vt = t < len;
+      const float G = sG[t * kGP + c];
+      const float qt = vt ? to_tf32(p.scale * s_rq[t] * expf(G) * bf16_at(sQ, t, c)) : 0.f;
+      const float kt = vt ? to_tf32(s_rk[t] * expf(glc - G) * bf16_at(sK, t, c)) : 0.f;
+      p.Qt[tile * kTileW + size_t(t) * kD + c] = qt;
+      p.KtT[tile * kTileKtT + size_t(c) * kC + t] = kt;
+      if (p.Kt) p.Kt[tile * kTileW + size_t(t) * kD + c] = kt;
+      if (p.QtT) p.QtT[tile * kTileKtT + size_t(c) * kC + t] = qt;
+      if (p.Gc) p.Gc[(tile * kC + t) * kD + c] = G;
+    }
+    if (tid < kC) {
+      if (p.rq) p.rq[tile * kC + tid] = s_rq[tid];
+      if (p.rk) p.rk[tile * kC + tid] = s_rk[tid];
+      if (p.beff) p.beff[tile * kC + tid] = s_b[tid];
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) tmem_dealloc(tb, 256);
+}
+
+cudaError_t launch_prep_kda(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
+                            const PrepParams& p, cudaStream_t s) {
+  static bool attr = false;
+  if (!attr) {
+    cudaError_t e = cudaFuncSetAttribute(k_prep_kda, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    if (e != cudaSuccess) return e;
+    attr = true;
+  }
+  dim3 grid(p.NC, p.H);
+  k_prep_kda<<<grid, kThreads, kSmemBytes, s>>>(mq, mk, mv, p);
+  return cudaGetLastError();
+}
+
+}  // namespace gdn
