@@ -349,11 +349,10 @@ int run_bwd(const gdn_desc_t* d, const gdn_bwd_args_t* a, void* stream, bool kda
   for (const void* o : outs)
     for (const void* i : ins)
       if (overlaps(o, nqk, i, nqk)) return fail(GDN_EINVAL, "gradient outputs must not alias the inputs");
-  const Layout L = make_layout(P, true);
+  const Layout L = make_layout(P, true, kda);
   if (!a->workspace || a->workspace_bytes < L.total)
     return fail(GDN_EINVAL, "workspace missing or smaller than the required size");
   if (reinterpret_cast<uintptr_t>(a->workspace) & 255) return fail(GDN_EINVAL, "workspace must be 256-byte aligned");
-  if (kda) return fail(GDN_EUNSUPPORTED, "per-channel gate backward is not built yet");
   rc = device_check();
   if (rc) return rc;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -381,13 +380,15 @@ int run_bwd(const gdn_desc_t* d, const gdn_bwd_args_t* a, void* stream, bool kda
   pp.status = a->status;
   {
     TimedLaunch tl_(kKPrep, s);
-    rc = check_cuda(launch_prep_gdn(M.q, M.k, M.v, pp, s), "prepare kernel");
+    rc = check_cuda(kda ? launch_prep_kda(M.q, M.k, M.v, pp, s) : launch_prep_gdn(M.q, M.k, M.v, pp, s),
+                    "prepare kernel");
   }
   if (rc) return rc;
 
   ChainParams cp{};
   cp.seqs = reinterpret_cast<const SeqEntry*>(ws + L.seqs);
   cp.chunks = chunks;
+  cp.kda = kda ? 1 : 0;
   cp.N = P.N;
   cp.H = P.H;
   cp.gam = F(L.gam);
@@ -407,6 +408,7 @@ int run_bwd(const gdn_desc_t* d, const gdn_bwd_args_t* a, void* stream, bool kda
   rp.N = P.N;
   rp.H = P.H;
   rp.gam = F(L.gam);
+  rp.kda = kda ? 1 : 0;
   rp.dO = static_cast<const __nv_bfloat16*>(a->dO);
   rp.dht = a->dht;
   rp.dh0 = a->dh0;
@@ -423,6 +425,7 @@ int run_bwd(const gdn_desc_t* d, const gdn_bwd_args_t* a, void* stream, bool kda
   fp.chunks = chunks;
   fp.NC = P.NC;
   fp.H = P.H;
+  fp.kda = kda ? 1 : 0;
   fp.h = F(L.hs);
   fp.dh = F(L.dhs);
   fp.dO = rp.dO;
@@ -455,8 +458,11 @@ int run_bwd(const gdn_desc_t* d, const gdn_bwd_args_t* a, void* stream, bool kda
   tp.dbeta = static_cast<__nv_bfloat16*>(a->dbeta);
   tp.dg = a->dg;
   tp.status = a->status;
+  tp.kda = kda ? 1 : 0;
   TimedLaunch tl_(kKBwdTok, s);
-  return check_cuda(launch_bwd_tok(M.q, M.k, M.v, M.VN, M.DW, M.DVN, tp, s), "token-major backward kernel");
+  return check_cuda(kda ? launch_bwd_tok_kda(M.q, M.k, M.v, M.VN, M.DW, M.DVN, tp, s)
+                        : launch_bwd_tok(M.q, M.k, M.v, M.VN, M.DW, M.DVN, tp, s),
+                    "token-major backward kernel");
 }
 
 }  // namespace
@@ -505,7 +511,11 @@ size_t gdn_bwd_workspace_size(const gdn_desc_t* desc) {
   return make_layout(P, true).total;
 }
 
-size_t kda_bwd_workspace_size(const gdn_desc_t* desc) { return gdn_bwd_workspace_size(desc); }
+size_t kda_bwd_workspace_size(const gdn_desc_t* desc) {
+  Problem P;
+  if (validate_desc(desc, &P)) return 0;
+  return make_layout(P, true, true).total;
+}
 
 int gdn_timing_enable(int enable) {
   g_tim.on = enable != 0;

@@ -129,6 +129,9 @@ cudaError_t launch_chain_bwd(const CUtensorMap& mKt, const CUtensorMap& mAqkT, c
 cudaError_t launch_bwd_feat(const CUtensorMap& mVN, const CUtensorMap& mDVN, const BwdFeatParams& p, cudaStream_t s);
 cudaError_t launch_bwd_tok(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, const CUtensorMap& mVN,
                            const CUtensorMap& mDW, const CUtensorMap& mDVN, const BwdTokParams& p, cudaStream_t s);
+cudaError_t launch_bwd_tok_kda(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
+                               const CUtensorMap& mVN, const CUtensorMap& mDW, const CUtensorMap& mDVN,
+                               const BwdTokParams& p, cudaStream_t s);
 cudaError_t launch_chain_fwd(const CUtensorMap& mW, const CUtensorMap& mQt, const CUtensorMap& mKtT,
                              const CUtensorMap& mAqk, const CUtensorMap& mU, const ChainParams& p,
                              cudaStream_t s);

@@ -1,0 +1,373 @@
+// Backward, token-major part for the per-channel gate (Kimi Delta Attention), one CTA per
+// chunk and head.
+//
+// Same chunk quantities as the scalar-gate kernel, with every decay per key channel c:
+//   L_ij   = beta_i sum_c k^_ic k^_jc Gam_ijc,  Aqk_ij = scale sum_c q^_ic k^_jc Gam_ijc,
+//   Gam_ijc = exp(G_ic - G_jc);  K1_jc = beta_j exp(G_jc) k^_jc;  Qt_ic = scale exp(G_ic) q^_ic;
+//   Kt_ic = exp(G_last,c - G_ic) k^_ic;  gam_c = exp(G_last,c).
+// With D = dL (strictly lower) and N = dAqk (lower), the decayed pair sums
+//   X1_ic = sum_{j<i} D_ij k^_jc Gam_ijc          Y1_ic = scale sum_{j<=i} N_ij k^_jc Gam_ijc
+//   Z_jc  = sum_{i>j} beta_i D_ij k^_ic Gam_ijc + scale sum_{i>=j} N_ij q^_ic Gam_ijc
+// give
+//   dk^ = beta X1 + Z + diag(beta) exp(G) (.) dK1 + exp(G_last - G) (.) dKt
+//   dq^ = Y1 + scale exp(G) (.) dQt
+//   dG  = beta k^ (.) X1 + q^ (.) Y1 - k^ (.) Z + beta exp(G) (.) dK1 (.) k^
+//         + scale exp(G) (.) dQt (.) q^ - exp(G_last - G) (.) dKt (.) k^       (per channel)
+//   dG_last,c += sum_i exp(G_last,c - G_ic) dKt_ic k^_ic + gam_c dgam_c
+//   dbeta_i = sum_c k^_ic X1_ic + sum_c exp(G_ic) dK1_ic k^_ic + sum_c dV1_ic v_ic
+//   dg = reverse cumulative sum of dG over the chunk's tokens, per channel.
+// GB300 mapping: dAqk, dA = [dW | dU][K1 | V1]^T, A^T dA and (A^T dA) A^T are 64-row
+// tcgen05 MMAs (kind::tf32) as in the scalar-gate kernel. The decayed pair sums need one
+// exp(G_ic - G_jc) per (pair, channel); they run on the CUDA cores with one thread per channel
+// (two per channel, interleaving rows), each exponent evaluated once and shared by the four
+// sums, which keeps every decay exact (no factorisation, no range limit on the gates).
+#include "common.cuh"
+#include "umma.cuh"
+
+namespace gdn {
+
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kP = kD + 1;                                   // padded row stride (floats)
+constexpr uint32_t kOffQ = 0, kOffK = 16384, kOffV = 32768;  // bf16 [64][128]
+constexpr uint32_t kOffG = 49152;                            // G * log2(e), fp32 [64][129]
+constexpr uint32_t kR1 = 83968, kR2 = 116736, kR3 = 149504, kR4 = 182272;  // 32 KB each
+constexpr uint32_t kSmemBytes = kR4 + 32768 + 1024;
+constexpr uint32_t kTAqk = 0, kTdA = 64, kTX = 128;
+constexpr float kLog2e = 1.4426950408889634f;
+
+__device__ __forceinline__ uint8_t* align1k(uint8_t* p) {
+  return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
+}
+__device__ __forceinline__ float bf16_at(const uint8_t* tile, int row, int col) {
+  return __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(tile + sw128_offset(row, col, kC, 2)));
+}
+__device__ __forceinline__ void put32(uint8_t* tile, int rows, int row, int col, float x) {
+  *reinterpret_cast<float*>(tile + sw128_offset(row, col, rows, 4)) = x;
+}
+
+}  // namespace
+
+__global__ void __launch_bounds__(kThreads, 1)
+    k_bwd_tok_kda(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
+                  const __grid_constant__ CUtensorMap mv, const __grid_constant__ CUtensorMap mVN,
+                  const __grid_constant__ CUtensorMap mDW, const __grid_constant__ CUtensorMap mDVN,
+                  const BwdTokParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = align1k(smem_raw);
+  uint8_t* sQ = sm + kOffQ;
+  uint8_t* sK = sm + kOffK;
+  uint8_t* sV = sm + kOffV;
+  float* sG2 = reinterpret_cast<float*>(sm + kOffG);
+  __shared__ uint64_t bar_tma, bar_mma;
+  __shared__ uint32_t tslot;
+  __shared__ int abort_flag;
+  __shared__ float s_rq[kC], s_rk[kC], s_b[kC], s_db[kC], s_dotq[kC], s_dotk[kC], s_glast[2][kD];
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int wq = warp & 3, half = warp >> 2;
+  const int c_idx = blockIdx.x, h = blockIdx.y, H = p.H;
+  const size_t tile = size_t(c_idx) * H + h;
+  const ChunkEntry ch = p.chunks[c_idx];
+  const int len = ch.y;
+  const bool owner = lane < 16;
+  const int rr = 16 * wq + (lane & 15);
+  const float scale = p.scale;
+  const int cc = tid & 127;   // channel handled in the CUDA-core phases
+
+  if (warp == 0) tmem_alloc(&tslot, 256);
+  if (tid == 0) {
+    abort_flag = 0;
+    mbar_init(&bar_tma, 1);
+    mbar_init(&bar_mma, 1);
+    fence_mbar_init();
+  }
+  if (tid < kC) {
+    const bool ok = tid < len;
+    s_rq[tid] = ok ? p.rq[tile * kC + tid] : 0.f;
+    s_rk[tid] = ok ? p.rk[tile * kC + tid] : 0.f;
+    s_b[tid] = ok ? p.beff[tile * kC + tid] : 0.f;
+    s_db[tid] = 0.f;
+    s_dotq[tid] = 0.f;
+    s_dotk[tid] = 0.f;
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tb = tslot;
+  const uint32_t tl = tb + tmem_lane_base(warp);
+  if (tid == 0) {
+    mbar_expect_tx(&bar_tma, 3u * 16384u + 3u * 32768u);
+    for (int pp = 0; pp < 2; ++pp) {
+      const int x = h * kD + 64 * pp;
+      tma_load_2d(sQ + pp * 8192, &mq, x, ch.x, &bar_tma);
+      tma_load_2d(sK + pp * 8192, &mk, x, ch.x, &bar_tma);
+      tma_load_2d(sV + pp * 8192, &mv, x, ch.x, &bar_tma);
+    }
+    for (int pp = 0; pp < 4; ++pp) {
+      tma_load_2d(sm + kR2 + pp * 8192, &mVN, pp * 32, int(tile) * kC, &bar_tma);
+      tma_load_2d(sm + kR3 + pp * 8192, &mDW, pp * 32, int(tile) * kC, &bar_tma);
+      tma_load_2d(sm + kR4 + pp * 8192, &mDVN, pp * 32, int(tile) * kC, &bar_tma);
+    }
+  }
+  // G (scaled to log2 units) and dO as a 64-row tf32 operand; rows past the chunk are zero.
+  {
+    const int t0 = 32 * half;
+    const float* gsrc = p.Gc + (tile * kC + t0) * kD + cc;
+    const __nv_bfloat16* src = p.dO + (size_t(ch.x) * H + h) * kD + cc;
+    float bg[32], bo[32];
+#pragma unroll
+    for (int e = 0; e < 32; ++e) {
+      bg[e] = gsrc[size_t(e) * kD];
+      bo[e] = (t0 + e < len) ? __bfloat162float(src[size_t(t0 + e) * H * kD]) : 0.f;
+    }
+#pragma unroll
+    for (int e = 0; e < 32; ++e) {
+      sG2[(t0 + e) * kP + cc] = bg[e] * kLog2e;
+      put32(sm + kR1, kC, t0 + e, cc, bo[e]);
+    }
+  }
+  fence_async_smem();
+  __syncthreads();
+  const bool tma_ok = mbar_wait(&bar_tma, 0, &abort_flag, p.status, kDevTimeoutTma);
+  if (tid >= len && tid < kC) {
+    for (int c16 = 0; c16 < 16; ++c16) {
+      const uint32_t off = sw128_offset(tid, c16 * 8, kC, 2);
+      *reinterpret_cast<uint4*>(sQ + off) = make_uint4(0, 0, 0, 0);
+      *reinterpret_cast<uint4*>(sK + off) = make_uint4(0, 0, 0, 0);
+      *reinterpret_cast<uint4*>(sV + off) = make_uint4(0, 0, 0, 0);
+    }
+  }
+  fence_async_smem();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  // ---- dAqk = dO v_new^T
+  if (tid == 0 && tma_ok) {
+    const uint32_t id = idesc_tf32(64, 64);
+    const uint32_t r1 = smem_u32(sm + kR1), r2 = smem_u32(sm + kR2);
+    for (int s = 0; s < 16; ++s) mma_tf32_ss(tb + kTAqk, desc_kmajor(r1, 8192, s), desc_kmajor(r2, 8192, s), id, s > 0);
+    mma_commit(&bar_mma);
+  }
+  __syncwarp();
+  bool ok = tma_ok && mbar_wait(&bar_mma, 0, &abort_flag, p.status, kDevTimeoutMma);
+  tc_fence_after();
+  // ---- K1 = beta r_k exp(G) (.) k and V1 = beta v as 64-row operands [j][c]
+  for (int j = 32 * half; j < 32 * half + 32; ++j) {
+    const float s1 = s_b[j] * s_rk[j];
+    put32(sm + kR1, kC, j, cc, to_tf32(s1 * exp2f(sG2[j * kP + cc]) * bf16_at(sK, j, cc)));
+    put32(sm + kR2, kC, j, cc, to_tf32(s_b[j] * bf16_at(sV, j, cc)));
+  }
+  fence_async_smem();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  // ---- dA = [dW | dU] [K1 | V1]^T
+  if (tid == 0 && ok) {
+    const uint32_t id = idesc_tf32(64, 64);
+    const uint32_t r1 = smem_u32(sm + kR1), r2 = smem_u32(sm + kR2), r3 = smem_u32(sm + kR3), r4 = smem_u32(sm + kR4);
+    for (int s = 0; s < 16; ++s) mma_tf32_ss(tb + kTdA, desc_kmajor(r3, 8192, s), desc_kmajor(r1, 8192, s), id, s > 0);
+    for (int s = 0; s < 16; ++s) mma_tf32_ss(tb + kTdA, desc_kmajor(r4, 8192, s), desc_kmajor(r2, 8192, s), id, true);
+    mma_commit(&bar_mma);
+  }
+  __syncwarp();
+  ok = ok && mbar_wait(&bar_mma, 1, &abort_flag, p.status, kDevTimeoutMma);
+  tc_fence_after();
+  // ---- dL = -A^T dA A^T
+  uint8_t* sAT = sm + kR3;
+  uint8_t* sdAT = sm + kR3 + 16384;
+  uint8_t* sA = sm + kR4;
+  uint8_t* sX = sm + kR4 + 16384;
+  {
+    float r[32];
+    tmem_ld32(tl + kTdA + 32 * half, r);
+    tmem_wait_ld_regs(r);
+    if (owner) {
+#pragma unroll
+      for (int m = 0; m < 32; ++m) put32(sdAT, kC, 32 * half + m, rr, to_tf32(r[m]));
+    }
+    const float* a = p.A + tile * kTileAqk;
+    const int j = tid & 63, grp = tid >> 6;
+    const int i0 = 32 * (grp & 1);
+    float buf[32];
+    if (grp < 2) {
+#pragma unroll
+      for (int e = 0; e < 32; ++e) buf[e] = a[size_t(i0 + e) * kC + j];
+#pragma unroll
+      for (int e = 0; e < 32; ++e) put32(sAT, kC, j, i0 + e, to_tf32(buf[e]));
+    } else {
+#pragma unroll
+      for (int e = 0; e < 32; ++e) buf[e] = a[size_t(j) * kC + i0 + e];
+#pragma unroll
+      for (int e = 0; e < 32; ++e) put32(sA, kC, j, i0 + e, to_tf32(buf[e]));
+    }
+  }
+  fence_async_smem();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (tid == 0 && ok) {
+    const uint32_t id = idesc_tf32(64, 64);
+    for (int s = 0; s < 8; ++s)
+      mma_tf32_ss(tb + kTX, desc_kmajor(smem_u32(sAT), 8192, s), desc_kmajor(smem_u32(sdAT), 8192, s), id, s > 0);
+    mma_commit(&bar_mma);
+  }
+  __syncwarp();
+  ok = ok && mbar_wait(&bar_mma, 0, &abort_flag, p.status, kDevTimeoutMma);
+  tc_fence_after();
+  {
+    float r[32];
+    tmem_ld32(tl + kTX + 32 * half, r);
+    tmem_wait_ld_regs(r);
+    if (owner) {
+#pragma unroll
+      for (int m = 0; m < 32; ++m) put32(sX, kC, rr, 32 * half + m, to_tf32(r[m]));
+    }
+  }
+  fence_async_smem();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (tid == 0 && ok) {
+    const uint32_t id = idesc_tf32(64, 64);
+    for (int s = 0; s < 8; ++s)
+      mma_tf32_ss(tb + kTX, desc_kmajor(smem_u32(sX), 8192, s), desc_kmajor(smem_u32(sA), 8192, s), id, s > 0);
+    mma_commit(&bar_mma);
+  }
+  __syncwarp();
+  ok = ok && mbar_wait(&bar_mma, 1, &abort_flag, p.status, kDevTimeoutMma);
+  tc_fence_after();
+  // ---- stage D = dL (strictly lower) and N = scale dAqk (lower), fp32 [64][64] (every thread
+  // reads the same element at a time, so no padding is needed)
+  float* sD = reinterpret_cast<float*>(sm + kR1);
+  float* sN = sD + kC * kC;
+  {
+    float dl[32], nn[32];
+    tmem_ld32(tl + kTX + 32 * half, dl);
+    tmem_ld32(tl + kTAqk + 32 * half, nn);
+    tmem_wait_ld_regs(dl);
+    tmem_wait_ld_regs(nn);
+    if (owner) {
+      const int i = rr;
+      const bool vi = i < len;
+#pragma unroll
+      for (int jj = 0; jj < 32; ++jj) {
+        const int j = 32 * half + jj;
+        const float D = (j < i && vi) ? -dl[jj] : 0.f;
+        sD[i * kC + j] = D;
+        sN[i * kC + j] = (j <= i && vi) ? scale * nn[jj] : 0.f;
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  // ---- decayed pair sums on CUDA cores: thread (channel cc, rows of parity `half`).
+  float* sKacc = reinterpret_cast<float*>(sm + kR2);           // dk^ accumulator [64][128]
+  float* sQacc = reinterpret_cast<float*>(sm + kR3);           // dq^ accumulator [64][128]
+  float* sGacc = reinterpret_cast<float*>(sm + kR4);           // dG accumulator [64][128]
+  for (int i = half; i < len; i += 2) {
+    const float Gi = sG2[i * kP + cc];
+    float x1 = 0.f, y1 = 0.f;
+    for (int j = 0; j <= i; ++j) {
+      const float gam = exp2f(Gi - sG2[j * kP + cc]);
+      const float kj = s_rk[j] * bf16_at(sK, j, cc) * gam;
+      x1 = fmaf(sD[i * kC + j], kj, x1);
+      y1 = fmaf(sN[i * kC + j], kj, y1);
+    }
+    const float khi = s_rk[i] * bf16_at(sK, i, cc);
+    const float qhi = s_rq[i] * bf16_at(sQ, i, cc);
+    float z = 0.f;
+    for (int r = i; r < len; ++r) {   // Z_ic: rows r >= i act on column i
+      const float gam = exp2f(sG2[r * kP + cc] - Gi);
+      const float kr = s_rk[r] * bf16_at(sK, r, cc);
+      const float qr = s_rq[r] * bf16_at(sQ, r, cc);
+      z = fmaf(s_b[r] * sD[r * kC + i] * kr + sN[r * kC + i] * qr, gam, z);
+    }
+    sKacc[i * kD + cc] = s_b[i] * x1 + z;
+    sQacc[i * kD + cc] = y1;
+    sGacc[i * kD + cc] = s_b[i] * khi * x1 + qhi * y1 - khi * z;
+    // dbeta_i gets sum over channels of k^_ic X1_ic: warp-reduce, one atomic per warp
+    float part = khi * x1;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) part += __shfl_xor_sync(0xffffffffu, part, off);
+    if (lane == 0) atomicAdd(&s_db[i], part);
+  }
+  __syncthreads();
+  // ---- per-token assembly (thread: channel cc, rows of parity `half`)
+  float glast_part = 0.f;
+  const float glc = sG2[(len - 1) * kP + cc];
+  const size_t rowbase = tile * kTileW;
+  for (int t = half; t < len; t += 2) {
+    const float G = sG2[t * kP + cc];
+    const float eG = exp2f(G), eL = exp2f(glc - G);
+    const float qh = s_rq[t] * bf16_at(sQ, t, cc), kh = s_rk[t] * bf16_at(sK, t, cc);
+    const float dqt = p.dQt[rowbase + size_t(t) * kD + cc];
+    const float dk1 = p.dK1[rowbase + size_t(t) * kD + cc];
+    const float dkt = p.dKt[rowbase + size_t(t) * kD + cc];
+    const float dv1 = p.dV1[rowbase + size_t(t) * kD + cc];
+    const float dqh = sQacc[t * kD + cc] + scale * eG * dqt;
+    const float dkh = sKacc[t * kD + cc] + s_b[t] * eG * dk1 + eL * dkt;
+    sQacc[t * kD + cc] = dqh;
+    sKacc[t * kD + cc] = dkh;
+    sGacc[t * kD + cc] += s_b[t] * eG * dk1 * kh + scale * eG * dqt * qh - eL * dkt * kh;
+    glast_part = fmaf(eL * dkt, kh, glast_part);
+    p.dv[(size_t(ch.x + t) * H + h) * kD + cc] = __float2bfloat16_rn(s_b[t] * dv1);
+    float pb = eG * dk1 * kh + dv1 * bf16_at(sV, t, cc);
+    float pq = dqh * qh, pk = dkh * kh;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+      pb += __shfl_xor_sync(0xffffffffu, pb, off);
+      pq += __shfl_xor_sync(0xffffffffu, pq, off);
+      pk += __shfl_xor_sync(0xffffffffu, pk, off);
+    }
+    if (lane == 0) {
+      atomicAdd(&s_db[t], pb);
+      atomicAdd(&s_dotq[t], pq);
+      atomicAdd(&s_dotk[t], pk);
+    }
+  }
+  s_glast[half][cc] = glast_part;
+  __syncthreads();
+  // ---- L2-norm backward and writes; dg by reverse cumulative sum per channel
+  for (int t = half; t < len; t += 2) {
+    const float rq = s_rq[t], rk = s_rk[t];
+    const float qh = rq * bf16_at(sQ, t, cc), kh = rk * bf16_at(sK, t, cc);
+    const float dq = p.l2norm ? rq * (sQacc[t * kD + cc] - qh * s_dotq[t]) : sQacc[t * kD + cc];
+    const float dk = p.l2norm ? rk * (sKacc[t * kD + cc] - kh * s_dotk[t]) : sKacc[t * kD + cc];
+    const size_t o = (size_t(ch.x + t) * H + h) * kD + cc;
+    p.dq[o] = __float2bfloat16_rn(dq);
+    p.dk[o] = __float2bfloat16_rn(dk);
+  }
+  if (half == 0) {
+    float acc = s_glast[0][cc] + s_glast[1][cc] + exp2f(glc) * p.dgam[tile * kD + cc];
+    for (int t = len - 1; t >= 0; --t) {
+      acc += sGacc[t * kD + cc];
+      p.dg[(size_t(ch.x + t) * H + h) * kD + cc] = acc;
+    }
+  }
+  if (tid < len) {
+    float db = s_db[tid];
+    if (p.beta_sigmoid) db *= s_b[tid] * (1.f - s_b[tid]);
+    p.dbeta[size_t(ch.x + tid) * H + h] = __float2bfloat16_rn(db);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) tmem_dealloc(tb, 256);
+}
+
+cudaError_t launch_bwd_tok_kda(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
+                               const CUtensorMap& mVN, const CUtensorMap& mDW, const CUtensorMap& mDVN,
+                               const BwdTokParams& p, cudaStream_t s) {
+  static bool attr = false;
+  if (!attr) {
+    cudaError_t e = cudaFuncSetAttribute(k_bwd_tok_kda, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    if (e != cudaSuccess) return e;
+    attr = true;
+  }
+  dim3 grid(p.NC, p.H);
+  k_bwd_tok_kda<<<grid, kThreads, kSmemBytes, s>>>(mq, mk, mv, mVN, mDW, mDVN, p);
+  return cudaGetLastError();
+}
+
+}  // namespace gdn

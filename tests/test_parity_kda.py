@@ -42,3 +42,34 @@ def test_kda_fwd_batch_and_packed():
 
 def test_kda_fwd_strong_gates():
     check_fwd(synth.custom(1, 192, 2, per_channel=True, beta_logits=True, seed=43, g_scale=2.0))
+
+
+def check_bwd(d, **kw):
+    from chunked_gated_delta_05_gb300 import kda_bwd
+    from tests._util import oracle_bwd
+    dc = to_cuda(d)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out = kda_bwd(dc["q"], dc["k"], dc["v"], dc["g"], dc["beta"], dc["dO"], dht=dc["dht"],
+                  initial_state=dc["h0"], cu_seqlens=d["cu_seqlens"], status=status, **kw)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    dq, dk, dv, db, dg, dh0 = [None if x is None else x.float().cpu().numpy() for x in out]
+    ref = oracle_bwd(d, use_beta_sigmoid=kw.get("use_beta_sigmoid", True), use_qk_l2norm=kw.get("use_qk_l2norm", True))
+    msgs = []
+    for name, x in (("dq", dq), ("dk", dk), ("dv", dv), ("dbeta", db), ("dg", dg)):
+        r = assert_output(name, x, ref[name])
+        msgs.append(f"{name} {r[0]:.1e}")
+    if d["h0"] is not None:
+        msgs.append(f"dh0 {assert_state('dh0', dh0, ref['dh0']):.1e}")
+    print("parity kda bwd rel-L2: " + ", ".join(msgs))
+
+
+@pytest.mark.parametrize("T", [64, 100, 200])
+def test_kda_bwd_dense(T):
+    check_bwd(synth.custom(1, T, 2, per_channel=True, beta_logits=True, h0_std=0.02, dht_std=0.01, seed=50 + T))
+
+
+def test_kda_bwd_packed():
+    lens = [1, 63, 64, 65, 130, 7]
+    check_bwd(synth.custom(1, sum(lens), 2, per_channel=True, beta_logits=True, h0_std=0.02, dht_std=0.01,
+                           lengths=lens, seed=51))
