@@ -1,6 +1,6 @@
 """Benchmark of the chunked gated delta rule on GB300: one step = forward + backward of the
-whole path (gdn_fwd then gdn_bwd, which recomputes the forward internally) over one batch of
-synthetic inputs. Prints one JSON line.
+whole path (gdn_fwd in save mode, then gdn_bwd on the saved chunk intermediates) over one
+batch of synthetic inputs. Prints one JSON line.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--workload NAME]
 
@@ -213,10 +213,11 @@ def main():
     status = torch.zeros(1, dtype=torch.int32, device=dev)
 
     def step(inp):
-        o, hT = fwd_fn(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"], initial_state=inp["h0"],
-                       output_final_state=True, status=status, **kw)
+        # training step: the forward saves its chunk intermediates, the backward consumes them
+        o, hT, saved = fwd_fn(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"], initial_state=inp["h0"],
+                              output_final_state=True, status=status, save=True, **kw)
         grads = bwd_fn(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"], inp["dO"], dht=inp["dht"],
-                       initial_state=inp["h0"], status=status, **kw)
+                       initial_state=inp["h0"], status=status, saved=saved, **kw)
         return (o, hT) + tuple(grads)
 
     for _ in range(args.warmup):

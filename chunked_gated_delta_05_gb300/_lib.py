@@ -23,7 +23,7 @@ class FwdArgs(ctypes.Structure):
     _fields_ = [("q", c_void_p), ("k", c_void_p), ("v", c_void_p), ("g", c_void_p),
                 ("beta", c_void_p), ("initial_state", c_void_p), ("o", c_void_p),
                 ("final_state", c_void_p), ("workspace", c_void_p), ("workspace_bytes", c_size_t),
-                ("status", c_void_p)]
+                ("status", c_void_p), ("saved", c_void_p), ("saved_bytes", c_size_t)]
 
 
 class BwdArgs(ctypes.Structure):
@@ -31,7 +31,8 @@ class BwdArgs(ctypes.Structure):
                 ("beta", c_void_p), ("initial_state", c_void_p), ("dO", c_void_p),
                 ("dht", c_void_p), ("dq", c_void_p), ("dk", c_void_p), ("dv", c_void_p),
                 ("dbeta", c_void_p), ("dg", c_void_p), ("dh0", c_void_p),
-                ("workspace", c_void_p), ("workspace_bytes", c_size_t), ("status", c_void_p)]
+                ("workspace", c_void_p), ("workspace_bytes", c_size_t), ("status", c_void_p),
+                ("saved", c_void_p), ("saved_bytes", c_size_t)]
 
 
 # Every symbol include/gdn.h declares, with its ctypes signature.
@@ -43,6 +44,8 @@ SIGNATURES = {
     "gdn_bwd_workspace_size": ([ctypes.POINTER(Desc)], c_size_t),
     "kda_fwd_workspace_size": ([ctypes.POINTER(Desc)], c_size_t),
     "kda_bwd_workspace_size": ([ctypes.POINTER(Desc)], c_size_t),
+    "gdn_saved_size": ([ctypes.POINTER(Desc)], c_size_t),
+    "kda_saved_size": ([ctypes.POINTER(Desc)], c_size_t),
     "gdn_fwd": ([ctypes.POINTER(Desc), ctypes.POINTER(FwdArgs), c_void_p], c_int),
     "gdn_bwd": ([ctypes.POINTER(Desc), ctypes.POINTER(BwdArgs), c_void_p], c_int),
     "kda_fwd": ([ctypes.POINTER(Desc), ctypes.POINTER(FwdArgs), c_void_p], c_int),

@@ -100,15 +100,17 @@ int validate_desc(const gdn_desc_t* d, Problem* P) {
   return GDN_OK;
 }
 
-// Workspace carve-up. Forward: tables + the prepare tiles the chain reads. Backward adds
-// the transposed tiles of the reverse chain, the per-chunk saves of both chains and the
-// outputs of the feature-major backward kernel. Every region is 256-byte aligned.
+// Buffer carve-up. The "saved" part holds the chunk tables, the prepare tiles and (for a
+// training forward / backward) the chain saves; the "rest" part holds what only the backward
+// uses. Inference forward: saved part only (forward subset). Backward without a saved buffer:
+// both parts in the workspace. With a saved buffer: saved part there, rest part in the
+// workspace. Every region is 256-byte aligned; rest offsets are relative to the rest base.
 struct Layout {
   size_t cu, seqs, chunks, W, U, Qt, KtT, Aqk, gam;               // forward
   size_t Kt, QtT, AqkT, WT, A, Gc, rq, rk, beff;                  // prepare, backward mode
-  size_t hs, vns, dhs, dvns;                                       // chain saves
-  size_t dQt, dKt, dW, dK1, dV1, dgam;                             // feature-major backward
-  size_t total;
+  size_t hs, vns;                                                  // forward chain saves
+  size_t dhs, dvns, dQt, dKt, dW, dK1, dV1, dgam;                  // rest part (relative)
+  size_t saved_total, rest_total, total;
 };
 
 Layout make_layout(const Problem& P, bool backward, bool kda = false) {
@@ -141,6 +143,10 @@ Layout make_layout(const Problem& P, bool backward, bool kda = false) {
     L.beff = take(4 * tiles * kC);
     L.hs = take(4 * tiles * kD * kD);
     L.vns = take(4 * tiles * kTileW);
+  }
+  L.saved_total = off;
+  off = 0;
+  if (backward) {
     L.dhs = take(4 * tiles * kD * kD);
     L.dvns = take(4 * tiles * kTileW);
     L.dQt = take(4 * tiles * kTileW);
@@ -150,7 +156,8 @@ Layout make_layout(const Problem& P, bool backward, bool kda = false) {
     L.dV1 = take(4 * tiles * kTileW);
     L.dgam = take(4 * tiles * kD);
   }
-  L.total = off;
+  L.rest_total = off;
+  L.total = L.saved_total + L.rest_total;
   return L;
 }
 
@@ -232,12 +239,35 @@ bool fwd_maps(const Problem& P, const void* q, const void* k, const void* v, con
          tile_map(&M->Aqk, ws + L.Aqk, kC, r64, 64, true);
 }
 
-bool bwd_maps(const Problem& P, const char* ws, const Layout& L, Maps* M) {
+bool bwd_maps(const Problem& P, const char* sv, const char* rs, const Layout& L, Maps* M) {
   const uint64_t r64 = uint64_t(P.NC) * P.H * kC, r128 = uint64_t(P.NC) * P.H * kD;
-  return tile_map(&M->Kt, ws + L.Kt, kD, r64, 64, true) && tile_map(&M->AqkT, ws + L.AqkT, kC, r64, 64, true) &&
-         tile_map(&M->QtT, ws + L.QtT, kC, r128, 128, true) && tile_map(&M->WT, ws + L.WT, kC, r128, 128, true) &&
-         tile_map(&M->VN, ws + L.vns, kD, r64, 64, true) && tile_map(&M->DVN, ws + L.dvns, kD, r64, 64, true) &&
-         tile_map(&M->DW, ws + L.dW, kD, r64, 64, true);
+  return tile_map(&M->Kt, sv + L.Kt, kD, r64, 64, true) && tile_map(&M->AqkT, sv + L.AqkT, kC, r64, 64, true) &&
+         tile_map(&M->QtT, sv + L.QtT, kC, r128, 128, true) && tile_map(&M->WT, sv + L.WT, kC, r128, 128, true) &&
+         tile_map(&M->VN, sv + L.vns, kD, r64, 64, true) && tile_map(&M->DVN, rs + L.dvns, kD, r64, 64, true) &&
+         tile_map(&M->DW, rs + L.dW, kD, r64, 64, true);
+}
+
+// Prepare-kernel parameters for a buffer carved by make_layout at `sv` (backward-mode outputs
+// only when `backward`).
+PrepParams prep_params(const gdn_desc_t* d, const Problem& P, char* sv, const Layout& L, const float* g,
+                       const void* beta, bool backward, int* status) {
+  auto F = [&](size_t off) { return reinterpret_cast<float*>(sv + off); };
+  PrepParams pp{};
+  pp.chunks = reinterpret_cast<const ChunkEntry*>(sv + L.chunks);
+  pp.NC = P.NC;
+  pp.H = P.H;
+  pp.g = g;
+  pp.beta = static_cast<const __nv_bfloat16*>(beta);
+  pp.scale = P.scale;
+  pp.l2norm = d->use_qk_l2norm;
+  pp.beta_sigmoid = d->use_beta_sigmoid;
+  pp.W = F(L.W); pp.U = F(L.U); pp.Qt = F(L.Qt); pp.KtT = F(L.KtT); pp.Aqk = F(L.Aqk); pp.gam = F(L.gam);
+  if (backward) {
+    pp.Gc = F(L.Gc); pp.rq = F(L.rq); pp.rk = F(L.rk); pp.beff = F(L.beff);
+    pp.Kt = F(L.Kt); pp.QtT = F(L.QtT); pp.AqkT = F(L.AqkT); pp.WT = F(L.WT); pp.A = F(L.A);
+  }
+  pp.status = status;
+  return pp;
 }
 
 // Copy the packed offsets into the workspace through kernel parameters (no host staging
@@ -281,37 +311,28 @@ int run_fwd(const gdn_desc_t* d, const gdn_fwd_args_t* a, void* stream, bool kda
   const size_t nqk = size_t(P.R) * P.H * kD * 2;
   if (overlaps(a->o, nqk, a->q, nqk) || overlaps(a->o, nqk, a->k, nqk) || overlaps(a->o, nqk, a->v, nqk))
     return fail(GDN_EINVAL, "o must not alias q, k or v");
-  const Layout L = make_layout(P, false);
-  if (!a->workspace || a->workspace_bytes < L.total)
-    return fail(GDN_EINVAL, "workspace missing or smaller than the required size");
-  if (reinterpret_cast<uintptr_t>(a->workspace) & 255) return fail(GDN_EINVAL, "workspace must be 256-byte aligned");
+  const bool training = a->saved != nullptr;
+  const Layout L = make_layout(P, training, kda);
+  char* ws = nullptr;
+  if (training) {
+    if (a->saved_bytes < L.saved_total) return fail(GDN_EINVAL, "saved buffer smaller than the required size");
+    if (reinterpret_cast<uintptr_t>(a->saved) & 255) return fail(GDN_EINVAL, "saved buffer must be 256-byte aligned");
+    ws = static_cast<char*>(a->saved);
+  } else {
+    if (!a->workspace || a->workspace_bytes < L.saved_total)
+      return fail(GDN_EINVAL, "workspace missing or smaller than the required size");
+    if (reinterpret_cast<uintptr_t>(a->workspace) & 255) return fail(GDN_EINVAL, "workspace must be 256-byte aligned");
+    ws = static_cast<char*>(a->workspace);
+  }
   rc = device_check();
   if (rc) return rc;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  char* ws = static_cast<char*>(a->workspace);
 
   rc = build_tables(P, ws, L, a->status, s);
   if (rc) return rc;
-
   Maps M;
   if (!fwd_maps(P, a->q, a->k, a->v, ws, L, &M)) return fail(GDN_ECUDA, "cuTensorMapEncodeTiled failed");
-
-  PrepParams pp{};
-  pp.chunks = reinterpret_cast<const ChunkEntry*>(ws + L.chunks);
-  pp.NC = P.NC;
-  pp.H = P.H;
-  pp.g = a->g;
-  pp.beta = static_cast<const __nv_bfloat16*>(a->beta);
-  pp.scale = P.scale;
-  pp.l2norm = d->use_qk_l2norm;
-  pp.beta_sigmoid = d->use_beta_sigmoid;
-  pp.W = reinterpret_cast<float*>(ws + L.W);
-  pp.U = reinterpret_cast<float*>(ws + L.U);
-  pp.Qt = reinterpret_cast<float*>(ws + L.Qt);
-  pp.KtT = reinterpret_cast<float*>(ws + L.KtT);
-  pp.Aqk = reinterpret_cast<float*>(ws + L.Aqk);
-  pp.gam = reinterpret_cast<float*>(ws + L.gam);
-  pp.status = a->status;
+  const PrepParams pp = prep_params(d, P, ws, L, a->g, a->beta, training, a->status);
   {
     TimedLaunch tl_(kKPrep, s);
     rc = check_cuda(kda ? launch_prep_kda(M.q, M.k, M.v, pp, s) : launch_prep_gdn(M.q, M.k, M.v, pp, s),
@@ -329,6 +350,10 @@ int run_fwd(const gdn_desc_t* d, const gdn_fwd_args_t* a, void* stream, bool kda
   cp.h0 = a->initial_state;
   cp.hT = d->output_final_state ? a->final_state : nullptr;
   cp.o = static_cast<__nv_bfloat16*>(a->o);
+  if (training) {
+    cp.h_save = reinterpret_cast<float*>(ws + L.hs);
+    cp.vnew_save = reinterpret_cast<float*>(ws + L.vns);
+  }
   cp.status = a->status;
   TimedLaunch tl_(kKChainFwd, s);
   return check_cuda(launch_chain_fwd(M.W, M.Qt, M.KtT, M.Aqk, M.U, cp, s), "chain kernel");
@@ -350,60 +375,62 @@ int run_bwd(const gdn_desc_t* d, const gdn_bwd_args_t* a, void* stream, bool kda
     for (const void* i : ins)
       if (overlaps(o, nqk, i, nqk)) return fail(GDN_EINVAL, "gradient outputs must not alias the inputs");
   const Layout L = make_layout(P, true, kda);
-  if (!a->workspace || a->workspace_bytes < L.total)
+  const bool have_saved = a->saved != nullptr;
+  if (have_saved) {
+    if (a->saved_bytes < L.saved_total) return fail(GDN_EINVAL, "saved buffer smaller than the required size");
+    if (reinterpret_cast<uintptr_t>(a->saved) & 255) return fail(GDN_EINVAL, "saved buffer must be 256-byte aligned");
+  }
+  const size_t need = have_saved ? L.rest_total : L.total;
+  if (!a->workspace || a->workspace_bytes < need)
     return fail(GDN_EINVAL, "workspace missing or smaller than the required size");
   if (reinterpret_cast<uintptr_t>(a->workspace) & 255) return fail(GDN_EINVAL, "workspace must be 256-byte aligned");
   rc = device_check();
   if (rc) return rc;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  char* ws = static_cast<char*>(a->workspace);
-  rc = build_tables(P, ws, L, a->status, s);
-  if (rc) return rc;
+  char* sv = have_saved ? const_cast<char*>(static_cast<const char*>(a->saved)) : static_cast<char*>(a->workspace);
+  char* rs = have_saved ? static_cast<char*>(a->workspace) : static_cast<char*>(a->workspace) + L.saved_total;
   Maps M;
-  if (!fwd_maps(P, a->q, a->k, a->v, ws, L, &M) || !bwd_maps(P, ws, L, &M))
+  if (!fwd_maps(P, a->q, a->k, a->v, sv, L, &M) || !bwd_maps(P, sv, rs, L, &M))
     return fail(GDN_ECUDA, "cuTensorMapEncodeTiled failed");
-  auto F = [&](size_t off) { return reinterpret_cast<float*>(ws + off); };
-  const ChunkEntry* chunks = reinterpret_cast<const ChunkEntry*>(ws + L.chunks);
-
-  PrepParams pp{};
-  pp.chunks = chunks;
-  pp.NC = P.NC;
-  pp.H = P.H;
-  pp.g = a->g;
-  pp.beta = static_cast<const __nv_bfloat16*>(a->beta);
-  pp.scale = P.scale;
-  pp.l2norm = d->use_qk_l2norm;
-  pp.beta_sigmoid = d->use_beta_sigmoid;
-  pp.W = F(L.W); pp.U = F(L.U); pp.Qt = F(L.Qt); pp.KtT = F(L.KtT); pp.Aqk = F(L.Aqk); pp.gam = F(L.gam);
-  pp.Gc = F(L.Gc); pp.rq = F(L.rq); pp.rk = F(L.rk); pp.beff = F(L.beff);
-  pp.Kt = F(L.Kt); pp.QtT = F(L.QtT); pp.AqkT = F(L.AqkT); pp.WT = F(L.WT); pp.A = F(L.A);
-  pp.status = a->status;
-  {
-    TimedLaunch tl_(kKPrep, s);
-    rc = check_cuda(kda ? launch_prep_kda(M.q, M.k, M.v, pp, s) : launch_prep_gdn(M.q, M.k, M.v, pp, s),
-                    "prepare kernel");
+  auto F = [&](size_t off) { return reinterpret_cast<float*>(sv + off); };
+  auto R = [&](size_t off) { return reinterpret_cast<float*>(rs + off); };
+  const ChunkEntry* chunks = reinterpret_cast<const ChunkEntry*>(sv + L.chunks);
+  if (have_saved) {
+    // the forward already built the tables and saved its intermediates; reset the status word
+    if (a->status) {
+      rc = check_cuda(cudaMemsetAsync(a->status, 0, sizeof(int), s), "status reset");
+      if (rc) return rc;
+    }
+  } else {
+    rc = build_tables(P, sv, L, a->status, s);
+    if (rc) return rc;
+    const PrepParams pp = prep_params(d, P, sv, L, a->g, a->beta, true, a->status);
+    {
+      TimedLaunch tl_(kKPrep, s);
+      rc = check_cuda(kda ? launch_prep_kda(M.q, M.k, M.v, pp, s) : launch_prep_gdn(M.q, M.k, M.v, pp, s),
+                      "prepare kernel");
+    }
+    if (rc) return rc;
+    ChainParams cp{};
+    cp.seqs = reinterpret_cast<const SeqEntry*>(sv + L.seqs);
+    cp.chunks = chunks;
+    cp.kda = kda ? 1 : 0;
+    cp.N = P.N;
+    cp.H = P.H;
+    cp.gam = F(L.gam);
+    cp.h0 = a->initial_state;
+    cp.h_save = F(L.hs);
+    cp.vnew_save = F(L.vns);
+    cp.status = a->status;
+    {
+      TimedLaunch tl_(kKChainFwd, s);
+      rc = check_cuda(launch_chain_fwd(M.W, M.Qt, M.KtT, M.Aqk, M.U, cp, s), "chain kernel");
+    }
+    if (rc) return rc;
   }
-  if (rc) return rc;
-
-  ChainParams cp{};
-  cp.seqs = reinterpret_cast<const SeqEntry*>(ws + L.seqs);
-  cp.chunks = chunks;
-  cp.kda = kda ? 1 : 0;
-  cp.N = P.N;
-  cp.H = P.H;
-  cp.gam = F(L.gam);
-  cp.h0 = a->initial_state;
-  cp.h_save = F(L.hs);
-  cp.vnew_save = F(L.vns);
-  cp.status = a->status;
-  {
-    TimedLaunch tl_(kKChainFwd, s);
-    rc = check_cuda(launch_chain_fwd(M.W, M.Qt, M.KtT, M.Aqk, M.U, cp, s), "chain kernel");
-  }
-  if (rc) return rc;
 
   RevChainParams rp{};
-  rp.seqs = cp.seqs;
+  rp.seqs = reinterpret_cast<const SeqEntry*>(sv + L.seqs);
   rp.chunks = chunks;
   rp.N = P.N;
   rp.H = P.H;
@@ -412,8 +439,8 @@ int run_bwd(const gdn_desc_t* d, const gdn_bwd_args_t* a, void* stream, bool kda
   rp.dO = static_cast<const __nv_bfloat16*>(a->dO);
   rp.dht = a->dht;
   rp.dh0 = a->dh0;
-  rp.dh_save = F(L.dhs);
-  rp.dvn_save = F(L.dvns);
+  rp.dh_save = R(L.dhs);
+  rp.dvn_save = R(L.dvns);
   rp.status = a->status;
   {
     TimedLaunch tl_(kKChainBwd, s);
@@ -427,12 +454,12 @@ int run_bwd(const gdn_desc_t* d, const gdn_bwd_args_t* a, void* stream, bool kda
   fp.H = P.H;
   fp.kda = kda ? 1 : 0;
   fp.h = F(L.hs);
-  fp.dh = F(L.dhs);
+  fp.dh = R(L.dhs);
   fp.dO = rp.dO;
   fp.A = F(L.A);
-  fp.dvn = F(L.dvns);
-  fp.dQt = F(L.dQt); fp.dKt = F(L.dKt); fp.dW = F(L.dW); fp.dK1 = F(L.dK1); fp.dV1 = F(L.dV1);
-  fp.dgam = F(L.dgam);
+  fp.dvn = R(L.dvns);
+  fp.dQt = R(L.dQt); fp.dKt = R(L.dKt); fp.dW = R(L.dW); fp.dK1 = R(L.dK1); fp.dV1 = R(L.dV1);
+  fp.dgam = R(L.dgam);
   fp.status = a->status;
   {
     TimedLaunch tl_(kKBwdFeat, s);
@@ -450,8 +477,8 @@ int run_bwd(const gdn_desc_t* d, const gdn_bwd_args_t* a, void* stream, bool kda
   tp.dO = rp.dO;
   tp.A = F(L.A);
   tp.Gc = F(L.Gc); tp.rq = F(L.rq); tp.rk = F(L.rk); tp.beff = F(L.beff);
-  tp.dQt = F(L.dQt); tp.dKt = F(L.dKt); tp.dK1 = F(L.dK1); tp.dV1 = F(L.dV1);
-  tp.gam = F(L.gam); tp.dgam = F(L.dgam);
+  tp.dQt = R(L.dQt); tp.dKt = R(L.dKt); tp.dK1 = R(L.dK1); tp.dV1 = R(L.dV1);
+  tp.gam = F(L.gam); tp.dgam = R(L.dgam);
   tp.dq = static_cast<__nv_bfloat16*>(a->dq);
   tp.dk = static_cast<__nv_bfloat16*>(a->dk);
   tp.dv = static_cast<__nv_bfloat16*>(a->dv);
@@ -500,7 +527,19 @@ int gdn_device_supported(int device) {
 size_t gdn_fwd_workspace_size(const gdn_desc_t* desc) {
   Problem P;
   if (validate_desc(desc, &P)) return 0;
-  return make_layout(P, false).total;
+  return make_layout(P, false).saved_total;
+}
+
+size_t gdn_saved_size(const gdn_desc_t* desc) {
+  Problem P;
+  if (validate_desc(desc, &P)) return 0;
+  return make_layout(P, true, false).saved_total;
+}
+
+size_t kda_saved_size(const gdn_desc_t* desc) {
+  Problem P;
+  if (validate_desc(desc, &P)) return 0;
+  return make_layout(P, true, true).saved_total;
 }
 
 size_t kda_fwd_workspace_size(const gdn_desc_t* desc) { return gdn_fwd_workspace_size(desc); }

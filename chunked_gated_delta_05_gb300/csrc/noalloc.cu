@@ -46,8 +46,8 @@ extern "C" size_t gdn_fwd_noalloc_capacity(void) { return kNoAllocScratchBytes; 
 
 extern "C" int gdn_fwd_noalloc(const gdn_desc_t* desc, const gdn_fwd_args_t* args, void* stream) {
   if (!args) return gdn_fwd(desc, args, stream);  // reports the NULL-args contract error
-  if (args->workspace || args->workspace_bytes)
-    return gdn::set_last_error(GDN_EINVAL, "gdn_fwd_noalloc takes no workspace: pass NULL and 0");
+  if (args->workspace || args->workspace_bytes || args->saved || args->saved_bytes)
+    return gdn::set_last_error(GDN_EINVAL, "gdn_fwd_noalloc takes no workspace or saved buffer: pass NULL and 0");
   const size_t need = gdn_fwd_workspace_size(desc);
   if (need == 0) return gdn_fwd(desc, args, stream);  // reports the description error
   if (need > kNoAllocScratchBytes) {

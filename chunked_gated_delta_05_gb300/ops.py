@@ -81,33 +81,39 @@ def _common_checks(q, k, v, g, beta, per_channel, offsets):
 
 
 def _fwd(per_channel, q, k, v, g, beta, initial_state, output_final_state, use_qk_l2norm,
-         use_beta_sigmoid, cu_seqlens, scale, status):
+         use_beta_sigmoid, cu_seqlens, scale, status, save=False):
     lib = _lib.load()
     offsets = _offsets(cu_seqlens, q.shape[1] if q.dim() == 4 else 0)
     B, T, H, N, dev = _common_checks(q, k, v, g, beta, per_channel, offsets)
     if initial_state is not None:
         _check_tensor("initial_state", initial_state, torch.float32, (N, H, K_DIM, K_DIM), dev)
     desc = _desc(B, T, H, scale, use_qk_l2norm, use_beta_sigmoid, output_final_state, offsets)
-    size_fn = lib.kda_fwd_workspace_size if per_channel else lib.gdn_fwd_workspace_size
+    if save:
+        size_fn = lib.kda_saved_size if per_channel else lib.gdn_saved_size
+    else:
+        size_fn = lib.kda_fwd_workspace_size if per_channel else lib.gdn_fwd_workspace_size
     ws_bytes = size_fn(ctypes.byref(desc))
     if ws_bytes == 0:
         _lib.check(_lib.GDN_EINVAL)
     o = torch.empty((B, T, H, K_DIM), dtype=torch.bfloat16, device=dev)
     final = torch.empty((N, H, K_DIM, K_DIM), dtype=torch.float32, device=dev) if output_final_state else None
-    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    buf = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
     if status is None:
         status = torch.empty(1, dtype=torch.int32, device=dev)
     a = _lib.FwdArgs(q=_ptr(q), k=_ptr(k), v=_ptr(v), g=_ptr(g), beta=_ptr(beta),
                      initial_state=_ptr(initial_state), o=_ptr(o), final_state=_ptr(final),
-                     workspace=_ptr(ws), workspace_bytes=ws_bytes, status=_ptr(status))
+                     workspace=None if save else _ptr(buf), workspace_bytes=0 if save else ws_bytes,
+                     status=_ptr(status), saved=_ptr(buf) if save else None, saved_bytes=ws_bytes if save else 0)
     stream = ctypes.c_void_p(torch.cuda.current_stream(dev).cuda_stream)
     fn = lib.kda_fwd if per_channel else lib.gdn_fwd
     _lib.check(fn(ctypes.byref(desc), ctypes.byref(a), stream))
+    if save:
+        return o, final, buf
     return o, final
 
 
 def _bwd(per_channel, q, k, v, g, beta, dO, dht, initial_state, use_qk_l2norm, use_beta_sigmoid,
-         cu_seqlens, scale, status):
+         cu_seqlens, scale, status, saved=None):
     lib = _lib.load()
     offsets = _offsets(cu_seqlens, q.shape[1] if q.dim() == 4 else 0)
     B, T, H, N, dev = _common_checks(q, k, v, g, beta, per_channel, offsets)
@@ -121,6 +127,12 @@ def _bwd(per_channel, q, k, v, g, beta, dO, dht, initial_state, use_qk_l2norm, u
     ws_bytes = size_fn(ctypes.byref(desc))
     if ws_bytes == 0:
         _lib.check(_lib.GDN_EINVAL)
+    saved_bytes = 0
+    if saved is not None:
+        saved_bytes = (lib.kda_saved_size if per_channel else lib.gdn_saved_size)(ctypes.byref(desc))
+        if not isinstance(saved, torch.Tensor) or saved.device != dev or saved.numel() < saved_bytes:
+            raise ValueError("saved must be the buffer returned by the forward with save=True")
+        ws_bytes -= saved_bytes
     dq = torch.empty_like(q)
     dk = torch.empty_like(k)
     dv = torch.empty_like(v)
@@ -133,7 +145,8 @@ def _bwd(per_channel, q, k, v, g, beta, dO, dht, initial_state, use_qk_l2norm, u
     a = _lib.BwdArgs(q=_ptr(q), k=_ptr(k), v=_ptr(v), g=_ptr(g), beta=_ptr(beta),
                      initial_state=_ptr(initial_state), dO=_ptr(dO), dht=_ptr(dht), dq=_ptr(dq),
                      dk=_ptr(dk), dv=_ptr(dv), dbeta=_ptr(dbeta), dg=_ptr(dg), dh0=_ptr(dh0),
-                     workspace=_ptr(ws), workspace_bytes=ws_bytes, status=_ptr(status))
+                     workspace=_ptr(ws), workspace_bytes=ws_bytes, status=_ptr(status),
+                     saved=_ptr(saved), saved_bytes=saved_bytes)
     stream = ctypes.c_void_p(torch.cuda.current_stream(dev).cuda_stream)
     fn = lib.kda_bwd if per_channel else lib.gdn_bwd
     _lib.check(fn(ctypes.byref(desc), ctypes.byref(a), stream))
@@ -141,53 +154,57 @@ def _bwd(per_channel, q, k, v, g, beta, dO, dht, initial_state, use_qk_l2norm, u
 
 
 def gdn_fwd(q, k, v, g, beta, *, initial_state=None, output_final_state=False, use_qk_l2norm=True,
-            use_beta_sigmoid=False, cu_seqlens: Optional[Sequence[int]] = None, scale=None, status=None):
-    """Gated DeltaNet forward. Returns ``(o [B,T,H,128] bf16, final_state [N,H,128,128] fp32 or None)``."""
+            use_beta_sigmoid=False, cu_seqlens: Optional[Sequence[int]] = None, scale=None, status=None,
+            save=False):
+    """Gated DeltaNet forward. Returns ``(o [B,T,H,128] bf16, final_state [N,H,128,128] fp32 or
+    None)``; with ``save=True`` also the saved-intermediates buffer to hand to :func:`gdn_bwd`."""
     return _fwd(False, q, k, v, g, beta, initial_state, output_final_state, use_qk_l2norm,
-                use_beta_sigmoid, cu_seqlens, scale, status)
+                use_beta_sigmoid, cu_seqlens, scale, status, save)
 
 
 def kda_fwd(q, k, v, g, beta, *, initial_state=None, output_final_state=False, use_qk_l2norm=True,
-            use_beta_sigmoid=True, cu_seqlens: Optional[Sequence[int]] = None, scale=None, status=None):
+            use_beta_sigmoid=True, cu_seqlens: Optional[Sequence[int]] = None, scale=None, status=None,
+            save=False):
     """Kimi Delta Attention forward (per-channel gate g [B,T,H,128])."""
     return _fwd(True, q, k, v, g, beta, initial_state, output_final_state, use_qk_l2norm,
-                use_beta_sigmoid, cu_seqlens, scale, status)
+                use_beta_sigmoid, cu_seqlens, scale, status, save)
 
 
 def gdn_bwd(q, k, v, g, beta, dO, *, dht=None, initial_state=None, use_qk_l2norm=True,
-            use_beta_sigmoid=False, cu_seqlens=None, scale=None, status=None):
-    """Gated DeltaNet backward. Returns ``(dq, dk, dv, dbeta, dg, dh0 or None)``."""
+            use_beta_sigmoid=False, cu_seqlens=None, scale=None, status=None, saved=None):
+    """Gated DeltaNet backward. Returns ``(dq, dk, dv, dbeta, dg, dh0 or None)``. ``saved`` is the
+    buffer of a ``save=True`` forward on the same inputs (else the forward is recomputed)."""
     return _bwd(False, q, k, v, g, beta, dO, dht, initial_state, use_qk_l2norm, use_beta_sigmoid,
-                cu_seqlens, scale, status)
+                cu_seqlens, scale, status, saved)
 
 
 def kda_bwd(q, k, v, g, beta, dO, *, dht=None, initial_state=None, use_qk_l2norm=True,
-            use_beta_sigmoid=True, cu_seqlens=None, scale=None, status=None):
+            use_beta_sigmoid=True, cu_seqlens=None, scale=None, status=None, saved=None):
     """Kimi Delta Attention backward. Returns ``(dq, dk, dv, dbeta, dg, dh0 or None)``."""
     return _bwd(True, q, k, v, g, beta, dO, dht, initial_state, use_qk_l2norm, use_beta_sigmoid,
-                cu_seqlens, scale, status)
+                cu_seqlens, scale, status, saved)
 
 
 class ChunkGatedDeltaRule(torch.autograd.Function):
-    """Autograd wrapper: forward through gdn_fwd/kda_fwd, backward through gdn_bwd/kda_bwd
-    (the backward recomputes the forward's intermediates from the saved inputs)."""
+    """Autograd wrapper: forward through gdn_fwd/kda_fwd in save mode, backward through
+    gdn_bwd/kda_bwd with the saved intermediates."""
 
     @staticmethod
     def forward(ctx, q, k, v, g, beta, initial_state, per_channel, use_qk_l2norm, use_beta_sigmoid,
                 cu_seqlens, scale, output_final_state):
-        o, final = _fwd(per_channel, q, k, v, g, beta, initial_state, output_final_state, use_qk_l2norm,
-                        use_beta_sigmoid, cu_seqlens, scale, None)
-        ctx.save_for_backward(q, k, v, g, beta, initial_state)
+        o, final, saved = _fwd(per_channel, q, k, v, g, beta, initial_state, output_final_state,
+                               use_qk_l2norm, use_beta_sigmoid, cu_seqlens, scale, None, save=True)
+        ctx.save_for_backward(q, k, v, g, beta, initial_state, saved)
         ctx.cfg = (per_channel, use_qk_l2norm, use_beta_sigmoid, cu_seqlens, scale)
         return o, final
 
     @staticmethod
     def backward(ctx, dO, dfinal):
-        q, k, v, g, beta, h0 = ctx.saved_tensors
+        q, k, v, g, beta, h0, saved = ctx.saved_tensors
         per_channel, l2, sig, cu, scale = ctx.cfg
         dq, dk, dv, dbeta, dg, dh0 = _bwd(per_channel, q, k, v, g, beta, dO.contiguous(),
                                           None if dfinal is None else dfinal.contiguous(), h0, l2, sig,
-                                          cu, scale, None)
+                                          cu, scale, None, saved)
         return dq, dk, dv, dg, dbeta, dh0, None, None, None, None, None, None
 
 

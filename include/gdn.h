@@ -81,9 +81,14 @@ typedef struct {
   const float* initial_state;/* [N,H,K,V] or NULL (zeros) */
   void* o;                   /* bf16 [B,T,H,V], written */
   float* final_state;        /* [N,H,K,V], written when output_final_state (else may be NULL) */
-  void* workspace;           /* device, >= *_fwd_workspace_size() bytes, 256-byte aligned */
+  void* workspace;           /* device, >= *_fwd_workspace_size() bytes, 256-byte aligned
+                                (ignored, may be NULL, when `saved` is given) */
   size_t workspace_bytes;
   int* status;               /* device int or NULL: nonzero after a bounded wait ran out */
+  void* saved;               /* training: device buffer of >= *_saved_size() bytes (256-byte
+                                aligned) that receives the chunk intermediates the backward
+                                needs; NULL for inference */
+  size_t saved_bytes;
 } gdn_fwd_args_t;
 
 typedef struct {
@@ -101,9 +106,14 @@ typedef struct {
   void* dbeta;               /* bf16 [B,T,H]: w.r.t. beta as passed (the logit when use_beta_sigmoid) */
   float* dg;                 /* fp32, same shape as g: w.r.t. the raw per-token gate */
   float* dh0;                /* [N,H,K,V] or NULL */
-  void* workspace;
+  void* workspace;           /* >= *_bwd_workspace_size() bytes; with `saved`, >= that minus
+                                *_saved_size() bytes */
   size_t workspace_bytes;
   int* status;
+  const void* saved;         /* the `saved` buffer of a forward with the same description and
+                                inputs (the backward then skips recomputing the forward), or
+                                NULL (the backward recomputes it) */
+  size_t saved_bytes;
 } gdn_bwd_args_t;
 
 /* Human-readable name of an error code. */
@@ -118,11 +128,16 @@ size_t gdn_fwd_workspace_size(const gdn_desc_t* desc);
 size_t gdn_bwd_workspace_size(const gdn_desc_t* desc);
 size_t kda_fwd_workspace_size(const gdn_desc_t* desc);
 size_t kda_bwd_workspace_size(const gdn_desc_t* desc);
+/* Size of the optional saved-intermediates buffer a training forward fills for its backward
+ * (the save mode of the pages' native interfaces; recompute when it is not used). */
+size_t gdn_saved_size(const gdn_desc_t* desc);
+size_t kda_saved_size(const gdn_desc_t* desc);
 
 /* Gated DeltaNet forward: o (and final_state). */
 int gdn_fwd(const gdn_desc_t* desc, const gdn_fwd_args_t* args, void* stream);
 /* Gated DeltaNet backward: gradients of <dO, o> + <dht, final_state> w.r.t. q, k, v, beta,
- * g and initial_state (dh0). The forward is recomputed from the inputs. */
+ * g and initial_state (dh0). The forward's intermediates come from `saved`, or are
+ * recomputed from the inputs when `saved` is NULL. */
 int gdn_bwd(const gdn_desc_t* desc, const gdn_bwd_args_t* args, void* stream);
 /* Kimi Delta Attention forward / backward: as above with the per-channel gate g [B,T,H,K]. */
 int kda_fwd(const gdn_desc_t* desc, const gdn_fwd_args_t* args, void* stream);
@@ -131,8 +146,8 @@ int kda_bwd(const gdn_desc_t* desc, const gdn_bwd_args_t* args, void* stream);
 /* Allocation-free forward (no counterpart in the paper: an interface addition for callers
  * that cannot allocate device memory when they run the layer, such as code inside a CUDA
  * graph capture, embedders bound to a framework allocator, or latency-critical paths).
- * Same computation and arguments as gdn_fwd, except that args->workspace must be NULL and
- * args->workspace_bytes 0: the workspace is a fixed static device array of
+ * Same computation and arguments as gdn_fwd, except that args->workspace and args->saved
+ * must be NULL and their sizes 0: the workspace is a fixed static device array of
  * gdn_fwd_noalloc_capacity() bytes (32 MiB) inside this library, held by every GPU that loads
  * it until exit. Problems whose gdn_fwd_workspace_size() exceeds it return GDN_EINVAL. The call
  * itself allocates nothing. All calls on a device share that array (it keeps the last call's

@@ -29,8 +29,8 @@ def test_exports_every_declared_symbol():
 def test_struct_sizes_match_header_layout():
     # desc: 6 ints, pointer, int, float, 3 ints (x86-64 / aarch64 LP64 alignment)
     assert ctypes.sizeof(_lib.Desc) == 56
-    assert ctypes.sizeof(_lib.FwdArgs) == 11 * 8
-    assert ctypes.sizeof(_lib.BwdArgs) == 17 * 8
+    assert ctypes.sizeof(_lib.FwdArgs) == 13 * 8
+    assert ctypes.sizeof(_lib.BwdArgs) == 19 * 8
 
 
 def desc(**kw):

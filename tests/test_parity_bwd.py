@@ -55,3 +55,22 @@ def test_no_l2norm():
     d["k"] = (d["k"].float() * 0.08).to(torch.bfloat16)
     d["q"] = (d["q"].float() * 0.08).to(torch.bfloat16)
     check(d, use_qk_l2norm=False, scale=0.3)
+
+
+def test_saved_mode_matches_recompute():
+    """The backward on the forward's saved intermediates equals the recomputing backward."""
+    from chunked_gated_delta_05_gb300 import gdn_fwd
+    d = synth.custom(1, 200, 2, h0_std=0.02, dht_std=0.01, seed=25)
+    dc = to_cuda(d)
+    o1, h1, saved = gdn_fwd(dc["q"], dc["k"], dc["v"], dc["g"], dc["beta"], initial_state=dc["h0"],
+                            output_final_state=True, save=True)
+    o2, h2 = gdn_fwd(dc["q"], dc["k"], dc["v"], dc["g"], dc["beta"], initial_state=dc["h0"],
+                     output_final_state=True)
+    g1 = gdn_bwd(dc["q"], dc["k"], dc["v"], dc["g"], dc["beta"], dc["dO"], dht=dc["dht"],
+                 initial_state=dc["h0"], saved=saved)
+    g2 = gdn_bwd(dc["q"], dc["k"], dc["v"], dc["g"], dc["beta"], dc["dO"], dht=dc["dht"],
+                 initial_state=dc["h0"])
+    torch.cuda.synchronize()
+    assert torch.equal(o1, o2) and torch.equal(h1, h2)
+    for a, b in zip(g1, g2):
+        assert torch.equal(a, b)
