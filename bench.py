@@ -38,6 +38,15 @@ KERNEL_FLOP_PER_CHUNK_HEAD = {
     "tables": (0, "none"),
 }
 TF32_OVER_BF16 = 1.1 / 2.25    # nominal dense tf32 / bf16 tensor rates of a GB300
+# DRAM bytes (read + write) of one launch, from an `ncu --set full` capture of the same kernel
+# build on the same workload (profiles/kernels_gdn_b2_t4096_h16.md); None elsewhere.
+NCU_TRAFFIC_BYTES = {
+    ("bwd_tok", "gdn_b2_t4096_h16"): (640.279552 + 89.481472) * 1e6,
+    ("chain_bwd", "gdn_b2_t4096_h16"): (268.789760 + 163.746560) * 1e6,
+    ("bwd_feat", "gdn_b2_t4096_h16"): (470.668288 + 294.395648) * 1e6,
+    ("prepare", "gdn_b2_t4096_h16"): (104.316672 + 515.707648) * 1e6,
+    ("chain_fwd", "gdn_b2_t4096_h16"): (304.646656 + 196.257024) * 1e6,
+}
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
@@ -267,8 +276,11 @@ def main():
     achieved = flop_chunk * n_chunk_heads / (avg_ms * 1e-3) / 1e12
     peak = bf16_sus * (TF32_OVER_BF16 if kind == "tf32" else 1.0)
     kernel_share = {k: round(v[0] / max(1e-9, sum(x[0] for x in per_kernel.values())), 4) for k, v in per_kernel.items()}
+    traffic = NCU_TRAFFIC_BYTES.get((name, w.name))
     roofline = {"bound": "tensor", "kernel": name, "operands": kind, "achieved": achieved, "peak": peak,
-                "unit": "TFLOP/s", "frac": achieved / peak, "traffic": None,
+                "unit": "TFLOP/s", "frac": achieved / peak, "traffic": traffic,
+                "traffic_gbs": None if traffic is None else traffic / (avg_ms * 1e-3) / 1e9,
+                "traffic_frac_of_hbm": None if traffic is None else traffic / (avg_ms * 1e-3) / 1e9 / peaks["hbm_gbs"],
                 "peak_source": f"{peak_src} bf16 sustained" + (" x nominal tf32/bf16 ratio" if kind == "tf32" else ""),
                 "avg_launch_ms": avg_ms, "kernel_time_share": kernel_share}
     gpu_launches = sum(v[1] for v in per_kernel.values())

@@ -54,20 +54,17 @@ __device__ __forceinline__ uint8_t* align1k(uint8_t* p) {
   return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
 }
 
-// S pass for chunk c (one thread: lane v, state columns [k0, k0+64)): record the entry state,
-// write its tf32 copy (the MMA operand) and pre-apply the chunk's end decay to the fp32 master
-// copy (the MMA then adds k~^T v_new in place).
+// S pass for chunk c (one thread: lane v, state columns [k0, k0+64)): write the entry state's
+// tf32 copy (the MMA operand), pre-apply the chunk's end decay to the fp32 master copy (the
+// MMA then adds k~^T v_new in place), release the MMA issuer, and only then record the entry
+// state for the backward (the tf32 copy: every later use of it is a tf32 operand or a sum of
+// its products), so the global stores stay off the serial path.
 __device__ __forceinline__ void chain_state_pass(const ChainParams& p, int c, int h, int v, int k0,
-                                                 uint32_t tl, uint64_t* sready) {
+                                                 uint32_t tl, uint64_t* sready, float g0) {
   const size_t tile = size_t(c) * p.H + h;
   float s[64];
   tmem_ld64(tl + kTSM + k0, s);
   tmem_wait_ld_regs(s);
-  if (p.h_save) {
-    float* hs = p.h_save + tile * kD * kD + size_t(k0) * kD + v;
-#pragma unroll
-    for (int e = 0; e < 64; ++e) hs[size_t(e) * kD] = s[e];
-  }
 #pragma unroll
   for (int half = 0; half < 2; ++half) {
     float t[32];
@@ -86,7 +83,6 @@ __device__ __forceinline__ void chain_state_pass(const ChainParams& p, int c, in
       s[4 * e + 3] *= g4.w;
     }
   } else {
-    const float g0 = p.gam[tile * kD];
 #pragma unroll
     for (int e = 0; e < 64; ++e) s[e] *= g0;
   }
@@ -95,6 +91,14 @@ __device__ __forceinline__ void chain_state_pass(const ChainParams& p, int c, in
   tmem_wait_st();
   tc_fence_before();
   mbar_arrive(sready);
+  if (p.h_save) {
+    // re-read the tf32 copy (the MMAs only read it) and store it
+    tmem_ld64(tl + kTST + k0, s);
+    tmem_wait_ld_regs(s);
+    float* hs = p.h_save + tile * kD * kD + size_t(k0) * kD + v;
+#pragma unroll
+    for (int e = 0; e < 64; ++e) hs[size_t(e) * kD] = s[e];
+  }
 }
 
 }  // namespace
@@ -212,13 +216,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_st32(tb + lb + kTSM + k0 + 32, buf + 32);
       tmem_wait_st();
     }
-    chain_state_pass(p, first, h, v, k0, tb + lb, &sready);
+    chain_state_pass(p, first, h, v, k0, tb + lb, &sready, p.kda ? 0.f : p.gam[(size_t(first) * H + h) * kD]);
     bool alive = true;
     for (int j = 0; j < nc; ++j) {
       const uint32_t par = j & 1;
       const int c = first + j;
       const ChunkEntry ch = p.chunks[c];
       const size_t tile = size_t(c) * H + h;
+      // next chunk's scalar gate, loaded early so the state pass does not wait for it
+      const float gnext = (j + 1 < nc && !p.kda) ? p.gam[(size_t(c + 1) * H + h) * kD] : 0.f;
       if (!mbar_wait(&full2, par, &abort_flag, p.status, kDevTimeoutTma)) { alive = false; break; }
       float u[32];
 #pragma unroll
@@ -229,20 +235,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         float r[32];
         tmem_ld32(tb + lb + kTP + t0, r);
         tmem_wait_ld_regs(r);
-        float* vsave = p.vnew_save ? p.vnew_save + tile * kTileW + size_t(t0) * kD + v : nullptr;
 #pragma unroll
-        for (int t = 0; t < 32; ++t) {
-          r[t] = to_tf32(u[t] - r[t]);
-          if (vsave) vsave[size_t(t) * kD] = r[t];
-        }
+        for (int t = 0; t < 32; ++t) r[t] = to_tf32(u[t] - r[t]);
         tmem_st32(tb + lb + kTVN + t0, r);
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(&vready);
+        if (p.vnew_save) {
+          float* vsave = p.vnew_save + tile * kTileW + size_t(t0) * kD + v;
+#pragma unroll
+          for (int t = 0; t < 32; ++t) vsave[size_t(t) * kD] = r[t];
+        }
       }
-      tmem_wait_st();
-      tc_fence_before();
-      mbar_arrive(&vready);
       if (!mbar_wait(&mma2, par, &abort_flag, p.status, kDevTimeoutMma)) { alive = false; break; }
       tc_fence_after();
-      if (j + 1 < nc) chain_state_pass(p, c + 1, h, v, k0, tb + lb, &sready);
+      if (j + 1 < nc) chain_state_pass(p, c + 1, h, v, k0, tb + lb, &sready, gnext);
       if (!mbar_wait(&mma3, par, &abort_flag, p.status, kDevTimeoutMma)) { alive = false; break; }
       tc_fence_after();
       {

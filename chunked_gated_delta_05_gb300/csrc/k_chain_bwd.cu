@@ -21,6 +21,18 @@
 
 namespace gdn {
 
+#ifdef GDN_TRACE
+// Optional timeline of the first CTA (compiled only with -DGDN_TRACE; never in the library).
+__device__ unsigned long long g_trace_rev[64 * 8];
+#define RTRACE(j, slot) \
+  do { if (blockIdx.x == 0 && blockIdx.y == 0 && (j) < 64) g_trace_rev[(j) * 8 + (slot)] = globaltimer(); } while (0)
+extern "C" int gdn_trace_rev_read(unsigned long long* host) {
+  return cudaMemcpyFromSymbol(host, g_trace_rev, sizeof(g_trace_rev)) == cudaSuccess ? 0 : -1;
+}
+#else
+#define RTRACE(j, slot) do {} while (0)
+#endif
+
 namespace {
 
 constexpr int kChainThreads = 256;
@@ -37,21 +49,30 @@ __device__ __forceinline__ uint8_t* align1k(uint8_t* p) {
   return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
 }
 
-// dS pass for chunk c (lane v, state columns [k0, k0+64); token columns [t0, t0+32)):
-// save dS' (the gradient w.r.t. the state leaving chunk c), write its tf32 copy, pre-apply
-// the chunk decay to the master copy, and stage dO^T for this chunk as an A operand.
-__device__ __forceinline__ void rev_pass(const RevChainParams& p, int c, int h, int v, int k0, int t0,
-                                         uint32_t tl, uint64_t* ready) {
-  const size_t tile = size_t(c) * p.H + h;
+// Loads this thread's 32 dO values (token columns [t0, t0+32) of lane v) for chunk c, two
+// bf16 per 32-bit register (rows past the chunk read as zero).
+__device__ __forceinline__ void load_dO(const RevChainParams& p, int c, int h, int v, int t0, uint32_t* d) {
   const ChunkEntry ch = p.chunks[c];
+  const unsigned short* src =
+      reinterpret_cast<const unsigned short*>(p.dO) + (size_t(ch.x + t0) * p.H + h) * kD + v;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    const uint32_t lo = (t0 + 2 * i < ch.y) ? src[size_t(2 * i) * p.H * kD] : 0u;
+    const uint32_t hi = (t0 + 2 * i + 1 < ch.y) ? src[size_t(2 * i + 1) * p.H * kD] : 0u;
+    d[i] = lo | (hi << 16);
+  }
+}
+
+// dS pass for chunk c (lane v, state columns [k0, k0+64); token columns [t0, t0+32)): write
+// the tf32 copy of dS' (the gradient w.r.t. the state leaving chunk c) and dO^T (prefetched
+// into `d`) as A operands, pre-apply the chunk decay to the master copy, release the MMA
+// issuer, then save dS' (its tf32 copy) for the feature-major backward kernel.
+__device__ __forceinline__ void rev_pass(const RevChainParams& p, int c, int h, int v, int k0, int t0,
+                                         uint32_t tl, uint64_t* ready, const uint32_t* d, float g0) {
+  const size_t tile = size_t(c) * p.H + h;
   float s[64];
   tmem_ld64(tl + kTDM + k0, s);
   tmem_wait_ld_regs(s);
-  {
-    float* ds = p.dh_save + tile * kD * kD + size_t(k0) * kD + v;
-#pragma unroll
-    for (int e = 0; e < 64; ++e) ds[size_t(e) * kD] = s[e];
-  }
 #pragma unroll
   for (int half = 0; half < 2; ++half) {
     float t[32];
@@ -70,22 +91,29 @@ __device__ __forceinline__ void rev_pass(const RevChainParams& p, int c, int h, 
       s[4 * e + 3] *= g4.w;
     }
   } else {
-    const float g0 = p.gam[tile * kD];
 #pragma unroll
     for (int e = 0; e < 64; ++e) s[e] *= g0;
   }
   tmem_st32(tl + kTDM + k0, s);
   tmem_st32(tl + kTDM + k0 + 32, s + 32);
   {
-    float d[32];
-    const __nv_bfloat16* src = p.dO + (size_t(ch.x + t0) * p.H + h) * kD + v;
+    float df[32];
 #pragma unroll
-    for (int i = 0; i < 32; ++i) d[i] = (t0 + i < ch.y) ? __bfloat162float(src[size_t(i) * p.H * kD]) : 0.f;
-    tmem_st32(tl + kTDO + t0, d);
+    for (int i = 0; i < 16; ++i) {
+      df[2 * i] = __uint_as_float(d[i] << 16);
+      df[2 * i + 1] = __uint_as_float(d[i] & 0xffff0000u);
+    }
+    tmem_st32(tl + kTDO + t0, df);
   }
   tmem_wait_st();
   tc_fence_before();
   mbar_arrive(ready);
+  // re-read the tf32 copy (the MMAs only read it) and save it
+  tmem_ld64(tl + kTDT + k0, s);
+  tmem_wait_ld_regs(s);
+  float* ds = p.dh_save + tile * kD * kD + size_t(k0) * kD + v;
+#pragma unroll
+  for (int e = 0; e < 64; ++e) ds[size_t(e) * kD] = s[e];
 }
 
 }  // namespace
@@ -142,21 +170,27 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int c = last - j, st = j & 1;
         const uint32_t par = j & 1;
         const uint32_t base = smem_u32(sm + st * kStage);
+        RTRACE(j, 0);
         if (!mbar_wait(&full[st], (j >> 1) & 1, &abort_flag, p.status, kDevTimeoutTma)) break;
+        RTRACE(j, 1);
         if (!mbar_wait(&dready, par, &abort_flag, p.status, kDevTimeoutSync)) break;
+        RTRACE(j, 2);
         tc_fence_after();
         // dv_new^T = dO^T Aqk + dS'^T Kt^T
         for (int s = 0; s < 8; ++s) mma_tf32_ts(tb + kTDV, tb + kTDO + s * 8, desc_kmajor(base + kOffAqkT, 8192, s), id64, s > 0);
         for (int s = 0; s < 16; ++s) mma_tf32_ts(tb + kTDV, tb + kTDT + s * 8, desc_kmajor(base + kOffKt, 8192, s), id64, true);
         mma_commit(&mma1);
+        RTRACE(j, 6);
         // dS^T += dO^T Qt   (master copy already holds gam dS'^T)
         for (int s = 0; s < 8; ++s) mma_tf32_ts(tb + kTDM, tb + kTDO + s * 8, desc_kmajor(base + kOffQtT, 16384, s), id128, true);
         if (!mbar_wait(&vready, par, &abort_flag, p.status, kDevTimeoutSync)) break;
+        RTRACE(j, 3);
         tc_fence_after();
         // dS^T += (-dv_new^T) W
         for (int s = 0; s < 8; ++s) mma_tf32_ts(tb + kTDM, tb + kTDN + s * 8, desc_kmajor(base + kOffWT, 16384, s), id128, true);
         mma_commit(&mma2);
         if (!mbar_wait(&mma2, par, &abort_flag, p.status, kDevTimeoutMma)) break;
+        RTRACE(j, 4);
         if (j + 2 < nc) load(c - 2, st);
       }
     }
@@ -173,33 +207,39 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_st32(tl + kTDM + k0 + 32, buf + 32);
       tmem_wait_st();
     }
-    rev_pass(p, last, h, v, k0, t0, tl, &dready);
+    uint32_t dnext[16];
+    load_dO(p, last, h, v, t0, dnext);
+    rev_pass(p, last, h, v, k0, t0, tl, &dready, dnext, p.kda ? 0.f : p.gam[(size_t(last) * H + h) * kD]);
     bool alive = true;
     for (int j = 0; j < nc; ++j) {
       const int c = last - j;
       const uint32_t par = j & 1;
       const size_t tile = size_t(c) * H + h;
+      // next chunk's scalar gate, loaded early so the dS pass does not wait for it
+      const float gnext = (j + 1 < nc && !p.kda) ? p.gam[(size_t(c - 1) * H + h) * kD] : 0.f;
       if (!mbar_wait(&mma1, par, &abort_flag, p.status, kDevTimeoutMma)) { alive = false; break; }
+      if (tid == 0) RTRACE(j, 5);
       tc_fence_after();
       {
         float r[32];
         tmem_ld32(tl + kTDV + t0, r);
         tmem_wait_ld_regs(r);
+#pragma unroll
+        for (int t = 0; t < 32; ++t) r[t] = -to_tf32(r[t]);
+        tmem_st32(tl + kTDN + t0, r);
+        tmem_wait_st();
+        tc_fence_before();
+        if (tid == 0) RTRACE(j, 7);
+        mbar_arrive(&vready);
         float* dv = p.dvn_save + tile * kTileW + size_t(t0) * kD + v;
 #pragma unroll
-        for (int t = 0; t < 32; ++t) {
-          r[t] = to_tf32(r[t]);
-          dv[size_t(t) * kD] = r[t];
-          r[t] = -r[t];
-        }
-        tmem_st32(tl + kTDN + t0, r);
+        for (int t = 0; t < 32; ++t) dv[size_t(t) * kD] = -r[t];
       }
-      tmem_wait_st();
-      tc_fence_before();
-      mbar_arrive(&vready);
+      // prefetch the next chunk's dO while the second MMA group runs
+      if (j + 1 < nc) load_dO(p, c - 1, h, v, t0, dnext);
       if (!mbar_wait(&mma2, par, &abort_flag, p.status, kDevTimeoutMma)) { alive = false; break; }
       tc_fence_after();
-      if (j + 1 < nc) rev_pass(p, c - 1, h, v, k0, t0, tl, &dready);
+      if (j + 1 < nc) rev_pass(p, c - 1, h, v, k0, t0, tl, &dready, dnext, gnext);
     }
     if (alive && p.dh0) {
       float s[64];
