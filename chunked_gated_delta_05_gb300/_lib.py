@@ -52,6 +52,8 @@ SIGNATURES = {
     "kda_bwd": ([ctypes.POINTER(Desc), ctypes.POINTER(BwdArgs), c_void_p], c_int),
     "gdn_fwd_noalloc": ([ctypes.POINTER(Desc), ctypes.POINTER(FwdArgs), c_void_p], c_int),
     "gdn_fwd_noalloc_capacity": ([], c_size_t),
+    "gdn_set_chain_segment": ([c_int], c_int),
+    "gdn_chain_plan": ([ctypes.POINTER(Desc), ctypes.POINTER(c_int), ctypes.POINTER(c_int)], c_int),
     "gdn_timing_enable": ([c_int], c_int),
     "gdn_timing_kinds": ([], c_int),
     "gdn_timing_name": ([c_int], ctypes.c_char_p),

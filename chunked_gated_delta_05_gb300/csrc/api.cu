@@ -9,6 +9,7 @@
 // RuntimeError).
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <cmath>
 #include <cstdio>
 #include <mutex>
@@ -100,6 +101,74 @@ int validate_desc(const gdn_desc_t* d, Problem* P) {
   return GDN_OK;
 }
 
+// ------------------------------------------------------------------ segmented chain plan
+// Segment length (in chunks) forced by gdn_set_chain_segment(); 0 = chosen by plan_scan().
+int g_chain_segment = 0;
+
+// Wave model of the chain scan on a GB300 (152 SMs, one chain CTA per SM): pass 0 runs
+// 1 + 2 (ns - 2) CTAs per (sequence, head), pass 1 runs ns - 1, each for about L chunk steps;
+// the compose kernel walks ns - 2 segments.
+constexpr int kWaveSMs = 152;
+constexpr double kChunkStepUs = 3.7, kComposeStepUs = 3.0, kLaunchUs = 3.0;
+constexpr int kMaxSegments = 64;
+
+struct ScanPlan {
+  int L = 1;     // chunks per segment
+  int maxS = 1;  // most segments of any sequence
+};
+
+ScanPlan plan_scan(const Problem& P) {
+  // distinct per-sequence chunk counts with their multiplicities
+  std::vector<std::pair<int, int>> lens;
+  int maxNC = 0;
+  if (P.packed) {
+    std::vector<int> nc(P.N);
+    for (int n = 0; n < P.N; ++n) nc[n] = (P.cu[n + 1] - P.cu[n] + kC - 1) / kC;
+    std::sort(nc.begin(), nc.end());
+    for (int x : nc) {
+      if (lens.empty() || lens.back().first != x) lens.push_back({x, 0});
+      ++lens.back().second;
+    }
+    maxNC = nc.back();
+  } else {
+    maxNC = (P.T + kC - 1) / kC;
+    lens.push_back({maxNC, P.N});
+  }
+  auto segments = [&](int L) {
+    int m = 0;
+    for (auto& e : lens) m = std::max(m, (e.first + L - 1) / L);
+    return m;
+  };
+  ScanPlan best;
+  if (g_chain_segment > 0) {
+    best.L = std::min(g_chain_segment, maxNC);
+    best.maxS = segments(best.L);
+    return best;
+  }
+  double best_t = 1e300;
+  for (int S = 1; S <= std::min(maxNC, kMaxSegments); ++S) {
+    const int L = (maxNC + S - 1) / S;
+    long long runs0 = 0, runs1 = 0;
+    int maxS = 0;
+    for (auto& e : lens) {
+      const int ns = (e.first + L - 1) / L;
+      maxS = std::max(maxS, ns);
+      runs0 += (long long)e.second * (ns <= 2 ? 1 : 2 * ns - 3);
+      runs1 += (long long)e.second * (ns - 1);
+    }
+    auto waves = [&](long long r) { return double((r * P.H + kWaveSMs - 1) / kWaveSMs); };
+    double t = waves(runs0) * L * kChunkStepUs;
+    if (maxS >= 2) t += waves(runs1) * L * kChunkStepUs + kLaunchUs;
+    if (maxS >= 3) t += (maxS - 2) * kComposeStepUs + kLaunchUs;
+    if (t < best_t - 1e-9) {
+      best_t = t;
+      best.L = L;
+      best.maxS = maxS;
+    }
+  }
+  return best;
+}
+
 // Buffer carve-up. The "saved" part holds the chunk tables, the prepare tiles and (for a
 // training forward / backward) the chain saves; the "rest" part holds what only the backward
 // uses. Inference forward: saved part only (forward subset). Backward without a saved buffer:
@@ -109,8 +178,11 @@ struct Layout {
   size_t cu, seqs, chunks, W, U, Qt, KtT, Aqk, gam;               // forward
   size_t Kt, QtT, AqkT, WT, A, Gc, rq, rk, beff;                  // prepare, backward mode
   size_t hs, vns;                                                  // forward chain saves
+  size_t fE, fPhi, fPlo, fB;                                       // forward chain scan (scratch)
   size_t dhs, dvns, dQt, dKt, dW, dK1, dV1, dgam;                  // rest part (relative)
+  size_t rE, rPhi, rPlo, rB;                                       // reverse chain scan (rest part)
   size_t saved_total, rest_total, total;
+  ScanPlan plan;
 };
 
 Layout make_layout(const Problem& P, bool backward, bool kda = false) {
@@ -144,6 +216,12 @@ Layout make_layout(const Problem& P, bool backward, bool kda = false) {
     L.hs = take(4 * tiles * kD * kD);
     L.vns = take(4 * tiles * kTileW);
   }
+  L.plan = plan_scan(P);
+  const size_t scan_states = L.plan.maxS > 1 ? size_t(P.N) * L.plan.maxS * P.H * kD * kD * 4 : 0;
+  L.fE = take(scan_states);
+  L.fPhi = take(scan_states);
+  L.fPlo = take(scan_states);
+  L.fB = take(scan_states);
   L.saved_total = off;
   off = 0;
   if (backward) {
@@ -155,6 +233,10 @@ Layout make_layout(const Problem& P, bool backward, bool kda = false) {
     L.dK1 = take(4 * tiles * kTileW);
     L.dV1 = take(4 * tiles * kTileW);
     L.dgam = take(4 * tiles * kD);
+    L.rE = take(scan_states);
+    L.rPhi = take(scan_states);
+    L.rPlo = take(scan_states);
+    L.rB = take(scan_states);
   }
   L.rest_total = off;
   L.total = L.saved_total + L.rest_total;
@@ -187,8 +269,9 @@ int check_cuda(cudaError_t e, const char* what) {
 
 // Optional per-kernel timing (CUDA events recorded on the launching stream around every
 // launch while enabled). Process-global and not thread-safe: a profiling aid.
-enum KernelKind { kKTables = 0, kKPrep, kKChainFwd, kKChainBwd, kKBwdFeat, kKBwdTok, kKinds };
-const char* const kKindNames[kKinds] = {"tables", "prepare", "chain_fwd", "chain_bwd", "bwd_feat", "bwd_tok"};
+enum KernelKind { kKTables = 0, kKPrep, kKChainFwd, kKChainBwd, kKBwdFeat, kKBwdTok, kKCompose, kKinds };
+const char* const kKindNames[kKinds] = {"tables", "prepare", "chain_fwd", "chain_bwd", "bwd_feat", "bwd_tok",
+                                        "compose"};
 struct Timing {
   bool on = false;
   std::vector<std::pair<cudaEvent_t, cudaEvent_t>> ev[kKinds];
@@ -298,6 +381,65 @@ int build_tables(const Problem& P, void* ws, const Layout& L, int* status, cudaS
   return check_cuda(launch_tables(tp, s), "chunk tables");
 }
 
+SegPlan seg_plan(const ScanPlan& sc, char* base, size_t E, size_t Phi, size_t Plo, size_t B) {
+  SegPlan sp{};
+  sp.L = sc.L;
+  sp.maxS = sc.maxS;
+  sp.pass = 0;
+  sp.E = reinterpret_cast<float*>(base + E);
+  sp.Phi = reinterpret_cast<float*>(base + Phi);
+  sp.Plo = reinterpret_cast<float*>(base + Plo);
+  sp.Bm = reinterpret_cast<float*>(base + B);
+  return sp;
+}
+
+// Compose step between the two chain passes (sequences with three or more segments).
+int run_compose(const Problem& P, const SeqEntry* seqs, const SegPlan& sp, int* status, cudaStream_t s) {
+  const uint64_t rows = uint64_t(P.N) * sp.maxS * P.H * kD;
+  CUtensorMap mPhi, mPlo;
+  if (!tile_map(&mPhi, reinterpret_cast<const char*>(sp.Phi), kD, rows, 128, true) ||
+      !tile_map(&mPlo, reinterpret_cast<const char*>(sp.Plo), kD, rows, 128, true))
+    return fail(GDN_ECUDA, "cuTensorMapEncodeTiled failed");
+  ComposeParams cp{};
+  cp.seqs = seqs;
+  cp.N = P.N;
+  cp.H = P.H;
+  cp.sp = sp;
+  cp.status = status;
+  TimedLaunch tl_(kKCompose, s);
+  return check_cuda(launch_compose(mPhi, mPlo, cp, s), "compose kernel");
+}
+
+// Forward chain: one plain pass, or pass 0, compose, pass 1 of the segmented chain.
+int run_chain_fwd(const Problem& P, const Maps& M, ChainParams cp, cudaStream_t s) {
+  for (int pass = 0; pass < (cp.sp.maxS > 1 ? 2 : 1); ++pass) {
+    if (pass == 1 && cp.sp.maxS >= 3) {
+      int rc = run_compose(P, cp.seqs, cp.sp, cp.status, s);
+      if (rc) return rc;
+    }
+    cp.sp.pass = pass;
+    TimedLaunch tl_(kKChainFwd, s);
+    int rc = check_cuda(launch_chain_fwd(M.W, M.Qt, M.KtT, M.Aqk, M.U, cp, s), "chain kernel");
+    if (rc) return rc;
+  }
+  return GDN_OK;
+}
+
+// Reverse chain, same structure.
+int run_chain_bwd(const Problem& P, const Maps& M, RevChainParams rp, cudaStream_t s) {
+  for (int pass = 0; pass < (rp.sp.maxS > 1 ? 2 : 1); ++pass) {
+    if (pass == 1 && rp.sp.maxS >= 3) {
+      int rc = run_compose(P, rp.seqs, rp.sp, rp.status, s);
+      if (rc) return rc;
+    }
+    rp.sp.pass = pass;
+    TimedLaunch tl_(kKChainBwd, s);
+    int rc = check_cuda(launch_chain_bwd(M.Kt, M.AqkT, M.QtT, M.WT, rp, s), "reverse chain kernel");
+    if (rc) return rc;
+  }
+  return GDN_OK;
+}
+
 int run_fwd(const gdn_desc_t* d, const gdn_fwd_args_t* a, void* stream, bool kda) {
   Problem P;
   int rc = validate_desc(d, &P);
@@ -355,8 +497,8 @@ int run_fwd(const gdn_desc_t* d, const gdn_fwd_args_t* a, void* stream, bool kda
     cp.vnew_save = reinterpret_cast<float*>(ws + L.vns);
   }
   cp.status = a->status;
-  TimedLaunch tl_(kKChainFwd, s);
-  return check_cuda(launch_chain_fwd(M.W, M.Qt, M.KtT, M.Aqk, M.U, cp, s), "chain kernel");
+  cp.sp = seg_plan(L.plan, ws, L.fE, L.fPhi, L.fPlo, L.fB);
+  return run_chain_fwd(P, M, cp, s);
 }
 
 int run_bwd(const gdn_desc_t* d, const gdn_bwd_args_t* a, void* stream, bool kda) {
@@ -422,10 +564,8 @@ int run_bwd(const gdn_desc_t* d, const gdn_bwd_args_t* a, void* stream, bool kda
     cp.h_save = F(L.hs);
     cp.vnew_save = F(L.vns);
     cp.status = a->status;
-    {
-      TimedLaunch tl_(kKChainFwd, s);
-      rc = check_cuda(launch_chain_fwd(M.W, M.Qt, M.KtT, M.Aqk, M.U, cp, s), "chain kernel");
-    }
+    cp.sp = seg_plan(L.plan, sv, L.fE, L.fPhi, L.fPlo, L.fB);
+    rc = run_chain_fwd(P, M, cp, s);
     if (rc) return rc;
   }
 
@@ -442,10 +582,8 @@ int run_bwd(const gdn_desc_t* d, const gdn_bwd_args_t* a, void* stream, bool kda
   rp.dh_save = R(L.dhs);
   rp.dvn_save = R(L.dvns);
   rp.status = a->status;
-  {
-    TimedLaunch tl_(kKChainBwd, s);
-    rc = check_cuda(launch_chain_bwd(M.Kt, M.AqkT, M.QtT, M.WT, rp, s), "reverse chain kernel");
-  }
+  rp.sp = seg_plan(L.plan, rs, L.rE, L.rPhi, L.rPlo, L.rB);
+  rc = run_chain_bwd(P, M, rp, s);
   if (rc) return rc;
 
   BwdFeatParams fp{};
@@ -554,6 +692,23 @@ size_t kda_bwd_workspace_size(const gdn_desc_t* desc) {
   Problem P;
   if (validate_desc(desc, &P)) return 0;
   return make_layout(P, true, true).total;
+}
+
+int gdn_set_chain_segment(int chunks) {
+  if (chunks < 0) return fail(GDN_EINVAL, "segment length must be >= 0");
+  g_chain_segment = chunks;
+  return GDN_OK;
+}
+
+int gdn_chain_plan(const gdn_desc_t* desc, int* chunks_per_segment, int* max_segments) {
+  Problem P;
+  int rc = validate_desc(desc, &P);
+  if (rc) return rc;
+  if (!chunks_per_segment || !max_segments) return fail(GDN_EINVAL, "NULL output pointer");
+  const ScanPlan sc = plan_scan(P);
+  *chunks_per_segment = sc.L;
+  *max_segments = sc.maxS;
+  return GDN_OK;
 }
 
 int gdn_timing_enable(int enable) {

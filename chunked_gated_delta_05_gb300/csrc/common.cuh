@@ -30,6 +30,52 @@ constexpr size_t kTileW = size_t(kC) * kD;
 constexpr size_t kTileKtT = size_t(kD) * kC;
 constexpr size_t kTileAqk = size_t(kC) * kC;
 
+// Segmented chain (chunk-parallel affine state scan). The chunk map of the chain is affine
+// in the state, S_out = M_c S_in + B_c with M_c = diag(gam) - k~^T W and B_c = k~^T U
+// (the affine state summary of the pages' context-parallel GDN path, composed over chunks);
+// the reverse chain's map is its adjoint. Each sequence's chunks are cut into segments of L
+// chunks (the last may be shorter), numbered in processing order (reverse chain: from the
+// sequence's end). Pass 0 runs segment 0 in full from the true initial state and, for every
+// segment 1..ns-2, the segment's map twice: from the identity with no input (giving M) and
+// from zero with the input (giving B). A compose kernel then walks the segments, E[s+1] =
+// M_s E[s] + B_s, and pass 1 runs segments 1..ns-1 in full from E[s]. L >= every sequence's
+// chunk count (maxS == 1) is the plain serial chain.
+enum RunMode : int { kRunFull = 0, kRunMapM = 1, kRunMapB = 2 };
+
+struct SegPlan {
+  int L;       // chunks per segment
+  int maxS;    // most segments of any sequence (1 = plain chain)
+  int pass;    // 0 or 1
+  float* E;    // [N*maxS*H][128][128] entry state (reverse: exit gradient) of each segment
+  float* Phi;  // [N*maxS*H][128][128] segment map M, tf32 high part
+  float* Plo;  // [N*maxS*H][128][128] segment map M, tf32 low part (M - Phi, rounded)
+  float* Bm;   // [N*maxS*H][128][128] segment offset B
+};
+
+// CTAs per sequence (and head) of a chain pass.
+__host__ __device__ inline int runs_per_seq(int maxS, int pass) {
+  return pass == 0 ? (maxS <= 2 ? 1 : 2 * maxS - 3) : maxS - 1;
+}
+
+// Segment and mode of run `slot` of a pass for a sequence of `ns` segments; false when the
+// sequence has no such run (the CTA exits at once).
+__host__ __device__ inline bool decode_run(int slot, int pass, int ns, int* seg, int* mode) {
+  if (pass == 0) {
+    if (slot == 0) {
+      *seg = 0;
+      *mode = kRunFull;
+      return true;
+    }
+    const int i = (slot - 1) >> 1;
+    *seg = 1 + i;
+    *mode = ((slot - 1) & 1) ? kRunMapB : kRunMapM;
+    return 1 + i <= ns - 2;
+  }
+  *seg = 1 + slot;
+  *mode = kRunFull;
+  return 1 + slot <= ns - 1;
+}
+
 struct PrepParams {
   const ChunkEntry* chunks;
   int NC, H;
@@ -53,6 +99,7 @@ struct RevChainParams {
   const ChunkEntry* chunks;
   int N, H;
   int kda;
+  SegPlan sp;
   const float* gam;            // [NC,H,128]
   const __nv_bfloat16* dO;     // [R,H,V]
   const float* dht;            // [N,H,K,V] or null
@@ -67,6 +114,7 @@ struct ChainParams {
   const ChunkEntry* chunks;
   int N, H;
   int kda;
+  SegPlan sp;
   const float* gam;
   const float* h0;             // [N,H,K,V] or null
   float* hT;                   // [N,H,K,V] or null
@@ -132,6 +180,15 @@ cudaError_t launch_bwd_tok(const CUtensorMap& mq, const CUtensorMap& mk, const C
 cudaError_t launch_bwd_tok_kda(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
                                const CUtensorMap& mVN, const CUtensorMap& mDW, const CUtensorMap& mDVN,
                                const BwdTokParams& p, cudaStream_t s);
+struct ComposeParams {
+  const SeqEntry* seqs;
+  int N, H;
+  SegPlan sp;
+  int* status;
+};
+
+cudaError_t launch_compose(const CUtensorMap& mPhi, const CUtensorMap& mPlo, const ComposeParams& p,
+                           cudaStream_t s);
 cudaError_t launch_chain_fwd(const CUtensorMap& mW, const CUtensorMap& mQt, const CUtensorMap& mKtT,
                              const CUtensorMap& mAqk, const CUtensorMap& mU, const ChainParams& p,
                              cudaStream_t s);

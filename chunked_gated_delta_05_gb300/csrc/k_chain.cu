@@ -18,6 +18,11 @@
 // products run on the tensor pipe while the chain threads work. Eight chain warps share the
 // TMEM lanes (two threads per lane, each on half of the columns); warp 8 streams the tiles
 // with TMA (KtT/Aqk double-buffered) and issues the MMAs from one thread. All waits bounded.
+//
+// A CTA runs one segment of a sequence's chunks in one of three modes (the segmented chain
+// of common.cuh): in full (from the true entry state, with the output and the backward
+// saves), or as the segment's affine map, from the identity with U = 0 (M) or from zero
+// (B), with no outputs and the output products, Qt and Aqk left out.
 #include "common.cuh"
 #include "umma.cuh"
 
@@ -59,8 +64,8 @@ __device__ __forceinline__ uint8_t* align1k(uint8_t* p) {
 // MMA then adds k~^T v_new in place), release the MMA issuer, and only then record the entry
 // state for the backward (the tf32 copy: every later use of it is a tf32 operand or a sum of
 // its products), so the global stores stay off the serial path.
-__device__ __forceinline__ void chain_state_pass(const ChainParams& p, int c, int h, int v, int k0,
-                                                 uint32_t tl, uint64_t* sready, float g0) {
+__device__ __forceinline__ void chain_state_pass(const ChainParams& p, float* h_save, int c, int h, int v,
+                                                 int k0, uint32_t tl, uint64_t* sready, float g0) {
   const size_t tile = size_t(c) * p.H + h;
   float s[64];
   tmem_ld64(tl + kTSM + k0, s);
@@ -91,11 +96,11 @@ __device__ __forceinline__ void chain_state_pass(const ChainParams& p, int c, in
   tmem_wait_st();
   tc_fence_before();
   mbar_arrive(sready);
-  if (p.h_save) {
+  if (h_save) {
     // re-read the tf32 copy (the MMAs only read it) and store it
     tmem_ld64(tl + kTST + k0, s);
     tmem_wait_ld_regs(s);
-    float* hs = p.h_save + tile * kD * kD + size_t(k0) * kD + v;
+    float* hs = h_save + tile * kD * kD + size_t(k0) * kD + v;
 #pragma unroll
     for (int e = 0; e < 64; ++e) hs[size_t(e) * kD] = s[e];
   }
@@ -114,9 +119,19 @@ __global__ void __launch_bounds__(kThreads, 1)
   __shared__ int abort_flag;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int n = blockIdx.x, h = blockIdx.y, H = p.H;
+  const int h = blockIdx.y, H = p.H;
+  // which segment of which sequence, and how
+  const SegPlan& sp = p.sp;
+  const int runs = runs_per_seq(sp.maxS, sp.pass);
+  const int n = blockIdx.x / runs, slot = blockIdx.x % runs;
   const SeqEntry seq = p.seqs[n];
-  const int first = seq.x, nc = seq.y;
+  const int ns = (seq.y + sp.L - 1) / sp.L;
+  int seg = 0, mode = kRunFull;
+  if (!decode_run(slot, sp.pass, ns, &seg, &mode)) return;
+  const int first = seq.x + seg * sp.L, nc = min(sp.L, seq.y - seg * sp.L);
+  const bool outs = mode == kRunFull;     // output, saves and the output products
+  const bool use_u = mode != kRunMapM;    // U enters v_new
+  const size_t slot_base = size_t(n) * sp.maxS;
 
   if (warp == 0) tmem_alloc(&tslot, 512);
   if (tid == 0) {
@@ -144,10 +159,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t sW = smem_u32(sm + kOffW), sQt = smem_u32(sm + kOffQt);
       auto load_g1 = [&](int c) {
         const int y = (c * H + h) * kC;
-        mbar_expect_tx(&full1, 65536u);
+        mbar_expect_tx(&full1, outs ? 65536u : 32768u);
         for (int pp = 0; pp < 4; ++pp) {
           tma_load_2d(sm + kOffW + pp * 8192, &mW, pp * 32, y, &full1);
-          tma_load_2d(sm + kOffQt + pp * 8192, &mQt, pp * 32, y, &full1);
+          if (outs) tma_load_2d(sm + kOffQt + pp * 8192, &mQt, pp * 32, y, &full1);
         }
       };
       auto load_g2 = [&](int c) {
@@ -157,14 +172,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       };
       auto load_g3 = [&](int c, int st) {
         uint8_t* base = sm + kOffG3 + st * kG3Stage;
-        mbar_expect_tx(&full3[st], 49152u);
+        mbar_expect_tx(&full3[st], outs ? 49152u : 32768u);
         for (int pp = 0; pp < 2; ++pp) {
           tma_load_2d(base + pp * 16384, &mKtT, pp * 32, (c * H + h) * kD, &full3[st]);
-          tma_load_2d(base + 32768 + pp * 8192, &mAqk, pp * 32, (c * H + h) * kC, &full3[st]);
+          if (outs) tma_load_2d(base + 32768 + pp * 8192, &mAqk, pp * 32, (c * H + h) * kC, &full3[st]);
         }
       };
       load_g1(first);
-      load_g2(first);
+      if (use_u) load_g2(first);
       load_g3(first, 0);
       if (nc > 1) load_g3(first + 1, 1);
       const uint32_t id64 = idesc_tf32(128, 64), id128 = idesc_tf32(128, 128);
@@ -180,20 +195,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         for (int s = 0; s < 16; ++s) mma_tf32_ts(tb + kTP, tb + kTST + s * 8, desc_kmajor(sW, 8192, s), id64, s > 0);
         mma_commit(&mma1);
-        for (int s = 0; s < 16; ++s) mma_tf32_ts(tO, tb + kTST + s * 8, desc_kmajor(sQt, 8192, s), id64, s > 0);
+        if (outs)
+          for (int s = 0; s < 16; ++s) mma_tf32_ts(tO, tb + kTST + s * 8, desc_kmajor(sQt, 8192, s), id64, s > 0);
         mma_commit(&mma1b);
         if (!mbar_wait(&mma1b, par, &abort_flag, p.status, kDevTimeoutMma)) break;
         TRACE(j, 2);
         if (j + 1 < nc) load_g1(c + 1);
         if (!mbar_wait(&vready, par, &abort_flag, p.status, kDevTimeoutSync)) break;
         TRACE(j, 3);
-        if (j + 1 < nc) load_g2(c + 1);
+        if (j + 1 < nc && use_u) load_g2(c + 1);
         if (!mbar_wait(&full3[st], (j >> 1) & 1, &abort_flag, p.status, kDevTimeoutTma)) break;
         TRACE(j, 4);
         tc_fence_after();
         for (int s = 0; s < 8; ++s) mma_tf32_ts(tb + kTSM, tb + kTVN + s * 8, desc_kmajor(sKtT, 16384, s), id128, true);
         mma_commit(&mma2);
-        for (int s = 0; s < 8; ++s) mma_tf32_ts(tO, tb + kTVN + s * 8, desc_kmajor(sAqk, 8192, s), id64, true);
+        if (outs)
+          for (int s = 0; s < 8; ++s) mma_tf32_ts(tO, tb + kTVN + s * 8, desc_kmajor(sAqk, 8192, s), id64, true);
         mma_commit(&mma3);
         if (!mbar_wait(&mma3, par, &abort_flag, p.status, kDevTimeoutMma)) break;
         TRACE(j, 5);
@@ -207,16 +224,25 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float* sU = reinterpret_cast<const float*>(sm + kOffU);
     const int k0 = 64 * half;  // state columns handled by this thread
     const int t0 = 32 * half;  // token columns handled by this thread
+    float* h_save = outs ? p.h_save : nullptr;
+    float* vnew_save = outs ? p.vnew_save : nullptr;
+    __nv_bfloat16* o = outs ? p.o : nullptr;
     {
+      // entry state: the initial state, a composed segment entry, the identity (map M) or zero
+      const float* src = nullptr;
+      if (mode == kRunFull)
+        src = seg == 0 ? (p.h0 ? p.h0 + (size_t(n) * H + h) * kD * kD : nullptr) : sp.E + ((slot_base + seg) * H + h) * kD * kD;
       float buf[64];
-      const float* src = p.h0 ? p.h0 + (size_t(n) * H + h) * kD * kD + size_t(k0) * kD + v : nullptr;
+      if (src) src += size_t(k0) * kD + v;
 #pragma unroll
-      for (int e = 0; e < 64; ++e) buf[e] = src ? src[size_t(e) * kD] : 0.f;
+      for (int e = 0; e < 64; ++e)
+        buf[e] = src ? src[size_t(e) * kD] : (mode == kRunMapM && k0 + e == v ? 1.f : 0.f);
       tmem_st32(tb + lb + kTSM + k0, buf);
       tmem_st32(tb + lb + kTSM + k0 + 32, buf + 32);
       tmem_wait_st();
     }
-    chain_state_pass(p, first, h, v, k0, tb + lb, &sready, p.kda ? 0.f : p.gam[(size_t(first) * H + h) * kD]);
+    chain_state_pass(p, h_save, first, h, v, k0, tb + lb, &sready,
+                     p.kda ? 0.f : p.gam[(size_t(first) * H + h) * kD]);
     bool alive = true;
     for (int j = 0; j < nc; ++j) {
       const uint32_t par = j & 1;
@@ -225,10 +251,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       const size_t tile = size_t(c) * H + h;
       // next chunk's scalar gate, loaded early so the state pass does not wait for it
       const float gnext = (j + 1 < nc && !p.kda) ? p.gam[(size_t(c + 1) * H + h) * kD] : 0.f;
-      if (!mbar_wait(&full2, par, &abort_flag, p.status, kDevTimeoutTma)) { alive = false; break; }
       float u[32];
+      if (use_u) {
+        if (!mbar_wait(&full2, par, &abort_flag, p.status, kDevTimeoutTma)) { alive = false; break; }
 #pragma unroll
-      for (int t = 0; t < 32; ++t) u[t] = sU[(v >> 5) * 2048 + (t0 + t) * 32 + (v & 31)];
+        for (int t = 0; t < 32; ++t) u[t] = sU[(v >> 5) * 2048 + (t0 + t) * 32 + (v & 31)];
+      } else {
+#pragma unroll
+        for (int t = 0; t < 32; ++t) u[t] = 0.f;
+      }
       if (!mbar_wait(&mma1, par, &abort_flag, p.status, kDevTimeoutMma)) { alive = false; break; }
       tc_fence_after();
       {
@@ -241,37 +272,56 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_wait_st();
         tc_fence_before();
         mbar_arrive(&vready);
-        if (p.vnew_save) {
-          float* vsave = p.vnew_save + tile * kTileW + size_t(t0) * kD + v;
+        if (vnew_save) {
+          float* vsave = vnew_save + tile * kTileW + size_t(t0) * kD + v;
 #pragma unroll
           for (int t = 0; t < 32; ++t) vsave[size_t(t) * kD] = r[t];
         }
       }
       if (!mbar_wait(&mma2, par, &abort_flag, p.status, kDevTimeoutMma)) { alive = false; break; }
       tc_fence_after();
-      if (j + 1 < nc) chain_state_pass(p, c + 1, h, v, k0, tb + lb, &sready, gnext);
-      if (!mbar_wait(&mma3, par, &abort_flag, p.status, kDevTimeoutMma)) { alive = false; break; }
-      tc_fence_after();
-      {
+      if (j + 1 < nc) chain_state_pass(p, h_save, c + 1, h, v, k0, tb + lb, &sready, gnext);
+      if (o) {
+        if (!mbar_wait(&mma3, par, &abort_flag, p.status, kDevTimeoutMma)) { alive = false; break; }
+        tc_fence_after();
         const uint32_t tO = tb + kTO + (j & 1) * 64;
         float r[32];
         tmem_ld32(tO + lb + t0, r);
         tmem_wait_ld_regs(r);
-        if (p.o) {
-          __nv_bfloat16* op = p.o + (size_t(ch.x + t0) * H + h) * kD + v;
+        __nv_bfloat16* op = o + (size_t(ch.x + t0) * H + h) * kD + v;
 #pragma unroll
-          for (int t = 0; t < 32; ++t)
-            if (t0 + t < ch.y) op[size_t(t) * H * kD] = __float2bfloat16_rn(r[t]);
-        }
+        for (int t = 0; t < 32; ++t)
+          if (t0 + t < ch.y) op[size_t(t) * H * kD] = __float2bfloat16_rn(r[t]);
       }
     }
-    if (alive && p.hT) {
+    // exit state: the final state, the next segment's entry (pass 0), or the segment's map
+    float* dst = nullptr;
+    float* dst_lo = nullptr;
+    if (mode == kRunFull) {
+      if (seg == ns - 1) dst = p.hT ? p.hT + (size_t(n) * H + h) * kD * kD : nullptr;
+      else if (sp.pass == 0) dst = sp.E + ((slot_base + seg + 1) * H + h) * kD * kD;
+    } else if (mode == kRunMapM) {
+      dst = sp.Phi + ((slot_base + seg) * H + h) * kD * kD;
+      dst_lo = sp.Plo + ((slot_base + seg) * H + h) * kD * kD;
+    } else {
+      dst = sp.Bm + ((slot_base + seg) * H + h) * kD * kD;
+    }
+    if (alive && dst) {  // the loop's last mma2 wait covers the final state update
       float s[64];
       tmem_ld64(tb + lb + kTSM + k0, s);
       tmem_wait_ld_regs(s);
-      float* dst = p.hT + (size_t(n) * H + h) * kD * kD + size_t(k0) * kD + v;
+      const size_t off = size_t(k0) * kD + v;
+      if (dst_lo) {
 #pragma unroll
-      for (int e = 0; e < 64; ++e) dst[size_t(e) * kD] = s[e];
+        for (int e = 0; e < 64; ++e) {
+          const float hi = to_tf32(s[e]);
+          dst[off + size_t(e) * kD] = hi;
+          dst_lo[off + size_t(e) * kD] = to_tf32(s[e] - hi);
+        }
+      } else {
+#pragma unroll
+        for (int e = 0; e < 64; ++e) dst[off + size_t(e) * kD] = s[e];
+      }
     }
   }
   tc_fence_before();
@@ -294,7 +344,7 @@ cudaError_t launch_chain_fwd(const CUtensorMap& mW, const CUtensorMap& mQt, cons
     if (e != cudaSuccess) return e;
     attr = true;
   }
-  dim3 grid(p.N, p.H);
+  dim3 grid(p.N * runs_per_seq(p.sp.maxS, p.sp.pass), p.H);
   k_chain_fwd<<<grid, kThreads, kSmemBytes, s>>>(mW, mQt, mKtT, mAqk, mU, p);
   return cudaGetLastError();
 }

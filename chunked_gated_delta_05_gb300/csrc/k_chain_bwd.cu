@@ -16,6 +16,10 @@
 // double-buffered) are TMA-loaded SW128 B operands; every product is a 128-lane tf32 MMA.
 // The products that do not depend on dS (Aqk^T dO, Qt^T dO) are issued alongside the chain
 // ones. Eight chain warps, one producer warp; all waits bounded.
+//
+// As in the forward chain, a CTA runs one segment (segments counted from the sequence's end)
+// in full, or as the segment's adjoint map: from the identity with dO = 0 (M^T, the products
+// of dO and their tiles left out) or from zero (the offset), with no saves.
 #include "common.cuh"
 #include "umma.cuh"
 
@@ -67,8 +71,9 @@ __device__ __forceinline__ void load_dO(const RevChainParams& p, int c, int h, i
 // the tf32 copy of dS' (the gradient w.r.t. the state leaving chunk c) and dO^T (prefetched
 // into `d`) as A operands, pre-apply the chunk decay to the master copy, release the MMA
 // issuer, then save dS' (its tf32 copy) for the feature-major backward kernel.
-__device__ __forceinline__ void rev_pass(const RevChainParams& p, int c, int h, int v, int k0, int t0,
-                                         uint32_t tl, uint64_t* ready, const uint32_t* d, float g0) {
+__device__ __forceinline__ void rev_pass(const RevChainParams& p, float* dh_save, bool use_do, int c, int h,
+                                         int v, int k0, int t0, uint32_t tl, uint64_t* ready, const uint32_t* d,
+                                         float g0) {
   const size_t tile = size_t(c) * p.H + h;
   float s[64];
   tmem_ld64(tl + kTDM + k0, s);
@@ -96,7 +101,7 @@ __device__ __forceinline__ void rev_pass(const RevChainParams& p, int c, int h, 
   }
   tmem_st32(tl + kTDM + k0, s);
   tmem_st32(tl + kTDM + k0 + 32, s + 32);
-  {
+  if (use_do) {
     float df[32];
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
@@ -108,10 +113,11 @@ __device__ __forceinline__ void rev_pass(const RevChainParams& p, int c, int h, 
   tmem_wait_st();
   tc_fence_before();
   mbar_arrive(ready);
+  if (!dh_save) return;
   // re-read the tf32 copy (the MMAs only read it) and save it
   tmem_ld64(tl + kTDT + k0, s);
   tmem_wait_ld_regs(s);
-  float* ds = p.dh_save + tile * kD * kD + size_t(k0) * kD + v;
+  float* ds = dh_save + tile * kD * kD + size_t(k0) * kD + v;
 #pragma unroll
   for (int e = 0; e < 64; ++e) ds[size_t(e) * kD] = s[e];
 }
@@ -129,10 +135,21 @@ __global__ void __launch_bounds__(kThreads, 1)
   __shared__ int abort_flag;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int n = blockIdx.x, h = blockIdx.y, H = p.H;
+  const int h = blockIdx.y, H = p.H;
+  // which segment of which sequence (processing order: from the end), and how
+  const SegPlan& sp = p.sp;
+  const int runs = runs_per_seq(sp.maxS, sp.pass);
+  const int n = blockIdx.x / runs, slot = blockIdx.x % runs;
   const SeqEntry seq = p.seqs[n];
-  const int first = seq.x, nc = seq.y;
-  const int last = first + nc - 1;
+  const int ns = (seq.y + sp.L - 1) / sp.L;
+  int seg = 0, mode = kRunFull;
+  if (!decode_run(slot, sp.pass, ns, &seg, &mode)) return;
+  const int lo = (ns - 1 - seg) * sp.L;          // first chunk of the segment within the sequence
+  const int nc = min(sp.L, seq.y - lo);
+  const int last = seq.x + lo + nc - 1;
+  const bool outs = mode == kRunFull;            // saves and dh0
+  const bool use_do = mode != kRunMapM;          // dO enters the recurrence
+  const size_t slot_base = size_t(n) * sp.maxS;
 
   if (warp == 0) tmem_alloc(&tslot, 512);
   if (tid == 0) {
@@ -155,11 +172,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       auto load = [&](int c, int st) {
         uint8_t* base = sm + st * kStage;
         const int y64 = (c * H + h) * kC, y128 = (c * H + h) * kD;
-        mbar_expect_tx(&full[st], kStage);
+        mbar_expect_tx(&full[st], use_do ? kStage : 65536u);
         for (int pp = 0; pp < 4; ++pp) tma_load_2d(base + kOffKt + pp * 8192, &mKt, pp * 32, y64, &full[st]);
         for (int pp = 0; pp < 2; ++pp) {
-          tma_load_2d(base + kOffAqkT + pp * 8192, &mAqkT, pp * 32, y64, &full[st]);
-          tma_load_2d(base + kOffQtT + pp * 16384, &mQtT, pp * 32, y128, &full[st]);
+          if (use_do) {
+            tma_load_2d(base + kOffAqkT + pp * 8192, &mAqkT, pp * 32, y64, &full[st]);
+            tma_load_2d(base + kOffQtT + pp * 16384, &mQtT, pp * 32, y128, &full[st]);
+          }
           tma_load_2d(base + kOffWT + pp * 16384, &mWT, pp * 32, y128, &full[st]);
         }
       };
@@ -177,12 +196,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         RTRACE(j, 2);
         tc_fence_after();
         // dv_new^T = dO^T Aqk + dS'^T Kt^T
-        for (int s = 0; s < 8; ++s) mma_tf32_ts(tb + kTDV, tb + kTDO + s * 8, desc_kmajor(base + kOffAqkT, 8192, s), id64, s > 0);
-        for (int s = 0; s < 16; ++s) mma_tf32_ts(tb + kTDV, tb + kTDT + s * 8, desc_kmajor(base + kOffKt, 8192, s), id64, true);
+        if (use_do)
+          for (int s = 0; s < 8; ++s) mma_tf32_ts(tb + kTDV, tb + kTDO + s * 8, desc_kmajor(base + kOffAqkT, 8192, s), id64, s > 0);
+        for (int s = 0; s < 16; ++s)
+          mma_tf32_ts(tb + kTDV, tb + kTDT + s * 8, desc_kmajor(base + kOffKt, 8192, s), id64, use_do || s > 0);
         mma_commit(&mma1);
         RTRACE(j, 6);
         // dS^T += dO^T Qt   (master copy already holds gam dS'^T)
-        for (int s = 0; s < 8; ++s) mma_tf32_ts(tb + kTDM, tb + kTDO + s * 8, desc_kmajor(base + kOffQtT, 16384, s), id128, true);
+        if (use_do)
+          for (int s = 0; s < 8; ++s) mma_tf32_ts(tb + kTDM, tb + kTDO + s * 8, desc_kmajor(base + kOffQtT, 16384, s), id128, true);
         if (!mbar_wait(&vready, par, &abort_flag, p.status, kDevTimeoutSync)) break;
         RTRACE(j, 3);
         tc_fence_after();
@@ -198,18 +220,27 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int v = tid & 127, half = tid >> 7;
     const uint32_t tl = tb + tmem_lane_base(warp);
     const int k0 = 64 * half, t0 = 32 * half;
+    float* dh_save = outs ? p.dh_save : nullptr;
+    float* dvn_save = outs ? p.dvn_save : nullptr;
     {
+      // seed: dht, a composed segment seed, the identity (map M) or zero
+      const float* src = nullptr;
+      if (mode == kRunFull)
+        src = seg == 0 ? (p.dht ? p.dht + (size_t(n) * H + h) * kD * kD : nullptr)
+                       : sp.E + ((slot_base + seg) * H + h) * kD * kD;
       float buf[64];
-      const float* src = p.dht ? p.dht + (size_t(n) * H + h) * kD * kD + size_t(k0) * kD + v : nullptr;
+      if (src) src += size_t(k0) * kD + v;
 #pragma unroll
-      for (int e = 0; e < 64; ++e) buf[e] = src ? src[size_t(e) * kD] : 0.f;
+      for (int e = 0; e < 64; ++e)
+        buf[e] = src ? src[size_t(e) * kD] : (mode == kRunMapM && k0 + e == v ? 1.f : 0.f);
       tmem_st32(tl + kTDM + k0, buf);
       tmem_st32(tl + kTDM + k0 + 32, buf + 32);
       tmem_wait_st();
     }
     uint32_t dnext[16];
-    load_dO(p, last, h, v, t0, dnext);
-    rev_pass(p, last, h, v, k0, t0, tl, &dready, dnext, p.kda ? 0.f : p.gam[(size_t(last) * H + h) * kD]);
+    if (use_do) load_dO(p, last, h, v, t0, dnext);
+    rev_pass(p, dh_save, use_do, last, h, v, k0, t0, tl, &dready, dnext,
+             p.kda ? 0.f : p.gam[(size_t(last) * H + h) * kD]);
     bool alive = true;
     for (int j = 0; j < nc; ++j) {
       const int c = last - j;
@@ -231,23 +262,46 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_before();
         if (tid == 0) RTRACE(j, 7);
         mbar_arrive(&vready);
-        float* dv = p.dvn_save + tile * kTileW + size_t(t0) * kD + v;
+        if (dvn_save) {
+          float* dv = dvn_save + tile * kTileW + size_t(t0) * kD + v;
 #pragma unroll
-        for (int t = 0; t < 32; ++t) dv[size_t(t) * kD] = -r[t];
+          for (int t = 0; t < 32; ++t) dv[size_t(t) * kD] = -r[t];
+        }
       }
       // prefetch the next chunk's dO while the second MMA group runs
-      if (j + 1 < nc) load_dO(p, c - 1, h, v, t0, dnext);
+      if (j + 1 < nc && use_do) load_dO(p, c - 1, h, v, t0, dnext);
       if (!mbar_wait(&mma2, par, &abort_flag, p.status, kDevTimeoutMma)) { alive = false; break; }
       tc_fence_after();
-      if (j + 1 < nc) rev_pass(p, c - 1, h, v, k0, t0, tl, &dready, dnext, gnext);
+      if (j + 1 < nc) rev_pass(p, dh_save, use_do, c - 1, h, v, k0, t0, tl, &dready, dnext, gnext);
     }
-    if (alive && p.dh0) {
+    // exit gradient: dh0, the next segment's seed (pass 0), or the segment's map
+    float* dst = nullptr;
+    float* dst_lo = nullptr;
+    if (mode == kRunFull) {
+      if (seg == ns - 1) dst = p.dh0 ? p.dh0 + (size_t(n) * H + h) * kD * kD : nullptr;
+      else if (sp.pass == 0) dst = sp.E + ((slot_base + seg + 1) * H + h) * kD * kD;
+    } else if (mode == kRunMapM) {
+      dst = sp.Phi + ((slot_base + seg) * H + h) * kD * kD;
+      dst_lo = sp.Plo + ((slot_base + seg) * H + h) * kD * kD;
+    } else {
+      dst = sp.Bm + ((slot_base + seg) * H + h) * kD * kD;
+    }
+    if (alive && dst) {  // the loop's last mma2 wait covers the final update
       float s[64];
       tmem_ld64(tl + kTDM + k0, s);
       tmem_wait_ld_regs(s);
-      float* dst = p.dh0 + (size_t(n) * H + h) * kD * kD + size_t(k0) * kD + v;
+      const size_t off = size_t(k0) * kD + v;
+      if (dst_lo) {
 #pragma unroll
-      for (int e = 0; e < 64; ++e) dst[size_t(e) * kD] = s[e];
+        for (int e = 0; e < 64; ++e) {
+          const float hi = to_tf32(s[e]);
+          dst[off + size_t(e) * kD] = hi;
+          dst_lo[off + size_t(e) * kD] = to_tf32(s[e] - hi);
+        }
+      } else {
+#pragma unroll
+        for (int e = 0; e < 64; ++e) dst[off + size_t(e) * kD] = s[e];
+      }
     }
   }
   tc_fence_before();
@@ -263,7 +317,7 @@ cudaError_t launch_chain_bwd(const CUtensorMap& mKt, const CUtensorMap& mAqkT, c
     if (e != cudaSuccess) return e;
     attr = true;
   }
-  dim3 grid(p.N, p.H);
+  dim3 grid(p.N * runs_per_seq(p.sp.maxS, p.sp.pass), p.H);
   k_chain_bwd<<<grid, kThreads, kSmemBytes, s>>>(mKt, mAqkT, mQtT, mWT, p);
   return cudaGetLastError();
 }

@@ -153,6 +153,21 @@ def _bwd(per_channel, q, k, v, g, beta, dO, dht, initial_state, use_qk_l2norm, u
     return dq, dk, dv, dbeta, dg, dh0
 
 
+def set_chain_segment(chunks: int) -> None:
+    """Force the segment length (in chunks) of the segmented state chain for every later call
+    of the process; 0 restores the automatic choice. Workspace and saved sizes depend on it."""
+    _lib.check(_lib.load().gdn_set_chain_segment(int(chunks)))
+
+
+def chain_plan(B: int, T: int, H: int, cu_seqlens: Optional[Sequence[int]] = None):
+    """``(chunks per segment, most segments of any sequence)`` the library picks for a shape."""
+    offsets = _offsets(cu_seqlens, T)
+    desc = _desc(B, T, H, None, True, False, False, offsets)
+    L, S = ctypes.c_int(), ctypes.c_int()
+    _lib.check(_lib.load().gdn_chain_plan(ctypes.byref(desc), ctypes.byref(L), ctypes.byref(S)))
+    return L.value, S.value
+
+
 def gdn_fwd(q, k, v, g, beta, *, initial_state=None, output_final_state=False, use_qk_l2norm=True,
             use_beta_sigmoid=False, cu_seqlens: Optional[Sequence[int]] = None, scale=None, status=None,
             save=False):

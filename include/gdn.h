@@ -157,6 +157,22 @@ int kda_bwd(const gdn_desc_t* desc, const gdn_bwd_args_t* args, void* stream);
 int gdn_fwd_noalloc(const gdn_desc_t* desc, const gdn_fwd_args_t* args, void* stream);
 size_t gdn_fwd_noalloc_capacity(void);
 
+/* Segmented state chain (no counterpart in the paper's kernels; it runs the pages' affine
+ * state summary, state_out = M state_in + S and its adjoint, inside one GPU instead of across
+ * context-parallel ranks: hyper-parallel GDN Diff Coverage page,
+ * `_compute_gdn_state_summary_from_prepared` / `_apply_gdn_state_summary`). The serial
+ * inter-chunk recurrence of each (sequence, head) is cut into segments of L chunks; the
+ * segments' affine maps are computed in parallel, composed, and the segments rerun from their
+ * entry states. The result equals the plain chain up to rounding. L is chosen per call from
+ * the problem's shape (gdn_chain_plan() reports the choice: L and the largest number of
+ * segments of any sequence; 1 segment = the plain chain). gdn_set_chain_segment(L) forces L
+ * for every later call and size query of the process (0 restores the automatic choice; a
+ * value at least the longest sequence's chunk count selects the plain chain); the workspace
+ * and saved sizes depend on it, so it must not change between a size query and the calls
+ * that use the buffers. Process-global, not thread-safe. Negative L: GDN_EINVAL. */
+int gdn_set_chain_segment(int chunks);
+int gdn_chain_plan(const gdn_desc_t* desc, int* chunks_per_segment, int* max_segments);
+
 /* Profiling hooks (not part of the computation). While enabled, every kernel launch of the
  * calls above is bracketed by CUDA events on its stream. gdn_timing_read() synchronizes the
  * recorded events of one kernel kind (0 .. gdn_timing_kinds()-1, named by gdn_timing_name()),

@@ -116,3 +116,49 @@ def test_python_wrapper_rejects_bad_offsets_without_gpu():
         ops._offsets([0, True, 5], 5)
     with pytest.raises(ValueError):
         ops._offsets(torch.tensor([0.0, 5.0]), 5)
+
+
+def plan(d):
+    L, S = ctypes.c_int(), ctypes.c_int()
+    rc = _lib.load().gdn_chain_plan(ctypes.byref(d), ctypes.byref(L), ctypes.byref(S))
+    assert rc == _lib.GDN_OK
+    return L.value, S.value
+
+
+@pytest.fixture
+def auto_plan():
+    lib = _lib.load()
+    yield lib
+    assert lib.gdn_set_chain_segment(0) == _lib.GDN_OK
+
+
+def test_chain_plan_covers_every_chunk(auto_plan):
+    # few long chains: the segmented chain is chosen; many short ones: the plain chain
+    for B, T, H in [(2, 4096, 16), (1, 8192, 16), (1, 32768, 16), (1, 8192, 32), (1, 256, 2), (64, 512, 16)]:
+        nc = (T + 63) // 64
+        L, S = plan(desc(B=B, T=T, H=H, num_seqs=B))
+        assert 1 <= L <= nc and S == (nc + L - 1) // L, (B, T, H, L, S)
+    assert plan(desc(B=1, T=8192, H=16))[1] > 1
+    assert plan(desc(B=64, T=512, H=16, num_seqs=64))[1] == 1
+
+
+def test_chain_plan_packed_documents(auto_plan):
+    vals = [0, 100, 3000, 3100, 9000]
+    arr, ptr = offsets(vals)
+    L, S = plan(desc(B=1, T=9000, H=4, cu_seqlens=ptr, num_seqs=4))
+    longest = (5900 + 63) // 64
+    assert S == (longest + L - 1) // L
+
+
+def test_chain_segment_override(auto_plan):
+    lib = auto_plan
+    d = desc(B=1, T=64 * 10 + 5, H=2)
+    assert lib.gdn_set_chain_segment(3) == _lib.GDN_OK
+    assert plan(d) == (3, 4)
+    scan_ws = ws_size(d)
+    assert lib.gdn_set_chain_segment(1 << 20) == _lib.GDN_OK
+    assert plan(d) == (11, 1)
+    plain_ws = ws_size(d)
+    # four 128x128 fp32 state buffers per (segment, head) for the scan
+    assert scan_ws - plain_ws >= 4 * 4 * 2 * 128 * 128 * 4
+    assert lib.gdn_set_chain_segment(-1) == _lib.GDN_EINVAL
