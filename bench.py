@@ -36,16 +36,15 @@ KERNEL_FLOP_PER_CHUNK_HEAD = {
     "bwd_feat": (3 * 2 * 64 * 128 * 128 + 2 * 2 * 64 * 64 * 128, "tf32"),
     "bwd_tok": (2 * 64 * 64 * 128 * 3 + 2 * 64 * 64 * 256 + 2 * 2 * 64 * 64 * 64 + 4 * 2 * 64 * 64 * 128, "tf32"),
     "tables": (0, "none"),
+    "compose": (0, "none"),     # segmented-chain overhead: no algorithmic work of its own
 }
 TF32_OVER_BF16 = 1.1 / 2.25    # nominal dense tf32 / bf16 tensor rates of a GB300
-# DRAM bytes (read + write) of one launch, from an `ncu --set full` capture of the same kernel
-# build on the same workload (profiles/kernels_gdn_b2_t4096_h16.md); None elsewhere.
+# DRAM bytes (read + write) of one step's launches of a kernel, from an `ncu --set full`
+# capture of the same kernel build on the same workload (profiles/kernels_gdn_b2_t4096_h16.md);
+# None elsewhere, and None for a kernel changed since its capture.
 NCU_TRAFFIC_BYTES = {
-    ("bwd_tok", "gdn_b2_t4096_h16"): (640.279552 + 89.481472) * 1e6,
-    ("chain_bwd", "gdn_b2_t4096_h16"): (268.789760 + 163.746560) * 1e6,
     ("bwd_feat", "gdn_b2_t4096_h16"): (470.668288 + 294.395648) * 1e6,
     ("prepare", "gdn_b2_t4096_h16"): (104.316672 + 515.707648) * 1e6,
-    ("chain_fwd", "gdn_b2_t4096_h16"): (304.646656 + 196.257024) * 1e6,
 }
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
@@ -273,16 +272,19 @@ def main():
     name, (tot_ms, launches) = max(per_kernel.items(), key=lambda kv: kv[1][0])
     flop_chunk, kind = KERNEL_FLOP_PER_CHUNK_HEAD[name]
     avg_ms = tot_ms / max(launches, 1)
-    achieved = flop_chunk * n_chunk_heads / (avg_ms * 1e-3) / 1e12
+    # the kernel's device time per step (the chains launch twice per step when segmented)
+    step_ms = tot_ms / args.steps
+    achieved = flop_chunk * n_chunk_heads / (step_ms * 1e-3) / 1e12
     peak = bf16_sus * (TF32_OVER_BF16 if kind == "tf32" else 1.0)
     kernel_share = {k: round(v[0] / max(1e-9, sum(x[0] for x in per_kernel.values())), 4) for k, v in per_kernel.items()}
     traffic = NCU_TRAFFIC_BYTES.get((name, w.name))
     roofline = {"bound": "tensor", "kernel": name, "operands": kind, "achieved": achieved, "peak": peak,
                 "unit": "TFLOP/s", "frac": achieved / peak, "traffic": traffic,
-                "traffic_gbs": None if traffic is None else traffic / (avg_ms * 1e-3) / 1e9,
-                "traffic_frac_of_hbm": None if traffic is None else traffic / (avg_ms * 1e-3) / 1e9 / peaks["hbm_gbs"],
+                "traffic_gbs": None if traffic is None else traffic / (step_ms * 1e-3) / 1e9,
+                "traffic_frac_of_hbm": None if traffic is None else traffic / (step_ms * 1e-3) / 1e9 / peaks["hbm_gbs"],
                 "peak_source": f"{peak_src} bf16 sustained" + (" x nominal tf32/bf16 ratio" if kind == "tf32" else ""),
-                "avg_launch_ms": avg_ms, "kernel_time_share": kernel_share}
+                "avg_launch_ms": avg_ms, "launches_per_step": launches / args.steps, "kernel_ms_per_step": step_ms,
+                "kernel_time_share": kernel_share}
     gpu_launches = sum(v[1] for v in per_kernel.values())
 
     # end-to-end through the public API with host buffers (pinned), copies inside the region

@@ -302,7 +302,7 @@ struct TimedLaunch {
 
 struct Maps {
   CUtensorMap q, k, v, W, Qt, KtT, Aqk, U;           // forward
-  CUtensorMap Kt, AqkT, QtT, WT, VN, DVN, DW;         // backward
+  CUtensorMap Kt, AqkT, QtT, WT, VN, DVN, DW, dO;     // backward
 };
 
 // Row-major fp32 workspace tiles as TMA sources: `cols` per row, boxes of 32 columns.
@@ -508,8 +508,8 @@ int run_bwd(const gdn_desc_t* d, const gdn_bwd_args_t* a, void* stream, bool kda
   if (!a) return fail(GDN_EINVAL, "args is NULL");
   if (!a->q || !a->k || !a->v || !a->g || !a->beta || !a->dO || !a->dq || !a->dk || !a->dv || !a->dbeta || !a->dg)
     return fail(GDN_EINVAL, "q, k, v, g, beta, dO and every gradient output except dh0 must be non-NULL");
-  if (!aligned16(a->q) || !aligned16(a->k) || !aligned16(a->v))
-    return fail(GDN_EINVAL, "q, k and v must be 16-byte aligned");
+  if (!aligned16(a->q) || !aligned16(a->k) || !aligned16(a->v) || !aligned16(a->dO))
+    return fail(GDN_EINVAL, "q, k, v and dO must be 16-byte aligned");
   const size_t nqk = size_t(P.R) * P.H * kD * 2;
   const void* ins[] = {a->q, a->k, a->v, a->dO};
   const void* outs[] = {a->dq, a->dk, a->dv};
@@ -532,7 +532,9 @@ int run_bwd(const gdn_desc_t* d, const gdn_bwd_args_t* a, void* stream, bool kda
   char* sv = have_saved ? const_cast<char*>(static_cast<const char*>(a->saved)) : static_cast<char*>(a->workspace);
   char* rs = have_saved ? static_cast<char*>(a->workspace) : static_cast<char*>(a->workspace) + L.saved_total;
   Maps M;
-  if (!fwd_maps(P, a->q, a->k, a->v, sv, L, &M) || !bwd_maps(P, sv, rs, L, &M))
+  const uint64_t HD = uint64_t(P.H) * kD;
+  if (!fwd_maps(P, a->q, a->k, a->v, sv, L, &M) || !bwd_maps(P, sv, rs, L, &M) ||
+      !make_map(&M.dO, a->dO, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, HD, P.R, HD * 2, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B))
     return fail(GDN_ECUDA, "cuTensorMapEncodeTiled failed");
   auto F = [&](size_t off) { return reinterpret_cast<float*>(sv + off); };
   auto R = [&](size_t off) { return reinterpret_cast<float*>(rs + off); };
@@ -626,7 +628,7 @@ int run_bwd(const gdn_desc_t* d, const gdn_bwd_args_t* a, void* stream, bool kda
   tp.kda = kda ? 1 : 0;
   TimedLaunch tl_(kKBwdTok, s);
   return check_cuda(kda ? launch_bwd_tok_kda(M.q, M.k, M.v, M.VN, M.DW, M.DVN, tp, s)
-                        : launch_bwd_tok(M.q, M.k, M.v, M.VN, M.DW, M.DVN, tp, s),
+                        : launch_bwd_tok(M.q, M.k, M.v, M.dO, M.VN, M.DW, M.DVN, tp, s),
                     "token-major backward kernel");
 }
 

@@ -175,8 +175,9 @@ cudaError_t launch_prep_kda(const CUtensorMap& mq, const CUtensorMap& mk, const 
 cudaError_t launch_chain_bwd(const CUtensorMap& mKt, const CUtensorMap& mAqkT, const CUtensorMap& mQtT,
                              const CUtensorMap& mWT, const RevChainParams& p, cudaStream_t s);
 cudaError_t launch_bwd_feat(const CUtensorMap& mVN, const CUtensorMap& mDVN, const BwdFeatParams& p, cudaStream_t s);
-cudaError_t launch_bwd_tok(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, const CUtensorMap& mVN,
-                           const CUtensorMap& mDW, const CUtensorMap& mDVN, const BwdTokParams& p, cudaStream_t s);
+cudaError_t launch_bwd_tok(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, const CUtensorMap& mdO,
+                           const CUtensorMap& mVN, const CUtensorMap& mDW, const CUtensorMap& mDVN, const BwdTokParams& p,
+                           cudaStream_t s);
 cudaError_t launch_bwd_tok_kda(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
                                const CUtensorMap& mVN, const CUtensorMap& mDW, const CUtensorMap& mDVN,
                                const BwdTokParams& p, cudaStream_t s);

@@ -30,9 +30,12 @@
 namespace gdn {
 
 #ifdef GDN_TRACE
-__device__ unsigned long long g_trace_tok[16];
-#define TTRACE(slot) \
-  do { if (blockIdx.x == 5 && blockIdx.y == 0 && threadIdx.x == 0) g_trace_tok[slot] = globaltimer(); } while (0)
+__device__ unsigned long long g_trace_tok[4 * 16];
+#define TTRACE(slot)                                                                                    \
+  do {                                                                                                  \
+    if (blockIdx.y == 3 && threadIdx.x == 0 && blockIdx.x % 32 == 5 && blockIdx.x < 128)                \
+      g_trace_tok[(blockIdx.x / 32) * 16 + (slot)] = globaltimer();                                      \
+  } while (0)
 extern "C" int gdn_trace_tok_read(unsigned long long* host) {
   return cudaMemcpyFromSymbol(host, g_trace_tok, sizeof(g_trace_tok)) == cudaSuccess ? 0 : -1;
 }
@@ -45,7 +48,8 @@ namespace {
 constexpr int kThreads = 256;   // 8 warps; two threads per TMEM lane (halves of the columns)
 constexpr uint32_t kOffQ = 0, kOffK = 16384, kOffV = 32768;   // bf16 [64][128], 2 panels of 8 KB
 constexpr uint32_t kR1 = 49152, kR2 = 81920, kR3 = 114688, kR4 = 147456;  // 32 KB regions
-constexpr uint32_t kSmemBytes = 180224 + 1024;
+constexpr uint32_t kOffDO = 180224;                            // dO bf16 [64][128] (TMA)
+constexpr uint32_t kSmemBytes = 196608 + 1024;
 // TMEM columns (64-row results)
 constexpr uint32_t kTAqk = 0, kTKK = 64, kTQK = 128, kTdA = 192, kTX = 192, kTdL = 192;
 constexpr uint32_t kTRq = 0, kTRk = 128;  // reuse after the first products are consumed
@@ -65,9 +69,9 @@ __device__ __forceinline__ void put32(uint8_t* tile, int rows, int row, int col,
 
 __global__ void __launch_bounds__(kThreads, 1)
     k_bwd_tok(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
-              const __grid_constant__ CUtensorMap mv, const __grid_constant__ CUtensorMap mVN,
-              const __grid_constant__ CUtensorMap mDW, const __grid_constant__ CUtensorMap mDVN,
-              const BwdTokParams p) {
+              const __grid_constant__ CUtensorMap mv, const __grid_constant__ CUtensorMap mdO,
+              const __grid_constant__ CUtensorMap mVN, const __grid_constant__ CUtensorMap mDW,
+              const __grid_constant__ CUtensorMap mDVN, const BwdTokParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = align1k(smem_raw);
   __shared__ uint64_t bar_tma, bar_mma;
@@ -112,34 +116,37 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tl = tb + tmem_lane_base(warp);
   const float Glast = s_G[len - 1];
   if (tid == 0) {
-    mbar_expect_tx(&bar_tma, 3u * 16384u + 3u * 32768u);
+    mbar_expect_tx(&bar_tma, 4u * 16384u + 3u * 32768u);
     for (int pp = 0; pp < 2; ++pp) {
       const int x = h * kD + 64 * pp;
       tma_load_2d(sQ + pp * 8192, &mq, x, ch.x, &bar_tma);
       tma_load_2d(sK + pp * 8192, &mk, x, ch.x, &bar_tma);
       tma_load_2d(sV + pp * 8192, &mv, x, ch.x, &bar_tma);
+      tma_load_2d(sm + kOffDO + pp * 8192, &mdO, x, ch.x, &bar_tma);
     }
     for (int pp = 0; pp < 4; ++pp) {
       tma_load_2d(sm + kR2 + pp * 8192, &mVN, pp * 32, int(tile) * kC, &bar_tma);
       tma_load_2d(sm + kR3 + pp * 8192, &mDW, pp * 32, int(tile) * kC, &bar_tma);
       tma_load_2d(sm + kR4 + pp * 8192, &mDVN, pp * 32, int(tile) * kC, &bar_tma);
     }
+    // inputs of the later phases: start their trip from HBM now
+    const size_t rows = tile * kTileW;
+    prefetch_l2(p.A + tile * kTileAqk, 4u * kTileAqk);
+    prefetch_l2(p.dQt + rows, 4u * kTileW);
+    prefetch_l2(p.dKt + rows, 4u * kTileW);
+    prefetch_l2(p.dK1 + rows, 4u * kTileW);
+    prefetch_l2(p.dV1 + rows, 4u * kTileW);
   }
-  // dO as a 64-row tf32 operand [i][v] (rows past the chunk are zero).
-  {
-    const int v = tid & 127, t0 = 32 * half;
-    const __nv_bfloat16* src = p.dO + (size_t(ch.x) * H + h) * kD + v;
-    float buf[32];
-#pragma unroll
-    for (int e = 0; e < 32; ++e) buf[e] = (t0 + e < len) ? __bfloat162float(src[size_t(t0 + e) * H * kD]) : 0.f;
-#pragma unroll
-    for (int e = 0; e < 32; ++e) put32(sm + kR1, kC, t0 + e, v, buf[e]);
-  }
-  fence_async_smem();
-  __syncthreads();
   TTRACE(1);
   const bool tma_ok = mbar_wait(&bar_tma, 0, &abort_flag, p.status, kDevTimeoutTma);
   TTRACE(2);
+  // dO as a 64-row tf32 operand [i][v] (rows past the chunk are zero).
+  {
+    const int v = tid & 127, t0 = 32 * half;
+#pragma unroll 8
+    for (int e = 0; e < 32; ++e)
+      put32(sm + kR1, kC, t0 + e, v, (t0 + e < len) ? bf16_at(sm + kOffDO, t0 + e, v) : 0.f);
+  }
   // Rows of q, k, v past the chunk belong to the next document (or are zero): clear them so
   // the exact Gram products below see zeros there.
   if (tid >= len && tid < kC) {
@@ -296,6 +303,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_wait_ld_regs(nn);
       tmem_wait_ld_regs(kk);
       tmem_wait_ld_regs(qk);
+      TTRACE(11);
       if (owner) {
 #pragma unroll
         for (int jj = 0; jj < 32; ++jj) {
@@ -322,6 +330,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       atomicAdd(&s_dG[i], rowP);
       atomicAdd(&s_db[i], dbi);
     }
+    TTRACE(12);
   }
   // transposed raw tiles k^T [d][j], q^T [d][i] (zero past the chunk: cleared above)
   {
@@ -331,6 +340,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       put32(sQT, kD, d, j, to_tf32(bf16_at(sQ, j, d)));
     }
   }
+  TTRACE(13);
   fence_async_smem();
   tc_fence_before();
   __syncthreads();
@@ -381,6 +391,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
   __syncthreads();
+  TTRACE(14);
   if (ok) {
     const size_t rowbase = tile * kTileW;
     const int d0 = 4 * lane;
@@ -402,72 +413,91 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int off = 16; off > 0; off >>= 1) x += __shfl_xor_sync(0xffffffffu, x, off);
       return x;
     };
-#pragma unroll 2
-    for (int t = warp; t < len; t += 8) {
-      const float Gt = s_G[t], rqt = s_rq[t], rkt = s_rk[t], bt = s_b[t];
-      const float eG = expf(Gt), eL = expf(Glast - Gt);
-      const size_t orow = (size_t(ch.x + t) * H + h) * kD + d0;
-      // dq
-      float qv[4], a[4], x[4];
-      bf4(sQ, t, qv);
-      const float4 dqt = *reinterpret_cast<const float4*>(p.dQt + rowbase + size_t(t) * kD + d0);
-      const float4 rq4 = *reinterpret_cast<const float4*>(sRq + t * kPad + d0);
-      const float dqtv[4] = {dqt.x, dqt.y, dqt.z, dqt.w}, rqv[4] = {rq4.x, rq4.y, rq4.z, rq4.w};
-      float dot = 0.f, qdq = 0.f;
+    // rows t = warp + 8 m; each batch of four rows loads its fp32 inputs first (read-only
+    // for this kernel), so their latencies overlap instead of queueing behind the stores
+#pragma unroll 1
+    for (int m0 = 0; m0 < 8; m0 += 4) {
+      float4 in[4][4];
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const float qh = rqt * qv[e];
-        a[e] = fmaf(scale * eG, dqtv[e], rqv[e]);
-        dot = fmaf(a[e], qh, dot);
-        qdq = fmaf(dqtv[e], qh, qdq);
+      for (int m = 0; m < 4; ++m) {
+        const int t = warp + 8 * (m0 + m);
+        const size_t ro = rowbase + size_t(t) * kD + d0;
+        if (t < len) {
+          in[m][0] = __ldg(reinterpret_cast<const float4*>(p.dQt + ro));
+          in[m][1] = __ldg(reinterpret_cast<const float4*>(p.dK1 + ro));
+          in[m][2] = __ldg(reinterpret_cast<const float4*>(p.dKt + ro));
+          in[m][3] = __ldg(reinterpret_cast<const float4*>(p.dV1 + ro));
+        }
       }
-      dot = allsum(dot);
-      qdq = allsum(qdq);
-      if (!p.l2norm) dot = 0.f;
 #pragma unroll
-      for (int e = 0; e < 4; ++e) x[e] = rqt * (a[e] - rqt * qv[e] * dot);
-      store4(p.dq + orow, x);
-      // dk
-      float kv[4];
-      bf4(sK, t, kv);
-      const float4 k1 = *reinterpret_cast<const float4*>(p.dK1 + rowbase + size_t(t) * kD + d0);
-      const float4 kt = *reinterpret_cast<const float4*>(p.dKt + rowbase + size_t(t) * kD + d0);
-      const float4 rk4 = *reinterpret_cast<const float4*>(sRk + t * kPad + d0);
-      const float k1v[4] = {k1.x, k1.y, k1.z, k1.w}, ktv[4] = {kt.x, kt.y, kt.z, kt.w};
-      const float rkv[4] = {rk4.x, rk4.y, rk4.z, rk4.w};
-      float kdot = 0.f, k1k = 0.f, ktk = 0.f;
+      for (int m = 0; m < 4; ++m) {
+        const int t = warp + 8 * (m0 + m);
+        if (t >= len) break;
+        const float Gt = s_G[t], rqt = s_rq[t], rkt = s_rk[t], bt = s_b[t];
+        const float eG = expf(Gt), eL = expf(Glast - Gt);
+        const size_t orow = (size_t(ch.x + t) * H + h) * kD + d0;
+        // dq
+        float qv[4], a[4], x[4];
+        bf4(sQ, t, qv);
+        const float4 dqt = in[m][0];
+        const float4 rq4 = *reinterpret_cast<const float4*>(sRq + t * kPad + d0);
+        const float dqtv[4] = {dqt.x, dqt.y, dqt.z, dqt.w}, rqv[4] = {rq4.x, rq4.y, rq4.z, rq4.w};
+        float dot = 0.f, qdq = 0.f;
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const float kh = rkt * kv[e];
-        a[e] = rkv[e] + bt * eG * k1v[e] + eL * ktv[e];
-        kdot = fmaf(a[e], kh, kdot);
-        k1k = fmaf(k1v[e], kh, k1k);
-        ktk = fmaf(ktv[e], kh, ktk);
-      }
-      kdot = allsum(kdot);
-      k1k = allsum(k1k);
-      ktk = allsum(ktk);
-      if (!p.l2norm) kdot = 0.f;
+        for (int e = 0; e < 4; ++e) {
+          const float qh = rqt * qv[e];
+          a[e] = fmaf(scale * eG, dqtv[e], rqv[e]);
+          dot = fmaf(a[e], qh, dot);
+          qdq = fmaf(dqtv[e], qh, qdq);
+        }
+        dot = allsum(dot);
+        qdq = allsum(qdq);
+        if (!p.l2norm) dot = 0.f;
 #pragma unroll
-      for (int e = 0; e < 4; ++e) x[e] = rkt * (a[e] - rkt * kv[e] * kdot);
-      store4(p.dk + orow, x);
-      // dv and the v part of dbeta
-      float vv4[4];
-      bf4(sV, t, vv4);
-      const float4 v1 = *reinterpret_cast<const float4*>(p.dV1 + rowbase + size_t(t) * kD + d0);
-      const float v1v[4] = {v1.x, v1.y, v1.z, v1.w};
-      float vv = 0.f;
+        for (int e = 0; e < 4; ++e) x[e] = rqt * (a[e] - rqt * qv[e] * dot);
+        store4(p.dq + orow, x);
+        // dk
+        float kv[4];
+        bf4(sK, t, kv);
+        const float4 k1 = in[m][1];
+        const float4 kt = in[m][2];
+        const float4 rk4 = *reinterpret_cast<const float4*>(sRk + t * kPad + d0);
+        const float k1v[4] = {k1.x, k1.y, k1.z, k1.w}, ktv[4] = {kt.x, kt.y, kt.z, kt.w};
+        const float rkv[4] = {rk4.x, rk4.y, rk4.z, rk4.w};
+        float kdot = 0.f, k1k = 0.f, ktk = 0.f;
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        vv = fmaf(v1v[e], vv4[e], vv);
-        x[e] = bt * v1v[e];
-      }
-      vv = allsum(vv);
-      store4(p.dv + orow, x);
-      if (lane == 0) {
-        s_dG[t] += scale * eG * qdq + bt * eG * k1k - eL * ktk;
-        s_db[t] += eG * k1k + vv;
-        s_P[t][0] = eL * ktk;   // this row's share of dG_last (column 0 of P is free now)
+        for (int e = 0; e < 4; ++e) {
+          const float kh = rkt * kv[e];
+          a[e] = rkv[e] + bt * eG * k1v[e] + eL * ktv[e];
+          kdot = fmaf(a[e], kh, kdot);
+          k1k = fmaf(k1v[e], kh, k1k);
+          ktk = fmaf(ktv[e], kh, ktk);
+        }
+        kdot = allsum(kdot);
+        k1k = allsum(k1k);
+        ktk = allsum(ktk);
+        if (!p.l2norm) kdot = 0.f;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) x[e] = rkt * (a[e] - rkt * kv[e] * kdot);
+        store4(p.dk + orow, x);
+        // dv and the v part of dbeta
+        float vv4[4];
+        bf4(sV, t, vv4);
+        const float4 v1 = in[m][3];
+        const float v1v[4] = {v1.x, v1.y, v1.z, v1.w};
+        float vv = 0.f;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          vv = fmaf(v1v[e], vv4[e], vv);
+          x[e] = bt * v1v[e];
+        }
+        vv = allsum(vv);
+        store4(p.dv + orow, x);
+        if (lane == 0) {
+          s_dG[t] += scale * eG * qdq + bt * eG * k1k - eL * ktk;
+          s_db[t] += eG * k1k + vv;
+          s_P[t][0] = eL * ktk;   // this row's share of dG_last (column 0 of P is free now)
+        }
       }
     }
   }
@@ -497,8 +527,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0) tmem_dealloc(tb, 256);
 }
 
-cudaError_t launch_bwd_tok(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, const CUtensorMap& mVN,
-                           const CUtensorMap& mDW, const CUtensorMap& mDVN, const BwdTokParams& p, cudaStream_t s) {
+cudaError_t launch_bwd_tok(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, const CUtensorMap& mdO,
+                           const CUtensorMap& mVN, const CUtensorMap& mDW, const CUtensorMap& mDVN, const BwdTokParams& p,
+                           cudaStream_t s) {
   static bool attr = false;
   if (!attr) {
     cudaError_t e = cudaFuncSetAttribute(k_bwd_tok, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
@@ -506,7 +537,7 @@ cudaError_t launch_bwd_tok(const CUtensorMap& mq, const CUtensorMap& mk, const C
     attr = true;
   }
   dim3 grid(p.NC, p.H);
-  k_bwd_tok<<<grid, kThreads, kSmemBytes, s>>>(mq, mk, mv, mVN, mDW, mDVN, p);
+  k_bwd_tok<<<grid, kThreads, kSmemBytes, s>>>(mq, mk, mv, mdO, mVN, mDW, mDVN, p);
   return cudaGetLastError();
 }
 

@@ -24,6 +24,20 @@
 
 namespace gdn {
 
+#ifdef GDN_TRACE
+__device__ unsigned long long g_trace_prep[4 * 16];
+#define PTRACE(slot)                                                                                    \
+  do {                                                                                                  \
+    if (blockIdx.y == 3 && threadIdx.x == 0 && blockIdx.x % 16 == 5 && blockIdx.x < 64)                 \
+      g_trace_prep[(blockIdx.x / 16) * 16 + (slot)] = globaltimer();                                     \
+  } while (0)
+extern "C" int gdn_trace_prep_read(unsigned long long* host) {
+  return cudaMemcpyFromSymbol(host, g_trace_prep, sizeof(g_trace_prep)) == cudaSuccess ? 0 : -1;
+}
+#else
+#define PTRACE(slot) do {} while (0)
+#endif
+
 namespace {
 
 constexpr int kThreads = 128;
@@ -108,6 +122,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int tid = threadIdx.x, warp = tid >> 5;
   const int h = blockIdx.y, pair = blockIdx.x, H = p.H;
+  PTRACE(0);
   const int blk = tid >> 6, il = tid & 63;
 
   if (tid < 2) {
@@ -166,6 +181,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   s_g[tid] = gi;
   s_b[tid] = bi;
   mbar_wait(&bar_tma, 0, &abort_flag, p.status, kDevTimeoutTma);
+  PTRACE(1);
 
   // L2-norm factors from the staged rows.
   float ssq = 0.f, ssk = 0.f;
@@ -191,6 +207,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const float Glast = len > 0 ? s_G[blk * kC + len - 1] : 0.f;
+  PTRACE(2);
 
   // Gram products: TMEM cols [0,128) = K K^T, [128,256) = Q K^T (pair-stacked).
   if (tid == 0 && !abort_flag) {
@@ -237,6 +254,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (p.beff) p.beff[tile * kC + il] = bi;
   }
 
+  PTRACE(3);
   const bool ok1 = mbar_wait(&bar_mma, 0, &abort_flag, p.status, kDevTimeoutMma);
   tc_fence_after();
   if (ok1) {
@@ -267,6 +285,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   tc_fence_before();
   __syncthreads();
+  PTRACE(4);
 
   // Column il of A = (I + L)^-1 for this thread's chunk (into sX, which reuses the q tile:
   // q is no longer needed once Qt and the Q K^T product are done); then the scaled
@@ -278,6 +297,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     float* a = p.A + tile * kTileAqk + il;
     for (int r = 0; r < kC; ++r) a[size_t(r) * kC] = sX[r * kC + il];
   }
+  PTRACE(5);
   {
     const float s1 = bi * expf(G) * rk, s2 = bi;
     const int col = tid;
@@ -298,6 +318,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  PTRACE(6);
 
   // W = A1 k (TMEM cols [0,128)), U = A2 v (cols [128,256)); k, v as MN-major B operands.
   // A1, A2 carry only the strictly lower part of A (bf16); the identity part, which dominates
@@ -313,6 +334,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   const bool ok2 = mbar_wait(&bar_mma, 1, &abort_flag, p.status, kDevTimeoutMma);
   tc_fence_after();
+  PTRACE(7);
   if (ok2 && len > 0) {
     const float dw_scale = bi * expf(G) * rk, du_scale = bi;
     for (int which = 0; which < 2; ++which) {
@@ -344,6 +366,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   }
+  PTRACE(8);
   tc_fence_before();
   __syncthreads();
   if (warp == 0) tmem_dealloc(tb, 256);

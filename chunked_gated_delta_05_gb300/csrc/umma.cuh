@@ -98,6 +98,13 @@ __device__ __forceinline__ void tma_store_2d(const CUtensorMap* m, int x, int y,
 __device__ __forceinline__ void tma_store_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void tma_store_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
+// Fetch `bytes` (a multiple of 16, 16-byte aligned source) into L2 ahead of use; no
+// completion to wait for.
+__device__ __forceinline__ void prefetch_l2(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(src)), "r"(bytes)
+               : "memory");
+}
+
 // Generic-proxy shared-memory writes -> visible to the async proxy (tensor core, TMA).
 __device__ __forceinline__ void fence_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
