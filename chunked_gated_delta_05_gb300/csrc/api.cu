@@ -262,6 +262,14 @@ bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
 
+// SM count of the current device (a prefetch distance for the chunk kernels).
+int sm_count() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return 148;
+  return n > 0 ? n : 148;
+}
+
 int check_cuda(cudaError_t e, const char* what) {
   if (e != cudaSuccess) return fail(GDN_ECUDA, std::string(what) + ": " + cudaGetErrorString(e));
   return GDN_OK;
@@ -301,7 +309,7 @@ struct TimedLaunch {
 };
 
 struct Maps {
-  CUtensorMap q, k, v, W, Qt, KtT, Aqk, U;           // forward
+  CUtensorMap q, k, v, W, Qt, KtT, Aqk, U, Usw;      // forward (Usw: U as a swizzled store target)
   CUtensorMap Kt, AqkT, QtT, WT, VN, DVN, DW, dO;     // backward
 };
 
@@ -311,6 +319,9 @@ bool tile_map(CUtensorMap* m, const char* base, uint64_t cols, uint64_t rows, ui
                   swz ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE);
 }
 
+// Whether the layout carries the backward-mode prepare tiles.
+bool backward_tiles(const Layout& L) { return L.Kt != 0; }
+
 bool fwd_maps(const Problem& P, const void* q, const void* k, const void* v, const char* ws, const Layout& L, Maps* M) {
   const uint64_t HD = uint64_t(P.H) * kD;
   const uint64_t r64 = uint64_t(P.NC) * P.H * kC, r128 = uint64_t(P.NC) * P.H * kD;
@@ -318,8 +329,9 @@ bool fwd_maps(const Problem& P, const void* q, const void* k, const void* v, con
          make_map(&M->k, k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, HD, P.R, HD * 2, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B) &&
          make_map(&M->v, v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, HD, P.R, HD * 2, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B) &&
          tile_map(&M->W, ws + L.W, kD, r64, 64, true) && tile_map(&M->Qt, ws + L.Qt, kD, r64, 64, true) &&
-         tile_map(&M->U, ws + L.U, kD, r64, 64, false) && tile_map(&M->KtT, ws + L.KtT, kC, r128, 128, true) &&
-         tile_map(&M->Aqk, ws + L.Aqk, kC, r64, 64, true);
+         tile_map(&M->U, ws + L.U, kD, r64, 64, false) && tile_map(&M->Usw, ws + L.U, kD, r64, 64, true) &&
+         tile_map(&M->KtT, ws + L.KtT, kC, r128, 128, true) && tile_map(&M->Aqk, ws + L.Aqk, kC, r64, 64, true) &&
+         (!backward_tiles(L) || tile_map(&M->Kt, ws + L.Kt, kD, r64, 64, true));
 }
 
 bool bwd_maps(const Problem& P, const char* sv, const char* rs, const Layout& L, Maps* M) {
@@ -477,7 +489,8 @@ int run_fwd(const gdn_desc_t* d, const gdn_fwd_args_t* a, void* stream, bool kda
   const PrepParams pp = prep_params(d, P, ws, L, a->g, a->beta, training, a->status);
   {
     TimedLaunch tl_(kKPrep, s);
-    rc = check_cuda(kda ? launch_prep_kda(M.q, M.k, M.v, pp, s) : launch_prep_gdn(M.q, M.k, M.v, pp, s),
+    rc = check_cuda(kda ? launch_prep_kda(M.q, M.k, M.v, pp, s)
+                        : launch_prep_gdn(M.q, M.k, M.v, M.Qt, training ? M.Kt : M.Qt, M.Aqk, M.W, M.Usw, pp, s),
                     "prepare kernel");
   }
   if (rc) return rc;
@@ -551,7 +564,8 @@ int run_bwd(const gdn_desc_t* d, const gdn_bwd_args_t* a, void* stream, bool kda
     const PrepParams pp = prep_params(d, P, sv, L, a->g, a->beta, true, a->status);
     {
       TimedLaunch tl_(kKPrep, s);
-      rc = check_cuda(kda ? launch_prep_kda(M.q, M.k, M.v, pp, s) : launch_prep_gdn(M.q, M.k, M.v, pp, s),
+      rc = check_cuda(kda ? launch_prep_kda(M.q, M.k, M.v, pp, s)
+                          : launch_prep_gdn(M.q, M.k, M.v, M.Qt, M.Kt, M.Aqk, M.W, M.Usw, pp, s),
                       "prepare kernel");
     }
     if (rc) return rc;
@@ -600,10 +614,11 @@ int run_bwd(const gdn_desc_t* d, const gdn_bwd_args_t* a, void* stream, bool kda
   fp.dvn = R(L.dvns);
   fp.dQt = R(L.dQt); fp.dKt = R(L.dKt); fp.dW = R(L.dW); fp.dK1 = R(L.dK1); fp.dV1 = R(L.dV1);
   fp.dgam = R(L.dgam);
+  fp.sms = sm_count();
   fp.status = a->status;
   {
     TimedLaunch tl_(kKBwdFeat, s);
-    rc = check_cuda(launch_bwd_feat(M.VN, M.DVN, fp, s), "feature-major backward kernel");
+    rc = check_cuda(launch_bwd_feat(M.VN, M.DVN, M.dO, fp, s), "feature-major backward kernel");
   }
   if (rc) return rc;
 
@@ -626,6 +641,7 @@ int run_bwd(const gdn_desc_t* d, const gdn_bwd_args_t* a, void* stream, bool kda
   tp.dg = a->dg;
   tp.status = a->status;
   tp.kda = kda ? 1 : 0;
+  tp.sms = fp.sms;
   TimedLaunch tl_(kKBwdTok, s);
   return check_cuda(kda ? launch_bwd_tok_kda(M.q, M.k, M.v, M.VN, M.DW, M.DVN, tp, s)
                         : launch_bwd_tok(M.q, M.k, M.v, M.dO, M.VN, M.DW, M.DVN, tp, s),

@@ -147,6 +147,7 @@ struct BwdFeatParams {
   const float* dvn;            // [NC,H,64,V]
   float *dQt, *dKt, *dW, *dK1, *dV1;  // [NC,H,64,128] token-major
   float* dgam;                 // [NC,H,128] (GDN: entry 0)
+  int sms;                     // SM count (the distance to the next wave's CTA for prefetching)
   int* status;
 };
 
@@ -162,6 +163,7 @@ struct BwdTokParams {
   const float *gam, *dgam;     // [NC,H,128]
   __nv_bfloat16 *dq, *dk, *dv, *dbeta;
   float* dg;
+  int sms;                     // SM count (the distance to the next wave's CTA for prefetching)
   int* status;
 };
 
@@ -169,12 +171,14 @@ struct BwdTokParams {
 cudaError_t launch_upload(const UploadParams& p, int* dst, cudaStream_t s);
 cudaError_t launch_tables(const TableParams& p, cudaStream_t s);
 cudaError_t launch_prep_gdn(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
-                            const PrepParams& p, cudaStream_t s);
+                            const CUtensorMap& mQt, const CUtensorMap& mKt, const CUtensorMap& mAqk,
+                            const CUtensorMap& mW, const CUtensorMap& mU, const PrepParams& p, cudaStream_t s);
 cudaError_t launch_prep_kda(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
                             const PrepParams& p, cudaStream_t s);
 cudaError_t launch_chain_bwd(const CUtensorMap& mKt, const CUtensorMap& mAqkT, const CUtensorMap& mQtT,
                              const CUtensorMap& mWT, const RevChainParams& p, cudaStream_t s);
-cudaError_t launch_bwd_feat(const CUtensorMap& mVN, const CUtensorMap& mDVN, const BwdFeatParams& p, cudaStream_t s);
+cudaError_t launch_bwd_feat(const CUtensorMap& mVN, const CUtensorMap& mDVN, const CUtensorMap& mdO,
+                            const BwdFeatParams& p, cudaStream_t s);
 cudaError_t launch_bwd_tok(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, const CUtensorMap& mdO,
                            const CUtensorMap& mVN, const CUtensorMap& mDW, const CUtensorMap& mDVN, const BwdTokParams& p,
                            cudaStream_t s);

@@ -27,7 +27,8 @@ constexpr uint32_t kOffDO = 0;        // dO   [t][v] tf32, 4 panels x 64 rows (3
 constexpr uint32_t kOffVN = 32768;    // v_new [t][v] (TMA)
 constexpr uint32_t kOffDVN = 65536;   // dv_new [t][v] (TMA)
 constexpr uint32_t kOffAT = 98304;    // A^T  [j][i] tf32, 2 panels x 64 rows (16 KB)
-constexpr uint32_t kSmemBytes = 114688 + 1024;
+constexpr uint32_t kOffDO16 = 114688; // dO   [t][v] bf16 (TMA), 2 panels x 64 rows (16 KB)
+constexpr uint32_t kSmemBytes = 131072 + 1024;
 constexpr uint32_t kTH = 0, kTDH = 128, kTP1 = 256, kTP2 = 320, kTP3 = 384, kTP5 = 448;
 
 __device__ __forceinline__ uint8_t* align1k(uint8_t* p) {
@@ -38,7 +39,7 @@ __device__ __forceinline__ uint8_t* align1k(uint8_t* p) {
 
 __global__ void __launch_bounds__(kThreads, 1)
     k_bwd_feat(const __grid_constant__ CUtensorMap mVN, const __grid_constant__ CUtensorMap mDVN,
-               const BwdFeatParams p) {
+               const __grid_constant__ CUtensorMap mdO, const BwdFeatParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = align1k(smem_raw);
   __shared__ uint64_t bar_tma, bar_mma;
@@ -66,10 +67,25 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tb = tslot;
   const uint32_t tl = tb + tmem_lane_base(warp);
   if (tid == 0) {
-    mbar_expect_tx(&bar_tma, 65536u);
+    mbar_expect_tx(&bar_tma, 65536u + 16384u);
     for (int pp = 0; pp < 4; ++pp) {
       tma_load_2d(sm + kOffVN + pp * 8192, &mVN, pp * 32, int(tile) * kC, &bar_tma);
       tma_load_2d(sm + kOffDVN + pp * 8192, &mDVN, pp * 32, int(tile) * kC, &bar_tma);
+    }
+    for (int pp = 0; pp < 2; ++pp) tma_load_2d(sm + kOffDO16 + pp * 8192, &mdO, h * kD + 64 * pp, ch.x, &bar_tma);
+    // the next wave's CTA finds its inputs in L2
+    int nx, ny;
+    if (next_wave_block(p.sms, &nx, &ny)) {
+      const size_t nt = size_t(nx) * H + ny;
+      prefetch_l2(p.h + nt * kD * kD, 4u * kD * kD);
+      prefetch_l2(p.dh + nt * kD * kD, 4u * kD * kD);
+      prefetch_l2(p.A + nt * kTileAqk, 4u * kTileAqk);
+      for (int pp = 0; pp < 4; ++pp) {
+        prefetch_l2_tile(&mVN, pp * 32, int(nt) * kC);
+        prefetch_l2_tile(&mDVN, pp * 32, int(nt) * kC);
+      }
+      const ChunkEntry nch = p.chunks[nx];
+      for (int pp = 0; pp < 2; ++pp) prefetch_l2_tile(&mdO, ny * kD + 64 * pp, nch.x);
     }
   }
   // h and dh' rows -> TMEM (tf32 A operands); dgam partial sums in fp32. Each warp stages its
@@ -108,17 +124,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_st32(tl + kTDH + 32 * g4, b);
     }
   }
-  // dO^T operand: element (t, v=f) of the K-major [t][v] tile; rows past the chunk are zero.
-  {
-    const __nv_bfloat16* src = p.dO + (size_t(ch.x) * H + h) * kD + f;
-    for (int t0 = 0; t0 < kC; t0 += 32) {
-      float buf[32];
-#pragma unroll
-      for (int e = 0; e < 32; ++e) buf[e] = (t0 + e < ch.y) ? __bfloat162float(src[size_t(t0 + e) * H * kD]) : 0.f;
-#pragma unroll
-      for (int e = 0; e < 32; ++e) *reinterpret_cast<float*>(sm + kOffDO + sw128_offset(t0 + e, f, kC, 4)) = buf[e];
-    }
-  }
   // A^T operand: element (j, i) = A[i][j]; thread pairs split the 64 rows i of column j = f % 64.
   {
     const int j = f & 63, i0 = (f >> 6) * 32;
@@ -129,6 +134,18 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
     for (int e = 0; e < 32; ++e) *reinterpret_cast<float*>(sm + kOffAT + sw128_offset(j, i0 + e, kC, 4)) = to_tf32(buf[e]);
   }
+  // dO^T operand: element (t, v=f) of the K-major [t][v] tile from the bf16 TMA tile; rows past
+  // the chunk (the next document's, or out of range) are zero.
+  const bool tma_ok = mbar_wait(&bar_tma, 0, &abort_flag, p.status, kDevTimeoutTma);
+  if (tma_ok) {
+#pragma unroll 8
+    for (int t = 0; t < kC; ++t) {
+      const float x = t < ch.y ? __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(
+                                     sm + kOffDO16 + sw128_offset(t, f, kC, 2)))
+                               : 0.f;
+      *reinterpret_cast<float*>(sm + kOffDO + sw128_offset(t, f, kC, 4)) = x;
+    }
+  }
   tmem_wait_st();
   fence_async_smem();
   tc_fence_before();
@@ -136,7 +153,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
 
   if (tid == 0) {
-    if (mbar_wait(&bar_tma, 0, &abort_flag, p.status, kDevTimeoutTma)) {
+    if (tma_ok) {
       tc_fence_after();
       const uint32_t id64 = idesc_tf32(128, 64);
       const uint32_t sDO = smem_u32(sm + kOffDO), sVN = smem_u32(sm + kOffVN), sDVN = smem_u32(sm + kOffDVN);
@@ -174,10 +191,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     tmem_st32(tl + kTP2, r);
     tmem_st32(tl + kTP2 + 32, r + 32);
-    // dv_new^T row f (lane f = value column f) as the A operand of A^T dv_new (reuses h's columns).
-    const float* dvn = p.dvn + tile * kTileW + f;
+    // dv_new^T row f (lane f = value column f) as the A operand of A^T dv_new (reuses h's
+    // columns), read from the TMA copy of dv_new already in shared memory.
 #pragma unroll
-    for (int t = 0; t < kC; ++t) r[t] = to_tf32(dvn[size_t(t) * kD]);
+    for (int t = 0; t < kC; ++t)
+      r[t] = to_tf32(*reinterpret_cast<const float*>(sm + kOffDVN + sw128_offset(t, f, kC, 4)));
     tmem_st32(tl + kTH, r);
     tmem_st32(tl + kTH + 32, r + 32);
     tmem_wait_st();
@@ -222,7 +240,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0) tmem_dealloc(tb, 512);
 }
 
-cudaError_t launch_bwd_feat(const CUtensorMap& mVN, const CUtensorMap& mDVN, const BwdFeatParams& p, cudaStream_t s) {
+cudaError_t launch_bwd_feat(const CUtensorMap& mVN, const CUtensorMap& mDVN, const CUtensorMap& mdO,
+                            const BwdFeatParams& p, cudaStream_t s) {
   static bool attr = false;
   if (!attr) {
     cudaError_t e = cudaFuncSetAttribute(k_bwd_feat, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
@@ -230,7 +249,7 @@ cudaError_t launch_bwd_feat(const CUtensorMap& mVN, const CUtensorMap& mDVN, con
     attr = true;
   }
   dim3 grid(p.NC, p.H);
-  k_bwd_feat<<<grid, kThreads, kSmemBytes, s>>>(mVN, mDVN, p);
+  k_bwd_feat<<<grid, kThreads, kSmemBytes, s>>>(mVN, mDVN, mdO, p);
   return cudaGetLastError();
 }
 

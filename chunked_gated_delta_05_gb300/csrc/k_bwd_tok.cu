@@ -64,6 +64,17 @@ __device__ __forceinline__ float bf16_at(const uint8_t* tile, int row, int col) 
 __device__ __forceinline__ void put32(uint8_t* tile, int rows, int row, int col, float x) {
   *reinterpret_cast<float*>(tile + sw128_offset(row, col, rows, 4)) = x;
 }
+// Four consecutive fp32 columns (col % 4 == 0: one 16-byte chunk of the swizzled row).
+__device__ __forceinline__ void put32x4(uint8_t* tile, int rows, int row, int col, float a, float b, float c, float d) {
+  *reinterpret_cast<float4*>(tile + sw128_offset(row, col, rows, 4)) = make_float4(a, b, c, d);
+}
+// Four consecutive bf16 columns (col % 4 == 0) of a 64-row bf16 tile, as fp32.
+__device__ __forceinline__ void bf16x4_at(const uint8_t* tile, int row, int col, float* f) {
+  const uint2 u = *reinterpret_cast<const uint2*>(tile + sw128_offset(row, col, kC, 2));
+  const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.x));
+  const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.y));
+  f[0] = a.x; f[1] = a.y; f[2] = b.x; f[3] = b.y;
+}
 
 }  // namespace
 
@@ -177,12 +188,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   TTRACE(3);
   tc_fence_after();
   // ---- K1 = diag(beta exp(G) r_k) k and V1 = diag(beta) v as 64-row operands [j][d]
+  // (a warp converts one row per step: lane l takes columns 4l..4l+3, one 16-byte chunk)
   {
-    const int f = tid & 127;
-    for (int j = 32 * half; j < 32 * half + 32; ++j) {
-      const float s1 = s_b[j] * expf(s_G[j]) * s_rk[j];
-      put32(sm + kR1, kC, j, f, to_tf32(s1 * bf16_at(sK, j, f)));
-      put32(sm + kR2, kC, j, f, to_tf32(s_b[j] * bf16_at(sV, j, f)));
+    const int c0 = 4 * lane;
+#pragma unroll 2
+    for (int j = warp; j < kC; j += 8) {
+      const float s1 = s_b[j] * expf(s_G[j]) * s_rk[j], s2 = s_b[j];
+      float kf[4], vf[4];
+      bf16x4_at(sK, j, c0, kf);
+      bf16x4_at(sV, j, c0, vf);
+      put32x4(sm + kR1, kC, j, c0, to_tf32(s1 * kf[0]), to_tf32(s1 * kf[1]), to_tf32(s1 * kf[2]), to_tf32(s1 * kf[3]));
+      put32x4(sm + kR2, kC, j, c0, to_tf32(s2 * vf[0]), to_tf32(s2 * vf[1]), to_tf32(s2 * vf[2]), to_tf32(s2 * vf[3]));
     }
   }
   fence_async_smem();
@@ -333,11 +349,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     TTRACE(12);
   }
   // transposed raw tiles k^T [d][j], q^T [d][i] (zero past the chunk: cleared above)
+  // (thread: row d, four consecutive token columns per step, one 16-byte chunk)
   {
     const int d = tid & 127;
-    for (int j = 32 * half; j < 32 * half + 32; ++j) {
-      put32(sKT, kD, d, j, to_tf32(bf16_at(sK, j, d)));
-      put32(sQT, kD, d, j, to_tf32(bf16_at(sQ, j, d)));
+#pragma unroll 2
+    for (int j = 4 * half; j < kC; j += 8) {
+      put32x4(sKT, kD, d, j, to_tf32(bf16_at(sK, j, d)), to_tf32(bf16_at(sK, j + 1, d)),
+              to_tf32(bf16_at(sK, j + 2, d)), to_tf32(bf16_at(sK, j + 3, d)));
+      put32x4(sQT, kD, d, j, to_tf32(bf16_at(sQ, j, d)), to_tf32(bf16_at(sQ, j + 1, d)),
+              to_tf32(bf16_at(sQ, j + 2, d)), to_tf32(bf16_at(sQ, j + 3, d)));
     }
   }
   TTRACE(13);

@@ -18,7 +18,10 @@
 // two diagonal 64x64 blocks are used; W and U are block-diagonal (A) times the raw k / v tile
 // (MN-major B operand). L2-norm factors and decays are applied to the fp32 MMA results, never
 // to the bf16 operands. The unit-lower-triangular inverse runs in fp32 registers, one column
-// per thread (forward substitution, the same recurrence as the page's row loop).
+// per thread (forward substitution, the same recurrence as the page's row loop). Row-major
+// output tiles (Qt, Kt, Aqk, W, U) are staged in shared memory in the swizzled operand layout
+// and written by TMA stores, so the row-per-thread results leave as whole lines; the
+// transposed tiles are written directly (consecutive threads, consecutive addresses).
 #include "common.cuh"
 #include "umma.cuh"
 
@@ -43,7 +46,8 @@ namespace {
 constexpr int kThreads = 128;
 constexpr uint32_t kPanel = 16384;  // 128 rows x 128 B
 constexpr uint32_t kOffQ = 0, kOffK = 32768, kOffV = 65536, kOffA1 = 98304, kOffA2 = 131072,
-                   kOffL = 163840, kSmemBytes = 196608 + 1024;
+                   kOffL = 163840, kOffS0 = 196608, kSmemBytes = 229376 + 1024;
+constexpr uint32_t kStage = 32768;  // one chunk's [64][128] fp32 tile: 4 panels x 64 rows x 128 B
 
 __device__ __forceinline__ uint8_t* align1k(uint8_t* p) {
   return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
@@ -105,7 +109,9 @@ __device__ __forceinline__ void unit_lower_inverse_column(const float* __restric
 
 __global__ void __launch_bounds__(kThreads, 1)
     k_prep_gdn(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
-               const __grid_constant__ CUtensorMap mv, const PrepParams p) {
+               const __grid_constant__ CUtensorMap mv, const __grid_constant__ CUtensorMap mQt,
+               const __grid_constant__ CUtensorMap mKt, const __grid_constant__ CUtensorMap mAqk,
+               const __grid_constant__ CUtensorMap mW, const __grid_constant__ CUtensorMap mU, const PrepParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = align1k(smem_raw);
   uint8_t* sQ = sm + kOffQ;
@@ -114,6 +120,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* sA1 = sm + kOffA1;
   uint8_t* sA2 = sm + kOffA2;
   float* sL = reinterpret_cast<float*>(sm + kOffL);
+  uint8_t* sS0 = sm + kOffS0;
   __shared__ uint64_t bar_tma, bar_mma;
   __shared__ uint32_t tslot;
   __shared__ int abort_flag;
@@ -219,21 +226,25 @@ __global__ void __launch_bounds__(kThreads, 1)
     mma_commit(&bar_mma);
   }
 
-  // Gated queries and end-decayed keys (state-independent operands of the chunk loop).
+  // Gated queries and end-decayed keys (state-independent operands of the chunk loop): the
+  // row-major Qt and Kt tiles are staged (A1/A2 and L/S0 are free until the inverse) and
+  // stored by TMA; the transposed KtT and QtT go straight out.
   const size_t tile = size_t(c_idx) * H + h;
+  uint8_t* stQt = blk ? sA2 : sA1;
+  uint8_t* stKt = blk ? sS0 : reinterpret_cast<uint8_t*>(sL);
   if (len > 0) {
     const float fq = valid ? p.scale * rq * expf(G) : 0.f;
     const float fk = valid ? rk * expf(Glast - G) : 0.f;
-    float* qt = p.Qt + tile * kTileW + size_t(il) * kD;
     float* ktt = p.KtT + tile * kTileKtT + il;
 #pragma unroll
     for (int c16 = 0; c16 < 16; ++c16) {
       const uint32_t off = sw128_offset(tid, c16 * 8, 128, 2);
       float f[8];
       bf16x8_to_f32(*reinterpret_cast<const uint4*>(sQ + off), f);
-      float4* dst = reinterpret_cast<float4*>(qt + c16 * 8);
-      dst[0] = make_float4(to_tf32(f[0] * fq), to_tf32(f[1] * fq), to_tf32(f[2] * fq), to_tf32(f[3] * fq));
-      dst[1] = make_float4(to_tf32(f[4] * fq), to_tf32(f[5] * fq), to_tf32(f[6] * fq), to_tf32(f[7] * fq));
+#pragma unroll
+      for (int e = 0; e < 8; e += 4)
+        *reinterpret_cast<float4*>(stQt + sw128_offset(il, c16 * 8 + e, kC, 4)) =
+            make_float4(to_tf32(f[e] * fq), to_tf32(f[e + 1] * fq), to_tf32(f[e + 2] * fq), to_tf32(f[e + 3] * fq));
       if (p.QtT) {
 #pragma unroll
         for (int e = 0; e < 8; ++e) p.QtT[tile * kTileKtT + size_t(c16 * 8 + e) * kC + il] = to_tf32(f[e] * fq);
@@ -242,9 +253,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int e = 0; e < 8; ++e) ktt[size_t(c16 * 8 + e) * kC] = to_tf32(f[e] * fk);
       if (p.Kt) {
-        float4* kt = reinterpret_cast<float4*>(p.Kt + tile * kTileW + size_t(il) * kD + c16 * 8);
-        kt[0] = make_float4(to_tf32(f[0] * fk), to_tf32(f[1] * fk), to_tf32(f[2] * fk), to_tf32(f[3] * fk));
-        kt[1] = make_float4(to_tf32(f[4] * fk), to_tf32(f[5] * fk), to_tf32(f[6] * fk), to_tf32(f[7] * fk));
+#pragma unroll
+        for (int e = 0; e < 8; e += 4)
+          *reinterpret_cast<float4*>(stKt + sw128_offset(il, c16 * 8 + e, kC, 4)) =
+              make_float4(to_tf32(f[e] * fk), to_tf32(f[e + 1] * fk), to_tf32(f[e + 2] * fk), to_tf32(f[e + 3] * fk));
       }
     }
     if (il == 0) p.gam[tile * kD] = expf(Glast);
@@ -253,13 +265,27 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (p.rk) p.rk[tile * kC + il] = rk;
     if (p.beff) p.beff[tile * kC + il] = bi;
   }
-
+  fence_async_smem();
+  __syncthreads();
+  if (tid == 0) {
+    for (int b = 0; b < 2; ++b) {
+      if (s_chunk[b].y <= 0) continue;
+      const int y = (int(2 * pair + b) * H + h) * kC;
+      for (int pp = 0; pp < 4; ++pp) {
+        tma_store_2d(&mQt, pp * 32, y, (b ? sA2 : sA1) + pp * 8192);
+        if (p.Kt) tma_store_2d(&mKt, pp * 32, y, (b ? sS0 : reinterpret_cast<uint8_t*>(sL)) + pp * 8192);
+      }
+    }
+    tma_store_commit();
+  }
   PTRACE(3);
   const bool ok1 = mbar_wait(&bar_mma, 0, &abort_flag, p.status, kDevTimeoutMma);
   tc_fence_after();
+  if (tid == 0) tma_store_wait_read();  // L and A1 are rewritten next
+  __syncthreads();
+  uint8_t* stAqk = sA1 + blk * (kStage / 2);
   if (ok1) {
     float* LT = sL + blk * (kC * kC) + il;  // column il of L^T
-    float* aqk = p.Aqk + tile * kTileAqk + size_t(il) * kC;
     float kk[kC], qk[kC];
     tmem_ld64(tb + lane_base + blk * kC, kk);
     tmem_ld64(tb + lane_base + 128 + blk * kC, qk);
@@ -273,9 +299,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       qk[j] = (j <= il && valid) ? to_tf32(p.scale * rq * qk[j] * dec) : 0.f;
     }
     if (len > 0) {
-      float4* dst = reinterpret_cast<float4*>(aqk);
 #pragma unroll
-      for (int e = 0; e < kC / 4; ++e) dst[e] = make_float4(qk[4 * e], qk[4 * e + 1], qk[4 * e + 2], qk[4 * e + 3]);
+      for (int e = 0; e < kC / 4; ++e)
+        *reinterpret_cast<float4*>(stAqk + sw128_offset(il, 4 * e, kC, 4)) =
+            make_float4(qk[4 * e], qk[4 * e + 1], qk[4 * e + 2], qk[4 * e + 3]);
       if (p.AqkT) {
         float* at = p.AqkT + tile * kTileAqk + il;
 #pragma unroll
@@ -283,8 +310,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   }
+  fence_async_smem();
   tc_fence_before();
   __syncthreads();
+  if (tid == 0) {
+    for (int b = 0; b < 2; ++b) {
+      if (s_chunk[b].y <= 0) continue;
+      const int y = (int(2 * pair + b) * H + h) * kC;
+      for (int pp = 0; pp < 2; ++pp) tma_store_2d(&mAqk, pp * 32, y, sA1 + b * (kStage / 2) + pp * 8192);
+    }
+    tma_store_commit();
+  }
   PTRACE(4);
 
   // Column il of A = (I + L)^-1 for this thread's chunk (into sX, which reuses the q tile:
@@ -298,6 +334,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int r = 0; r < kC; ++r) a[size_t(r) * kC] = sX[r * kC + il];
   }
   PTRACE(5);
+  if (tid == 0) tma_store_wait_read();  // A1 held the staged Aqk tiles
+  __syncthreads();
   {
     const float s1 = bi * expf(G) * rk, s2 = bi;
     const int col = tid;
@@ -335,10 +373,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   const bool ok2 = mbar_wait(&bar_mma, 1, &abort_flag, p.status, kDevTimeoutMma);
   tc_fence_after();
   PTRACE(7);
+  // W -> staged in L (chunk 0) / S0 (chunk 1), U -> A1 / A2 (free once the MMAs are done)
   if (ok2 && len > 0) {
     const float dw_scale = bi * expf(G) * rk, du_scale = bi;
     for (int which = 0; which < 2; ++which) {
-      float* dst = (which == 0 ? p.W : p.U) + tile * kTileW + size_t(il) * kD;
+      uint8_t* stage = which == 0 ? (blk ? sS0 : reinterpret_cast<uint8_t*>(sL)) : (blk ? sA2 : sA1);
       const uint8_t* src = which == 0 ? sK : sV;
       const float sc = which == 0 ? dw_scale : du_scale;
       for (int half = 0; half < 2; ++half) {
@@ -355,9 +394,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             r[c8 * 8 + e] = which == 0 ? to_tf32(val) : val;
           }
         }
-        float4* d4 = reinterpret_cast<float4*>(dst + half * 64);
 #pragma unroll
-        for (int e = 0; e < 16; ++e) d4[e] = make_float4(r[4 * e], r[4 * e + 1], r[4 * e + 2], r[4 * e + 3]);
+        for (int e = 0; e < 16; ++e)
+          *reinterpret_cast<float4*>(stage + sw128_offset(il, half * 64 + 4 * e, kC, 4)) =
+              make_float4(r[4 * e], r[4 * e + 1], r[4 * e + 2], r[4 * e + 3]);
         if (which == 0 && p.WT) {
           float* wt = p.WT + tile * kTileKtT + size_t(half * 64) * kC + il;
 #pragma unroll
@@ -366,6 +406,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   }
+  fence_async_smem();
+  __syncthreads();
+  if (tid == 0) {
+    for (int b = 0; b < 2; ++b) {
+      if (s_chunk[b].y <= 0 || !ok2) continue;
+      const int y = (int(2 * pair + b) * H + h) * kC;
+      for (int pp = 0; pp < 4; ++pp) {
+        tma_store_2d(&mW, pp * 32, y, (b ? sS0 : reinterpret_cast<uint8_t*>(sL)) + pp * 8192);
+        tma_store_2d(&mU, pp * 32, y, (b ? sA2 : sA1) + pp * 8192);
+      }
+    }
+    tma_store_commit();
+    tma_store_wait_all();
+  }
   PTRACE(8);
   tc_fence_before();
   __syncthreads();
@@ -373,7 +427,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 cudaError_t launch_prep_gdn(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
-                            const PrepParams& p, cudaStream_t s) {
+                            const CUtensorMap& mQt, const CUtensorMap& mKt, const CUtensorMap& mAqk,
+                            const CUtensorMap& mW, const CUtensorMap& mU, const PrepParams& p, cudaStream_t s) {
   static bool attr = false;
   if (!attr) {
     cudaError_t e = cudaFuncSetAttribute(k_prep_gdn, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
@@ -381,7 +436,7 @@ cudaError_t launch_prep_gdn(const CUtensorMap& mq, const CUtensorMap& mk, const 
     attr = true;
   }
   dim3 grid((p.NC + 1) / 2, p.H);
-  k_prep_gdn<<<grid, kThreads, kSmemBytes, s>>>(mq, mk, mv, p);
+  k_prep_gdn<<<grid, kThreads, kSmemBytes, s>>>(mq, mk, mv, mQt, mKt, mAqk, mW, mU, p);
   return cudaGetLastError();
 }
 

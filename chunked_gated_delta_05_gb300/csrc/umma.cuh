@@ -97,12 +97,31 @@ __device__ __forceinline__ void tma_store_2d(const CUtensorMap* m, int x, int y,
 }
 __device__ __forceinline__ void tma_store_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void tma_store_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+// The committed stores have finished reading their shared-memory sources (which may be reused).
+__device__ __forceinline__ void tma_store_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
 
 // Fetch `bytes` (a multiple of 16, 16-byte aligned source) into L2 ahead of use; no
 // completion to wait for.
 __device__ __forceinline__ void prefetch_l2(const void* src, uint32_t bytes) {
   asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(src)), "r"(bytes)
                : "memory");
+}
+
+// L2 prefetch of one box of a tensor map (no shared memory involved).
+__device__ __forceinline__ void prefetch_l2_tile(const CUtensorMap* m, int x, int y) {
+  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];"
+               ::"l"(reinterpret_cast<uint64_t>(m)), "r"(x), "r"(y)
+               : "memory");
+}
+
+// The CTA that starts about one wave after this one when every SM runs one CTA at a time
+// (linear block index + `sms`), as (x, y) of a 2-D grid; false past the end of the grid.
+__device__ __forceinline__ bool next_wave_block(int sms, int* x, int* y) {
+  const long long next = (long long)blockIdx.y * gridDim.x + blockIdx.x + sms;
+  if (next >= (long long)gridDim.x * gridDim.y) return false;
+  *x = int(next % gridDim.x);
+  *y = int(next / gridDim.x);
+  return true;
 }
 
 // Generic-proxy shared-memory writes -> visible to the async proxy (tensor core, TMA).
