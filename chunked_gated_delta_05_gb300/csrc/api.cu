@@ -107,9 +107,11 @@ int g_chain_segment = 0;
 
 // Wave model of the chain scan on a GB300 (152 SMs, one chain CTA per SM): pass 0 runs
 // 1 + 2 (ns - 2) CTAs per (sequence, head), pass 1 runs ns - 1, each for about L chunk steps;
-// the compose kernel walks ns - 2 segments.
+// the compose kernel walks ns - 2 segments. The step costs are GB300 measurements (a chain
+// step averaged over the forward and reverse chains and over full and map runs under a full
+// wave of CTAs; one compose step).
 constexpr int kWaveSMs = 152;
-constexpr double kChunkStepUs = 3.7, kComposeStepUs = 3.0, kLaunchUs = 3.0;
+constexpr double kChunkStepUs = 4.25, kComposeStepUs = 6.0, kLaunchUs = 3.0;
 constexpr int kMaxSegments = 64;
 
 struct ScanPlan {
@@ -408,9 +410,10 @@ SegPlan seg_plan(const ScanPlan& sc, char* base, size_t E, size_t Phi, size_t Pl
 // Compose step between the two chain passes (sequences with three or more segments).
 int run_compose(const Problem& P, const SeqEntry* seqs, const SegPlan& sp, int* status, cudaStream_t s) {
   const uint64_t rows = uint64_t(P.N) * sp.maxS * P.H * kD;
-  CUtensorMap mPhi, mPlo;
+  CUtensorMap mPhi, mPlo, mB;
   if (!tile_map(&mPhi, reinterpret_cast<const char*>(sp.Phi), kD, rows, 128, true) ||
-      !tile_map(&mPlo, reinterpret_cast<const char*>(sp.Plo), kD, rows, 128, true))
+      !tile_map(&mPlo, reinterpret_cast<const char*>(sp.Plo), kD, rows, 128, true) ||
+      !tile_map(&mB, reinterpret_cast<const char*>(sp.Bm), kD, rows, 128, false))
     return fail(GDN_ECUDA, "cuTensorMapEncodeTiled failed");
   ComposeParams cp{};
   cp.seqs = seqs;
@@ -419,7 +422,7 @@ int run_compose(const Problem& P, const SeqEntry* seqs, const SegPlan& sp, int* 
   cp.sp = sp;
   cp.status = status;
   TimedLaunch tl_(kKCompose, s);
-  return check_cuda(launch_compose(mPhi, mPlo, cp, s), "compose kernel");
+  return check_cuda(launch_compose(mPhi, mPlo, mB, cp, s), "compose kernel");
 }
 
 // Forward chain: one plain pass, or pass 0, compose, pass 1 of the segmented chain.
@@ -446,7 +449,7 @@ int run_chain_bwd(const Problem& P, const Maps& M, RevChainParams rp, cudaStream
     }
     rp.sp.pass = pass;
     TimedLaunch tl_(kKChainBwd, s);
-    int rc = check_cuda(launch_chain_bwd(M.Kt, M.AqkT, M.QtT, M.WT, rp, s), "reverse chain kernel");
+    int rc = check_cuda(launch_chain_bwd(M.Kt, M.AqkT, M.QtT, M.WT, M.dO, rp, s), "reverse chain kernel");
     if (rc) return rc;
   }
   return GDN_OK;
@@ -460,8 +463,8 @@ int run_fwd(const gdn_desc_t* d, const gdn_fwd_args_t* a, void* stream, bool kda
   if (!a->q || !a->k || !a->v || !a->g || !a->beta || !a->o)
     return fail(GDN_EINVAL, "q, k, v, g, beta and o must be non-NULL");
   if (d->output_final_state && !a->final_state) return fail(GDN_EINVAL, "final_state is NULL but requested");
-  if (!aligned16(a->q) || !aligned16(a->k) || !aligned16(a->v))
-    return fail(GDN_EINVAL, "q, k and v must be 16-byte aligned");
+  if (!aligned16(a->q) || !aligned16(a->k) || !aligned16(a->v) || !aligned16(a->o))
+    return fail(GDN_EINVAL, "q, k, v and o must be 16-byte aligned");
   const size_t nqk = size_t(P.R) * P.H * kD * 2;
   if (overlaps(a->o, nqk, a->q, nqk) || overlaps(a->o, nqk, a->k, nqk) || overlaps(a->o, nqk, a->v, nqk))
     return fail(GDN_EINVAL, "o must not alias q, k or v");

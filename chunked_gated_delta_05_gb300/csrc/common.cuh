@@ -176,7 +176,8 @@ cudaError_t launch_prep_gdn(const CUtensorMap& mq, const CUtensorMap& mk, const 
 cudaError_t launch_prep_kda(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
                             const PrepParams& p, cudaStream_t s);
 cudaError_t launch_chain_bwd(const CUtensorMap& mKt, const CUtensorMap& mAqkT, const CUtensorMap& mQtT,
-                             const CUtensorMap& mWT, const RevChainParams& p, cudaStream_t s);
+                             const CUtensorMap& mWT, const CUtensorMap& mdO, const RevChainParams& p,
+                             cudaStream_t s);
 cudaError_t launch_bwd_feat(const CUtensorMap& mVN, const CUtensorMap& mDVN, const CUtensorMap& mdO,
                             const BwdFeatParams& p, cudaStream_t s);
 cudaError_t launch_bwd_tok(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, const CUtensorMap& mdO,
@@ -192,8 +193,8 @@ struct ComposeParams {
   int* status;
 };
 
-cudaError_t launch_compose(const CUtensorMap& mPhi, const CUtensorMap& mPlo, const ComposeParams& p,
-                           cudaStream_t s);
+cudaError_t launch_compose(const CUtensorMap& mPhi, const CUtensorMap& mPlo, const CUtensorMap& mB,
+                           const ComposeParams& p, cudaStream_t s);
 cudaError_t launch_chain_fwd(const CUtensorMap& mW, const CUtensorMap& mQt, const CUtensorMap& mKtT,
                              const CUtensorMap& mAqk, const CUtensorMap& mU, const ChainParams& p,
                              cudaStream_t s);

@@ -11,13 +11,15 @@
 // (V x K), lane v = column v of S, as an fp32 master copy plus a round-to-nearest tf32 copy
 // that the MMAs read as their TMEM-resident A operand (kind::tf32). The chunk tiles from the
 // prepare kernel are TMA-loaded SW128 B operands:
-//   P    = S^T W^T           (v_new^T = U^T - P)           -- on the serial chain
+//   [P | O] = S^T [W; Qt]^T  (one N=128 product: P = S^T W^T, O = S^T Qt^T)  -- on the chain
+//   v_new^T = U^T - P        (written over P in TMEM)
 //   S^T += v_new^T KtT^T     (master pre-decayed by gam)   -- on the serial chain
-//   O    = S^T Qt^T + v_new^T Aqk^T                        -- off the chain, issued after
-// The MMAs on the chain are issued first and committed on their own barriers, so the output
-// products run on the tensor pipe while the chain threads work. Eight chain warps share the
-// TMEM lanes (two threads per lane, each on half of the columns); warp 8 streams the tiles
-// with TMA (KtT/Aqk double-buffered) and issues the MMAs from one thread. All waits bounded.
+//   O   += v_new^T Aqk^T                                   -- off the chain, issued after
+// An MMA instruction costs about the same for N = 64 and N = 128, so stacking W and Qt into
+// one 128-row B operand gives the output's state product for free alongside P. P/v_new and O
+// are double-buffered in TMEM by chunk parity. Eight chain warps share the TMEM lanes (two
+// threads per lane, each on half of the columns); warp 8 streams the tiles with TMA (KtT/Aqk
+// double-buffered) and issues the MMAs from one thread. All waits bounded.
 //
 // A CTA runs one segment of a sequence's chunks in one of three modes (the segmented chain
 // of common.cuh): in full (from the true entry state, with the output and the backward
@@ -30,10 +32,14 @@ namespace gdn {
 
 #ifdef GDN_TRACE
 // Optional timeline of the first CTA (compiled only with -DGDN_TRACE; never in the library).
-__device__ unsigned long long g_trace[64 * 8];
-#define TRACE(j, slot)                                                                          \
-  do {                                                                                          \
-    if (blockIdx.x == 0 && blockIdx.y == 0 && (j) < 64) g_trace[(j) * 8 + (slot)] = globaltimer(); \
+__device__ unsigned long long g_trace[64 * 16];
+__device__ int g_trace_block = 0;
+extern "C" int g_trace_set_block(int b) {
+  return cudaMemcpyToSymbol(g_trace_block, &b, sizeof(int)) == cudaSuccess ? 0 : -1;
+}
+#define TRACE(j, slot)                                                                           \
+  do {                                                                                           \
+    if (blockIdx.x == g_trace_block && blockIdx.y == 0 && (j) < 64) g_trace[(j) * 16 + (slot)] = globaltimer(); \
   } while (0)
 #else
 #define TRACE(j, slot) \
@@ -46,14 +52,15 @@ namespace {
 constexpr int kChainThreads = 256;            // 8 warps: lane v = tid % 128, half = tid / 128
 constexpr int kThreads = kChainThreads + 32;  // + producer warp
 // shared memory tile offsets (bytes, 1024-aligned)
-constexpr uint32_t kOffW = 0;          // 4 panels x 64 rows x 128 B   (W   [t][k], K-major)
-constexpr uint32_t kOffQt = 32768;     // 4 panels x 64 rows x 128 B   (Qt  [t][k])
+constexpr uint32_t kOffWQ = 0;         // 4 panels x 128 rows x 128 B: rows 0-63 W [t][k], 64-127 Qt [t][k]
 constexpr uint32_t kOffU = 65536;      // 4 panels x [64][32] fp32, no swizzle
 constexpr uint32_t kOffG3 = 98304;     // 2 stages x {KtT 32 KB (2 panels x 128 rows), Aqk 16 KB}
 constexpr uint32_t kG3Stage = 49152;
 constexpr uint32_t kSmemBytes = kOffG3 + 2 * kG3Stage + 1024;
-// TMEM columns
-constexpr uint32_t kTSM = 0, kTST = 128, kTP = 256, kTVN = 320, kTO = 384;
+// TMEM columns: master, tf32 copy, then per chunk parity [P, later v_new | O]
+constexpr uint32_t kTSM = 0, kTST = 128, kTB = 256;
+__device__ __forceinline__ uint32_t tpv(int j) { return kTB + uint32_t(j & 1) * 128; }
+__device__ __forceinline__ uint32_t tout(int j) { return kTB + uint32_t(j & 1) * 128 + 64; }
 
 __device__ __forceinline__ uint8_t* align1k(uint8_t* p) {
   return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
@@ -114,7 +121,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const __grid_constant__ CUtensorMap mU, const ChainParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = align1k(smem_raw);
-  __shared__ uint64_t full1, full2, full3[2], mma1, mma1b, mma2, mma3, sready, vready;
+  __shared__ uint64_t full1, full2, full3[2], mma1, mma2, mma3, sready, vready;
   __shared__ uint32_t tslot;
   __shared__ int abort_flag;
 
@@ -141,7 +148,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&full3[0], 1);
     mbar_init(&full3[1], 1);
     mbar_init(&mma1, 1);
-    mbar_init(&mma1b, 1);
     mbar_init(&mma2, 1);
     mbar_init(&mma3, 1);
     mbar_init(&sready, kChainThreads);
@@ -156,13 +162,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == kChainThreads / 32) {
     if (lane == 0) {
       // ---------------- producer + MMA issuer ----------------
-      const uint32_t sW = smem_u32(sm + kOffW), sQt = smem_u32(sm + kOffQt);
+      const uint32_t sWQ = smem_u32(sm + kOffWQ);
       auto load_g1 = [&](int c) {
         const int y = (c * H + h) * kC;
         mbar_expect_tx(&full1, outs ? 65536u : 32768u);
         for (int pp = 0; pp < 4; ++pp) {
-          tma_load_2d(sm + kOffW + pp * 8192, &mW, pp * 32, y, &full1);
-          if (outs) tma_load_2d(sm + kOffQt + pp * 8192, &mQt, pp * 32, y, &full1);
+          tma_load_2d(sm + kOffWQ + pp * 16384, &mW, pp * 32, y, &full1);
+          if (outs) tma_load_2d(sm + kOffWQ + pp * 16384 + 8192, &mQt, pp * 32, y, &full1);
         }
       };
       auto load_g2 = [&](int c) {
@@ -183,22 +189,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       load_g3(first, 0);
       if (nc > 1) load_g3(first + 1, 1);
       const uint32_t id64 = idesc_tf32(128, 64), id128 = idesc_tf32(128, 128);
+      const uint32_t id_first = outs ? id128 : id64;  // [P | O] or P alone
       for (int j = 0; j < nc; ++j) {
         const uint32_t par = j & 1;
         const int c = first + j, st = j & 1;
-        const uint32_t tO = tb + kTO + (j & 1) * 64;
+        const uint32_t tPV = tb + tpv(j), tO = tb + tout(j);
         const uint32_t sKtT = smem_u32(sm + kOffG3 + st * kG3Stage), sAqk = sKtT + 32768;
         TRACE(j, 0);
         if (!mbar_wait(&full1, par, &abort_flag, p.status, kDevTimeoutTma)) break;
         if (!mbar_wait(&sready, par, &abort_flag, p.status, kDevTimeoutSync)) break;
         TRACE(j, 1);
         tc_fence_after();
-        for (int s = 0; s < 16; ++s) mma_tf32_ts(tb + kTP, tb + kTST + s * 8, desc_kmajor(sW, 8192, s), id64, s > 0);
+        for (int s = 0; s < 16; ++s) mma_tf32_ts(tPV, tb + kTST + s * 8, desc_kmajor(sWQ, 16384, s), id_first, s > 0);
         mma_commit(&mma1);
-        if (outs)
-          for (int s = 0; s < 16; ++s) mma_tf32_ts(tO, tb + kTST + s * 8, desc_kmajor(sQt, 8192, s), id64, s > 0);
-        mma_commit(&mma1b);
-        if (!mbar_wait(&mma1b, par, &abort_flag, p.status, kDevTimeoutMma)) break;
+        if (!mbar_wait(&mma1, par, &abort_flag, p.status, kDevTimeoutMma)) break;
         TRACE(j, 2);
         if (j + 1 < nc) load_g1(c + 1);
         if (!mbar_wait(&vready, par, &abort_flag, p.status, kDevTimeoutSync)) break;
@@ -207,10 +211,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!mbar_wait(&full3[st], (j >> 1) & 1, &abort_flag, p.status, kDevTimeoutTma)) break;
         TRACE(j, 4);
         tc_fence_after();
-        for (int s = 0; s < 8; ++s) mma_tf32_ts(tb + kTSM, tb + kTVN + s * 8, desc_kmajor(sKtT, 16384, s), id128, true);
+        for (int s = 0; s < 8; ++s) mma_tf32_ts(tb + kTSM, tPV + s * 8, desc_kmajor(sKtT, 16384, s), id128, true);
         mma_commit(&mma2);
         if (outs)
-          for (int s = 0; s < 8; ++s) mma_tf32_ts(tO, tb + kTVN + s * 8, desc_kmajor(sAqk, 8192, s), id64, true);
+          for (int s = 0; s < 8; ++s) mma_tf32_ts(tO, tPV + s * 8, desc_kmajor(sAqk, 8192, s), id64, true);
         mma_commit(&mma3);
         if (!mbar_wait(&mma3, par, &abort_flag, p.status, kDevTimeoutMma)) break;
         TRACE(j, 5);
@@ -261,37 +265,50 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int t = 0; t < 32; ++t) u[t] = 0.f;
       }
       if (!mbar_wait(&mma1, par, &abort_flag, p.status, kDevTimeoutMma)) { alive = false; break; }
+      if (tid == 0) TRACE(j, 8);
       tc_fence_after();
       {
         float r[32];
-        tmem_ld32(tb + lb + kTP + t0, r);
+        tmem_ld32(tb + lb + tpv(j) + t0, r);
         tmem_wait_ld_regs(r);
 #pragma unroll
         for (int t = 0; t < 32; ++t) r[t] = to_tf32(u[t] - r[t]);
-        tmem_st32(tb + lb + kTVN + t0, r);
+        tmem_st32(tb + lb + tpv(j) + t0, r);
         tmem_wait_st();
         tc_fence_before();
         mbar_arrive(&vready);
+        if (tid == 0) TRACE(j, 9);
         if (vnew_save) {
           float* vsave = vnew_save + tile * kTileW + size_t(t0) * kD + v;
 #pragma unroll
           for (int t = 0; t < 32; ++t) vsave[size_t(t) * kD] = r[t];
         }
       }
+      if (tid == 0) TRACE(j, 10);
       if (!mbar_wait(&mma2, par, &abort_flag, p.status, kDevTimeoutMma)) { alive = false; break; }
+      if (tid == 0) TRACE(j, 11);
       tc_fence_after();
       if (j + 1 < nc) chain_state_pass(p, h_save, c + 1, h, v, k0, tb + lb, &sready, gnext);
+      if (tid == 0) TRACE(j, 12);
       if (o) {
         if (!mbar_wait(&mma3, par, &abort_flag, p.status, kDevTimeoutMma)) { alive = false; break; }
         tc_fence_after();
-        const uint32_t tO = tb + kTO + (j & 1) * 64;
         float r[32];
-        tmem_ld32(tO + lb + t0, r);
+        tmem_ld32(tb + lb + tout(j) + t0, r);
         tmem_wait_ld_regs(r);
-        __nv_bfloat16* op = o + (size_t(ch.x + t0) * H + h) * kD + v;
+        // lane pairs (v, v^1) swap halves so each lane stores two adjacent bf16 of a row: the
+        // even lane rows t0..t0+15, the odd lane rows t0+16..t0+31
+        const int odd = v & 1;
+        __nv_bfloat162* op = reinterpret_cast<__nv_bfloat162*>(o + (size_t(ch.x + t0 + 16 * odd) * H + h) * kD + (v & ~1));
 #pragma unroll
-        for (int t = 0; t < 32; ++t)
-          if (t0 + t < ch.y) op[size_t(t) * H * kD] = __float2bfloat16_rn(r[t]);
+        for (int t = 0; t < 16; ++t) {
+          const float mine = odd ? r[16 + t] : r[t];
+          const float give = odd ? r[t] : r[16 + t];
+          const float other = __shfl_xor_sync(0xffffffffu, give, 1);
+          const __nv_bfloat162 pr = odd ? __floats2bfloat162_rn(other, mine) : __floats2bfloat162_rn(mine, other);
+          if (t0 + 16 * odd + t < ch.y) op[size_t(t) * H * kD / 2] = pr;
+        }
+        if (tid == 0) TRACE(j, 13);
       }
     }
     // exit state: the final state, the next segment's entry (pass 0), or the segment's map

@@ -27,9 +27,13 @@ namespace gdn {
 
 #ifdef GDN_TRACE
 // Optional timeline of the first CTA (compiled only with -DGDN_TRACE; never in the library).
-__device__ unsigned long long g_trace_rev[64 * 8];
+__device__ unsigned long long g_trace_rev[64 * 16];
+__device__ int g_trace_rev_block = 0;
+extern "C" int g_trace_rev_set_block(int b) {
+  return cudaMemcpyToSymbol(g_trace_rev_block, &b, sizeof(int)) == cudaSuccess ? 0 : -1;
+}
 #define RTRACE(j, slot) \
-  do { if (blockIdx.x == 0 && blockIdx.y == 0 && (j) < 64) g_trace_rev[(j) * 8 + (slot)] = globaltimer(); } while (0)
+  do { if (blockIdx.x == g_trace_rev_block && blockIdx.y == 0 && (j) < 64) g_trace_rev[(j) * 16 + (slot)] = globaltimer(); } while (0)
 extern "C" int gdn_trace_rev_read(unsigned long long* host) {
   return cudaMemcpyFromSymbol(host, g_trace_rev, sizeof(g_trace_rev)) == cudaSuccess ? 0 : -1;
 }
@@ -73,7 +77,7 @@ __device__ __forceinline__ void load_dO(const RevChainParams& p, int c, int h, i
 // issuer, then save dS' (its tf32 copy) for the feature-major backward kernel.
 __device__ __forceinline__ void rev_pass(const RevChainParams& p, float* dh_save, bool use_do, int c, int h,
                                          int v, int k0, int t0, uint32_t tl, uint64_t* ready, const uint32_t* d,
-                                         float g0) {
+                                         float g0, int jt = 63) {
   const size_t tile = size_t(c) * p.H + h;
   float s[64];
   tmem_ld64(tl + kTDM + k0, s);
@@ -101,6 +105,7 @@ __device__ __forceinline__ void rev_pass(const RevChainParams& p, float* dh_save
   }
   tmem_st32(tl + kTDM + k0, s);
   tmem_st32(tl + kTDM + k0 + 32, s + 32);
+  if (threadIdx.x == 0) RTRACE(jt, 9);
   if (use_do) {
     float df[32];
 #pragma unroll
@@ -113,6 +118,7 @@ __device__ __forceinline__ void rev_pass(const RevChainParams& p, float* dh_save
   tmem_wait_st();
   tc_fence_before();
   mbar_arrive(ready);
+  if (threadIdx.x == 0) RTRACE(jt, 10);
   if (!dh_save) return;
   // re-read the tf32 copy (the MMAs only read it) and save it
   tmem_ld64(tl + kTDT + k0, s);
@@ -127,7 +133,7 @@ __device__ __forceinline__ void rev_pass(const RevChainParams& p, float* dh_save
 __global__ void __launch_bounds__(kThreads, 1)
     k_chain_bwd(const __grid_constant__ CUtensorMap mKt, const __grid_constant__ CUtensorMap mAqkT,
                 const __grid_constant__ CUtensorMap mQtT, const __grid_constant__ CUtensorMap mWT,
-                const RevChainParams p) {
+                const __grid_constant__ CUtensorMap mdO, const RevChainParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = align1k(smem_raw);
   __shared__ uint64_t full[2], mma1, mma2, dready, vready;
@@ -182,8 +188,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           tma_load_2d(base + kOffWT + pp * 16384, &mWT, pp * 32, y128, &full[st]);
         }
       };
+      // dO rows of a chunk into L2 ahead of the chain warps' loads of them
+      auto prefetch_do = [&](int c) {
+        const int row = p.chunks[c].x;
+        prefetch_l2_tile(&mdO, h * kD, row);
+        prefetch_l2_tile(&mdO, h * kD + 64, row);
+      };
       load(last, 0);
       if (nc > 1) load(last - 1, 1);
+      if (use_do && nc > 1) prefetch_do(last - 1);
+      if (use_do && nc > 2) prefetch_do(last - 2);
       const uint32_t id64 = idesc_tf32(128, 64), id128 = idesc_tf32(128, 128);
       for (int j = 0; j < nc; ++j) {
         const int c = last - j, st = j & 1;
@@ -211,6 +225,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // dS^T += (-dv_new^T) W
         for (int s = 0; s < 8; ++s) mma_tf32_ts(tb + kTDM, tb + kTDN + s * 8, desc_kmajor(base + kOffWT, 16384, s), id128, true);
         mma_commit(&mma2);
+        if (use_do && j + 3 < nc) prefetch_do(c - 3);
         if (!mbar_wait(&mma2, par, &abort_flag, p.status, kDevTimeoutMma)) break;
         RTRACE(j, 4);
         if (j + 2 < nc) load(c - 2, st);
@@ -237,10 +252,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_st32(tl + kTDM + k0 + 32, buf + 32);
       tmem_wait_st();
     }
+    // dO of the chunk after the one being prepared is loaded a whole step ahead of its use
     uint32_t dnext[16];
     if (use_do) load_dO(p, last, h, v, t0, dnext);
     rev_pass(p, dh_save, use_do, last, h, v, k0, t0, tl, &dready, dnext,
              p.kda ? 0.f : p.gam[(size_t(last) * H + h) * kD]);
+    if (use_do && nc > 1) load_dO(p, last - 1, h, v, t0, dnext);
     bool alive = true;
     for (int j = 0; j < nc; ++j) {
       const int c = last - j;
@@ -268,11 +285,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int t = 0; t < 32; ++t) dv[size_t(t) * kD] = -r[t];
         }
       }
-      // prefetch the next chunk's dO while the second MMA group runs
-      if (j + 1 < nc && use_do) load_dO(p, c - 1, h, v, t0, dnext);
       if (!mbar_wait(&mma2, par, &abort_flag, p.status, kDevTimeoutMma)) { alive = false; break; }
+      if (tid == 0) RTRACE(j, 8);
       tc_fence_after();
-      if (j + 1 < nc) rev_pass(p, dh_save, use_do, c - 1, h, v, k0, t0, tl, &dready, dnext, gnext);
+      if (j + 1 < nc) {
+        rev_pass(p, dh_save, use_do, c - 1, h, v, k0, t0, tl, &dready, dnext, gnext, j);
+        if (use_do && j + 2 < nc) load_dO(p, c - 2, h, v, t0, dnext);
+      }
+      if (tid == 0) RTRACE(j, 11);
     }
     // exit gradient: dh0, the next segment's seed (pass 0), or the segment's map
     float* dst = nullptr;
@@ -310,7 +330,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 cudaError_t launch_chain_bwd(const CUtensorMap& mKt, const CUtensorMap& mAqkT, const CUtensorMap& mQtT,
-                             const CUtensorMap& mWT, const RevChainParams& p, cudaStream_t s) {
+                             const CUtensorMap& mWT, const CUtensorMap& mdO, const RevChainParams& p,
+                             cudaStream_t s) {
   static bool attr = false;
   if (!attr) {
     cudaError_t e = cudaFuncSetAttribute(k_chain_bwd, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
@@ -318,7 +339,7 @@ cudaError_t launch_chain_bwd(const CUtensorMap& mKt, const CUtensorMap& mAqkT, c
     attr = true;
   }
   dim3 grid(p.N * runs_per_seq(p.sp.maxS, p.sp.pass), p.H);
-  k_chain_bwd<<<grid, kThreads, kSmemBytes, s>>>(mKt, mAqkT, mQtT, mWT, p);
+  k_chain_bwd<<<grid, kThreads, kSmemBytes, s>>>(mKt, mAqkT, mQtT, mWT, mdO, p);
   return cudaGetLastError();
 }
 

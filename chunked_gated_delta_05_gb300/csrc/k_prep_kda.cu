@@ -55,14 +55,16 @@ __device__ __forceinline__ void inverse_column(const float* __restrict__ LT, flo
   for (int b = 0; b < 4; ++b) {
     const int r0 = 16 * b;
     float x[16];
-    if (r0 + 15 < c) {
+    if (r0 + 15 < (c & ~31)) {  // above the diagonal for the whole warp
 #pragma unroll
       for (int e = 0; e < 16; ++e) x[e] = 0.f;
     } else {
       float y[16];
 #pragma unroll
       for (int e = 0; e < 16; ++e) y[e] = 0.f;
-      for (int j = c; j < r0; ++j) {
+      // warp-uniform rows (the warp's columns share c & ~31; X[j][c] = 0 for j < c is already
+      // in sX), so every L^T row read is a broadcast
+      for (int j = c & ~31; j < r0; ++j) {
         const float xj = sX[j * kC + c];
         const float4* l4 = reinterpret_cast<const float4*>(LT + j * kC + r0);
 #pragma unroll

@@ -32,8 +32,8 @@
  *
  * Ownership. Every pointer in the argument structs is a DEVICE pointer owned by the caller,
  * except cu_seqlens (HOST). The library never allocates or frees memory: the caller passes a
- * device workspace of at least *_workspace_size() bytes (256-byte aligned). q, k, v (and dO
- * in the backward) must be 16-byte aligned (they are read by tensor-memory-access copies).
+ * device workspace of at least *_workspace_size() bytes (256-byte aligned). q, k, v, o (and
+ * dO in the backward) must be 16-byte aligned (tensor-memory-access copies and paired stores).
  * No output may alias an input. cu_seqlens is read during the call only.
  *
  * Asynchrony and errors. Validation is host-side and synchronous; on success the work is
