@@ -37,6 +37,7 @@ KERNEL_FLOP_PER_CHUNK_HEAD = {
     "bwd_tok": (2 * 64 * 64 * 128 * 3 + 2 * 64 * 64 * 256 + 2 * 2 * 64 * 64 * 64 + 4 * 2 * 64 * 64 * 128, "tf32"),
     "tables": (0, "none"),
     "compose": (0, "none"),     # segmented-chain overhead: no algorithmic work of its own
+    "group_sum": (0, "none"),   # grouped q/k heads only
 }
 TF32_OVER_BF16 = 1.1 / 2.25    # nominal dense tf32 / bf16 tensor rates of a GB300
 # DRAM bytes (read + write) of one step's launches of a kernel, from an `ncu --set full`

@@ -16,7 +16,7 @@ class Desc(ctypes.Structure):
     _fields_ = [("B", c_int), ("T", c_int), ("H", c_int), ("K", c_int), ("V", c_int),
                 ("chunk_size", c_int), ("cu_seqlens", ctypes.POINTER(ctypes.c_int32)),
                 ("num_seqs", c_int), ("scale", c_float), ("use_qk_l2norm", c_int),
-                ("use_beta_sigmoid", c_int), ("output_final_state", c_int)]
+                ("use_beta_sigmoid", c_int), ("output_final_state", c_int), ("num_k_heads", c_int)]
 
 
 class FwdArgs(ctypes.Structure):

@@ -60,6 +60,7 @@ bool make_map(CUtensorMap* m, const void* base, CUtensorMapDataType dt, uint64_t
 
 struct Problem {
   int B, T, H, N, NC, R;
+  int Hk, G;                // q/k heads and value heads per q/k head
   float scale;
   bool packed;
   std::vector<int32_t> cu;  // packed offsets (host copy)
@@ -74,6 +75,10 @@ int validate_desc(const gdn_desc_t* d, Problem* P) {
   P->B = d->B;
   P->T = d->T;
   P->H = d->H;
+  if (d->num_k_heads < 0 || (d->num_k_heads > 0 && d->H % d->num_k_heads != 0))
+    return fail(GDN_EINVAL, "num_k_heads must be 0 or divide H");
+  P->Hk = d->num_k_heads > 0 ? d->num_k_heads : d->H;
+  P->G = d->H / P->Hk;
   P->scale = d->scale > 0.f ? d->scale : 1.0f / std::sqrt(float(d->K));
   P->packed = d->cu_seqlens != nullptr;
   const long long R = (long long)d->B * d->T;
@@ -183,6 +188,7 @@ struct Layout {
   size_t fE, fPhi, fPlo, fB;                                       // forward chain scan (scratch)
   size_t dhs, dvns, dQt, dKt, dW, dK1, dV1, dgam;                  // rest part (relative)
   size_t rE, rPhi, rPlo, rB;                                       // reverse chain scan (rest part)
+  size_t dq32, dk32;                                               // grouped q/k: per-value-head dq, dk
   size_t saved_total, rest_total, total;
   ScanPlan plan;
 };
@@ -239,6 +245,9 @@ Layout make_layout(const Problem& P, bool backward, bool kda = false) {
     L.rPhi = take(scan_states);
     L.rPlo = take(scan_states);
     L.rB = take(scan_states);
+    const size_t per_head = P.G > 1 ? size_t(P.R) * P.H * kD * 4 : 0;
+    L.dq32 = take(per_head);
+    L.dk32 = take(per_head);
   }
   L.rest_total = off;
   L.total = L.saved_total + L.rest_total;
@@ -279,9 +288,9 @@ int check_cuda(cudaError_t e, const char* what) {
 
 // Optional per-kernel timing (CUDA events recorded on the launching stream around every
 // launch while enabled). Process-global and not thread-safe: a profiling aid.
-enum KernelKind { kKTables = 0, kKPrep, kKChainFwd, kKChainBwd, kKBwdFeat, kKBwdTok, kKCompose, kKinds };
+enum KernelKind { kKTables = 0, kKPrep, kKChainFwd, kKChainBwd, kKBwdFeat, kKBwdTok, kKCompose, kKGroupSum, kKinds };
 const char* const kKindNames[kKinds] = {"tables", "prepare", "chain_fwd", "chain_bwd", "bwd_feat", "bwd_tok",
-                                        "compose"};
+                                        "compose", "group_sum"};
 struct Timing {
   bool on = false;
   std::vector<std::pair<cudaEvent_t, cudaEvent_t>> ev[kKinds];
@@ -325,10 +334,10 @@ bool tile_map(CUtensorMap* m, const char* base, uint64_t cols, uint64_t rows, ui
 bool backward_tiles(const Layout& L) { return L.Kt != 0; }
 
 bool fwd_maps(const Problem& P, const void* q, const void* k, const void* v, const char* ws, const Layout& L, Maps* M) {
-  const uint64_t HD = uint64_t(P.H) * kD;
+  const uint64_t HD = uint64_t(P.H) * kD, HDk = uint64_t(P.Hk) * kD;
   const uint64_t r64 = uint64_t(P.NC) * P.H * kC, r128 = uint64_t(P.NC) * P.H * kD;
-  return make_map(&M->q, q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, HD, P.R, HD * 2, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B) &&
-         make_map(&M->k, k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, HD, P.R, HD * 2, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B) &&
+  return make_map(&M->q, q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, HDk, P.R, HDk * 2, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B) &&
+         make_map(&M->k, k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, HDk, P.R, HDk * 2, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B) &&
          make_map(&M->v, v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, HD, P.R, HD * 2, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B) &&
          tile_map(&M->W, ws + L.W, kD, r64, 64, true) && tile_map(&M->Qt, ws + L.Qt, kD, r64, 64, true) &&
          tile_map(&M->U, ws + L.U, kD, r64, 64, false) && tile_map(&M->Usw, ws + L.U, kD, r64, 64, true) &&
@@ -358,6 +367,7 @@ PrepParams prep_params(const gdn_desc_t* d, const Problem& P, char* sv, const La
   pp.scale = P.scale;
   pp.l2norm = d->use_qk_l2norm;
   pp.beta_sigmoid = d->use_beta_sigmoid;
+  pp.qk_group = P.G;
   pp.W = F(L.W); pp.U = F(L.U); pp.Qt = F(L.Qt); pp.KtT = F(L.KtT); pp.Aqk = F(L.Aqk); pp.gam = F(L.gam);
   if (backward) {
     pp.Gc = F(L.Gc); pp.rq = F(L.rq); pp.rk = F(L.rk); pp.beff = F(L.beff);
@@ -465,8 +475,8 @@ int run_fwd(const gdn_desc_t* d, const gdn_fwd_args_t* a, void* stream, bool kda
   if (d->output_final_state && !a->final_state) return fail(GDN_EINVAL, "final_state is NULL but requested");
   if (!aligned16(a->q) || !aligned16(a->k) || !aligned16(a->v) || !aligned16(a->o))
     return fail(GDN_EINVAL, "q, k, v and o must be 16-byte aligned");
-  const size_t nqk = size_t(P.R) * P.H * kD * 2;
-  if (overlaps(a->o, nqk, a->q, nqk) || overlaps(a->o, nqk, a->k, nqk) || overlaps(a->o, nqk, a->v, nqk))
+  const size_t nqk = size_t(P.R) * P.Hk * kD * 2, nv = size_t(P.R) * P.H * kD * 2;
+  if (overlaps(a->o, nv, a->q, nqk) || overlaps(a->o, nv, a->k, nqk) || overlaps(a->o, nv, a->v, nv))
     return fail(GDN_EINVAL, "o must not alias q, k or v");
   const bool training = a->saved != nullptr;
   const Layout L = make_layout(P, training, kda);
@@ -524,14 +534,18 @@ int run_bwd(const gdn_desc_t* d, const gdn_bwd_args_t* a, void* stream, bool kda
   if (!a) return fail(GDN_EINVAL, "args is NULL");
   if (!a->q || !a->k || !a->v || !a->g || !a->beta || !a->dO || !a->dq || !a->dk || !a->dv || !a->dbeta || !a->dg)
     return fail(GDN_EINVAL, "q, k, v, g, beta, dO and every gradient output except dh0 must be non-NULL");
-  if (!aligned16(a->q) || !aligned16(a->k) || !aligned16(a->v) || !aligned16(a->dO))
-    return fail(GDN_EINVAL, "q, k, v and dO must be 16-byte aligned");
-  const size_t nqk = size_t(P.R) * P.H * kD * 2;
+  if (!aligned16(a->q) || !aligned16(a->k) || !aligned16(a->v) || !aligned16(a->dO) || !aligned16(a->dq) ||
+      !aligned16(a->dk) || !aligned16(a->dv))
+    return fail(GDN_EINVAL, "q, k, v, dO, dq, dk and dv must be 16-byte aligned");
+  const size_t nqk = size_t(P.R) * P.Hk * kD * 2, nv = size_t(P.R) * P.H * kD * 2;
   const void* ins[] = {a->q, a->k, a->v, a->dO};
+  const size_t in_bytes[] = {nqk, nqk, nv, nv};
   const void* outs[] = {a->dq, a->dk, a->dv};
-  for (const void* o : outs)
-    for (const void* i : ins)
-      if (overlaps(o, nqk, i, nqk)) return fail(GDN_EINVAL, "gradient outputs must not alias the inputs");
+  const size_t out_bytes[] = {nqk, nqk, nv};
+  for (int oi = 0; oi < 3; ++oi)
+    for (int ii = 0; ii < 4; ++ii)
+      if (overlaps(outs[oi], out_bytes[oi], ins[ii], in_bytes[ii]))
+        return fail(GDN_EINVAL, "gradient outputs must not alias the inputs");
   const Layout L = make_layout(P, true, kda);
   const bool have_saved = a->saved != nullptr;
   if (have_saved) {
@@ -645,10 +659,28 @@ int run_bwd(const gdn_desc_t* d, const gdn_bwd_args_t* a, void* stream, bool kda
   tp.status = a->status;
   tp.kda = kda ? 1 : 0;
   tp.sms = fp.sms;
-  TimedLaunch tl_(kKBwdTok, s);
-  return check_cuda(kda ? launch_bwd_tok_kda(M.q, M.k, M.v, M.VN, M.DW, M.DVN, tp, s)
+  tp.qk_group = P.G;
+  if (P.G > 1) {
+    tp.dq32 = R(L.dq32);
+    tp.dk32 = R(L.dk32);
+  }
+  {
+    TimedLaunch tl_(kKBwdTok, s);
+    rc = check_cuda(kda ? launch_bwd_tok_kda(M.q, M.k, M.v, M.VN, M.DW, M.DVN, tp, s)
                         : launch_bwd_tok(M.q, M.k, M.v, M.dO, M.VN, M.DW, M.DVN, tp, s),
                     "token-major backward kernel");
+  }
+  if (rc || P.G == 1) return rc;
+  GroupSumParams gp{};
+  gp.dq32 = tp.dq32;
+  gp.dk32 = tp.dk32;
+  gp.dq = tp.dq;
+  gp.dk = tp.dk;
+  gp.R = P.R;
+  gp.H = P.H;
+  gp.G = P.G;
+  TimedLaunch tl_(kKGroupSum, s);
+  return check_cuda(launch_group_sum(gp, s), "group sum kernel");
 }
 
 }  // namespace

@@ -83,6 +83,7 @@ struct PrepParams {
   const __nv_bfloat16* beta;   // [R,H]
   float scale;
   int l2norm, beta_sigmoid;
+  int qk_group;                // value heads per q/k head (q/k head of value head h: h / qk_group)
   float *W, *U, *Qt, *KtT, *Aqk, *gam;
   float *Gc, *rq, *rk, *beff;  // optional per-token saves [NC*H*64] (KDA Gc: [NC*H*64*128]); may be null
   // Backward-only tiles (all null in the forward):
@@ -163,6 +164,8 @@ struct BwdTokParams {
   const float *gam, *dgam;     // [NC,H,128]
   __nv_bfloat16 *dq, *dk, *dv, *dbeta;
   float* dg;
+  int qk_group;                // value heads per q/k head
+  float *dq32, *dk32;          // qk_group > 1: per-value-head dq, dk [R,H,K] fp32 (summed later)
   int sms;                     // SM count (the distance to the next wave's CTA for prefetching)
   int* status;
 };
@@ -186,6 +189,13 @@ cudaError_t launch_bwd_tok(const CUtensorMap& mq, const CUtensorMap& mk, const C
 cudaError_t launch_bwd_tok_kda(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
                                const CUtensorMap& mVN, const CUtensorMap& mDW, const CUtensorMap& mDVN,
                                const BwdTokParams& p, cudaStream_t s);
+struct GroupSumParams {
+  const float *dq32, *dk32;    // [R,H,K]
+  __nv_bfloat16 *dq, *dk;      // [R,H/G,K]
+  long long R;
+  int H, G;
+};
+
 struct ComposeParams {
   const SeqEntry* seqs;
   int N, H;
@@ -193,6 +203,7 @@ struct ComposeParams {
   int* status;
 };
 
+cudaError_t launch_group_sum(const GroupSumParams& p, cudaStream_t s);
 cudaError_t launch_compose(const CUtensorMap& mPhi, const CUtensorMap& mPlo, const CUtensorMap& mB,
                            const ComposeParams& p, cudaStream_t s);
 cudaError_t launch_chain_fwd(const CUtensorMap& mW, const CUtensorMap& mQt, const CUtensorMap& mKtT,

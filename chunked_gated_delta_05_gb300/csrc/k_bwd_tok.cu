@@ -129,9 +129,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (tid == 0) {
     mbar_expect_tx(&bar_tma, 4u * 16384u + 3u * 32768u);
     for (int pp = 0; pp < 2; ++pp) {
-      const int x = h * kD + 64 * pp;
-      tma_load_2d(sQ + pp * 8192, &mq, x, ch.x, &bar_tma);
-      tma_load_2d(sK + pp * 8192, &mk, x, ch.x, &bar_tma);
+      const int x = h * kD + 64 * pp, xqk = (h / p.qk_group) * kD + 64 * pp;
+      tma_load_2d(sQ + pp * 8192, &mq, xqk, ch.x, &bar_tma);
+      tma_load_2d(sK + pp * 8192, &mk, xqk, ch.x, &bar_tma);
       tma_load_2d(sV + pp * 8192, &mv, x, ch.x, &bar_tma);
       tma_load_2d(sm + kOffDO + pp * 8192, &mdO, x, ch.x, &bar_tma);
     }
@@ -421,6 +421,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.y));
       f[0] = a.x; f[1] = a.y; f[2] = b.x; f[3] = b.y;
     };
+    // dq, dk: bf16 at [R,Hk,K] directly, or fp32 per value head [R,H,K] for the group sum
+    const int Hk = H / p.qk_group;
+    auto store_qk = [&](__nv_bfloat16* dst16, float* dst32, int t, const float* x) {
+      if (dst32) {
+        *reinterpret_cast<float4*>(dst32 + (size_t(ch.x + t) * H + h) * kD + d0) = make_float4(x[0], x[1], x[2], x[3]);
+      } else {
+        __nv_bfloat162 a = __floats2bfloat162_rn(x[0], x[1]), b = __floats2bfloat162_rn(x[2], x[3]);
+        uint2 u;
+        u.x = *reinterpret_cast<uint32_t*>(&a);
+        u.y = *reinterpret_cast<uint32_t*>(&b);
+        *reinterpret_cast<uint2*>(dst16 + (size_t(ch.x + t) * Hk + h) * kD + d0) = u;
+      }
+    };
     auto store4 = [&](__nv_bfloat16* dst, const float* x) {
       __nv_bfloat162 a = __floats2bfloat162_rn(x[0], x[1]), b = __floats2bfloat162_rn(x[2], x[3]);
       uint2 u;
@@ -475,7 +488,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!p.l2norm) dot = 0.f;
 #pragma unroll
         for (int e = 0; e < 4; ++e) x[e] = rqt * (a[e] - rqt * qv[e] * dot);
-        store4(p.dq + orow, x);
+        store_qk(p.dq, p.dq32, t, x);
         // dk
         float kv[4];
         bf4(sK, t, kv);
@@ -499,7 +512,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!p.l2norm) kdot = 0.f;
 #pragma unroll
         for (int e = 0; e < 4; ++e) x[e] = rkt * (a[e] - rkt * kv[e] * kdot);
-        store4(p.dk + orow, x);
+        store_qk(p.dk, p.dk32, t, x);
         // dv and the v part of dbeta
         float vv4[4];
         bf4(sV, t, vv4);

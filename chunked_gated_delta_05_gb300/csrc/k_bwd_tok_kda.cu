@@ -100,9 +100,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (tid == 0) {
     mbar_expect_tx(&bar_tma, 3u * 16384u + 3u * 32768u);
     for (int pp = 0; pp < 2; ++pp) {
-      const int x = h * kD + 64 * pp;
-      tma_load_2d(sQ + pp * 8192, &mq, x, ch.x, &bar_tma);
-      tma_load_2d(sK + pp * 8192, &mk, x, ch.x, &bar_tma);
+      const int x = h * kD + 64 * pp, xqk = (h / p.qk_group) * kD + 64 * pp;
+      tma_load_2d(sQ + pp * 8192, &mq, xqk, ch.x, &bar_tma);
+      tma_load_2d(sK + pp * 8192, &mk, xqk, ch.x, &bar_tma);
       tma_load_2d(sV + pp * 8192, &mv, x, ch.x, &bar_tma);
     }
     for (int pp = 0; pp < 4; ++pp) {
@@ -335,9 +335,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float qh = rq * bf16_at(sQ, t, cc), kh = rk * bf16_at(sK, t, cc);
     const float dq = p.l2norm ? rq * (sQacc[t * kD + cc] - qh * s_dotq[t]) : sQacc[t * kD + cc];
     const float dk = p.l2norm ? rk * (sKacc[t * kD + cc] - kh * s_dotk[t]) : sKacc[t * kD + cc];
-    const size_t o = (size_t(ch.x + t) * H + h) * kD + cc;
-    p.dq[o] = __float2bfloat16_rn(dq);
-    p.dk[o] = __float2bfloat16_rn(dk);
+    if (p.dq32) {  // per value head, summed over the q/k group later
+      const size_t o = (size_t(ch.x + t) * H + h) * kD + cc;
+      p.dq32[o] = dq;
+      p.dk32[o] = dk;
+    } else {
+      const size_t o = (size_t(ch.x + t) * (H / p.qk_group) + h) * kD + cc;
+      p.dq[o] = __float2bfloat16_rn(dq);
+      p.dk[o] = __float2bfloat16_rn(dk);
+    }
   }
   if (half == 0) {
     float acc = s_glast[0][cc] + s_glast[1][cc] + exp2f(glc) * p.dgam[tile * kD + cc];

@@ -162,9 +162,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int b = 0; b < 2; ++b) {
       if (s_chunk[b].y <= 0) continue;
       for (int pp = 0; pp < 2; ++pp) {
-        const int x = h * kD + 64 * pp, y = s_chunk[b].x;
-        tma_load_2d(sQ + pp * kPanel + b * 8192, &mq, x, y, &bar_tma);
-        tma_load_2d(sK + pp * kPanel + b * 8192, &mk, x, y, &bar_tma);
+        const int x = h * kD + 64 * pp, xqk = (h / p.qk_group) * kD + 64 * pp, y = s_chunk[b].x;
+        tma_load_2d(sQ + pp * kPanel + b * 8192, &mq, xqk, y, &bar_tma);
+        tma_load_2d(sK + pp * kPanel + b * 8192, &mk, xqk, y, &bar_tma);
         tma_load_2d(sV + pp * kPanel + b * 8192, &mv, x, y, &bar_tma);
       }
     }

@@ -127,9 +127,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (tid == 0) {
     mbar_expect_tx(&bar_tma, 3u * 16384u);
     for (int pp = 0; pp < 2; ++pp) {
-      const int x = h * kD + 64 * pp;
-      tma_load_2d(sQ + pp * 8192, &mq, x, ch.x, &bar_tma);
-      tma_load_2d(sK + pp * 8192, &mk, x, ch.x, &bar_tma);
+      const int x = h * kD + 64 * pp, xqk = (h / p.qk_group) * kD + 64 * pp;
+      tma_load_2d(sQ + pp * 8192, &mq, xqk, ch.x, &bar_tma);
+      tma_load_2d(sK + pp * 8192, &mk, xqk, ch.x, &bar_tma);
       tma_load_2d(sV + pp * 8192, &mv, x, ch.x, &bar_tma);
     }
   }

@@ -49,9 +49,10 @@ def _offsets(cu_seqlens, T):
     return (ctypes.c_int32 * len(vals))(*vals), len(vals) - 1
 
 
-def _desc(B, T, H, scale, l2, sig, final, offsets):
+def _desc(B, T, H, scale, l2, sig, final, offsets, Hk=None):
     d = _lib.Desc()
     d.B, d.T, d.H, d.K, d.V, d.chunk_size = B, T, H, K_DIM, K_DIM, CHUNK
+    d.num_k_heads = 0 if Hk is None or Hk == H else int(Hk)
     if offsets is not None:
         arr, n = offsets
         d.cu_seqlens = ctypes.cast(arr, ctypes.POINTER(ctypes.c_int32))
@@ -64,30 +65,35 @@ def _desc(B, T, H, scale, l2, sig, final, offsets):
 
 
 def _common_checks(q, k, v, g, beta, per_channel, offsets):
-    if q.dim() != 4:
-        raise ValueError("q must have shape [B,T,H,K]")
-    B, T, H, K = q.shape
+    """Shapes: q, k [B,T,Hk,K]; v [B,T,H,V] with Hk dividing H (grouped q/k heads when
+    Hk < H); g [B,T,H] or [B,T,H,K]; beta [B,T,H]. Returns (B, T, H, Hk, N, device)."""
+    if q.dim() != 4 or v.dim() != 4:
+        raise ValueError("q and v must have shape [B,T,H,D]")
+    B, T, Hk, K = q.shape
+    H = v.shape[2]
     dev = q.device
     if dev.type != "cuda":
         raise ValueError("inputs must be CUDA tensors")
-    _check_tensor("q", q, torch.bfloat16, (B, T, H, K), dev)
-    _check_tensor("k", k, torch.bfloat16, (B, T, H, K), dev)
-    _check_tensor("v", v, torch.bfloat16, (B, T, H, v.shape[-1] if v.dim() == 4 else -1), dev)
+    if H % Hk != 0:
+        raise ValueError("the value heads must be a multiple of the q/k heads")
+    _check_tensor("q", q, torch.bfloat16, (B, T, Hk, K), dev)
+    _check_tensor("k", k, torch.bfloat16, (B, T, Hk, K), dev)
+    _check_tensor("v", v, torch.bfloat16, (B, T, H, v.shape[-1]), dev)
     gshape = (B, T, H, K) if per_channel else (B, T, H)
     _check_tensor("g", g, torch.float32, gshape, dev)
     _check_tensor("beta", beta, torch.bfloat16, (B, T, H), dev)
     N = B if offsets is None else offsets[1]
-    return B, T, H, N, dev
+    return B, T, H, Hk, N, dev
 
 
 def _fwd(per_channel, q, k, v, g, beta, initial_state, output_final_state, use_qk_l2norm,
          use_beta_sigmoid, cu_seqlens, scale, status, save=False):
     lib = _lib.load()
     offsets = _offsets(cu_seqlens, q.shape[1] if q.dim() == 4 else 0)
-    B, T, H, N, dev = _common_checks(q, k, v, g, beta, per_channel, offsets)
+    B, T, H, Hk, N, dev = _common_checks(q, k, v, g, beta, per_channel, offsets)
     if initial_state is not None:
         _check_tensor("initial_state", initial_state, torch.float32, (N, H, K_DIM, K_DIM), dev)
-    desc = _desc(B, T, H, scale, use_qk_l2norm, use_beta_sigmoid, output_final_state, offsets)
+    desc = _desc(B, T, H, scale, use_qk_l2norm, use_beta_sigmoid, output_final_state, offsets, Hk)
     if save:
         size_fn = lib.kda_saved_size if per_channel else lib.gdn_saved_size
     else:
@@ -95,7 +101,7 @@ def _fwd(per_channel, q, k, v, g, beta, initial_state, output_final_state, use_q
     ws_bytes = size_fn(ctypes.byref(desc))
     if ws_bytes == 0:
         _lib.check(_lib.GDN_EINVAL)
-    o = torch.empty((B, T, H, K_DIM), dtype=torch.bfloat16, device=dev)
+    o = torch.empty((B, T, H, K_DIM), dtype=torch.bfloat16, device=dev)  # value heads
     final = torch.empty((N, H, K_DIM, K_DIM), dtype=torch.float32, device=dev) if output_final_state else None
     buf = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
     if status is None:
@@ -116,13 +122,13 @@ def _bwd(per_channel, q, k, v, g, beta, dO, dht, initial_state, use_qk_l2norm, u
          cu_seqlens, scale, status, saved=None):
     lib = _lib.load()
     offsets = _offsets(cu_seqlens, q.shape[1] if q.dim() == 4 else 0)
-    B, T, H, N, dev = _common_checks(q, k, v, g, beta, per_channel, offsets)
+    B, T, H, Hk, N, dev = _common_checks(q, k, v, g, beta, per_channel, offsets)
     _check_tensor("dO", dO, torch.bfloat16, (B, T, H, K_DIM), dev)
     if initial_state is not None:
         _check_tensor("initial_state", initial_state, torch.float32, (N, H, K_DIM, K_DIM), dev)
     if dht is not None:
         _check_tensor("dht", dht, torch.float32, (N, H, K_DIM, K_DIM), dev)
-    desc = _desc(B, T, H, scale, use_qk_l2norm, use_beta_sigmoid, False, offsets)
+    desc = _desc(B, T, H, scale, use_qk_l2norm, use_beta_sigmoid, False, offsets, Hk)
     size_fn = lib.kda_bwd_workspace_size if per_channel else lib.gdn_bwd_workspace_size
     ws_bytes = size_fn(ctypes.byref(desc))
     if ws_bytes == 0:

@@ -33,7 +33,8 @@
  * Ownership. Every pointer in the argument structs is a DEVICE pointer owned by the caller,
  * except cu_seqlens (HOST). The library never allocates or frees memory: the caller passes a
  * device workspace of at least *_workspace_size() bytes (256-byte aligned). q, k, v, o (and
- * dO in the backward) must be 16-byte aligned (tensor-memory-access copies and paired stores).
+ * dO, dq, dk, dv in the backward) must be 16-byte aligned (tensor-memory-access copies and
+ * vector stores).
  * No output may alias an input. cu_seqlens is read during the call only.
  *
  * Asynchrony and errors. Validation is host-side and synchronous; on success the work is
@@ -71,11 +72,15 @@ typedef struct {
   int use_qk_l2norm;         /* L2-normalise q and k per token and head (eps 1e-6) */
   int use_beta_sigmoid;      /* beta holds logits; the kernel applies sigmoid */
   int output_final_state;    /* write final_state */
+  int num_k_heads;           /* heads of q and k (grouped-query layout: H value heads share them,
+                                value head h reads q/k head h / (H / num_k_heads), the pages'
+                                `repeat_interleave` of q and k, done by indexing); must divide H;
+                                0 means H. dq and dk are the sums over each group. */
 } gdn_desc_t;
 
 typedef struct {
-  const void* q;             /* bf16 [B,T,H,K] */
-  const void* k;             /* bf16 [B,T,H,K] */
+  const void* q;             /* bf16 [B,T,Hk,K] (Hk = num_k_heads, or H) */
+  const void* k;             /* bf16 [B,T,Hk,K] */
   const void* v;             /* bf16 [B,T,H,V] */
   const float* g;            /* GDN [B,T,H], KDA [B,T,H,K]: natural-log decay, <= 0 expected */
   const void* beta;          /* bf16 [B,T,H] */
@@ -101,8 +106,8 @@ typedef struct {
   const float* initial_state;/* [N,H,K,V] or NULL */
   const void* dO;            /* bf16 [B,T,H,V]: gradient of the output */
   const float* dht;          /* [N,H,K,V] gradient of the final state, or NULL */
-  void* dq;                  /* bf16 [B,T,H,K] */
-  void* dk;                  /* bf16 [B,T,H,K] */
+  void* dq;                  /* bf16 [B,T,Hk,K] (summed over each group of value heads) */
+  void* dk;                  /* bf16 [B,T,Hk,K] */
   void* dv;                  /* bf16 [B,T,H,V] */
   void* dbeta;               /* bf16 [B,T,H]: w.r.t. beta as passed (the logit when use_beta_sigmoid) */
   float* dg;                 /* fp32, same shape as g: w.r.t. the raw per-token gate */

@@ -85,23 +85,41 @@ def _sequences(B, T, cu_seqlens):
 
 
 def _dims(q, v, g):
-    B, T, H, K = q.shape
-    V = v.shape[-1]
+    B, T, _, K = q.shape
+    H, V = v.shape[2], v.shape[-1]
     per_channel = int(g.ndim == 4)
     return B, T, H, K, V, per_channel
+
+
+def _repeat_heads(x, H):
+    """Grouped q/k heads: ``x [B,T,Hk,K]`` repeated to the ``H`` value heads, each q/k head
+    ``H // Hk`` times in a row (``repeat_interleave`` of the hyper-parallel GDN and KDA pages,
+    value head h reading q/k head h // (H // Hk))."""
+    Hk = x.shape[2]
+    if H % Hk:
+        raise ValueError("the value heads must be a multiple of the q/k heads")
+    return np.repeat(x, H // Hk, axis=2) if Hk != H else x
+
+
+def _sum_groups(dx, Hk):
+    """Gradient of a repeated q/k head: the sum over the value heads that read it."""
+    B, T, H, K = dx.shape
+    return dx.reshape(B, T, Hk, H // Hk, K).sum(axis=3) if Hk != H else dx
 
 
 def gdr_fwd(q, k, v, g, beta, *, scale=None, initial_state=None, output_final_state=True,
             use_qk_l2norm=False, use_beta_sigmoid=False, cu_seqlens=None, threads=0):
     """Token recurrence forward in fp64.
 
-    q, k ``[B,T,H,K]``; v ``[B,T,H,V]``; g ``[B,T,H]`` (GDN) or ``[B,T,H,K]`` (KDA), natural
+    q, k ``[B,T,Hk,K]`` (Hk dividing H: grouped q/k heads, see ``_repeat_heads``); v ``[B,T,H,V]``;
+    g ``[B,T,H]`` (GDN) or ``[B,T,H,K]`` (KDA), natural
     log decay; beta ``[B,T,H]``; initial_state ``[N,H,K,V]`` (N = B, or the number of
     documents when ``cu_seqlens`` is given). Returns ``(o [B,T,H,V], final [N,H,K,V] or None)``.
     """
     q, k, v, g, beta = (_f64(x) for x in (q, k, v, g, beta))
     h0 = _f64(initial_state)
     B, T, H, K, V, per_channel = _dims(q, v, g)
+    q, k = np.ascontiguousarray(_repeat_heads(q, H)), np.ascontiguousarray(_repeat_heads(k, H))
     starts, lens = _sequences(B, T, cu_seqlens)
     N = len(lens)
     if scale is None:
@@ -128,6 +146,8 @@ def gdr_bwd(q, k, v, g, beta, dO, *, dht=None, scale=None, initial_state=None,
     q, k, v, g, beta, dO = (_f64(x) for x in (q, k, v, g, beta, dO))
     h0, dht = _f64(initial_state), _f64(dht)
     B, T, H, K, V, per_channel = _dims(q, v, g)
+    Hk = q.shape[2]
+    q, k = np.ascontiguousarray(_repeat_heads(q, H)), np.ascontiguousarray(_repeat_heads(k, H))
     starts, lens = _sequences(B, T, cu_seqlens)
     N = len(lens)
     if scale is None:
@@ -143,4 +163,5 @@ def gdr_bwd(q, k, v, g, beta, dO, *, dht=None, scale=None, initial_state=None,
         _ptr(out["dh0"]), int(threads))
     if rc != 0:
         raise ValueError("oracle_gdr_bwd rejected its arguments")
+    out["dq"], out["dk"] = _sum_groups(out["dq"], Hk), _sum_groups(out["dk"], Hk)
     return out

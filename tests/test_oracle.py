@@ -306,3 +306,52 @@ def test_backward_elementwise_small():
             pm[name][idx] -= eps
             fd[idx] = (_loss(pp, dO, dht, kw) - _loss(pm, dO, dht, kw)) / (2 * eps)
         np.testing.assert_allclose(grads[name_map[name]], fd, rtol=1e-6, atol=1e-8)
+
+
+# ---------------------------------------------------------------- grouped q/k heads
+
+def test_grouped_heads_forward_matches_single_head_runs():
+    # value head h reads q/k head h // G (repeat_interleave order): each output head equals
+    # an independent single-head run on the matching slices
+    B, T, Hk, G, K, V = 1, 70, 2, 3, 4, 4
+    H = Hk * G
+    rng = np.random.default_rng(31)
+    q = rng.standard_normal((B, T, Hk, K))
+    k = rng.standard_normal((B, T, Hk, K))
+    v = rng.standard_normal((B, T, H, V))
+    g = -np.log1p(np.exp(rng.standard_normal((B, T, H))))
+    beta = 1 / (1 + np.exp(-rng.standard_normal((B, T, H))))
+    h0 = rng.standard_normal((B, H, K, V)) * 0.3
+    o, hT = oracle.gdr_fwd(q, k, v, g, beta, scale=0.5, initial_state=h0, use_qk_l2norm=True)
+    for h in range(H):
+        hk = h // G
+        o1, hT1 = oracle.gdr_fwd(q[:, :, hk:hk + 1], k[:, :, hk:hk + 1], v[:, :, h:h + 1], g[:, :, h:h + 1],
+                                 beta[:, :, h:h + 1], scale=0.5, initial_state=h0[:, h:h + 1], use_qk_l2norm=True)
+        np.testing.assert_allclose(o[:, :, h:h + 1], o1, rtol=0, atol=1e-12)
+        np.testing.assert_allclose(hT[:, h:h + 1], hT1, rtol=0, atol=1e-12)
+
+
+def test_grouped_heads_backward_matches_finite_differences():
+    B, T, Hk, G, K, V = 1, 9, 2, 2, 4, 4
+    H = Hk * G
+    rng = np.random.default_rng(32)
+    q = rng.standard_normal((B, T, Hk, K))
+    k = rng.standard_normal((B, T, Hk, K))
+    v = rng.standard_normal((B, T, H, V))
+    g = -np.log1p(np.exp(rng.standard_normal((B, T, H))))
+    beta = 1 / (1 + np.exp(-rng.standard_normal((B, T, H))))
+    dO = rng.standard_normal((B, T, H, V))
+    kw = dict(scale=0.6, use_qk_l2norm=True)
+    grads = oracle.gdr_bwd(q, k, v, g, beta, dO, **kw)
+    assert grads["dq"].shape == q.shape and grads["dk"].shape == k.shape
+    eps = 1e-6
+    for name, x in (("q", q), ("k", k)):
+        direction = rng.standard_normal(x.shape)
+        def loss(xx):
+            args = dict(q=q, k=k)
+            args[name] = xx
+            o, _ = oracle.gdr_fwd(args["q"], args["k"], v, g, beta, output_final_state=False, **kw)
+            return (o * dO).sum()
+        fd = (loss(x + eps * direction) - loss(x - eps * direction)) / (2 * eps)
+        an = (grads["d" + name] * direction).sum()
+        assert abs(fd - an) <= 1e-6 * max(1.0, abs(fd)), (name, fd, an)
