@@ -5,9 +5,10 @@ The computation lives in ``libgdn.so`` (hand-written sm_103a CUDA behind the C A
 Importing the package does not touch the GPU; calling an op without the built library or
 without a compute-capability 10.3 device raises.
 """
-from .ops import (ChunkGatedDeltaRule, chain_plan, chunk_gated_delta_rule, gdn_bwd, gdn_fwd,
-                  kda_bwd, kda_fwd, set_chain_segment)
+from .ops import (CausalConv1d, ChunkGatedDeltaRule, causal_conv1d, causal_conv1d_bwd, causal_conv1d_fwd,
+                  chain_plan, chunk_gated_delta_rule, gdn_bwd, gdn_fwd, kda_bwd, kda_fwd, set_chain_segment)
 from ._lib import GdnError, load as load_library
 
 __all__ = ["gdn_fwd", "gdn_bwd", "kda_fwd", "kda_bwd", "chunk_gated_delta_rule",
-           "ChunkGatedDeltaRule", "GdnError", "load_library", "set_chain_segment", "chain_plan"]
+           "ChunkGatedDeltaRule", "GdnError", "load_library", "set_chain_segment", "chain_plan",
+           "causal_conv1d", "causal_conv1d_fwd", "causal_conv1d_bwd", "CausalConv1d"]

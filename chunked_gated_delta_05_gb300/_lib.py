@@ -35,6 +35,22 @@ class BwdArgs(ctypes.Structure):
                 ("saved", c_void_p), ("saved_bytes", c_size_t)]
 
 
+class ConvDesc(ctypes.Structure):
+    _fields_ = [("B", c_int), ("T", c_int), ("C", c_int), ("W", c_int), ("dilation", c_int),
+                ("cu_seqlens", ctypes.POINTER(ctypes.c_int32)), ("num_seqs", c_int), ("activation", c_int)]
+
+
+class ConvFwdArgs(ctypes.Structure):
+    _fields_ = [("x", c_void_p), ("weight", c_void_p), ("bias", c_void_p), ("halo", c_void_p),
+                ("y", c_void_p), ("workspace", c_void_p), ("workspace_bytes", c_size_t)]
+
+
+class ConvBwdArgs(ctypes.Structure):
+    _fields_ = [("x", c_void_p), ("weight", c_void_p), ("bias", c_void_p), ("halo", c_void_p),
+                ("dy", c_void_p), ("dx", c_void_p), ("dweight", c_void_p), ("dbias", c_void_p),
+                ("dhalo", c_void_p), ("workspace", c_void_p), ("workspace_bytes", c_size_t)]
+
+
 # Every symbol include/gdn.h declares, with its ctypes signature.
 SIGNATURES = {
     "gdn_strerror": ([c_int], ctypes.c_char_p),
@@ -54,6 +70,10 @@ SIGNATURES = {
     "gdn_fwd_noalloc_capacity": ([], c_size_t),
     "gdn_set_chain_segment": ([c_int], c_int),
     "gdn_chain_plan": ([ctypes.POINTER(Desc), ctypes.POINTER(c_int), ctypes.POINTER(c_int)], c_int),
+    "gdn_conv_fwd_workspace_size": ([ctypes.POINTER(ConvDesc)], c_size_t),
+    "gdn_conv_bwd_workspace_size": ([ctypes.POINTER(ConvDesc)], c_size_t),
+    "gdn_conv_fwd": ([ctypes.POINTER(ConvDesc), ctypes.POINTER(ConvFwdArgs), c_void_p], c_int),
+    "gdn_conv_bwd": ([ctypes.POINTER(ConvDesc), ctypes.POINTER(ConvBwdArgs), c_void_p], c_int),
     "gdn_timing_enable": ([c_int], c_int),
     "gdn_timing_kinds": ([], c_int),
     "gdn_timing_name": ([c_int], ctypes.c_char_p),

@@ -288,9 +288,8 @@ int check_cuda(cudaError_t e, const char* what) {
 
 // Optional per-kernel timing (CUDA events recorded on the launching stream around every
 // launch while enabled). Process-global and not thread-safe: a profiling aid.
-enum KernelKind { kKTables = 0, kKPrep, kKChainFwd, kKChainBwd, kKBwdFeat, kKBwdTok, kKCompose, kKGroupSum, kKinds };
 const char* const kKindNames[kKinds] = {"tables", "prepare", "chain_fwd", "chain_bwd", "bwd_feat", "bwd_tok",
-                                        "compose", "group_sum"};
+                                        "compose", "group_sum", "conv_fwd", "conv_bwd"};
 struct Timing {
   bool on = false;
   std::vector<std::pair<cudaEvent_t, cudaEvent_t>> ev[kKinds];
@@ -687,6 +686,22 @@ int run_bwd(const gdn_desc_t* d, const gdn_bwd_args_t* a, void* stream, bool kda
 
 // Records `msg` as the calling thread's last error (for entry points defined in other files).
 int set_last_error(int code, const char* msg) { return fail(code, msg); }
+
+// Timing hook brackets for launches made in other files (no-ops while timing is off).
+TimedScope::TimedScope(int kind, cudaStream_t s) : impl_(new TimedLaunch(kind, s)) {}
+TimedScope::~TimedScope() { delete static_cast<TimedLaunch*>(impl_); }
+
+// Copies host offsets into device memory through kernel parameters (no staging buffer).
+int upload_offsets(const int32_t* host, int count, int* dst, cudaStream_t s) {
+  for (int off = 0; off < count; off += kMaxUploadInts) {
+    UploadParams up;
+    up.count = std::min(kMaxUploadInts, count - off);
+    for (int i = 0; i < up.count; ++i) up.vals[i] = host[off + i];
+    int rc = check_cuda(launch_upload(up, dst + off, s), "upload offsets");
+    if (rc) return rc;
+  }
+  return GDN_OK;
+}
 
 }  // namespace gdn
 

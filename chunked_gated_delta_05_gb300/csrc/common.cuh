@@ -170,6 +170,23 @@ struct BwdTokParams {
   int* status;
 };
 
+// Kernel kinds of the per-launch timing hook (names in api.cu).
+enum KernelKind {
+  kKTables = 0, kKPrep, kKChainFwd, kKChainBwd, kKBwdFeat, kKBwdTok, kKCompose, kKGroupSum, kKConvFwd, kKConvBwd,
+  kKinds
+};
+
+// Host helpers shared by the entry points of several files (api.cu).
+int set_last_error(int code, const char* msg);
+int upload_offsets(const int32_t* host, int count, int* dst, cudaStream_t s);
+class TimedScope {  // records CUDA events around the launches in its scope while timing is on
+ public:
+  TimedScope(int kind, cudaStream_t s);
+  ~TimedScope();
+ private:
+  void* impl_;
+};
+
 // Launchers (defined next to their kernels). Return the cudaError_t of the launch.
 cudaError_t launch_upload(const UploadParams& p, int* dst, cudaStream_t s);
 cudaError_t launch_tables(const TableParams& p, cudaStream_t s);

@@ -237,3 +237,105 @@ def chunk_gated_delta_rule(q, k, v, g, beta, *, initial_state=None, output_final
         use_beta_sigmoid = per_channel
     return ChunkGatedDeltaRule.apply(q, k, v, g, beta, initial_state, per_channel, use_qk_l2norm,
                                      use_beta_sigmoid, cu_seqlens, scale, output_final_state)
+
+
+# ---------------------------------------------------------------- short convolution
+
+def _conv_desc(x, weight, dilation, activation, offsets):
+    if x.dim() != 3 or weight.dim() != 2 or weight.shape[0] != x.shape[2]:
+        raise ValueError("x must be [B,T,C] and weight [C,W]")
+    d = _lib.ConvDesc()
+    d.B, d.T, d.C = x.shape
+    d.W, d.dilation, d.activation = weight.shape[1], int(dilation), int(bool(activation))
+    if offsets is not None:
+        arr, n = offsets
+        d.cu_seqlens = ctypes.cast(arr, ctypes.POINTER(ctypes.c_int32))
+        d.num_seqs = n
+    else:
+        d.num_seqs = d.B
+    return d
+
+
+def _conv_checks(x, weight, bias, halo, N, HW):
+    dev = x.device
+    if dev.type != "cuda":
+        raise ValueError("inputs must be CUDA tensors")
+    B, T, C = x.shape
+    _check_tensor("x", x, torch.bfloat16, (B, T, C), dev)
+    _check_tensor("weight", weight, torch.float32, (C, weight.shape[1]), dev)
+    if bias is not None:
+        _check_tensor("bias", bias, torch.float32, (C,), dev)
+    if halo is not None:
+        _check_tensor("halo", halo, torch.bfloat16, (N, HW, C), dev)
+    return dev
+
+
+def causal_conv1d_fwd(x, weight, bias=None, *, dilation=1, activation=True, cu_seqlens=None, halo=None):
+    """Causal depthwise Conv1d (+ SiLU) over the token axis of ``x [B,T,C]`` (bf16) with
+    ``weight [C,W]`` (fp32), optional ``bias [C]`` and ``halo [N,(W-1)*dilation,C]``, per packed
+    document when ``cu_seqlens`` is given. Returns ``y [B,T,C]`` (bf16)."""
+    lib = _lib.load()
+    offsets = _offsets(cu_seqlens, x.shape[1] if x.dim() == 3 else 0)
+    desc = _conv_desc(x, weight, dilation, activation, offsets)
+    N = desc.num_seqs
+    dev = _conv_checks(x, weight, bias, halo, N, (weight.shape[1] - 1) * dilation)
+    ws_bytes = lib.gdn_conv_fwd_workspace_size(ctypes.byref(desc))
+    if ws_bytes == 0:
+        _lib.check(_lib.GDN_EINVAL)
+    y = torch.empty_like(x)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    a = _lib.ConvFwdArgs(x=_ptr(x), weight=_ptr(weight), bias=_ptr(bias), halo=_ptr(halo), y=_ptr(y),
+                         workspace=_ptr(ws), workspace_bytes=ws_bytes)
+    stream = ctypes.c_void_p(torch.cuda.current_stream(dev).cuda_stream)
+    _lib.check(lib.gdn_conv_fwd(ctypes.byref(desc), ctypes.byref(a), stream))
+    return y
+
+
+def causal_conv1d_bwd(x, weight, bias, dy, *, dilation=1, activation=True, cu_seqlens=None, halo=None):
+    """Gradients of ``<dy, causal_conv1d_fwd(...)>``: ``(dx bf16, dweight fp32, dbias fp32 or
+    None, dhalo fp32 or None)``."""
+    lib = _lib.load()
+    offsets = _offsets(cu_seqlens, x.shape[1] if x.dim() == 3 else 0)
+    desc = _conv_desc(x, weight, dilation, activation, offsets)
+    N = desc.num_seqs
+    HW = (weight.shape[1] - 1) * dilation
+    dev = _conv_checks(x, weight, bias, halo, N, HW)
+    _check_tensor("dy", dy, torch.bfloat16, tuple(x.shape), dev)
+    ws_bytes = lib.gdn_conv_bwd_workspace_size(ctypes.byref(desc))
+    if ws_bytes == 0:
+        _lib.check(_lib.GDN_EINVAL)
+    dx = torch.empty_like(x)
+    dw = torch.empty_like(weight)
+    db = torch.empty_like(bias) if bias is not None else None
+    dh = torch.empty((N, HW, x.shape[2]), dtype=torch.float32, device=dev) if halo is not None else None
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    a = _lib.ConvBwdArgs(x=_ptr(x), weight=_ptr(weight), bias=_ptr(bias), halo=_ptr(halo), dy=_ptr(dy),
+                         dx=_ptr(dx), dweight=_ptr(dw), dbias=_ptr(db), dhalo=_ptr(dh), workspace=_ptr(ws),
+                         workspace_bytes=ws_bytes)
+    stream = ctypes.c_void_p(torch.cuda.current_stream(dev).cuda_stream)
+    _lib.check(lib.gdn_conv_bwd(ctypes.byref(desc), ctypes.byref(a), stream))
+    return dx, dw, db, dh
+
+
+class CausalConv1d(torch.autograd.Function):
+    """Autograd wrapper of the short convolution."""
+
+    @staticmethod
+    def forward(ctx, x, weight, bias, halo, dilation, activation, cu_seqlens):
+        ctx.save_for_backward(x, weight, bias, halo)
+        ctx.cfg = (dilation, activation, cu_seqlens)
+        return causal_conv1d_fwd(x, weight, bias, dilation=dilation, activation=activation,
+                                 cu_seqlens=cu_seqlens, halo=halo)
+
+    @staticmethod
+    def backward(ctx, dy):
+        x, weight, bias, halo = ctx.saved_tensors
+        dilation, activation, cu = ctx.cfg
+        dx, dw, db, dh = causal_conv1d_bwd(x, weight, bias, dy.contiguous(), dilation=dilation,
+                                           activation=activation, cu_seqlens=cu, halo=halo)
+        return dx, dw, db, (None if dh is None else dh.to(halo.dtype)), None, None, None
+
+
+def causal_conv1d(x, weight, bias=None, *, dilation=1, activation=True, cu_seqlens=None, halo=None):
+    """Differentiable short convolution (see :func:`causal_conv1d_fwd`)."""
+    return CausalConv1d.apply(x, weight, bias, halo, dilation, activation, cu_seqlens)

@@ -179,6 +179,51 @@ size_t gdn_fwd_noalloc_capacity(void);
 int gdn_set_chain_segment(int chunks);
 int gdn_chain_plan(const gdn_desc_t* desc, int* chunks_per_segment, int* max_segments);
 
+/* Short convolution ahead of the path: causal depthwise Conv1d over the token axis with
+ * optional bias and SiLU, per packed document (hyper-parallel GDN Diff Coverage page,
+ * `_causal_conv1d_with_cp_halo` and the packed ShortConv path, which produce q, k and v):
+ *   z[t][c] = bias[c] + sum_{i<W} weight[c][i] x[t - (W-1-i) dilation][c],  y = silu(z) or z.
+ * Positions before a sequence's first token read that sequence's halo (its (W-1) dilation
+ * preceding tokens, e.g. another context-parallel rank's tail) or zero. Rows never read
+ * across packed-document boundaries. */
+typedef struct {
+  int B, T, C;               /* x is [B,T,C]; packed (cu_seqlens != NULL): B == 1. C % 8 == 0 */
+  int W;                     /* taps, 1..8 */
+  int dilation;              /* >= 1 */
+  const int32_t* cu_seqlens; /* HOST, num_seqs + 1 offsets, or NULL for dense */
+  int num_seqs;
+  int activation;            /* 1: SiLU, 0: none */
+} gdn_conv_desc_t;
+
+typedef struct {
+  const void* x;             /* bf16 [B,T,C], 16-byte aligned */
+  const float* weight;       /* fp32 [C,W] */
+  const float* bias;         /* fp32 [C] or NULL */
+  const void* halo;          /* bf16 [N,(W-1)*dilation,C] or NULL (zeros) */
+  void* y;                   /* bf16 [B,T,C], 16-byte aligned, written */
+  void* workspace;           /* >= gdn_conv_fwd_workspace_size() bytes, 256-byte aligned */
+  size_t workspace_bytes;
+} gdn_conv_fwd_args_t;
+
+typedef struct {
+  const void* x;             /* forward inputs, as passed to the forward */
+  const float* weight;
+  const float* bias;
+  const void* halo;
+  const void* dy;            /* bf16 [B,T,C] gradient of y */
+  void* dx;                  /* bf16 [B,T,C], written */
+  float* dweight;            /* fp32 [C,W], written */
+  float* dbias;              /* fp32 [C], written, or NULL */
+  float* dhalo;              /* fp32 [N,(W-1)*dilation,C], written, or NULL */
+  void* workspace;           /* >= gdn_conv_bwd_workspace_size() bytes, 256-byte aligned */
+  size_t workspace_bytes;
+} gdn_conv_bwd_args_t;
+
+size_t gdn_conv_fwd_workspace_size(const gdn_conv_desc_t* desc);
+size_t gdn_conv_bwd_workspace_size(const gdn_conv_desc_t* desc);
+int gdn_conv_fwd(const gdn_conv_desc_t* desc, const gdn_conv_fwd_args_t* args, void* stream);
+int gdn_conv_bwd(const gdn_conv_desc_t* desc, const gdn_conv_bwd_args_t* args, void* stream);
+
 /* Profiling hooks (not part of the computation). While enabled, every kernel launch of the
  * calls above is bracketed by CUDA events on its stream. gdn_timing_read() synchronizes the
  * recorded events of one kernel kind (0 .. gdn_timing_kinds()-1, named by gdn_timing_name()),

@@ -1,0 +1,53 @@
+"""GPU parity of the short convolution (causal depthwise Conv1d + SiLU) against the fp64
+oracle: dense and packed rows, halos, dilation, activation off, ragged channel blocks."""
+import numpy as np
+import pytest
+import torch
+
+from chunked_gated_delta_05_gb300 import causal_conv1d_bwd, causal_conv1d_fwd
+from oracle import conv
+from tests._util import assert_output
+
+pytestmark = pytest.mark.gpu
+
+
+def make(B, T, C, W, seed, halo_rows=0, N=None):
+    g = torch.Generator(device="cpu")
+    g.manual_seed(seed)
+    x = torch.randn(B, T, C, generator=g).to(torch.bfloat16)
+    w = (torch.randn(C, W, generator=g) * 0.5).float()
+    b = (torch.randn(C, generator=g) * 0.1).float()
+    dy = torch.randn(B, T, C, generator=g).to(torch.bfloat16)
+    halo = torch.randn(N or B, halo_rows, C, generator=g).to(torch.bfloat16) if halo_rows else None
+    return x, w, b, dy, halo
+
+
+def f64(t):
+    return None if t is None else t.double().numpy()
+
+
+@pytest.mark.parametrize("B,T,C,W,dil,act,packed,halo", [
+    (1, 300, 256, 4, 1, True, None, False),
+    (2, 77, 1032, 4, 1, True, None, True),
+    (1, 200, 64, 3, 2, False, [0, 1, 70, 71, 200], False),
+    (1, 333, 136, 8, 1, True, [0, 100, 333], True),
+    (3, 65, 8, 1, 1, True, None, False),
+])
+def test_conv_parity(B, T, C, W, dil, act, packed, halo):
+    N = B if packed is None else len(packed) - 1
+    HW = (W - 1) * dil
+    x, w, b, dy, h = make(B, T, C, W, seed=T + C + W, halo_rows=HW if halo and HW else 0, N=N)
+    dev = "cuda"
+    kw = dict(dilation=dil, activation=act, cu_seqlens=packed)
+    y = causal_conv1d_fwd(x.to(dev), w.to(dev), b.to(dev), halo=None if h is None else h.to(dev), **kw)
+    dx, dw, db, dh = causal_conv1d_bwd(x.to(dev), w.to(dev), b.to(dev), dy.to(dev),
+                                       halo=None if h is None else h.to(dev), **kw)
+    torch.cuda.synchronize()
+    ref_y = conv.causal_conv1d(f64(x), f64(w), f64(b), halo=f64(h), **kw)
+    ref = conv.causal_conv1d_bwd(f64(x), f64(w), f64(b), f64(dy), halo=f64(h), **kw)
+    assert_output("y", y.float().cpu().numpy(), ref_y)
+    assert_output("dx", dx.float().cpu().numpy(), ref["dx"])
+    assert_output("dweight", dw.cpu().numpy(), ref["dweight"])
+    assert_output("dbias", db.cpu().numpy(), ref["dbias"])
+    if h is not None:
+        assert_output("dhalo", dh.cpu().numpy(), ref["dhalo"])
