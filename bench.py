@@ -180,6 +180,45 @@ def run_reference(args, rank):
     print(json.dumps(line), flush=True)
 
 
+def measure_short_conv(w, dev, peaks, iters=10):
+    """HBM roofline of the short convolution ahead of the path (causal depthwise Conv1d + SiLU,
+    W = 4) on the mixed q/k/v channels of the workload (3 H 128 channels, B*T rows). Two input
+    sets larger than L2 together alternate between launches. Algorithmic bytes: forward reads
+    x and writes y (4 B per element); backward reads x and dy and writes dx (6 B per element)."""
+    import torch
+    from chunked_gated_delta_05_gb300 import _lib, causal_conv1d_bwd, causal_conv1d_fwd
+    C, Wt = 3 * w.H * w.K, 4
+    gen = torch.Generator(device="cpu")
+    gen.manual_seed(7)
+    sets = []
+    for _ in range(2):
+        x = torch.randn(w.B, w.T, C, generator=gen).to(torch.bfloat16).to(dev)
+        dy = torch.randn(w.B, w.T, C, generator=gen).to(torch.bfloat16).to(dev)
+        sets.append((x, dy))
+    weight = (torch.randn(C, Wt, generator=gen) * 0.5).to(dev)
+    bias = (torch.randn(C, generator=gen) * 0.1).to(dev)
+    elems = w.B * w.T * C
+    out = {}
+    for name, fn, nbytes in (("fwd", lambda x, dy: causal_conv1d_fwd(x, weight, bias), 4 * elems),
+                             ("bwd", lambda x, dy: causal_conv1d_bwd(x, weight, bias, dy), 6 * elems)):
+        for i in range(3):
+            fn(*sets[i % 2])
+        torch.cuda.synchronize(dev)
+        # device time of the library's launches (CUDA events on the launching stream around each
+        # call's kernels), so the wrapper's host work between calls is not counted
+        _lib.timing_enable(True)
+        for i in range(iters):
+            fn(*sets[i % 2])
+        torch.cuda.synchronize(dev)
+        t = _lib.timing_read()
+        _lib.timing_enable(False)
+        ms = t["conv_" + name][0] / iters
+        gbs = nbytes / (ms * 1e-3) / 1e9
+        out[name] = {"ms": ms, "algorithmic_bytes": nbytes, "achieved_gbs": gbs,
+                     "frac_of_hbm": gbs / peaks["hbm_gbs"], "timing": "CUDA events around the kernels"}
+    return {"shape": {"rows": w.B * w.T, "channels": C, "taps": Wt, "activation": "silu"}, "bound": "hbm", **out}
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -327,7 +366,8 @@ def main():
     line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16 io, bf16/tf32 mma, fp32 accumulate", "data": "synthetic",
-            "config": {"workload": w.name, "B": w.B, "T": w.T, "H": w.H, "K": w.K, "V": w.V, "chunk": 64,
+            "config": {"workload": w.name, "B": w.B, "T": w.T, "H": w.H, "Hk": w.num_k_heads or w.H, "K": w.K,
+                       "V": w.V, "chunk": 64,
                        "gate": "per-channel" if w.per_channel else "scalar", "l2norm": w.use_qk_l2norm,
                        "parallelism": f"replicas x{world}",
                        "l2": "per-step working set (67 MB inputs + ~1 GB workspace) exceeds the 129 MB L2"},
@@ -335,6 +375,8 @@ def main():
             "roofline": roofline, "clocks": clocks, "gpu_launches": gpu_launches,
             "e2e": {"value": tokens * world / (e_ms * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "ms_per_step": e_ms}}
+    if rank == 0:
+        line["next_rows"] = {"short_conv": measure_short_conv(w, dev, peaks)}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu_tps, dt = oracle_sample_tokens_per_s(w, host, "")
         line["cpu_baseline"] = {"value": cpu_tps, "unit": "tokens/s", "cores": os.cpu_count(), "kind": "oracle",

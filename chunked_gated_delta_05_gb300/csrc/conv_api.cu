@@ -127,8 +127,9 @@ int gdn_conv_fwd(const gdn_conv_desc_t* desc, const gdn_conv_fwd_args_t* a, void
   int rc = validate_conv(desc, &P);
   if (rc) return rc;
   if (!a || !a->x || !a->weight || !a->y) return set_last_error(GDN_EINVAL, "x, weight and y must be non-NULL");
-  if (!aligned16(a->x) || !aligned16(a->y) || (a->halo && !aligned16(a->halo)))
-    return set_last_error(GDN_EINVAL, "x, y and halo must be 16-byte aligned");
+  if (!aligned16(a->x) || !aligned16(a->y) || (a->halo && !aligned16(a->halo)) || !aligned16(a->weight) ||
+      (a->bias && !aligned16(a->bias)))
+    return set_last_error(GDN_EINVAL, "x, y, halo, weight and bias must be 16-byte aligned");
   const size_t bytes = size_t(P.R) * P.C * 2;
   const char *xb = static_cast<const char*>(a->x), *yb = static_cast<const char*>(a->y);
   if (xb < yb + bytes && yb < xb + bytes) return set_last_error(GDN_EINVAL, "y must not alias x");
@@ -156,8 +157,8 @@ int gdn_conv_bwd(const gdn_conv_desc_t* desc, const gdn_conv_bwd_args_t* a, void
   if (!a || !a->x || !a->weight || !a->dy || !a->dx || !a->dweight)
     return set_last_error(GDN_EINVAL, "x, weight, dy, dx and dweight must be non-NULL");
   if (!aligned16(a->x) || !aligned16(a->dy) || !aligned16(a->dx) || (a->halo && !aligned16(a->halo)) ||
-      (a->dhalo && !aligned16(a->dhalo)))
-    return set_last_error(GDN_EINVAL, "x, dy, dx, halo and dhalo must be 16-byte aligned");
+      (a->dhalo && !aligned16(a->dhalo)) || !aligned16(a->weight) || (a->bias && !aligned16(a->bias)))
+    return set_last_error(GDN_EINVAL, "x, dy, dx, halo, dhalo, weight and bias must be 16-byte aligned");
   if (a->dhalo && !a->halo) return set_last_error(GDN_EINVAL, "dhalo needs the halo input");
   const size_t bytes = size_t(P.R) * P.C * 2;
   const char* dxb = static_cast<const char*>(a->dx);

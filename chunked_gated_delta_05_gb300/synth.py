@@ -38,6 +38,7 @@ class Workload:
     backward: bool = True
     seed: int = 0
     use_qk_l2norm: bool = True
+    num_k_heads: int = 0            # >0: grouped q/k heads (q, k drawn with this many heads)
     extra: dict = field(default_factory=dict)
 
     @property
@@ -45,7 +46,8 @@ class Workload:
         return self.B * self.T
 
 
-# The five workloads of the method's benchmark plan plus the forward target shape.
+# The five workloads of the method's benchmark plan, the forward target shape, and a grouped-head
+# variant of the training shape.
 WORKLOADS = {
     "gdn_smoke_b1_t256_h2": Workload("gdn_smoke_b1_t256_h2", 1, 256, 2, backward=False, seed=0),
     "gdn_b2_t4096_h16": Workload("gdn_b2_t4096_h16", 2, 4096, 16, h0_std=0.02, seed=1),
@@ -55,6 +57,9 @@ WORKLOADS = {
     "kda_b1_t8192_h32": Workload("kda_b1_t8192_h32", 1, 8192, 32, per_channel=True,
                                  beta_logits=True, seed=4),
     "gdn_b1_t8192_h16": Workload("gdn_b1_t8192_h16", 1, 8192, 16, seed=5),
+    # grouped q/k heads (next row of the plan): 16 value heads over 4 q/k heads
+    "gdn_gqa_b2_t4096_h16_hk4": Workload("gdn_gqa_b2_t4096_h16_hk4", 2, 4096, 16, h0_std=0.02, seed=6,
+                                         num_k_heads=4),
 }
 
 
@@ -91,8 +96,9 @@ def make_inputs(w: Workload, *, seed: Optional[int] = None, lengths=None) -> dic
     def randn(*shape):
         return torch.randn(*shape, generator=gen, dtype=torch.float32)
 
-    q = randn(B, T, H, K).to(torch.bfloat16)
-    k = randn(B, T, H, K).to(torch.bfloat16)
+    Hk = w.num_k_heads if w.num_k_heads > 0 else H
+    q = randn(B, T, Hk, K).to(torch.bfloat16)
+    k = randn(B, T, Hk, K).to(torch.bfloat16)
     v = randn(B, T, H, V).to(torch.bfloat16)
     gshape = (B, T, H, K) if w.per_channel else (B, T, H)
     g = -torch.nn.functional.softplus(randn(*gshape))

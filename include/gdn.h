@@ -197,8 +197,8 @@ typedef struct {
 
 typedef struct {
   const void* x;             /* bf16 [B,T,C], 16-byte aligned */
-  const float* weight;       /* fp32 [C,W] */
-  const float* bias;         /* fp32 [C] or NULL */
+  const float* weight;       /* fp32 [C,W], 16-byte aligned */
+  const float* bias;         /* fp32 [C] or NULL, 16-byte aligned */
   const void* halo;          /* bf16 [N,(W-1)*dilation,C] or NULL (zeros) */
   void* y;                   /* bf16 [B,T,C], 16-byte aligned, written */
   void* workspace;           /* >= gdn_conv_fwd_workspace_size() bytes, 256-byte aligned */
