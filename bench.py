@@ -44,8 +44,12 @@ TF32_OVER_BF16 = 1.1 / 2.25    # nominal dense tf32 / bf16 tensor rates of a GB3
 # capture of the same kernel build on the same workload (profiles/kernels_gdn_b2_t4096_h16.md);
 # None elsewhere, and None for a kernel changed since its capture.
 NCU_TRAFFIC_BYTES = {
-    ("bwd_feat", "gdn_b2_t4096_h16"): (470.668288 + 294.395648) * 1e6,
-    ("prepare", "gdn_b2_t4096_h16"): (104.316672 + 515.707648) * 1e6,
+    ("prepare", "gdn_b2_t4096_h16"): (104.885248 + 510.984448) * 1e6,
+    ("chain_fwd", "gdn_b2_t4096_h16"): (186.488832 + 38.409728 + 249.328128 + 138.250496) * 1e6,
+    ("compose", "gdn_b2_t4096_h16"): 2 * 21.011456e6,
+    ("chain_bwd", "gdn_b2_t4096_h16"): (216.477440 + 35.716352 + 230.844416 + 118.377984) * 1e6,
+    ("bwd_feat", "gdn_b2_t4096_h16"): (613.202176 + 294.521600) * 1e6,
+    ("bwd_tok", "gdn_b2_t4096_h16"): (640.715520 + 89.759744) * 1e6,
 }
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
