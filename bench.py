@@ -223,6 +223,33 @@ def measure_short_conv(w, dev, peaks, iters=10):
     return {"shape": {"rows": w.B * w.T, "channels": C, "taps": Wt, "activation": "silu"}, "bound": "hbm", **out}
 
 
+def measure_forward_target(dev, peaks, iters=10):
+    """Forward alone (inference: no saves) at T = 8192, H = 16, the shape of the forward
+    target: chunked-form FLOP / device time of the forward's kernels, against the bf16 peak.
+    Inputs larger than L2 (67 MB of q/k/v plus the workspace tiles) are rewritten each call."""
+    import torch
+    from chunked_gated_delta_05_gb300 import _lib, gdn_fwd, synth
+    w = synth.WORKLOADS["gdn_b1_t8192_h16"]
+    d = synth.make_inputs(w)
+    dc = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in d.items()}
+    fwd = lambda: gdn_fwd(dc["q"], dc["k"], dc["v"], dc["g"], dc["beta"], output_final_state=True)
+    for _ in range(3):
+        fwd()
+    torch.cuda.synchronize(dev)
+    _lib.timing_enable(True)
+    for _ in range(iters):
+        fwd()
+    torch.cuda.synchronize(dev)
+    t = _lib.timing_read()
+    _lib.timing_enable(False)
+    ms = sum(v[0] for v in t.values()) / iters
+    flop = FWD_FLOP_PER_TOKEN_HEAD * w.B * w.T * w.H
+    tflops = flop / (ms * 1e-3) / 1e12
+    return {"workload": w.name, "ms": ms, "tflops": tflops, "pct_of_bf16_peak": tflops / peaks["bf16_tflops"],
+            "peak_kind": "bf16 burst", "kernels_ms": {k: v[0] / iters for k, v in t.items() if v[1]},
+            "timing": "CUDA events around the forward's kernels"}
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -381,6 +408,7 @@ def main():
                     "d2h_bytes_per_step": d2h, "ms_per_step": e_ms}}
     if rank == 0:
         line["next_rows"] = {"short_conv": measure_short_conv(w, dev, peaks)}
+        line["forward_target"] = measure_forward_target(dev, peaks)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu_tps, dt = oracle_sample_tokens_per_s(w, host, "")
         line["cpu_baseline"] = {"value": cpu_tps, "unit": "tokens/s", "cores": os.cpu_count(), "kind": "oracle",

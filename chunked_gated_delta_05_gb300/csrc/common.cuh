@@ -12,6 +12,7 @@ namespace gdn {
 constexpr int kC = 64;     // chunk length (tokens)
 constexpr int kD = 128;    // head dim K == V
 constexpr int kMaxUploadInts = 4000;  // cu_seqlens entries per upload launch
+constexpr float kLog2e = 1.4426950408889634f;  // log2(e): exp(x) = exp2(x log2(e))
 
 // One chunk of one sequence: {first token row (flattened B*T), valid rows (1..64),
 // sequence index, chunk index within the sequence}.

@@ -85,10 +85,10 @@ __global__ void __launch_bounds__(kThreads, 1)
               const __grid_constant__ CUtensorMap mDVN, const BwdTokParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = align1k(smem_raw);
-  __shared__ uint64_t bar_tma, bar_mma;
+  __shared__ uint64_t bar_tma, bar_tma2, bar_mma;
   __shared__ uint32_t tslot;
   __shared__ int abort_flag;
-  __shared__ float s_G[kC], s_rq[kC], s_rk[kC], s_b[kC], s_dG[kC], s_db[kC], s_P[kC][kC + 1];
+  __shared__ float s_G[kC], s_G2[kC], s_rq[kC], s_rk[kC], s_b[kC], s_dG[kC], s_db[kC], s_P[kC][kC + 1];
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int c = blockIdx.x, h = blockIdx.y, H = p.H;
@@ -108,12 +108,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (tid == 0) {
     abort_flag = 0;
     mbar_init(&bar_tma, 1);
+    mbar_init(&bar_tma2, 1);
     mbar_init(&bar_mma, 1);
     fence_mbar_init();
   }
   if (tid < kC) {
     const bool ok = tid < len;
     s_G[tid] = p.Gc[tile * kC + tid];
+    s_G2[tid] = s_G[tid] * kLog2e;  // exp(G_i - G_j) = exp2(G2_i - G2_j) in the pair loop
     s_rq[tid] = ok ? p.rq[tile * kC + tid] : 0.f;
     s_rk[tid] = ok ? p.rk[tile * kC + tid] : 0.f;
     s_b[tid] = ok ? p.beff[tile * kC + tid] : 0.f;
@@ -127,7 +129,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tl = tb + tmem_lane_base(warp);
   const float Glast = s_G[len - 1];
   if (tid == 0) {
-    mbar_expect_tx(&bar_tma, 4u * 16384u + 3u * 32768u);
+    // first group (q, k, v, dO, v_new) feeds the first products; dW, dU arrive on their own
+    // barrier and are first read by the dA product
+    mbar_expect_tx(&bar_tma, 4u * 16384u + 32768u);
+    mbar_expect_tx(&bar_tma2, 2u * 32768u);
     for (int pp = 0; pp < 2; ++pp) {
       const int x = h * kD + 64 * pp, xqk = (h / p.qk_group) * kD + 64 * pp;
       tma_load_2d(sQ + pp * 8192, &mq, xqk, ch.x, &bar_tma);
@@ -137,8 +142,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int pp = 0; pp < 4; ++pp) {
       tma_load_2d(sm + kR2 + pp * 8192, &mVN, pp * 32, int(tile) * kC, &bar_tma);
-      tma_load_2d(sm + kR3 + pp * 8192, &mDW, pp * 32, int(tile) * kC, &bar_tma);
-      tma_load_2d(sm + kR4 + pp * 8192, &mDVN, pp * 32, int(tile) * kC, &bar_tma);
+      tma_load_2d(sm + kR3 + pp * 8192, &mDW, pp * 32, int(tile) * kC, &bar_tma2);
+      tma_load_2d(sm + kR4 + pp * 8192, &mDVN, pp * 32, int(tile) * kC, &bar_tma2);
     }
     // inputs of the later phases: start their trip from HBM now
     const size_t rows = tile * kTileW;
@@ -207,6 +212,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   TTRACE(4);
   // ---- product 2: dA = [dW | dU] [K1 | V1]^T  (K = 256)
+  if (tid == 0 && ok) ok = mbar_wait(&bar_tma2, 0, &abort_flag, p.status, kDevTimeoutTma);
   if (tid == 0 && ok) {
     const uint32_t id_tf = idesc_tf32(64, 64);
     const uint32_t r1 = smem_u32(sm + kR1), r2 = smem_u32(sm + kR2), r3 = smem_u32(sm + kR3), r4 = smem_u32(sm + kR4);
@@ -307,7 +313,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   {
     const int i = rr;
     const bool vi = i < len;
-    const float Gi = s_G[i], bi = s_b[i], rki = s_rk[i], rqi = s_rq[i];
+    const float Gi2 = s_G2[i], bi = s_b[i], rki = s_rk[i], rqi = s_rq[i];
     float rowP = 0.f, dbi = 0.f;
     {
       float dl[32], nn[32], kk[32], qk[32];
@@ -324,7 +330,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int jj = 0; jj < 32; ++jj) {
           const int j = 32 * half + jj;
-          const float gam = (j <= i && vi) ? expf(Gi - s_G[j]) : 0.f;
+          const float gam = (j <= i && vi) ? exp2f(Gi2 - s_G2[j]) : 0.f;
           const float D = (j < i && vi) ? -dl[jj] : 0.f;                 // dL_ij
           const float N = (j <= i && vi) ? nn[jj] : 0.f;                 // dAqk_ij
           const float Lij = bi * rki * s_rk[j] * kk[jj] * gam;

@@ -35,7 +35,6 @@ constexpr uint32_t kOffG = 49152;                            // G * log2(e), fp3
 constexpr uint32_t kR1 = 83968, kR2 = 116736, kR3 = 149504, kR4 = 182272;  // 32 KB each
 constexpr uint32_t kSmemBytes = kR4 + 32768 + 1024;
 constexpr uint32_t kTAqk = 0, kTdA = 64, kTX = 128;
-constexpr float kLog2e = 1.4426950408889634f;
 
 __device__ __forceinline__ uint8_t* align1k(uint8_t* p) {
   return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));

@@ -81,6 +81,7 @@ __device__ __forceinline__ void unit_lower_inverse_column(const float* __restric
       for (int e = 0; e < 16; ++e) y[e] = 0.f;
       // warp-uniform rows (the warp's columns share c & ~31; X[j][c] = 0 for j < c is already
       // in sX), so every L^T row read is a broadcast
+#pragma unroll 4
       for (int j = c & ~31; j < r0; ++j) {
         const float xj = sX[j * kC + c];
         const float4* l4 = reinterpret_cast<const float4*>(LT + j * kC + r0);
@@ -95,9 +96,14 @@ __device__ __forceinline__ void unit_lower_inverse_column(const float* __restric
       }
 #pragma unroll
       for (int r = 0; r < 16; ++r) {
-        float acc = y[r];
+        // two interleaved partial sums halve the dependent FMA chain of the 16x16 solve
+        float acc0 = y[r], acc1 = 0.f;
 #pragma unroll
-        for (int j = 0; j < r; ++j) acc = fmaf(-LT[(r0 + j) * kC + r0 + r], x[j], acc);
+        for (int j = 0; j < r; ++j) {
+          if (j & 1) acc1 = fmaf(-LT[(r0 + j) * kC + r0 + r], x[j], acc1);
+          else acc0 = fmaf(-LT[(r0 + j) * kC + r0 + r], x[j], acc0);
+        }
+        const float acc = acc0 + acc1;
         const int R = r0 + r;
         x[r] = (R < c) ? 0.f : ((R == c) ? 1.f : acc);
       }
@@ -126,7 +132,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __shared__ uint64_t bar_tma, bar_mma;
   __shared__ uint32_t tslot;
   __shared__ int abort_flag;
-  __shared__ float s_g[kThreads], s_b[kThreads], s_rk[kThreads], s_G[kThreads];
+  __shared__ float s_g[kThreads], s_b[kThreads], s_rk[kThreads], s_G2[kThreads];  // s_G2 = G log2(e)
   __shared__ int4 s_chunk[2];
 
   const int tid = threadIdx.x, warp = tid >> 5;
@@ -211,11 +217,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   float G = 0.f;
   for (int j = 0; j <= il; ++j) G += s_g[blk * kC + j];
-  s_G[tid] = G;
+  s_G2[tid] = G * kLog2e;  // exp(G_i - G_j) = exp2(G2_i - G2_j)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  const float Glast = len > 0 ? s_G[blk * kC + len - 1] : 0.f;
+  const float Glast2 = len > 0 ? s_G2[blk * kC + len - 1] : 0.f;  // G_last log2(e)
   PTRACE(2);
 
   // Gram products: TMEM cols [0,128) = K K^T, [128,256) = Q K^T (pair-stacked).
@@ -236,7 +242,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* stKt = blk ? sS0 : reinterpret_cast<uint8_t*>(sL);
   if (len > 0) {
     const float fq = valid ? p.scale * rq * expf(G) : 0.f;
-    const float fk = valid ? rk * expf(Glast - G) : 0.f;
+    const float fk = valid ? rk * exp2f(Glast2 - G * kLog2e) : 0.f;
     float* ktt = p.KtT + tile * kTileKtT + il;
 #pragma unroll
     for (int c16 = 0; c16 < 16; ++c16) {
@@ -261,7 +267,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               make_float4(to_tf32(f[e] * fk), to_tf32(f[e + 1] * fk), to_tf32(f[e + 2] * fk), to_tf32(f[e + 3] * fk));
       }
     }
-    if (il == 0) p.gam[tile * kD] = expf(Glast);
+    if (il == 0) p.gam[tile * kD] = exp2f(Glast2);
     if (p.Gc) p.Gc[tile * kC + il] = G;
     if (p.rq) p.rq[tile * kC + il] = rq;
     if (p.rk) p.rk[tile * kC + il] = rk;
@@ -296,7 +302,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
     for (int j = 0; j < kC; ++j) {
       const int pj = blk * kC + j;
-      const float dec = expf(G - s_G[pj]) * s_rk[pj];
+      const float dec = exp2f(G * kLog2e - s_G2[pj]) * s_rk[pj];
       LT[j * kC] = (j < il) ? bi * rk * kk[j] * dec : 0.f;
       qk[j] = (j <= il && valid) ? to_tf32(p.scale * rq * qk[j] * dec) : 0.f;
     }

@@ -64,6 +64,7 @@ __device__ __forceinline__ void inverse_column(const float* __restrict__ LT, flo
       for (int e = 0; e < 16; ++e) y[e] = 0.f;
       // warp-uniform rows (the warp's columns share c & ~31; X[j][c] = 0 for j < c is already
       // in sX), so every L^T row read is a broadcast
+#pragma unroll 4
       for (int j = c & ~31; j < r0; ++j) {
         const float xj = sX[j * kC + c];
         const float4* l4 = reinterpret_cast<const float4*>(LT + j * kC + r0);
@@ -78,9 +79,14 @@ __device__ __forceinline__ void inverse_column(const float* __restrict__ LT, flo
       }
 #pragma unroll
       for (int r = 0; r < 16; ++r) {
-        float acc = y[r];
+        // two interleaved partial sums halve the dependent FMA chain of the 16x16 solve
+        float acc0 = y[r], acc1 = 0.f;
 #pragma unroll
-        for (int j = 0; j < r; ++j) acc = fmaf(-LT[(r0 + j) * kC + r0 + r], x[j], acc);
+        for (int j = 0; j < r; ++j) {
+          if (j & 1) acc1 = fmaf(-LT[(r0 + j) * kC + r0 + r], x[j], acc1);
+          else acc0 = fmaf(-LT[(r0 + j) * kC + r0 + r], x[j], acc0);
+        }
+        const float acc = acc0 + acc1;
         const int R = r0 + r;
         x[r] = (R < c) ? 0.f : ((R == c) ? 1.f : acc);
       }
