@@ -230,14 +230,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* sdAT = sm + kR3 + 16384;
   uint8_t* sA = sm + kR4;
   uint8_t* sX = sm + kR4 + 16384;
+  // a 64-row result read with the 16x64b shape: lane t holds row ri of the warp's 16 at
+  // columns cj + 2 r (all 32 lanes busy)
+  const int ri = 16 * wq + (lane >> 2) + 8 * (lane & 1), cj = 32 * half + ((lane >> 1) & 1);
   {
-    float r[32];
-    tmem_ld32(tl + kTdA + 32 * half, r);
+    float r[16];
+    tmem_ld16x64b_x16(tl + kTdA + 32 * half, r);
     tmem_wait_ld_regs(r);
-    if (owner) {
 #pragma unroll
-      for (int m = 0; m < 32; ++m) put32(sdAT, kC, 32 * half + m, rr, to_tf32(r[m]));
-    }
+    for (int m = 0; m < 16; ++m) put32(sdAT, kC, cj + 2 * m, ri, to_tf32(r[m]));
     {
       // thread groups of 64: 0,1 write A^T (j, i) = A[i][j] for i in their half; 2,3 write
       // A (l = j, m) = A[l][m] for m in their half.
@@ -278,13 +279,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   ok = ok && mbar_wait(&bar_mma, 0, &abort_flag, p.status, kDevTimeoutMma);
   tc_fence_after();
   {
-    float r[32];
-    tmem_ld32(tl + kTX + 32 * half, r);
+    float r[16];
+    tmem_ld16x64b_x16(tl + kTX + 32 * half, r);
     tmem_wait_ld_regs(r);
-    if (owner) {
 #pragma unroll
-      for (int m = 0; m < 32; ++m) put32(sX, kC, rr, 32 * half + m, to_tf32(r[m]));
-    }
+    for (int m = 0; m < 16; ++m) put32(sX, kC, ri, cj + 2 * m, to_tf32(r[m]));
   }
   fence_async_smem();
   tc_fence_before();
@@ -311,44 +310,50 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* sKT = sm + kR3;   // [128][64]: 2 panels x 128 rows
   uint8_t* sQT = sm + kR4;
   {
-    const int i = rr;
+    // the 16x64b TMEM shape spreads a quadrant's 16 rows over all 32 lanes: lane t holds row
+    // (t >> 2) + 8 (t & 1) at columns ((t >> 1) & 1) + 2 r, so a row's 32 columns of this half
+    // sit on the lane pair (t, t ^ 2)
+    const int i = ri;
+    const int jb = cj;
     const bool vi = i < len;
     const float Gi2 = s_G2[i], bi = s_b[i], rki = s_rk[i], rqi = s_rq[i];
     float rowP = 0.f, dbi = 0.f;
     {
-      float dl[32], nn[32], kk[32], qk[32];
-      tmem_ld32(tl + kTdL + 32 * half, dl);
-      tmem_ld32(tl + kTAqk + 32 * half, nn);
-      tmem_ld32(tl + kTKK + 32 * half, kk);
-      tmem_ld32(tl + kTQK + 32 * half, qk);
+      float dl[16], nn[16], kk[16], qk[16];
+      tmem_ld16x64b_x16(tl + kTdL + 32 * half, dl);
+      tmem_ld16x64b_x16(tl + kTAqk + 32 * half, nn);
+      tmem_ld16x64b_x16(tl + kTKK + 32 * half, kk);
+      tmem_ld16x64b_x16(tl + kTQK + 32 * half, qk);
       tmem_wait_ld_regs(dl);
       tmem_wait_ld_regs(nn);
       tmem_wait_ld_regs(kk);
       tmem_wait_ld_regs(qk);
       TTRACE(11);
-      if (owner) {
 #pragma unroll
-        for (int jj = 0; jj < 32; ++jj) {
-          const int j = 32 * half + jj;
-          const float gam = (j <= i && vi) ? exp2f(Gi2 - s_G2[j]) : 0.f;
-          const float D = (j < i && vi) ? -dl[jj] : 0.f;                 // dL_ij
-          const float N = (j <= i && vi) ? nn[jj] : 0.f;                 // dAqk_ij
-          const float Lij = bi * rki * s_rk[j] * kk[jj] * gam;
-          const float Aij = scale * rqi * s_rk[j] * qk[jj] * gam;
-          const float P = D * Lij + N * Aij;
-          rowP += P;
-          s_P[i][j] = P;
-          dbi = fmaf(D * rki * s_rk[j] * kk[jj], gam, dbi);
-          const float e = D * bi * gam;
-          put32(sE1, kC, i, j, to_tf32(e * s_rk[j]));
-          put32(sE2T, kC, j, i, to_tf32(e * rki));
-          const float nq = scale * N * gam;
-          put32(sNq, kC, i, j, to_tf32(nq * s_rk[j]));
-          put32(sNkT, kC, j, i, to_tf32(nq * rqi));
-        }
+      for (int jj = 0; jj < 16; ++jj) {
+        const int j = jb + 2 * jj;
+        const float gam = (j <= i && vi) ? exp2f(Gi2 - s_G2[j]) : 0.f;
+        const float D = (j < i && vi) ? -dl[jj] : 0.f;                 // dL_ij
+        const float N = (j <= i && vi) ? nn[jj] : 0.f;                 // dAqk_ij
+        const float rkj = s_rk[j];
+        const float Lij = bi * rki * rkj * kk[jj] * gam;
+        const float Aij = scale * rqi * rkj * qk[jj] * gam;
+        const float P = D * Lij + N * Aij;
+        rowP += P;
+        s_P[i][j] = P;
+        dbi = fmaf(D * rki * rkj * kk[jj], gam, dbi);
+        const float e = D * bi * gam;
+        put32(sE1, kC, i, j, to_tf32(e * rkj));
+        put32(sE2T, kC, j, i, to_tf32(e * rki));
+        const float nq = scale * N * gam;
+        put32(sNq, kC, i, j, to_tf32(nq * rkj));
+        put32(sNkT, kC, j, i, to_tf32(nq * rqi));
       }
     }
-    if (owner) {
+    // the row's two lanes combine, then one adds the half-row sums
+    rowP += __shfl_xor_sync(0xffffffffu, rowP, 2);
+    dbi += __shfl_xor_sync(0xffffffffu, dbi, 2);
+    if (((lane >> 1) & 1) == 0) {
       atomicAdd(&s_dG[i], rowP);
       atomicAdd(&s_db[i], dbi);
     }

@@ -169,6 +169,17 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const float* r) {
       : "memory");
 }
 
+// 16 lanes x 64 bits, 16 repetitions (32 columns) over the warp: lane t receives row
+// (t >> 2) + 8 (t & 1) of the warp's 16 lanes at columns ((t >> 1) & 1) + 2 r, r = 0..15.
+__device__ __forceinline__ void tmem_ld16x64b_x16(uint32_t taddr, float* r) {
+  uint32_t* u = reinterpret_cast<uint32_t*>(r);
+  asm volatile(
+      "tcgen05.ld.sync.aligned.16x64b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(u[0]), "=r"(u[1]), "=r"(u[2]), "=r"(u[3]), "=r"(u[4]), "=r"(u[5]), "=r"(u[6]), "=r"(u[7]),
+        "=r"(u[8]), "=r"(u[9]), "=r"(u[10]), "=r"(u[11]), "=r"(u[12]), "=r"(u[13]), "=r"(u[14]), "=r"(u[15])
+      : "r"(taddr));
+}
+
 // 32 lanes x 32 consecutive 32-bit columns per thread (no wait; pair with tmem_wait_ld).
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float* r) {
   uint32_t* u = reinterpret_cast<uint32_t*>(r);
