@@ -424,120 +424,142 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   TTRACE(14);
   if (ok) {
+    // eight lanes per token row (lane l8 of the group: features 32 m + 4 l8 + e, m, e < 4, so
+    // the group's loads and stores of one m are 128 contiguous bytes), four rows per warp at a
+    // time, so each 3-level butterfly reduces four rows' dots at once; warp w takes rows
+    // 8 w .. 8 w + 7. Lanes of rows past the chunk run with zeros and store nothing.
     const size_t rowbase = tile * kTileW;
-    const int d0 = 4 * lane;
-    auto bf4 = [&](const uint8_t* tl16, int t, float* f) {
-      const uint2 u = *reinterpret_cast<const uint2*>(tl16 + sw128_offset(t, d0, kC, 2));
-      const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.x));
-      const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.y));
-      f[0] = a.x; f[1] = a.y; f[2] = b.x; f[3] = b.y;
-    };
-    // dq, dk: bf16 at [R,Hk,K] directly, or fp32 per value head [R,H,K] for the group sum
+    const int g = lane >> 3, l8 = lane & 7, d0 = 4 * l8;
     const int Hk = H / p.qk_group;
-    auto store_qk = [&](__nv_bfloat16* dst16, float* dst32, int t, const float* x) {
-      if (dst32) {
-        *reinterpret_cast<float4*>(dst32 + (size_t(ch.x + t) * H + h) * kD + d0) = make_float4(x[0], x[1], x[2], x[3]);
-      } else {
-        __nv_bfloat162 a = __floats2bfloat162_rn(x[0], x[1]), b = __floats2bfloat162_rn(x[2], x[3]);
+    auto sum8 = [](float x) {
+      x += __shfl_xor_sync(0xffffffffu, x, 4);
+      x += __shfl_xor_sync(0xffffffffu, x, 2);
+      x += __shfl_xor_sync(0xffffffffu, x, 1);
+      return x;
+    };
+    // element 4 m + e of a lane's 16 is feature d0 + 32 m + e
+    auto bf16x16 = [&](const uint8_t* tile16, int t, float* f) {
+#pragma unroll
+      for (int m = 0; m < 4; ++m) {
+        const uint2 u = *reinterpret_cast<const uint2*>(tile16 + sw128_offset(t, d0 + 32 * m, kC, 2));
+        const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.x));
+        const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.y));
+        f[4 * m] = a.x; f[4 * m + 1] = a.y; f[4 * m + 2] = b.x; f[4 * m + 3] = b.y;
+      }
+    };
+    auto store16 = [&](__nv_bfloat16* dst, const float* x) {
+#pragma unroll
+      for (int m = 0; m < 4; ++m) {
+        __nv_bfloat162 a = __floats2bfloat162_rn(x[4 * m], x[4 * m + 1]), b = __floats2bfloat162_rn(x[4 * m + 2], x[4 * m + 3]);
         uint2 u;
         u.x = *reinterpret_cast<uint32_t*>(&a);
         u.y = *reinterpret_cast<uint32_t*>(&b);
-        *reinterpret_cast<uint2*>(dst16 + (size_t(ch.x + t) * Hk + h) * kD + d0) = u;
+        *reinterpret_cast<uint2*>(dst + 32 * m) = u;
       }
     };
-    auto store4 = [&](__nv_bfloat16* dst, const float* x) {
-      __nv_bfloat162 a = __floats2bfloat162_rn(x[0], x[1]), b = __floats2bfloat162_rn(x[2], x[3]);
-      uint2 u;
-      u.x = *reinterpret_cast<uint32_t*>(&a);
-      u.y = *reinterpret_cast<uint32_t*>(&b);
-      *reinterpret_cast<uint2*>(dst) = u;
-    };
-    auto allsum = [](float x) {
+    auto load16 = [&](const float* src, bool v, float* f) {   // read-only for this kernel
 #pragma unroll
-      for (int off = 16; off > 0; off >>= 1) x += __shfl_xor_sync(0xffffffffu, x, off);
-      return x;
+      for (int m = 0; m < 4; ++m) {
+        const float4 x = v ? __ldg(reinterpret_cast<const float4*>(src + 32 * m)) : make_float4(0.f, 0.f, 0.f, 0.f);
+        f[4 * m] = x.x; f[4 * m + 1] = x.y; f[4 * m + 2] = x.z; f[4 * m + 3] = x.w;
+      }
     };
-    // rows t = warp + 8 m; each batch of four rows loads its fp32 inputs first (read-only
-    // for this kernel), so their latencies overlap instead of queueing behind the stores
+    auto smem16 = [&](const float* src, float* f) {
+#pragma unroll
+      for (int m = 0; m < 4; ++m) {
+        const float4 x = *reinterpret_cast<const float4*>(src + 32 * m);
+        f[4 * m] = x.x; f[4 * m + 1] = x.y; f[4 * m + 2] = x.z; f[4 * m + 3] = x.w;
+      }
+    };
 #pragma unroll 1
-    for (int m0 = 0; m0 < 8; m0 += 4) {
-      float4 in[4][4];
+    for (int it = 0; it < 2; ++it) {
+      const int t = 8 * warp + 4 * it + g;
+      const bool valid = t < len;
+      const int tt = valid ? t : 0;
+      const size_t ro = rowbase + size_t(tt) * kD + d0;
+      float dqt[16], k1v[16], ktv[16], v1v[16];
+      load16(p.dQt + ro, valid, dqt);
+      load16(p.dK1 + ro, valid, k1v);
+      load16(p.dKt + ro, valid, ktv);
+      load16(p.dV1 + ro, valid, v1v);
+      const float Gt = s_G[tt], rqt = s_rq[tt], rkt = s_rk[tt], bt = s_b[tt];
+      const float eG = expf(Gt), eL = expf(Glast - Gt);
+      const size_t orow = (size_t(ch.x + tt) * H + h) * kD + d0;
+      const size_t oqk = (size_t(ch.x + tt) * Hk + h / p.qk_group) * kD + d0;
+      float x[16];
+      // dq
+      float dot = 0.f, qdq = 0.f;
+      {
+        float qv[16], a[16], rq[16];
+        bf16x16(sQ, tt, qv);
+        smem16(sRq + tt * kPad + d0, rq);
 #pragma unroll
-      for (int m = 0; m < 4; ++m) {
-        const int t = warp + 8 * (m0 + m);
-        const size_t ro = rowbase + size_t(t) * kD + d0;
-        if (t < len) {
-          in[m][0] = __ldg(reinterpret_cast<const float4*>(p.dQt + ro));
-          in[m][1] = __ldg(reinterpret_cast<const float4*>(p.dK1 + ro));
-          in[m][2] = __ldg(reinterpret_cast<const float4*>(p.dKt + ro));
-          in[m][3] = __ldg(reinterpret_cast<const float4*>(p.dV1 + ro));
-        }
-      }
-#pragma unroll
-      for (int m = 0; m < 4; ++m) {
-        const int t = warp + 8 * (m0 + m);
-        if (t >= len) break;
-        const float Gt = s_G[t], rqt = s_rq[t], rkt = s_rk[t], bt = s_b[t];
-        const float eG = expf(Gt), eL = expf(Glast - Gt);
-        const size_t orow = (size_t(ch.x + t) * H + h) * kD + d0;
-        // dq
-        float qv[4], a[4], x[4];
-        bf4(sQ, t, qv);
-        const float4 dqt = in[m][0];
-        const float4 rq4 = *reinterpret_cast<const float4*>(sRq + t * kPad + d0);
-        const float dqtv[4] = {dqt.x, dqt.y, dqt.z, dqt.w}, rqv[4] = {rq4.x, rq4.y, rq4.z, rq4.w};
-        float dot = 0.f, qdq = 0.f;
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
+        for (int e = 0; e < 16; ++e) {
           const float qh = rqt * qv[e];
-          a[e] = fmaf(scale * eG, dqtv[e], rqv[e]);
+          a[e] = fmaf(scale * eG, dqt[e], rq[e]);
           dot = fmaf(a[e], qh, dot);
-          qdq = fmaf(dqtv[e], qh, qdq);
+          qdq = fmaf(dqt[e], qh, qdq);
         }
-        dot = allsum(dot);
-        qdq = allsum(qdq);
+        dot = sum8(dot);
+        qdq = sum8(qdq);
         if (!p.l2norm) dot = 0.f;
 #pragma unroll
-        for (int e = 0; e < 4; ++e) x[e] = rqt * (a[e] - rqt * qv[e] * dot);
-        store_qk(p.dq, p.dq32, t, x);
-        // dk
-        float kv[4];
-        bf4(sK, t, kv);
-        const float4 k1 = in[m][1];
-        const float4 kt = in[m][2];
-        const float4 rk4 = *reinterpret_cast<const float4*>(sRk + t * kPad + d0);
-        const float k1v[4] = {k1.x, k1.y, k1.z, k1.w}, ktv[4] = {kt.x, kt.y, kt.z, kt.w};
-        const float rkv[4] = {rk4.x, rk4.y, rk4.z, rk4.w};
-        float kdot = 0.f, k1k = 0.f, ktk = 0.f;
+        for (int e = 0; e < 16; ++e) x[e] = rqt * (a[e] - rqt * qv[e] * dot);
+      }
+      if (valid) {
+        if (p.dq32) {
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
+          for (int m = 0; m < 4; ++m)
+            *reinterpret_cast<float4*>(p.dq32 + orow + 32 * m) = make_float4(x[4 * m], x[4 * m + 1], x[4 * m + 2], x[4 * m + 3]);
+        } else {
+          store16(p.dq + oqk, x);
+        }
+      }
+      // dk
+      float kdot = 0.f, k1k = 0.f, ktk = 0.f;
+      {
+        float kv[16], a[16], rk[16];
+        bf16x16(sK, tt, kv);
+        smem16(sRk + tt * kPad + d0, rk);
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
           const float kh = rkt * kv[e];
-          a[e] = rkv[e] + bt * eG * k1v[e] + eL * ktv[e];
+          a[e] = rk[e] + bt * eG * k1v[e] + eL * ktv[e];
           kdot = fmaf(a[e], kh, kdot);
           k1k = fmaf(k1v[e], kh, k1k);
           ktk = fmaf(ktv[e], kh, ktk);
         }
-        kdot = allsum(kdot);
-        k1k = allsum(k1k);
-        ktk = allsum(ktk);
+        kdot = sum8(kdot);
+        k1k = sum8(k1k);
+        ktk = sum8(ktk);
         if (!p.l2norm) kdot = 0.f;
 #pragma unroll
-        for (int e = 0; e < 4; ++e) x[e] = rkt * (a[e] - rkt * kv[e] * kdot);
-        store_qk(p.dk, p.dk32, t, x);
-        // dv and the v part of dbeta
-        float vv4[4];
-        bf4(sV, t, vv4);
-        const float4 v1 = in[m][3];
-        const float v1v[4] = {v1.x, v1.y, v1.z, v1.w};
-        float vv = 0.f;
+        for (int e = 0; e < 16; ++e) x[e] = rkt * (a[e] - rkt * kv[e] * kdot);
+      }
+      if (valid) {
+        if (p.dk32) {
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          vv = fmaf(v1v[e], vv4[e], vv);
+          for (int m = 0; m < 4; ++m)
+            *reinterpret_cast<float4*>(p.dk32 + orow + 32 * m) = make_float4(x[4 * m], x[4 * m + 1], x[4 * m + 2], x[4 * m + 3]);
+        } else {
+          store16(p.dk + oqk, x);
+        }
+      }
+      // dv and the v part of dbeta
+      float vv = 0.f;
+      {
+        float vvv[16];
+        bf16x16(sV, tt, vvv);
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          vv = fmaf(v1v[e], vvv[e], vv);
           x[e] = bt * v1v[e];
         }
-        vv = allsum(vv);
-        store4(p.dv + orow, x);
-        if (lane == 0) {
+        vv = sum8(vv);
+      }
+      if (valid) {
+        store16(p.dv + orow, x);
+        if (l8 == 0) {
           s_dG[t] += scale * eG * qdq + bt * eG * k1k - eL * ktk;
           s_db[t] += eG * k1k + vv;
           s_P[t][0] = eL * ktk;   // this row's share of dG_last (column 0 of P is free now)
