@@ -569,15 +569,25 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   __syncthreads();
   TTRACE(9);
-  if (tid == 0 && ok) {
-    // gate: G_last collects the end-decay terms; reverse cumulative sum gives dg.
-    const float dgam = p.dgam[tile * kD];
-    float acc = expf(Glast) * dgam;
-    for (int t = 0; t < len; ++t) acc += s_P[t][0];
-    for (int t = len - 1; t >= 0; --t) {
-      acc += s_dG[t];
-      s_dG[t] = acc;
+  if (warp == 0 && ok) {
+    // gate: G_last collects the end-decay terms; the reverse cumulative sum gives dg. Lane l
+    // holds rows 2 l and 2 l + 1; a suffix scan over the lanes replaces the serial loop.
+    const int t0 = 2 * lane, t1 = 2 * lane + 1;
+    float base = (t0 < len ? s_P[t0][0] : 0.f) + (t1 < len ? s_P[t1][0] : 0.f);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) base += __shfl_xor_sync(0xffffffffu, base, off);
+    base += expf(Glast) * p.dgam[tile * kD];
+    const float a0 = t0 < len ? s_dG[t0] : 0.f, a1 = t1 < len ? s_dG[t1] : 0.f;
+    const float pair = a0 + a1;
+    float suf = pair;   // inclusive suffix sum over lanes >= l
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const float y = __shfl_down_sync(0xffffffffu, suf, off);
+      if (lane + off < 32) suf += y;
     }
+    const float after = base + suf - pair;   // rows past 2 l + 1
+    if (t1 < len) s_dG[t1] = after + a1;
+    if (t0 < len) s_dG[t0] = after + a1 + a0;
   }
   __syncthreads();
   if (tid < len && ok) {
