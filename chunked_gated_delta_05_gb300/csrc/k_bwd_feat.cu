@@ -11,14 +11,28 @@
 //   dV1  = A^T dv_new        (gradient of beta v,        the right factor of U = A V1)
 //   dgam = sum over v of h (.) dh'   (per key row; summed over keys for the scalar gate)
 // GB300 mapping: one CTA per chunk and head, 128 threads, thread f = feature f = TMEM lane f.
-// h and dh' rows are staged through shared memory (coalesced) and stored to TMEM (tf32) by
-// their lane owner as A operands of kind::tf32 MMAs; dO^T, v_new, dv_new and A^T are SW128 K-major B operands in shared memory
+// h and dh' rows are loaded by their lane owner (thread f reads row f) and stored to TMEM (tf32)
+// as A operands of kind::tf32 MMAs; dO^T, v_new, dv_new and A^T are SW128 K-major B operands in shared memory
 // (v_new, dv_new by TMA). Results leave as token-major fp32 rows [t][f] (coalesced: the 128
 // threads of one token row write 512 contiguous bytes).
 #include "common.cuh"
 #include "umma.cuh"
 
 namespace gdn {
+
+#ifdef GDN_TRACE
+__device__ unsigned long long g_trace_feat[4 * 16];
+#define FTRACE(slot)                                                                                    \
+  do {                                                                                                  \
+    if (blockIdx.y == 3 && threadIdx.x == 0 && blockIdx.x % 32 == 5 && blockIdx.x < 128)                \
+      g_trace_feat[(blockIdx.x / 32) * 16 + (slot)] = globaltimer();                                     \
+  } while (0)
+extern "C" int gdn_trace_feat_read(unsigned long long* host) {
+  return cudaMemcpyFromSymbol(host, g_trace_feat, sizeof(g_trace_feat)) == cudaSuccess ? 0 : -1;
+}
+#else
+#define FTRACE(slot) do {} while (0)
+#endif
 
 namespace {
 
@@ -46,13 +60,25 @@ __global__ void __launch_bounds__(kThreads, 1)
   __shared__ uint32_t tslot;
   __shared__ int abort_flag;
   __shared__ float s_red[4];
-  __shared__ float s_stage[4 * 2 * 32 * 33];
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int c = blockIdx.x, h = blockIdx.y, H = p.H;
   const size_t tile = size_t(c) * H + h;
-  const ChunkEntry ch = p.chunks[c];
   const int f = tid;
+  FTRACE(0);
+  // h and dh' row f (thread f = TMEM lane f): the first 64 columns of both are requested before
+  // the setup below, the last 64 right after it (each thread reads its own 512-byte rows; the
+  // group of loads of one instruction touches 32 rows, every sector of which is used by the
+  // thread's neighbouring loads)
+  const float4* hrow = reinterpret_cast<const float4*>(p.h + tile * kD * kD + size_t(f) * kD);
+  const float4* drow = reinterpret_cast<const float4*>(p.dh + tile * kD * kD + size_t(f) * kD);
+  float4 hv[16], dv4[16];
+#pragma unroll
+  for (int e = 0; e < 16; ++e) {
+    hv[e] = __ldg(hrow + e);
+    dv4[e] = __ldg(drow + e);
+  }
+  const ChunkEntry ch = p.chunks[c];
 
   if (warp == 0) tmem_alloc(&tslot, 512);
   if (tid == 0) {
@@ -73,57 +99,38 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_load_2d(sm + kOffDVN + pp * 8192, &mDVN, pp * 32, int(tile) * kC, &bar_tma);
     }
     for (int pp = 0; pp < 2; ++pp) tma_load_2d(sm + kOffDO16 + pp * 8192, &mdO, h * kD + 64 * pp, ch.x, &bar_tma);
-    // the next wave's CTA finds its inputs in L2
-    int nx, ny;
-    if (next_wave_block(p.sms, &nx, &ny)) {
-      const size_t nt = size_t(nx) * H + ny;
-      prefetch_l2(p.h + nt * kD * kD, 4u * kD * kD);
-      prefetch_l2(p.dh + nt * kD * kD, 4u * kD * kD);
-      prefetch_l2(p.A + nt * kTileAqk, 4u * kTileAqk);
-      for (int pp = 0; pp < 4; ++pp) {
-        prefetch_l2_tile(&mVN, pp * 32, int(nt) * kC);
-        prefetch_l2_tile(&mDVN, pp * 32, int(nt) * kC);
-      }
-      const ChunkEntry nch = p.chunks[nx];
-      for (int pp = 0; pp < 2; ++pp) prefetch_l2_tile(&mdO, ny * kD + 64 * pp, nch.x);
-    }
   }
-  // h and dh' rows -> TMEM (tf32 A operands); dgam partial sums in fp32. Each warp stages its
-  // 32 rows in 32-column groups through shared memory so the global reads are coalesced
-  // (a lane reads 16 B of a row, 8 lanes cover 128 contiguous bytes), then every thread
-  // picks up its own row from the padded staging tile.
+  FTRACE(1);
+  // h and dh' rows -> TMEM (tf32 A operands); dgam partial sums in fp32
   float dg = 0.f;
-  {
-    float* stg_h = s_stage + warp * (2 * 32 * 33);
-    float* stg_d = stg_h + 32 * 33;
-    const float* hb = p.h + tile * kD * kD + size_t(32 * warp) * kD;
-    const float* db = p.dh + tile * kD * kD + size_t(32 * warp) * kD;
-    for (int g4 = 0; g4 < 4; ++g4) {
 #pragma unroll
-      for (int it = 0; it < 8; ++it) {
-        const int row = 4 * it + (lane >> 3), col = 4 * (lane & 7);
-        const float4 x = *reinterpret_cast<const float4*>(hb + size_t(row) * kD + 32 * g4 + col);
-        const float4 y = *reinterpret_cast<const float4*>(db + size_t(row) * kD + 32 * g4 + col);
-        float* sh = stg_h + row * 33 + col;
-        float* sd = stg_d + row * 33 + col;
-        sh[0] = x.x; sh[1] = x.y; sh[2] = x.z; sh[3] = x.w;
-        sd[0] = y.x; sd[1] = y.y; sd[2] = y.z; sd[3] = y.w;
+  for (int half = 0; half < 2; ++half) {
+    if (half == 1) {
+#pragma unroll
+      for (int e = 0; e < 16; ++e) {
+        hv[e] = __ldg(hrow + 16 + e);
+        dv4[e] = __ldg(drow + 16 + e);
       }
-      __syncwarp();
+    }
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
       float a[32], b[32];
 #pragma unroll
-      for (int e = 0; e < 32; ++e) {
-        a[e] = stg_h[lane * 33 + e];
-        b[e] = stg_d[lane * 33 + e];
-        dg = fmaf(a[e], b[e], dg);
-        a[e] = to_tf32(a[e]);
-        b[e] = to_tf32(b[e]);
+      for (int e = 0; e < 8; ++e) {
+        const float4 x = hv[8 * q + e], y = dv4[8 * q + e];
+        const float xs[4] = {x.x, x.y, x.z, x.w}, ys[4] = {y.x, y.y, y.z, y.w};
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          dg = fmaf(xs[u], ys[u], dg);
+          a[4 * e + u] = to_tf32(xs[u]);
+          b[4 * e + u] = to_tf32(ys[u]);
+        }
       }
-      __syncwarp();
-      tmem_st32(tl + kTH + 32 * g4, a);
-      tmem_st32(tl + kTDH + 32 * g4, b);
+      tmem_st32(tl + kTH + 64 * half + 32 * q, a);
+      tmem_st32(tl + kTDH + 64 * half + 32 * q, b);
     }
   }
+  FTRACE(2);
   // A^T operand: element (j, i) = A[i][j]; thread pairs split the 64 rows i of column j = f % 64.
   {
     const int j = f & 63, i0 = (f >> 6) * 32;
@@ -134,6 +141,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
     for (int e = 0; e < 32; ++e) *reinterpret_cast<float*>(sm + kOffAT + sw128_offset(j, i0 + e, kC, 4)) = to_tf32(buf[e]);
   }
+  FTRACE(3);
   // dO^T operand: element (t, v=f) of the K-major [t][v] tile from the bf16 TMA tile; rows past
   // the chunk (the next document's, or out of range) are zero.
   const bool tma_ok = mbar_wait(&bar_tma, 0, &abort_flag, p.status, kDevTimeoutTma);
@@ -151,6 +159,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  FTRACE(4);
 
   if (tid == 0) {
     if (tma_ok) {
@@ -162,9 +171,22 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int s = 0; s < 16; ++s) mma_tf32_ts(tb + kTP3, tb + kTDH + s * 8, desc_kmajor(sVN, 8192, s), id64, s > 0);
       mma_commit(&bar_mma);
     }
+    // while the products run: the next wave's CTA finds its inputs in L2
+    int nx, ny;
+    if (next_wave_block(p.sms, &nx, &ny)) {
+      const size_t nt = size_t(nx) * H + ny;
+      prefetch_l2(p.h + nt * kD * kD, 4u * kD * kD);
+      prefetch_l2(p.dh + nt * kD * kD, 4u * kD * kD);
+      prefetch_l2(p.A + nt * kTileAqk, 4u * kTileAqk);
+      for (int pp = 0; pp < 4; ++pp) {
+        prefetch_l2_tile(&mVN, pp * 32, int(nt) * kC);
+        prefetch_l2_tile(&mDVN, pp * 32, int(nt) * kC);
+      }
+    }
   }
   __syncwarp();
   const bool ok = mbar_wait(&bar_mma, 0, &abort_flag, p.status, kDevTimeoutMma);
+  FTRACE(5);
   tc_fence_after();
   if (ok) {
     float r[64];
@@ -211,7 +233,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     mma_commit(&bar_mma);
   }
   __syncwarp();
+  FTRACE(6);
   const bool ok2 = ok && mbar_wait(&bar_mma, 1, &abort_flag, p.status, kDevTimeoutMma);
+  FTRACE(7);
   tc_fence_after();
   if (ok2) {
     float r[64];
@@ -226,6 +250,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
     for (int t = 0; t < kC; ++t) v1[size_t(t) * kD] = r[t];
   }
+  FTRACE(8);
   // dgam: per key row (KDA) or summed over the block (GDN).
   if (p.kda) {
     p.dgam[tile * kD + f] = dg;
