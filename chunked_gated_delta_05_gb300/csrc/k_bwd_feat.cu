@@ -10,11 +10,12 @@
 //   dK1  = A^T dW            (gradient of beta exp(G) k^, the right factor of W = A K1)
 //   dV1  = A^T dv_new        (gradient of beta v,        the right factor of U = A V1)
 //   dgam = sum over v of h (.) dh'   (per key row; summed over keys for the scalar gate)
-// GB300 mapping: one CTA per chunk and head, 128 threads, thread f = feature f = TMEM lane f.
-// h and dh' rows are loaded by their lane owner (thread f reads row f) and stored to TMEM (tf32)
-// as A operands of kind::tf32 MMAs; dO^T, v_new, dv_new and A^T are SW128 K-major B operands in shared memory
-// (v_new, dv_new by TMA). Results leave as token-major fp32 rows [t][f] (coalesced: the 128
-// threads of one token row write 512 contiguous bytes).
+// GB300 mapping: one CTA per chunk and head, 256 threads; threads f and f + 128 own feature f
+// (= TMEM lane f) and split its columns in halves. h and dh' rows are loaded by their lane
+// owners and stored to TMEM (tf32) as A operands of kind::tf32 MMAs; dO^T, v_new, dv_new and A^T
+// are SW128 K-major B operands in shared memory (v_new, dv_new by TMA). Results leave as
+// token-major fp32 rows [t][f] (coalesced: the 128 threads of one token row write 512
+// contiguous bytes).
 #include "common.cuh"
 #include "umma.cuh"
 
@@ -36,7 +37,7 @@ extern "C" int gdn_trace_feat_read(unsigned long long* host) {
 
 namespace {
 
-constexpr int kThreads = 128;
+constexpr int kThreads = 256;
 constexpr uint32_t kOffDO = 0;        // dO   [t][v] tf32, 4 panels x 64 rows (32 KB)
 constexpr uint32_t kOffVN = 32768;    // v_new [t][v] (TMA)
 constexpr uint32_t kOffDVN = 65536;   // dv_new [t][v] (TMA)
@@ -59,19 +60,19 @@ __global__ void __launch_bounds__(kThreads, 1)
   __shared__ uint64_t bar_tma, bar_mma;
   __shared__ uint32_t tslot;
   __shared__ int abort_flag;
-  __shared__ float s_red[4];
+  __shared__ float s_red[8];
+  __shared__ float s_dg[kThreads];
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int c = blockIdx.x, h = blockIdx.y, H = p.H;
   const size_t tile = size_t(c) * H + h;
-  const int f = tid;
+  const int f = tid & 127, hf = tid >> 7;  // feature (TMEM lane) and column half
   FTRACE(0);
-  // h and dh' row f (thread f = TMEM lane f): the first 64 columns of both are requested before
-  // the setup below, the last 64 right after it (each thread reads its own 512-byte rows; the
-  // group of loads of one instruction touches 32 rows, every sector of which is used by the
-  // thread's neighbouring loads)
-  const float4* hrow = reinterpret_cast<const float4*>(p.h + tile * kD * kD + size_t(f) * kD);
-  const float4* drow = reinterpret_cast<const float4*>(p.dh + tile * kD * kD + size_t(f) * kD);
+  // Half hf of h and dh' row f, requested before the setup below (each thread reads 256
+  // contiguous bytes of each; the loads of one instruction touch 32 rows, every sector of
+  // which is used by the thread's neighbouring loads).
+  const float4* hrow = reinterpret_cast<const float4*>(p.h + tile * kD * kD + size_t(f) * kD + 64 * hf);
+  const float4* drow = reinterpret_cast<const float4*>(p.dh + tile * kD * kD + size_t(f) * kD + 64 * hf);
   float4 hv[16], dv4[16];
 #pragma unroll
   for (int e = 0; e < 16; ++e) {
@@ -104,50 +105,40 @@ __global__ void __launch_bounds__(kThreads, 1)
   // h and dh' rows -> TMEM (tf32 A operands); dgam partial sums in fp32
   float dg = 0.f;
 #pragma unroll
-  for (int half = 0; half < 2; ++half) {
-    if (half == 1) {
+  for (int q = 0; q < 2; ++q) {
+    float a[32], b[32];
 #pragma unroll
-      for (int e = 0; e < 16; ++e) {
-        hv[e] = __ldg(hrow + 16 + e);
-        dv4[e] = __ldg(drow + 16 + e);
+    for (int e = 0; e < 8; ++e) {
+      const float4 x = hv[8 * q + e], y = dv4[8 * q + e];
+      const float xs[4] = {x.x, x.y, x.z, x.w}, ys[4] = {y.x, y.y, y.z, y.w};
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        dg = fmaf(xs[u], ys[u], dg);
+        a[4 * e + u] = to_tf32(xs[u]);
+        b[4 * e + u] = to_tf32(ys[u]);
       }
     }
-#pragma unroll
-    for (int q = 0; q < 2; ++q) {
-      float a[32], b[32];
-#pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        const float4 x = hv[8 * q + e], y = dv4[8 * q + e];
-        const float xs[4] = {x.x, x.y, x.z, x.w}, ys[4] = {y.x, y.y, y.z, y.w};
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          dg = fmaf(xs[u], ys[u], dg);
-          a[4 * e + u] = to_tf32(xs[u]);
-          b[4 * e + u] = to_tf32(ys[u]);
-        }
-      }
-      tmem_st32(tl + kTH + 64 * half + 32 * q, a);
-      tmem_st32(tl + kTDH + 64 * half + 32 * q, b);
-    }
+    tmem_st32(tl + kTH + 64 * hf + 32 * q, a);
+    tmem_st32(tl + kTDH + 64 * hf + 32 * q, b);
   }
   FTRACE(2);
-  // A^T operand: element (j, i) = A[i][j]; thread pairs split the 64 rows i of column j = f % 64.
+  // A^T operand: element (j, i) = A[i][j]; four threads split the 64 rows i of column j = tid % 64.
   {
-    const int j = f & 63, i0 = (f >> 6) * 32;
+    const int j = tid & 63, i0 = (tid >> 6) * 16;
     const float* a = p.A + tile * kTileAqk + j;
-    float buf[32];
+    float buf[16];
 #pragma unroll
-    for (int e = 0; e < 32; ++e) buf[e] = a[size_t(i0 + e) * kC];
+    for (int e = 0; e < 16; ++e) buf[e] = a[size_t(i0 + e) * kC];
 #pragma unroll
-    for (int e = 0; e < 32; ++e) *reinterpret_cast<float*>(sm + kOffAT + sw128_offset(j, i0 + e, kC, 4)) = to_tf32(buf[e]);
+    for (int e = 0; e < 16; ++e) *reinterpret_cast<float*>(sm + kOffAT + sw128_offset(j, i0 + e, kC, 4)) = to_tf32(buf[e]);
   }
   FTRACE(3);
-  // dO^T operand: element (t, v=f) of the K-major [t][v] tile from the bf16 TMA tile; rows past
-  // the chunk (the next document's, or out of range) are zero.
+  // dO^T operand: element (t, v=f) of the K-major [t][v] tile from the bf16 TMA tile (half hf
+  // of the tokens); rows past the chunk (the next document's, or out of range) are zero.
   const bool tma_ok = mbar_wait(&bar_tma, 0, &abort_flag, p.status, kDevTimeoutTma);
   if (tma_ok) {
 #pragma unroll 8
-    for (int t = 0; t < kC; ++t) {
+    for (int t = 32 * hf; t < 32 * hf + 32; ++t) {
       const float x = t < ch.y ? __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(
                                      sm + kOffDO16 + sw128_offset(t, f, kC, 2)))
                                : 0.f;
@@ -189,37 +180,37 @@ __global__ void __launch_bounds__(kThreads, 1)
   FTRACE(5);
   tc_fence_after();
   if (ok) {
-    float r[64];
+    // this thread's tokens t = t0 + e of the 64-token columns
+    const int t0 = 32 * hf;
+    float r[32];
     // dQt and dKt: token-major rows
-    tmem_ld64(tl + kTP1, r);
+    tmem_ld32(tl + kTP1 + t0, r);
     tmem_wait_ld_regs(r);
-    float* dq = p.dQt + tile * kTileW + f;
+    float* dq = p.dQt + tile * kTileW + size_t(t0) * kD + f;
 #pragma unroll
-    for (int t = 0; t < kC; ++t) dq[size_t(t) * kD] = r[t];
-    tmem_ld64(tl + kTP3, r);
+    for (int e = 0; e < 32; ++e) dq[size_t(e) * kD] = r[e];
+    tmem_ld32(tl + kTP3 + t0, r);
     tmem_wait_ld_regs(r);
-    float* dk = p.dKt + tile * kTileW + f;
+    float* dk = p.dKt + tile * kTileW + size_t(t0) * kD + f;
 #pragma unroll
-    for (int t = 0; t < kC; ++t) dk[size_t(t) * kD] = r[t];
+    for (int e = 0; e < 32; ++e) dk[size_t(e) * kD] = r[e];
     // dW^T = -(h dv_new^T): saved token-major (tf32, an MMA operand later) and written back
     // to TMEM as the A operand of A^T dW.
-    tmem_ld64(tl + kTP2, r);
+    tmem_ld32(tl + kTP2 + t0, r);
     tmem_wait_ld_regs(r);
-    float* dw = p.dW + tile * kTileW + f;
+    float* dw = p.dW + tile * kTileW + size_t(t0) * kD + f;
 #pragma unroll
-    for (int t = 0; t < kC; ++t) {
-      r[t] = to_tf32(-r[t]);
-      dw[size_t(t) * kD] = r[t];
+    for (int e = 0; e < 32; ++e) {
+      r[e] = to_tf32(-r[e]);
+      dw[size_t(e) * kD] = r[e];
     }
-    tmem_st32(tl + kTP2, r);
-    tmem_st32(tl + kTP2 + 32, r + 32);
+    tmem_st32(tl + kTP2 + t0, r);
     // dv_new^T row f (lane f = value column f) as the A operand of A^T dv_new (reuses h's
     // columns), read from the TMA copy of dv_new already in shared memory.
 #pragma unroll
-    for (int t = 0; t < kC; ++t)
-      r[t] = to_tf32(*reinterpret_cast<const float*>(sm + kOffDVN + sw128_offset(t, f, kC, 4)));
-    tmem_st32(tl + kTH, r);
-    tmem_st32(tl + kTH + 32, r + 32);
+    for (int e = 0; e < 32; ++e)
+      r[e] = to_tf32(*reinterpret_cast<const float*>(sm + kOffDVN + sw128_offset(t0 + e, f, kC, 4)));
+    tmem_st32(tl + kTH + t0, r);
     tmem_wait_st();
   }
   tc_fence_before();
@@ -238,22 +229,23 @@ __global__ void __launch_bounds__(kThreads, 1)
   FTRACE(7);
   tc_fence_after();
   if (ok2) {
-    float r[64];
-    tmem_ld64(tl + kTP5, r);
+    const int t0 = 32 * hf;
+    float r[32];
+    tmem_ld32(tl + kTP5 + t0, r);
     tmem_wait_ld_regs(r);
-    float* k1 = p.dK1 + tile * kTileW + f;
+    float* k1 = p.dK1 + tile * kTileW + size_t(t0) * kD + f;
 #pragma unroll
-    for (int t = 0; t < kC; ++t) k1[size_t(t) * kD] = r[t];
-    tmem_ld64(tl + kTDH, r);
+    for (int e = 0; e < 32; ++e) k1[size_t(e) * kD] = r[e];
+    tmem_ld32(tl + kTDH + t0, r);
     tmem_wait_ld_regs(r);
-    float* v1 = p.dV1 + tile * kTileW + f;
+    float* v1 = p.dV1 + tile * kTileW + size_t(t0) * kD + f;
 #pragma unroll
-    for (int t = 0; t < kC; ++t) v1[size_t(t) * kD] = r[t];
+    for (int e = 0; e < 32; ++e) v1[size_t(e) * kD] = r[e];
   }
   FTRACE(8);
-  // dgam: per key row (KDA) or summed over the block (GDN).
+  // dgam: per key row (KDA: the two column halves of row f) or summed over the block (GDN).
   if (p.kda) {
-    p.dgam[tile * kD + f] = dg;
+    s_dg[tid] = dg;
   } else {
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) dg += __shfl_xor_sync(0xffffffffu, dg, off);
@@ -261,7 +253,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   tc_fence_before();
   __syncthreads();
-  if (!p.kda && tid == 0) p.dgam[tile * kD] = s_red[0] + s_red[1] + s_red[2] + s_red[3];
+  if (p.kda) {
+    if (hf == 0) p.dgam[tile * kD + f] = s_dg[f] + s_dg[f + 128];
+  } else if (tid == 0) {
+    float sum = 0.f;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) sum += s_red[w];
+    p.dgam[tile * kD] = sum;
+  }
   if (warp == 0) tmem_dealloc(tb, 512);
 }
 
