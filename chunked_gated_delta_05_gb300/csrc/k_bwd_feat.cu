@@ -38,13 +38,16 @@ extern "C" int gdn_trace_feat_read(unsigned long long* host) {
 namespace {
 
 constexpr int kThreads = 256;
-constexpr uint32_t kOffDO = 0;        // dO   [t][v] tf32, 4 panels x 64 rows (32 KB)
-constexpr uint32_t kOffVN = 32768;    // v_new [t][v] (TMA)
-constexpr uint32_t kOffDVN = 65536;   // dv_new [t][v] (TMA)
+// [dO ; dv_new] as one 128-row operand [t][v] tf32, 4 panels x 128 rows (64 KB): rows 0-63 dO
+// (converted from the bf16 tile), rows 64-127 dv_new (TMA), so h dO^T and h dv_new^T are one
+// N = 128 product.
+constexpr uint32_t kOffC = 0;
+constexpr uint32_t kOffVN = 65536;    // v_new [t][v] (TMA), 4 panels x 64 rows
 constexpr uint32_t kOffAT = 98304;    // A^T  [j][i] tf32, 2 panels x 64 rows (16 KB)
 constexpr uint32_t kOffDO16 = 114688; // dO   [t][v] bf16 (TMA), 2 panels x 64 rows (16 KB)
 constexpr uint32_t kSmemBytes = 131072 + 1024;
 constexpr uint32_t kTH = 0, kTDH = 128, kTP1 = 256, kTP2 = 320, kTP3 = 384, kTP5 = 448;
+static_assert(kTP2 == kTP1 + 64, "h [dO ; dv_new]^T lands in P1 | P2");
 
 __device__ __forceinline__ uint8_t* align1k(uint8_t* p) {
   return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
@@ -68,6 +71,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const size_t tile = size_t(c) * H + h;
   const int f = tid & 127, hf = tid >> 7;  // feature (TMEM lane) and column half
   FTRACE(0);
+  const ChunkEntry ch = p.chunks[c];  // requested first: the dO load below waits on it
   // Half hf of h and dh' row f, requested before the setup below (each thread reads 256
   // contiguous bytes of each; the loads of one instruction touch 32 rows, every sector of
   // which is used by the thread's neighbouring loads).
@@ -79,28 +83,26 @@ __global__ void __launch_bounds__(kThreads, 1)
     hv[e] = __ldg(hrow + e);
     dv4[e] = __ldg(drow + e);
   }
-  const ChunkEntry ch = p.chunks[c];
 
   if (warp == 0) tmem_alloc(&tslot, 512);
   if (tid == 0) {
+    // the barriers are this thread's alone until the block barrier below: start the loads now
     abort_flag = 0;
     mbar_init(&bar_tma, 1);
     mbar_init(&bar_mma, 1);
     fence_mbar_init();
+    mbar_expect_tx(&bar_tma, 65536u + 16384u);
+    for (int pp = 0; pp < 4; ++pp) {
+      tma_load_2d(sm + kOffVN + pp * 8192, &mVN, pp * 32, int(tile) * kC, &bar_tma);
+      tma_load_2d(sm + kOffC + pp * 16384 + 8192, &mDVN, pp * 32, int(tile) * kC, &bar_tma);
+    }
+    for (int pp = 0; pp < 2; ++pp) tma_load_2d(sm + kOffDO16 + pp * 8192, &mdO, h * kD + 64 * pp, ch.x, &bar_tma);
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tb = tslot;
   const uint32_t tl = tb + tmem_lane_base(warp);
-  if (tid == 0) {
-    mbar_expect_tx(&bar_tma, 65536u + 16384u);
-    for (int pp = 0; pp < 4; ++pp) {
-      tma_load_2d(sm + kOffVN + pp * 8192, &mVN, pp * 32, int(tile) * kC, &bar_tma);
-      tma_load_2d(sm + kOffDVN + pp * 8192, &mDVN, pp * 32, int(tile) * kC, &bar_tma);
-    }
-    for (int pp = 0; pp < 2; ++pp) tma_load_2d(sm + kOffDO16 + pp * 8192, &mdO, h * kD + 64 * pp, ch.x, &bar_tma);
-  }
   FTRACE(1);
   // h and dh' rows -> TMEM (tf32 A operands); dgam partial sums in fp32
   float dg = 0.f;
@@ -142,7 +144,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float x = t < ch.y ? __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(
                                      sm + kOffDO16 + sw128_offset(t, f, kC, 2)))
                                : 0.f;
-      *reinterpret_cast<float*>(sm + kOffDO + sw128_offset(t, f, kC, 4)) = x;
+      *reinterpret_cast<float*>(sm + kOffC + sw128_offset(t, f, 2 * kC, 4)) = x;
     }
   }
   tmem_wait_st();
@@ -155,10 +157,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (tid == 0) {
     if (tma_ok) {
       tc_fence_after();
-      const uint32_t id64 = idesc_tf32(128, 64);
-      const uint32_t sDO = smem_u32(sm + kOffDO), sVN = smem_u32(sm + kOffVN), sDVN = smem_u32(sm + kOffDVN);
-      for (int s = 0; s < 16; ++s) mma_tf32_ts(tb + kTP1, tb + kTH + s * 8, desc_kmajor(sDO, 8192, s), id64, s > 0);
-      for (int s = 0; s < 16; ++s) mma_tf32_ts(tb + kTP2, tb + kTH + s * 8, desc_kmajor(sDVN, 8192, s), id64, s > 0);
+      const uint32_t id64 = idesc_tf32(128, 64), id128 = idesc_tf32(128, 128);
+      const uint32_t sC = smem_u32(sm + kOffC), sVN = smem_u32(sm + kOffVN);
+      // [P1 | P2] (kTP2 = kTP1 + 64) = h [dO ; dv_new]^T, then P3 = dh' v_new^T
+      for (int s = 0; s < 16; ++s) mma_tf32_ts(tb + kTP1, tb + kTH + s * 8, desc_kmajor(sC, 16384, s), id128, s > 0);
       for (int s = 0; s < 16; ++s) mma_tf32_ts(tb + kTP3, tb + kTDH + s * 8, desc_kmajor(sVN, 8192, s), id64, s > 0);
       mma_commit(&bar_mma);
     }
@@ -209,7 +211,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // columns), read from the TMA copy of dv_new already in shared memory.
 #pragma unroll
     for (int e = 0; e < 32; ++e)
-      r[e] = to_tf32(*reinterpret_cast<const float*>(sm + kOffDVN + sw128_offset(t0 + e, f, kC, 4)));
+      r[e] = to_tf32(*reinterpret_cast<const float*>(sm + kOffC + sw128_offset(kC + t0 + e, f, 2 * kC, 4)));
     tmem_st32(tl + kTH + t0, r);
     tmem_wait_st();
   }

@@ -106,44 +106,27 @@ __global__ void __launch_bounds__(kThreads, 1)
   TTRACE(0);
   if (warp == 0) tmem_alloc(&tslot, 256);
   if (tid == 0) {
+    // The barriers are this thread's alone until the block barrier below, so the loads start
+    // right after their initialisation. First group (q, k, v, dO, v_new) feeds the first
+    // products; dW, dU arrive on their own barrier and are first read by the dA product.
     abort_flag = 0;
     mbar_init(&bar_tma, 1);
     mbar_init(&bar_tma2, 1);
     mbar_init(&bar_mma, 1);
     fence_mbar_init();
-  }
-  if (tid < kC) {
-    const bool ok = tid < len;
-    s_G[tid] = p.Gc[tile * kC + tid];
-    s_G2[tid] = s_G[tid] * kLog2e;  // exp(G_i - G_j) = exp2(G2_i - G2_j) in the pair loop
-    s_rq[tid] = ok ? p.rq[tile * kC + tid] : 0.f;
-    s_rk[tid] = ok ? p.rk[tile * kC + tid] : 0.f;
-    s_b[tid] = ok ? p.beff[tile * kC + tid] : 0.f;
-    s_dG[tid] = 0.f;
-    s_db[tid] = 0.f;
-  }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tb = tslot;
-  const uint32_t tl = tb + tmem_lane_base(warp);
-  const float Glast = s_G[len - 1];
-  if (tid == 0) {
-    // first group (q, k, v, dO, v_new) feeds the first products; dW, dU arrive on their own
-    // barrier and are first read by the dA product
     mbar_expect_tx(&bar_tma, 4u * 16384u + 32768u);
     mbar_expect_tx(&bar_tma2, 2u * 32768u);
+    for (int pp = 0; pp < 4; ++pp) {  // chunk-tile rows: no wait for the chunk table
+      tma_load_2d(sm + kR2 + pp * 8192, &mVN, pp * 32, int(tile) * kC, &bar_tma);
+      tma_load_2d(sm + kR3 + pp * 8192, &mDW, pp * 32, int(tile) * kC, &bar_tma2);
+      tma_load_2d(sm + kR4 + pp * 8192, &mDVN, pp * 32, int(tile) * kC, &bar_tma2);
+    }
     for (int pp = 0; pp < 2; ++pp) {
       const int x = h * kD + 64 * pp, xqk = (h / p.qk_group) * kD + 64 * pp;
       tma_load_2d(sQ + pp * 8192, &mq, xqk, ch.x, &bar_tma);
       tma_load_2d(sK + pp * 8192, &mk, xqk, ch.x, &bar_tma);
       tma_load_2d(sV + pp * 8192, &mv, x, ch.x, &bar_tma);
       tma_load_2d(sm + kOffDO + pp * 8192, &mdO, x, ch.x, &bar_tma);
-    }
-    for (int pp = 0; pp < 4; ++pp) {
-      tma_load_2d(sm + kR2 + pp * 8192, &mVN, pp * 32, int(tile) * kC, &bar_tma);
-      tma_load_2d(sm + kR3 + pp * 8192, &mDW, pp * 32, int(tile) * kC, &bar_tma2);
-      tma_load_2d(sm + kR4 + pp * 8192, &mDVN, pp * 32, int(tile) * kC, &bar_tma2);
     }
     // inputs of the later phases: start their trip from HBM now
     const size_t rows = tile * kTileW;
@@ -153,6 +136,25 @@ __global__ void __launch_bounds__(kThreads, 1)
     prefetch_l2(p.dK1 + rows, 4u * kTileW);
     prefetch_l2(p.dV1 + rows, 4u * kTileW);
   }
+  if (tid < kC) {
+    // requested before the chunk length is known, masked after
+    const float G = p.Gc[tile * kC + tid], rq = p.rq[tile * kC + tid], rk = p.rk[tile * kC + tid],
+                b = p.beff[tile * kC + tid];
+    const bool ok = tid < len;
+    s_G[tid] = G;
+    s_G2[tid] = G * kLog2e;  // exp(G_i - G_j) = exp2(G2_i - G2_j) in the pair loop
+    s_rq[tid] = ok ? rq : 0.f;
+    s_rk[tid] = ok ? rk : 0.f;
+    s_b[tid] = ok ? b : 0.f;
+    s_dG[tid] = 0.f;
+    s_db[tid] = 0.f;
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tb = tslot;
+  const uint32_t tl = tb + tmem_lane_base(warp);
+  const float Glast = s_G[len - 1];
   TTRACE(1);
   const bool tma_ok = mbar_wait(&bar_tma, 0, &abort_flag, p.status, kDevTimeoutTma);
   TTRACE(2);

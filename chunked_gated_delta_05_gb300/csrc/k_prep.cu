@@ -152,16 +152,27 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int rt = tid & (kRows - 1), hf = tid >> 7;
   const int blk = rt >> 6, il = rt & 63;
 
-  if (tid < 2) {
-    const int c = 2 * pair + tid;
-    s_chunk[tid] = c < p.NC ? p.chunks[c] : make_int4(0, 0, 0, 0);
-  }
   if (warp == 0) tmem_alloc(&tslot, 256);
   if (tid == 0) {
+    // the barriers are this thread's alone until the block barrier below: start the loads now
+    int4 cb[2];
+    for (int b = 0; b < 2; ++b) cb[b] = 2 * pair + b < p.NC ? p.chunks[2 * pair + b] : make_int4(0, 0, 0, 0);
     abort_flag = 0;
     mbar_init(&bar_tma, 1);
     mbar_init(&bar_mma, 1);
     fence_mbar_init();
+    const int nexist = (cb[0].y > 0) + (cb[1].y > 0);
+    mbar_expect_tx(&bar_tma, uint32_t(nexist) * 6u * 8192u);
+    for (int b = 0; b < 2; ++b) {
+      s_chunk[b] = cb[b];
+      if (cb[b].y <= 0) continue;
+      for (int pp = 0; pp < 2; ++pp) {
+        const int x = h * kD + 64 * pp, xqk = (h / p.qk_group) * kD + 64 * pp, y = cb[b].x;
+        tma_load_2d(sQ + pp * kPanel + b * 8192, &mq, xqk, y, &bar_tma);
+        tma_load_2d(sK + pp * kPanel + b * 8192, &mk, xqk, y, &bar_tma);
+        tma_load_2d(sV + pp * kPanel + b * 8192, &mv, x, y, &bar_tma);
+      }
+    }
   }
   tc_fence_before();
   __syncthreads();
@@ -174,19 +185,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   const bool valid = il < len;
   const int row = ch.x + il;
 
-  if (tid == 0) {
-    const int nexist = (s_chunk[0].y > 0) + (s_chunk[1].y > 0);
-    mbar_expect_tx(&bar_tma, uint32_t(nexist) * 6u * 8192u);
-    for (int b = 0; b < 2; ++b) {
-      if (s_chunk[b].y <= 0) continue;
-      for (int pp = 0; pp < 2; ++pp) {
-        const int x = h * kD + 64 * pp, xqk = (h / p.qk_group) * kD + 64 * pp, y = s_chunk[b].x;
-        tma_load_2d(sQ + pp * kPanel + b * 8192, &mq, xqk, y, &bar_tma);
-        tma_load_2d(sK + pp * kPanel + b * 8192, &mk, xqk, y, &bar_tma);
-        tma_load_2d(sV + pp * kPanel + b * 8192, &mv, x, y, &bar_tma);
-      }
-    }
-  }
   // A missing second chunk leaves its tile rows unloaded: zero them so that the products
   // with zero coefficients stay exactly zero.
   if (len == 0) {
