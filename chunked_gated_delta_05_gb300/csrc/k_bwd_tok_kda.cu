@@ -17,10 +17,10 @@
 //   dbeta_i = sum_c k^_ic X1_ic + sum_c exp(G_ic) dK1_ic k^_ic + sum_c dV1_ic v_ic
 //   dg = reverse cumulative sum of dG over the chunk's tokens, per channel.
 // GB300 mapping: dAqk, dA = [dW | dU][K1 | V1]^T, A^T dA and (A^T dA) A^T are 64-row
-// tcgen05 MMAs (kind::tf32) as in the scalar-gate kernel. The decayed pair sums need one
-// exp(G_ic - G_jc) per (pair, channel); they run on the CUDA cores with one thread per channel
-// (two per channel, interleaving rows), each exponent evaluated once and shared by the four
-// sums, which keeps every decay exact (no factorisation, no range limit on the gates).
+// tcgen05 MMAs (kind::tf32) as in the scalar-gate kernel. The decayed pair sums run on the CUDA
+// cores in fp32, one thread per (channel, pair of 16-row blocks): pairs inside a block take
+// exp(G_ic - G_jc) directly, pairs across blocks factor it through the block's first or last
+// row into two factors of at most 1 (G falls along the chunk), so no exponent is per pair.
 #include "common.cuh"
 #include "umma.cuh"
 
@@ -44,6 +44,115 @@ __device__ __forceinline__ float bf16_at(const uint8_t* tile, int row, int col) 
 }
 __device__ __forceinline__ void put32(uint8_t* tile, int rows, int row, int col, float x) {
   *reinterpret_cast<float*>(tile + sw128_offset(row, col, rows, 4)) = x;
+}
+
+
+// Decayed pair sums of the 16-row block I of the chunk for key channel c: rows i of the block
+// get X1 and Y1, columns j of the block get Z (sums defined in the kernel header; G in log2
+// units). Pairs across blocks factor through the block's reference rows, and since G falls
+// along the chunk both factors are at most 1: for j < 16 I <= i,
+//   exp(G_i - G_j) = exp(G_i - G_r) exp(G_r - G_j),  r = 16 I,
+// and for i > 16 I + 15 >= j,
+//   exp(G_i - G_j) = exp(G_i - G_s) exp(G_s - G_j),  s = 16 I + 15.
+// The 136 pairs inside the block take their exponent directly, shared by the three sums.
+// Everything stays in fp32. The block's rows are then written to the dk^ / dq^ / dG
+// accumulators, and k^ . X1 goes to dbeta.
+template <int I>
+__device__ __forceinline__ void kda_pair_block(const float* __restrict__ sG2, const uint8_t* sK, const uint8_t* sQ,
+                                               const float* s_rk, const float* s_rq, const float* s_b,
+                                               const float* __restrict__ sD, const float* __restrict__ sN,
+                                               float* sKacc, float* sQacc, float* sGacc, float* s_db, int c,
+                                               int lane) {
+  constexpr int r0 = 16 * I;
+  float x1[16], y1[16], kb[16], gb[16];
+#pragma unroll
+  for (int r = 0; r < 16; ++r) {
+    const int t = r0 + r;
+    gb[r] = sG2[t * kP + c];
+    kb[r] = s_rk[t] * bf16_at(sK, t, c);
+    x1[r] = 0.f;
+    y1[r] = 0.f;
+  }
+  if constexpr (I > 0) {  // rows of the block against the earlier columns, four at a time
+    const float R = gb[0];
+#pragma unroll 1
+    for (int m = 0; m < r0 / 4; ++m) {
+      float P[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int j = 4 * m + e;
+        P[e] = s_rk[j] * bf16_at(sK, j, c) * exp2f(R - sG2[j * kP + c]);
+      }
+#pragma unroll
+      for (int r = 0; r < 16; ++r) {
+        const float4 d = reinterpret_cast<const float4*>(sD + (r0 + r) * kC)[m];
+        const float4 n = reinterpret_cast<const float4*>(sN + (r0 + r) * kC)[m];
+        x1[r] = fmaf(d.x, P[0], fmaf(d.y, P[1], fmaf(d.z, P[2], fmaf(d.w, P[3], x1[r]))));
+        y1[r] = fmaf(n.x, P[0], fmaf(n.y, P[1], fmaf(n.z, P[2], fmaf(n.w, P[3], y1[r]))));
+      }
+    }
+#pragma unroll
+    for (int r = 0; r < 16; ++r) {
+      const float e = exp2f(gb[r] - R);
+      x1[r] *= e;
+      y1[r] *= e;
+    }
+  }
+  {  // later rows against the columns of the block; Z collects in the dG accumulator's rows
+    float z[16];
+#pragma unroll
+    for (int s = 0; s < 16; ++s) z[s] = 0.f;
+    if constexpr (I < 3) {
+      const float S = gb[15];
+#pragma unroll 4
+      for (int i = r0 + 16; i < kC; ++i) {
+        const float u = exp2f(sG2[i * kP + c] - S);
+        const float a = s_b[i] * s_rk[i] * bf16_at(sK, i, c) * u;
+        const float b = s_rq[i] * bf16_at(sQ, i, c) * u;
+        const float4* d4 = reinterpret_cast<const float4*>(sD + i * kC + r0);
+        const float4* n4 = reinterpret_cast<const float4*>(sN + i * kC + r0);
+#pragma unroll
+        for (int m = 0; m < 4; ++m) {
+          const float4 d = d4[m], n = n4[m];
+          z[4 * m] = fmaf(d.x, a, fmaf(n.x, b, z[4 * m]));
+          z[4 * m + 1] = fmaf(d.y, a, fmaf(n.y, b, z[4 * m + 1]));
+          z[4 * m + 2] = fmaf(d.z, a, fmaf(n.z, b, z[4 * m + 2]));
+          z[4 * m + 3] = fmaf(d.w, a, fmaf(n.w, b, z[4 * m + 3]));
+        }
+      }
+#pragma unroll
+      for (int s = 0; s < 16; ++s) z[s] *= exp2f(S - gb[s]);
+    }
+#pragma unroll
+    for (int s = 0; s < 16; ++s) sGacc[(r0 + s) * kD + c] = z[s];
+  }
+#pragma unroll
+  for (int r = 0; r < 16; ++r) {  // pairs inside the block, i = r0 + r >= j = r0 + s
+    const int i = r0 + r;
+    const float bi = s_b[i], qi = s_rq[i] * bf16_at(sQ, i, c);
+    const float ci = bi * kb[r];
+#pragma unroll
+    for (int s = 0; s <= r; ++s) {
+      const float e = exp2f(gb[r] - gb[s]);
+      const float dij = sD[i * kC + r0 + s], nij = sN[i * kC + r0 + s];
+      x1[r] = fmaf(dij * kb[s], e, x1[r]);
+      y1[r] = fmaf(nij * kb[s], e, y1[r]);
+      float* zs = sGacc + (r0 + s) * kD + c;
+      *zs = fmaf(fmaf(ci, dij, nij * qi), e, *zs);
+    }
+  }
+#pragma unroll
+  for (int r = 0; r < 16; ++r) {
+    const int t = r0 + r;
+    const float bt = s_b[t], qt = s_rq[t] * bf16_at(sQ, t, c), zt = sGacc[t * kD + c];
+    sKacc[t * kD + c] = bt * x1[r] + zt;
+    sQacc[t * kD + c] = y1[r];
+    sGacc[t * kD + c] = bt * kb[r] * x1[r] + qt * y1[r] - kb[r] * zt;
+    float part = kb[r] * x1[r];
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) part += __shfl_xor_sync(0xffffffffu, part, off);
+    if (lane == 0) atomicAdd(&s_db[t], part);
+  }
 }
 
 }  // namespace
@@ -261,69 +370,62 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   tc_fence_before();
   __syncthreads();
-  // ---- decayed pair sums on CUDA cores: thread (channel cc, rows of parity `half`).
+  // ---- decayed pair sums on CUDA cores: thread (channel cc, row blocks 2 half and 2 half + 1,
+  // which balances the two halves' work). Rows past the chunk come out zero.
   float* sKacc = reinterpret_cast<float*>(sm + kR2);           // dk^ accumulator [64][128]
   float* sQacc = reinterpret_cast<float*>(sm + kR3);           // dq^ accumulator [64][128]
   float* sGacc = reinterpret_cast<float*>(sm + kR4);           // dG accumulator [64][128]
-  for (int i = half; i < len; i += 2) {
-    const float Gi = sG2[i * kP + cc];
-    float x1 = 0.f, y1 = 0.f;
-    for (int j = 0; j <= i; ++j) {
-      const float gam = exp2f(Gi - sG2[j * kP + cc]);
-      const float kj = s_rk[j] * bf16_at(sK, j, cc) * gam;
-      x1 = fmaf(sD[i * kC + j], kj, x1);
-      y1 = fmaf(sN[i * kC + j], kj, y1);
-    }
-    const float khi = s_rk[i] * bf16_at(sK, i, cc);
-    const float qhi = s_rq[i] * bf16_at(sQ, i, cc);
-    float z = 0.f;
-    for (int r = i; r < len; ++r) {   // Z_ic: rows r >= i act on column i
-      const float gam = exp2f(sG2[r * kP + cc] - Gi);
-      const float kr = s_rk[r] * bf16_at(sK, r, cc);
-      const float qr = s_rq[r] * bf16_at(sQ, r, cc);
-      z = fmaf(s_b[r] * sD[r * kC + i] * kr + sN[r * kC + i] * qr, gam, z);
-    }
-    sKacc[i * kD + cc] = s_b[i] * x1 + z;
-    sQacc[i * kD + cc] = y1;
-    sGacc[i * kD + cc] = s_b[i] * khi * x1 + qhi * y1 - khi * z;
-    // dbeta_i gets sum over channels of k^_ic X1_ic: warp-reduce, one atomic per warp
-    float part = khi * x1;
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) part += __shfl_xor_sync(0xffffffffu, part, off);
-    if (lane == 0) atomicAdd(&s_db[i], part);
+  if (half == 0) {
+    kda_pair_block<0>(sG2, sK, sQ, s_rk, s_rq, s_b, sD, sN, sKacc, sQacc, sGacc, s_db, cc, lane);
+    kda_pair_block<1>(sG2, sK, sQ, s_rk, s_rq, s_b, sD, sN, sKacc, sQacc, sGacc, s_db, cc, lane);
+  } else {
+    kda_pair_block<2>(sG2, sK, sQ, s_rk, s_rq, s_b, sD, sN, sKacc, sQacc, sGacc, s_db, cc, lane);
+    kda_pair_block<3>(sG2, sK, sQ, s_rk, s_rq, s_b, sD, sN, sKacc, sQacc, sGacc, s_db, cc, lane);
   }
   __syncthreads();
   // ---- per-token assembly (thread: channel cc, rows of parity `half`)
   float glast_part = 0.f;
   const float glc = sG2[(len - 1) * kP + cc];
   const size_t rowbase = tile * kTileW;
-  for (int t = half; t < len; t += 2) {
-    const float G = sG2[t * kP + cc];
-    const float eG = exp2f(G), eL = exp2f(glc - G);
-    const float qh = s_rq[t] * bf16_at(sQ, t, cc), kh = s_rk[t] * bf16_at(sK, t, cc);
-    const float dqt = p.dQt[rowbase + size_t(t) * kD + cc];
-    const float dk1 = p.dK1[rowbase + size_t(t) * kD + cc];
-    const float dkt = p.dKt[rowbase + size_t(t) * kD + cc];
-    const float dv1 = p.dV1[rowbase + size_t(t) * kD + cc];
-    const float dqh = sQacc[t * kD + cc] + scale * eG * dqt;
-    const float dkh = sKacc[t * kD + cc] + s_b[t] * eG * dk1 + eL * dkt;
-    sQacc[t * kD + cc] = dqh;
-    sKacc[t * kD + cc] = dkh;
-    sGacc[t * kD + cc] += s_b[t] * eG * dk1 * kh + scale * eG * dqt * qh - eL * dkt * kh;
-    glast_part = fmaf(eL * dkt, kh, glast_part);
-    p.dv[(size_t(ch.x + t) * H + h) * kD + cc] = __float2bfloat16_rn(s_b[t] * dv1);
-    float pb = eG * dk1 * kh + dv1 * bf16_at(sV, t, cc);
-    float pq = dqh * qh, pk = dkh * kh;
+  // rows t0 + 2 e, e < 8: the four gradient tiles of eight rows are requested together
+  for (int t0 = half; t0 < len; t0 += 16) {
+    float dqt8[8], dk18[8], dkt8[8], dv18[8];
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) {
-      pb += __shfl_xor_sync(0xffffffffu, pb, off);
-      pq += __shfl_xor_sync(0xffffffffu, pq, off);
-      pk += __shfl_xor_sync(0xffffffffu, pk, off);
+    for (int e = 0; e < 8; ++e) {  // t0 + 2 e < 64: inside the chunk tile
+      const size_t o = rowbase + size_t(t0 + 2 * e) * kD + cc;
+      dqt8[e] = p.dQt[o];
+      dk18[e] = p.dK1[o];
+      dkt8[e] = p.dKt[o];
+      dv18[e] = p.dV1[o];
     }
-    if (lane == 0) {
-      atomicAdd(&s_db[t], pb);
-      atomicAdd(&s_dotq[t], pq);
-      atomicAdd(&s_dotk[t], pk);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      const int t = t0 + 2 * e;
+      if (t >= len) break;  // warp-uniform
+      const float dqt = dqt8[e], dk1 = dk18[e], dkt = dkt8[e], dv1 = dv18[e];
+      const float G = sG2[t * kP + cc];
+      const float eG = exp2f(G), eL = exp2f(glc - G);
+      const float qh = s_rq[t] * bf16_at(sQ, t, cc), kh = s_rk[t] * bf16_at(sK, t, cc);
+      const float dqh = sQacc[t * kD + cc] + scale * eG * dqt;
+      const float dkh = sKacc[t * kD + cc] + s_b[t] * eG * dk1 + eL * dkt;
+      sQacc[t * kD + cc] = dqh;
+      sKacc[t * kD + cc] = dkh;
+      sGacc[t * kD + cc] += s_b[t] * eG * dk1 * kh + scale * eG * dqt * qh - eL * dkt * kh;
+      glast_part = fmaf(eL * dkt, kh, glast_part);
+      p.dv[(size_t(ch.x + t) * H + h) * kD + cc] = __float2bfloat16_rn(s_b[t] * dv1);
+      float pb = eG * dk1 * kh + dv1 * bf16_at(sV, t, cc);
+      float pq = dqh * qh, pk = dkh * kh;
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) {
+        pb += __shfl_xor_sync(0xffffffffu, pb, off);
+        pq += __shfl_xor_sync(0xffffffffu, pq, off);
+        pk += __shfl_xor_sync(0xffffffffu, pk, off);
+      }
+      if (lane == 0) {
+        atomicAdd(&s_db[t], pb);
+        atomicAdd(&s_dotq[t], pq);
+        atomicAdd(&s_dotk[t], pk);
+      }
     }
   }
   s_glast[half][cc] = glast_part;

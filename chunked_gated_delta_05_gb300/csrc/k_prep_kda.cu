@@ -20,6 +20,7 @@
 // carries the per-channel decay (tf32, thread-written); U uses the raw v tile (bf16); the
 // unit diagonal of A is applied in fp32 from the exact inputs.
 #include "common.cuh"
+#include "tri_inverse.cuh"
 #include "umma.cuh"
 
 namespace gdn {
@@ -39,6 +40,12 @@ constexpr uint32_t kOffX = kOffAS + 16384;                 // inverse columns fp
 constexpr uint32_t kOffA1 = kOffAS + 32768;                // (A - I) diag(beta r_k), tf32 [64][64]
 constexpr uint32_t kOffA2 = kOffAS + 49152;                // (A - I) diag(beta), bf16 [64][64]
 constexpr uint32_t kOffK1T = kOffB;                        // (k (.) exp(G))^T, tf32 [128][64]
+constexpr int kAP = kC + 1;                                // padded row stride of the Aqk staging
+constexpr uint32_t kOffAqkS = kOffB + 32768;               // Aqk staging fp32 [64][65] (beside K1T)
+constexpr int kWP = kD + 1, kTP = kC + 1;                  // padded strides of the W/U and KtT/QtT staging
+constexpr uint32_t kOffWS = kOffAS, kOffUS = kOffB;        // after the WY products: [64][129] / [128][65]
+static_assert(kOffAqkS + 4 * kC * kAP <= kOffB + 65536, "Aqk staging fits the B region");
+static_assert(4 * kC * kWP <= 65536 && 4 * kD * kTP <= 65536, "W/U and KtT/QtT staging fit their regions");
 
 __device__ __forceinline__ uint8_t* align1k(uint8_t* p) {
   return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
@@ -49,50 +56,13 @@ __device__ __forceinline__ float bf16_at(const uint8_t* tile, int row, int col) 
 __device__ __forceinline__ void put32(uint8_t* tile, int rows, int row, int col, float x) {
   *reinterpret_cast<float*>(tile + sw128_offset(row, col, rows, 4)) = x;
 }
-
-// Column c of (I + L)^-1 from L^T in shared memory (see the scalar-gate prepare kernel).
-__device__ __forceinline__ void inverse_column(const float* __restrict__ LT, float* sX, int c) {
-  for (int b = 0; b < 4; ++b) {
-    const int r0 = 16 * b;
-    float x[16];
-    if (r0 + 15 < (c & ~31)) {  // above the diagonal for the whole warp
+__device__ __forceinline__ void bf16x8_to_f32(const uint4& u, float* f) {
+  const __nv_bfloat162* b = reinterpret_cast<const __nv_bfloat162*>(&u);
 #pragma unroll
-      for (int e = 0; e < 16; ++e) x[e] = 0.f;
-    } else {
-      float y[16];
-#pragma unroll
-      for (int e = 0; e < 16; ++e) y[e] = 0.f;
-      // warp-uniform rows (the warp's columns share c & ~31; X[j][c] = 0 for j < c is already
-      // in sX), so every L^T row read is a broadcast
-#pragma unroll 4
-      for (int j = c & ~31; j < r0; ++j) {
-        const float xj = sX[j * kC + c];
-        const float4* l4 = reinterpret_cast<const float4*>(LT + j * kC + r0);
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const float4 l = l4[q];
-          y[4 * q] = fmaf(-l.x, xj, y[4 * q]);
-          y[4 * q + 1] = fmaf(-l.y, xj, y[4 * q + 1]);
-          y[4 * q + 2] = fmaf(-l.z, xj, y[4 * q + 2]);
-          y[4 * q + 3] = fmaf(-l.w, xj, y[4 * q + 3]);
-        }
-      }
-#pragma unroll
-      for (int r = 0; r < 16; ++r) {
-        // two interleaved partial sums halve the dependent FMA chain of the 16x16 solve
-        float acc0 = y[r], acc1 = 0.f;
-#pragma unroll
-        for (int j = 0; j < r; ++j) {
-          if (j & 1) acc1 = fmaf(-LT[(r0 + j) * kC + r0 + r], x[j], acc1);
-          else acc0 = fmaf(-LT[(r0 + j) * kC + r0 + r], x[j], acc0);
-        }
-        const float acc = acc0 + acc1;
-        const int R = r0 + r;
-        x[r] = (R < c) ? 0.f : ((R == c) ? 1.f : acc);
-      }
-    }
-#pragma unroll
-    for (int e = 0; e < 16; ++e) sX[(r0 + e) * kC + c] = x[e];
+  for (int e = 0; e < 4; ++e) {
+    const float2 t = __bfloat1622float2(b[e]);
+    f[2 * e] = t.x;
+    f[2 * e + 1] = t.y;
   }
 }
 
@@ -120,17 +90,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == 0) tmem_alloc(&tslot, 256);
   if (tid == 0) {
+    // the barriers are this thread's alone until the block barrier below: start the loads now
     abort_flag = 0;
     mbar_init(&bar_tma, 1);
     mbar_init(&bar_mma, 1);
     fence_mbar_init();
-  }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tb = tslot;
-  const uint32_t tl = tb + tmem_lane_base(warp);
-  if (tid == 0) {
     mbar_expect_tx(&bar_tma, 3u * 16384u);
     for (int pp = 0; pp < 2; ++pp) {
       const int x = h * kD + 64 * pp, xqk = (h / p.qk_group) * kD + 64 * pp;
@@ -163,6 +127,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     s_b[tid] = b;
   }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tb = tslot;
+  const uint32_t tl = tb + tmem_lane_base(warp);
   mbar_wait(&bar_tma, 0, &abort_flag, p.status, kDevTimeoutTma);
   // rows past the chunk belong to the next document (or are zero): clear them
   if (tid >= len && tid < kC) {
@@ -174,14 +143,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
   __syncthreads();
-  // L2-norm factors: threads 0..63 for q rows, 64..127 for k rows.
+  // L2-norm factors: threads 0..63 for q rows, 64..127 for k rows (eight columns per load).
   {
     const int t = tid & 63;
     const uint8_t* src = tid < kC ? sQ : sK;
     float ss = 0.f;
-    for (int d = 0; d < kD; ++d) {
-      const float x = bf16_at(src, t, d);
-      ss = fmaf(x, x, ss);
+#pragma unroll
+    for (int c16 = 0; c16 < 16; ++c16) {
+      float f[8];
+      bf16x8_to_f32(*reinterpret_cast<const uint4*>(src + sw128_offset(t, c16 * 8, kC, 2)), f);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) ss = fmaf(f[e], f[e], ss);
     }
     const float r = p.l2norm ? 1.f / sqrtf(ss + 1e-6f) : 1.f;
     if (tid < kC) s_rq[t] = r; else s_rk[t] = r;
@@ -196,11 +168,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool isq = tid >= kC;
     const int rref = i & ~15;
     const float rs = isq ? s_rq[i] : s_rk[i];
-    const uint8_t* src = isq ? sQ : sK;
     const bool vi = i < len;
-    for (int c = 0; c < kD; ++c) {
-      const float val = vi ? rs * bf16_at(src, i, c) * expf(sG[i * kGP + c] - sG[rref * kGP + c]) : 0.f;
-      put32(sAS, 128, tid, c, to_tf32(val));
+    const uint8_t* src = isq ? sQ : sK;
+#pragma unroll 2
+    for (int c16 = 0; c16 < 16; ++c16) {
+      float f[8];
+      bf16x8_to_f32(*reinterpret_cast<const uint4*>(src + sw128_offset(i, c16 * 8, kC, 2)), f);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const int c = 8 * c16 + e;
+        f[e] = vi ? to_tf32(rs * f[e] * expf(sG[i * kGP + c] - sG[rref * kGP + c])) : 0.f;
+      }
+      *reinterpret_cast<float4*>(sAS + sw128_offset(tid, 8 * c16, 128, 4)) = make_float4(f[0], f[1], f[2], f[3]);
+      *reinterpret_cast<float4*>(sAS + sw128_offset(tid, 8 * c16 + 4, 128, 4)) = make_float4(f[4], f[5], f[6], f[7]);
     }
   }
   // B_I = k^_j exp(G_{r_I} - G_j) for j <= 16 I + 15 (zero elsewhere), two blocks at a time.
@@ -208,11 +188,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int j = tid & 63, I = I0 + (tid >> 6);
     const int rref = 16 * I;
     uint8_t* dst = sm + kOffB + (tid >> 6) * 32768;
-    const bool vj = j < len && j <= 16 * I + 15;
+    const bool vj = j < len && j <= 16 * I + 15;  // a select: the exponent is unbounded elsewhere
     const float rs = s_rk[j];
-    for (int c = 0; c < kD; ++c) {
-      const float val = vj ? rs * bf16_at(sK, j, c) * expf(sG[rref * kGP + c] - sG[j * kGP + c]) : 0.f;
-      put32(dst, kC, j, c, to_tf32(val));
+#pragma unroll 2
+    for (int c16 = 0; c16 < 16; ++c16) {
+      float f[8];
+      bf16x8_to_f32(*reinterpret_cast<const uint4*>(sK + sw128_offset(j, c16 * 8, kC, 2)), f);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const int c = 8 * c16 + e;
+        f[e] = vj ? to_tf32(rs * f[e] * expf(sG[rref * kGP + c] - sG[j * kGP + c])) : 0.f;
+      }
+      *reinterpret_cast<float4*>(dst + sw128_offset(j, 8 * c16, kC, 4)) = make_float4(f[0], f[1], f[2], f[3]);
+      *reinterpret_cast<float4*>(dst + sw128_offset(j, 8 * c16 + 4, kC, 4)) = make_float4(f[4], f[5], f[6], f[7]);
     }
   };
   const uint32_t id_g = idesc_tf32(128, 64);
@@ -243,7 +231,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
 
   // Row blocks of L (lanes 0..63) and Aqk (lanes 64..127) from D_I, I = block of the row.
+  // Aqk rows are staged (padded [64][65]) and leave as whole lines, row-major and transposed.
   float* sLT = reinterpret_cast<float*>(sm + kOffLT);
+  float* sAqk = reinterpret_cast<float*>(sm + kOffAqkS);
   if (ok) {
     const int i = tid & 63;
     const bool isq = tid >= kC;
@@ -261,40 +251,39 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int j = 0; j < kC; ++j) sLT[j * kC + i] = (j < i && vi) ? s_b[i] * (second ? r1[j] : r0[j]) : 0.f;
     } else {
-      float a[kC];
 #pragma unroll
-      for (int j = 0; j < kC; ++j) a[j] = (j <= i && vi) ? to_tf32(p.scale * (second ? r1[j] : r0[j])) : 0.f;
-      float4* dst = reinterpret_cast<float4*>(p.Aqk + tile * kTileAqk + size_t(i) * kC);
-#pragma unroll
-      for (int e = 0; e < kC / 4; ++e) dst[e] = make_float4(a[4 * e], a[4 * e + 1], a[4 * e + 2], a[4 * e + 3]);
-      if (p.AqkT) {
-        float* at = p.AqkT + tile * kTileAqk + i;
-#pragma unroll
-        for (int j = 0; j < kC; ++j) at[size_t(j) * kC] = a[j];
-      }
+      for (int j = 0; j < kC; ++j) sAqk[i * kAP + j] = (j <= i && vi) ? to_tf32(p.scale * (second ? r1[j] : r0[j])) : 0.f;
     }
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  if (ok) {
+    float* aqk = p.Aqk + tile * kTileAqk;
+#pragma unroll 4
+    for (int m = 0; m < kC * kC / kThreads; ++m) {
+      const int idx = m * kThreads + tid, r = idx >> 6, col = idx & 63;
+      aqk[idx] = sAqk[r * kAP + col];
+      if (p.AqkT) p.AqkT[tile * kTileAqk + idx] = sAqk[col * kAP + r];  // (r, col) of Aqk^T
+    }
+  }
   float* sX = reinterpret_cast<float*>(sm + kOffX);
-  if (tid < kC) inverse_column(sLT, sX, tid);
+  unit_lower_inverse_column(sLT, sX, 16 * warp + (lane & 15), lane >> 4);
   __syncthreads();
   // WY operands: A1 = (A - I) diag(beta r_k) (tf32), A2 = (A - I) diag(beta) (bf16), both
   // K-major [i][j]; K1T = (k (.) exp(G))^T (tf32, K-major [c][j]).
   {
-    const int j = tid & 63;
-    if (tid < kC) {
-      const float s1 = s_b[j] * s_rk[j], s2 = s_b[j];
-      for (int i = 0; i < kC; ++i) {
-        const float x = i == j ? 0.f : sX[i * kC + j];
-        put32(sm + kOffA1, kC, i, j, to_tf32(x * s1));
-        *reinterpret_cast<__nv_bfloat16*>(sm + kOffA2 + sw128_offset(i, j, kC, 2)) = __float2bfloat16_rn(x * s2);
-      }
-      if (p.A) {
-        float* a = p.A + tile * kTileAqk + j;
-        for (int i = 0; i < kC; ++i) a[size_t(i) * kC] = sX[i * kC + j];
-      }
+    const int j = tid & 63, i0 = 32 * (tid >> 6);
+    const float s1 = s_b[j] * s_rk[j], s2 = s_b[j];
+#pragma unroll 4
+    for (int i = i0; i < i0 + 32; ++i) {
+      const float x = i == j ? 0.f : sX[i * kC + j];
+      put32(sm + kOffA1, kC, i, j, to_tf32(x * s1));
+      *reinterpret_cast<__nv_bfloat16*>(sm + kOffA2 + sw128_offset(i, j, kC, 2)) = __float2bfloat16_rn(x * s2);
+    }
+    if (p.A) {
+      float* a = p.A + tile * kTileAqk + j;
+      for (int i = i0; i < i0 + 32; ++i) a[size_t(i) * kC] = sX[i * kC + j];
     }
     const int c = tid;
     for (int jj = 0; jj < kC; ++jj) {
@@ -317,36 +306,60 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncwarp();
   ok = ok && mbar_wait(&bar_mma, mma_phase, &abort_flag, p.status, kDevTimeoutMma);
   tc_fence_after();
-  // W and U rows (64-row MMA results: lane 32*(r/16) + r%16 holds row r).
+  __syncthreads();  // the operand regions are free from here: W and U are staged over them
+  // W and U rows (64-row MMA results: lane 32*(r/16) + r%16 holds row r), staged padded
+  // [64][129] and written back as whole lines.
+  float* sWs = reinterpret_cast<float*>(sm + kOffWS);
+  float* sUs = reinterpret_cast<float*>(sm + kOffUS);
   if (ok) {
     const bool owner = lane < 16;
     const int r = 16 * warp + (lane & 15);
     const bool vr = owner && r < len;
     const float dw = s_b[r] * s_rk[r], du = s_b[r];
     for (int which = 0; which < 2; ++which) {
+      float* st = which == 0 ? sWs : sUs;
       for (int half = 0; half < 2; ++half) {
         float x[64];
         tmem_ld64(tl + which * 128 + half * 64, x);
         tmem_wait_ld_regs(x);
-        if (vr) {
-          float* dst = (which == 0 ? p.W : p.U) + tile * kTileW + size_t(r) * kD + half * 64;
+        if (owner) {
 #pragma unroll
           for (int e = 0; e < 64; ++e) {
             const int c = half * 64 + e;
-            float val;
-            if (which == 0) {
-              val = to_tf32(fmaf(dw * expf(sG[r * kGP + c]), bf16_at(sK, r, c), x[e]));
-              if (p.WT) p.WT[tile * kTileKtT + size_t(c) * kC + r] = val;
-            } else {
-              val = fmaf(du, bf16_at(sV, r, c), x[e]);
+            float val = 0.f;
+            if (vr) {
+              val = which == 0 ? to_tf32(fmaf(dw * expf(sG[r * kGP + c]), bf16_at(sK, r, c), x[e]))
+                               : fmaf(du, bf16_at(sV, r, c), x[e]);
             }
-            dst[e] = val;
+            st[r * kWP + c] = val;
           }
         }
       }
     }
   }
-  // Per-element outputs: thread c writes channel c of every row.
+  __syncthreads();
+  if (ok && len > 0) {
+    float* w = p.W + tile * kTileW;
+    float* u = p.U + tile * kTileW;
+#pragma unroll 4
+    for (int r = 0; r < kC; ++r) {
+      w[size_t(r) * kD + tid] = sWs[r * kWP + tid];
+      u[size_t(r) * kD + tid] = sUs[r * kWP + tid];
+    }
+    if (p.WT) {  // W^T [c][r]: consecutive threads take consecutive rows r
+      float* wt = p.WT + tile * kTileKtT;
+#pragma unroll 4
+      for (int m = 0; m < kD * kC / kThreads; ++m) {
+        const int idx = m * kThreads + tid, c = idx >> 6, r = idx & 63;
+        wt[idx] = sWs[r * kWP + c];
+      }
+    }
+  }
+  __syncthreads();  // the W / U staging is reused for the transposed gated keys and queries
+  // Per-element outputs: thread c writes channel c of every row; KtT and QtT are staged padded
+  // [128][65] and leave as whole lines.
+  float* sKT = reinterpret_cast<float*>(sm + kOffWS);
+  float* sQT = reinterpret_cast<float*>(sm + kOffUS);
   {
     const int c = tid;
     const float glc = s_gl[c];
@@ -357,15 +370,25 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float qt = vt ? to_tf32(p.scale * s_rq[t] * expf(G) * bf16_at(sQ, t, c)) : 0.f;
       const float kt = vt ? to_tf32(s_rk[t] * expf(glc - G) * bf16_at(sK, t, c)) : 0.f;
       p.Qt[tile * kTileW + size_t(t) * kD + c] = qt;
-      p.KtT[tile * kTileKtT + size_t(c) * kC + t] = kt;
+      sKT[c * kTP + t] = kt;
       if (p.Kt) p.Kt[tile * kTileW + size_t(t) * kD + c] = kt;
-      if (p.QtT) p.QtT[tile * kTileKtT + size_t(c) * kC + t] = qt;
+      sQT[c * kTP + t] = qt;
       if (p.Gc) p.Gc[(tile * kC + t) * kD + c] = G;
     }
     if (tid < kC) {
       if (p.rq) p.rq[tile * kC + tid] = s_rq[tid];
       if (p.rk) p.rk[tile * kC + tid] = s_rk[tid];
       if (p.beff) p.beff[tile * kC + tid] = s_b[tid];
+    }
+  }
+  __syncthreads();
+  {
+    float* ktt = p.KtT + tile * kTileKtT;
+#pragma unroll 4
+    for (int m = 0; m < kD * kC / kThreads; ++m) {
+      const int idx = m * kThreads + tid, c = idx >> 6, t = idx & 63;
+      ktt[idx] = sKT[c * kTP + t];
+      if (p.QtT) p.QtT[tile * kTileKtT + idx] = sQT[c * kTP + t];
     }
   }
   tc_fence_before();

@@ -73,3 +73,9 @@ def test_kda_bwd_packed():
     lens = [1, 63, 64, 65, 130, 7]
     check_bwd(synth.custom(1, sum(lens), 2, per_channel=True, beta_logits=True, h0_std=0.02, dht_std=0.01,
                            lengths=lens, seed=51))
+
+
+def test_kda_bwd_strong_gates():
+    # decays of up to several units per token: the pair sums' block factorisation must stay finite
+    check_bwd(synth.custom(1, 192, 2, per_channel=True, beta_logits=True, h0_std=0.02, dht_std=0.01,
+                           seed=52, g_scale=2.0))
