@@ -26,6 +26,20 @@
 
 namespace gdn {
 
+#ifdef GDN_TRACE
+__device__ unsigned long long g_trace_tkda[4 * 16];
+#define BTRACE(slot)                                                                                    \
+  do {                                                                                                  \
+    if (blockIdx.y == 3 && threadIdx.x == 0 && blockIdx.x % 16 == 5 && blockIdx.x < 64)                 \
+      g_trace_tkda[(blockIdx.x / 16) * 16 + (slot)] = globaltimer();                                     \
+  } while (0)
+extern "C" int gdn_trace_tkda_read(unsigned long long* host) {
+  return cudaMemcpyFromSymbol(host, g_trace_tkda, sizeof(g_trace_tkda)) == cudaSuccess ? 0 : -1;
+}
+#else
+#define BTRACE(slot) do {} while (0)
+#endif
+
 namespace {
 
 constexpr int kThreads = 256;
@@ -58,13 +72,14 @@ __device__ __forceinline__ void put32(uint8_t* tile, int rows, int row, int col,
 // Everything stays in fp32. The block's rows are then written to the dk^ / dq^ / dG
 // accumulators, and k^ . X1 goes to dbeta.
 template <int I>
-__device__ __forceinline__ void kda_pair_block(const float* __restrict__ sG2, const uint8_t* sK, const uint8_t* sQ,
-                                               const float* s_rk, const float* s_rq, const float* s_b,
+__device__ __forceinline__ void kda_pair_block(const float* __restrict__ sG2, const uint8_t* __restrict__ sK,
+                                               const uint8_t* __restrict__ sQ, const float* __restrict__ s_rk,
+                                               const float* __restrict__ s_rq, const float* __restrict__ s_b,
                                                const float* __restrict__ sD, const float* __restrict__ sN,
-                                               float* sKacc, float* sQacc, float* sGacc, float* s_db, int c,
-                                               int lane) {
+                                               float* __restrict__ sKacc, float* __restrict__ sQacc,
+                                               float* __restrict__ sGacc, float* s_db, int c, int lane) {
   constexpr int r0 = 16 * I;
-  float x1[16], y1[16], kb[16], gb[16];
+  float x1[16], y1[16], z[16], kb[16], gb[16];
 #pragma unroll
   for (int r = 0; r < 16; ++r) {
     const int t = r0 + r;
@@ -72,6 +87,7 @@ __device__ __forceinline__ void kda_pair_block(const float* __restrict__ sG2, co
     kb[r] = s_rk[t] * bf16_at(sK, t, c);
     x1[r] = 0.f;
     y1[r] = 0.f;
+    z[r] = 0.f;
   }
   if constexpr (I > 0) {  // rows of the block against the earlier columns, four at a time
     const float R = gb[0];
@@ -98,56 +114,56 @@ __device__ __forceinline__ void kda_pair_block(const float* __restrict__ sG2, co
       y1[r] *= e;
     }
   }
-  {  // later rows against the columns of the block; Z collects in the dG accumulator's rows
-    float z[16];
+  if constexpr (I < 3) {  // later rows against the columns of the block
+    const float S = gb[15];
+#pragma unroll 2
+    for (int i = r0 + 16; i < kC; ++i) {
+      const float u = exp2f(sG2[i * kP + c] - S);
+      const float a = s_b[i] * s_rk[i] * bf16_at(sK, i, c) * u;
+      const float b = s_rq[i] * bf16_at(sQ, i, c) * u;
+      const float4* d4 = reinterpret_cast<const float4*>(sD + i * kC + r0);
+      const float4* n4 = reinterpret_cast<const float4*>(sN + i * kC + r0);
 #pragma unroll
-    for (int s = 0; s < 16; ++s) z[s] = 0.f;
-    if constexpr (I < 3) {
-      const float S = gb[15];
-#pragma unroll 4
-      for (int i = r0 + 16; i < kC; ++i) {
-        const float u = exp2f(sG2[i * kP + c] - S);
-        const float a = s_b[i] * s_rk[i] * bf16_at(sK, i, c) * u;
-        const float b = s_rq[i] * bf16_at(sQ, i, c) * u;
-        const float4* d4 = reinterpret_cast<const float4*>(sD + i * kC + r0);
-        const float4* n4 = reinterpret_cast<const float4*>(sN + i * kC + r0);
-#pragma unroll
-        for (int m = 0; m < 4; ++m) {
-          const float4 d = d4[m], n = n4[m];
-          z[4 * m] = fmaf(d.x, a, fmaf(n.x, b, z[4 * m]));
-          z[4 * m + 1] = fmaf(d.y, a, fmaf(n.y, b, z[4 * m + 1]));
-          z[4 * m + 2] = fmaf(d.z, a, fmaf(n.z, b, z[4 * m + 2]));
-          z[4 * m + 3] = fmaf(d.w, a, fmaf(n.w, b, z[4 * m + 3]));
-        }
+      for (int m = 0; m < 4; ++m) {
+        const float4 d = d4[m], n = n4[m];
+        z[4 * m] = fmaf(d.x, a, fmaf(n.x, b, z[4 * m]));
+        z[4 * m + 1] = fmaf(d.y, a, fmaf(n.y, b, z[4 * m + 1]));
+        z[4 * m + 2] = fmaf(d.z, a, fmaf(n.z, b, z[4 * m + 2]));
+        z[4 * m + 3] = fmaf(d.w, a, fmaf(n.w, b, z[4 * m + 3]));
       }
-#pragma unroll
-      for (int s = 0; s < 16; ++s) z[s] *= exp2f(S - gb[s]);
     }
 #pragma unroll
-    for (int s = 0; s < 16; ++s) sGacc[(r0 + s) * kD + c] = z[s];
+    for (int s = 0; s < 16; ++s) z[s] *= exp2f(S - gb[s]);
   }
 #pragma unroll
   for (int r = 0; r < 16; ++r) {  // pairs inside the block, i = r0 + r >= j = r0 + s
     const int i = r0 + r;
-    const float bi = s_b[i], qi = s_rq[i] * bf16_at(sQ, i, c);
-    const float ci = bi * kb[r];
+    const float ci = s_b[i] * kb[r], qi = s_rq[i] * bf16_at(sQ, i, c);
+    const float4* d4 = reinterpret_cast<const float4*>(sD + i * kC + r0);
+    const float4* n4 = reinterpret_cast<const float4*>(sN + i * kC + r0);
 #pragma unroll
-    for (int s = 0; s <= r; ++s) {
-      const float e = exp2f(gb[r] - gb[s]);
-      const float dij = sD[i * kC + r0 + s], nij = sN[i * kC + r0 + s];
-      x1[r] = fmaf(dij * kb[s], e, x1[r]);
-      y1[r] = fmaf(nij * kb[s], e, y1[r]);
-      float* zs = sGacc + (r0 + s) * kD + c;
-      *zs = fmaf(fmaf(ci, dij, nij * qi), e, *zs);
+    for (int m = 0; m <= r / 4; ++m) {
+      const float4 d = d4[m], n = n4[m];
+      const float dd[4] = {d.x, d.y, d.z, d.w}, nn[4] = {n.x, n.y, n.z, n.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int s = 4 * m + e;
+        if (s <= r) {
+          const float ex = exp2f(gb[r] - gb[s]);
+          x1[r] = fmaf(dd[e] * kb[s], ex, x1[r]);
+          y1[r] = fmaf(nn[e] * kb[s], ex, y1[r]);
+          z[s] = fmaf(fmaf(ci, dd[e], nn[e] * qi), ex, z[s]);
+        }
+      }
     }
   }
 #pragma unroll
   for (int r = 0; r < 16; ++r) {
     const int t = r0 + r;
-    const float bt = s_b[t], qt = s_rq[t] * bf16_at(sQ, t, c), zt = sGacc[t * kD + c];
-    sKacc[t * kD + c] = bt * x1[r] + zt;
+    const float bt = s_b[t], qt = s_rq[t] * bf16_at(sQ, t, c);
+    sKacc[t * kD + c] = bt * x1[r] + z[r];
     sQacc[t * kD + c] = y1[r];
-    sGacc[t * kD + c] = bt * kb[r] * x1[r] + qt * y1[r] - kb[r] * zt;
+    sGacc[t * kD + c] = bt * kb[r] * x1[r] + qt * y1[r] - kb[r] * z[r];
     float part = kb[r] * x1[r];
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) part += __shfl_xor_sync(0xffffffffu, part, off);
@@ -184,6 +200,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const float scale = p.scale;
   const int cc = tid & 127;   // channel handled in the CUDA-core phases
 
+  BTRACE(0);
   if (warp == 0) tmem_alloc(&tslot, 256);
   if (tid == 0) {
     abort_flag = 0;
@@ -239,6 +256,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   fence_async_smem();
   __syncthreads();
   const bool tma_ok = mbar_wait(&bar_tma, 0, &abort_flag, p.status, kDevTimeoutTma);
+  BTRACE(1);
   if (tid >= len && tid < kC) {
     for (int c16 = 0; c16 < 16; ++c16) {
       const uint32_t off = sw128_offset(tid, c16 * 8, kC, 2);
@@ -260,6 +278,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   __syncwarp();
   bool ok = tma_ok && mbar_wait(&bar_mma, 0, &abort_flag, p.status, kDevTimeoutMma);
+  BTRACE(2);
   tc_fence_after();
   // ---- K1 = beta r_k exp(G) (.) k and V1 = beta v as 64-row operands [j][c]
   for (int j = 32 * half; j < 32 * half + 32; ++j) {
@@ -283,6 +302,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   ok = ok && mbar_wait(&bar_mma, 1, &abort_flag, p.status, kDevTimeoutMma);
   tc_fence_after();
   // ---- dL = -A^T dA A^T
+  BTRACE(3);
   uint8_t* sAT = sm + kR3;
   uint8_t* sdAT = sm + kR3 + 16384;
   uint8_t* sA = sm + kR4;
@@ -370,6 +390,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   tc_fence_before();
   __syncthreads();
+  BTRACE(4);
   // ---- decayed pair sums on CUDA cores: thread (channel cc, row blocks 2 half and 2 half + 1,
   // which balances the two halves' work). Rows past the chunk come out zero.
   float* sKacc = reinterpret_cast<float*>(sm + kR2);           // dk^ accumulator [64][128]
@@ -383,6 +404,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     kda_pair_block<3>(sG2, sK, sQ, s_rk, s_rq, s_b, sD, sN, sKacc, sQacc, sGacc, s_db, cc, lane);
   }
   __syncthreads();
+  BTRACE(5);
   // ---- per-token assembly (thread: channel cc, rows of parity `half`)
   float glast_part = 0.f;
   const float glc = sG2[(len - 1) * kP + cc];
@@ -430,6 +452,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   s_glast[half][cc] = glast_part;
   __syncthreads();
+  BTRACE(6);
   // ---- L2-norm backward and writes; dg by reverse cumulative sum per channel
   for (int t = half; t < len; t += 2) {
     const float rq = s_rq[t], rk = s_rk[t];
@@ -460,6 +483,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   tc_fence_before();
   __syncthreads();
+  BTRACE(7);
   if (warp == 0) tmem_dealloc(tb, 256);
 }
 

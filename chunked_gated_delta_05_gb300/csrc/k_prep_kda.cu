@@ -25,6 +25,20 @@
 
 namespace gdn {
 
+#ifdef GDN_TRACE
+__device__ unsigned long long g_trace_pkda[4 * 16];
+#define KTRACE(slot)                                                                                    \
+  do {                                                                                                  \
+    if (blockIdx.y == 3 && threadIdx.x == 0 && blockIdx.x % 16 == 5 && blockIdx.x < 64)                 \
+      g_trace_pkda[(blockIdx.x / 16) * 16 + (slot)] = globaltimer();                                     \
+  } while (0)
+extern "C" int gdn_trace_pkda_read(unsigned long long* host) {
+  return cudaMemcpyFromSymbol(host, g_trace_pkda, sizeof(g_trace_pkda)) == cudaSuccess ? 0 : -1;
+}
+#else
+#define KTRACE(slot) do {} while (0)
+#endif
+
 namespace {
 
 constexpr int kThreads = 128;
@@ -88,6 +102,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const ChunkEntry ch = p.chunks[c_idx];
   const int len = ch.y;
 
+  KTRACE(0);
   if (warp == 0) tmem_alloc(&tslot, 256);
   if (tid == 0) {
     // the barriers are this thread's alone until the block barrier below: start the loads now
@@ -133,6 +148,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tb = tslot;
   const uint32_t tl = tb + tmem_lane_base(warp);
   mbar_wait(&bar_tma, 0, &abort_flag, p.status, kDevTimeoutTma);
+  KTRACE(1);
   // rows past the chunk belong to the next document (or are zero): clear them
   if (tid >= len && tid < kC) {
     for (int c16 = 0; c16 < 16; ++c16) {
@@ -160,6 +176,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   s_gl[tid] = sG[(len - 1) * kGP + tid];
   __syncthreads();
+  KTRACE(2);
 
   // Stacked operand: rows 0..63 k^_i, rows 64..127 q^_i, each times exp(G_i - G_{r(i)}).
   uint8_t* sAS = sm + kOffAS;
@@ -229,6 +246,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  KTRACE(3);
 
   // Row blocks of L (lanes 0..63) and Aqk (lanes 64..127) from D_I, I = block of the row.
   // Aqk rows are staged (padded [64][65]) and leave as whole lines, row-major and transposed.
@@ -258,6 +276,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  KTRACE(4);
   if (ok) {
     float* aqk = p.Aqk + tile * kTileAqk;
 #pragma unroll 4
@@ -270,6 +289,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   float* sX = reinterpret_cast<float*>(sm + kOffX);
   unit_lower_inverse_column(sLT, sX, 16 * warp + (lane & 15), lane >> 4);
   __syncthreads();
+  KTRACE(5);
   // WY operands: A1 = (A - I) diag(beta r_k) (tf32), A2 = (A - I) diag(beta) (bf16), both
   // K-major [i][j]; K1T = (k (.) exp(G))^T (tf32, K-major [c][j]).
   {
@@ -286,15 +306,22 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int i = i0; i < i0 + 32; ++i) a[size_t(i) * kC] = sX[i * kC + j];
     }
     const int c = tid;
-    for (int jj = 0; jj < kC; ++jj) {
-      const float val = jj < len ? bf16_at(sK, jj, c) * expf(sG[jj * kGP + c]) : 0.f;
-      put32(sm + kOffK1T, kD, c, jj, to_tf32(val));
+#pragma unroll 2
+    for (int j4 = 0; j4 < kC; j4 += 4) {  // four columns of row c: one 16-byte chunk
+      float v4[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int jj = j4 + e;
+        v4[e] = jj < len ? to_tf32(bf16_at(sK, jj, c) * expf(sG[jj * kGP + c])) : 0.f;
+      }
+      *reinterpret_cast<float4*>(sm + kOffK1T + sw128_offset(c, j4, kD, 4)) = make_float4(v4[0], v4[1], v4[2], v4[3]);
     }
   }
   fence_async_smem();
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  KTRACE(6);
   if (tid == 0 && ok) {
     const uint32_t a1 = smem_u32(sm + kOffA1), a2 = smem_u32(sm + kOffA2), k1t = smem_u32(sm + kOffK1T);
     const uint32_t v0 = smem_u32(sV);
@@ -307,37 +334,38 @@ __global__ void __launch_bounds__(kThreads, 1)
   ok = ok && mbar_wait(&bar_mma, mma_phase, &abort_flag, p.status, kDevTimeoutMma);
   tc_fence_after();
   __syncthreads();  // the operand regions are free from here: W and U are staged over them
-  // W and U rows (64-row MMA results: lane 32*(r/16) + r%16 holds row r), staged padded
-  // [64][129] and written back as whole lines.
+  KTRACE(7);
+  // W and U rows (64-row MMA results: lane 32*(r/16) + r%16 holds row r), read with the
+  // 16x64b shape so that all 32 lanes work (lane t: row (t >> 2) + 8 (t & 1) of the warp's 16,
+  // columns ((t >> 1) & 1) + 2 e), staged padded [64][129] and written back as whole lines.
   float* sWs = reinterpret_cast<float*>(sm + kOffWS);
   float* sUs = reinterpret_cast<float*>(sm + kOffUS);
   if (ok) {
-    const bool owner = lane < 16;
-    const int r = 16 * warp + (lane & 15);
-    const bool vr = owner && r < len;
+    const int r = 16 * warp + (lane >> 2) + 8 * (lane & 1);
+    const int cpar = (lane >> 1) & 1;
+    const bool vr = r < len;
     const float dw = s_b[r] * s_rk[r], du = s_b[r];
     for (int which = 0; which < 2; ++which) {
       float* st = which == 0 ? sWs : sUs;
-      for (int half = 0; half < 2; ++half) {
-        float x[64];
-        tmem_ld64(tl + which * 128 + half * 64, x);
+      for (int q = 0; q < 4; ++q) {
+        float x[16];
+        tmem_ld16x64b_x16(tl + which * 128 + 32 * q, x);
         tmem_wait_ld_regs(x);
-        if (owner) {
 #pragma unroll
-          for (int e = 0; e < 64; ++e) {
-            const int c = half * 64 + e;
-            float val = 0.f;
-            if (vr) {
-              val = which == 0 ? to_tf32(fmaf(dw * expf(sG[r * kGP + c]), bf16_at(sK, r, c), x[e]))
-                               : fmaf(du, bf16_at(sV, r, c), x[e]);
-            }
-            st[r * kWP + c] = val;
+        for (int e = 0; e < 16; ++e) {
+          const int c = 32 * q + cpar + 2 * e;
+          float val = 0.f;
+          if (vr) {
+            val = which == 0 ? to_tf32(fmaf(dw * expf(sG[r * kGP + c]), bf16_at(sK, r, c), x[e]))
+                             : fmaf(du, bf16_at(sV, r, c), x[e]);
           }
+          st[r * kWP + c] = val;
         }
       }
     }
   }
   __syncthreads();
+  KTRACE(8);
   if (ok && len > 0) {
     float* w = p.W + tile * kTileW;
     float* u = p.U + tile * kTileW;
@@ -356,6 +384,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
   __syncthreads();  // the W / U staging is reused for the transposed gated keys and queries
+  KTRACE(9);
   // Per-element outputs: thread c writes channel c of every row; KtT and QtT are staged padded
   // [128][65] and leave as whole lines.
   float* sKT = reinterpret_cast<float*>(sm + kOffWS);
@@ -382,6 +411,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
   __syncthreads();
+  KTRACE(10);
   {
     float* ktt = p.KtT + tile * kTileKtT;
 #pragma unroll 4
@@ -393,6 +423,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   tc_fence_before();
   __syncthreads();
+  KTRACE(11);
   if (warp == 0) tmem_dealloc(tb, 256);
 }
 
