@@ -40,16 +40,16 @@ KERNEL_FLOP_PER_CHUNK_HEAD = {
     "group_sum": (0, "none"),   # grouped q/k heads only
 }
 TF32_OVER_BF16 = 1.1 / 2.25    # nominal dense tf32 / bf16 tensor rates of a GB300
-# DRAM bytes (read + write) of one step's launches of a kernel, from an `ncu --set full`
-# capture of the same kernel build on the same workload (profiles/kernels_gdn_b2_t4096_h16.md);
-# None elsewhere, and None for a kernel changed since its capture.
+# DRAM bytes (read + write) of one step's launches of a kernel, from an ncu capture of
+# dram__bytes_read.sum and dram__bytes_write.sum on the same kernel build and workload
+# (profiles/kernels_gdn_b2_t4096_h16.md); None elsewhere, and None for a kernel changed since.
 NCU_TRAFFIC_BYTES = {
-    ("prepare", "gdn_b2_t4096_h16"): (104.885248 + 510.984448) * 1e6,
-    ("chain_fwd", "gdn_b2_t4096_h16"): (186.488832 + 38.409728 + 249.328128 + 138.250496) * 1e6,
-    ("compose", "gdn_b2_t4096_h16"): 2 * 21.011456e6,
-    ("chain_bwd", "gdn_b2_t4096_h16"): (216.477440 + 35.716352 + 230.844416 + 118.377984) * 1e6,
-    ("bwd_feat", "gdn_b2_t4096_h16"): (613.202176 + 294.521600) * 1e6,
-    ("bwd_tok", "gdn_b2_t4096_h16"): (640.715520 + 89.759744) * 1e6,
+    ("prepare", "gdn_b2_t4096_h16"): (104.809728 + 511.356416) * 1e6,
+    ("chain_fwd", "gdn_b2_t4096_h16"): (186.430720 + 34.938368 + 249.328384 + 136.796160) * 1e6,
+    ("compose", "gdn_b2_t4096_h16"): (21.011968 + 21.011712) * 1e6,
+    ("chain_bwd", "gdn_b2_t4096_h16"): (215.723008 + 31.762944 + 230.894080 + 114.701824) * 1e6,
+    ("bwd_feat", "gdn_b2_t4096_h16"): (476.296704 + 289.297664) * 1e6,
+    ("bwd_tok", "gdn_b2_t4096_h16"): (644.940288 + 85.933824) * 1e6,
 }
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
