@@ -1,4 +1,4 @@
-// Prepare kernel for Kimi Delta Attention (per-channel gate), one chunk per CTA.
+// Prepare kernel for Kimi Delta Attention (per-channel gate), one chunk per CTA of eight warps.
 //
 // With G[t][c] the chunk-local cumulative gate of key channel c (the `gk` slot of the KDA
 // staged native interface, `_KDAPrepared.gk`, kimi_delta_attention_ascendc.py coverage page)
@@ -41,7 +41,7 @@ extern "C" int gdn_trace_pkda_read(unsigned long long* host) {
 
 namespace {
 
-constexpr int kThreads = 128;
+constexpr int kThreads = 256;  // eight warps: two threads per row or channel in most phases
 constexpr int kGP = kD + 1;                                // padded row stride of G (floats)
 constexpr uint32_t kOffQ = 0, kOffK = 16384, kOffV = 32768;  // bf16 [64][128] tiles
 constexpr uint32_t kOffG = 49152;                          // fp32 [64][129]
@@ -97,6 +97,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __shared__ float s_rq[kC], s_rk[kC], s_b[kC], s_gl[kD];
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int hf = tid >> 7;     // which half of the block (rows or columns, per phase)
   const int c_idx = blockIdx.x, h = blockIdx.y, H = p.H;
   const size_t tile = size_t(c_idx) * H + h;
   const ChunkEntry ch = p.chunks[c_idx];
@@ -118,20 +119,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_load_2d(sV + pp * 8192, &mv, x, ch.x, &bar_tma);
     }
   }
-  // Cumulative gate of channel c = tid (rows past the chunk repeat the last value).
+  // Cumulative gate of channel c: each half sums its 32 rows; the second half adds the first
+  // half's total after the barrier (rows past the chunk repeat the last value).
   {
-    const int c = tid;
+    const int c = tid & 127, t0 = 32 * hf;
     const float* src = p.g + (size_t(ch.x) * H + h) * kD + c;
+    float buf[32];
+#pragma unroll
+    for (int e = 0; e < 32; ++e) buf[e] = (t0 + e < len) ? src[size_t(t0 + e) * H * kD] : 0.f;
     float run = 0.f;
-    for (int t0 = 0; t0 < kC; t0 += 32) {
-      float buf[32];
 #pragma unroll
-      for (int e = 0; e < 32; ++e) buf[e] = (t0 + e < len) ? src[size_t(t0 + e) * H * kD] : 0.f;
-#pragma unroll
-      for (int e = 0; e < 32; ++e) {
-        run += buf[e];
-        sG[(t0 + e) * kGP + c] = run;
-      }
+    for (int e = 0; e < 32; ++e) {
+      run += buf[e];
+      sG[(t0 + e) * kGP + c] = run;
     }
   }
   if (tid < kC) {
@@ -145,6 +145,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  if (hf == 1) {
+    const int c = tid & 127;
+    const float base = sG[31 * kGP + c];
+#pragma unroll 8
+    for (int t = 32; t < kC; ++t) sG[t * kGP + c] += base;
+  }
   const uint32_t tb = tslot;
   const uint32_t tl = tb + tmem_lane_base(warp);
   mbar_wait(&bar_tma, 0, &abort_flag, p.status, kDevTimeoutTma);
@@ -159,36 +165,41 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
   __syncthreads();
-  // L2-norm factors: threads 0..63 for q rows, 64..127 for k rows (eight columns per load).
+  // L2-norm factors: thread pairs (2 p, 2 p + 1) share row p % 64 of q (p < 64) or k, half the
+  // columns each (eight per load).
   {
-    const int t = tid & 63;
-    const uint8_t* src = tid < kC ? sQ : sK;
+    const int pr = tid >> 1, part = tid & 1, t = pr & 63;
+    const uint8_t* src = pr < kC ? sQ : sK;
     float ss = 0.f;
 #pragma unroll
-    for (int c16 = 0; c16 < 16; ++c16) {
+    for (int c16 = 8 * part; c16 < 8 * part + 8; ++c16) {
       float f[8];
       bf16x8_to_f32(*reinterpret_cast<const uint4*>(src + sw128_offset(t, c16 * 8, kC, 2)), f);
 #pragma unroll
       for (int e = 0; e < 8; ++e) ss = fmaf(f[e], f[e], ss);
     }
+    ss += __shfl_xor_sync(0xffffffffu, ss, 1);
     const float r = p.l2norm ? 1.f / sqrtf(ss + 1e-6f) : 1.f;
-    if (tid < kC) s_rq[t] = r; else s_rk[t] = r;
+    if (part == 0) {
+      if (pr < kC) s_rq[t] = r; else s_rk[t] = r;
+    }
   }
-  s_gl[tid] = sG[(len - 1) * kGP + tid];
+  if (tid < kD) s_gl[tid] = sG[(len - 1) * kGP + tid];
   __syncthreads();
   KTRACE(2);
 
-  // Stacked operand: rows 0..63 k^_i, rows 64..127 q^_i, each times exp(G_i - G_{r(i)}).
+  // Stacked operand: rows 0..63 k^_i, rows 64..127 q^_i, each times exp(G_i - G_{r(i)}); each
+  // thread builds half a row.
   uint8_t* sAS = sm + kOffAS;
   {
-    const int i = tid & 63;
-    const bool isq = tid >= kC;
+    const int row = tid & 127, i = row & 63;
+    const bool isq = row >= kC;
     const int rref = i & ~15;
     const float rs = isq ? s_rq[i] : s_rk[i];
     const bool vi = i < len;
     const uint8_t* src = isq ? sQ : sK;
 #pragma unroll 2
-    for (int c16 = 0; c16 < 16; ++c16) {
+    for (int c16 = 8 * hf; c16 < 8 * hf + 8; ++c16) {
       float f[8];
       bf16x8_to_f32(*reinterpret_cast<const uint4*>(src + sw128_offset(i, c16 * 8, kC, 2)), f);
 #pragma unroll
@@ -196,19 +207,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int c = 8 * c16 + e;
         f[e] = vi ? to_tf32(rs * f[e] * expf(sG[i * kGP + c] - sG[rref * kGP + c])) : 0.f;
       }
-      *reinterpret_cast<float4*>(sAS + sw128_offset(tid, 8 * c16, 128, 4)) = make_float4(f[0], f[1], f[2], f[3]);
-      *reinterpret_cast<float4*>(sAS + sw128_offset(tid, 8 * c16 + 4, 128, 4)) = make_float4(f[4], f[5], f[6], f[7]);
+      *reinterpret_cast<float4*>(sAS + sw128_offset(row, 8 * c16, 128, 4)) = make_float4(f[0], f[1], f[2], f[3]);
+      *reinterpret_cast<float4*>(sAS + sw128_offset(row, 8 * c16 + 4, 128, 4)) = make_float4(f[4], f[5], f[6], f[7]);
     }
   }
-  // B_I = k^_j exp(G_{r_I} - G_j) for j <= 16 I + 15 (zero elsewhere), two blocks at a time.
+  // B_I = k^_j exp(G_{r_I} - G_j) for j <= 16 I + 15 (zero elsewhere), two blocks at a time;
+  // each thread builds half a row.
   auto build_b = [&](int I0) {
-    const int j = tid & 63, I = I0 + (tid >> 6);
+    const int j = tid & 63, which = (tid >> 6) & 1, I = I0 + which;
     const int rref = 16 * I;
-    uint8_t* dst = sm + kOffB + (tid >> 6) * 32768;
+    uint8_t* dst = sm + kOffB + which * 32768;
     const bool vj = j < len && j <= 16 * I + 15;  // a select: the exponent is unbounded elsewhere
     const float rs = s_rk[j];
 #pragma unroll 2
-    for (int c16 = 0; c16 < 16; ++c16) {
+    for (int c16 = 8 * hf; c16 < 8 * hf + 8; ++c16) {
       float f[8];
       bf16x8_to_f32(*reinterpret_cast<const uint4*>(sK + sw128_offset(j, c16 * 8, kC, 2)), f);
 #pragma unroll
@@ -248,29 +260,36 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   KTRACE(3);
 
-  // Row blocks of L (lanes 0..63) and Aqk (lanes 64..127) from D_I, I = block of the row.
-  // Aqk rows are staged (padded [64][65]) and leave as whole lines, row-major and transposed.
+  // Row blocks of L (lanes 0..63) and Aqk (lanes 64..127) from D_I, I = block of the row; the
+  // two halves of the block take 32 columns j each. Aqk rows are staged (padded [64][65]) and
+  // leave as whole lines, row-major and transposed.
   float* sLT = reinterpret_cast<float*>(sm + kOffLT);
   float* sAqk = reinterpret_cast<float*>(sm + kOffAqkS);
   if (ok) {
-    const int i = tid & 63;
-    const bool isq = tid >= kC;
+    const int row = tid & 127, i = row & 63, j0 = 32 * hf;
+    const bool isq = row >= kC;
     // The lanes of one warp cover two row blocks (I0, I0 + 1); the TMEM load address must be
     // warp-uniform, so load both and select per lane.
     const int I0 = 2 * (warp & 1);
     const bool second = ((i >> 4) & 1) != 0;
-    float r0[64], r1[64];
-    tmem_ld64(tl + I0 * 64, r0);
-    tmem_ld64(tl + (I0 + 1) * 64, r1);
+    float r0[32], r1[32];
+    tmem_ld32(tl + I0 * 64 + j0, r0);
+    tmem_ld32(tl + (I0 + 1) * 64 + j0, r1);
     tmem_wait_ld_regs(r0);
     tmem_wait_ld_regs(r1);
     const bool vi = i < len;
     if (!isq) {
 #pragma unroll
-      for (int j = 0; j < kC; ++j) sLT[j * kC + i] = (j < i && vi) ? s_b[i] * (second ? r1[j] : r0[j]) : 0.f;
+      for (int jj = 0; jj < 32; ++jj) {
+        const int j = j0 + jj;
+        sLT[j * kC + i] = (j < i && vi) ? s_b[i] * (second ? r1[jj] : r0[jj]) : 0.f;
+      }
     } else {
 #pragma unroll
-      for (int j = 0; j < kC; ++j) sAqk[i * kAP + j] = (j <= i && vi) ? to_tf32(p.scale * (second ? r1[j] : r0[j])) : 0.f;
+      for (int jj = 0; jj < 32; ++jj) {
+        const int j = j0 + jj;
+        sAqk[i * kAP + j] = (j <= i && vi) ? to_tf32(p.scale * (second ? r1[jj] : r0[jj])) : 0.f;
+      }
     }
   }
   tc_fence_before();
@@ -287,27 +306,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
   float* sX = reinterpret_cast<float*>(sm + kOffX);
-  unit_lower_inverse_column(sLT, sX, 16 * warp + (lane & 15), lane >> 4);
-  __syncthreads();
-  KTRACE(5);
-  // WY operands: A1 = (A - I) diag(beta r_k) (tf32), A2 = (A - I) diag(beta) (bf16), both
-  // K-major [i][j]; K1T = (k (.) exp(G))^T (tf32, K-major [c][j]).
-  {
-    const int j = tid & 63, i0 = 32 * (tid >> 6);
-    const float s1 = s_b[j] * s_rk[j], s2 = s_b[j];
-#pragma unroll 4
-    for (int i = i0; i < i0 + 32; ++i) {
-      const float x = i == j ? 0.f : sX[i * kC + j];
-      put32(sm + kOffA1, kC, i, j, to_tf32(x * s1));
-      *reinterpret_cast<__nv_bfloat16*>(sm + kOffA2 + sw128_offset(i, j, kC, 2)) = __float2bfloat16_rn(x * s2);
-    }
-    if (p.A) {
-      float* a = p.A + tile * kTileAqk + j;
-      for (int i = i0; i < i0 + 32; ++i) a[size_t(i) * kC] = sX[i * kC + j];
-    }
-    const int c = tid;
+  if (hf == 0) {
+    // warps 0-3: A = (I + L)^-1, one column per lane pair
+    unit_lower_inverse_column(sLT, sX, 16 * warp + (lane & 15), lane >> 4);
+  } else {
+    // warps 4-7 meanwhile: K1T = (k (.) exp(G))^T (tf32, K-major [c][j]), row c, 16-byte chunks
+    const int c = tid - 128;
 #pragma unroll 2
-    for (int j4 = 0; j4 < kC; j4 += 4) {  // four columns of row c: one 16-byte chunk
+    for (int j4 = 0; j4 < kC; j4 += 4) {
       float v4[4];
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
@@ -315,6 +321,24 @@ __global__ void __launch_bounds__(kThreads, 1)
         v4[e] = jj < len ? to_tf32(bf16_at(sK, jj, c) * expf(sG[jj * kGP + c])) : 0.f;
       }
       *reinterpret_cast<float4*>(sm + kOffK1T + sw128_offset(c, j4, kD, 4)) = make_float4(v4[0], v4[1], v4[2], v4[3]);
+    }
+  }
+  __syncthreads();
+  KTRACE(5);
+  // WY operands: A1 = (A - I) diag(beta r_k) (tf32), A2 = (A - I) diag(beta) (bf16), both
+  // K-major [i][j]; four threads per column j, 16 rows each.
+  {
+    const int j = tid & 63, i0 = 16 * (tid >> 6);
+    const float s1 = s_b[j] * s_rk[j], s2 = s_b[j];
+#pragma unroll 4
+    for (int i = i0; i < i0 + 16; ++i) {
+      const float x = i == j ? 0.f : sX[i * kC + j];
+      put32(sm + kOffA1, kC, i, j, to_tf32(x * s1));
+      *reinterpret_cast<__nv_bfloat16*>(sm + kOffA2 + sw128_offset(i, j, kC, 2)) = __float2bfloat16_rn(x * s2);
+    }
+    if (p.A) {
+      float* a = p.A + tile * kTileAqk + j;
+      for (int i = i0; i < i0 + 16; ++i) a[size_t(i) * kC] = sX[i * kC + j];
     }
   }
   fence_async_smem();
@@ -337,17 +361,18 @@ __global__ void __launch_bounds__(kThreads, 1)
   KTRACE(7);
   // W and U rows (64-row MMA results: lane 32*(r/16) + r%16 holds row r), read with the
   // 16x64b shape so that all 32 lanes work (lane t: row (t >> 2) + 8 (t & 1) of the warp's 16,
-  // columns ((t >> 1) & 1) + 2 e), staged padded [64][129] and written back as whole lines.
+  // columns ((t >> 1) & 1) + 2 e); warps w and w + 4 take two 32-column groups each. Staged
+  // padded [64][129] and written back as whole lines.
   float* sWs = reinterpret_cast<float*>(sm + kOffWS);
   float* sUs = reinterpret_cast<float*>(sm + kOffUS);
   if (ok) {
-    const int r = 16 * warp + (lane >> 2) + 8 * (lane & 1);
+    const int r = 16 * (warp & 3) + (lane >> 2) + 8 * (lane & 1);
     const int cpar = (lane >> 1) & 1;
     const bool vr = r < len;
     const float dw = s_b[r] * s_rk[r], du = s_b[r];
     for (int which = 0; which < 2; ++which) {
       float* st = which == 0 ? sWs : sUs;
-      for (int q = 0; q < 4; ++q) {
+      for (int q = 2 * hf; q < 2 * hf + 2; ++q) {
         float x[16];
         tmem_ld16x64b_x16(tl + which * 128 + 32 * q, x);
         tmem_wait_ld_regs(x);
@@ -367,12 +392,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   KTRACE(8);
   if (ok && len > 0) {
+    const int col = tid & 127;
     float* w = p.W + tile * kTileW;
     float* u = p.U + tile * kTileW;
 #pragma unroll 4
-    for (int r = 0; r < kC; ++r) {
-      w[size_t(r) * kD + tid] = sWs[r * kWP + tid];
-      u[size_t(r) * kD + tid] = sUs[r * kWP + tid];
+    for (int r = 32 * hf; r < 32 * hf + 32; ++r) {
+      w[size_t(r) * kD + col] = sWs[r * kWP + col];
+      u[size_t(r) * kD + col] = sUs[r * kWP + col];
     }
     if (p.WT) {  // W^T [c][r]: consecutive threads take consecutive rows r
       float* wt = p.WT + tile * kTileKtT;
@@ -385,15 +411,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   __syncthreads();  // the W / U staging is reused for the transposed gated keys and queries
   KTRACE(9);
-  // Per-element outputs: thread c writes channel c of every row; KtT and QtT are staged padded
-  // [128][65] and leave as whole lines.
+  // Per-element outputs: thread (c, half) writes channel c of 32 rows; KtT and QtT are staged
+  // padded [128][65] and leave as whole lines.
   float* sKT = reinterpret_cast<float*>(sm + kOffWS);
   float* sQT = reinterpret_cast<float*>(sm + kOffUS);
   {
-    const int c = tid;
+    const int c = tid & 127;
     const float glc = s_gl[c];
-    p.gam[tile * kD + c] = expf(glc);
-    for (int t = 0; t < kC; ++t) {
+    if (hf == 0) p.gam[tile * kD + c] = expf(glc);
+    for (int t = 32 * hf; t < 32 * hf + 32; ++t) {
       const bool vt = t < len;
       const float G = sG[t * kGP + c];
       const float qt = vt ? to_tf32(p.scale * s_rq[t] * expf(G) * bf16_at(sQ, t, c)) : 0.f;
