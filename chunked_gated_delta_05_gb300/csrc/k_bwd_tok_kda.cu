@@ -70,15 +70,15 @@ __device__ __forceinline__ void put32(uint8_t* tile, int rows, int row, int col,
 //   exp(G_i - G_j) = exp(G_i - G_s) exp(G_s - G_j),  s = 16 I + 15.
 // The 136 pairs inside the block take their exponent directly, shared by the three sums.
 // Everything stays in fp32. The block's rows are then written to the dk^ / dq^ / dG
-// accumulators, and k^ . X1 goes to dbeta.
-template <int I>
-__device__ __forceinline__ void kda_pair_block(const float* __restrict__ sG2, const uint8_t* __restrict__ sK,
+// accumulators, and k^ . X1 goes to dbeta. One copy of the code serves every block (I is a
+// run-time value), which keeps the kernel's instruction footprint small.
+__device__ __forceinline__ void kda_pair_block(int I, const float* __restrict__ sG2, const uint8_t* __restrict__ sK,
                                                const uint8_t* __restrict__ sQ, const float* __restrict__ s_rk,
                                                const float* __restrict__ s_rq, const float* __restrict__ s_b,
                                                const float* __restrict__ sD, const float* __restrict__ sN,
                                                float* __restrict__ sKacc, float* __restrict__ sQacc,
                                                float* __restrict__ sGacc, float* s_db, int c, int lane) {
-  constexpr int r0 = 16 * I;
+  const int r0 = 16 * I;
   float x1[16], y1[16], z[16], kb[16], gb[16];
 #pragma unroll
   for (int r = 0; r < 16; ++r) {
@@ -89,7 +89,7 @@ __device__ __forceinline__ void kda_pair_block(const float* __restrict__ sG2, co
     y1[r] = 0.f;
     z[r] = 0.f;
   }
-  if constexpr (I > 0) {  // rows of the block against the earlier columns, four at a time
+  {  // rows of the block against the earlier columns, four at a time
     const float R = gb[0];
 #pragma unroll 1
     for (int m = 0; m < r0 / 4; ++m) {
@@ -114,7 +114,7 @@ __device__ __forceinline__ void kda_pair_block(const float* __restrict__ sG2, co
       y1[r] *= e;
     }
   }
-  if constexpr (I < 3) {  // later rows against the columns of the block
+  {  // later rows against the columns of the block
     const float S = gb[15];
 #pragma unroll 2
     for (int i = r0 + 16; i < kC; ++i) {
@@ -315,21 +315,18 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int m = 0; m < 32; ++m) put32(sdAT, kC, 32 * half + m, rr, to_tf32(r[m]));
     }
+    // A [i][j] read once, coalesced (thread: column j, 16 rows i), into both operands: A^T
+    // (row j, four consecutive i per 16-byte chunk) and A (row i, column j)
     const float* a = p.A + tile * kTileAqk;
-    const int j = tid & 63, grp = tid >> 6;
-    const int i0 = 32 * (grp & 1);
-    float buf[32];
-    if (grp < 2) {
+    const int j = tid & 63, i0 = 16 * (tid >> 6);
+    float buf[16];
 #pragma unroll
-      for (int e = 0; e < 32; ++e) buf[e] = a[size_t(i0 + e) * kC + j];
+    for (int e = 0; e < 16; ++e) buf[e] = to_tf32(a[size_t(i0 + e) * kC + j]);
 #pragma unroll
-      for (int e = 0; e < 32; ++e) put32(sAT, kC, j, i0 + e, to_tf32(buf[e]));
-    } else {
+    for (int e = 0; e < 16; e += 4)
+      *reinterpret_cast<float4*>(sAT + sw128_offset(j, i0 + e, kC, 4)) = make_float4(buf[e], buf[e + 1], buf[e + 2], buf[e + 3]);
 #pragma unroll
-      for (int e = 0; e < 32; ++e) buf[e] = a[size_t(j) * kC + i0 + e];
-#pragma unroll
-      for (int e = 0; e < 32; ++e) put32(sA, kC, j, i0 + e, to_tf32(buf[e]));
-    }
+    for (int e = 0; e < 16; ++e) put32(sA, kC, i0 + e, j, buf[e]);
   }
   fence_async_smem();
   tc_fence_before();
@@ -396,13 +393,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   float* sKacc = reinterpret_cast<float*>(sm + kR2);           // dk^ accumulator [64][128]
   float* sQacc = reinterpret_cast<float*>(sm + kR3);           // dq^ accumulator [64][128]
   float* sGacc = reinterpret_cast<float*>(sm + kR4);           // dG accumulator [64][128]
-  if (half == 0) {
-    kda_pair_block<0>(sG2, sK, sQ, s_rk, s_rq, s_b, sD, sN, sKacc, sQacc, sGacc, s_db, cc, lane);
-    kda_pair_block<1>(sG2, sK, sQ, s_rk, s_rq, s_b, sD, sN, sKacc, sQacc, sGacc, s_db, cc, lane);
-  } else {
-    kda_pair_block<2>(sG2, sK, sQ, s_rk, s_rq, s_b, sD, sN, sKacc, sQacc, sGacc, s_db, cc, lane);
-    kda_pair_block<3>(sG2, sK, sQ, s_rk, s_rq, s_b, sD, sN, sKacc, sQacc, sGacc, s_db, cc, lane);
-  }
+#pragma unroll 1
+  for (int b = 0; b < 2; ++b)
+    kda_pair_block(2 * half + b, sG2, sK, sQ, s_rk, s_rq, s_b, sD, sN, sKacc, sQacc, sGacc, s_db, cc, lane);
   __syncthreads();
   BTRACE(5);
   // ---- per-token assembly (thread: channel cc, rows of parity `half`)

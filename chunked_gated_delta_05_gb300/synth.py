@@ -57,6 +57,8 @@ WORKLOADS = {
     "kda_b1_t8192_h32": Workload("kda_b1_t8192_h32", 1, 8192, 32, per_channel=True,
                                  beta_logits=True, seed=4),
     "gdn_b1_t8192_h16": Workload("gdn_b1_t8192_h16", 1, 8192, 16, seed=5),
+    # a smaller KDA case for kernel profiles (inputs still larger than L2)
+    "kda_b1_t4096_h32": Workload("kda_b1_t4096_h32", 1, 4096, 32, per_channel=True, beta_logits=True, seed=7),
     # grouped q/k heads (next row of the plan): 16 value heads over 4 q/k heads
     "gdn_gqa_b2_t4096_h16_hk4": Workload("gdn_gqa_b2_t4096_h16_hk4", 2, 4096, 16, h0_std=0.02, seed=6,
                                          num_k_heads=4),
