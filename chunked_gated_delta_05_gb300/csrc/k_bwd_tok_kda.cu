@@ -199,6 +199,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int rr = 16 * wq + (lane & 15);
   const float scale = p.scale;
   const int cc = tid & 127;   // channel handled in the CUDA-core phases
+  const float dgam_c = p.dgam[tile * kD + cc];  // requested now, used by the last phase
 
   BTRACE(0);
   if (warp == 0) tmem_alloc(&tslot, 256);
@@ -413,33 +414,50 @@ __global__ void __launch_bounds__(kThreads, 1)
       dkt8[e] = p.dKt[o];
       dv18[e] = p.dV1[o];
     }
+    // per-row sums over the channels of dbeta, q^ . dq^ and k^ . dk^: 24 values per thread,
+    // reduce-scattered over the warp (each lane group of four ends with three of the sums)
+    float v[24];
 #pragma unroll
     for (int e = 0; e < 8; ++e) {
       const int t = t0 + 2 * e;
-      if (t >= len) break;  // warp-uniform
-      const float dqt = dqt8[e], dk1 = dk18[e], dkt = dkt8[e], dv1 = dv18[e];
-      const float G = sG2[t * kP + cc];
-      const float eG = exp2f(G), eL = exp2f(glc - G);
-      const float qh = s_rq[t] * bf16_at(sQ, t, cc), kh = s_rk[t] * bf16_at(sK, t, cc);
-      const float dqh = sQacc[t * kD + cc] + scale * eG * dqt;
-      const float dkh = sKacc[t * kD + cc] + s_b[t] * eG * dk1 + eL * dkt;
-      sQacc[t * kD + cc] = dqh;
-      sKacc[t * kD + cc] = dkh;
-      sGacc[t * kD + cc] += s_b[t] * eG * dk1 * kh + scale * eG * dqt * qh - eL * dkt * kh;
-      glast_part = fmaf(eL * dkt, kh, glast_part);
-      p.dv[(size_t(ch.x + t) * H + h) * kD + cc] = __float2bfloat16_rn(s_b[t] * dv1);
-      float pb = eG * dk1 * kh + dv1 * bf16_at(sV, t, cc);
-      float pq = dqh * qh, pk = dkh * kh;
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) {
-        pb += __shfl_xor_sync(0xffffffffu, pb, off);
-        pq += __shfl_xor_sync(0xffffffffu, pq, off);
-        pk += __shfl_xor_sync(0xffffffffu, pk, off);
+      v[e] = v[8 + e] = v[16 + e] = 0.f;
+      if (t < len) {  // warp-uniform
+        const float dqt = dqt8[e], dk1 = dk18[e], dkt = dkt8[e], dv1 = dv18[e];
+        const float G = sG2[t * kP + cc];
+        const float eG = exp2f(G), eL = exp2f(glc - G);
+        const float qh = s_rq[t] * bf16_at(sQ, t, cc), kh = s_rk[t] * bf16_at(sK, t, cc);
+        const float dqh = sQacc[t * kD + cc] + scale * eG * dqt;
+        const float dkh = sKacc[t * kD + cc] + s_b[t] * eG * dk1 + eL * dkt;
+        sQacc[t * kD + cc] = dqh;
+        sKacc[t * kD + cc] = dkh;
+        sGacc[t * kD + cc] += s_b[t] * eG * dk1 * kh + scale * eG * dqt * qh - eL * dkt * kh;
+        glast_part = fmaf(eL * dkt, kh, glast_part);
+        p.dv[(size_t(ch.x + t) * H + h) * kD + cc] = __float2bfloat16_rn(s_b[t] * dv1);
+        v[e] = eG * dk1 * kh + dv1 * bf16_at(sV, t, cc);
+        v[8 + e] = dqh * qh;
+        v[16 + e] = dkh * kh;
       }
-      if (lane == 0) {
-        atomicAdd(&s_db[t], pb);
-        atomicAdd(&s_dotq[t], pq);
-        atomicAdd(&s_dotk[t], pk);
+    }
+    const bool b4 = lane & 16, b3 = lane & 8, b2 = lane & 4;
+    float w[12], u[6], y[3];
+#pragma unroll
+    for (int k = 0; k < 12; ++k)
+      w[k] = (b4 ? v[12 + k] : v[k]) + __shfl_xor_sync(0xffffffffu, b4 ? v[k] : v[12 + k], 16);
+#pragma unroll
+    for (int k = 0; k < 6; ++k)
+      u[k] = (b3 ? w[6 + k] : w[k]) + __shfl_xor_sync(0xffffffffu, b3 ? w[k] : w[6 + k], 8);
+#pragma unroll
+    for (int k = 0; k < 3; ++k) {
+      y[k] = (b2 ? u[3 + k] : u[k]) + __shfl_xor_sync(0xffffffffu, b2 ? u[k] : u[3 + k], 4);
+      y[k] += __shfl_xor_sync(0xffffffffu, y[k], 2);
+      y[k] += __shfl_xor_sync(0xffffffffu, y[k], 1);
+    }
+    if ((lane & 3) == 0) {
+      const int base = (b4 ? 12 : 0) + (b3 ? 6 : 0) + (b2 ? 3 : 0);
+#pragma unroll
+      for (int k = 0; k < 3; ++k) {
+        const int n = base + k, t = t0 + 2 * (n & 7);
+        if (t < len) atomicAdd((n < 8 ? s_db : (n < 16 ? s_dotq : s_dotk)) + t, y[k]);
       }
     }
   }
@@ -463,7 +481,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
   if (half == 0) {
-    float acc = s_glast[0][cc] + s_glast[1][cc] + exp2f(glc) * p.dgam[tile * kD + cc];
+    float acc = s_glast[0][cc] + s_glast[1][cc] + exp2f(glc) * dgam_c;
     for (int t = len - 1; t >= 0; --t) {
       acc += sGacc[t * kD + cc];
       p.dg[(size_t(ch.x + t) * H + h) * kD + cc] = acc;
