@@ -48,7 +48,6 @@ NCU_TRAFFIC_BYTES = {
     ("chain_fwd", "gdn_b2_t4096_h16"): (186.430720 + 34.938368 + 249.328384 + 136.796160) * 1e6,
     ("compose", "gdn_b2_t4096_h16"): (21.011968 + 21.011712) * 1e6,
     ("chain_bwd", "gdn_b2_t4096_h16"): (215.723008 + 31.762944 + 230.894080 + 114.701824) * 1e6,
-    ("bwd_feat", "gdn_b2_t4096_h16"): (476.296704 + 289.297664) * 1e6,
     ("bwd_tok", "gdn_b2_t4096_h16"): (644.940288 + 85.933824) * 1e6,
 }
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}

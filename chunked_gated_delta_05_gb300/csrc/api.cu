@@ -321,6 +321,7 @@ struct TimedLaunch {
 struct Maps {
   CUtensorMap q, k, v, W, Qt, KtT, Aqk, U, Usw;      // forward (Usw: U as a swizzled store target)
   CUtensorMap Kt, AqkT, QtT, WT, VN, DVN, DW, dO;     // backward
+  CUtensorMap Hs, DHs;                               // saved states h, dh' [tile][128][128] (128-row boxes)
 };
 
 // Row-major fp32 workspace tiles as TMA sources: `cols` per row, boxes of 32 columns.
@@ -349,7 +350,8 @@ bool bwd_maps(const Problem& P, const char* sv, const char* rs, const Layout& L,
   return tile_map(&M->Kt, sv + L.Kt, kD, r64, 64, true) && tile_map(&M->AqkT, sv + L.AqkT, kC, r64, 64, true) &&
          tile_map(&M->QtT, sv + L.QtT, kC, r128, 128, true) && tile_map(&M->WT, sv + L.WT, kC, r128, 128, true) &&
          tile_map(&M->VN, sv + L.vns, kD, r64, 64, true) && tile_map(&M->DVN, rs + L.dvns, kD, r64, 64, true) &&
-         tile_map(&M->DW, rs + L.dW, kD, r64, 64, true);
+         tile_map(&M->DW, rs + L.dW, kD, r64, 64, true) && tile_map(&M->Hs, sv + L.hs, kD, r128, 128, true) &&
+         tile_map(&M->DHs, rs + L.dhs, kD, r128, 128, true);
 }
 
 // Prepare-kernel parameters for a buffer carved by make_layout at `sv` (backward-mode outputs
@@ -634,7 +636,7 @@ int run_bwd(const gdn_desc_t* d, const gdn_bwd_args_t* a, void* stream, bool kda
   fp.status = a->status;
   {
     TimedLaunch tl_(kKBwdFeat, s);
-    rc = check_cuda(launch_bwd_feat(M.VN, M.DVN, M.dO, fp, s), "feature-major backward kernel");
+    rc = check_cuda(launch_bwd_feat(M.VN, M.DVN, M.dO, M.Hs, M.DHs, fp, s), "feature-major backward kernel");
   }
   if (rc) return rc;
 

@@ -200,7 +200,7 @@ cudaError_t launch_chain_bwd(const CUtensorMap& mKt, const CUtensorMap& mAqkT, c
                              const CUtensorMap& mWT, const CUtensorMap& mdO, const RevChainParams& p,
                              cudaStream_t s);
 cudaError_t launch_bwd_feat(const CUtensorMap& mVN, const CUtensorMap& mDVN, const CUtensorMap& mdO,
-                            const BwdFeatParams& p, cudaStream_t s);
+                            const CUtensorMap& mH, const CUtensorMap& mDH, const BwdFeatParams& p, cudaStream_t s);
 cudaError_t launch_bwd_tok(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, const CUtensorMap& mdO,
                            const CUtensorMap& mVN, const CUtensorMap& mDW, const CUtensorMap& mDVN, const BwdTokParams& p,
                            cudaStream_t s);

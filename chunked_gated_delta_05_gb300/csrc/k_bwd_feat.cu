@@ -13,9 +13,10 @@
 // GB300 mapping: one CTA per chunk and head, 256 threads; threads f and f + 128 own feature f
 // (= TMEM lane f) and split its columns in halves. h and dh' rows are loaded by their lane
 // owners and stored to TMEM (tf32) as A operands of kind::tf32 MMAs; dO^T, v_new, dv_new and A^T
-// are SW128 K-major B operands in shared memory (v_new, dv_new by TMA). Results leave as
-// token-major fp32 rows [t][f] (coalesced: the 128 threads of one token row write 512
-// contiguous bytes).
+// are SW128 K-major B operands in shared memory (v_new, dv_new by TMA). h and dh' arrive by
+// TMA too (128-row boxes, 128-byte swizzle), so each thread reads its row from shared memory
+// without bank conflicts. Results leave as token-major fp32 rows [t][f] (coalesced: the 128
+// threads of one token row write 512 contiguous bytes).
 #include "common.cuh"
 #include "umma.cuh"
 
@@ -42,10 +43,11 @@ constexpr int kThreads = 256;
 // (converted from the bf16 tile), rows 64-127 dv_new (TMA), so h dO^T and h dv_new^T are one
 // N = 128 product.
 constexpr uint32_t kOffC = 0;
-constexpr uint32_t kOffVN = 65536;    // v_new [t][v] (TMA), 4 panels x 64 rows
+constexpr uint32_t kOffVN = 65536;    // v_new [t][v] (TMA), 4 panels x 64 rows; first dh' panels 2-3
 constexpr uint32_t kOffAT = 98304;    // A^T  [j][i] tf32, 2 panels x 64 rows (16 KB)
 constexpr uint32_t kOffDO16 = 114688; // dO   [t][v] bf16 (TMA), 2 panels x 64 rows (16 KB)
-constexpr uint32_t kSmemBytes = 131072 + 1024;
+constexpr uint32_t kOffHS = 131072;   // h [f][v], 4 panels x 128 rows (64 KB), then dh' panels 0-1
+constexpr uint32_t kSmemBytes = kOffHS + 98304 + 1024;
 constexpr uint32_t kTH = 0, kTDH = 128, kTP1 = 256, kTP2 = 320, kTP3 = 384, kTP5 = 448;
 static_assert(kTP2 == kTP1 + 64, "h [dO ; dv_new]^T lands in P1 | P2");
 
@@ -57,10 +59,11 @@ __device__ __forceinline__ uint8_t* align1k(uint8_t* p) {
 
 __global__ void __launch_bounds__(kThreads, 1)
     k_bwd_feat(const __grid_constant__ CUtensorMap mVN, const __grid_constant__ CUtensorMap mDVN,
-               const __grid_constant__ CUtensorMap mdO, const BwdFeatParams p) {
+               const __grid_constant__ CUtensorMap mdO, const __grid_constant__ CUtensorMap mH,
+               const __grid_constant__ CUtensorMap mDH, const BwdFeatParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = align1k(smem_raw);
-  __shared__ uint64_t bar_tma, bar_mma;
+  __shared__ uint64_t bar_tma, bar_tma2, bar_mma;
   __shared__ uint32_t tslot;
   __shared__ int abort_flag;
   __shared__ float s_red[8];
@@ -72,28 +75,21 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int f = tid & 127, hf = tid >> 7;  // feature (TMEM lane) and column half
   FTRACE(0);
   const ChunkEntry ch = p.chunks[c];  // requested first: the dO load below waits on it
-  // Half hf of h and dh' row f, requested before the setup below (each thread reads 256
-  // contiguous bytes of each; the loads of one instruction touch 32 rows, every sector of
-  // which is used by the thread's neighbouring loads).
-  const float4* hrow = reinterpret_cast<const float4*>(p.h + tile * kD * kD + size_t(f) * kD + 64 * hf);
-  const float4* drow = reinterpret_cast<const float4*>(p.dh + tile * kD * kD + size_t(f) * kD + 64 * hf);
-  float4 hv[16], dv4[16];
-#pragma unroll
-  for (int e = 0; e < 16; ++e) {
-    hv[e] = __ldg(hrow + e);
-    dv4[e] = __ldg(drow + e);
-  }
 
   if (warp == 0) tmem_alloc(&tslot, 512);
   if (tid == 0) {
-    // the barriers are this thread's alone until the block barrier below: start the loads now
+    // the barriers are this thread's alone until the block barrier below: start the loads now.
+    // First group: h, dh' (dh' panels 2-3 sit in the v_new region until consumed), dv_new, dO.
     abort_flag = 0;
     mbar_init(&bar_tma, 1);
+    mbar_init(&bar_tma2, 1);
     mbar_init(&bar_mma, 1);
     fence_mbar_init();
-    mbar_expect_tx(&bar_tma, 65536u + 16384u);
+    mbar_expect_tx(&bar_tma, 2u * 65536u + 32768u + 16384u);
+    const int yh = int(tile) * kD;
     for (int pp = 0; pp < 4; ++pp) {
-      tma_load_2d(sm + kOffVN + pp * 8192, &mVN, pp * 32, int(tile) * kC, &bar_tma);
+      tma_load_2d(sm + kOffHS + pp * 16384, &mH, pp * 32, yh, &bar_tma);
+      tma_load_2d(sm + (pp < 2 ? kOffHS + 65536 + pp * 16384 : kOffVN + (pp - 2) * 16384), &mDH, pp * 32, yh, &bar_tma);
       tma_load_2d(sm + kOffC + pp * 16384 + 8192, &mDVN, pp * 32, int(tile) * kC, &bar_tma);
     }
     for (int pp = 0; pp < 2; ++pp) tma_load_2d(sm + kOffDO16 + pp * 8192, &mdO, h * kD + 64 * pp, ch.x, &bar_tma);
@@ -104,24 +100,39 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tb = tslot;
   const uint32_t tl = tb + tmem_lane_base(warp);
   FTRACE(1);
-  // h and dh' rows -> TMEM (tf32 A operands); dgam partial sums in fp32
+  // Half hf of the h and dh' rows f (shared memory -> TMEM as tf32 A operands); dgam partial
+  // sums in fp32. The rows are already tf32 values (the chains save their tf32 copies).
+  const bool tma_ok = mbar_wait(&bar_tma, 0, &abort_flag, p.status, kDevTimeoutTma);
   float dg = 0.f;
+  if (tma_ok) {
+    const uint8_t* dsrc = hf ? sm + kOffVN : sm + kOffHS + 65536;
 #pragma unroll
-  for (int q = 0; q < 2; ++q) {
-    float a[32], b[32];
+    for (int q = 0; q < 2; ++q) {
+      float a[32], b[32];
 #pragma unroll
-    for (int e = 0; e < 8; ++e) {
-      const float4 x = hv[8 * q + e], y = dv4[8 * q + e];
-      const float xs[4] = {x.x, x.y, x.z, x.w}, ys[4] = {y.x, y.y, y.z, y.w};
+      for (int e = 0; e < 8; ++e) {
+        const int col = 64 * hf + 32 * q + 4 * e;
+        const float4 x = *reinterpret_cast<const float4*>(sm + kOffHS + sw128_offset(f, col, 128, 4));
+        const float4 y = *reinterpret_cast<const float4*>(dsrc + sw128_offset(f, col - 64 * hf, 128, 4));
+        const float xs[4] = {x.x, x.y, x.z, x.w}, ys[4] = {y.x, y.y, y.z, y.w};
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        dg = fmaf(xs[u], ys[u], dg);
-        a[4 * e + u] = to_tf32(xs[u]);
-        b[4 * e + u] = to_tf32(ys[u]);
+        for (int u = 0; u < 4; ++u) {
+          dg = fmaf(xs[u], ys[u], dg);
+          a[4 * e + u] = xs[u];
+          b[4 * e + u] = ys[u];
+        }
       }
+      tmem_st32(tl + kTH + 64 * hf + 32 * q, a);
+      tmem_st32(tl + kTDH + 64 * hf + 32 * q, b);
     }
-    tmem_st32(tl + kTH + 64 * hf + 32 * q, a);
-    tmem_st32(tl + kTDH + 64 * hf + 32 * q, b);
+  }
+  // the v_new region is free once every thread has read its dh' rows: load v_new there
+  fence_async_smem();
+  __syncthreads();
+  if (tid == 0 && tma_ok) {
+    mbar_expect_tx(&bar_tma2, 32768u);
+    for (int pp = 0; pp < 4; ++pp)
+      tma_load_2d(sm + kOffVN + pp * 8192, &mVN, pp * 32, int(tile) * kC, &bar_tma2);
   }
   FTRACE(2);
   // A^T operand: element (j, i) = A[i][j]; four threads split the 64 rows i of column j = tid % 64.
@@ -137,7 +148,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   FTRACE(3);
   // dO^T operand: element (t, v=f) of the K-major [t][v] tile from the bf16 TMA tile (half hf
   // of the tokens); rows past the chunk (the next document's, or out of range) are zero.
-  const bool tma_ok = mbar_wait(&bar_tma, 0, &abort_flag, p.status, kDevTimeoutTma);
   if (tma_ok) {
 #pragma unroll 8
     for (int t = 32 * hf; t < 32 * hf + 32; ++t) {
@@ -161,7 +171,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t sC = smem_u32(sm + kOffC), sVN = smem_u32(sm + kOffVN);
       // [P1 | P2] (kTP2 = kTP1 + 64) = h [dO ; dv_new]^T, then P3 = dh' v_new^T
       for (int s = 0; s < 16; ++s) mma_tf32_ts(tb + kTP1, tb + kTH + s * 8, desc_kmajor(sC, 16384, s), id128, s > 0);
-      for (int s = 0; s < 16; ++s) mma_tf32_ts(tb + kTP3, tb + kTDH + s * 8, desc_kmajor(sVN, 8192, s), id64, s > 0);
+      if (mbar_wait(&bar_tma2, 0, &abort_flag, p.status, kDevTimeoutTma)) {
+        for (int s = 0; s < 16; ++s) mma_tf32_ts(tb + kTP3, tb + kTDH + s * 8, desc_kmajor(sVN, 8192, s), id64, s > 0);
+      }
       mma_commit(&bar_mma);
     }
     // while the products run: the next wave's CTA finds its inputs in L2
@@ -267,7 +279,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 cudaError_t launch_bwd_feat(const CUtensorMap& mVN, const CUtensorMap& mDVN, const CUtensorMap& mdO,
-                            const BwdFeatParams& p, cudaStream_t s) {
+                            const CUtensorMap& mH, const CUtensorMap& mDH, const BwdFeatParams& p, cudaStream_t s) {
   static bool attr = false;
   if (!attr) {
     cudaError_t e = cudaFuncSetAttribute(k_bwd_feat, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
@@ -275,7 +287,7 @@ cudaError_t launch_bwd_feat(const CUtensorMap& mVN, const CUtensorMap& mDVN, con
     attr = true;
   }
   dim3 grid(p.NC, p.H);
-  k_bwd_feat<<<grid, kThreads, kSmemBytes, s>>>(mVN, mDVN, mdO, p);
+  k_bwd_feat<<<grid, kThreads, kSmemBytes, s>>>(mVN, mDVN, mdO, mH, mDH, p);
   return cudaGetLastError();
 }
 
