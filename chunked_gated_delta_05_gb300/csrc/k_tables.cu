@@ -3,6 +3,8 @@
 // Each document is chunked from its own first token (the per-document chunk list of the
 // packed KDA interface, `_packed_metadata`: ceil(len/64) chunks per document, in document
 // order); a document's last chunk may be partial and is masked, never padded in memory.
+#include <algorithm>
+
 #include "common.cuh"
 
 namespace gdn {
@@ -57,7 +59,9 @@ cudaError_t launch_upload(const UploadParams& p, int* dst, cudaStream_t s) {
 }
 
 cudaError_t launch_tables(const TableParams& p, cudaStream_t s) {
-  k_tables<<<1, 1024, 0, s>>>(p);
+  // as many threads as sequences (whole warps, at most 1024): a short scan for a small batch
+  const int threads = std::min(1024, std::max(32, (p.N + 31) / 32 * 32));
+  k_tables<<<1, threads, 0, s>>>(p);
   return cudaGetLastError();
 }
 
