@@ -44,11 +44,12 @@ TF32_OVER_BF16 = 1.1 / 2.25    # nominal dense tf32 / bf16 tensor rates of a GB3
 # dram__bytes_read.sum and dram__bytes_write.sum on the same kernel build and workload
 # (profiles/kernels_gdn_b2_t4096_h16.md); None elsewhere, and None for a kernel changed since.
 NCU_TRAFFIC_BYTES = {
-    ("prepare", "gdn_b2_t4096_h16"): (104.809728 + 511.356416) * 1e6,
-    ("chain_fwd", "gdn_b2_t4096_h16"): (186.430720 + 34.938368 + 249.328384 + 136.796160) * 1e6,
-    ("compose", "gdn_b2_t4096_h16"): (21.011968 + 21.011712) * 1e6,
-    ("chain_bwd", "gdn_b2_t4096_h16"): (215.723008 + 31.762944 + 230.894080 + 114.701824) * 1e6,
-    ("bwd_tok", "gdn_b2_t4096_h16"): (644.940288 + 85.933824) * 1e6,
+    ("prepare", "gdn_b2_t4096_h16"): (104.790272 + 511.031040) * 1e6,
+    ("chain_fwd", "gdn_b2_t4096_h16"): (186.442752 + 35.709184 + 249.326592 + 136.108032) * 1e6,
+    ("compose", "gdn_b2_t4096_h16"): (21.011200 + 21.011200) * 1e6,
+    ("chain_bwd", "gdn_b2_t4096_h16"): (215.708160 + 31.632640 + 230.861568 + 115.156992) * 1e6,
+    ("bwd_feat", "gdn_b2_t4096_h16"): (479.928576 + 288.795392) * 1e6,
+    ("bwd_tok", "gdn_b2_t4096_h16"): (644.455168 + 85.959680) * 1e6,
 }
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
