@@ -19,8 +19,9 @@
 // GB300 mapping: dAqk, dA = [dW | dU][K1 | V1]^T, A^T dA and (A^T dA) A^T are 64-row
 // tcgen05 MMAs (kind::tf32) as in the scalar-gate kernel. The decayed pair sums run on the CUDA
 // cores in fp32, one thread per (channel, pair of 16-row blocks): pairs inside a block take
-// exp(G_ic - G_jc) directly, pairs across blocks factor it through the block's first or last
-// row into two factors of at most 1 (G falls along the chunk), so no exponent is per pair.
+// exp(G_ic - G_jc) as a running product of the per-token decays, pairs across blocks factor it
+// through the block's first or last row into two factors of at most 1 (G falls along the
+// chunk), so no exponent is per pair.
 #include "common.cuh"
 #include "umma.cuh"
 
@@ -68,7 +69,8 @@ __device__ __forceinline__ void put32(uint8_t* tile, int rows, int row, int col,
 //   exp(G_i - G_j) = exp(G_i - G_r) exp(G_r - G_j),  r = 16 I,
 // and for i > 16 I + 15 >= j,
 //   exp(G_i - G_j) = exp(G_i - G_s) exp(G_s - G_j),  s = 16 I + 15.
-// The 136 pairs inside the block take their exponent directly, shared by the three sums.
+// The 136 pairs inside the block take exp(G_i - G_j) as a running product of the per-token
+// decays (each <= 1), one exponent per row, shared by the three sums.
 // Everything stays in fp32. The block's rows are then written to the dk^ / dq^ / dG
 // accumulators, and k^ . X1 goes to dbeta. One copy of the code serves every block (I is a
 // run-time value), which keeps the kernel's instruction footprint small.
@@ -79,18 +81,17 @@ __device__ __forceinline__ void kda_pair_block(int I, const float* __restrict__ 
                                                float* __restrict__ sKacc, float* __restrict__ sQacc,
                                                float* __restrict__ sGacc, float* s_db, int c, int lane) {
   const int r0 = 16 * I;
-  float x1[16], y1[16], z[16], kb[16], gb[16];
+  const float R = sG2[r0 * kP + c], S = sG2[(r0 + 15) * kP + c];  // the block's first and last rows
+  float x1[16], y1[16], z[16], kb[16];
 #pragma unroll
   for (int r = 0; r < 16; ++r) {
     const int t = r0 + r;
-    gb[r] = sG2[t * kP + c];
     kb[r] = s_rk[t] * bf16_at(sK, t, c);
     x1[r] = 0.f;
     y1[r] = 0.f;
     z[r] = 0.f;
   }
   {  // rows of the block against the earlier columns, four at a time
-    const float R = gb[0];
 #pragma unroll 1
     for (int m = 0; m < r0 / 4; ++m) {
       float P[4];
@@ -109,13 +110,12 @@ __device__ __forceinline__ void kda_pair_block(int I, const float* __restrict__ 
     }
 #pragma unroll
     for (int r = 0; r < 16; ++r) {
-      const float e = exp2f(gb[r] - R);
+      const float e = exp2f(sG2[(r0 + r) * kP + c] - R);
       x1[r] *= e;
       y1[r] *= e;
     }
   }
   {  // later rows against the columns of the block
-    const float S = gb[15];
 #pragma unroll 2
     for (int i = r0 + 16; i < kC; ++i) {
       const float u = exp2f(sG2[i * kP + c] - S);
@@ -133,11 +133,23 @@ __device__ __forceinline__ void kda_pair_block(int I, const float* __restrict__ 
       }
     }
 #pragma unroll
-    for (int s = 0; s < 16; ++s) z[s] *= exp2f(S - gb[s]);
+    for (int s = 0; s < 16; ++s) z[s] *= exp2f(S - sG2[(r0 + s) * kP + c]);
   }
+  // Pairs inside the block, i = r0 + r >= j = r0 + s. ex[s] = exp(G_i - G_j) follows the rows
+  // as a running product of the per-token decays exp(G_r - G_{r-1}) <= 1: one exponent per row.
+  float ex[16];
+  float gprev = R;
 #pragma unroll
-  for (int r = 0; r < 16; ++r) {  // pairs inside the block, i = r0 + r >= j = r0 + s
+  for (int r = 0; r < 16; ++r) {
     const int i = r0 + r;
+    const float gr = sG2[i * kP + c];
+    if (r > 0) {
+      const float a = exp2f(gr - gprev);
+#pragma unroll
+      for (int s = 0; s < r; ++s) ex[s] *= a;
+    }
+    ex[r] = 1.f;
+    gprev = gr;
     const float ci = s_b[i] * kb[r], qi = s_rq[i] * bf16_at(sQ, i, c);
     const float4* d4 = reinterpret_cast<const float4*>(sD + i * kC + r0);
     const float4* n4 = reinterpret_cast<const float4*>(sN + i * kC + r0);
@@ -149,10 +161,9 @@ __device__ __forceinline__ void kda_pair_block(int I, const float* __restrict__ 
       for (int e = 0; e < 4; ++e) {
         const int s = 4 * m + e;
         if (s <= r) {
-          const float ex = exp2f(gb[r] - gb[s]);
-          x1[r] = fmaf(dd[e] * kb[s], ex, x1[r]);
-          y1[r] = fmaf(nn[e] * kb[s], ex, y1[r]);
-          z[s] = fmaf(fmaf(ci, dd[e], nn[e] * qi), ex, z[s]);
+          x1[r] = fmaf(dd[e] * kb[s], ex[s], x1[r]);
+          y1[r] = fmaf(nn[e] * kb[s], ex[s], y1[r]);
+          z[s] = fmaf(fmaf(ci, dd[e], nn[e] * qi), ex[s], z[s]);
         }
       }
     }

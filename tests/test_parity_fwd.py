@@ -68,3 +68,10 @@ def test_two_calls_identical():
     o2, h2 = run_gdn(d)
     np.testing.assert_array_equal(o1, o2)
     np.testing.assert_array_equal(h1, h2)
+
+
+@pytest.mark.parametrize("n_docs", [40, 1100])
+def test_many_short_documents(n_docs):
+    # more sequences than one warp, and more than one 1024-wide pass of the chunk-table scan
+    lens = [int(x) for x in np.random.RandomState(n_docs).randint(1, 5, size=n_docs)]
+    check(synth.custom(1, sum(lens), 1, lengths=lens, seed=6))
