@@ -32,6 +32,11 @@ def f64(t):
     (1, 200, 64, 3, 2, False, [0, 1, 70, 71, 200], False),
     (1, 333, 136, 8, 1, True, [0, 100, 333], True),
     (3, 65, 8, 1, 1, True, None, False),
+    # the halo length (W-1) d selects the kernels: up to 64 rows the shared-memory tiled ones,
+    # beyond that the per-row ones
+    (1, 200, 264, 6, 3, True, [0, 50, 200], False),
+    (1, 400, 256, 8, 5, True, None, False),
+    (1, 300, 64, 5, 20, False, None, False),
 ])
 def test_conv_parity(B, T, C, W, dil, act, packed, halo):
     N = B if packed is None else len(packed) - 1
