@@ -277,8 +277,8 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 
 int sm_count() {
   int dev = 0, n = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-    return 148;
-  return n > 0 ? n : 148;
+    return 152;  // a GB300's SM count
+  return n > 0 ? n : 152;
 }
 
 int check_cuda(cudaError_t e, const char* what) {
