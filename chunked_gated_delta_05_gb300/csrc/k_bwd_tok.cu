@@ -242,29 +242,17 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
     for (int m = 0; m < 16; ++m) put32(sdAT, kC, cj + 2 * m, ri, to_tf32(r[m]));
     {
-      // thread groups of 64: 0,1 write A^T (j, i) = A[i][j] for i in their half; 2,3 write
-      // A (l = j, m) = A[l][m] for m in their half.
+      // A [i][j] read once, coalesced (thread: column j, 16 rows i), into both operands: A^T
+      // (row j, four consecutive i per 16-byte chunk) and A (row i, column j)
       const float* a = p.A + tile * kTileAqk;
-      const int j = tid & 63, grp = tid >> 6;
-      {
-        const int i0 = 32 * (grp & 1);
-        float buf[32];
-        if (grp < 2) {
+      const int j = tid & 63, i0 = 16 * (tid >> 6);
+      float buf[16];
 #pragma unroll
-          for (int e = 0; e < 32; ++e) buf[e] = a[size_t(i0 + e) * kC + j];
+      for (int e = 0; e < 16; ++e) buf[e] = to_tf32(a[size_t(i0 + e) * kC + j]);
 #pragma unroll
-          for (int e = 0; e < 32; ++e) put32(sAT, kC, j, i0 + e, to_tf32(buf[e]));
-        } else {
-          const float4* row = reinterpret_cast<const float4*>(a + size_t(j) * kC + i0);
+      for (int e = 0; e < 16; e += 4) put32x4(sAT, kC, j, i0 + e, buf[e], buf[e + 1], buf[e + 2], buf[e + 3]);
 #pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            const float4 x = row[e];
-            buf[4 * e] = x.x; buf[4 * e + 1] = x.y; buf[4 * e + 2] = x.z; buf[4 * e + 3] = x.w;
-          }
-#pragma unroll
-          for (int e = 0; e < 32; ++e) put32(sA, kC, j, i0 + e, to_tf32(buf[e]));
-        }
-      }
+      for (int e = 0; e < 16; ++e) put32(sA, kC, i0 + e, j, buf[e]);
     }
   }
   fence_async_smem();
