@@ -49,7 +49,7 @@ NCU_TRAFFIC_BYTES = {
     ("compose", "gdn_b2_t4096_h16"): (21.011200 + 21.011200) * 1e6,
     ("chain_bwd", "gdn_b2_t4096_h16"): (215.708160 + 31.632640 + 230.861568 + 115.156992) * 1e6,
     ("bwd_feat", "gdn_b2_t4096_h16"): (479.928576 + 288.795392) * 1e6,
-    ("bwd_tok", "gdn_b2_t4096_h16"): (644.455168 + 85.959680) * 1e6,
+    ("bwd_tok", "gdn_b2_t4096_h16"): (644.071168 + 88.860416) * 1e6,
 }
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
