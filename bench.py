@@ -54,6 +54,22 @@ NCU_TRAFFIC_BYTES = {
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
+def max_over_ranks(x: float, device) -> float:
+    """The largest of every rank's x (the slowest rank's time); x itself on a single rank."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(units_per_rank: float, world: int, ms: float) -> float:
+    """Whole-job throughput: the units all ranks processed over the slowest rank's time."""
+    return units_per_rank * world / (ms * 1e-3)
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -323,13 +339,10 @@ def main():
     ms = t0.elapsed_time(t1) / args.steps
     per_kernel = _lib.timing_read()
     _lib.timing_enable(False)
-    if world > 1:
-        tms = torch.tensor([ms], device=dev)
-        dist.all_reduce(tms, op=dist.ReduceOp.MAX)
-        ms = float(tms.item())
+    ms = max_over_ranks(ms, dev)
 
     tokens = w.B * w.T
-    value = tokens * world / (ms * 1e-3)
+    value = job_throughput(tokens, world, ms)
     flop = (FWD_FLOP_PER_TOKEN_HEAD + BWD_FLOP_PER_TOKEN_HEAD) * tokens * w.H
     tflops = flop * world / (ms * 1e-3) / 1e12
     peaks, peak_src = load_peaks()
@@ -418,10 +431,7 @@ def main():
     e1.record(stream)
     torch.cuda.synchronize(dev)
     e_ms = e0.elapsed_time(e1) / args.steps
-    if world > 1:
-        tms = torch.tensor([e_ms], device=dev)
-        dist.all_reduce(tms, op=dist.ReduceOp.MAX)
-        e_ms = float(tms.item())
+    e_ms = max_over_ranks(e_ms, dev)
     if int(status.item()) != 0:
         raise RuntimeError(f"device status {int(status.item())} during the timed region")
 
@@ -435,7 +445,7 @@ def main():
                        "l2": "per-step working set (67 MB inputs + ~1 GB workspace) exceeds the 129 MB L2"},
             "tflops": tflops, "pct_of_bf16_peak": tflops / bf16_sus,
             "roofline": roofline, "clocks": clocks, "gpu_launches": gpu_launches,
-            "e2e": {"value": tokens * world / (e_ms * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+            "e2e": {"value": job_throughput(tokens, world, e_ms), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "ms_per_step": e_ms,
                     "copies": "pinned host buffers; inputs of step i+1 and outputs of step i-1 copied on two "
                               "streams while step i computes"}}
