@@ -1,8 +1,18 @@
 """Benchmark of the chunked gated delta rule on GB300: one step = forward + backward of the
-whole path (gdn_fwd in save mode, then gdn_bwd on the saved chunk intermediates) over one
-batch of synthetic inputs. Prints one JSON line.
+whole path (the forward in save mode, then the backward on its saved chunk intermediates) over
+one batch of synthetic input. Prints one JSON line.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--workload NAME]
+
+The headline is the largest single-GPU workload of the benchmark plan (GDN, B=1, T=32768,
+H=16); the other forward+backward workloads of the plan (the B=2 T=4096 training shape, packed
+documents, KDA, grouped q/k heads) are measured the same way and reported under `workloads`.
+
+Timing. Every timed region is exactly K steps between CUDA events on the launching stream,
+with a synchronize (and a barrier across ranks) on both sides. The region is repeated until
+the repeats span at least --min-seconds, and `ms_per_step` is the median over the repeats
+(all repeat times are reported). The library's per-launch timing hook is off in these regions;
+per-kernel device times come from a separate pass afterwards. Inputs are larger than L2.
 
 Under torchrun (N > 1) every rank runs the same workload on its own GPU (independent
 replicas, no collective on the data path); the reported value is all ranks' tokens divided
@@ -11,6 +21,7 @@ by the slowest rank's time.
 from __future__ import annotations
 
 import argparse
+import hashlib
 import json
 import os
 import statistics
@@ -23,11 +34,17 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "GDN/KDA fwd+bwd tokens/s and TFLOP/s on 1 GB300; % of bf16 TC peak"
-DEFAULT_WORKLOAD = "gdn_b2_t4096_h16"
+DEFAULT_WORKLOAD = "gdn_b1_t32768_h16"
+SECONDARY_WORKLOADS = ("gdn_b2_t4096_h16", "gdn_varlen_t16384_12docs_h16", "kda_b1_t8192_h32",
+                       "gdn_gqa_b2_t4096_h16_hk4", "gdn_b1_t8192_h16")
 # Algorithmic tensor-core work of the chunked form per (token, head), C=64, K=V=128:
 # forward 6CK + 4CV + 6KV, backward 12CK + 8CV + 12KV + 4C^2 (FLOP; recomputation excluded).
 FWD_FLOP_PER_TOKEN_HEAD = 180_224
 BWD_FLOP_PER_TOKEN_HEAD = 376_832
+# Minimal HBM bytes per (token, head): the inputs read and the outputs written once
+# (GDN: q, k, v, o 256 B each, g 4 B, beta 2 B; the backward adds dO and the gradients).
+IO_BYTES_PER_TOKEN_HEAD = {("gdn", "fwd"): 1030, ("gdn", "bwd"): 1804, ("kda", "fwd"): 1538,
+                           ("kda", "bwd"): 2820}
 # Useful MMA FLOP per (chunk, head) of each kernel (C=64, K=V=128) and its operand kind.
 KERNEL_FLOP_PER_CHUNK_HEAD = {
     "prepare": (4 * 2 * 64 * 64 * 128, "bf16"),            # K K^T, Q K^T, A K1, A V1
@@ -40,17 +57,14 @@ KERNEL_FLOP_PER_CHUNK_HEAD = {
     "group_sum": (0, "none"),   # grouped q/k heads only
 }
 TF32_OVER_BF16 = 1.1 / 2.25    # nominal dense tf32 / bf16 tensor rates of a GB300
-# DRAM bytes (read + write) of one step's launches of a kernel, from an ncu capture of
-# dram__bytes_read.sum and dram__bytes_write.sum on the same kernel build and workload
-# (profiles/kernels_gdn_b2_t4096_h16.md); None elsewhere, and None for a kernel changed since.
-NCU_TRAFFIC_BYTES = {
-    ("prepare", "gdn_b2_t4096_h16"): (104.790272 + 511.031040) * 1e6,
-    ("chain_fwd", "gdn_b2_t4096_h16"): (186.442752 + 35.709184 + 249.326592 + 136.108032) * 1e6,
-    ("compose", "gdn_b2_t4096_h16"): (21.011200 + 21.011200) * 1e6,
-    ("chain_bwd", "gdn_b2_t4096_h16"): (215.708160 + 31.632640 + 230.861568 + 115.156992) * 1e6,
-    ("bwd_feat", "gdn_b2_t4096_h16"): (479.928576 + 288.795392) * 1e6,
-    ("bwd_tok", "gdn_b2_t4096_h16"): (644.071168 + 88.860416) * 1e6,
-}
+# Kernel name of the timing hook -> source file of that kernel.
+KERNEL_SOURCES = {"prepare": "k_prep.cu", "chain_fwd": "k_chain.cu", "chain_bwd": "k_chain_bwd.cu",
+                  "bwd_feat": "k_bwd_feat.cu", "bwd_tok": "k_bwd_tok.cu", "compose": "k_scan.cu"}
+# DRAM bytes (read + write) of one step's launches of a kernel from an ncu capture of
+# dram__bytes_read.sum and dram__bytes_write.sum: (kernel, workload) -> (bytes, the first 16
+# hex digits of the SHA-256 of the kernel's source file when captured). Reported only while
+# the source is unchanged; null otherwise.
+NCU_TRAFFIC_BYTES = {}
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
@@ -68,6 +82,28 @@ def max_over_ranks(x: float, device) -> float:
 def job_throughput(units_per_rank: float, world: int, ms: float) -> float:
     """Whole-job throughput: the units all ranks processed over the slowest rank's time."""
     return units_per_rank * world / (ms * 1e-3)
+
+
+def source_hash(kernel: str):
+    name = KERNEL_SOURCES.get(kernel)
+    if name is None:
+        return None
+    path = os.path.join(ROOT, "chunked_gated_delta_05_gb300", "csrc", name)
+    try:
+        with open(path, "rb") as f:
+            return hashlib.sha256(f.read()).hexdigest()[:16]
+    except OSError:
+        return None
+
+
+def ncu_traffic(kernel: str, workload: str):
+    """Per-step DRAM bytes of `kernel` on `workload` from the ncu table, or None when the table
+    has no entry or the kernel's source has changed since the capture."""
+    entry = NCU_TRAFFIC_BYTES.get((kernel, workload))
+    if entry is None:
+        return None
+    nbytes, digest = entry
+    return nbytes if digest == source_hash(kernel) else None
 
 
 def load_peaks():
@@ -107,7 +143,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
-                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.thread = threading.Thread(target=self._read, daemon=True)
             self.thread.start()
         except OSError:
@@ -120,13 +156,13 @@ class ClockSampler:
     def stop(self):
         if self.proc is None:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
-        time.sleep(0.25)
+        time.sleep(0.15)
         self.proc.terminate()
         try:
             self.proc.wait(timeout=5)
         except subprocess.TimeoutExpired:
             self.proc.kill()
-        sm, smax, reasons = [], [], set()
+        sm, smax, power, reasons = [], [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for line in self.lines:
             parts = [p.strip() for p in line.split(",")]
@@ -135,17 +171,19 @@ class ClockSampler:
             try:
                 sm.append(float(parts[1]))
                 smax.append(float(parts[2]))
+                power.append(float(parts[3]))
             except ValueError:
                 continue
             for name, val in zip(names, parts[5:9]):
                 if val.lower() == "active":
                     reasons.add(name)
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
-                "reasons": sorted(reasons), "samples": len(sm)}
+                "sm_mhz_min": min(sm) if sm else None, "power_w_max": max(power) if power else None,
+                "reasons": sorted(reasons), "samples": len(sm), "interval_ms": 100}
 
 
-def oracle_sample_tokens_per_s(w, d, seconds_hint: str):
-    """Time the CPU oracle (fp64 recurrence, forward + backward) on the workload's inputs."""
+def oracle_sample_tokens_per_s(w, d):
+    """Time the CPU oracle (fp64 recurrence, forward + backward) on the given inputs."""
     import oracle
     f = lambda t: None if t is None else t.double().numpy()
     t0 = time.time()
@@ -159,10 +197,11 @@ def oracle_sample_tokens_per_s(w, d, seconds_hint: str):
     return tokens / dt, dt
 
 
-def sample_inputs(w, tokens: int):
+def sample_inputs(w, tokens: int, d=None):
     """The first `tokens` tokens of batch row 0 of workload `w` (same draws, sliced)."""
     from chunked_gated_delta_05_gb300 import synth
-    d = synth.make_inputs(w)
+    if d is None:
+        d = synth.make_inputs(w)
     out = {}
     for key in ("q", "k", "v", "g", "beta", "dO"):
         out[key] = d[key][:1, :tokens].contiguous()
@@ -181,10 +220,10 @@ def run_reference(args, rank):
     sample_tokens = min(w.T, args.reference_tokens)
     d = sample_inputs(w, sample_tokens)
     for _ in range(args.warmup):
-        oracle_sample_tokens_per_s(w, d, "")
+        oracle_sample_tokens_per_s(w, d)
     times = []
     for _ in range(args.steps):
-        _, dt = oracle_sample_tokens_per_s(w, d, "")
+        _, dt = oracle_sample_tokens_per_s(w, d)
         times.append(dt)
     total = sum(times)
     value = sample_tokens * args.steps / total
@@ -198,6 +237,196 @@ def run_reference(args, rank):
             "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle", "sample": sample},
             "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
+
+
+def n_chunk_heads(w, cu):
+    if cu is not None:
+        return sum((cu[i + 1] - cu[i] + 63) // 64 for i in range(len(cu) - 1)) * w.H
+    return w.B * ((w.T + 63) // 64) * w.H
+
+
+class Runner:
+    """One workload on one GPU: device inputs, the training step, and its timers."""
+
+    def __init__(self, w, dev, world, barrier):
+        import torch
+        from chunked_gated_delta_05_gb300 import gdn_bwd, gdn_fwd, kda_bwd, kda_fwd, synth
+        self.torch = torch
+        self.w, self.dev, self.world, self.barrier = w, dev, world, barrier
+        self.host = synth.make_inputs(w)
+        self.d = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in self.host.items()}
+        self.kw = dict(use_qk_l2norm=w.use_qk_l2norm, use_beta_sigmoid=w.beta_logits,
+                       cu_seqlens=self.d["cu_seqlens"])
+        self.fwd_fn, self.bwd_fn = (kda_fwd, kda_bwd) if w.per_channel else (gdn_fwd, gdn_bwd)
+        self.status = torch.zeros(1, dtype=torch.int32, device=dev)
+        self.stream = torch.cuda.current_stream(dev)
+        self.tokens = w.B * w.T
+
+    def step(self, inp):
+        # training step: the forward saves its chunk intermediates, the backward consumes them
+        o, hT, saved = self.fwd_fn(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"], initial_state=inp["h0"],
+                                   output_final_state=True, status=self.status, save=True, **self.kw)
+        grads = self.bwd_fn(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"], inp["dO"], dht=inp["dht"],
+                            initial_state=inp["h0"], status=self.status, saved=saved, **self.kw)
+        return (o, hT) + tuple(grads)
+
+    def check_status(self, where):
+        if int(self.status.item()) != 0:
+            raise RuntimeError(f"device status {int(self.status.item())} {where} ({self.w.name})")
+
+    def warmup(self, n):
+        for _ in range(n):
+            self.step(self.d)
+        self.torch.cuda.synchronize(self.dev)
+        self.check_status("during warm-up")
+
+    def timed_regions(self, steps, min_seconds, run=None):
+        """Repeats of an exactly-`steps`-step region until they span `min_seconds`; returns the
+        per-step time of each repeat (ms, slowest rank)."""
+        torch = self.torch
+        run = run or (lambda n: [self.step(self.d) for _ in range(n)])
+        per_step = []
+        spent = 0.0
+        while not per_step or spent < min_seconds:
+            self.barrier()
+            torch.cuda.synchronize(self.dev)
+            t0 = torch.cuda.Event(enable_timing=True)
+            t1 = torch.cuda.Event(enable_timing=True)
+            t0.record(self.stream)
+            run(steps)
+            t1.record(self.stream)
+            torch.cuda.synchronize(self.dev)
+            self.barrier()
+            ms = max_over_ranks(t0.elapsed_time(t1), self.dev)
+            per_step.append(ms / steps)
+            spent += ms * 1e-3
+            if len(per_step) >= 1000:
+                break
+        return per_step
+
+    def kernel_pass(self, steps):
+        """Per-kernel device times of `steps` steps with the library's timing hook on."""
+        from chunked_gated_delta_05_gb300 import _lib
+        torch = self.torch
+        torch.cuda.synchronize(self.dev)
+        _lib.timing_enable(True)
+        for _ in range(steps):
+            self.step(self.d)
+        torch.cuda.synchronize(self.dev)
+        t = _lib.timing_read()
+        _lib.timing_enable(False)
+        return t
+
+    def e2e(self, steps, min_seconds):
+        """End to end through the public API with host buffers (pinned), every copy inside the
+        timed region: step i's inputs go host -> device on a copy stream while step i-1 computes,
+        and step i's outputs (every gradient, o and the final state) go device -> host on a second
+        copy stream while step i+1 computes. Two input slots; a slot is refilled only after the
+        step that read it has finished. No copy starts before the region's first event."""
+        torch, dev, stream = self.torch, self.dev, self.stream
+        host = self.host
+        pinned_in = {k: (v.pin_memory() if isinstance(v, torch.Tensor) else v) for k, v in host.items()}
+        slots = [{k: (torch.empty_like(v, device=dev) if isinstance(v, torch.Tensor) else v)
+                  for k, v in host.items()} for _ in range(2)]
+        outs_dev = self.step(self.d)
+        pinned_out = [[None if x is None else torch.empty(x.shape, dtype=x.dtype, pin_memory=True)
+                       for x in outs_dev] for _ in range(2)]
+        h2d = sum(v.numel() * v.element_size() for v in pinned_in.values() if isinstance(v, torch.Tensor))
+        d2h = sum(x.numel() * x.element_size() for x in outs_dev if x is not None)
+        s_in = torch.cuda.Stream(dev)
+        s_out = torch.cuda.Stream(dev)
+        slot_free = [torch.cuda.Event(), torch.cuda.Event()]
+        for ev in slot_free:
+            ev.record(stream)
+
+        def run(n):
+            start = torch.cuda.Event()
+            start.record(stream)
+            s_in.wait_event(start)
+            s_out.wait_event(start)
+            last_out = None
+            for i in range(n):
+                sl = i % 2
+                with torch.cuda.stream(s_in):
+                    s_in.wait_event(slot_free[sl])
+                    for k, v in pinned_in.items():
+                        if isinstance(v, torch.Tensor):
+                            slots[sl][k].copy_(v, non_blocking=True)
+                    loaded = torch.cuda.Event()
+                    loaded.record(s_in)
+                stream.wait_event(loaded)
+                outs = self.step(slots[sl])
+                done = torch.cuda.Event()
+                done.record(stream)
+                slot_free[sl] = done
+                with torch.cuda.stream(s_out):
+                    s_out.wait_event(done)
+                    for src, dst in zip(outs, pinned_out[sl]):
+                        if src is not None:
+                            src.record_stream(s_out)
+                            dst.copy_(src, non_blocking=True)
+                    last_out = torch.cuda.Event()
+                    last_out.record(s_out)
+            stream.wait_event(last_out)   # the region ends after the last result is on the host
+
+        run(2)
+        torch.cuda.synchronize(dev)
+        per_step = self.timed_regions(steps, min_seconds, run)
+        self.check_status("during the end-to-end region")
+        ms = statistics.median(per_step)
+        return {"value": job_throughput(self.tokens, self.world, ms), "unit": "tokens/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": ms,
+                "repeats": len(per_step),
+                "copies": "pinned host buffers; inputs of step i+1 and outputs of step i-1 copied on two "
+                          "streams while step i computes"}
+
+
+def roofline_of(runner, per_kernel, steps, peaks, peak_src):
+    """Roofline of the kernel with the largest device time in the kernel pass: algorithmic MMA
+    FLOP per step / that kernel's device time per step, against the sustained bf16 peak (x the
+    nominal tf32/bf16 ratio for tf32 operands)."""
+    w = runner.w
+    nch = n_chunk_heads(w, runner.d["cu_seqlens"])
+    name, (tot_ms, launches) = max(per_kernel.items(), key=lambda kv: kv[1][0])
+    flop_chunk, kind = KERNEL_FLOP_PER_CHUNK_HEAD.get(name, (0, "none"))
+    step_ms = tot_ms / steps
+    achieved = flop_chunk * nch / (step_ms * 1e-3) / 1e12
+    peak = peaks["bf16_tflops_sustained"] * (TF32_OVER_BF16 if kind == "tf32" else 1.0)
+    total = max(1e-9, sum(x[0] for x in per_kernel.values()))
+    traffic = ncu_traffic(name, w.name)
+    return {"bound": "tensor", "kernel": name, "operands": kind, "achieved": achieved, "peak": peak,
+            "unit": "TFLOP/s", "frac": achieved / peak, "traffic": traffic,
+            "traffic_gbs": None if traffic is None else traffic / (step_ms * 1e-3) / 1e9,
+            "traffic_frac_of_hbm": None if traffic is None else traffic / (step_ms * 1e-3) / 1e9 / peaks["hbm_gbs"],
+            "traffic_source": "ncu dram__bytes_read.sum + dram__bytes_write.sum, same kernel source"
+                              if traffic is not None else "no capture of the current kernel source",
+            "peak_source": f"{peak_src} bf16 sustained" + (" x nominal tf32/bf16 ratio" if kind == "tf32" else ""),
+            "algorithmic_flop_per_chunk_head": flop_chunk, "chunk_heads": nch,
+            "avg_launch_ms": tot_ms / max(launches, 1), "launches_per_step": launches / steps,
+            "kernel_ms_per_step": step_ms,
+            "kernel_time_share": {k: round(v[0] / total, 4) for k, v in per_kernel.items() if v[1]},
+            "kernel_ms_per_step_all": {k: round(v[0] / steps, 5) for k, v in per_kernel.items() if v[1]}}
+
+
+def measure_workload(runner, args, peaks, with_e2e=True):
+    w = runner.w
+    runner.warmup(args.warmup)
+    per_step = runner.timed_regions(args.steps, args.min_seconds)
+    runner.check_status("during the timed region")
+    ms = statistics.median(per_step)
+    flop = (FWD_FLOP_PER_TOKEN_HEAD + BWD_FLOP_PER_TOKEN_HEAD) * runner.tokens * w.H
+    tflops_gpu = flop / (ms * 1e-3) / 1e12
+    gate = "kda" if w.per_channel else "gdn"
+    io = (IO_BYTES_PER_TOKEN_HEAD[(gate, "fwd")] + IO_BYTES_PER_TOKEN_HEAD[(gate, "bwd")]) * runner.tokens * w.H
+    out = {"ms_per_step": ms, "tokens_per_s": job_throughput(runner.tokens, runner.world, ms),
+           "tflops": tflops_gpu * runner.world, "pct_of_bf16_peak": tflops_gpu / peaks["bf16_tflops_sustained"],
+           "io_gbs": io / (ms * 1e-3) / 1e9, "pct_of_hbm_io": io / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"],
+           "timing": {"steps_per_region": args.steps, "repeats": len(per_step),
+                      "region_ms_per_step": [round(x, 5) for x in per_step],
+                      "mean_ms_per_step": statistics.fmean(per_step), "min_ms_per_step": min(per_step)}}
+    if with_e2e:
+        out["e2e"] = runner.e2e(args.steps, args.min_seconds)
+    return out
 
 
 def measure_short_conv(w, dev, peaks, iters=10):
@@ -239,31 +468,48 @@ def measure_short_conv(w, dev, peaks, iters=10):
     return {"shape": {"rows": w.B * w.T, "channels": C, "taps": Wt, "activation": "silu"}, "bound": "hbm", **out}
 
 
-def measure_forward_target(dev, peaks, iters=10):
+def measure_forward_target(dev, peaks, iters=20):
     """Forward alone (inference: no saves) at T = 8192, H = 16, the shape of the forward
-    target: chunked-form FLOP / device time of the forward's kernels, against the bf16 peak.
-    Inputs larger than L2 (67 MB of q/k/v plus the workspace tiles) are rewritten each call."""
+    target: chunked-form FLOP / wall time of the whole call (CUDA events around each call, so
+    launch gaps and the wrapper's host work count), against the bf16 burst peak. Two input sets
+    (q, k, v, g, beta: 2 x 100 MB, together larger than L2) alternate between calls."""
     import torch
     from chunked_gated_delta_05_gb300 import _lib, gdn_fwd, synth
     w = synth.WORKLOADS["gdn_b1_t8192_h16"]
-    d = synth.make_inputs(w)
-    dc = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in d.items()}
-    fwd = lambda: gdn_fwd(dc["q"], dc["k"], dc["v"], dc["g"], dc["beta"], output_final_state=True)
-    for _ in range(3):
-        fwd()
+    sets = []
+    for seed in (w.seed, w.seed + 100):
+        d = synth.make_inputs(w, seed=seed)
+        sets.append({k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in d.items()})
+    fwd = lambda d: gdn_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], output_final_state=True)
+    stream = torch.cuda.current_stream(dev)
+    for i in range(4):
+        fwd(sets[i % 2])
     torch.cuda.synchronize(dev)
+    times = []
+    for i in range(iters):
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        fwd(sets[i % 2])
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        times.append(e0.elapsed_time(e1))
+    ms = statistics.median(times)
     _lib.timing_enable(True)
-    for _ in range(iters):
-        fwd()
+    for i in range(iters):
+        fwd(sets[i % 2])
     torch.cuda.synchronize(dev)
     t = _lib.timing_read()
     _lib.timing_enable(False)
-    ms = sum(v[0] for v in t.values()) / iters
     flop = FWD_FLOP_PER_TOKEN_HEAD * w.B * w.T * w.H
     tflops = flop / (ms * 1e-3) / 1e12
+    io = IO_BYTES_PER_TOKEN_HEAD[("gdn", "fwd")] * w.B * w.T * w.H
     return {"workload": w.name, "ms": ms, "tflops": tflops, "pct_of_bf16_peak": tflops / peaks["bf16_tflops"],
-            "peak_kind": "bf16 burst", "kernels_ms": {k: v[0] / iters for k, v in t.items() if v[1]},
-            "timing": "CUDA events around the forward's kernels"}
+            "peak_kind": "bf16 burst (measured)", "io_gbs": io / (ms * 1e-3) / 1e9,
+            "pct_of_hbm_io": io / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"],
+            "kernels_ms": {k: v[0] / iters for k, v in t.items() if v[1]},
+            "timing": "median of CUDA-event times around each whole call; kernels_ms from a separate pass "
+                      "with the library's timing hook"}
 
 
 def main():
@@ -273,8 +519,11 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--min-seconds", type=float, default=1.0,
+                    help="repeat the K-step timed region until the repeats span this long")
     ap.add_argument("--reference-tokens", type=int, default=256)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extras", action="store_true", help="headline workload only")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     rank = int(os.environ.get("RANK", "0"))
@@ -286,7 +535,7 @@ def main():
 
     import torch
     import torch.distributed as dist
-    from chunked_gated_delta_05_gb300 import _lib, gdn_bwd, gdn_fwd, synth
+    from chunked_gated_delta_05_gb300 import synth
 
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
@@ -297,163 +546,56 @@ def main():
         if world > 1:
             dist.barrier()
 
-    w = synth.WORKLOADS[args.workload]
-    host = synth.make_inputs(w)
-    d = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in host.items()}
-    kw = dict(use_qk_l2norm=w.use_qk_l2norm, use_beta_sigmoid=w.beta_logits, cu_seqlens=d["cu_seqlens"])
-    fwd_fn, bwd_fn = gdn_fwd, gdn_bwd
-    if w.per_channel:
-        from chunked_gated_delta_05_gb300 import kda_bwd, kda_fwd
-        fwd_fn, bwd_fn = kda_fwd, kda_bwd
-    status = torch.zeros(1, dtype=torch.int32, device=dev)
-
-    def step(inp):
-        # training step: the forward saves its chunk intermediates, the backward consumes them
-        o, hT, saved = fwd_fn(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"], initial_state=inp["h0"],
-                              output_final_state=True, status=status, save=True, **kw)
-        grads = bwd_fn(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"], inp["dO"], dht=inp["dht"],
-                       initial_state=inp["h0"], status=status, saved=saved, **kw)
-        return (o, hT) + tuple(grads)
-
-    for _ in range(args.warmup):
-        step(d)
-    torch.cuda.synchronize(dev)
-    if int(status.item()) != 0:
-        raise RuntimeError(f"device status {int(status.item())} during warm-up")
-
-    stream = torch.cuda.current_stream(dev)
-    _lib.timing_enable(True)
-    sampler = ClockSampler(local_rank)
-    barrier()
-    torch.cuda.synchronize(dev)
-    sampler.start()
-    t0 = torch.cuda.Event(enable_timing=True)
-    t1 = torch.cuda.Event(enable_timing=True)
-    t0.record(stream)
-    for _ in range(args.steps):
-        step(d)
-    t1.record(stream)
-    torch.cuda.synchronize(dev)
-    barrier()
-    clocks = sampler.stop()
-    ms = t0.elapsed_time(t1) / args.steps
-    per_kernel = _lib.timing_read()
-    _lib.timing_enable(False)
-    ms = max_over_ranks(ms, dev)
-
-    tokens = w.B * w.T
-    value = job_throughput(tokens, world, ms)
-    flop = (FWD_FLOP_PER_TOKEN_HEAD + BWD_FLOP_PER_TOKEN_HEAD) * tokens * w.H
-    tflops = flop * world / (ms * 1e-3) / 1e12
     peaks, peak_src = load_peaks()
-    bf16_sus = peaks["bf16_tflops_sustained"]
-
-    # roofline of the dominant kernel (largest device time in the timed region)
-    n_chunk_heads = sum((min(64, w.T - 64 * j) > 0) for j in range((w.T + 63) // 64)) * w.B * w.H
-    if d["cu_seqlens"] is not None:
-        cu = d["cu_seqlens"]
-        n_chunk_heads = sum((cu[i + 1] - cu[i] + 63) // 64 for i in range(len(cu) - 1)) * w.H
-    name, (tot_ms, launches) = max(per_kernel.items(), key=lambda kv: kv[1][0])
-    flop_chunk, kind = KERNEL_FLOP_PER_CHUNK_HEAD[name]
-    avg_ms = tot_ms / max(launches, 1)
-    # the kernel's device time per step (the chains launch twice per step when segmented)
-    step_ms = tot_ms / args.steps
-    achieved = flop_chunk * n_chunk_heads / (step_ms * 1e-3) / 1e12
-    peak = bf16_sus * (TF32_OVER_BF16 if kind == "tf32" else 1.0)
-    kernel_share = {k: round(v[0] / max(1e-9, sum(x[0] for x in per_kernel.values())), 4) for k, v in per_kernel.items()}
-    traffic = NCU_TRAFFIC_BYTES.get((name, w.name))
-    roofline = {"bound": "tensor", "kernel": name, "operands": kind, "achieved": achieved, "peak": peak,
-                "unit": "TFLOP/s", "frac": achieved / peak, "traffic": traffic,
-                "traffic_gbs": None if traffic is None else traffic / (step_ms * 1e-3) / 1e9,
-                "traffic_frac_of_hbm": None if traffic is None else traffic / (step_ms * 1e-3) / 1e9 / peaks["hbm_gbs"],
-                "peak_source": f"{peak_src} bf16 sustained" + (" x nominal tf32/bf16 ratio" if kind == "tf32" else ""),
-                "avg_launch_ms": avg_ms, "launches_per_step": launches / args.steps, "kernel_ms_per_step": step_ms,
-                "kernel_time_share": kernel_share}
+    w = synth.WORKLOADS[args.workload]
+    runner = Runner(w, dev, world, barrier)
+    sampler = ClockSampler(local_rank)
+    runner.warmup(args.warmup)
+    sampler.start()
+    head = measure_workload(runner, args, peaks, with_e2e=False)
+    clocks = sampler.stop()
+    head_e2e = runner.e2e(args.steps, args.min_seconds)
+    per_kernel = runner.kernel_pass(args.steps)
+    roofline = roofline_of(runner, per_kernel, args.steps, peaks, peak_src)
     gpu_launches = sum(v[1] for v in per_kernel.values())
+    ms = head["ms_per_step"]
+    if clocks.get("sm_mhz"):
+        clocks["ms_x_median_sm_mhz"] = ms * clocks["sm_mhz"]
 
-    # End to end through the public API with host buffers (pinned), every copy inside the timed
-    # region: step i's inputs go host -> device on a copy stream while step i-1 computes, and
-    # step i's outputs (every gradient, o and the final state) go device -> host on a second copy
-    # stream while step i+1 computes. Two input slots; a slot is refilled only after the step
-    # that read it has finished.
-    pinned_in = {k: (v.pin_memory() if isinstance(v, torch.Tensor) else v) for k, v in host.items()}
-    slots = [{k: (torch.empty_like(v, device=dev) if isinstance(v, torch.Tensor) else v) for k, v in host.items()}
-             for _ in range(2)]
-    outs_dev = step(d)
-    pinned_out = [[None if x is None else torch.empty(x.shape, dtype=x.dtype, pin_memory=True) for x in outs_dev]
-                  for _ in range(2)]
-    h2d = sum(v.numel() * v.element_size() for v in pinned_in.values() if isinstance(v, torch.Tensor))
-    d2h = sum(x.numel() * x.element_size() for x in outs_dev if x is not None)
-    s_in = torch.cuda.Stream(dev)
-    s_out = torch.cuda.Stream(dev)
-    slot_free = [torch.cuda.Event(), torch.cuda.Event()]
-    for ev in slot_free:
-        ev.record(stream)
-
-    def e2e_run(n):
-        # no copy starts before this point of the compute stream (the timed region's start)
-        start = torch.cuda.Event()
-        start.record(stream)
-        s_in.wait_event(start)
-        s_out.wait_event(start)
-        last_out = None
-        for i in range(n):
-            sl = i % 2
-            with torch.cuda.stream(s_in):
-                s_in.wait_event(slot_free[sl])
-                for k, v in pinned_in.items():
-                    if isinstance(v, torch.Tensor):
-                        slots[sl][k].copy_(v, non_blocking=True)
-                loaded = torch.cuda.Event()
-                loaded.record(s_in)
-            stream.wait_event(loaded)
-            outs = step(slots[sl])
-            done = torch.cuda.Event()
-            done.record(stream)
-            slot_free[sl] = done
-            with torch.cuda.stream(s_out):
-                s_out.wait_event(done)
-                for src, dst in zip(outs, pinned_out[sl]):
-                    if src is not None:
-                        src.record_stream(s_out)
-                        dst.copy_(src, non_blocking=True)
-                last_out = torch.cuda.Event()
-                last_out.record(s_out)
-        stream.wait_event(last_out)   # the timed region ends after the last result is on the host
-
-    e2e_run(2)
-    torch.cuda.synchronize(dev)
-    barrier()
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    e2e_run(args.steps)
-    e1.record(stream)
-    torch.cuda.synchronize(dev)
-    e_ms = e0.elapsed_time(e1) / args.steps
-    e_ms = max_over_ranks(e_ms, dev)
-    if int(status.item()) != 0:
-        raise RuntimeError(f"device status {int(status.item())} during the timed region")
-
-    line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
-            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "bf16 io, bf16/tf32 mma, fp32 accumulate", "data": "synthetic",
+    line = {"metric": METRIC, "value": head["tokens_per_s"], "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16 io, bf16/tf32 mma, fp32 accumulate",
+            "data": "synthetic",
             "config": {"workload": w.name, "B": w.B, "T": w.T, "H": w.H, "Hk": w.num_k_heads or w.H, "K": w.K,
-                       "V": w.V, "chunk": 64,
-                       "gate": "per-channel" if w.per_channel else "scalar", "l2norm": w.use_qk_l2norm,
-                       "parallelism": f"replicas x{world}",
-                       "l2": "per-step working set (67 MB inputs + ~1 GB workspace) exceeds the 129 MB L2"},
-            "tflops": tflops, "pct_of_bf16_peak": tflops / bf16_sus,
+                       "V": w.V, "chunk": 64, "gate": "per-channel" if w.per_channel else "scalar",
+                       "l2norm": w.use_qk_l2norm, "parallelism": f"replicas x{world}",
+                       "l2": "inputs larger than L2 (q/k/v/dO alone exceed the 129 MB L2), no flush",
+                       "timing": "median over repeats of an exactly-K-step region (>= "
+                                 f"{args.min_seconds:g} s of repeats); timing hook off"},
+            "tflops": head["tflops"], "pct_of_bf16_peak": head["pct_of_bf16_peak"],
+            "pct_of_hbm_io": head["pct_of_hbm_io"], "timing": head["timing"],
             "roofline": roofline, "clocks": clocks, "gpu_launches": gpu_launches,
-            "e2e": {"value": job_throughput(tokens, world, e_ms), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
-                    "d2h_bytes_per_step": d2h, "ms_per_step": e_ms,
-                    "copies": "pinned host buffers; inputs of step i+1 and outputs of step i-1 copied on two "
-                              "streams while step i computes"}}
-    if rank == 0:
-        line["next_rows"] = {"short_conv": measure_short_conv(w, dev, peaks)}
+            "gpu_launches_note": "library kernel launches in one K-step region (counted by the timing hook "
+                                 "in a separate pass of K steps)",
+            "e2e": head_e2e}
+    del runner
+    torch.cuda.empty_cache()
+    if not args.no_extras:
+        # every rank runs the secondary workloads (their regions are bracketed by barriers)
+        works = {}
+        for name in SECONDARY_WORKLOADS:
+            if name == w.name:
+                continue
+            r = Runner(synth.WORKLOADS[name], dev, world, barrier)
+            works[name] = measure_workload(r, args, peaks)
+            del r
+            torch.cuda.empty_cache()
+        line["workloads"] = works
+    if rank == 0 and not args.no_extras:
+        line["next_rows"] = {"short_conv": measure_short_conv(synth.WORKLOADS["gdn_b2_t4096_h16"], dev, peaks)}
         line["forward_target"] = measure_forward_target(dev, peaks)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        cpu_tps, dt = oracle_sample_tokens_per_s(w, host, "")
+        cpu_tps, dt = oracle_sample_tokens_per_s(w, synth.make_inputs(w))
         line["cpu_baseline"] = {"value": cpu_tps, "unit": "tokens/s", "cores": os.cpu_count(), "kind": "oracle",
                                 "sample": f"the full {w.name} batch once (fwd+bwd), {dt:.1f} s wall"}
     if rank == 0:

@@ -110,12 +110,12 @@ int validate_desc(const gdn_desc_t* d, Problem* P) {
 // Segment length (in chunks) forced by gdn_set_chain_segment(); 0 = chosen by plan_scan().
 int g_chain_segment = 0;
 
-// Wave model of the chain scan on a GB300 (152 SMs, one chain CTA per SM): pass 0 runs
+// Wave model of the chain scan (one chain CTA per SM, waves of sm_count() CTAs): pass 0 runs
 // 1 + 2 (ns - 2) CTAs per (sequence, head), pass 1 runs ns - 1, each for about L chunk steps;
 // the compose kernel walks ns - 2 segments. The step costs are GB300 measurements (a chain
 // step averaged over the forward and reverse chains and over full and map runs under a full
 // wave of CTAs; one compose step).
-constexpr int kWaveSMs = 152;
+int sm_count();
 constexpr double kChunkStepUs = 4.25, kComposeStepUs = 6.0, kLaunchUs = 3.0;
 constexpr int kMaxSegments = 64;
 
@@ -153,6 +153,7 @@ ScanPlan plan_scan(const Problem& P) {
     return best;
   }
   double best_t = 1e300;
+  const int sms = sm_count();
   for (int S = 1; S <= std::min(maxNC, kMaxSegments); ++S) {
     const int L = (maxNC + S - 1) / S;
     long long runs0 = 0, runs1 = 0;
@@ -163,7 +164,7 @@ ScanPlan plan_scan(const Problem& P) {
       runs0 += (long long)e.second * (ns <= 2 ? 1 : 2 * ns - 3);
       runs1 += (long long)e.second * (ns - 1);
     }
-    auto waves = [&](long long r) { return double((r * P.H + kWaveSMs - 1) / kWaveSMs); };
+    auto waves = [&](long long r) { return double((r * P.H + sms - 1) / sms); };
     double t = waves(runs0) * L * kChunkStepUs;
     if (maxS >= 2) t += waves(runs1) * L * kChunkStepUs + kLaunchUs;
     if (maxS >= 3) t += (maxS - 2) * kComposeStepUs + kLaunchUs;
@@ -657,6 +658,7 @@ int run_bwd(const gdn_desc_t* d, const gdn_bwd_args_t* a, void* stream, bool kda
   tp.dv = static_cast<__nv_bfloat16*>(a->dv);
   tp.dbeta = static_cast<__nv_bfloat16*>(a->dbeta);
   tp.dg = a->dg;
+  tp.g = a->g;
   tp.status = a->status;
   tp.kda = kda ? 1 : 0;
   tp.sms = fp.sms;
@@ -680,6 +682,7 @@ int run_bwd(const gdn_desc_t* d, const gdn_bwd_args_t* a, void* stream, bool kda
   gp.R = P.R;
   gp.H = P.H;
   gp.G = P.G;
+  gp.sms = fp.sms;
   TimedLaunch tl_(kKGroupSum, s);
   return check_cuda(launch_group_sum(gp, s), "group sum kernel");
 }
@@ -718,6 +721,7 @@ const char* gdn_strerror(int code) {
     case GDN_EUNSUPPORTED: return "unsupported device or feature";
     case GDN_ECUDA: return "CUDA runtime error";
     case GDN_ETIMEOUT: return "bounded device wait expired";
+    case GDN_ERANGE: return "per-channel gate outside the supported range";
     default: return "unknown error";
   }
 }

@@ -13,6 +13,18 @@ constexpr int kC = 64;     // chunk length (tokens)
 constexpr int kD = 128;    // head dim K == V
 constexpr int kMaxUploadInts = 4000;  // cu_seqlens entries per upload launch
 constexpr float kLog2e = 1.4426950408889634f;  // log2(e): exp(x) = exp2(x log2(e))
+// Floor on the scalar per-token log-decay g of Gated DeltaNet. exp(-128) is below the smallest
+// fp32 subnormal after the log2 scaling (2^-184.7), so every decay factor that spans a floored
+// token is exactly 0 in fp32, which is what exp(g) gives for g = -inf (a hard state reset).
+// Flooring keeps the chunk-local cumulative gate finite, so differences G_i - G_j of two
+// positions after a reset stay exact sums instead of (-inf) - (-inf).
+constexpr float kGateFloor = -128.f;
+// Largest drop of a per-channel cumulative gate (natural log) within one 16-token block that
+// the per-channel prepare kernel accepts: its block factorisation splits exp(G_i - G_j) into
+// exp(G_i - G_r) exp(G_r - G_j) around the block's first row r, and both factors stay normal
+// fp32 numbers while the drop is at most 80 (exp(-80) = 1.8e-35). Gates in the pages'
+// safe-gate range [-5, 0] drop at most 75 over 15 tokens.
+constexpr float kKdaBlockDropMax = 80.f;
 
 // One chunk of one sequence: {first token row (flattened B*T), valid rows (1..64),
 // sequence index, chunk index within the sequence}.
@@ -165,6 +177,7 @@ struct BwdTokParams {
   const float *gam, *dgam;     // [NC,H,128]
   __nv_bfloat16 *dq, *dk, *dv, *dbeta;
   float* dg;
+  const float* g;              // the raw gate as passed ([R,H]; GDN's floor test)
   int qk_group;                // value heads per q/k head
   float *dq32, *dk32;          // qk_group > 1: per-value-head dq, dk [R,H,K] fp32 (summed later)
   int sms;                     // SM count (the distance to the next wave's CTA for prefetching)
@@ -212,6 +225,7 @@ struct GroupSumParams {
   __nv_bfloat16 *dq, *dk;      // [R,H/G,K]
   long long R;
   int H, G;
+  int sms;                     // SM count of the device (grid size)
 };
 
 struct ComposeParams {

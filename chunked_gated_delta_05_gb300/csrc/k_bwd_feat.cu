@@ -22,20 +22,6 @@
 
 namespace gdn {
 
-#ifdef GDN_TRACE
-__device__ unsigned long long g_trace_feat[4 * 16];
-#define FTRACE(slot)                                                                                    \
-  do {                                                                                                  \
-    if (blockIdx.y == 3 && threadIdx.x == 0 && blockIdx.x % 32 == 5 && blockIdx.x < 128)                \
-      g_trace_feat[(blockIdx.x / 32) * 16 + (slot)] = globaltimer();                                     \
-  } while (0)
-extern "C" int gdn_trace_feat_read(unsigned long long* host) {
-  return cudaMemcpyFromSymbol(host, g_trace_feat, sizeof(g_trace_feat)) == cudaSuccess ? 0 : -1;
-}
-#else
-#define FTRACE(slot) do {} while (0)
-#endif
-
 namespace {
 
 constexpr int kThreads = 256;
@@ -73,7 +59,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int c = blockIdx.x, h = blockIdx.y, H = p.H;
   const size_t tile = size_t(c) * H + h;
   const int f = tid & 127, hf = tid >> 7;  // feature (TMEM lane) and column half
-  FTRACE(0);
   const ChunkEntry ch = p.chunks[c];  // requested first: the dO load below waits on it
 
   if (warp == 0) tmem_alloc(&tslot, 512);
@@ -99,7 +84,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tb = tslot;
   const uint32_t tl = tb + tmem_lane_base(warp);
-  FTRACE(1);
   // Half hf of the h and dh' rows f (shared memory -> TMEM as tf32 A operands); dgam partial
   // sums in fp32. The rows are already tf32 values (the chains save their tf32 copies).
   const bool tma_ok = mbar_wait(&bar_tma, 0, &abort_flag, p.status, kDevTimeoutTma);
@@ -134,7 +118,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int pp = 0; pp < 4; ++pp)
       tma_load_2d(sm + kOffVN + pp * 8192, &mVN, pp * 32, int(tile) * kC, &bar_tma2);
   }
-  FTRACE(2);
   // A^T operand: element (j, i) = A[i][j]; four threads split the 64 rows i of column j = tid % 64.
   {
     const int j = tid & 63, i0 = (tid >> 6) * 16;
@@ -145,7 +128,6 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
     for (int e = 0; e < 16; ++e) *reinterpret_cast<float*>(sm + kOffAT + sw128_offset(j, i0 + e, kC, 4)) = to_tf32(buf[e]);
   }
-  FTRACE(3);
   // dO^T operand: element (t, v=f) of the K-major [t][v] tile from the bf16 TMA tile (half hf
   // of the tokens); rows past the chunk (the next document's, or out of range) are zero.
   if (tma_ok) {
@@ -162,7 +144,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  FTRACE(4);
 
   if (tid == 0) {
     if (tma_ok) {
@@ -191,7 +172,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   __syncwarp();
   const bool ok = mbar_wait(&bar_mma, 0, &abort_flag, p.status, kDevTimeoutMma);
-  FTRACE(5);
   tc_fence_after();
   if (ok) {
     // this thread's tokens t = t0 + e of the 64-token columns
@@ -238,9 +218,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mma_commit(&bar_mma);
   }
   __syncwarp();
-  FTRACE(6);
   const bool ok2 = ok && mbar_wait(&bar_mma, 1, &abort_flag, p.status, kDevTimeoutMma);
-  FTRACE(7);
   tc_fence_after();
   if (ok2) {
     const int t0 = 32 * hf;
@@ -256,7 +234,6 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
     for (int e = 0; e < 32; ++e) v1[size_t(e) * kD] = r[e];
   }
-  FTRACE(8);
   // dgam: per key row (KDA: the two column halves of row f) or summed over the block (GDN).
   if (p.kda) {
     s_dg[tid] = dg;

@@ -29,20 +29,6 @@
 
 namespace gdn {
 
-#ifdef GDN_TRACE
-__device__ unsigned long long g_trace_tok[4 * 16];
-#define TTRACE(slot)                                                                                    \
-  do {                                                                                                  \
-    if (blockIdx.y == 3 && threadIdx.x == 0 && blockIdx.x % 32 == 5 && blockIdx.x < 128)                \
-      g_trace_tok[(blockIdx.x / 32) * 16 + (slot)] = globaltimer();                                      \
-  } while (0)
-extern "C" int gdn_trace_tok_read(unsigned long long* host) {
-  return cudaMemcpyFromSymbol(host, g_trace_tok, sizeof(g_trace_tok)) == cudaSuccess ? 0 : -1;
-}
-#else
-#define TTRACE(slot) do {} while (0)
-#endif
-
 namespace {
 
 constexpr int kThreads = 256;   // 8 warps; two threads per TMEM lane (halves of the columns)
@@ -103,7 +89,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* sK = sm + kOffK;
   uint8_t* sV = sm + kOffV;
 
-  TTRACE(0);
   if (warp == 0) tmem_alloc(&tslot, 256);
   if (tid == 0) {
     // The barriers are this thread's alone until the block barrier below, so the loads start
@@ -155,9 +140,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tb = tslot;
   const uint32_t tl = tb + tmem_lane_base(warp);
   const float Glast = s_G[len - 1];
-  TTRACE(1);
   const bool tma_ok = mbar_wait(&bar_tma, 0, &abort_flag, p.status, kDevTimeoutTma);
-  TTRACE(2);
   // dO as a 64-row tf32 operand [i][v] (rows past the chunk are zero).
   {
     const int v = tid & 127, t0 = 32 * half;
@@ -192,7 +175,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   __syncwarp();
   bool ok = tma_ok && mbar_wait(&bar_mma, 0, &abort_flag, p.status, kDevTimeoutMma);
-  TTRACE(3);
   tc_fence_after();
   // ---- K1 = diag(beta exp(G) r_k) k and V1 = diag(beta) v as 64-row operands [j][d]
   // (a warp converts one row per step: lane l takes columns 4l..4l+3, one 16-byte chunk)
@@ -212,7 +194,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  TTRACE(4);
   // ---- product 2: dA = [dW | dU] [K1 | V1]^T  (K = 256)
   if (tid == 0 && ok) ok = mbar_wait(&bar_tma2, 0, &abort_flag, p.status, kDevTimeoutTma);
   if (tid == 0 && ok) {
@@ -224,7 +205,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   __syncwarp();
   ok = ok && mbar_wait(&bar_mma, 1, &abort_flag, p.status, kDevTimeoutMma);
-  TTRACE(5);
   tc_fence_after();
   // ---- dL = -A^T dA A^T: X = A^T dA, then X A^T.
   // Operands (64x64 tf32, 16 KB each): AT [j][i] (A op), dAT [m][i] (B op), A [l][m] (B op), X.
@@ -289,7 +269,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   ok = ok && mbar_wait(&bar_mma, 1, &abort_flag, p.status, kDevTimeoutMma);
   tc_fence_after();
 
-  TTRACE(6);
   // ---- elementwise on token pairs: row owner i holds row i of dL', dAqk, KK, QK.
   // A operands for the last products: E1 [i][j], E2^T [j][i], Nq [i][j], Nk^T [j][i];
   // B operands: k^T [d][j], q^T [d][i] (raw tiles, tf32).
@@ -318,7 +297,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_wait_ld_regs(nn);
       tmem_wait_ld_regs(kk);
       tmem_wait_ld_regs(qk);
-      TTRACE(11);
 #pragma unroll
       for (int jj = 0; jj < 16; ++jj) {
         const int j = jb + 2 * jj;
@@ -347,7 +325,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       atomicAdd(&s_dG[i], rowP);
       atomicAdd(&s_db[i], dbi);
     }
-    TTRACE(12);
   }
   // transposed raw tiles k^T [d][j], q^T [d][i] (zero past the chunk: cleared above)
   // (thread: row d, four consecutive token columns per step, one 16-byte chunk)
@@ -361,12 +338,10 @@ __global__ void __launch_bounds__(kThreads, 1)
               to_tf32(bf16_at(sQ, j + 2, d)), to_tf32(bf16_at(sQ, j + 3, d)));
     }
   }
-  TTRACE(13);
   fence_async_smem();
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  TTRACE(7);
   // column sums of P
   if (tid < kC) {
     float col = 0.f;
@@ -387,7 +362,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   ok = ok && mbar_wait(&bar_mma, 0, &abort_flag, p.status, kDevTimeoutMma);
   tc_fence_after();
 
-  TTRACE(8);
   // ---- per-token assembly. Owner threads stage their rows of the two last products from
   // TMEM into padded shared rows; then each warp takes whole token rows (lane l: columns
   // 4l..4l+3) with coalesced float4 loads of the fp32 intermediates and shuffle-reduced dots.
@@ -412,7 +386,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
   __syncthreads();
-  TTRACE(14);
   if (ok) {
     // eight lanes per token row (lane l8 of the group: features 32 m + 4 l8 + e, m, e < 4, so
     // the group's loads and stores of one m are 128 contiguous bytes), four rows per warp at a
@@ -558,7 +531,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
   __syncthreads();
-  TTRACE(9);
   if (warp == 0 && ok) {
     // gate: G_last collects the end-decay terms; the reverse cumulative sum gives dg. Lane l
     // holds rows 2 l and 2 l + 1; a suffix scan over the lanes replaces the serial loop.
@@ -582,14 +554,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   if (tid < len && ok) {
     const size_t o = size_t(ch.x + tid) * H + h;
-    p.dg[o] = s_dG[tid];
+    // a gate below the floor was clamped in the forward: its gradient is 0
+    p.dg[o] = p.g[o] < kGateFloor ? 0.f : s_dG[tid];
     float db = s_db[tid];
     if (p.beta_sigmoid) db *= s_b[tid] * (1.f - s_b[tid]);
     p.dbeta[o] = __float2bfloat16_rn(db);
   }
   tc_fence_before();
   __syncthreads();
-  TTRACE(10);
   if (warp == 0) tmem_dealloc(tb, 256);
 }
 

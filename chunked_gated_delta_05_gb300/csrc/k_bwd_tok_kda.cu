@@ -27,20 +27,6 @@
 
 namespace gdn {
 
-#ifdef GDN_TRACE
-__device__ unsigned long long g_trace_tkda[4 * 16];
-#define BTRACE(slot)                                                                                    \
-  do {                                                                                                  \
-    if (blockIdx.y == 3 && threadIdx.x == 0 && blockIdx.x % 16 == 5 && blockIdx.x < 64)                 \
-      g_trace_tkda[(blockIdx.x / 16) * 16 + (slot)] = globaltimer();                                     \
-  } while (0)
-extern "C" int gdn_trace_tkda_read(unsigned long long* host) {
-  return cudaMemcpyFromSymbol(host, g_trace_tkda, sizeof(g_trace_tkda)) == cudaSuccess ? 0 : -1;
-}
-#else
-#define BTRACE(slot) do {} while (0)
-#endif
-
 namespace {
 
 constexpr int kThreads = 256;
@@ -212,7 +198,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int cc = tid & 127;   // channel handled in the CUDA-core phases
   const float dgam_c = p.dgam[tile * kD + cc];  // requested now, used by the last phase
 
-  BTRACE(0);
   if (warp == 0) tmem_alloc(&tslot, 256);
   if (tid == 0) {
     abort_flag = 0;
@@ -268,7 +253,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   fence_async_smem();
   __syncthreads();
   const bool tma_ok = mbar_wait(&bar_tma, 0, &abort_flag, p.status, kDevTimeoutTma);
-  BTRACE(1);
   if (tid >= len && tid < kC) {
     for (int c16 = 0; c16 < 16; ++c16) {
       const uint32_t off = sw128_offset(tid, c16 * 8, kC, 2);
@@ -290,7 +274,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   __syncwarp();
   bool ok = tma_ok && mbar_wait(&bar_mma, 0, &abort_flag, p.status, kDevTimeoutMma);
-  BTRACE(2);
   tc_fence_after();
   // ---- K1 = beta r_k exp(G) (.) k and V1 = beta v as 64-row operands [j][c]
   for (int j = 32 * half; j < 32 * half + 32; ++j) {
@@ -314,7 +297,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   ok = ok && mbar_wait(&bar_mma, 1, &abort_flag, p.status, kDevTimeoutMma);
   tc_fence_after();
   // ---- dL = -A^T dA A^T
-  BTRACE(3);
   uint8_t* sAT = sm + kR3;
   uint8_t* sdAT = sm + kR3 + 16384;
   uint8_t* sA = sm + kR4;
@@ -399,7 +381,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   tc_fence_before();
   __syncthreads();
-  BTRACE(4);
   // ---- decayed pair sums on CUDA cores: thread (channel cc, row blocks 2 half and 2 half + 1,
   // which balances the two halves' work). Rows past the chunk come out zero.
   float* sKacc = reinterpret_cast<float*>(sm + kR2);           // dk^ accumulator [64][128]
@@ -409,7 +390,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   for (int b = 0; b < 2; ++b)
     kda_pair_block(2 * half + b, sG2, sK, sQ, s_rk, s_rq, s_b, sD, sN, sKacc, sQacc, sGacc, s_db, cc, lane);
   __syncthreads();
-  BTRACE(5);
   // ---- per-token assembly (thread: channel cc, rows of parity `half`)
   float glast_part = 0.f;
   const float glc = sG2[(len - 1) * kP + cc];
@@ -474,7 +454,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   s_glast[half][cc] = glast_part;
   __syncthreads();
-  BTRACE(6);
   // ---- L2-norm backward and writes; dg by reverse cumulative sum per channel
   for (int t = half; t < len; t += 2) {
     const float rq = s_rq[t], rk = s_rk[t];
@@ -505,7 +484,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   tc_fence_before();
   __syncthreads();
-  BTRACE(7);
   if (warp == 0) tmem_dealloc(tb, 256);
 }
 

@@ -30,23 +30,6 @@
 
 namespace gdn {
 
-#ifdef GDN_TRACE
-// Optional timeline of the first CTA (compiled only with -DGDN_TRACE; never in the library).
-__device__ unsigned long long g_trace[64 * 16];
-__device__ int g_trace_block = 0;
-extern "C" int g_trace_set_block(int b) {
-  return cudaMemcpyToSymbol(g_trace_block, &b, sizeof(int)) == cudaSuccess ? 0 : -1;
-}
-#define TRACE(j, slot)                                                                           \
-  do {                                                                                           \
-    if (blockIdx.x == g_trace_block && blockIdx.y == 0 && (j) < 64) g_trace[(j) * 16 + (slot)] = globaltimer(); \
-  } while (0)
-#else
-#define TRACE(j, slot) \
-  do {                 \
-  } while (0)
-#endif
-
 namespace {
 
 constexpr int kChainThreads = 256;            // 8 warps: lane v = tid % 128, half = tid / 128
@@ -195,21 +178,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int c = first + j, st = j & 1;
         const uint32_t tPV = tb + tpv(j), tO = tb + tout(j);
         const uint32_t sKtT = smem_u32(sm + kOffG3 + st * kG3Stage), sAqk = sKtT + 32768;
-        TRACE(j, 0);
         if (!mbar_wait(&full1, par, &abort_flag, p.status, kDevTimeoutTma)) break;
         if (!mbar_wait(&sready, par, &abort_flag, p.status, kDevTimeoutSync)) break;
-        TRACE(j, 1);
         tc_fence_after();
         for (int s = 0; s < 16; ++s) mma_tf32_ts(tPV, tb + kTST + s * 8, desc_kmajor(sWQ, 16384, s), id_first, s > 0);
         mma_commit(&mma1);
         if (!mbar_wait(&mma1, par, &abort_flag, p.status, kDevTimeoutMma)) break;
-        TRACE(j, 2);
         if (j + 1 < nc) load_g1(c + 1);
         if (!mbar_wait(&vready, par, &abort_flag, p.status, kDevTimeoutSync)) break;
-        TRACE(j, 3);
         if (j + 1 < nc && use_u) load_g2(c + 1);
         if (!mbar_wait(&full3[st], (j >> 1) & 1, &abort_flag, p.status, kDevTimeoutTma)) break;
-        TRACE(j, 4);
         tc_fence_after();
         for (int s = 0; s < 8; ++s) mma_tf32_ts(tb + kTSM, tPV + s * 8, desc_kmajor(sKtT, 16384, s), id128, true);
         mma_commit(&mma2);
@@ -217,7 +195,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int s = 0; s < 8; ++s) mma_tf32_ts(tO, tPV + s * 8, desc_kmajor(sAqk, 8192, s), id64, true);
         mma_commit(&mma3);
         if (!mbar_wait(&mma3, par, &abort_flag, p.status, kDevTimeoutMma)) break;
-        TRACE(j, 5);
         if (j + 2 < nc) load_g3(c + 2, st);
       }
     }
@@ -265,7 +242,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int t = 0; t < 32; ++t) u[t] = 0.f;
       }
       if (!mbar_wait(&mma1, par, &abort_flag, p.status, kDevTimeoutMma)) { alive = false; break; }
-      if (tid == 0) TRACE(j, 8);
       tc_fence_after();
       {
         float r[32];
@@ -277,19 +253,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_wait_st();
         tc_fence_before();
         mbar_arrive(&vready);
-        if (tid == 0) TRACE(j, 9);
         if (vnew_save) {
           float* vsave = vnew_save + tile * kTileW + size_t(t0) * kD + v;
 #pragma unroll
           for (int t = 0; t < 32; ++t) vsave[size_t(t) * kD] = r[t];
         }
       }
-      if (tid == 0) TRACE(j, 10);
       if (!mbar_wait(&mma2, par, &abort_flag, p.status, kDevTimeoutMma)) { alive = false; break; }
-      if (tid == 0) TRACE(j, 11);
       tc_fence_after();
       if (j + 1 < nc) chain_state_pass(p, h_save, c + 1, h, v, k0, tb + lb, &sready, gnext);
-      if (tid == 0) TRACE(j, 12);
       if (o) {
         if (!mbar_wait(&mma3, par, &abort_flag, p.status, kDevTimeoutMma)) { alive = false; break; }
         tc_fence_after();
@@ -308,7 +280,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           const __nv_bfloat162 pr = odd ? __floats2bfloat162_rn(other, mine) : __floats2bfloat162_rn(mine, other);
           if (t0 + 16 * odd + t < ch.y) op[size_t(t) * H * kD / 2] = pr;
         }
-        if (tid == 0) TRACE(j, 13);
       }
     }
     // exit state: the final state, the next segment's entry (pass 0), or the segment's map
@@ -345,12 +316,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   if (warp == 0) tmem_dealloc(tb, 512);
 }
-
-#ifdef GDN_TRACE
-extern "C" int gdn_trace_read(unsigned long long* host) {
-  return cudaMemcpyFromSymbol(host, g_trace, sizeof(g_trace)) == cudaSuccess ? 0 : -1;
-}
-#endif
 
 cudaError_t launch_chain_fwd(const CUtensorMap& mW, const CUtensorMap& mQt, const CUtensorMap& mKtT,
                              const CUtensorMap& mAqk, const CUtensorMap& mU, const ChainParams& p,

@@ -25,22 +25,6 @@
 
 namespace gdn {
 
-#ifdef GDN_TRACE
-// Optional timeline of the first CTA (compiled only with -DGDN_TRACE; never in the library).
-__device__ unsigned long long g_trace_rev[64 * 16];
-__device__ int g_trace_rev_block = 0;
-extern "C" int g_trace_rev_set_block(int b) {
-  return cudaMemcpyToSymbol(g_trace_rev_block, &b, sizeof(int)) == cudaSuccess ? 0 : -1;
-}
-#define RTRACE(j, slot) \
-  do { if (blockIdx.x == g_trace_rev_block && blockIdx.y == 0 && (j) < 64) g_trace_rev[(j) * 16 + (slot)] = globaltimer(); } while (0)
-extern "C" int gdn_trace_rev_read(unsigned long long* host) {
-  return cudaMemcpyFromSymbol(host, g_trace_rev, sizeof(g_trace_rev)) == cudaSuccess ? 0 : -1;
-}
-#else
-#define RTRACE(j, slot) do {} while (0)
-#endif
-
 namespace {
 
 constexpr int kChainThreads = 256;
@@ -105,7 +89,6 @@ __device__ __forceinline__ void rev_pass(const RevChainParams& p, float* dh_save
   }
   tmem_st32(tl + kTDM + k0, s);
   tmem_st32(tl + kTDM + k0 + 32, s + 32);
-  if (threadIdx.x == 0) RTRACE(jt, 9);
   if (use_do) {
     float df[32];
 #pragma unroll
@@ -118,7 +101,6 @@ __device__ __forceinline__ void rev_pass(const RevChainParams& p, float* dh_save
   tmem_wait_st();
   tc_fence_before();
   mbar_arrive(ready);
-  if (threadIdx.x == 0) RTRACE(jt, 10);
   if (!dh_save) return;
   // re-read the tf32 copy (the MMAs only read it) and save it
   tmem_ld64(tl + kTDT + k0, s);
@@ -203,11 +185,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int c = last - j, st = j & 1;
         const uint32_t par = j & 1;
         const uint32_t base = smem_u32(sm + st * kStage);
-        RTRACE(j, 0);
         if (!mbar_wait(&full[st], (j >> 1) & 1, &abort_flag, p.status, kDevTimeoutTma)) break;
-        RTRACE(j, 1);
         if (!mbar_wait(&dready, par, &abort_flag, p.status, kDevTimeoutSync)) break;
-        RTRACE(j, 2);
         tc_fence_after();
         // dv_new^T = dO^T Aqk + dS'^T Kt^T
         if (use_do)
@@ -215,19 +194,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int s = 0; s < 16; ++s)
           mma_tf32_ts(tb + kTDV, tb + kTDT + s * 8, desc_kmajor(base + kOffKt, 8192, s), id64, use_do || s > 0);
         mma_commit(&mma1);
-        RTRACE(j, 6);
         // dS^T += dO^T Qt   (master copy already holds gam dS'^T)
         if (use_do)
           for (int s = 0; s < 8; ++s) mma_tf32_ts(tb + kTDM, tb + kTDO + s * 8, desc_kmajor(base + kOffQtT, 16384, s), id128, true);
         if (!mbar_wait(&vready, par, &abort_flag, p.status, kDevTimeoutSync)) break;
-        RTRACE(j, 3);
         tc_fence_after();
         // dS^T += (-dv_new^T) W
         for (int s = 0; s < 8; ++s) mma_tf32_ts(tb + kTDM, tb + kTDN + s * 8, desc_kmajor(base + kOffWT, 16384, s), id128, true);
         mma_commit(&mma2);
         if (use_do && j + 3 < nc) prefetch_do(c - 3);
         if (!mbar_wait(&mma2, par, &abort_flag, p.status, kDevTimeoutMma)) break;
-        RTRACE(j, 4);
         if (j + 2 < nc) load(c - 2, st);
       }
     }
@@ -266,7 +242,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       // next chunk's scalar gate, loaded early so the dS pass does not wait for it
       const float gnext = (j + 1 < nc && !p.kda) ? p.gam[(size_t(c - 1) * H + h) * kD] : 0.f;
       if (!mbar_wait(&mma1, par, &abort_flag, p.status, kDevTimeoutMma)) { alive = false; break; }
-      if (tid == 0) RTRACE(j, 5);
       tc_fence_after();
       {
         float r[32];
@@ -277,7 +252,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_st32(tl + kTDN + t0, r);
         tmem_wait_st();
         tc_fence_before();
-        if (tid == 0) RTRACE(j, 7);
         mbar_arrive(&vready);
         if (dvn_save) {
           float* dv = dvn_save + tile * kTileW + size_t(t0) * kD + v;
@@ -286,13 +260,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       if (!mbar_wait(&mma2, par, &abort_flag, p.status, kDevTimeoutMma)) { alive = false; break; }
-      if (tid == 0) RTRACE(j, 8);
       tc_fence_after();
       if (j + 1 < nc) {
         rev_pass(p, dh_save, use_do, c - 1, h, v, k0, t0, tl, &dready, dnext, gnext, j);
         if (use_do && j + 2 < nc) load_dO(p, c - 2, h, v, t0, dnext);
       }
-      if (tid == 0) RTRACE(j, 11);
     }
     // exit gradient: dh0, the next segment's seed (pass 0), or the segment's map
     float* dst = nullptr;

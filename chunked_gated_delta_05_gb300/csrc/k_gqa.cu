@@ -37,7 +37,9 @@ __global__ void __launch_bounds__(256) k_group_sum(const GroupSumParams p) {
 cudaError_t launch_group_sum(const GroupSumParams& p, cudaStream_t s) {
   const long long n4 = p.R * (p.H / p.G) * (kD / 4);
   const long long want = (n4 + 255) / 256;
-  const int blocks = int(want < 152 * 16 ? want : 152 * 16);
+  // a grid-stride loop over at most 16 resident CTAs of 256 threads per SM
+  const long long cap = 16ll * (p.sms > 0 ? p.sms : 1);
+  const int blocks = int(want < cap ? want : cap);
   k_group_sum<<<blocks > 0 ? blocks : 1, 256, 0, s>>>(p);
   return cudaGetLastError();
 }

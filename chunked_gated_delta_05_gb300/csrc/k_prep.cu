@@ -30,20 +30,6 @@
 
 namespace gdn {
 
-#ifdef GDN_TRACE
-__device__ unsigned long long g_trace_prep[4 * 16];
-#define PTRACE(slot)                                                                                    \
-  do {                                                                                                  \
-    if (blockIdx.y == 3 && threadIdx.x == 0 && blockIdx.x % 16 == 5 && blockIdx.x < 64)                 \
-      g_trace_prep[(blockIdx.x / 16) * 16 + (slot)] = globaltimer();                                     \
-  } while (0)
-extern "C" int gdn_trace_prep_read(unsigned long long* host) {
-  return cudaMemcpyFromSymbol(host, g_trace_prep, sizeof(g_trace_prep)) == cudaSuccess ? 0 : -1;
-}
-#else
-#define PTRACE(slot) do {} while (0)
-#endif
-
 namespace {
 
 constexpr int kThreads = 256;  // two threads per row of the stacked 128-row tile
@@ -91,7 +77,6 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int h = blockIdx.y, pair = blockIdx.x, H = p.H;
-  PTRACE(0);
   // Row of the stacked tile (= TMEM lane) and column half of this thread.
   const int rt = tid & (kRows - 1), hf = tid >> 7;
   const int blk = rt >> 6, il = rt & 63;
@@ -143,7 +128,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   float gi = 0.f, bi = 0.f;
   if (valid) {
-    gi = p.g[size_t(row) * H + h];
+    gi = fmaxf(p.g[size_t(row) * H + h], kGateFloor);  // g = -inf: exact reset, finite cumsum
     bi = __bfloat162float(p.beta[size_t(row) * H + h]);
     if (p.beta_sigmoid) bi = 1.f / (1.f + expf(-bi));
   }
@@ -152,7 +137,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     s_b[rt] = bi;
   }
   mbar_wait(&bar_tma, 0, &abort_flag, p.status, kDevTimeoutTma);
-  PTRACE(1);
 
   // L2-norm factors from the staged rows: each half-row's partial sums meet in the A1 area,
   // which is free until Qt is staged there.
@@ -187,7 +171,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const float Glast2 = len > 0 ? s_G2[blk * kC + len - 1] : 0.f;  // G_last log2(e)
-  PTRACE(2);
 
   // Gram products: TMEM cols [0,128) = K K^T, [128,256) = Q K^T (pair-stacked).
   if (tid == 0 && !abort_flag) {
@@ -253,7 +236,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     tma_store_commit();
   }
-  PTRACE(3);
   const bool ok1 = mbar_wait(&bar_mma, 0, &abort_flag, p.status, kDevTimeoutMma);
   tc_fence_after();
   if (tid == 0) tma_store_wait_read();  // L and A1 are rewritten next
@@ -297,7 +279,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     tma_store_commit();
   }
-  PTRACE(4);
 
   // A = (I + L)^-1 per chunk, one column per lane pair (into sX, which reuses the q tile: q is
   // no longer needed once Qt and the Q K^T product are done); then the scaled block-diagonal
@@ -307,7 +288,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int cb = warp >> 2, cc = 16 * (warp & 3) + (lane & 15);
     unit_lower_inverse_column(sL + cb * (kC * kC), reinterpret_cast<float*>(sQ) + cb * (kC * kC), cc, lane >> 4);
   }
-  PTRACE(5);
   if (tid == 0) tma_store_wait_read();  // A1 held the staged Aqk tiles
   __syncthreads();
   const float* sX = reinterpret_cast<const float*>(sQ) + blk * (kC * kC);
@@ -335,7 +315,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  PTRACE(6);
 
   // W = A1 k (TMEM cols [0,128)), U = A2 v (cols [128,256)); k, v as MN-major B operands.
   // A1, A2 carry only the strictly lower part of A (bf16); the identity part, which dominates
@@ -351,7 +330,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   const bool ok2 = mbar_wait(&bar_mma, 1, &abort_flag, p.status, kDevTimeoutMma);
   tc_fence_after();
-  PTRACE(7);
   // Warps 0-3 finish W (staged in L for chunk 0, S0 for chunk 1), warps 4-7 finish U (staged
   // in A1 / A2, free once the MMAs are done).
   if (ok2 && len > 0) {
@@ -398,7 +376,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     tma_store_commit();
     tma_store_wait_read();  // the writes themselves complete before the grid does
   }
-  PTRACE(8);
   tc_fence_before();
   __syncthreads();
   if (warp == 0) tmem_dealloc(tb, 256);

@@ -25,20 +25,6 @@
 
 namespace gdn {
 
-#ifdef GDN_TRACE
-__device__ unsigned long long g_trace_pkda[4 * 16];
-#define KTRACE(slot)                                                                                    \
-  do {                                                                                                  \
-    if (blockIdx.y == 3 && threadIdx.x == 0 && blockIdx.x % 16 == 5 && blockIdx.x < 64)                 \
-      g_trace_pkda[(blockIdx.x / 16) * 16 + (slot)] = globaltimer();                                     \
-  } while (0)
-extern "C" int gdn_trace_pkda_read(unsigned long long* host) {
-  return cudaMemcpyFromSymbol(host, g_trace_pkda, sizeof(g_trace_pkda)) == cudaSuccess ? 0 : -1;
-}
-#else
-#define KTRACE(slot) do {} while (0)
-#endif
-
 namespace {
 
 constexpr int kThreads = 256;  // eight warps: two threads per row or channel in most phases
@@ -103,7 +89,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   const ChunkEntry ch = p.chunks[c_idx];
   const int len = ch.y;
 
-  KTRACE(0);
   if (warp == 0) tmem_alloc(&tslot, 256);
   if (tid == 0) {
     // the barriers are this thread's alone until the block barrier below: start the loads now
@@ -154,7 +139,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tb = tslot;
   const uint32_t tl = tb + tmem_lane_base(warp);
   mbar_wait(&bar_tma, 0, &abort_flag, p.status, kDevTimeoutTma);
-  KTRACE(1);
   // rows past the chunk belong to the next document (or are zero): clear them
   if (tid >= len && tid < kC) {
     for (int c16 = 0; c16 < 16; ++c16) {
@@ -165,6 +149,22 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
   __syncthreads();
+  // Domain of the block factorisation below: within each 16-row block the cumulative gate of
+  // every channel stays within kKdaBlockDropMax of its value at the block's first row (NaN and
+  // infinite gates fail the test too). Outside it the results are not defined and the status
+  // word reports kDevGateRange.
+  {
+    const int c = tid & 127;
+    bool in_range = true;
+    for (int I = 2 * hf; I < 2 * hf + 2; ++I) {
+      const int r = 16 * I;
+      if (r >= len) break;
+      const float gr = sG[r * kGP + c];
+      for (int i = r + 1; i < min(r + 16, len); ++i)
+        in_range = in_range && fabsf(sG[i * kGP + c] - gr) <= kKdaBlockDropMax;
+    }
+    if (!in_range && p.status) atomicCAS(p.status, 0, kDevGateRange);
+  }
   // L2-norm factors: thread pairs (2 p, 2 p + 1) share row p % 64 of q (p < 64) or k, half the
   // columns each (eight per load).
   {
@@ -186,7 +186,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   if (tid < kD) s_gl[tid] = sG[(len - 1) * kGP + tid];
   __syncthreads();
-  KTRACE(2);
 
   // Stacked operand: rows 0..63 k^_i, rows 64..127 q^_i, each times exp(G_i - G_{r(i)}); each
   // thread builds half a row.
@@ -258,7 +257,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  KTRACE(3);
 
   // Row blocks of L (lanes 0..63) and Aqk (lanes 64..127) from D_I, I = block of the row; the
   // two halves of the block take 32 columns j each. Aqk rows are staged (padded [64][65]) and
@@ -295,7 +293,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  KTRACE(4);
   if (ok) {
     float* aqk = p.Aqk + tile * kTileAqk;
 #pragma unroll 4
@@ -324,7 +321,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
   __syncthreads();
-  KTRACE(5);
   // WY operands: A1 = (A - I) diag(beta r_k) (tf32), A2 = (A - I) diag(beta) (bf16), both
   // K-major [i][j]; four threads per column j, 16 rows each.
   {
@@ -345,7 +341,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  KTRACE(6);
   if (tid == 0 && ok) {
     const uint32_t a1 = smem_u32(sm + kOffA1), a2 = smem_u32(sm + kOffA2), k1t = smem_u32(sm + kOffK1T);
     const uint32_t v0 = smem_u32(sV);
@@ -358,7 +353,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   ok = ok && mbar_wait(&bar_mma, mma_phase, &abort_flag, p.status, kDevTimeoutMma);
   tc_fence_after();
   __syncthreads();  // the operand regions are free from here: W and U are staged over them
-  KTRACE(7);
   // W and U rows (64-row MMA results: lane 32*(r/16) + r%16 holds row r), read with the
   // 16x64b shape so that all 32 lanes work (lane t: row (t >> 2) + 8 (t & 1) of the warp's 16,
   // columns ((t >> 1) & 1) + 2 e); warps w and w + 4 take two 32-column groups each. Staged
@@ -390,7 +384,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
   __syncthreads();
-  KTRACE(8);
   if (ok && len > 0) {
     const int col = tid & 127;
     float* w = p.W + tile * kTileW;
@@ -410,7 +403,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
   __syncthreads();  // the W / U staging is reused for the transposed gated keys and queries
-  KTRACE(9);
   // Per-element outputs: thread (c, half) writes channel c of 32 rows; KtT and QtT are staged
   // padded [128][65] and leave as whole lines.
   float* sKT = reinterpret_cast<float*>(sm + kOffWS);
@@ -437,7 +429,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
   __syncthreads();
-  KTRACE(10);
   {
     float* ktt = p.KtT + tile * kTileKtT;
 #pragma unroll 4
@@ -449,7 +440,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   tc_fence_before();
   __syncthreads();
-  KTRACE(11);
   if (warp == 0) tmem_dealloc(tb, 256);
 }
 

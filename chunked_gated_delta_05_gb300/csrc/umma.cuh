@@ -24,6 +24,7 @@ enum DevErr : int {
   kDevTimeoutTma = 1,
   kDevTimeoutMma = 2,
   kDevTimeoutSync = 3,
+  kDevGateRange = 5,  // a per-channel gate dropped faster than the kernels support (GDN_ERANGE)
 };
 
 // Spin limit for every mbarrier wait, in nanoseconds of %globaltimer.

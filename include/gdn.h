@@ -44,7 +44,16 @@
  * gives GDN_EUNSUPPORTED; a CUDA launch failure gives GDN_ECUDA. Device kernels never trap:
  * every wait inside a kernel is bounded and, when it runs out, records a nonzero code in the
  * caller's `status` word (an int in device memory, or NULL), which the caller may read after
- * synchronising (GDN_ETIMEOUT semantics).
+ * synchronising: 1, 2 or 3 (a TMA, MMA or thread wait ran out: GDN_ETIMEOUT semantics) or
+ * GDN_ERANGE (below). The first code recorded stays; every entry point that starts from the
+ * inputs resets the word to 0.
+ *
+ * Gate range. GDN: any g <= 0 is accepted; g is floored at -128 inside the kernels, where
+ * exp(g) is already 0 in fp32, so g = -inf (or any g <= -128) is an exact state reset and dg
+ * there is 0. KDA: within every 16-token block of a chunk (tokens 16i .. 16i+15 of the chunk),
+ * each channel's cumulative gate may change by at most 80 from its value at the block's first
+ * token. This covers the pages' safe-gate range (every g in [-5, 0]: at most 75). A call outside
+ * it records GDN_ERANGE in the status word and its results are undefined.
  */
 #ifndef GDN_GB300_H
 #define GDN_GB300_H
@@ -61,6 +70,7 @@ extern "C" {
 #define GDN_EUNSUPPORTED 2  /* not a compute-capability 10.3 device, or no device */
 #define GDN_ECUDA 3         /* a CUDA runtime call or kernel launch failed */
 #define GDN_ETIMEOUT 4      /* a bounded in-kernel wait ran out (reported via the status word) */
+#define GDN_ERANGE 5        /* a KDA gate outside the supported range (reported via the status word) */
 
 /* Problem description shared by every entry point. */
 typedef struct {

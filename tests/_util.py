@@ -4,12 +4,16 @@ import torch
 
 import oracle
 
-# Tolerances of the method's acceptance bar: bf16 outputs max-abs <= 2e-2 and rel-L2 <= 5e-3;
-# fp32 states rel-L2 <= 1e-3. Gradients in fp32 (dg) are judged like bf16 outputs, with the
+# Tolerances of the method's acceptance bar: bf16 outputs (o, dq, dk, dv, the convolution's y
+# and dx) max-abs <= 2e-2 and rel-L2 <= 5e-3, the max-abs bound absolute; fp32 states (final
+# state, dh0) rel-L2 <= 1e-3. The gate and beta gradients (dg, dgk, dbeta, and the gate
+# activation's parameter gradients) and the convolution's fp32 parameter gradients are sums over
+# many tokens with no stated bound of their own: they are judged like bf16 outputs, with the
 # max-abs bound scaled by max(1, |ref|_inf).
 OUT_MAX_ABS = 2e-2
 OUT_REL_L2 = 5e-3
 STATE_REL_L2 = 1e-3
+SCALED_MAX_ABS = ("dg", "dgk", "dbeta", "da_log", "ddt_bias", "dweight", "dbias", "dhalo")
 
 
 def f64(t):
@@ -23,13 +27,17 @@ def rel_l2(x, ref):
     return float(np.linalg.norm(x - ref) / (den if den > 0 else 1.0))
 
 
-def assert_output(name, x, ref):
+def assert_output(name, x, ref, scaled=None):
+    """rel-L2 <= 5e-3 and max-abs <= 2e-2; the max-abs bound is scaled by max(1, |ref|_inf)
+    only for the gradients named in SCALED_MAX_ABS (``scaled`` overrides the choice)."""
     x = np.asarray(x, np.float64)
     ref = np.asarray(ref, np.float64)
     assert np.isfinite(x).all(), f"{name}: non-finite values"
     r = rel_l2(x, ref)
     m = float(np.abs(x - ref).max()) if x.size else 0.0
-    bound = OUT_MAX_ABS * max(1.0, float(np.abs(ref).max()) if ref.size else 1.0)
+    if scaled is None:
+        scaled = name.split()[0] in SCALED_MAX_ABS
+    bound = OUT_MAX_ABS * (max(1.0, float(np.abs(ref).max()) if ref.size else 1.0) if scaled else 1.0)
     assert r <= OUT_REL_L2 and m <= bound, f"{name}: rel-L2 {r:.3e} (<= {OUT_REL_L2}), max-abs {m:.3e} (<= {bound:.3e})"
     return r, m
 

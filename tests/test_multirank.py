@@ -2,6 +2,7 @@
 would launch them on two GPUs) agree on the slowest rank's time, and the whole-job throughput
 counts every rank's units over that time."""
 import os
+import socket
 import sys
 
 import torch
@@ -24,8 +25,14 @@ def _rank(rank, world, port, out):
         dist.destroy_process_group()
 
 
+def _free_port():
+    with socket.socket(socket.AF_INET, socket.SOCK_STREAM) as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
 def test_two_gloo_ranks_agree_on_the_slowest_time():
-    world, port = 2, 29517
+    world, port = 2, _free_port()
     with mp.Manager() as m:
         out = m.dict()
         mp.start_processes(_rank, args=(world, port, out), nprocs=world, start_method="spawn", join=True)
