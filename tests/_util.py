@@ -27,17 +27,23 @@ def rel_l2(x, ref):
     return float(np.linalg.norm(x - ref) / (den if den > 0 else 1.0))
 
 
-def assert_output(name, x, ref, scaled=None):
+def assert_output(name, x, ref, scaled=None, bf16_rounding=False):
     """rel-L2 <= 5e-3 and max-abs <= 2e-2; the max-abs bound is scaled by max(1, |ref|_inf)
-    only for the gradients named in SCALED_MAX_ABS (``scaled`` overrides the choice)."""
+    only for the gradients named in SCALED_MAX_ABS (``scaled`` overrides the choice). With
+    ``bf16_rounding`` each element may also differ by the rounding of its reference value to
+    bf16 (2^-8 |ref|): for bf16 outputs whose values exceed 2e-2 / 2^-8 = 5.12 (the short
+    convolution's), where one correct rounding alone is larger than the absolute bound."""
     x = np.asarray(x, np.float64)
     ref = np.asarray(ref, np.float64)
     assert np.isfinite(x).all(), f"{name}: non-finite values"
     r = rel_l2(x, ref)
-    m = float(np.abs(x - ref).max()) if x.size else 0.0
     if scaled is None:
         scaled = name.split()[0] in SCALED_MAX_ABS
     bound = OUT_MAX_ABS * (max(1.0, float(np.abs(ref).max()) if ref.size else 1.0) if scaled else 1.0)
+    err = np.abs(x - ref)
+    if bf16_rounding:
+        err = err - 2.0 ** -8 * np.abs(ref)
+    m = float(err.max()) if x.size else 0.0
     assert r <= OUT_REL_L2 and m <= bound, f"{name}: rel-L2 {r:.3e} (<= {OUT_REL_L2}), max-abs {m:.3e} (<= {bound:.3e})"
     return r, m
 
