@@ -16,14 +16,16 @@ class Desc(ctypes.Structure):
     _fields_ = [("B", c_int), ("T", c_int), ("H", c_int), ("K", c_int), ("V", c_int),
                 ("chunk_size", c_int), ("cu_seqlens", ctypes.POINTER(ctypes.c_int32)),
                 ("num_seqs", c_int), ("scale", c_float), ("use_qk_l2norm", c_int),
-                ("use_beta_sigmoid", c_int), ("output_final_state", c_int), ("num_k_heads", c_int)]
+                ("use_beta_sigmoid", c_int), ("output_final_state", c_int), ("num_k_heads", c_int),
+                ("use_gate_in_kernel", c_int), ("lower_bound", c_float)]
 
 
 class FwdArgs(ctypes.Structure):
     _fields_ = [("q", c_void_p), ("k", c_void_p), ("v", c_void_p), ("g", c_void_p),
                 ("beta", c_void_p), ("initial_state", c_void_p), ("o", c_void_p),
                 ("final_state", c_void_p), ("workspace", c_void_p), ("workspace_bytes", c_size_t),
-                ("status", c_void_p), ("saved", c_void_p), ("saved_bytes", c_size_t)]
+                ("status", c_void_p), ("saved", c_void_p), ("saved_bytes", c_size_t),
+                ("A_log", c_void_p), ("dt_bias", c_void_p)]
 
 
 class BwdArgs(ctypes.Structure):
@@ -32,7 +34,8 @@ class BwdArgs(ctypes.Structure):
                 ("dht", c_void_p), ("dq", c_void_p), ("dk", c_void_p), ("dv", c_void_p),
                 ("dbeta", c_void_p), ("dg", c_void_p), ("dh0", c_void_p),
                 ("workspace", c_void_p), ("workspace_bytes", c_size_t), ("status", c_void_p),
-                ("saved", c_void_p), ("saved_bytes", c_size_t)]
+                ("saved", c_void_p), ("saved_bytes", c_size_t), ("A_log", c_void_p), ("dt_bias", c_void_p),
+                ("dA_log", c_void_p), ("ddt_bias", c_void_p)]
 
 
 class ConvDesc(ctypes.Structure):
@@ -78,6 +81,7 @@ SIGNATURES = {
     "gdn_timing_kinds": ([], c_int),
     "gdn_timing_name": ([c_int], ctypes.c_char_p),
     "gdn_timing_read": ([c_int, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(c_int)], c_int),
+    "gdn_wait_selftest": ([c_void_p, ctypes.c_longlong, c_void_p, c_void_p], c_int),
 }
 
 _lock = threading.Lock()

@@ -63,6 +63,7 @@ struct Problem {
   int Hk, G;                // q/k heads and value heads per q/k head
   float scale;
   bool packed;
+  bool gate;                // KDA in-kernel gate activation
   std::vector<int32_t> cu;  // packed offsets (host copy)
 };
 
@@ -80,6 +81,9 @@ int validate_desc(const gdn_desc_t* d, Problem* P) {
   P->Hk = d->num_k_heads > 0 ? d->num_k_heads : d->H;
   P->G = d->H / P->Hk;
   P->scale = d->scale > 0.f ? d->scale : 1.0f / std::sqrt(float(d->K));
+  P->gate = d->use_gate_in_kernel != 0;
+  if (P->gate && !(d->lower_bound >= -5.f && d->lower_bound < 0.f))
+    return fail(GDN_EINVAL, "lower_bound must lie in [-5, 0) with use_gate_in_kernel");
   P->packed = d->cu_seqlens != nullptr;
   const long long R = (long long)d->B * d->T;
   if (R > (1ll << 30)) return fail(GDN_EINVAL, "B*T too large");
@@ -190,6 +194,7 @@ struct Layout {
   size_t dhs, dvns, dQt, dKt, dW, dK1, dV1, dgam;                  // rest part (relative)
   size_t rE, rPhi, rPlo, rB;                                       // reverse chain scan (rest part)
   size_t dq32, dk32;                                               // grouped q/k: per-value-head dq, dk
+  size_t dA_part, ddt_part;                                        // in-kernel gate: parameter partials
   size_t saved_total, rest_total, total;
   ScanPlan plan;
 };
@@ -249,6 +254,9 @@ Layout make_layout(const Problem& P, bool backward, bool kda = false) {
     const size_t per_head = P.G > 1 ? size_t(P.R) * P.H * kD * 4 : 0;
     L.dq32 = take(per_head);
     L.dk32 = take(per_head);
+    const size_t gate_parts = P.gate ? 4 * tiles * kD : 0;
+    L.dA_part = take(gate_parts);
+    L.ddt_part = take(gate_parts);
   }
   L.rest_total = off;
   L.total = L.saved_total + L.rest_total;
@@ -290,7 +298,7 @@ int check_cuda(cudaError_t e, const char* what) {
 // Optional per-kernel timing (CUDA events recorded on the launching stream around every
 // launch while enabled). Process-global and not thread-safe: a profiling aid.
 const char* const kKindNames[kKinds] = {"tables", "prepare", "chain_fwd", "chain_bwd", "bwd_feat", "bwd_tok",
-                                        "compose", "group_sum", "conv_fwd", "conv_bwd"};
+                                        "compose", "group_sum", "conv_fwd", "conv_bwd", "gate_grad"};
 struct Timing {
   bool on = false;
   std::vector<std::pair<cudaEvent_t, cudaEvent_t>> ev[kKinds];
@@ -358,7 +366,7 @@ bool bwd_maps(const Problem& P, const char* sv, const char* rs, const Layout& L,
 // Prepare-kernel parameters for a buffer carved by make_layout at `sv` (backward-mode outputs
 // only when `backward`).
 PrepParams prep_params(const gdn_desc_t* d, const Problem& P, char* sv, const Layout& L, const float* g,
-                       const void* beta, bool backward, int* status) {
+                       const void* beta, bool backward, int* status, const float* A_log, const float* dt_bias) {
   auto F = [&](size_t off) { return reinterpret_cast<float*>(sv + off); };
   PrepParams pp{};
   pp.chunks = reinterpret_cast<const ChunkEntry*>(sv + L.chunks);
@@ -375,6 +383,10 @@ PrepParams prep_params(const gdn_desc_t* d, const Problem& P, char* sv, const La
     pp.Gc = F(L.Gc); pp.rq = F(L.rq); pp.rk = F(L.rk); pp.beff = F(L.beff);
     pp.Kt = F(L.Kt); pp.QtT = F(L.QtT); pp.AqkT = F(L.AqkT); pp.WT = F(L.WT); pp.A = F(L.A);
   }
+  pp.gate_act = P.gate ? 1 : 0;
+  pp.lower_bound = d->lower_bound;
+  pp.A_log = A_log;
+  pp.dt_bias = dt_bias;
   pp.status = status;
   return pp;
 }
@@ -475,6 +487,8 @@ int run_fwd(const gdn_desc_t* d, const gdn_fwd_args_t* a, void* stream, bool kda
   if (!a->q || !a->k || !a->v || !a->g || !a->beta || !a->o)
     return fail(GDN_EINVAL, "q, k, v, g, beta and o must be non-NULL");
   if (d->output_final_state && !a->final_state) return fail(GDN_EINVAL, "final_state is NULL but requested");
+  if (P.gate && !kda) return fail(GDN_EINVAL, "use_gate_in_kernel is a KDA option (the GDN gate comes in activated)");
+  if (P.gate && (!a->A_log || !a->dt_bias)) return fail(GDN_EINVAL, "use_gate_in_kernel needs A_log and dt_bias");
   if (!aligned16(a->q) || !aligned16(a->k) || !aligned16(a->v) || !aligned16(a->o))
     return fail(GDN_EINVAL, "q, k, v and o must be 16-byte aligned");
   const size_t nqk = size_t(P.R) * P.Hk * kD * 2, nv = size_t(P.R) * P.H * kD * 2;
@@ -501,7 +515,7 @@ int run_fwd(const gdn_desc_t* d, const gdn_fwd_args_t* a, void* stream, bool kda
   if (rc) return rc;
   Maps M;
   if (!fwd_maps(P, a->q, a->k, a->v, ws, L, &M)) return fail(GDN_ECUDA, "cuTensorMapEncodeTiled failed");
-  const PrepParams pp = prep_params(d, P, ws, L, a->g, a->beta, training, a->status);
+  const PrepParams pp = prep_params(d, P, ws, L, a->g, a->beta, training, a->status, a->A_log, a->dt_bias);
   {
     TimedLaunch tl_(kKPrep, s);
     rc = check_cuda(kda ? launch_prep_kda(M.q, M.k, M.v, pp, s)
@@ -536,6 +550,9 @@ int run_bwd(const gdn_desc_t* d, const gdn_bwd_args_t* a, void* stream, bool kda
   if (!a) return fail(GDN_EINVAL, "args is NULL");
   if (!a->q || !a->k || !a->v || !a->g || !a->beta || !a->dO || !a->dq || !a->dk || !a->dv || !a->dbeta || !a->dg)
     return fail(GDN_EINVAL, "q, k, v, g, beta, dO and every gradient output except dh0 must be non-NULL");
+  if (P.gate && !kda) return fail(GDN_EINVAL, "use_gate_in_kernel is a KDA option (the GDN gate comes in activated)");
+  if (P.gate && (!a->A_log || !a->dt_bias || !a->dA_log || !a->ddt_bias))
+    return fail(GDN_EINVAL, "use_gate_in_kernel needs A_log, dt_bias, dA_log and ddt_bias");
   if (!aligned16(a->q) || !aligned16(a->k) || !aligned16(a->v) || !aligned16(a->dO) || !aligned16(a->dq) ||
       !aligned16(a->dk) || !aligned16(a->dv))
     return fail(GDN_EINVAL, "q, k, v, dO, dq, dk and dv must be 16-byte aligned");
@@ -580,7 +597,7 @@ int run_bwd(const gdn_desc_t* d, const gdn_bwd_args_t* a, void* stream, bool kda
   } else {
     rc = build_tables(P, sv, L, a->status, s);
     if (rc) return rc;
-    const PrepParams pp = prep_params(d, P, sv, L, a->g, a->beta, true, a->status);
+    const PrepParams pp = prep_params(d, P, sv, L, a->g, a->beta, true, a->status, a->A_log, a->dt_bias);
     {
       TimedLaunch tl_(kKPrep, s);
       rc = check_cuda(kda ? launch_prep_kda(M.q, M.k, M.v, pp, s)
@@ -659,6 +676,14 @@ int run_bwd(const gdn_desc_t* d, const gdn_bwd_args_t* a, void* stream, bool kda
   tp.dbeta = static_cast<__nv_bfloat16*>(a->dbeta);
   tp.dg = a->dg;
   tp.g = a->g;
+  if (P.gate) {
+    tp.gate_act = 1;
+    tp.lower_bound = d->lower_bound;
+    tp.A_log = a->A_log;
+    tp.dt_bias = a->dt_bias;
+    tp.dA_part = R(L.dA_part);
+    tp.ddt_part = R(L.ddt_part);
+  }
   tp.status = a->status;
   tp.kda = kda ? 1 : 0;
   tp.sms = fp.sms;
@@ -673,7 +698,20 @@ int run_bwd(const gdn_desc_t* d, const gdn_bwd_args_t* a, void* stream, bool kda
                         : launch_bwd_tok(M.q, M.k, M.v, M.dO, M.VN, M.DW, M.DVN, tp, s),
                     "token-major backward kernel");
   }
-  if (rc || P.G == 1) return rc;
+  if (rc) return rc;
+  if (P.gate) {
+    GateGradParams gg{};
+    gg.dA_part = tp.dA_part;
+    gg.ddt_part = tp.ddt_part;
+    gg.dA_log = a->dA_log;
+    gg.ddt_bias = a->ddt_bias;
+    gg.NC = P.NC;
+    gg.H = P.H;
+    TimedLaunch tl_(kKGateGrad, s);
+    rc = check_cuda(launch_gate_grad(gg, s), "gate gradient kernel");
+    if (rc) return rc;
+  }
+  if (P.G == 1) return GDN_OK;
   GroupSumParams gp{};
   gp.dq32 = tp.dq32;
   gp.dk32 = tp.dk32;

@@ -105,6 +105,12 @@ struct PrepParams {
   float* AqkT;                 // [64][64]   Aqk^T
   float* WT;                   // [128][64]  W^T
   float* A;                    // [64][64]   (I + L)^-1
+  // In-kernel KDA gate activation: g holds logits x; the gate is
+  // lower_bound * sigmoid(exp(A_log[h]) (x + dt_bias[h][k])).
+  int gate_act;
+  float lower_bound;
+  const float* A_log;          // [H]
+  const float* dt_bias;        // [H,K]
   int* status;
 };
 
@@ -177,7 +183,12 @@ struct BwdTokParams {
   const float *gam, *dgam;     // [NC,H,128]
   __nv_bfloat16 *dq, *dk, *dv, *dbeta;
   float* dg;
-  const float* g;              // the raw gate as passed ([R,H]; GDN's floor test)
+  const float* g;              // the raw gate as passed ([R,H] GDN floor test; [R,H,K] KDA logits)
+  int gate_act;                // KDA in-kernel gate activation (see PrepParams)
+  float lower_bound;
+  const float* A_log;
+  const float* dt_bias;
+  float *dA_part, *ddt_part;   // gate_act: per (chunk, head, channel) partial sums [NC,H,K]
   int qk_group;                // value heads per q/k head
   float *dq32, *dk32;          // qk_group > 1: per-value-head dq, dk [R,H,K] fp32 (summed later)
   int sms;                     // SM count (the distance to the next wave's CTA for prefetching)
@@ -187,7 +198,7 @@ struct BwdTokParams {
 // Kernel kinds of the per-launch timing hook (names in api.cu).
 enum KernelKind {
   kKTables = 0, kKPrep, kKChainFwd, kKChainBwd, kKBwdFeat, kKBwdTok, kKCompose, kKGroupSum, kKConvFwd, kKConvBwd,
-  kKinds
+  kKGateGrad, kKinds
 };
 
 // Host helpers shared by the entry points of several files (api.cu).
@@ -236,6 +247,16 @@ struct ComposeParams {
 };
 
 cudaError_t launch_group_sum(const GroupSumParams& p, cudaStream_t s);
+
+// Gradients of the KDA gate parameters from the token-backward's per-chunk partial sums:
+// ddt_bias[h][k] = sum over chunks of ddt_part, dA_log[h] = sum over chunks and channels of
+// dA_part, in a fixed order (deterministic).
+struct GateGradParams {
+  const float *dA_part, *ddt_part;  // [NC,H,K]
+  float *dA_log, *ddt_bias;         // [H], [H,K]
+  int NC, H;
+};
+cudaError_t launch_gate_grad(const GateGradParams& p, cudaStream_t s);
 cudaError_t launch_compose(const CUtensorMap& mPhi, const CUtensorMap& mPlo, const CUtensorMap& mB,
                            const ComposeParams& p, cudaStream_t s);
 cudaError_t launch_chain_fwd(const CUtensorMap& mW, const CUtensorMap& mQt, const CUtensorMap& mKtT,

@@ -472,9 +472,30 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   if (half == 0) {
     float acc = s_glast[0][cc] + s_glast[1][cc] + exp2f(glc) * dgam_c;
-    for (int t = len - 1; t >= 0; --t) {
-      acc += sGacc[t * kD + cc];
-      p.dg[(size_t(ch.x + t) * H + h) * kD + cc] = acc;
+    if (p.gate_act) {
+      // chain rule through the safe gate g = lb sigmoid(z), z = a (x + dt_bias), a = exp(A_log):
+      // dx = dg lb s (1 - s) a; the parameter gradients are summed per chunk here and over the
+      // chunks by the gate-gradient kernel
+      const float a = expf(p.A_log[h]), dtb = p.dt_bias[h * kD + cc];
+      float pa = 0.f, pd = 0.f;
+      for (int t = len - 1; t >= 0; --t) {
+        acc += sGacc[t * kD + cc];
+        const size_t o = (size_t(ch.x + t) * H + h) * kD + cc;
+        const float z = a * (p.g[o] + dtb);
+        const float sg = 1.f / (1.f + expf(-z));
+        const float dsz = acc * p.lower_bound * sg * (1.f - sg);
+        const float dx = dsz * a;
+        p.dg[o] = dx;
+        pa = fmaf(dsz, z, pa);
+        pd += dx;
+      }
+      p.dA_part[tile * kD + cc] = pa;
+      p.ddt_part[tile * kD + cc] = pd;
+    } else {
+      for (int t = len - 1; t >= 0; --t) {
+        acc += sGacc[t * kD + cc];
+        p.dg[(size_t(ch.x + t) * H + h) * kD + cc] = acc;
+      }
     }
   }
   if (tid < len) {

@@ -112,6 +112,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     float buf[32];
 #pragma unroll
     for (int e = 0; e < 32; ++e) buf[e] = (t0 + e < len) ? src[size_t(t0 + e) * H * kD] : 0.f;
+    if (p.gate_act) {
+      // safe gate from the logits: lower_bound * sigmoid(exp(A_log) (x + dt_bias))
+      const float a = expf(p.A_log[h]), dtb = p.dt_bias[h * kD + c];
+#pragma unroll
+      for (int e = 0; e < 32; ++e)
+        buf[e] = (t0 + e < len) ? p.lower_bound / (1.f + expf(-a * (buf[e] + dtb))) : 0.f;
+    }
     float run = 0.f;
 #pragma unroll
     for (int e = 0; e < 32; ++e) {

@@ -67,18 +67,29 @@ __device__ __forceinline__ bool mbar_try(uint64_t* bar, uint32_t parity) {
 // *abort (shared) and *status (global), and returns false. Once *abort is set every later
 // wait returns false at once, so all threads reach the kernel's exit path.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort,
-                                          int* status, int code) {
+                                          int* status, int code,
+                                          unsigned long long limit_ns = kWaitLimitNs) {
   if (mbar_try(bar, parity)) return true;
   const unsigned long long t0 = globaltimer();
   while (true) {
     if (*abort) return false;
     if (mbar_try(bar, parity)) return true;
-    if (globaltimer() - t0 > kWaitLimitNs) {
+    if (globaltimer() - t0 > limit_ns) {
       *abort = 1;
       if (status) atomicCAS(status, 0, code);
       return false;
     }
   }
+}
+// Bounded wait that ignores the abort flag: an aborting CTA uses it to let its own copies and
+// MMAs that are already in flight finish before it frees their destinations. False after
+// `limit_ns` without completion.
+__device__ __forceinline__ bool mbar_drain(uint64_t* bar, uint32_t parity,
+                                           unsigned long long limit_ns = kWaitLimitNs) {
+  const unsigned long long t0 = globaltimer();
+  while (!mbar_try(bar, parity))
+    if (globaltimer() - t0 > limit_ns) return false;
+  return true;
 }
 
 // ------------------------------------------------------------------ TMA
@@ -100,6 +111,14 @@ __device__ __forceinline__ void tma_store_commit() { asm volatile("cp.async.bulk
 __device__ __forceinline__ void tma_store_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 // The committed stores have finished reading their shared-memory sources (which may be reused).
 __device__ __forceinline__ void tma_store_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+
+// Untiled bulk copy global -> shared of `bytes` (a multiple of 16; both addresses 16-byte
+// aligned), completing on `bar`.
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+               ::"r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar))
+               : "memory");
+}
 
 // Fetch `bytes` (a multiple of 16, 16-byte aligned source) into L2 ahead of use; no
 // completion to wait for.

@@ -49,7 +49,7 @@ def _offsets(cu_seqlens, T):
     return (ctypes.c_int32 * len(vals))(*vals), len(vals) - 1
 
 
-def _desc(B, T, H, scale, l2, sig, final, offsets, Hk=None):
+def _desc(B, T, H, scale, l2, sig, final, offsets, Hk=None, gate=None):
     d = _lib.Desc()
     d.B, d.T, d.H, d.K, d.V, d.chunk_size = B, T, H, K_DIM, K_DIM, CHUNK
     d.num_k_heads = 0 if Hk is None or Hk == H else int(Hk)
@@ -61,7 +61,24 @@ def _desc(B, T, H, scale, l2, sig, final, offsets, Hk=None):
         d.num_seqs = B
     d.scale = 0.0 if scale is None else float(scale)
     d.use_qk_l2norm, d.use_beta_sigmoid, d.output_final_state = int(bool(l2)), int(bool(sig)), int(bool(final))
+    if gate is not None:
+        d.use_gate_in_kernel, d.lower_bound = 1, float(gate[2])
     return d
+
+
+def _gate_checks(gate, H, dev):
+    """``gate = (A_log [H], dt_bias [H,128] or [H*128], lower_bound)`` of the in-kernel KDA gate,
+    or None. Returns fp32 contiguous parameter tensors (or Nones)."""
+    if gate is None:
+        return None, None
+    A_log, dt_bias, lb = gate
+    if lb is None:
+        raise ValueError("lower_bound is required with the in-kernel gate")
+    _check_tensor("A_log", A_log, torch.float32, (H,), dev)
+    if not isinstance(dt_bias, torch.Tensor) or dt_bias.numel() != H * K_DIM or dt_bias.dtype != torch.float32 \
+            or dt_bias.device != dev or not dt_bias.is_contiguous():
+        raise ValueError(f"dt_bias must be a contiguous fp32 tensor of {H}*{K_DIM} elements on {dev}")
+    return A_log, dt_bias
 
 
 def _common_checks(q, k, v, g, beta, per_channel, offsets):
@@ -87,13 +104,14 @@ def _common_checks(q, k, v, g, beta, per_channel, offsets):
 
 
 def _fwd(per_channel, q, k, v, g, beta, initial_state, output_final_state, use_qk_l2norm,
-         use_beta_sigmoid, cu_seqlens, scale, status, save=False):
+         use_beta_sigmoid, cu_seqlens, scale, status, save=False, gate=None):
     lib = _lib.load()
     offsets = _offsets(cu_seqlens, q.shape[1] if q.dim() == 4 else 0)
     B, T, H, Hk, N, dev = _common_checks(q, k, v, g, beta, per_channel, offsets)
     if initial_state is not None:
         _check_tensor("initial_state", initial_state, torch.float32, (N, H, K_DIM, K_DIM), dev)
-    desc = _desc(B, T, H, scale, use_qk_l2norm, use_beta_sigmoid, output_final_state, offsets, Hk)
+    A_log, dt_bias = _gate_checks(gate, H, dev)
+    desc = _desc(B, T, H, scale, use_qk_l2norm, use_beta_sigmoid, output_final_state, offsets, Hk, gate)
     if save:
         size_fn = lib.kda_saved_size if per_channel else lib.gdn_saved_size
     else:
@@ -109,7 +127,8 @@ def _fwd(per_channel, q, k, v, g, beta, initial_state, output_final_state, use_q
     a = _lib.FwdArgs(q=_ptr(q), k=_ptr(k), v=_ptr(v), g=_ptr(g), beta=_ptr(beta),
                      initial_state=_ptr(initial_state), o=_ptr(o), final_state=_ptr(final),
                      workspace=None if save else _ptr(buf), workspace_bytes=0 if save else ws_bytes,
-                     status=_ptr(status), saved=_ptr(buf) if save else None, saved_bytes=ws_bytes if save else 0)
+                     status=_ptr(status), saved=_ptr(buf) if save else None, saved_bytes=ws_bytes if save else 0,
+                     A_log=_ptr(A_log), dt_bias=_ptr(dt_bias))
     stream = ctypes.c_void_p(torch.cuda.current_stream(dev).cuda_stream)
     fn = lib.kda_fwd if per_channel else lib.gdn_fwd
     _lib.check(fn(ctypes.byref(desc), ctypes.byref(a), stream))
@@ -119,7 +138,7 @@ def _fwd(per_channel, q, k, v, g, beta, initial_state, output_final_state, use_q
 
 
 def _bwd(per_channel, q, k, v, g, beta, dO, dht, initial_state, use_qk_l2norm, use_beta_sigmoid,
-         cu_seqlens, scale, status, saved=None):
+         cu_seqlens, scale, status, saved=None, gate=None):
     lib = _lib.load()
     offsets = _offsets(cu_seqlens, q.shape[1] if q.dim() == 4 else 0)
     B, T, H, Hk, N, dev = _common_checks(q, k, v, g, beta, per_channel, offsets)
@@ -128,7 +147,8 @@ def _bwd(per_channel, q, k, v, g, beta, dO, dht, initial_state, use_qk_l2norm, u
         _check_tensor("initial_state", initial_state, torch.float32, (N, H, K_DIM, K_DIM), dev)
     if dht is not None:
         _check_tensor("dht", dht, torch.float32, (N, H, K_DIM, K_DIM), dev)
-    desc = _desc(B, T, H, scale, use_qk_l2norm, use_beta_sigmoid, False, offsets, Hk)
+    A_log, dt_bias = _gate_checks(gate, H, dev)
+    desc = _desc(B, T, H, scale, use_qk_l2norm, use_beta_sigmoid, False, offsets, Hk, gate)
     size_fn = lib.kda_bwd_workspace_size if per_channel else lib.gdn_bwd_workspace_size
     ws_bytes = size_fn(ctypes.byref(desc))
     if ws_bytes == 0:
@@ -145,6 +165,8 @@ def _bwd(per_channel, q, k, v, g, beta, dO, dht, initial_state, use_qk_l2norm, u
     dbeta = torch.empty_like(beta)
     dg = torch.empty_like(g)
     dh0 = torch.empty((N, H, K_DIM, K_DIM), dtype=torch.float32, device=dev) if initial_state is not None else None
+    dA_log = torch.empty_like(A_log) if gate is not None else None
+    ddt_bias = torch.empty_like(dt_bias) if gate is not None else None
     ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
     if status is None:
         status = torch.empty(1, dtype=torch.int32, device=dev)
@@ -152,10 +174,13 @@ def _bwd(per_channel, q, k, v, g, beta, dO, dht, initial_state, use_qk_l2norm, u
                      initial_state=_ptr(initial_state), dO=_ptr(dO), dht=_ptr(dht), dq=_ptr(dq),
                      dk=_ptr(dk), dv=_ptr(dv), dbeta=_ptr(dbeta), dg=_ptr(dg), dh0=_ptr(dh0),
                      workspace=_ptr(ws), workspace_bytes=ws_bytes, status=_ptr(status),
-                     saved=_ptr(saved), saved_bytes=saved_bytes)
+                     saved=_ptr(saved), saved_bytes=saved_bytes, A_log=_ptr(A_log), dt_bias=_ptr(dt_bias),
+                     dA_log=_ptr(dA_log), ddt_bias=_ptr(ddt_bias))
     stream = ctypes.c_void_p(torch.cuda.current_stream(dev).cuda_stream)
     fn = lib.kda_bwd if per_channel else lib.gdn_bwd
     _lib.check(fn(ctypes.byref(desc), ctypes.byref(a), stream))
+    if gate is not None:
+        return dq, dk, dv, dbeta, dg, dh0, dA_log, ddt_bias
     return dq, dk, dv, dbeta, dg, dh0
 
 
@@ -185,10 +210,13 @@ def gdn_fwd(q, k, v, g, beta, *, initial_state=None, output_final_state=False, u
 
 def kda_fwd(q, k, v, g, beta, *, initial_state=None, output_final_state=False, use_qk_l2norm=True,
             use_beta_sigmoid=True, cu_seqlens: Optional[Sequence[int]] = None, scale=None, status=None,
-            save=False):
-    """Kimi Delta Attention forward (per-channel gate g [B,T,H,128])."""
+            save=False, A_log=None, dt_bias=None, lower_bound=None):
+    """Kimi Delta Attention forward (per-channel gate g [B,T,H,128]). With ``A_log`` [H],
+    ``dt_bias`` [H,128] and ``lower_bound`` in [-5, 0), g holds gate logits x and the kernels
+    use the safe gate lower_bound * sigmoid(exp(A_log) (x + dt_bias))."""
+    gate = None if A_log is None else (A_log, dt_bias, lower_bound)
     return _fwd(True, q, k, v, g, beta, initial_state, output_final_state, use_qk_l2norm,
-                use_beta_sigmoid, cu_seqlens, scale, status, save)
+                use_beta_sigmoid, cu_seqlens, scale, status, save, gate)
 
 
 def gdn_bwd(q, k, v, g, beta, dO, *, dht=None, initial_state=None, use_qk_l2norm=True,
@@ -200,10 +228,14 @@ def gdn_bwd(q, k, v, g, beta, dO, *, dht=None, initial_state=None, use_qk_l2norm
 
 
 def kda_bwd(q, k, v, g, beta, dO, *, dht=None, initial_state=None, use_qk_l2norm=True,
-            use_beta_sigmoid=True, cu_seqlens=None, scale=None, status=None, saved=None):
-    """Kimi Delta Attention backward. Returns ``(dq, dk, dv, dbeta, dg, dh0 or None)``."""
+            use_beta_sigmoid=True, cu_seqlens=None, scale=None, status=None, saved=None,
+            A_log=None, dt_bias=None, lower_bound=None):
+    """Kimi Delta Attention backward. Returns ``(dq, dk, dv, dbeta, dg, dh0 or None)``; with the
+    in-kernel gate (``A_log``, ``dt_bias``, ``lower_bound`` as in :func:`kda_fwd`) dg is w.r.t.
+    the gate logits and ``dA_log [H]``, ``ddt_bias`` (dt_bias's shape) follow."""
+    gate = None if A_log is None else (A_log, dt_bias, lower_bound)
     return _bwd(True, q, k, v, g, beta, dO, dht, initial_state, use_qk_l2norm, use_beta_sigmoid,
-                cu_seqlens, scale, status, saved)
+                cu_seqlens, scale, status, saved, gate)
 
 
 class ChunkGatedDeltaRule(torch.autograd.Function):

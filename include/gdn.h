@@ -86,6 +86,12 @@ typedef struct {
                                 value head h reads q/k head h / (H / num_k_heads), the pages'
                                 `repeat_interleave` of q and k, done by indexing); must divide H;
                                 0 means H. dq and dk are the sums over each group. */
+  int use_gate_in_kernel;    /* KDA only (0 for GDN): g holds gate logits x and the kernels use the
+                                activated gate lower_bound * sigmoid(exp(A_log[h]) (x + dt_bias[h][k]))
+                                (the KDA page's `_prepare_kda` with use_gate_in_kernel and safe_gate;
+                                the formula is this library's reading: the pages give the interface,
+                                the range and the gradients, not the expression) */
+  float lower_bound;         /* the safe gate's bound, in [-5, 0) (used with use_gate_in_kernel) */
 } gdn_desc_t;
 
 typedef struct {
@@ -105,6 +111,8 @@ typedef struct {
                                 aligned) that receives the chunk intermediates the backward
                                 needs; NULL for inference */
   size_t saved_bytes;
+  const float* A_log;        /* use_gate_in_kernel: [H] fp32 (else ignored) */
+  const float* dt_bias;      /* use_gate_in_kernel: [H,K] fp32 (else ignored) */
 } gdn_fwd_args_t;
 
 typedef struct {
@@ -130,6 +138,11 @@ typedef struct {
                                 inputs (the backward then skips recomputing the forward), or
                                 NULL (the backward recomputes it) */
   size_t saved_bytes;
+  const float* A_log;        /* use_gate_in_kernel: the forward's gate parameters */
+  const float* dt_bias;
+  float* dA_log;             /* use_gate_in_kernel: [H] fp32, written (else ignored). dg is then the
+                                gradient w.r.t. the gate logits x */
+  float* ddt_bias;           /* use_gate_in_kernel: [H,K] fp32, written */
 } gdn_bwd_args_t;
 
 /* Human-readable name of an error code. */
@@ -243,6 +256,17 @@ int gdn_timing_enable(int enable);
 int gdn_timing_kinds(void);
 const char* gdn_timing_name(int kind);
 int gdn_timing_read(int kind, double* total_ms, int* launches);
+
+/* Self-test of the failure reporting of the bounded in-kernel waits (no counterpart in the
+ * pages: a check of this library's own error path, not part of the computation). Enqueues one
+ * small kernel on `stream` whose threads wait, with a limit of `limit_ns` nanoseconds
+ * (0 < limit_ns <= 2e9), on a barrier that nothing completes, while one 4096-byte copy from
+ * `src` (device, 16-byte aligned, at least 4096 bytes, only read) is in flight. The wait runs
+ * out, records 3 (a thread wait ran out: GDN_ETIMEOUT semantics) in the device int `*status`
+ * (which the caller zeroes beforehand) and the kernel exits normally after the copy has landed;
+ * the stream and the context stay usable. Returns GDN_EINVAL for bad arguments, GDN_EUNSUPPORTED
+ * off compute capability 10.3, else GDN_OK without synchronising. */
+int gdn_wait_selftest(const void* src, long long limit_ns, int* status, void* stream);
 
 #ifdef __cplusplus
 }

@@ -27,10 +27,29 @@ def test_exports_every_declared_symbol():
 
 
 def test_struct_sizes_match_header_layout():
-    # desc: 6 ints, pointer, int, float, 3 ints (x86-64 / aarch64 LP64 alignment)
-    assert ctypes.sizeof(_lib.Desc) == 56
-    assert ctypes.sizeof(_lib.FwdArgs) == 13 * 8
-    assert ctypes.sizeof(_lib.BwdArgs) == 19 * 8
+    # desc: 6 ints, pointer, int, float, 4 ints, float (x86-64 / aarch64 LP64 alignment)
+    assert ctypes.sizeof(_lib.Desc) == 64
+    assert ctypes.sizeof(_lib.FwdArgs) == 15 * 8
+    assert ctypes.sizeof(_lib.BwdArgs) == 23 * 8
+
+
+@pytest.mark.parametrize("lb", [0.0, 0.5, -5.5, float("nan")])
+def test_gate_lower_bound_outside_range_rejected(lb):
+    assert ws_size(desc(use_gate_in_kernel=1, lower_bound=lb), "kda_fwd_workspace_size") == 0
+    assert "lower_bound" in _lib.load().gdn_last_error().decode()
+
+
+def test_gate_in_kernel_is_kda_only_and_needs_parameters():
+    lib = _lib.load()
+    d = desc(use_gate_in_kernel=1, lower_bound=-5.0)
+    a = _lib.FwdArgs()
+    a.q = a.k = a.v = a.g = a.beta = 0x1000
+    a.o = 0x10000000
+    a.workspace, a.workspace_bytes = 0x20000000, 1 << 30
+    assert lib.gdn_fwd(ctypes.byref(d), ctypes.byref(a), None) == _lib.GDN_EINVAL
+    assert "KDA" in lib.gdn_last_error().decode()
+    assert lib.kda_fwd(ctypes.byref(d), ctypes.byref(a), None) == _lib.GDN_EINVAL
+    assert "A_log" in lib.gdn_last_error().decode()
 
 
 def desc(**kw):
