@@ -187,9 +187,7 @@ ScanPlan plan_scan(const Problem& P) {
 // both parts in the workspace. With a saved buffer: saved part there, rest part in the
 // workspace. Every region is 256-byte aligned; rest offsets are relative to the rest base.
 struct Layout {
-  bool lean;                                                       // scalar gate: W16, fq, fk
-  size_t cu, seqs, chunks, W, U, Qt, KtT, Aqk, gam;               // forward (W, Qt, KtT: fp32 layout)
-  size_t W16, fq, fk;                                              // forward (lean layout)
+  size_t cu, seqs, chunks, W, U, Qt, KtT, Aqk, gam;               // forward
   size_t Kt, QtT, AqkT, WT, A, Gc, rq, rk, beff;                  // prepare, backward mode
   size_t hs, vns;                                                  // forward chain saves
   size_t fE, fPhi, fPlo, fB;                                       // forward chain scan (scratch)
@@ -210,20 +208,13 @@ Layout make_layout(const Problem& P, bool backward, bool kda = false) {
     return o;
   };
   const size_t tiles = size_t(P.NC) * P.H;
-  L.lean = !kda;
   L.cu = take(sizeof(int) * (P.N + 1));
   L.seqs = take(sizeof(SeqEntry) * P.N);
   L.chunks = take(sizeof(ChunkEntry) * P.NC);
-  if (L.lean) {
-    L.W16 = take(2 * tiles * kTileW);
-    L.fq = take(4 * tiles * kC);
-    L.fk = take(4 * tiles * kC);
-  } else {
-    L.W = take(4 * tiles * kTileW);
-    L.Qt = take(4 * tiles * kTileW);
-    L.KtT = take(4 * tiles * kTileKtT);
-  }
+  L.W = take(4 * tiles * kTileW);
   L.U = take(4 * tiles * kTileW);
+  L.Qt = take(4 * tiles * kTileW);
+  L.KtT = take(4 * tiles * kTileKtT);
   L.Aqk = take(4 * tiles * kTileAqk);
   L.gam = take(4 * tiles * kD);
   if (backward) {
@@ -337,8 +328,7 @@ struct TimedLaunch {
 };
 
 struct Maps {
-  CUtensorMap q, k, v, W, Qt, KtT, Aqk, U, Usw;      // forward (Usw: U as a swizzled store target;
-                                                     // lean layout: W = the bf16 W rows, no Qt, KtT)
+  CUtensorMap q, k, v, W, Qt, KtT, Aqk, U, Usw;      // forward (Usw: U as a swizzled store target)
   CUtensorMap Kt, AqkT, QtT, WT, VN, DVN, DW, dO;     // backward
   CUtensorMap Hs, DHs;                               // saved states h, dh' [tile][128][128] (128-row boxes)
 };
@@ -355,22 +345,13 @@ bool backward_tiles(const Layout& L) { return L.Kt != 0; }
 bool fwd_maps(const Problem& P, const void* q, const void* k, const void* v, const char* ws, const Layout& L, Maps* M) {
   const uint64_t HD = uint64_t(P.H) * kD, HDk = uint64_t(P.Hk) * kD;
   const uint64_t r64 = uint64_t(P.NC) * P.H * kC, r128 = uint64_t(P.NC) * P.H * kD;
-  const bool ok = make_map(&M->q, q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, HDk, P.R, HDk * 2, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B) &&
+  return make_map(&M->q, q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, HDk, P.R, HDk * 2, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B) &&
          make_map(&M->k, k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, HDk, P.R, HDk * 2, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B) &&
          make_map(&M->v, v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, HD, P.R, HD * 2, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B) &&
+         tile_map(&M->W, ws + L.W, kD, r64, 64, true) && tile_map(&M->Qt, ws + L.Qt, kD, r64, 64, true) &&
          tile_map(&M->U, ws + L.U, kD, r64, 64, false) && tile_map(&M->Usw, ws + L.U, kD, r64, 64, true) &&
-         tile_map(&M->Aqk, ws + L.Aqk, kC, r64, 64, true) &&
+         tile_map(&M->KtT, ws + L.KtT, kC, r128, 128, true) && tile_map(&M->Aqk, ws + L.Aqk, kC, r64, 64, true) &&
          (!backward_tiles(L) || tile_map(&M->Kt, ws + L.Kt, kD, r64, 64, true));
-  if (!ok) return false;
-  if (L.lean) {
-    // bf16 W rows as the chain's staged source; Qt and KtT are built by the chain
-    M->Qt = M->Aqk;
-    M->KtT = M->Aqk;
-    return make_map(&M->W, ws + L.W16, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, kD, r64, kD * 2, 64, 64,
-                    CU_TENSOR_MAP_SWIZZLE_128B);
-  }
-  return tile_map(&M->W, ws + L.W, kD, r64, 64, true) && tile_map(&M->Qt, ws + L.Qt, kD, r64, 64, true) &&
-         tile_map(&M->KtT, ws + L.KtT, kC, r128, 128, true);
 }
 
 bool bwd_maps(const Problem& P, const char* sv, const char* rs, const Layout& L, Maps* M) {
@@ -397,14 +378,7 @@ PrepParams prep_params(const gdn_desc_t* d, const Problem& P, char* sv, const La
   pp.l2norm = d->use_qk_l2norm;
   pp.beta_sigmoid = d->use_beta_sigmoid;
   pp.qk_group = P.G;
-  pp.U = F(L.U); pp.Aqk = F(L.Aqk); pp.gam = F(L.gam);
-  if (L.lean) {
-    pp.W16 = reinterpret_cast<__nv_bfloat16*>(sv + L.W16);
-    pp.fq = F(L.fq);
-    pp.fk = F(L.fk);
-  } else {
-    pp.W = F(L.W); pp.Qt = F(L.Qt); pp.KtT = F(L.KtT);
-  }
+  pp.W = F(L.W); pp.U = F(L.U); pp.Qt = F(L.Qt); pp.KtT = F(L.KtT); pp.Aqk = F(L.Aqk); pp.gam = F(L.gam);
   if (backward) {
     pp.Gc = F(L.Gc); pp.rq = F(L.rq); pp.rk = F(L.rk); pp.beff = F(L.beff);
     pp.Kt = F(L.Kt); pp.QtT = F(L.QtT); pp.AqkT = F(L.AqkT); pp.WT = F(L.WT); pp.A = F(L.A);
@@ -484,9 +458,7 @@ int run_chain_fwd(const Problem& P, const Maps& M, ChainParams cp, cudaStream_t 
     }
     cp.sp.pass = pass;
     TimedLaunch tl_(kKChainFwd, s);
-    const bool lean = cp.lean != 0;
-    int rc = check_cuda(launch_chain_fwd(M.W, lean ? M.q : M.Qt, lean ? M.k : M.KtT, M.Aqk, M.U, cp, s),
-                        "chain kernel");
+    int rc = check_cuda(launch_chain_fwd(M.W, M.Qt, M.KtT, M.Aqk, M.U, cp, s), "chain kernel");
     if (rc) return rc;
   }
   return GDN_OK;
@@ -562,10 +534,6 @@ int run_fwd(const gdn_desc_t* d, const gdn_fwd_args_t* a, void* stream, bool kda
   cp.h0 = a->initial_state;
   cp.hT = d->output_final_state ? a->final_state : nullptr;
   cp.o = static_cast<__nv_bfloat16*>(a->o);
-  cp.lean = L.lean ? 1 : 0;
-  cp.fq = pp.fq;
-  cp.fk = pp.fk;
-  cp.qk_group = P.G;
   if (training) {
     cp.h_save = reinterpret_cast<float*>(ws + L.hs);
     cp.vnew_save = reinterpret_cast<float*>(ws + L.vns);
@@ -644,10 +612,6 @@ int run_bwd(const gdn_desc_t* d, const gdn_bwd_args_t* a, void* stream, bool kda
     cp.N = P.N;
     cp.H = P.H;
     cp.gam = F(L.gam);
-    cp.lean = L.lean ? 1 : 0;
-    cp.fq = pp.fq;
-    cp.fk = pp.fk;
-    cp.qk_group = P.G;
     cp.h0 = a->initial_state;
     cp.h_save = F(L.hs);
     cp.vnew_save = F(L.vns);
@@ -828,11 +792,7 @@ size_t kda_saved_size(const gdn_desc_t* desc) {
   return make_layout(P, true, true).saved_total;
 }
 
-size_t kda_fwd_workspace_size(const gdn_desc_t* desc) {
-  Problem P;
-  if (validate_desc(desc, &P)) return 0;
-  return make_layout(P, false, true).saved_total;
-}
+size_t kda_fwd_workspace_size(const gdn_desc_t* desc) { return gdn_fwd_workspace_size(desc); }
 
 size_t gdn_bwd_workspace_size(const gdn_desc_t* desc) {
   Problem P;

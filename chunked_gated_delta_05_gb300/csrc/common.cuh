@@ -97,12 +97,7 @@ struct PrepParams {
   float scale;
   int l2norm, beta_sigmoid;
   int qk_group;                // value heads per q/k head (q/k head of value head h: h / qk_group)
-  float *W, *U, *Qt, *KtT, *Aqk, *gam;  // W, Qt, KtT null in the lean layout (scalar gate)
-  // Lean layout (scalar gate): W as bf16 rows, and the per-token factors that turn the raw q, k
-  // rows into Qt and KtT inside the chain: fq = scale r_q exp(G), fk = r_k exp(G_last - G)
-  // (0 for rows past the chunk).
-  __nv_bfloat16* W16;          // [NC*H*64][128]
-  float *fq, *fk;              // [NC*H*64]
+  float *W, *U, *Qt, *KtT, *Aqk, *gam;
   float *Gc, *rq, *rk, *beff;  // optional per-token saves [NC*H*64] (KDA Gc: [NC*H*64*128]); may be null
   // Backward-only tiles (all null in the forward):
   float* Kt;                   // [64][128]  r_k exp(G_last - G) k   (row-major KtT^T)
@@ -146,9 +141,6 @@ struct ChainParams {
   __nv_bfloat16* o;            // [R,H,V] or null
   float* h_save;               // [NC,H,K,V] entry state of every chunk, or null
   float* vnew_save;            // [NC,H,64,V] or null
-  int lean;                    // scalar gate: bf16 W rows + raw q, k with per-token factors
-  const float *fq, *fk;        // lean: [NC*H*64]
-  int qk_group;                // lean: value heads per q/k head
   int* status;
 };
 

@@ -49,16 +49,6 @@ __device__ __forceinline__ uint8_t* align1k(uint8_t* p) {
   return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
 }
 
-__device__ __forceinline__ void bf16x8_to_f32(const uint4& u, float* f) {
-  const __nv_bfloat162* b = reinterpret_cast<const __nv_bfloat162*>(&u);
-#pragma unroll
-  for (int e = 0; e < 4; ++e) {
-    const float2 t = __bfloat1622float2(b[e]);
-    f[2 * e] = t.x;
-    f[2 * e + 1] = t.y;
-  }
-}
-
 // S pass for chunk c (one thread: lane v, state columns [k0, k0+64)): write the entry state's
 // tf32 copy (the MMA operand), pre-apply the chunk's end decay to the fp32 master copy (the
 // MMA then adds k~^T v_new in place), release the MMA issuer, and only then record the entry
@@ -108,70 +98,13 @@ __device__ __forceinline__ void chain_state_pass(const ChainParams& p, float* h_
 
 }  // namespace
 
-// Lean operand format (scalar gate): the prepare kernel leaves W as bf16 rows and the
-// per-token factors fq = scale r_q exp(G), fk = r_k exp(G_last - G); the CTA stages the raw
-// bf16 W, q and k rows of the next chunk with TMA and its chain warps build the tf32 operands
-// in shared memory, W and Qt = diag(fq) q into the [W; Qt] tile after the chunk's first MMA has
-// read it, and KtT = (diag(fk) k)^T after the state update has read the previous one. The
-// conversions run while the MMAs of the current chunk are in flight. Shared memory (bytes):
-constexpr uint32_t kLnOffU = 65536;      // U fp32, as above
-constexpr uint32_t kLnOffKtT = 98304;    // KtT tf32, one stage (2 panels x 128 rows)
-constexpr uint32_t kLnOffAqk = 131072;   // 2 stages x Aqk fp32 16 KB
-constexpr uint32_t kLnOffStage = 163840; // bf16 staging: W 16 KB, q 16 KB, k 16 KB (2 panels x 64 rows each)
-constexpr uint32_t kLnSmemBytes = kLnOffStage + 3 * 16384 + 1024;
-
-// [W; Qt] rows of the next chunk from the staging (thread: token row t, 32-column quarter qq).
-__device__ __forceinline__ void lean_convert_wq(const uint8_t* stage, uint8_t* wq, float fq, int t, int qq, bool with_q) {
-  const uint8_t* sw = stage;
-  const uint8_t* sq = stage + 16384;
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const int c = 32 * qq + 8 * i;
-    float f[8];
-    bf16x8_to_f32(*reinterpret_cast<const uint4*>(sw + sw128_offset(t, c, kC, 2)), f);
-    *reinterpret_cast<float4*>(wq + sw128_offset(t, c, 128, 4)) =
-        make_float4(to_tf32(f[0]), to_tf32(f[1]), to_tf32(f[2]), to_tf32(f[3]));
-    *reinterpret_cast<float4*>(wq + sw128_offset(t, c + 4, 128, 4)) =
-        make_float4(to_tf32(f[4]), to_tf32(f[5]), to_tf32(f[6]), to_tf32(f[7]));
-    if (with_q) {
-      bf16x8_to_f32(*reinterpret_cast<const uint4*>(sq + sw128_offset(t, c, kC, 2)), f);
-      *reinterpret_cast<float4*>(wq + sw128_offset(kC + t, c, 128, 4)) =
-          make_float4(to_tf32(fq * f[0]), to_tf32(fq * f[1]), to_tf32(fq * f[2]), to_tf32(fq * f[3]));
-      *reinterpret_cast<float4*>(wq + sw128_offset(kC + t, c + 4, 128, 4)) =
-          make_float4(to_tf32(fq * f[4]), to_tf32(fq * f[5]), to_tf32(fq * f[6]), to_tf32(fq * f[7]));
-    }
-  }
-}
-
-// KtT of the next chunk (warp w: key channels 16 w .. 16 w + 15; lane: tokens lane, lane + 32).
-__device__ __forceinline__ void lean_convert_ktt(const uint8_t* stage, uint8_t* ktt, const float* fk, int warp,
-                                                 int lane) {
-  const uint8_t* sk = stage + 32768;
-#pragma unroll
-  for (int ps = 0; ps < 2; ++ps) {
-    const int t = 32 * ps + lane;
-    const float f = fk[t];
-    float a[8], b[8];
-    bf16x8_to_f32(*reinterpret_cast<const uint4*>(sk + sw128_offset(t, 16 * warp, kC, 2)), a);
-    bf16x8_to_f32(*reinterpret_cast<const uint4*>(sk + sw128_offset(t, 16 * warp + 8, kC, 2)), b);
-#pragma unroll
-    for (int e = 0; e < 8; ++e) {
-      *reinterpret_cast<float*>(ktt + sw128_offset(16 * warp + e, t, 128, 4)) = to_tf32(f * a[e]);
-      *reinterpret_cast<float*>(ktt + sw128_offset(16 * warp + 8 + e, t, 128, 4)) = to_tf32(f * b[e]);
-    }
-  }
-}
-
-// Tensor maps: kLean = false: (W, Qt, KtT, Aqk, U) fp32 tiles of the prepare kernel;
-// kLean = true: (W bf16 rows, q, k inputs, Aqk, U).
-template <bool kLean>
 __global__ void __launch_bounds__(kThreads, 1)
     k_chain_fwd(const __grid_constant__ CUtensorMap mW, const __grid_constant__ CUtensorMap mQt,
                 const __grid_constant__ CUtensorMap mKtT, const __grid_constant__ CUtensorMap mAqk,
                 const __grid_constant__ CUtensorMap mU, const ChainParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = align1k(smem_raw);
-  __shared__ uint64_t full1, full2, full3[2], mma1, mma2, mma3, sready, vready, kready, sfree;
+  __shared__ uint64_t full1, full2, full3[2], mma1, mma2, mma3, sready, vready;
   __shared__ uint32_t tslot;
   __shared__ int abort_flag;
 
@@ -189,8 +122,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   const bool outs = mode == kRunFull;     // output, saves and the output products
   const bool use_u = mode != kRunMapM;    // U enters v_new
   const size_t slot_base = size_t(n) * sp.maxS;
-  const uint32_t offU = kLean ? kLnOffU : kOffU;
-  const int hk = h / p.qk_group;          // q/k head of this value head
 
   if (warp == 0) tmem_alloc(&tslot, 512);
   if (tid == 0) {
@@ -204,8 +135,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&mma3, 1);
     mbar_init(&sready, kChainThreads);
     mbar_init(&vready, kChainThreads);
-    mbar_init(&kready, kChainThreads);
-    mbar_init(&sfree, kChainThreads);
     fence_mbar_init();
   }
   tc_fence_before();
@@ -217,7 +146,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       // ---------------- producer + MMA issuer ----------------
       const uint32_t sWQ = smem_u32(sm + kOffWQ);
-      auto load_g1 = [&](int c) {  // fp32 [W; Qt] tiles
+      auto load_g1 = [&](int c) {
         const int y = (c * H + h) * kC;
         mbar_expect_tx(&full1, outs ? 65536u : 32768u);
         for (int pp = 0; pp < 4; ++pp) {
@@ -225,28 +154,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (outs) tma_load_2d(sm + kOffWQ + pp * 16384 + 8192, &mQt, pp * 32, y, &full1);
         }
       };
-      auto load_stage = [&](int c) {  // lean: bf16 W rows, q and k of chunk c (on full1)
-        const int y = (c * H + h) * kC, row = p.chunks[c].x;
-        mbar_expect_tx(&full1, outs ? 49152u : 32768u);
-        for (int pp = 0; pp < 2; ++pp) {
-          tma_load_2d(sm + kLnOffStage + pp * 8192, &mW, pp * 64, y, &full1);
-          if (outs) tma_load_2d(sm + kLnOffStage + 16384 + pp * 8192, &mQt, hk * kD + pp * 64, row, &full1);
-          tma_load_2d(sm + kLnOffStage + 32768 + pp * 8192, &mKtT, hk * kD + pp * 64, row, &full1);
-        }
-      };
       auto load_g2 = [&](int c) {
         const int y = (c * H + h) * kC;
         mbar_expect_tx(&full2, 32768u);
-        for (int pp = 0; pp < 4; ++pp) tma_load_2d(sm + offU + pp * 8192, &mU, pp * 32, y, &full2);
+        for (int pp = 0; pp < 4; ++pp) tma_load_2d(sm + kOffU + pp * 8192, &mU, pp * 32, y, &full2);
       };
-      auto load_g3 = [&](int c, int st) {  // fp32: KtT + Aqk; lean: Aqk alone
-        if (kLean) {
-          if (!outs) return;
-          mbar_expect_tx(&full3[st], 16384u);
-          for (int pp = 0; pp < 2; ++pp)
-            tma_load_2d(sm + kLnOffAqk + st * 16384 + pp * 8192, &mAqk, pp * 32, (c * H + h) * kC, &full3[st]);
-          return;
-        }
+      auto load_g3 = [&](int c, int st) {
         uint8_t* base = sm + kOffG3 + st * kG3Stage;
         mbar_expect_tx(&full3[st], outs ? 49152u : 32768u);
         for (int pp = 0; pp < 2; ++pp) {
@@ -254,46 +167,27 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (outs) tma_load_2d(base + 32768 + pp * 8192, &mAqk, pp * 32, (c * H + h) * kC, &full3[st]);
         }
       };
-      bool alive = true;
-      if (kLean) {
-        load_stage(first);
-        if (use_u) load_g2(first);
-        load_g3(first, 0);
-        if (nc > 1) load_g3(first + 1, 1);
-        // the staging is reloaded once the chain warps have converted the chunk it holds
-        if (nc > 1) {
-          alive = mbar_wait(&sfree, 0, &abort_flag, p.status, kDevTimeoutSync);
-          if (alive) load_stage(first + 1);
-        }
-      } else {
-        load_g1(first);
-        if (use_u) load_g2(first);
-        load_g3(first, 0);
-        if (nc > 1) load_g3(first + 1, 1);
-      }
+      load_g1(first);
+      if (use_u) load_g2(first);
+      load_g3(first, 0);
+      if (nc > 1) load_g3(first + 1, 1);
       const uint32_t id64 = idesc_tf32(128, 64), id128 = idesc_tf32(128, 128);
       const uint32_t id_first = outs ? id128 : id64;  // [P | O] or P alone
-      for (int j = 0; j < nc && alive; ++j) {
+      for (int j = 0; j < nc; ++j) {
         const uint32_t par = j & 1;
         const int c = first + j, st = j & 1;
         const uint32_t tPV = tb + tpv(j), tO = tb + tout(j);
-        const uint32_t sKtT = kLean ? smem_u32(sm + kLnOffKtT) : smem_u32(sm + kOffG3 + st * kG3Stage);
-        const uint32_t sAqk = kLean ? smem_u32(sm + kLnOffAqk + st * 16384) : sKtT + 32768;
-        if (!kLean && !mbar_wait(&full1, par, &abort_flag, p.status, kDevTimeoutTma)) break;
-        if (!mbar_wait(&sready, par, &abort_flag, p.status, kDevTimeoutSync)) break;  // lean: covers [W; Qt]
+        const uint32_t sKtT = smem_u32(sm + kOffG3 + st * kG3Stage), sAqk = sKtT + 32768;
+        if (!mbar_wait(&full1, par, &abort_flag, p.status, kDevTimeoutTma)) break;
+        if (!mbar_wait(&sready, par, &abort_flag, p.status, kDevTimeoutSync)) break;
         tc_fence_after();
         for (int s = 0; s < 16; ++s) mma_tf32_ts(tPV, tb + kTST + s * 8, desc_kmajor(sWQ, 16384, s), id_first, s > 0);
         mma_commit(&mma1);
         if (!mbar_wait(&mma1, par, &abort_flag, p.status, kDevTimeoutMma)) break;
-        if (!kLean && j + 1 < nc) load_g1(c + 1);
+        if (j + 1 < nc) load_g1(c + 1);
         if (!mbar_wait(&vready, par, &abort_flag, p.status, kDevTimeoutSync)) break;
         if (j + 1 < nc && use_u) load_g2(c + 1);
-        if (kLean) {
-          if (!mbar_wait(&kready, par, &abort_flag, p.status, kDevTimeoutSync)) break;
-          if (outs && !mbar_wait(&full3[st], (j >> 1) & 1, &abort_flag, p.status, kDevTimeoutTma)) break;
-        } else {
-          if (!mbar_wait(&full3[st], (j >> 1) & 1, &abort_flag, p.status, kDevTimeoutTma)) break;
-        }
+        if (!mbar_wait(&full3[st], (j >> 1) & 1, &abort_flag, p.status, kDevTimeoutTma)) break;
         tc_fence_after();
         for (int s = 0; s < 8; ++s) mma_tf32_ts(tb + kTSM, tPV + s * 8, desc_kmajor(sKtT, 16384, s), id128, true);
         mma_commit(&mma2);
@@ -302,25 +196,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         mma_commit(&mma3);
         if (!mbar_wait(&mma3, par, &abort_flag, p.status, kDevTimeoutMma)) break;
         if (j + 2 < nc) load_g3(c + 2, st);
-        if (kLean && j + 2 < nc) {
-          // the chain warps converted chunk j + 1 from the staging during this iteration
-          if (!mbar_wait(&sfree, (j + 1) & 1, &abort_flag, p.status, kDevTimeoutSync)) break;
-          load_stage(c + 2);
-        }
       }
     }
   } else if (warp < kChainThreads / 32) {
     // ---------------- chain warps: lane v of S^T, column half `half` ----------------
     const int v = tid & 127, half = tid >> 7;
     const uint32_t lb = tmem_lane_base(warp);
-    const float* sU = reinterpret_cast<const float*>(sm + offU);
+    const float* sU = reinterpret_cast<const float*>(sm + kOffU);
     const int k0 = 64 * half;  // state columns handled by this thread
     const int t0 = 32 * half;  // token columns handled by this thread
-    const int ct = tid & 63, cq = tid >> 6;  // lean conversion of [W; Qt]: token row, column quarter
     float* h_save = outs ? p.h_save : nullptr;
     float* vnew_save = outs ? p.vnew_save : nullptr;
     __nv_bfloat16* o = outs ? p.o : nullptr;
-    bool alive = true;
     {
       // entry state: the initial state, a composed segment entry, the identity (map M) or zero
       const float* src = nullptr;
@@ -335,20 +222,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_st32(tb + lb + kTSM + k0 + 32, buf + 32);
       tmem_wait_st();
     }
-    if (kLean) {
-      // operands of the first chunk from the staging (load 0)
-      alive = mbar_wait(&full1, 0, &abort_flag, p.status, kDevTimeoutTma);
-      if (alive) {
-        lean_convert_wq(sm + kLnOffStage, sm + kOffWQ, outs ? p.fq[(size_t(first) * H + h) * kC + ct] : 0.f, ct, cq, outs);
-        lean_convert_ktt(sm + kLnOffStage, sm + kLnOffKtT, p.fk + (size_t(first) * H + h) * kC, warp, lane);
-        fence_async_smem();
-        mbar_arrive(&kready);
-        mbar_arrive(&sfree);
-      }
-    }
-    if (alive)
-      chain_state_pass(p, h_save, first, h, v, k0, tb + lb, &sready, p.kda ? 0.f : p.gam[(size_t(first) * H + h) * kD]);
-    for (int j = 0; j < nc && alive; ++j) {
+    chain_state_pass(p, h_save, first, h, v, k0, tb + lb, &sready,
+                     p.kda ? 0.f : p.gam[(size_t(first) * H + h) * kD]);
+    bool alive = true;
+    for (int j = 0; j < nc; ++j) {
       const uint32_t par = j & 1;
       const int c = first + j;
       const ChunkEntry ch = p.chunks[c];
@@ -382,25 +259,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int t = 0; t < 32; ++t) vsave[size_t(t) * kD] = r[t];
         }
       }
-      // lean: [W; Qt] of the next chunk (staging load j + 1), now that this chunk's first
-      // product has read the tile
-      if (kLean && j + 1 < nc) {
-        if (!mbar_wait(&full1, (j + 1) & 1, &abort_flag, p.status, kDevTimeoutTma)) { alive = false; break; }
-        lean_convert_wq(sm + kLnOffStage, sm + kOffWQ, outs ? p.fq[(size_t(c + 1) * H + h) * kC + ct] : 0.f, ct, cq,
-                        outs);
-        fence_async_smem();
-      }
       if (!mbar_wait(&mma2, par, &abort_flag, p.status, kDevTimeoutMma)) { alive = false; break; }
       tc_fence_after();
       if (j + 1 < nc) chain_state_pass(p, h_save, c + 1, h, v, k0, tb + lb, &sready, gnext);
-      // lean: KtT of the next chunk, now that this chunk's state update has read it; the
-      // staging is then free for the chunk after
-      if (kLean && j + 1 < nc) {
-        lean_convert_ktt(sm + kLnOffStage, sm + kLnOffKtT, p.fk + (size_t(c + 1) * H + h) * kC, warp, lane);
-        fence_async_smem();
-        mbar_arrive(&kready);
-        mbar_arrive(&sfree);
-      }
       if (o) {
         if (!mbar_wait(&mma3, par, &abort_flag, p.status, kDevTimeoutMma)) { alive = false; break; }
         tc_fence_after();
@@ -461,17 +322,12 @@ cudaError_t launch_chain_fwd(const CUtensorMap& mW, const CUtensorMap& mQt, cons
                              cudaStream_t s) {
   static bool attr = false;
   if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(k_chain_fwd<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-    if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(k_chain_fwd<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kLnSmemBytes);
+    cudaError_t e = cudaFuncSetAttribute(k_chain_fwd, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     if (e != cudaSuccess) return e;
     attr = true;
   }
   dim3 grid(p.N * runs_per_seq(p.sp.maxS, p.sp.pass), p.H);
-  if (p.lean)
-    k_chain_fwd<true><<<grid, kThreads, kLnSmemBytes, s>>>(mW, mQt, mKtT, mAqk, mU, p);
-  else
-    k_chain_fwd<false><<<grid, kThreads, kSmemBytes, s>>>(mW, mQt, mKtT, mAqk, mU, p);
+  k_chain_fwd<<<grid, kThreads, kSmemBytes, s>>>(mW, mQt, mKtT, mAqk, mU, p);
   return cudaGetLastError();
 }
 

@@ -191,27 +191,23 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (len > 0) {
     const float fq = valid ? p.scale * rq * expf(G) : 0.f;
     const float fk = valid ? rk * exp2f(Glast2 - G * kLog2e) : 0.f;
+    float* ktt = p.KtT + tile * kTileKtT + il;
 #pragma unroll
     for (int c16 = 8 * hf; c16 < 8 * hf + 8; ++c16) {
       const uint32_t off = sw128_offset(rt, c16 * 8, 128, 2);
       float f[8];
       bf16x8_to_f32(*reinterpret_cast<const uint4*>(sQ + off), f);
-      if (p.Qt) {
 #pragma unroll
-        for (int e = 0; e < 8; e += 4)
-          *reinterpret_cast<float4*>(stQt + sw128_offset(il, c16 * 8 + e, kC, 4)) =
-              make_float4(to_tf32(f[e] * fq), to_tf32(f[e + 1] * fq), to_tf32(f[e + 2] * fq), to_tf32(f[e + 3] * fq));
-      }
+      for (int e = 0; e < 8; e += 4)
+        *reinterpret_cast<float4*>(stQt + sw128_offset(il, c16 * 8 + e, kC, 4)) =
+            make_float4(to_tf32(f[e] * fq), to_tf32(f[e + 1] * fq), to_tf32(f[e + 2] * fq), to_tf32(f[e + 3] * fq));
       if (p.QtT) {
 #pragma unroll
         for (int e = 0; e < 8; ++e) p.QtT[tile * kTileKtT + size_t(c16 * 8 + e) * kC + il] = to_tf32(f[e] * fq);
       }
       bf16x8_to_f32(*reinterpret_cast<const uint4*>(sK + off), f);
-      if (p.KtT) {
-        float* ktt = p.KtT + tile * kTileKtT + il;
 #pragma unroll
-        for (int e = 0; e < 8; ++e) ktt[size_t(c16 * 8 + e) * kC] = to_tf32(f[e] * fk);
-      }
+      for (int e = 0; e < 8; ++e) ktt[size_t(c16 * 8 + e) * kC] = to_tf32(f[e] * fk);
       if (p.Kt) {
 #pragma unroll
         for (int e = 0; e < 8; e += 4)
@@ -221,8 +217,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (hf == 0) {
       if (il == 0) p.gam[tile * kD] = exp2f(Glast2);
-      if (p.fq) p.fq[tile * kC + il] = fq;
-      if (p.fk) p.fk[tile * kC + il] = fk;
       if (p.Gc) p.Gc[tile * kC + il] = G;
       if (p.rq) p.rq[tile * kC + il] = rq;
       if (p.rk) p.rk[tile * kC + il] = rk;
@@ -236,7 +230,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (s_chunk[b].y <= 0) continue;
       const int y = (int(2 * pair + b) * H + h) * kC;
       for (int pp = 0; pp < 4; ++pp) {
-        if (p.Qt) tma_store_2d(&mQt, pp * 32, y, (b ? sA2 : sA1) + pp * 8192);
+        tma_store_2d(&mQt, pp * 32, y, (b ? sA2 : sA1) + pp * 8192);
         if (p.Kt) tma_store_2d(&mKt, pp * 32, y, (b ? sS0 : reinterpret_cast<uint8_t*>(sL)) + pp * 8192);
       }
     }
@@ -347,33 +341,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       float r[64];
       tmem_ld64(tb + lane_base + which * 128 + half * 64, r);
       tmem_wait_ld_regs(r);
-      const bool w16 = which == 0 && p.W16;  // W leaves as a bf16 row, straight from registers
-      uint4* w16row = w16 ? reinterpret_cast<uint4*>(p.W16 + (tile * kC + il) * kD + half * 64) : nullptr;
 #pragma unroll
       for (int c8 = 0; c8 < 8; ++c8) {
         float in[8];
         bf16x8_to_f32(*reinterpret_cast<const uint4*>(src + sw128_offset(rt, half * 64 + c8 * 8, 128, 2)), in);
 #pragma unroll
-        for (int e = 0; e < 8; ++e) in[e] = fmaf(sc, in[e], r[c8 * 8 + e]);
-        if (w16) {
-          uint4 u;
-          uint32_t* w = reinterpret_cast<uint32_t*>(&u);
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const __nv_bfloat162 b2 = __floats2bfloat162_rn(in[2 * e], in[2 * e + 1]);
-            w[e] = *reinterpret_cast<const uint32_t*>(&b2);
-          }
-          w16row[c8] = u;
+        for (int e = 0; e < 8; ++e) {
+          const float val = fmaf(sc, in[e], r[c8 * 8 + e]);
+          r[c8 * 8 + e] = which == 0 ? to_tf32(val) : val;
         }
-#pragma unroll
-        for (int e = 0; e < 8; ++e) r[c8 * 8 + e] = which == 0 ? to_tf32(in[e]) : in[e];
       }
-      if (!w16) {
 #pragma unroll
-        for (int e = 0; e < 16; ++e)
-          *reinterpret_cast<float4*>(stage + sw128_offset(il, half * 64 + 4 * e, kC, 4)) =
-              make_float4(r[4 * e], r[4 * e + 1], r[4 * e + 2], r[4 * e + 3]);
-      }
+      for (int e = 0; e < 16; ++e)
+        *reinterpret_cast<float4*>(stage + sw128_offset(il, half * 64 + 4 * e, kC, 4)) =
+            make_float4(r[4 * e], r[4 * e + 1], r[4 * e + 2], r[4 * e + 3]);
       if (which == 0 && p.WT) {
         float* wt = p.WT + tile * kTileKtT + size_t(half * 64) * kC + il;
 #pragma unroll
@@ -388,7 +369,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (s_chunk[b].y <= 0 || !ok2) continue;
       const int y = (int(2 * pair + b) * H + h) * kC;
       for (int pp = 0; pp < 4; ++pp) {
-        if (!p.W16) tma_store_2d(&mW, pp * 32, y, (b ? sS0 : reinterpret_cast<uint8_t*>(sL)) + pp * 8192);
+        tma_store_2d(&mW, pp * 32, y, (b ? sS0 : reinterpret_cast<uint8_t*>(sL)) + pp * 8192);
         tma_store_2d(&mU, pp * 32, y, (b ? sA2 : sA1) + pp * 8192);
       }
     }

@@ -308,11 +308,15 @@ __host__ __device__ __forceinline__ uint32_t sw128_offset(int row, int col, int 
   return uint32_t(panel * rows * 128 + (row >> 3) * 1024 + (row & 7) * 128 + (chunk << 4) + (byte & 15));
 }
 
-// Round-to-nearest fp32 -> tf32 (kept in an fp32 container; the low 13 bits are cleared).
+// fp32 -> tf32, round to nearest with ties away from zero, kept in an fp32 container (the low
+// 13 bits cleared). Done on the bit pattern: adding half a tf32 unit in the last place (bit 12)
+// to the magnitude bits and clearing bits 0..12 rounds the magnitude to the nearest tf32 value,
+// a carry out of the mantissa stepping into the exponent as rounding requires; the sign bit is
+// untouched. Two integer instructions instead of the conversion instruction, which is the
+// bottleneck of the conversion-heavy loops. Finite values and infinities only (a NaN whose low
+// 31 bits are all set would not stay a NaN).
 __device__ __forceinline__ float to_tf32(float x) {
-  uint32_t r;
-  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
-  return __uint_as_float(r);
+  return __uint_as_float((__float_as_uint(x) + 0x1000u) & 0xffffe000u);
 }
 
 }  // namespace gdn
