@@ -67,6 +67,11 @@ __device__ __forceinline__ void chain_state_pass(const ChainParams& p, float* h_
     for (int e = 0; e < 32; ++e) t[e] = to_tf32(s[32 * half + e]);
     tmem_st32(tl + kTST + k0 + 32 * half, t);
   }
+  tmem_wait_st();
+  tc_fence_before();
+  mbar_arrive(sready);  // the next W S product reads only the tf32 copy
+  // Decay the master for the coming state update; that MMA goes out after this thread's next
+  // arrival on the v_new barrier, which follows these stores.
   if (p.kda) {
     const float4* gam = reinterpret_cast<const float4*>(p.gam + tile * kD + k0);
 #pragma unroll
@@ -84,8 +89,6 @@ __device__ __forceinline__ void chain_state_pass(const ChainParams& p, float* h_
   tmem_st32(tl + kTSM + k0, s);
   tmem_st32(tl + kTSM + k0 + 32, s + 32);
   tmem_wait_st();
-  tc_fence_before();
-  mbar_arrive(sready);
   if (h_save) {
     // re-read the tf32 copy (the MMAs only read it) and store it
     tmem_ld64(tl + kTST + k0, s);

@@ -57,11 +57,13 @@ __device__ __forceinline__ void load_dO(const RevChainParams& p, int c, int h, i
 
 // dS pass for chunk c (lane v, state columns [k0, k0+64); token columns [t0, t0+32)): write
 // the tf32 copy of dS' (the gradient w.r.t. the state leaving chunk c) and dO^T (prefetched
-// into `d`) as A operands, pre-apply the chunk decay to the master copy, release the MMA
-// issuer, then save dS' (its tf32 copy) for the feature-major backward kernel.
+// into `d`) as A operands and release the dv_new product (`ready`); then pre-apply the chunk
+// decay to the master copy and release the products that accumulate into it (`mready`), so
+// the decay runs while dv_new is computed; then save dS' (its tf32 copy) for the feature-major
+// backward kernel.
 __device__ __forceinline__ void rev_pass(const RevChainParams& p, float* dh_save, bool use_do, int c, int h,
-                                         int v, int k0, int t0, uint32_t tl, uint64_t* ready, const uint32_t* d,
-                                         float g0, int jt = 63) {
+                                         int v, int k0, int t0, uint32_t tl, uint64_t* ready, uint64_t* mready,
+                                         const uint32_t* d, float g0) {
   const size_t tile = size_t(c) * p.H + h;
   float s[64];
   tmem_ld64(tl + kTDM + k0, s);
@@ -73,6 +75,18 @@ __device__ __forceinline__ void rev_pass(const RevChainParams& p, float* dh_save
     for (int e = 0; e < 32; ++e) t[e] = to_tf32(s[32 * half + e]);
     tmem_st32(tl + kTDT + k0 + 32 * half, t);
   }
+  if (use_do) {
+    float df[32];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      df[2 * i] = __uint_as_float(d[i] << 16);
+      df[2 * i + 1] = __uint_as_float(d[i] & 0xffff0000u);
+    }
+    tmem_st32(tl + kTDO + t0, df);
+  }
+  tmem_wait_st();
+  tc_fence_before();
+  mbar_arrive(ready);
   if (p.kda) {
     const float4* gam = reinterpret_cast<const float4*>(p.gam + tile * kD + k0);
 #pragma unroll
@@ -89,18 +103,9 @@ __device__ __forceinline__ void rev_pass(const RevChainParams& p, float* dh_save
   }
   tmem_st32(tl + kTDM + k0, s);
   tmem_st32(tl + kTDM + k0 + 32, s + 32);
-  if (use_do) {
-    float df[32];
-#pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      df[2 * i] = __uint_as_float(d[i] << 16);
-      df[2 * i + 1] = __uint_as_float(d[i] & 0xffff0000u);
-    }
-    tmem_st32(tl + kTDO + t0, df);
-  }
   tmem_wait_st();
   tc_fence_before();
-  mbar_arrive(ready);
+  mbar_arrive(mready);
   if (!dh_save) return;
   // re-read the tf32 copy (the MMAs only read it) and save it
   tmem_ld64(tl + kTDT + k0, s);
@@ -118,7 +123,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const __grid_constant__ CUtensorMap mdO, const RevChainParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = align1k(smem_raw);
-  __shared__ uint64_t full[2], mma1, mma2, dready, vready;
+  __shared__ uint64_t full[2], mma1, mma2, dready, mready, vready;
   __shared__ uint32_t tslot;
   __shared__ int abort_flag;
 
@@ -147,6 +152,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&mma1, 1);
     mbar_init(&mma2, 1);
     mbar_init(&dready, kChainThreads);
+    mbar_init(&mready, kChainThreads);
     mbar_init(&vready, kChainThreads);
     fence_mbar_init();
   }
@@ -170,9 +176,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           tma_load_2d(base + kOffWT + pp * 16384, &mWT, pp * 32, y128, &full[st]);
         }
       };
-      // dO rows of a chunk into L2 ahead of the chain warps' loads of them
+      // dO rows of a chunk into L2 ahead of the chain warps' loads of them (a sequence's chunks
+      // are consecutive 64-token runs, so the row follows from the last chunk's, read once)
+      const int row_last = p.chunks[last].x;
       auto prefetch_do = [&](int c) {
-        const int row = p.chunks[c].x;
+        const int row = row_last - kC * (last - c);
         prefetch_l2_tile(&mdO, h * kD, row);
         prefetch_l2_tile(&mdO, h * kD + 64, row);
       };
@@ -194,7 +202,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int s = 0; s < 16; ++s)
           mma_tf32_ts(tb + kTDV, tb + kTDT + s * 8, desc_kmajor(base + kOffKt, 8192, s), id64, use_do || s > 0);
         mma_commit(&mma1);
-        // dS^T += dO^T Qt   (master copy already holds gam dS'^T)
+        // dS^T += dO^T Qt, once the master copy holds gam dS'^T
+        if (!mbar_wait(&mready, par, &abort_flag, p.status, kDevTimeoutSync)) break;
+        tc_fence_after();
         if (use_do)
           for (int s = 0; s < 8; ++s) mma_tf32_ts(tb + kTDM, tb + kTDO + s * 8, desc_kmajor(base + kOffQtT, 16384, s), id128, true);
         if (!mbar_wait(&vready, par, &abort_flag, p.status, kDevTimeoutSync)) break;
@@ -231,7 +241,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // dO of the chunk after the one being prepared is loaded a whole step ahead of its use
     uint32_t dnext[16];
     if (use_do) load_dO(p, last, h, v, t0, dnext);
-    rev_pass(p, dh_save, use_do, last, h, v, k0, t0, tl, &dready, dnext,
+    rev_pass(p, dh_save, use_do, last, h, v, k0, t0, tl, &dready, &mready, dnext,
              p.kda ? 0.f : p.gam[(size_t(last) * H + h) * kD]);
     if (use_do && nc > 1) load_dO(p, last - 1, h, v, t0, dnext);
     bool alive = true;
@@ -262,7 +272,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!mbar_wait(&mma2, par, &abort_flag, p.status, kDevTimeoutMma)) { alive = false; break; }
       tc_fence_after();
       if (j + 1 < nc) {
-        rev_pass(p, dh_save, use_do, c - 1, h, v, k0, t0, tl, &dready, dnext, gnext, j);
+        rev_pass(p, dh_save, use_do, c - 1, h, v, k0, t0, tl, &dready, &mready, dnext, gnext);
         if (use_do && j + 2 < nc) load_dO(p, c - 2, h, v, t0, dnext);
       }
     }
