@@ -61,10 +61,18 @@ TF32_OVER_BF16 = 1.1 / 2.25    # nominal dense tf32 / bf16 tensor rates of a GB3
 KERNEL_SOURCES = {"prepare": "k_prep.cu", "chain_fwd": "k_chain.cu", "chain_bwd": "k_chain_bwd.cu",
                   "bwd_feat": "k_bwd_feat.cu", "bwd_tok": "k_bwd_tok.cu", "compose": "k_scan.cu"}
 # DRAM bytes (read + write) of one step's launches of a kernel from an ncu capture of
-# dram__bytes_read.sum and dram__bytes_write.sum: (kernel, workload) -> (bytes, the first 16
-# hex digits of the SHA-256 of the kernel's source file when captured). Reported only while
-# the source is unchanged; null otherwise.
-NCU_TRAFFIC_BYTES = {}
+# dram__bytes_read.sum and dram__bytes_write.sum: (kernel, workload) -> (bytes, source_hash()
+# of the kernel when captured). Reported only while the source is unchanged; null otherwise.
+# Captured on the B=2 T=4096 H=16 step (2048 chunk-heads); the B=1 T=32768 H=16 entries are
+# those bytes x 4 (8192 chunk-heads): the chunk kernels' traffic is per chunk-head.
+NCU_TRAFFIC_BYTES = {
+    ("prepare", "gdn_b2_t4096_h16"): (615_680_512, "abe6436cd7b863e8"),
+    ("bwd_feat", "gdn_b2_t4096_h16"): (767_980_800, "c0427530ea5dfa2f"),
+    ("bwd_tok", "gdn_b2_t4096_h16"): (731_747_072, "eaa9833b4a0b268a"),
+    ("prepare", "gdn_b1_t32768_h16"): (4 * 615_680_512, "abe6436cd7b863e8"),
+    ("bwd_feat", "gdn_b1_t32768_h16"): (4 * 767_980_800, "c0427530ea5dfa2f"),
+    ("bwd_tok", "gdn_b1_t32768_h16"): (4 * 731_747_072, "eaa9833b4a0b268a"),
+}
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
@@ -85,15 +93,19 @@ def job_throughput(units_per_rank: float, world: int, ms: float) -> float:
 
 
 def source_hash(kernel: str):
+    """First 16 hex digits of the SHA-256 of the kernel's source file and the headers every
+    kernel includes (common.cuh, umma.cuh), or None."""
     name = KERNEL_SOURCES.get(kernel)
     if name is None:
         return None
-    path = os.path.join(ROOT, "chunked_gated_delta_05_gb300", "csrc", name)
-    try:
-        with open(path, "rb") as f:
-            return hashlib.sha256(f.read()).hexdigest()[:16]
-    except OSError:
-        return None
+    h = hashlib.sha256()
+    for part in (name, "common.cuh", "umma.cuh"):
+        try:
+            with open(os.path.join(ROOT, "chunked_gated_delta_05_gb300", "csrc", part), "rb") as f:
+                h.update(f.read())
+        except OSError:
+            return None
+    return h.hexdigest()[:16]
 
 
 def ncu_traffic(kernel: str, workload: str):
@@ -512,6 +524,37 @@ def measure_forward_target(dev, peaks, iters=20):
                       "with the library's timing hook"}
 
 
+def run_forward_only(runner, args, peaks, rank):
+    """The inference forward alone (no saves): K calls per timed region, repeated as in the
+    training-step measurement; prints one JSON line."""
+    w = runner.w
+    d = runner.d
+
+    def fwd_steps(n):
+        for _ in range(n):
+            runner.fwd_fn(d["q"], d["k"], d["v"], d["g"], d["beta"], initial_state=d["h0"],
+                          output_final_state=True, status=runner.status, **runner.kw)
+
+    fwd_steps(args.warmup)
+    runner.torch.cuda.synchronize(runner.dev)
+    per_step = runner.timed_regions(args.steps, args.min_seconds, fwd_steps)
+    runner.check_status("during the forward-only region")
+    ms = statistics.median(per_step)
+    flop = FWD_FLOP_PER_TOKEN_HEAD * runner.tokens * w.H
+    gate = "kda" if w.per_channel else "gdn"
+    io = IO_BYTES_PER_TOKEN_HEAD[(gate, "fwd")] * runner.tokens * w.H
+    line = {"metric": "forward (inference) tokens/s", "value": job_throughput(runner.tokens, runner.world, ms),
+            "unit": "tokens/s", "n_gpus": runner.world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16 io, bf16/tf32 mma, fp32 accumulate", "data": "synthetic",
+            "config": {"workload": w.name, "B": w.B, "T": w.T, "H": w.H, "mode": "inference forward"},
+            "tflops": flop / (ms * 1e-3) / 1e12 * runner.world,
+            "pct_of_bf16_burst_peak": flop / (ms * 1e-3) / 1e12 / peaks["bf16_tflops"],
+            "io_gbs": io / (ms * 1e-3) / 1e9, "timing": {"repeats": len(per_step)}}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -524,6 +567,8 @@ def main():
     ap.add_argument("--reference-tokens", type=int, default=256)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-extras", action="store_true", help="headline workload only")
+    ap.add_argument("--forward-only", action="store_true",
+                    help="time the inference forward (no saves, no backward) of the workload instead")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     rank = int(os.environ.get("RANK", "0"))
@@ -549,6 +594,11 @@ def main():
     peaks, peak_src = load_peaks()
     w = synth.WORKLOADS[args.workload]
     runner = Runner(w, dev, world, barrier)
+    if args.forward_only:
+        run_forward_only(runner, args, peaks, rank)
+        if world > 1:
+            dist.destroy_process_group()
+        return
     sampler = ClockSampler(local_rank)
     runner.warmup(args.warmup)
     sampler.start()
