@@ -73,6 +73,7 @@ SIGNATURES = {
     "gdn_fwd_noalloc_capacity": ([], c_size_t),
     "gdn_set_chain_segment": ([c_int], c_int),
     "gdn_chain_plan": ([ctypes.POINTER(Desc), ctypes.POINTER(c_int), ctypes.POINTER(c_int)], c_int),
+    "gdn_set_head_groups": ([c_int], c_int),
     "gdn_conv_fwd_workspace_size": ([ctypes.POINTER(ConvDesc)], c_size_t),
     "gdn_conv_bwd_workspace_size": ([ctypes.POINTER(ConvDesc)], c_size_t),
     "gdn_conv_fwd": ([ctypes.POINTER(ConvDesc), ctypes.POINTER(ConvFwdArgs), c_void_p], c_int),

@@ -431,8 +431,82 @@ SegPlan seg_plan(const ScanPlan& sc, char* base, size_t E, size_t Phi, size_t Pl
   return sp;
 }
 
-// Compose step between the two chain passes (sequences with three or more segments).
-int run_compose(const Problem& P, const SeqEntry* seqs, const SegPlan& sp, int* status, cudaStream_t s) {
+// ------------------------------------------------------------------ head groups
+// A large problem splits its heads into two groups: the first runs on the caller's stream, the
+// second on a stream the library keeps per device, forked after the work already enqueued on
+// the caller's stream and joined back into it before the call returns, so the call keeps its
+// single-stream ordering. The two groups' kernels share the SMs, and the low-occupancy phases
+// of one group (the chain's second pass, the compose step) overlap the other group's work.
+// Every kernel computes each head independently, so the results do not depend on the grouping.
+int g_head_groups = 0;  // forced number of groups (1 or 2), 0 = automatic
+constexpr int kMaxDevices = 64;
+struct SideStream {
+  cudaStream_t s = nullptr;
+  cudaEvent_t fork = nullptr, join = nullptr;
+};
+std::mutex g_side_mu;
+SideStream g_side[kMaxDevices];
+
+// Automatic choice, from GB300 measurements of both forms on the benchmark workloads: the
+// backward gains from 1024 chunk-heads on, the forward from 4096 (below that its prepare and
+// chain passes already fill the GPU and the split only adds launches).
+int wanted_groups(const Problem& P, bool backward) {
+  if (g_head_groups > 0) return std::min(std::min(g_head_groups, 2), P.H);
+  const size_t chunk_heads = size_t(P.NC) * P.H;
+  return (P.H >= 8 && chunk_heads >= (backward ? 1024u : 4096u)) ? 2 : 1;
+}
+
+class HeadGroups {
+ public:
+  HeadGroups(const Problem& P, bool backward, cudaStream_t s) : s_(s), H_(P.H), n_(wanted_groups(P, backward)) {
+    if (n_ < 2) return;
+    lock_ = std::unique_lock<std::mutex>(g_side_mu);
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+      n_ = 1;
+      return;
+    }
+    SideStream& ss = g_side[dev];
+    if (!ss.s) {
+      if (cudaStreamCreateWithFlags(&ss.s, cudaStreamNonBlocking) != cudaSuccess ||
+          cudaEventCreateWithFlags(&ss.fork, cudaEventDisableTiming) != cudaSuccess ||
+          cudaEventCreateWithFlags(&ss.join, cudaEventDisableTiming) != cudaSuccess) {
+        n_ = 1;
+        return;
+      }
+    }
+    if (cudaEventRecord(ss.fork, s) != cudaSuccess || cudaStreamWaitEvent(ss.s, ss.fork, 0) != cudaSuccess) {
+      n_ = 1;
+      return;
+    }
+    side_ = &ss;
+  }
+  ~HeadGroups() { join(); }
+  int count() const { return n_; }
+  int first(int g) const { return n_ == 1 ? 0 : (g == 0 ? 0 : H_ / 2); }
+  int heads(int g) const { return n_ == 1 ? H_ : (g == 0 ? H_ / 2 : H_ - H_ / 2); }
+  cudaStream_t stream(int g) const { return g == 0 ? s_ : side_->s; }
+  // The caller's stream waits for the second group (idempotent).
+  int join() {
+    if (!side_) return GDN_OK;
+    SideStream* ss = side_;
+    side_ = nullptr;
+    if (cudaEventRecord(ss->join, ss->s) != cudaSuccess || cudaStreamWaitEvent(s_, ss->join, 0) != cudaSuccess)
+      return fail(GDN_ECUDA, "joining the head-group stream failed");
+    return GDN_OK;
+  }
+
+ private:
+  cudaStream_t s_;
+  int H_, n_;
+  SideStream* side_ = nullptr;
+  std::unique_lock<std::mutex> lock_;
+};
+
+// Compose step between the two chain passes (sequences with three or more segments), for the
+// heads hg0 .. hg0 + hgn - 1.
+int run_compose(const Problem& P, const SeqEntry* seqs, const SegPlan& sp, int* status, int hg0, int hgn,
+                cudaStream_t s) {
   const uint64_t rows = uint64_t(P.N) * sp.maxS * P.H * kD;
   CUtensorMap mPhi, mPlo, mB;
   if (!tile_map(&mPhi, reinterpret_cast<const char*>(sp.Phi), kD, rows, 128, true) ||
@@ -443,6 +517,8 @@ int run_compose(const Problem& P, const SeqEntry* seqs, const SegPlan& sp, int* 
   cp.seqs = seqs;
   cp.N = P.N;
   cp.H = P.H;
+  cp.hg0 = hg0;
+  cp.hgn = hgn;
   cp.sp = sp;
   cp.status = status;
   TimedLaunch tl_(kKCompose, s);
@@ -453,7 +529,7 @@ int run_compose(const Problem& P, const SeqEntry* seqs, const SegPlan& sp, int* 
 int run_chain_fwd(const Problem& P, const Maps& M, ChainParams cp, cudaStream_t s) {
   for (int pass = 0; pass < (cp.sp.maxS > 1 ? 2 : 1); ++pass) {
     if (pass == 1 && cp.sp.maxS >= 3) {
-      int rc = run_compose(P, cp.seqs, cp.sp, cp.status, s);
+      int rc = run_compose(P, cp.seqs, cp.sp, cp.status, cp.hg0, cp.hgn, s);
       if (rc) return rc;
     }
     cp.sp.pass = pass;
@@ -468,7 +544,7 @@ int run_chain_fwd(const Problem& P, const Maps& M, ChainParams cp, cudaStream_t 
 int run_chain_bwd(const Problem& P, const Maps& M, RevChainParams rp, cudaStream_t s) {
   for (int pass = 0; pass < (rp.sp.maxS > 1 ? 2 : 1); ++pass) {
     if (pass == 1 && rp.sp.maxS >= 3) {
-      int rc = run_compose(P, rp.seqs, rp.sp, rp.status, s);
+      int rc = run_compose(P, rp.seqs, rp.sp, rp.status, rp.hg0, rp.hgn, s);
       if (rc) return rc;
     }
     rp.sp.pass = pass;
@@ -515,15 +591,7 @@ int run_fwd(const gdn_desc_t* d, const gdn_fwd_args_t* a, void* stream, bool kda
   if (rc) return rc;
   Maps M;
   if (!fwd_maps(P, a->q, a->k, a->v, ws, L, &M)) return fail(GDN_ECUDA, "cuTensorMapEncodeTiled failed");
-  const PrepParams pp = prep_params(d, P, ws, L, a->g, a->beta, training, a->status, a->A_log, a->dt_bias);
-  {
-    TimedLaunch tl_(kKPrep, s);
-    rc = check_cuda(kda ? launch_prep_kda(M.q, M.k, M.v, pp, s)
-                        : launch_prep_gdn(M.q, M.k, M.v, M.Qt, training ? M.Kt : M.Qt, M.Aqk, M.W, M.Usw, pp, s),
-                    "prepare kernel");
-  }
-  if (rc) return rc;
-
+  PrepParams pp = prep_params(d, P, ws, L, a->g, a->beta, training, a->status, a->A_log, a->dt_bias);
   ChainParams cp{};
   cp.seqs = reinterpret_cast<const SeqEntry*>(ws + L.seqs);
   cp.chunks = pp.chunks;
@@ -540,7 +608,22 @@ int run_fwd(const gdn_desc_t* d, const gdn_fwd_args_t* a, void* stream, bool kda
   }
   cp.status = a->status;
   cp.sp = seg_plan(L.plan, ws, L.fE, L.fPhi, L.fPlo, L.fB);
-  return run_chain_fwd(P, M, cp, s);
+  HeadGroups groups(P, false, s);
+  for (int g = 0; g < groups.count(); ++g) {
+    const cudaStream_t sg = groups.stream(g);
+    pp.hg0 = cp.hg0 = groups.first(g);
+    pp.hgn = cp.hgn = groups.heads(g);
+    {
+      TimedLaunch tl_(kKPrep, sg);
+      rc = check_cuda(kda ? launch_prep_kda(M.q, M.k, M.v, pp, sg)
+                          : launch_prep_gdn(M.q, M.k, M.v, M.Qt, training ? M.Kt : M.Qt, M.Aqk, M.W, M.Usw, pp, sg),
+                      "prepare kernel");
+    }
+    if (rc) return rc;
+    rc = run_chain_fwd(P, M, cp, sg);
+    if (rc) return rc;
+  }
+  return groups.join();
 }
 
 int run_bwd(const gdn_desc_t* d, const gdn_bwd_args_t* a, void* stream, bool kda) {
@@ -588,6 +671,8 @@ int run_bwd(const gdn_desc_t* d, const gdn_bwd_args_t* a, void* stream, bool kda
   auto F = [&](size_t off) { return reinterpret_cast<float*>(sv + off); };
   auto R = [&](size_t off) { return reinterpret_cast<float*>(rs + off); };
   const ChunkEntry* chunks = reinterpret_cast<const ChunkEntry*>(sv + L.chunks);
+  PrepParams pp{};
+  ChainParams cp{};
   if (have_saved) {
     // the forward already built the tables and saved its intermediates; reset the status word
     if (a->status) {
@@ -597,15 +682,7 @@ int run_bwd(const gdn_desc_t* d, const gdn_bwd_args_t* a, void* stream, bool kda
   } else {
     rc = build_tables(P, sv, L, a->status, s);
     if (rc) return rc;
-    const PrepParams pp = prep_params(d, P, sv, L, a->g, a->beta, true, a->status, a->A_log, a->dt_bias);
-    {
-      TimedLaunch tl_(kKPrep, s);
-      rc = check_cuda(kda ? launch_prep_kda(M.q, M.k, M.v, pp, s)
-                          : launch_prep_gdn(M.q, M.k, M.v, M.Qt, M.Kt, M.Aqk, M.W, M.Usw, pp, s),
-                      "prepare kernel");
-    }
-    if (rc) return rc;
-    ChainParams cp{};
+    pp = prep_params(d, P, sv, L, a->g, a->beta, true, a->status, a->A_log, a->dt_bias);
     cp.seqs = reinterpret_cast<const SeqEntry*>(sv + L.seqs);
     cp.chunks = chunks;
     cp.kda = kda ? 1 : 0;
@@ -617,8 +694,6 @@ int run_bwd(const gdn_desc_t* d, const gdn_bwd_args_t* a, void* stream, bool kda
     cp.vnew_save = F(L.vns);
     cp.status = a->status;
     cp.sp = seg_plan(L.plan, sv, L.fE, L.fPhi, L.fPlo, L.fB);
-    rc = run_chain_fwd(P, M, cp, s);
-    if (rc) return rc;
   }
 
   RevChainParams rp{};
@@ -635,8 +710,6 @@ int run_bwd(const gdn_desc_t* d, const gdn_bwd_args_t* a, void* stream, bool kda
   rp.dvn_save = R(L.dvns);
   rp.status = a->status;
   rp.sp = seg_plan(L.plan, rs, L.rE, L.rPhi, L.rPlo, L.rB);
-  rc = run_chain_bwd(P, M, rp, s);
-  if (rc) return rc;
 
   BwdFeatParams fp{};
   fp.chunks = chunks;
@@ -652,11 +725,6 @@ int run_bwd(const gdn_desc_t* d, const gdn_bwd_args_t* a, void* stream, bool kda
   fp.dgam = R(L.dgam);
   fp.sms = sm_count();
   fp.status = a->status;
-  {
-    TimedLaunch tl_(kKBwdFeat, s);
-    rc = check_cuda(launch_bwd_feat(M.VN, M.DVN, M.dO, M.Hs, M.DHs, fp, s), "feature-major backward kernel");
-  }
-  if (rc) return rc;
 
   BwdTokParams tp{};
   tp.chunks = chunks;
@@ -692,11 +760,40 @@ int run_bwd(const gdn_desc_t* d, const gdn_bwd_args_t* a, void* stream, bool kda
     tp.dq32 = R(L.dq32);
     tp.dk32 = R(L.dk32);
   }
+
   {
-    TimedLaunch tl_(kKBwdTok, s);
-    rc = check_cuda(kda ? launch_bwd_tok_kda(M.q, M.k, M.v, M.VN, M.DW, M.DVN, tp, s)
-                        : launch_bwd_tok(M.q, M.k, M.v, M.dO, M.VN, M.DW, M.DVN, tp, s),
-                    "token-major backward kernel");
+    HeadGroups groups(P, true, s);
+    for (int g = 0; g < groups.count(); ++g) {
+      const cudaStream_t sg = groups.stream(g);
+      pp.hg0 = cp.hg0 = rp.hg0 = fp.hg0 = tp.hg0 = groups.first(g);
+      pp.hgn = cp.hgn = rp.hgn = fp.hgn = tp.hgn = groups.heads(g);
+      if (!have_saved) {
+        {
+          TimedLaunch tl_(kKPrep, sg);
+          rc = check_cuda(kda ? launch_prep_kda(M.q, M.k, M.v, pp, sg)
+                              : launch_prep_gdn(M.q, M.k, M.v, M.Qt, M.Kt, M.Aqk, M.W, M.Usw, pp, sg),
+                          "prepare kernel");
+        }
+        if (rc) return rc;
+        rc = run_chain_fwd(P, M, cp, sg);
+        if (rc) return rc;
+      }
+      rc = run_chain_bwd(P, M, rp, sg);
+      if (rc) return rc;
+      {
+        TimedLaunch tl_(kKBwdFeat, sg);
+        rc = check_cuda(launch_bwd_feat(M.VN, M.DVN, M.dO, M.Hs, M.DHs, fp, sg), "feature-major backward kernel");
+      }
+      if (rc) return rc;
+      {
+        TimedLaunch tl_(kKBwdTok, sg);
+        rc = check_cuda(kda ? launch_bwd_tok_kda(M.q, M.k, M.v, M.VN, M.DW, M.DVN, tp, sg)
+                            : launch_bwd_tok(M.q, M.k, M.v, M.dO, M.VN, M.DW, M.DVN, tp, sg),
+                        "token-major backward kernel");
+      }
+      if (rc) return rc;
+    }
+    rc = groups.join();
   }
   if (rc) return rc;
   if (P.gate) {
@@ -809,6 +906,12 @@ size_t kda_bwd_workspace_size(const gdn_desc_t* desc) {
 int gdn_set_chain_segment(int chunks) {
   if (chunks < 0) return fail(GDN_EINVAL, "segment length must be >= 0");
   g_chain_segment = chunks;
+  return GDN_OK;
+}
+
+int gdn_set_head_groups(int groups) {
+  if (groups < 0 || groups > 2) return fail(GDN_EINVAL, "head groups must be 0 (automatic), 1 or 2");
+  g_head_groups = groups;
   return GDN_OK;
 }
 

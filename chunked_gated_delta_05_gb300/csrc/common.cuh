@@ -92,6 +92,7 @@ __host__ __device__ inline bool decode_run(int slot, int pass, int ns, int* seg,
 struct PrepParams {
   const ChunkEntry* chunks;
   int NC, H;
+  int hg0, hgn;                // head group: heads hg0 .. hg0 + hgn - 1 (grid.y = hgn)
   const float* g;              // GDN [R,H]; KDA [R,H,K]
   const __nv_bfloat16* beta;   // [R,H]
   float scale;
@@ -118,6 +119,7 @@ struct RevChainParams {
   const SeqEntry* seqs;
   const ChunkEntry* chunks;
   int N, H;
+  int hg0, hgn;                // head group: heads hg0 .. hg0 + hgn - 1 (grid.y = hgn)
   int kda;
   SegPlan sp;
   const float* gam;            // [NC,H,128]
@@ -133,6 +135,7 @@ struct ChainParams {
   const SeqEntry* seqs;
   const ChunkEntry* chunks;
   int N, H;
+  int hg0, hgn;                // head group: heads hg0 .. hg0 + hgn - 1 (grid.y = hgn)
   int kda;
   SegPlan sp;
   const float* gam;
@@ -160,6 +163,7 @@ struct UploadParams {
 struct BwdFeatParams {
   const ChunkEntry* chunks;
   int NC, H, kda;
+  int hg0, hgn;                // head group: heads hg0 .. hg0 + hgn - 1 (grid.y = hgn)
   const float* h;              // [NC,H,K,V] state entering each chunk
   const float* dh;             // [NC,H,K,V] gradient w.r.t. the state leaving each chunk
   const __nv_bfloat16* dO;     // [R,H,V]
@@ -174,6 +178,7 @@ struct BwdFeatParams {
 struct BwdTokParams {
   const ChunkEntry* chunks;
   int NC, H, kda;
+  int hg0, hgn;                // head group: heads hg0 .. hg0 + hgn - 1 (grid.y = hgn)
   float scale;
   int beta_sigmoid, l2norm;
   const __nv_bfloat16* dO;     // [R,H,V]
@@ -242,6 +247,7 @@ struct GroupSumParams {
 struct ComposeParams {
   const SeqEntry* seqs;
   int N, H;
+  int hg0, hgn;                // head group: heads hg0 .. hg0 + hgn - 1 (grid.y = hgn)
   SegPlan sp;
   int* status;
 };

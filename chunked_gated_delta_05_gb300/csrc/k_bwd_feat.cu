@@ -56,7 +56,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __shared__ float s_dg[kThreads];
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int c = blockIdx.x, h = blockIdx.y, H = p.H;
+  const int c = blockIdx.x, h = blockIdx.y + p.hg0, H = p.H;
   const size_t tile = size_t(c) * H + h;
   const int f = tid & 127, hf = tid >> 7;  // feature (TMEM lane) and column half
   const ChunkEntry ch = p.chunks[c];  // requested first: the dO load below waits on it
@@ -160,7 +160,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // while the products run: the next wave's CTA finds its inputs in L2
     int nx, ny;
     if (next_wave_block(p.sms, &nx, &ny)) {
-      const size_t nt = size_t(nx) * H + ny;
+      const size_t nt = size_t(nx) * H + ny + p.hg0;
       prefetch_l2(p.h + nt * kD * kD, 4u * kD * kD);
       prefetch_l2(p.dh + nt * kD * kD, 4u * kD * kD);
       prefetch_l2(p.A + nt * kTileAqk, 4u * kTileAqk);
@@ -263,7 +263,7 @@ cudaError_t launch_bwd_feat(const CUtensorMap& mVN, const CUtensorMap& mDVN, con
     if (e != cudaSuccess) return e;
     attr = true;
   }
-  dim3 grid(p.NC, p.H);
+  dim3 grid(p.NC, p.hgn);
   k_bwd_feat<<<grid, kThreads, kSmemBytes, s>>>(mVN, mDVN, mdO, mH, mDH, p);
   return cudaGetLastError();
 }

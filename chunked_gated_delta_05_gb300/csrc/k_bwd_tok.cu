@@ -77,7 +77,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __shared__ float s_G[kC], s_G2[kC], s_rq[kC], s_rk[kC], s_b[kC], s_dG[kC], s_db[kC], s_P[kC][kC + 1];
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int c = blockIdx.x, h = blockIdx.y, H = p.H;
+  const int c = blockIdx.x, h = blockIdx.y + p.hg0, H = p.H;
   const size_t tile = size_t(c) * H + h;
   const ChunkEntry ch = p.chunks[c];
   const int len = ch.y;
@@ -574,7 +574,7 @@ cudaError_t launch_bwd_tok(const CUtensorMap& mq, const CUtensorMap& mk, const C
     if (e != cudaSuccess) return e;
     attr = true;
   }
-  dim3 grid(p.NC, p.H);
+  dim3 grid(p.NC, p.hgn);
   k_bwd_tok<<<grid, kThreads, kSmemBytes, s>>>(mq, mk, mv, mdO, mVN, mDW, mDVN, p);
   return cudaGetLastError();
 }

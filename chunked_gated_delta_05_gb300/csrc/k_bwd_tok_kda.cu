@@ -164,7 +164,7 @@ __device__ __forceinline__ void kda_pair_block(int I, const float* __restrict__ 
     float part = kb[r] * x1[r];
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) part += __shfl_xor_sync(0xffffffffu, part, off);
-    if (lane == 0) atomicAdd(&s_db[t], part);
+    if (lane == 0) s_db[t] = part;  // this warp's channel group's share (summed in a fixed order later)
   }
 }
 
@@ -184,11 +184,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   __shared__ uint64_t bar_tma, bar_mma;
   __shared__ uint32_t tslot;
   __shared__ int abort_flag;
-  __shared__ float s_rq[kC], s_rk[kC], s_b[kC], s_db[kC], s_dotq[kC], s_dotk[kC], s_glast[2][kD];
+  __shared__ float s_rq[kC], s_rk[kC], s_b[kC], s_glast[2][kD];
+  // per-token sums over the channels, one partial per group of 32 channels (warp % 4), added in
+  // a fixed order so that the result does not depend on warp scheduling
+  __shared__ float s_dbp[4][kC], s_dba[4][kC], s_dotq[4][kC], s_dotk[4][kC];
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int wq = warp & 3, half = warp >> 2;
-  const int c_idx = blockIdx.x, h = blockIdx.y, H = p.H;
+  const int c_idx = blockIdx.x, h = blockIdx.y + p.hg0, H = p.H;
   const size_t tile = size_t(c_idx) * H + h;
   const ChunkEntry ch = p.chunks[c_idx];
   const int len = ch.y;
@@ -210,9 +213,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     s_rq[tid] = ok ? p.rq[tile * kC + tid] : 0.f;
     s_rk[tid] = ok ? p.rk[tile * kC + tid] : 0.f;
     s_b[tid] = ok ? p.beff[tile * kC + tid] : 0.f;
-    s_db[tid] = 0.f;
-    s_dotq[tid] = 0.f;
-    s_dotk[tid] = 0.f;
   }
   tc_fence_before();
   __syncthreads();
@@ -388,7 +388,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   float* sGacc = reinterpret_cast<float*>(sm + kR4);           // dG accumulator [64][128]
 #pragma unroll 1
   for (int b = 0; b < 2; ++b)
-    kda_pair_block(2 * half + b, sG2, sK, sQ, s_rk, s_rq, s_b, sD, sN, sKacc, sQacc, sGacc, s_db, cc, lane);
+    kda_pair_block(2 * half + b, sG2, sK, sQ, s_rk, s_rq, s_b, sD, sN, sKacc, sQacc, sGacc, s_dbp[warp & 3], cc, lane);
   __syncthreads();
   // ---- per-token assembly (thread: channel cc, rows of parity `half`)
   float glast_part = 0.f;
@@ -448,7 +448,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int k = 0; k < 3; ++k) {
         const int n = base + k, t = t0 + 2 * (n & 7);
-        if (t < len) atomicAdd((n < 8 ? s_db : (n < 16 ? s_dotq : s_dotk)) + t, y[k]);
+        if (t < len) (n < 8 ? s_dba : (n < 16 ? s_dotq : s_dotk))[warp & 3][t] = y[k];
       }
     }
   }
@@ -458,8 +458,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   for (int t = half; t < len; t += 2) {
     const float rq = s_rq[t], rk = s_rk[t];
     const float qh = rq * bf16_at(sQ, t, cc), kh = rk * bf16_at(sK, t, cc);
-    const float dq = p.l2norm ? rq * (sQacc[t * kD + cc] - qh * s_dotq[t]) : sQacc[t * kD + cc];
-    const float dk = p.l2norm ? rk * (sKacc[t * kD + cc] - kh * s_dotk[t]) : sKacc[t * kD + cc];
+    const float dotq = (s_dotq[0][t] + s_dotq[1][t]) + (s_dotq[2][t] + s_dotq[3][t]);
+    const float dotk = (s_dotk[0][t] + s_dotk[1][t]) + (s_dotk[2][t] + s_dotk[3][t]);
+    const float dq = p.l2norm ? rq * (sQacc[t * kD + cc] - qh * dotq) : sQacc[t * kD + cc];
+    const float dk = p.l2norm ? rk * (sKacc[t * kD + cc] - kh * dotk) : sKacc[t * kD + cc];
     if (p.dq32) {  // per value head, summed over the q/k group later
       const size_t o = (size_t(ch.x + t) * H + h) * kD + cc;
       p.dq32[o] = dq;
@@ -499,7 +501,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
   if (tid < len) {
-    float db = s_db[tid];
+    float db = ((s_dbp[0][tid] + s_dbp[1][tid]) + (s_dbp[2][tid] + s_dbp[3][tid])) +
+               ((s_dba[0][tid] + s_dba[1][tid]) + (s_dba[2][tid] + s_dba[3][tid]));
     if (p.beta_sigmoid) db *= s_b[tid] * (1.f - s_b[tid]);
     p.dbeta[size_t(ch.x + tid) * H + h] = __float2bfloat16_rn(db);
   }
@@ -517,7 +520,7 @@ cudaError_t launch_bwd_tok_kda(const CUtensorMap& mq, const CUtensorMap& mk, con
     if (e != cudaSuccess) return e;
     attr = true;
   }
-  dim3 grid(p.NC, p.H);
+  dim3 grid(p.NC, p.hgn);
   k_bwd_tok_kda<<<grid, kThreads, kSmemBytes, s>>>(mq, mk, mv, mVN, mDW, mDVN, p);
   return cudaGetLastError();
 }

@@ -112,7 +112,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __shared__ int abort_flag;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int h = blockIdx.y, H = p.H;
+  const int h = blockIdx.y + p.hg0, H = p.H;
   // which segment of which sequence, and how
   const SegPlan& sp = p.sp;
   const int runs = runs_per_seq(sp.maxS, sp.pass);
@@ -329,7 +329,7 @@ cudaError_t launch_chain_fwd(const CUtensorMap& mW, const CUtensorMap& mQt, cons
     if (e != cudaSuccess) return e;
     attr = true;
   }
-  dim3 grid(p.N * runs_per_seq(p.sp.maxS, p.sp.pass), p.H);
+  dim3 grid(p.N * runs_per_seq(p.sp.maxS, p.sp.pass), p.hgn);
   k_chain_fwd<<<grid, kThreads, kSmemBytes, s>>>(mW, mQt, mKtT, mAqk, mU, p);
   return cudaGetLastError();
 }

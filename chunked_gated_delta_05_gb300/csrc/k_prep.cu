@@ -76,7 +76,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __shared__ int4 s_chunk[2];
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int h = blockIdx.y, pair = blockIdx.x, H = p.H;
+  const int h = blockIdx.y + p.hg0, pair = blockIdx.x, H = p.H;
   // Row of the stacked tile (= TMEM lane) and column half of this thread.
   const int rt = tid & (kRows - 1), hf = tid >> 7;
   const int blk = rt >> 6, il = rt & 63;
@@ -390,7 +390,7 @@ cudaError_t launch_prep_gdn(const CUtensorMap& mq, const CUtensorMap& mk, const 
     if (e != cudaSuccess) return e;
     attr = true;
   }
-  dim3 grid((p.NC + 1) / 2, p.H);
+  dim3 grid((p.NC + 1) / 2, p.hgn);
   k_prep_gdn<<<grid, kThreads, kSmemBytes, s>>>(mq, mk, mv, mQt, mKt, mAqk, mW, mU, p);
   return cudaGetLastError();
 }

@@ -84,7 +84,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int hf = tid >> 7;     // which half of the block (rows or columns, per phase)
-  const int c_idx = blockIdx.x, h = blockIdx.y, H = p.H;
+  const int c_idx = blockIdx.x, h = blockIdx.y + p.hg0, H = p.H;
   const size_t tile = size_t(c_idx) * H + h;
   const ChunkEntry ch = p.chunks[c_idx];
   const int len = ch.y;
@@ -458,7 +458,7 @@ cudaError_t launch_prep_kda(const CUtensorMap& mq, const CUtensorMap& mk, const 
     if (e != cudaSuccess) return e;
     attr = true;
   }
-  dim3 grid(p.NC, p.H);
+  dim3 grid(p.NC, p.hgn);
   k_prep_kda<<<grid, kThreads, kSmemBytes, s>>>(mq, mk, mv, p);
   return cudaGetLastError();
 }

@@ -45,7 +45,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __shared__ int abort_flag;
 
   const int tid = threadIdx.x, warp = tid >> 5;
-  const int n = blockIdx.x, h = blockIdx.y, H = p.H;
+  const int n = blockIdx.x, h = blockIdx.y + p.hg0, H = p.H;
   const SegPlan& sp = p.sp;
   const int ns = (p.seqs[n].y + sp.L - 1) / sp.L;
   if (ns < 3) return;  // nothing between the fully-run first segment and pass 1
@@ -172,7 +172,7 @@ cudaError_t launch_compose(const CUtensorMap& mPhi, const CUtensorMap& mPlo, con
     if (e != cudaSuccess) return e;
     attr = true;
   }
-  dim3 grid(p.N, p.H);
+  dim3 grid(p.N, p.hgn);
   k_compose<<<grid, kThreads, kSmemBytes, s>>>(mPhi, mPlo, mB, p);
   return cudaGetLastError();
 }

@@ -190,6 +190,12 @@ def set_chain_segment(chunks: int) -> None:
     _lib.check(_lib.load().gdn_set_chain_segment(int(chunks)))
 
 
+def set_head_groups(groups: int) -> None:
+    """Force 1 or 2 head groups (the second on the library's side stream) for every later call
+    of the process; 0 restores the automatic choice. Results do not depend on it."""
+    _lib.check(_lib.load().gdn_set_head_groups(int(groups)))
+
+
 def chain_plan(B: int, T: int, H: int, cu_seqlens: Optional[Sequence[int]] = None):
     """``(chunks per segment, most segments of any sequence)`` the library picks for a shape."""
     offsets = _offsets(cu_seqlens, T)

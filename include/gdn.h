@@ -202,6 +202,18 @@ size_t gdn_fwd_noalloc_capacity(void);
 int gdn_set_chain_segment(int chunks);
 int gdn_chain_plan(const gdn_desc_t* desc, int* chunks_per_segment, int* max_segments);
 
+/* Head groups (no counterpart in the paper; a scheduling choice of this library). A problem
+ * with at least 8 heads and enough chunk-heads (chunks of all sequences x heads: 1024 for a
+ * backward, 4096 for a forward) splits its heads into two groups: the first group's
+ * kernels run on the caller's stream, the second group's on a stream that the library creates
+ * once per device, forked after the work already enqueued on the caller's stream and joined
+ * back into it before the call returns, so ordering on the caller's stream is unchanged. The
+ * two groups then share the GPU, and one group's low-occupancy phases overlap the other's work.
+ * Results are identical with and without the split (every head is computed independently).
+ * gdn_set_head_groups(n) forces n groups (1 or 2) for every later call of the process; 0
+ * restores the automatic choice. Process-global, not thread-safe; other values: GDN_EINVAL. */
+int gdn_set_head_groups(int groups);
+
 /* Short convolution ahead of the path: causal depthwise Conv1d over the token axis with
  * optional bias and SiLU, per packed document (hyper-parallel GDN Diff Coverage page,
  * `_causal_conv1d_with_cp_halo` and the packed ShortConv path, which produce q, k and v):
