@@ -8,16 +8,19 @@
 // (gam is exp(G_last): a scalar for GDN, one value per key row for KDA.)
 //
 // GB300 mapping: one CTA per (sequence, head). The state lives in TMEM, transposed: S^T
-// (V x K), lane v = column v of S, as an fp32 master copy plus a round-to-nearest tf32 copy
-// that the MMAs read as their TMEM-resident A operand (kind::tf32). The chunk tiles from the
-// prepare kernel are TMA-loaded SW128 B operands:
+// (V x K), lane v = column v of S, as one fp32 copy that the MMAs read as their TMEM-resident
+// A operand (kind::tf32, which reads the operand's upper 19 bits; a CPU emulation of the chunked
+// algorithm gives the same state and output errors as with a round-to-nearest copy). The chunk
+// tiles from the prepare kernel are TMA-loaded SW128 B operands:
 //   [P | O] = S^T [W; Qt]^T  (one N=128 product: P = S^T W^T, O = S^T Qt^T)  -- on the chain
+//   S^T   *= diag(gam)       (by the chain warps once the product has read S)
 //   v_new^T = U^T - P        (written over P in TMEM)
-//   S^T += v_new^T KtT^T     (master pre-decayed by gam)   -- on the serial chain
+//   S^T += v_new^T KtT^T                                   -- on the serial chain
 //   O   += v_new^T Aqk^T                                   -- off the chain, issued after
-// An MMA instruction costs about the same for N = 64 and N = 128, so stacking W and Qt into
-// one 128-row B operand gives the output's state product for free alongside P. P/v_new and O
-// are double-buffered in TMEM by chunk parity. Eight chain warps share the TMEM lanes (two
+// The issuing thread starts the next chunk's product as soon as the state update completes;
+// the chain warps decay the state and form v_new while that product's successor is prepared,
+// and copy the entry state out for the backward while the next product reads it. P/v_new and
+// O are double-buffered in TMEM by chunk parity. Eight chain warps share the TMEM lanes (two
 // threads per lane, each on half of the columns); warp 8 streams the tiles with TMA (KtT/Aqk
 // double-buffered) and issues the MMAs from one thread. All waits bounded.
 //
@@ -40,8 +43,8 @@ constexpr uint32_t kOffU = 65536;      // 4 panels x [64][32] fp32, no swizzle
 constexpr uint32_t kOffG3 = 98304;     // 2 stages x {KtT 32 KB (2 panels x 128 rows), Aqk 16 KB}
 constexpr uint32_t kG3Stage = 49152;
 constexpr uint32_t kSmemBytes = kOffG3 + 2 * kG3Stage + 1024;
-// TMEM columns: master, tf32 copy, then per chunk parity [P, later v_new | O]
-constexpr uint32_t kTSM = 0, kTST = 128, kTB = 256;
+// TMEM columns: the state, then per chunk parity [P, later v_new | O]
+constexpr uint32_t kTS = 0, kTB = 128;
 __device__ __forceinline__ uint32_t tpv(int j) { return kTB + uint32_t(j & 1) * 128; }
 __device__ __forceinline__ uint32_t tout(int j) { return kTB + uint32_t(j & 1) * 128 + 64; }
 
@@ -49,31 +52,27 @@ __device__ __forceinline__ uint8_t* align1k(uint8_t* p) {
   return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
 }
 
-// S pass for chunk c (one thread: lane v, state columns [k0, k0+64)): write the entry state's
-// tf32 copy (the MMA operand), pre-apply the chunk's end decay to the fp32 master copy (the
-// MMA then adds k~^T v_new in place), release the MMA issuer, and only then record the entry
-// state for the backward (the tf32 copy: every later use of it is a tf32 operand or a sum of
-// its products), so the global stores stay off the serial path.
-__device__ __forceinline__ void chain_state_pass(const ChainParams& p, float* h_save, int c, int h, int v,
-                                                 int k0, uint32_t tl, uint64_t* sready, float g0) {
+// Entry state of chunk c (this thread: lane v, state columns [k0, k0+64)) to the backward's
+// save; the state is only read here (the chunk's product may be reading it too).
+__device__ __forceinline__ void chain_save_state(const ChainParams& p, float* h_save, int c, int h, int v, int k0,
+                                                 uint32_t tl) {
   const size_t tile = size_t(c) * p.H + h;
   float s[64];
-  tmem_ld64(tl + kTSM + k0, s);
+  tmem_ld64(tl + kTS + k0, s);
   tmem_wait_ld_regs(s);
+  float* hs = h_save + tile * kD * kD + size_t(k0) * kD + v;
 #pragma unroll
-  for (int half = 0; half < 2; ++half) {
-    float t[32];
-#pragma unroll
-    for (int e = 0; e < 32; ++e) t[e] = to_tf32(s[32 * half + e]);
-    tmem_st32(tl + kTST + k0 + 32 * half, t);
-  }
-  tmem_wait_st();
-  tc_fence_before();
-  mbar_arrive(sready);  // the next W S product reads only the tf32 copy
-  // Decay the master for the coming state update; that MMA goes out after this thread's next
-  // arrival on the v_new barrier, which follows these stores.
+  for (int e = 0; e < 64; ++e) hs[size_t(e) * kD] = s[e];
+}
+
+// Decay of the state by chunk c's end decay (gam), in place, once the chunk's product has read
+// the state; the state update then adds k~^T v_new to it.
+__device__ __forceinline__ void chain_decay(const ChainParams& p, int c, int h, int k0, uint32_t tl, float g0) {
+  float s[64];
+  tmem_ld64(tl + kTS + k0, s);
+  tmem_wait_ld_regs(s);
   if (p.kda) {
-    const float4* gam = reinterpret_cast<const float4*>(p.gam + tile * kD + k0);
+    const float4* gam = reinterpret_cast<const float4*>(p.gam + (size_t(c) * p.H + h) * kD + k0);
 #pragma unroll
     for (int e = 0; e < 16; ++e) {
       const float4 g4 = gam[e];
@@ -86,17 +85,8 @@ __device__ __forceinline__ void chain_state_pass(const ChainParams& p, float* h_
 #pragma unroll
     for (int e = 0; e < 64; ++e) s[e] *= g0;
   }
-  tmem_st32(tl + kTSM + k0, s);
-  tmem_st32(tl + kTSM + k0 + 32, s + 32);
-  tmem_wait_st();
-  if (h_save) {
-    // re-read the tf32 copy (the MMAs only read it) and store it
-    tmem_ld64(tl + kTST + k0, s);
-    tmem_wait_ld_regs(s);
-    float* hs = h_save + tile * kD * kD + size_t(k0) * kD + v;
-#pragma unroll
-    for (int e = 0; e < 64; ++e) hs[size_t(e) * kD] = s[e];
-  }
+  tmem_st32(tl + kTS + k0, s);
+  tmem_st32(tl + kTS + k0 + 32, s + 32);
 }
 
 }  // namespace
@@ -176,29 +166,36 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (nc > 1) load_g3(first + 1, 1);
       const uint32_t id64 = idesc_tf32(128, 64), id128 = idesc_tf32(128, 128);
       const uint32_t id_first = outs ? id128 : id64;  // [P | O] or P alone
-      for (int j = 0; j < nc; ++j) {
+      // the chain warps have written the entry state
+      bool alive = mbar_wait(&sready, 0, &abort_flag, p.status, kDevTimeoutSync);
+      for (int j = 0; j < nc && alive; ++j) {
         const uint32_t par = j & 1;
         const int c = first + j, st = j & 1;
         const uint32_t tPV = tb + tpv(j), tO = tb + tout(j);
         const uint32_t sKtT = smem_u32(sm + kOffG3 + st * kG3Stage), sAqk = sKtT + 32768;
         if (!mbar_wait(&full1, par, &abort_flag, p.status, kDevTimeoutTma)) break;
-        if (!mbar_wait(&sready, par, &abort_flag, p.status, kDevTimeoutSync)) break;
         tc_fence_after();
-        for (int s = 0; s < 16; ++s) mma_tf32_ts(tPV, tb + kTST + s * 8, desc_kmajor(sWQ, 16384, s), id_first, s > 0);
+        for (int s = 0; s < 16; ++s) mma_tf32_ts(tPV, tb + kTS + s * 8, desc_kmajor(sWQ, 16384, s), id_first, s > 0);
         mma_commit(&mma1);
+        // the previous chunk's output product has read its KtT / Aqk stage: refill it two chunks on
+        if (j > 0) {
+          if (!mbar_wait(&mma3, par ^ 1u, &abort_flag, p.status, kDevTimeoutMma)) break;
+          if (j + 1 < nc) load_g3(c + 1, st ^ 1);
+        }
         if (!mbar_wait(&mma1, par, &abort_flag, p.status, kDevTimeoutMma)) break;
         if (j + 1 < nc) load_g1(c + 1);
-        if (!mbar_wait(&vready, par, &abort_flag, p.status, kDevTimeoutSync)) break;
-        if (j + 1 < nc && use_u) load_g2(c + 1);
         if (!mbar_wait(&full3[st], (j >> 1) & 1, &abort_flag, p.status, kDevTimeoutTma)) break;
+        // the chain warps have decayed the state and written v_new
+        if (!mbar_wait(&vready, par, &abort_flag, p.status, kDevTimeoutSync)) break;
         tc_fence_after();
-        for (int s = 0; s < 8; ++s) mma_tf32_ts(tb + kTSM, tPV + s * 8, desc_kmajor(sKtT, 16384, s), id128, true);
+        for (int s = 0; s < 8; ++s) mma_tf32_ts(tb + kTS, tPV + s * 8, desc_kmajor(sKtT, 16384, s), id128, true);
         mma_commit(&mma2);
         if (outs)
           for (int s = 0; s < 8; ++s) mma_tf32_ts(tO, tPV + s * 8, desc_kmajor(sAqk, 8192, s), id64, true);
         mma_commit(&mma3);
-        if (!mbar_wait(&mma3, par, &abort_flag, p.status, kDevTimeoutMma)) break;
-        if (j + 2 < nc) load_g3(c + 2, st);
+        if (j + 1 < nc && use_u) load_g2(c + 1);  // the chain warps read U into registers before v_new
+        // the next chunk's product goes out as soon as the state update is complete
+        if (!mbar_wait(&mma2, par, &abort_flag, p.status, kDevTimeoutMma)) break;
       }
     }
   } else if (warp < kChainThreads / 32) {
@@ -221,34 +218,38 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int e = 0; e < 64; ++e)
         buf[e] = src ? src[size_t(e) * kD] : (mode == kRunMapM && k0 + e == v ? 1.f : 0.f);
-      tmem_st32(tb + lb + kTSM + k0, buf);
-      tmem_st32(tb + lb + kTSM + k0 + 32, buf + 32);
+      tmem_st32(tb + lb + kTS + k0, buf);
+      tmem_st32(tb + lb + kTS + k0 + 32, buf + 32);
       tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(&sready);
+      if (h_save) {
+        // the entry state of the first chunk, from the registers (identical to what was stored)
+        float* hs = h_save + (size_t(first) * H + h) * kD * kD + size_t(k0) * kD + v;
+#pragma unroll
+        for (int e = 0; e < 64; ++e) hs[size_t(e) * kD] = buf[e];
+      }
     }
-    chain_state_pass(p, h_save, first, h, v, k0, tb + lb, &sready,
-                     p.kda ? 0.f : p.gam[(size_t(first) * H + h) * kD]);
     bool alive = true;
+    float g_cur = p.kda ? 0.f : p.gam[(size_t(first) * H + h) * kD];
     for (int j = 0; j < nc; ++j) {
       const uint32_t par = j & 1;
       const int c = first + j;
       const ChunkEntry ch = p.chunks[c];
       const size_t tile = size_t(c) * H + h;
-      // next chunk's scalar gate, loaded early so the state pass does not wait for it
-      const float gnext = (j + 1 < nc && !p.kda) ? p.gam[(size_t(c + 1) * H + h) * kD] : 0.f;
-      float u[32];
-      if (use_u) {
-        if (!mbar_wait(&full2, par, &abort_flag, p.status, kDevTimeoutTma)) { alive = false; break; }
-#pragma unroll
-        for (int t = 0; t < 32; ++t) u[t] = sU[(v >> 5) * 2048 + (t0 + t) * 32 + (v & 31)];
-      } else {
-#pragma unroll
-        for (int t = 0; t < 32; ++t) u[t] = 0.f;
-      }
+      // next chunk's scalar gate, loaded a chunk ahead of its use
+      const float g_next = (j + 1 < nc && !p.kda) ? p.gam[(size_t(c + 1) * H + h) * kD] : 0.f;
+      if (use_u && !mbar_wait(&full2, par, &abort_flag, p.status, kDevTimeoutTma)) { alive = false; break; }
       if (!mbar_wait(&mma1, par, &abort_flag, p.status, kDevTimeoutMma)) { alive = false; break; }
       tc_fence_after();
+      // the product has read the state: decay it for the state update
+      chain_decay(p, c, h, k0, tb + lb, g_cur);
       {
         float r[32];
         tmem_ld32(tb + lb + tpv(j) + t0, r);
+        float u[32];
+#pragma unroll
+        for (int t = 0; t < 32; ++t) u[t] = use_u ? sU[(v >> 5) * 2048 + (t0 + t) * 32 + (v & 31)] : 0.f;
         tmem_wait_ld_regs(r);
 #pragma unroll
         for (int t = 0; t < 32; ++t) r[t] = to_tf32(u[t] - r[t]);
@@ -262,9 +263,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int t = 0; t < 32; ++t) vsave[size_t(t) * kD] = r[t];
         }
       }
+      g_cur = g_next;
       if (!mbar_wait(&mma2, par, &abort_flag, p.status, kDevTimeoutMma)) { alive = false; break; }
       tc_fence_after();
-      if (j + 1 < nc) chain_state_pass(p, h_save, c + 1, h, v, k0, tb + lb, &sready, gnext);
+      // the next chunk's entry state, read while its product reads it too
+      if (h_save && j + 1 < nc) chain_save_state(p, h_save, c + 1, h, v, k0, tb + lb);
       if (o) {
         if (!mbar_wait(&mma3, par, &abort_flag, p.status, kDevTimeoutMma)) { alive = false; break; }
         tc_fence_after();
@@ -299,7 +302,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (alive && dst) {  // the loop's last mma2 wait covers the final state update
       float s[64];
-      tmem_ld64(tb + lb + kTSM + k0, s);
+      tmem_ld64(tb + lb + kTS + k0, s);
       tmem_wait_ld_regs(s);
       const size_t off = size_t(k0) * kD + v;
       if (dst_lo) {
