@@ -246,35 +246,44 @@ def kda_bwd(q, k, v, g, beta, dO, *, dht=None, initial_state=None, use_qk_l2norm
 
 class ChunkGatedDeltaRule(torch.autograd.Function):
     """Autograd wrapper: forward through gdn_fwd/kda_fwd in save mode, backward through
-    gdn_bwd/kda_bwd with the saved intermediates."""
+    gdn_bwd/kda_bwd with the saved intermediates. With the KDA in-kernel gate, g holds the gate
+    logits and A_log, dt_bias receive gradients too."""
 
     @staticmethod
-    def forward(ctx, q, k, v, g, beta, initial_state, per_channel, use_qk_l2norm, use_beta_sigmoid,
-                cu_seqlens, scale, output_final_state):
+    def forward(ctx, q, k, v, g, beta, initial_state, A_log, dt_bias, per_channel, use_qk_l2norm,
+                use_beta_sigmoid, cu_seqlens, scale, output_final_state, lower_bound):
+        gate = None if A_log is None else (A_log, dt_bias, lower_bound)
         o, final, saved = _fwd(per_channel, q, k, v, g, beta, initial_state, output_final_state,
-                               use_qk_l2norm, use_beta_sigmoid, cu_seqlens, scale, None, save=True)
-        ctx.save_for_backward(q, k, v, g, beta, initial_state, saved)
-        ctx.cfg = (per_channel, use_qk_l2norm, use_beta_sigmoid, cu_seqlens, scale)
+                               use_qk_l2norm, use_beta_sigmoid, cu_seqlens, scale, None, save=True, gate=gate)
+        ctx.save_for_backward(q, k, v, g, beta, initial_state, A_log, dt_bias, saved)
+        ctx.cfg = (per_channel, use_qk_l2norm, use_beta_sigmoid, cu_seqlens, scale, lower_bound)
         return o, final
 
     @staticmethod
     def backward(ctx, dO, dfinal):
-        q, k, v, g, beta, h0, saved = ctx.saved_tensors
-        per_channel, l2, sig, cu, scale = ctx.cfg
-        dq, dk, dv, dbeta, dg, dh0 = _bwd(per_channel, q, k, v, g, beta, dO.contiguous(),
-                                          None if dfinal is None else dfinal.contiguous(), h0, l2, sig,
-                                          cu, scale, None, saved)
-        return dq, dk, dv, dg, dbeta, dh0, None, None, None, None, None, None
+        q, k, v, g, beta, h0, A_log, dt_bias, saved = ctx.saved_tensors
+        per_channel, l2, sig, cu, scale, lower_bound = ctx.cfg
+        gate = None if A_log is None else (A_log, dt_bias, lower_bound)
+        out = _bwd(per_channel, q, k, v, g, beta, dO.contiguous(), None if dfinal is None else dfinal.contiguous(),
+                   h0, l2, sig, cu, scale, None, saved, gate)
+        dq, dk, dv, dbeta, dg, dh0 = out[:6]
+        dA, ddt = (out[6], out[7]) if gate is not None else (None, None)
+        return dq, dk, dv, dg, dbeta, dh0, dA, ddt, None, None, None, None, None, None, None
 
 
 def chunk_gated_delta_rule(q, k, v, g, beta, *, initial_state=None, output_final_state=False,
-                           use_qk_l2norm=True, use_beta_sigmoid=None, cu_seqlens=None, scale=None):
-    """Differentiable entry point; the gate's rank selects GDN ([B,T,H]) or KDA ([B,T,H,K])."""
+                           use_qk_l2norm=True, use_beta_sigmoid=None, cu_seqlens=None, scale=None,
+                           A_log=None, dt_bias=None, lower_bound=None):
+    """Differentiable entry point; the gate's rank selects GDN ([B,T,H]) or KDA ([B,T,H,K]).
+    For KDA, ``A_log``, ``dt_bias`` and ``lower_bound`` select the in-kernel safe gate (g then
+    holds the gate logits; see :func:`kda_fwd`)."""
     per_channel = g.dim() == 4
     if use_beta_sigmoid is None:
         use_beta_sigmoid = per_channel
-    return ChunkGatedDeltaRule.apply(q, k, v, g, beta, initial_state, per_channel, use_qk_l2norm,
-                                     use_beta_sigmoid, cu_seqlens, scale, output_final_state)
+    if A_log is not None and not per_channel:
+        raise ValueError("the in-kernel gate is a KDA option (g must be [B,T,H,K])")
+    return ChunkGatedDeltaRule.apply(q, k, v, g, beta, initial_state, A_log, dt_bias, per_channel, use_qk_l2norm,
+                                     use_beta_sigmoid, cu_seqlens, scale, output_final_state, lower_bound)
 
 
 # ---------------------------------------------------------------- short convolution
