@@ -273,6 +273,7 @@ class Runner:
         self.status = torch.zeros(1, dtype=torch.int32, device=dev)
         self.stream = torch.cuda.current_stream(dev)
         self.tokens = w.B * w.T
+        self.head_groups = 0  # the library's setting for the timed steps (0: automatic)
 
     def step(self, inp):
         # training step: the forward saves its chunk intermediates, the backward consumes them
@@ -333,7 +334,7 @@ class Runner:
             t = _lib.timing_read()
             _lib.timing_enable(False)
         finally:
-            set_head_groups(0)
+            set_head_groups(self.head_groups)
         return t
 
     def e2e(self, steps, min_seconds):
@@ -514,6 +515,33 @@ def measure_forward_target(dev, peaks, iters=20):
         torch.cuda.synchronize(dev)
         times.append(e0.elapsed_time(e1))
     ms = statistics.median(times)
+    # the same calls captured in CUDA graphs (one per input set) and replayed: the device time of
+    # the forward without the call's host work
+    graphs = []
+    for dset in sets:
+        side = torch.cuda.Stream(dev)
+        side.wait_stream(stream)
+        with torch.cuda.stream(side):
+            fwd(dset)
+        stream.wait_stream(side)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            fwd(dset)
+        graphs.append(graph)
+    for i in range(4):
+        graphs[i % 2].replay()
+    torch.cuda.synchronize(dev)
+    gtimes = []
+    for i in range(iters):
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        graphs[i % 2].replay()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        gtimes.append(e0.elapsed_time(e1))
+    graph_ms = statistics.median(gtimes)
+    del graphs
     _lib.timing_enable(True)
     for i in range(iters):
         fwd(sets[i % 2])
@@ -523,7 +551,11 @@ def measure_forward_target(dev, peaks, iters=20):
     flop = FWD_FLOP_PER_TOKEN_HEAD * w.B * w.T * w.H
     tflops = flop / (ms * 1e-3) / 1e12
     io = IO_BYTES_PER_TOKEN_HEAD[("gdn", "fwd")] * w.B * w.T * w.H
+    gtflops = flop / (graph_ms * 1e-3) / 1e12
     return {"workload": w.name, "ms": ms, "tflops": tflops, "pct_of_bf16_peak": tflops / peaks["bf16_tflops"],
+            "graph_replay": {"ms": graph_ms, "tflops": gtflops, "pct_of_bf16_peak": gtflops / peaks["bf16_tflops"],
+                             "timing": "median of CUDA-event times around replays of the call captured in a "
+                                       "CUDA graph (no host work)"},
             "peak_kind": "bf16 burst (measured)", "io_gbs": io / (ms * 1e-3) / 1e9,
             "pct_of_hbm_io": io / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"],
             "kernels_ms": {k: v[0] / iters for k, v in t.items() if v[1]},
@@ -574,6 +606,8 @@ def main():
     ap.add_argument("--reference-tokens", type=int, default=256)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-extras", action="store_true", help="headline workload only")
+    ap.add_argument("--head-groups", type=int, default=0,
+                    help="force 1 or 2 head groups (0: the library's automatic choice)")
     ap.add_argument("--forward-only", action="store_true",
                     help="time the inference forward (no saves, no backward) of the workload instead")
     args = ap.parse_args()
@@ -599,8 +633,12 @@ def main():
             dist.barrier()
 
     peaks, peak_src = load_peaks()
+    if args.head_groups:
+        from chunked_gated_delta_05_gb300 import set_head_groups
+        set_head_groups(args.head_groups)
     w = synth.WORKLOADS[args.workload]
     runner = Runner(w, dev, world, barrier)
+    runner.head_groups = args.head_groups
     if args.forward_only:
         run_forward_only(runner, args, peaks, rank)
         if world > 1:
@@ -614,7 +652,7 @@ def main():
     head_e2e = runner.e2e(args.steps, args.min_seconds)
     per_kernel = runner.kernel_pass(args.steps)
     roofline = roofline_of(runner, per_kernel, args.steps, peaks, peak_src)
-    gpu_launches = sum(v[1] for v in runner.kernel_pass(args.steps, groups=0).values())
+    gpu_launches = sum(v[1] for v in runner.kernel_pass(args.steps, groups=args.head_groups).values())
     ms = head["ms_per_step"]
     if clocks.get("sm_mhz"):
         clocks["ms_x_median_sm_mhz"] = ms * clocks["sm_mhz"]
@@ -646,6 +684,7 @@ def main():
             if name == w.name:
                 continue
             r = Runner(synth.WORKLOADS[name], dev, world, barrier)
+            r.head_groups = args.head_groups
             works[name] = measure_workload(r, args, peaks)
             del r
             torch.cuda.empty_cache()
