@@ -60,19 +60,33 @@ TF32_OVER_BF16 = 1.1 / 2.25    # nominal dense tf32 / bf16 tensor rates of a GB3
 # Kernel name of the timing hook -> source file of that kernel.
 KERNEL_SOURCES = {"prepare": "k_prep.cu", "chain_fwd": "k_chain.cu", "chain_bwd": "k_chain_bwd.cu",
                   "bwd_feat": "k_bwd_feat.cu", "bwd_tok": "k_bwd_tok.cu", "compose": "k_scan.cu"}
+KERNEL_SOURCES_KDA = {**KERNEL_SOURCES, "prepare": "k_prep_kda.cu", "bwd_tok": "k_bwd_tok_kda.cu"}
 # DRAM bytes (read + write) of one step's launches of a kernel from an ncu capture of
 # dram__bytes_read.sum and dram__bytes_write.sum: (kernel, workload) -> (bytes, source_hash()
 # of the kernel when captured). Reported only while the source is unchanged; null otherwise.
-# Captured on the B=2 T=4096 H=16 step (2048 chunk-heads); the B=1 T=32768 H=16 entries are
-# those bytes x 4 (8192 chunk-heads): the chunk kernels' traffic is per chunk-head.
-NCU_TRAFFIC_BYTES = {
-    ("prepare", "gdn_b2_t4096_h16"): (615_680_512, "abe6436cd7b863e8"),
-    ("bwd_feat", "gdn_b2_t4096_h16"): (767_980_800, "c0427530ea5dfa2f"),
-    ("bwd_tok", "gdn_b2_t4096_h16"): (731_747_072, "eaa9833b4a0b268a"),
-    ("prepare", "gdn_b1_t32768_h16"): (4 * 615_680_512, "abe6436cd7b863e8"),
-    ("bwd_feat", "gdn_b1_t32768_h16"): (4 * 767_980_800, "c0427530ea5dfa2f"),
-    ("bwd_tok", "gdn_b1_t32768_h16"): (4 * 731_747_072, "eaa9833b4a0b268a"),
-}
+# Captured on the B=2 T=4096 H=16 GDN step and the B=1 T=4096 H=32 KDA step (2048 chunk-heads
+# each, all heads in one group). The chunk kernels' traffic is per chunk-head, so the
+# B=1 T=32768 H=16 entries are those bytes x 4 (8192 chunk-heads) and the B=1 T=8192 H=32 KDA
+# entries x 2 (4096); the chains' traffic depends on the segment plan and is not scaled.
+_GDN_T4096 = {"prepare": 615_838_976, "chain_fwd": 609_304_576, "compose": 42_014_464, "chain_bwd": 594_893_824,
+              "bwd_feat": 768_514_304, "bwd_tok": 731_632_896}
+_KDA_T4096 = {"prepare": 748_162_560, "chain_fwd": 610_627_840, "compose": 42_013_696, "chain_bwd": 593_397_504,
+              "bwd_feat": 774_079_488, "bwd_tok": 853_418_240}
+_HASHES = {("prepare", False): "aabf7e6125f0f065", ("bwd_feat", False): "5c86929f2f18a973",
+           ("bwd_tok", False): "40418ce70a38e1a1", ("chain_fwd", False): "2436ef14feb8b48b",
+           ("chain_bwd", False): "f2408d66f7b654b9", ("compose", False): "f43302a78ee98062",
+           ("prepare", True): "23c3e57d49b6616a", ("bwd_feat", True): "5c86929f2f18a973",
+           ("bwd_tok", True): "43b6d9807353fc18", ("chain_fwd", True): "2436ef14feb8b48b",
+           ("chain_bwd", True): "f2408d66f7b654b9", ("compose", True): "f43302a78ee98062"}
+NCU_TRAFFIC_BYTES = {}
+for _k, _v in _GDN_T4096.items():
+    NCU_TRAFFIC_BYTES[(_k, "gdn_b2_t4096_h16")] = (_v, _HASHES[(_k, False)])
+    if _k in ("prepare", "bwd_feat", "bwd_tok"):
+        NCU_TRAFFIC_BYTES[(_k, "gdn_b1_t32768_h16")] = (4 * _v, _HASHES[(_k, False)])
+for _k, _v in _KDA_T4096.items():
+    NCU_TRAFFIC_BYTES[(_k, "kda_b1_t4096_h32")] = (_v, _HASHES[(_k, True)])
+    if _k in ("prepare", "bwd_feat", "bwd_tok"):
+        NCU_TRAFFIC_BYTES[(_k, "kda_b1_t8192_h32")] = (2 * _v, _HASHES[(_k, True)])
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
@@ -92,10 +106,11 @@ def job_throughput(units_per_rank: float, world: int, ms: float) -> float:
     return units_per_rank * world / (ms * 1e-3)
 
 
-def source_hash(kernel: str):
-    """First 16 hex digits of the SHA-256 of the kernel's source file and the headers every
-    kernel includes (common.cuh, umma.cuh), or None."""
-    name = KERNEL_SOURCES.get(kernel)
+def source_hash(kernel: str, per_channel: bool = False):
+    """First 16 hex digits of the SHA-256 of the kernel's source file (the per-channel gate's
+    own file where it has one) and the headers every kernel includes (common.cuh, umma.cuh),
+    or None."""
+    name = (KERNEL_SOURCES_KDA if per_channel else KERNEL_SOURCES).get(kernel)
     if name is None:
         return None
     h = hashlib.sha256()
@@ -108,14 +123,14 @@ def source_hash(kernel: str):
     return h.hexdigest()[:16]
 
 
-def ncu_traffic(kernel: str, workload: str):
+def ncu_traffic(kernel: str, workload: str, per_channel: bool = False):
     """Per-step DRAM bytes of `kernel` on `workload` from the ncu table, or None when the table
     has no entry or the kernel's source has changed since the capture."""
     entry = NCU_TRAFFIC_BYTES.get((kernel, workload))
     if entry is None:
         return None
     nbytes, digest = entry
-    return nbytes if digest == source_hash(kernel) else None
+    return nbytes if digest == source_hash(kernel, per_channel) else None
 
 
 def load_peaks():
@@ -413,7 +428,7 @@ def roofline_of(runner, per_kernel, steps, peaks, peak_src):
     achieved = flop_chunk * nch / (step_ms * 1e-3) / 1e12
     peak = peaks["bf16_tflops_sustained"] * (TF32_OVER_BF16 if kind == "tf32" else 1.0)
     total = max(1e-9, sum(x[0] for x in per_kernel.values()))
-    traffic = ncu_traffic(name, w.name)
+    traffic = ncu_traffic(name, w.name, w.per_channel)
     return {"bound": "tensor", "kernel": name, "operands": kind, "achieved": achieved, "peak": peak,
             "unit": "TFLOP/s", "frac": achieved / peak, "traffic": traffic,
             "traffic_gbs": None if traffic is None else traffic / (step_ms * 1e-3) / 1e9,
