@@ -7,12 +7,18 @@
 // preceding it, e.g. the previous context-parallel rank's tail) or zero; packed documents
 // never read across their boundaries.
 //
-// GB300 mapping: a memory-bound stencil with every output row independent. Rows are
-// token-major [R][C] bf16; a warp takes whole rows of a 256-channel block (16 bytes per lane),
-// the 8 warps of a CTA interleave 64 consecutive rows so the W-row input windows overlap in
-// L1, and each thread keeps its 8 channels' taps in registers. The backward materialises
-// dz = dy silu'(z) in fp32, then forms dx from it, and the weight/bias gradients as per-tile
-// sums (over warps in shared memory, over tiles in a fixed order).
+// GB300 mapping: a memory-bound stencil. Rows are token-major [R][C] bf16 and a CTA covers 64
+// rows of a 256-channel block, staged in shared memory with asynchronous 16-byte copies.
+// - Unit dilation and up to 4 taps (the short convolution of the path): each warp walks a run
+//   of 32 consecutive rows for 64 channels with register windows of the last W rows, so every
+//   input is read from shared memory once; runs inside one sequence take a path with no
+//   per-row checks. The backward is one pass: dz = dy silu'(z) stays in registers and dx of a
+//   row is formed as soon as the dz it needs exist (k_conv_fwd_runs, k_conv_bwd_fused).
+// - Other dilations and widths: the 8 warps of a CTA interleave its rows (16 bytes of a row
+//   per lane), each thread keeps its 8 channels' taps in registers, and the backward
+//   materialises dz in fp32, then forms dx from it.
+// The weight/bias gradients are per-tile sums (over warps in shared memory, over tiles in a
+// fixed order).
 #include "common.cuh"
 #include "conv.cuh"
 
@@ -584,6 +590,336 @@ __global__ void __launch_bounds__(kThreads, 3) k_conv_dx_tiled(const ConvParams 
   }
 }
 
+// ---------------------------------------------------------------- fused backward, unit dilation
+// For d = 1 and W <= 4 the backward runs in one pass: the CTA stages x rows [r0 - HW, r0 + 64 + HW)
+// and dy rows [r0, r0 + 64 + HW) of its 256-channel block (HW = W - 1), then each warp walks a
+// run of 32 rows for 64 channels (2 per lane) with register windows of the last W inputs and
+// the last W dz values: dz of row u comes from z (window) and dy, and as soon as dz of row
+// t + HW exists, dx of row t = sum_k w'_k dz[t + k] (w'_k = w[W-1-k], the tap at offset k) is
+// complete and stored. dz never leaves registers (rows of a sequence's first HW positions are
+// written to the workspace for the halo gradient). The dz of a run's last HW rows is recomputed
+// by the next run. Weight and bias sums per warp are added over the CTA's two runs in a fixed
+// order and written as the tile's partials.
+constexpr int kFuseRun = 32;                        // rows per warp
+constexpr int kFuseRuns = kRowsPerTile / kFuseRun;  // 2 runs x 4 channel quarters = 8 warps
+
+__device__ __forceinline__ float2 smem2(const uint8_t* tile, int row, int cl) {
+  const uint32_t u = *reinterpret_cast<const uint32_t*>(tile + size_t(row) * (kBlockChannels * 2) + cl * 2);
+  return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u));
+}
+
+// Input at sequence position pos < 0 for channels c, c+1: the sequence's halo or zero.
+__device__ __forceinline__ float2 before_start2(const ConvParams& p, int n, long long pos, int c) {
+  if (p.halo && pos >= -p.HW) {
+    const uint32_t u = __ldg(reinterpret_cast<const unsigned int*>(p.halo + ((long long)n * p.HW + (p.HW + pos)) * p.C + c));
+    return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u));
+  }
+  return make_float2(0.f, 0.f);
+}
+
+template <int W>
+__global__ void __launch_bounds__(kThreads, 3) k_conv_bwd_fused(const ConvParams p) {
+  extern __shared__ __align__(16) uint8_t s_tile[];
+  constexpr int HW = W - 1;
+  constexpr int kRowBytes = kBlockChannels * 2;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int quarter = warp & 3, run = warp >> 2;
+  const int cb = blockIdx.x * kBlockChannels, cl = 64 * quarter + 2 * lane, c = cb + cl;
+  const long long r0 = (long long)blockIdx.y * kRowsPerTile;
+  uint8_t* s_x = s_tile;                                         // tile row i = global row r0 - HW + i
+  uint8_t* s_dy = s_tile + (kRowsPerTile + 2 * HW) * kRowBytes;  // tile row i = global row r0 + i
+  stage_rows<2>(p.x, p.R, p.C, cb, r0 - HW, kRowsPerTile + 2 * HW, s_x);
+  stage_rows<2>(p.dy, p.R, p.C, cb, r0, kRowsPerTile + HW, s_dy);
+  const bool active = c < p.C;
+  // taps by offset: wk[k] multiplies the input k rows back
+  float2 wk[W], bias = make_float2(0.f, 0.f);
+#pragma unroll
+  for (int k = 0; k < W; ++k)
+    wk[k] = active ? make_float2(__ldg(p.w + c * W + (W - 1 - k)), __ldg(p.w + (c + 1) * W + (W - 1 - k)))
+                   : make_float2(0.f, 0.f);
+  if (active && p.bias) bias = make_float2(__ldg(p.bias + c), __ldg(p.bias + c + 1));
+  float2 gw[W], gb = make_float2(0.f, 0.f);
+#pragma unroll
+  for (int k = 0; k < W; ++k) gw[k] = make_float2(0.f, 0.f);
+  stage_wait();
+  __syncthreads();
+  const long long t0 = r0 + kFuseRun * run;
+  if (active && t0 < p.R) {
+    float2 xw[W], dzw[W];   // xw[k]: input of row u - k; dzw[j]: dz of row u - j
+#pragma unroll
+    for (int k = 0; k < W; ++k) {
+      xw[k] = make_float2(0.f, 0.f);
+      dzw[k] = make_float2(0.f, 0.f);
+    }
+    SeqCursor su(p, t0), st(p, t0);
+    const long long pos0 = t0 - su.start;
+    if (su.end >= t0 + kFuseRun + HW && !(p.dhalo && pos0 < HW)) {
+      // Clean run: rows t0 .. t0 + kFuseRun + HW - 1 all lie in the sequence of t0, so no row
+      // needs a cursor, a mask or a range check. The windows are circular (row t0 + s in slot
+      // s % W), so the W-fold unrolled steps rename registers instead of moving them.
+#pragma unroll
+      for (int k = 1; k < W; ++k)
+        xw[W - k] = pos0 >= k ? smem2(s_x, int(t0 - k - (r0 - HW)), cl) : before_start2(p, su.n, pos0 - k, c);
+      const uint8_t* xs = s_x + size_t(t0 - (r0 - HW)) * kRowBytes;
+      const uint8_t* ds = s_dy + size_t(t0 - r0) * kRowBytes;
+      __nv_bfloat16* dxr = p.dx + t0 * p.C + c;
+#pragma unroll 1
+      for (int s0 = 0; s0 < kFuseRun + HW; s0 += W) {
+#pragma unroll
+        for (int j = 0; j < W; ++j) {
+          const int s = s0 + j;
+          if (s < kFuseRun + HW) {
+            xw[j] = smem2(xs, s, cl);
+            const float2 dy = smem2(ds, s, cl);
+            float z0 = bias.x, z1 = bias.y;
+#pragma unroll
+            for (int k = 0; k < W; ++k) {
+              z0 = fmaf(wk[k].x, xw[(j - k + W) % W].x, z0);
+              z1 = fmaf(wk[k].y, xw[(j - k + W) % W].y, z1);
+            }
+            float2 dz = dy;
+            if (p.silu) {
+              const float s0g = sigmoidf_(z0), s1g = sigmoidf_(z1);
+              dz.x = dy.x * s0g * (1.f + z0 * (1.f - s0g));
+              dz.y = dy.y * s1g * (1.f + z1 * (1.f - s1g));
+            }
+            if (s < kFuseRun) {
+              gb.x += dz.x;
+              gb.y += dz.y;
+#pragma unroll
+              for (int k = 0; k < W; ++k) {
+                gw[k].x = fmaf(dz.x, xw[(j - k + W) % W].x, gw[k].x);
+                gw[k].y = fmaf(dz.y, xw[(j - k + W) % W].y, gw[k].y);
+              }
+            }
+            dzw[j] = dz;
+            if (s >= HW) {   // dx of row t0 + s - HW from dz of rows t0 + s - HW .. t0 + s
+              float a0 = 0.f, a1 = 0.f;
+#pragma unroll
+              for (int k = 0; k < W; ++k) {
+                a0 = fmaf(wk[k].x, dzw[(j - HW + k + W) % W].x, a0);
+                a1 = fmaf(wk[k].y, dzw[(j - HW + k + W) % W].y, a1);
+              }
+              *reinterpret_cast<__nv_bfloat162*>(dxr) = __floats2bfloat162_rn(a0, a1);
+              dxr += p.C;
+            }
+          }
+        }
+      }
+    } else {
+    {
+      // the window as it stands before the first step's shift: xw[k - 1] = input at offset k
+      // of row t0 (rows before its sequence's start read that sequence's halo or zero)
+#pragma unroll
+      for (int k = 1; k < W; ++k)
+        xw[k - 1] = pos0 >= k ? smem2(s_x, int(t0 - k - (r0 - HW)), cl) : before_start2(p, su.n, pos0 - k, c);
+    }
+#pragma unroll 2
+    for (int s = 0; s < kFuseRun + HW; ++s) {
+      const long long u = t0 + s;
+#pragma unroll
+      for (int k = W - 1; k > 0; --k) {
+        xw[k] = xw[k - 1];
+        dzw[k] = dzw[k - 1];
+      }
+      float2 dz = make_float2(0.f, 0.f);
+      if (u < p.R) {
+        xw[0] = smem2(s_x, int(u - (r0 - HW)), cl);
+        su.advance(p, u);
+        const long long pos = u - su.start;
+        if (pos == 0 && s > 0) {
+          // a sequence starts at this row: the window's older entries become its halo or zero
+#pragma unroll
+          for (int k = 1; k < W; ++k) xw[k] = before_start2(p, su.n, -k, c);
+        }
+        const float2 dy = smem2(s_dy, int(u - r0), cl);
+        float z0 = bias.x, z1 = bias.y;
+#pragma unroll
+        for (int k = 0; k < W; ++k) {
+          z0 = fmaf(wk[k].x, xw[k].x, z0);
+          z1 = fmaf(wk[k].y, xw[k].y, z1);
+        }
+        if (p.silu) {
+          const float s0 = sigmoidf_(z0), s1 = sigmoidf_(z1);
+          dz.x = dy.x * s0 * (1.f + z0 * (1.f - s0));
+          dz.y = dy.y * s1 * (1.f + z1 * (1.f - s1));
+        } else {
+          dz = dy;
+        }
+        if (s < kFuseRun) {
+          gb.x += dz.x;
+          gb.y += dz.y;
+#pragma unroll
+          for (int k = 0; k < W; ++k) {
+            gw[k].x = fmaf(dz.x, xw[k].x, gw[k].x);
+            gw[k].y = fmaf(dz.y, xw[k].y, gw[k].y);
+          }
+          if (p.dhalo && pos < HW) *reinterpret_cast<float2*>(p.dz + u * p.C + c) = dz;
+        }
+      }
+      dzw[0] = dz;
+      const long long t = u - HW;   // dx of row t needs dz of rows t .. t + HW: complete now
+      if (t >= t0 && t < p.R) {
+        st.advance(p, t);
+        float a0 = 0.f, a1 = 0.f;
+#pragma unroll
+        for (int k = 0; k < W; ++k)
+          if (t + k < st.end) {
+            a0 = fmaf(wk[k].x, dzw[HW - k].x, a0);
+            a1 = fmaf(wk[k].y, dzw[HW - k].y, a1);
+          }
+        *reinterpret_cast<__nv_bfloat162*>(p.dx + t * p.C + c) = __floats2bfloat162_rn(a0, a1);
+      }
+    }
+    }
+  }
+  // partials of the tile: the two runs' sums per (channel, tap / bias), added in run order
+  __syncthreads();   // the staged tiles are no longer read: reuse them for the exchange
+  float* s_part = reinterpret_cast<float*>(s_tile);   // [run][256 channels][W + 1]
+  {
+    float* d0 = s_part + (size_t(run) * kBlockChannels + cl) * (W + 1);
+    float* d1 = d0 + (W + 1);
+#pragma unroll
+    for (int k = 0; k < W; ++k) {   // tap index i = W - 1 - k
+      d0[W - 1 - k] = gw[k].x;
+      d1[W - 1 - k] = gw[k].y;
+    }
+    d0[W] = gb.x;
+    d1[W] = gb.y;
+  }
+  __syncthreads();
+  for (int idx = threadIdx.x; idx < kBlockChannels * (W + 1); idx += kThreads) {
+    const int ch = idx / (W + 1), slot = idx % (W + 1);
+    if (cb + ch >= p.C) continue;
+    float acc = 0.f;
+#pragma unroll
+    for (int q = 0; q < kFuseRuns; ++q) acc += s_part[(size_t(q) * kBlockChannels + ch) * (W + 1) + slot];
+    p.part[(size_t(blockIdx.y) * p.C + cb + ch) * (W + 1) + slot] = acc;
+  }
+}
+
+// Forward for unit dilation and W <= 4, in the same layout: the CTA stages x rows
+// [r0 - HW, r0 + 64) of its 256-channel block, each warp walks a run of 32 rows for 64
+// channels (2 per lane) with a register window of the last W inputs. A run inside one sequence
+// takes the clean path (circular window, no per-row checks); a run that meets a sequence start
+// or the last row shifts its window and patches it with the new sequence's halo or zero.
+template <int W>
+__global__ void __launch_bounds__(kThreads) k_conv_fwd_runs(const ConvParams p) {
+  extern __shared__ __align__(16) uint8_t s_tile[];   // tile row i = global row r0 - HW + i
+  constexpr int HW = W - 1;
+  constexpr int kRowBytes = kBlockChannels * 2;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int quarter = warp & 3, run = warp >> 2;
+  const int cb = blockIdx.x * kBlockChannels, cl = 64 * quarter + 2 * lane, c = cb + cl;
+  const long long r0 = (long long)blockIdx.y * kRowsPerTile;
+  stage_rows<2>(p.x, p.R, p.C, cb, r0 - HW, kRowsPerTile + HW, s_tile);
+  const bool active = c < p.C;
+  float2 wk[W], bias = make_float2(0.f, 0.f);
+#pragma unroll
+  for (int k = 0; k < W; ++k)
+    wk[k] = active ? make_float2(__ldg(p.w + c * W + (W - 1 - k)), __ldg(p.w + (c + 1) * W + (W - 1 - k)))
+                   : make_float2(0.f, 0.f);
+  if (active && p.bias) bias = make_float2(__ldg(p.bias + c), __ldg(p.bias + c + 1));
+  stage_wait();
+  __syncthreads();
+  const long long t0 = r0 + kFuseRun * run;
+  if (!active || t0 >= p.R) return;   // no barrier follows
+  float2 xw[W];
+#pragma unroll
+  for (int k = 0; k < W; ++k) xw[k] = make_float2(0.f, 0.f);
+  SeqCursor su(p, t0);
+  const long long pos0 = t0 - su.start;
+  if (su.end >= t0 + kFuseRun) {
+#pragma unroll
+    for (int k = 1; k < W; ++k)
+      xw[W - k] = pos0 >= k ? smem2(s_tile, int(t0 - k - (r0 - HW)), cl) : before_start2(p, su.n, pos0 - k, c);
+    const uint8_t* xs = s_tile + size_t(t0 - (r0 - HW)) * kRowBytes;
+    __nv_bfloat16* yr = p.y + t0 * p.C + c;
+#pragma unroll 1
+    for (int s0 = 0; s0 < kFuseRun; s0 += W) {
+#pragma unroll
+      for (int j = 0; j < W; ++j) {
+        const int s = s0 + j;
+        if (s < kFuseRun) {
+          xw[j] = smem2(xs, s, cl);
+          float z0 = bias.x, z1 = bias.y;
+#pragma unroll
+          for (int k = 0; k < W; ++k) {
+            z0 = fmaf(wk[k].x, xw[(j - k + W) % W].x, z0);
+            z1 = fmaf(wk[k].y, xw[(j - k + W) % W].y, z1);
+          }
+          if (p.silu) {
+            z0 = __fdividef(z0, 1.f + __expf(-z0));
+            z1 = __fdividef(z1, 1.f + __expf(-z1));
+          }
+          *reinterpret_cast<__nv_bfloat162*>(yr) = __floats2bfloat162_rn(z0, z1);
+          yr += p.C;
+        }
+      }
+    }
+    return;
+  }
+#pragma unroll
+  for (int k = 1; k < W; ++k)
+    xw[k - 1] = pos0 >= k ? smem2(s_tile, int(t0 - k - (r0 - HW)), cl) : before_start2(p, su.n, pos0 - k, c);
+#pragma unroll 1
+  for (int s = 0; s < kFuseRun; ++s) {
+    const long long u = t0 + s;
+    if (u >= p.R) break;
+#pragma unroll
+    for (int k = W - 1; k > 0; --k) xw[k] = xw[k - 1];
+    xw[0] = smem2(s_tile, int(u - (r0 - HW)), cl);
+    su.advance(p, u);
+    if (u == su.start && s > 0) {
+      // a sequence starts at this row: the window's older entries become its halo or zero
+#pragma unroll
+      for (int k = 1; k < W; ++k) xw[k] = before_start2(p, su.n, -k, c);
+    }
+    float z0 = bias.x, z1 = bias.y;
+#pragma unroll
+    for (int k = 0; k < W; ++k) {
+      z0 = fmaf(wk[k].x, xw[k].x, z0);
+      z1 = fmaf(wk[k].y, xw[k].y, z1);
+    }
+    if (p.silu) {
+      z0 = __fdividef(z0, 1.f + __expf(-z0));
+      z1 = __fdividef(z1, 1.f + __expf(-z1));
+    }
+    *reinterpret_cast<__nv_bfloat162*>(p.y + u * p.C + c) = __floats2bfloat162_rn(z0, z1);
+  }
+}
+
+template <int W>
+cudaError_t conv_fwd_runs(const ConvParams& p, cudaStream_t s) {
+  dim3 grid(unsigned((p.C + kBlockChannels - 1) / kBlockChannels), unsigned((p.R + kRowsPerTile - 1) / kRowsPerTile));
+  const size_t smem = size_t(kRowsPerTile + W - 1) * kBlockChannels * 2;
+  k_conv_fwd_runs<W><<<grid, kThreads, smem, s>>>(p);
+  return cudaGetLastError();
+}
+
+template <int W>
+cudaError_t conv_bwd_fused(const ConvParams& p, cudaStream_t s) {
+  const unsigned tiles = unsigned((p.R + kRowsPerTile - 1) / kRowsPerTile);
+  dim3 grid(unsigned((p.C + kBlockChannels - 1) / kBlockChannels), tiles);
+  const size_t smem = size_t(2 * kRowsPerTile + 3 * (W - 1)) * kBlockChannels * 2;
+  static bool attr = false;
+  if (!attr) {
+    cudaError_t e = cudaFuncSetAttribute(k_conv_bwd_fused<W>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+    if (e != cudaSuccess) return e;
+    attr = true;
+  }
+  k_conv_bwd_fused<W><<<grid, kThreads, smem, s>>>(p);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  if (p.dhalo && p.HW > 0) {
+    dim3 g2(grid.x, unsigned((p.N * p.HW + kWarps - 1) / kWarps));
+    k_conv_dhalo<4><<<g2, kThreads, 0, s>>>(p);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
+  k_conv_reduce<<<(p.C * (p.W + 1) + 255) / 256, 256, 0, s>>>(p, int(tiles));
+  return cudaGetLastError();
+}
+
 template <int MW>
 cudaError_t conv_fwd_mw(const ConvParams& p, cudaStream_t s) {
   dim3 grid(unsigned((p.C + kBlockChannels - 1) / kBlockChannels), unsigned((p.R + kRowsPerTile - 1) / kRowsPerTile));
@@ -639,10 +975,28 @@ cudaError_t conv_bwd_mw(const ConvParams& p, cudaStream_t s) {
 
 // Kernels compiled for up to 4 taps (registers for the common short convolution) or 8.
 cudaError_t launch_conv_fwd(const ConvParams& p, cudaStream_t s) {
+  if (p.dil == 1) {
+    switch (p.W) {
+      case 1: return conv_fwd_runs<1>(p, s);
+      case 2: return conv_fwd_runs<2>(p, s);
+      case 3: return conv_fwd_runs<3>(p, s);
+      case 4: return conv_fwd_runs<4>(p, s);
+      default: break;
+    }
+  }
   return p.W <= 4 ? conv_fwd_mw<4>(p, s) : conv_fwd_mw<kConvMaxTaps>(p, s);
 }
 
 cudaError_t launch_conv_bwd(const ConvParams& p, cudaStream_t s) {
+  if (p.dil == 1) {
+    switch (p.W) {
+      case 1: return conv_bwd_fused<1>(p, s);
+      case 2: return conv_bwd_fused<2>(p, s);
+      case 3: return conv_bwd_fused<3>(p, s);
+      case 4: return conv_bwd_fused<4>(p, s);
+      default: break;
+    }
+  }
   return p.W <= 4 ? conv_bwd_mw<4>(p, s) : conv_bwd_mw<kConvMaxTaps>(p, s);
 }
 
