@@ -68,12 +68,12 @@ KERNEL_SOURCES_KDA = {**KERNEL_SOURCES, "prepare": "k_prep_kda.cu", "bwd_tok": "
 # each, all heads in one group). The chunk kernels' traffic is per chunk-head, so the
 # B=1 T=32768 H=16 entries are those bytes x 4 (8192 chunk-heads) and the B=1 T=8192 H=32 KDA
 # entries x 2 (4096); the chains' traffic depends on the segment plan and is not scaled.
-_GDN_T4096 = {"prepare": 615_838_976, "chain_fwd": 609_304_576, "compose": 42_014_464, "chain_bwd": 594_893_824,
+_GDN_T4096 = {"prepare": 615_838_976, "chain_fwd": 612_954_880, "compose": 42_014_464, "chain_bwd": 594_893_824,
               "bwd_feat": 768_514_304, "bwd_tok": 731_632_896}
-_KDA_T4096 = {"prepare": 748_162_560, "chain_fwd": 610_627_840, "compose": 42_013_696, "chain_bwd": 593_397_504,
+_KDA_T4096 = {"prepare": 748_162_560, "compose": 42_013_696, "chain_bwd": 593_397_504,
               "bwd_feat": 774_079_488, "bwd_tok": 853_418_240}
 _HASHES = {("prepare", False): "aabf7e6125f0f065", ("bwd_feat", False): "5c86929f2f18a973",
-           ("bwd_tok", False): "40418ce70a38e1a1", ("chain_fwd", False): "2436ef14feb8b48b",
+           ("bwd_tok", False): "40418ce70a38e1a1", ("chain_fwd", False): "806d6bdc6bfaed1f",
            ("chain_bwd", False): "f2408d66f7b654b9", ("compose", False): "f43302a78ee98062",
            ("prepare", True): "23c3e57d49b6616a", ("bwd_feat", True): "5c86929f2f18a973",
            ("bwd_tok", True): "43b6d9807353fc18", ("chain_fwd", True): "2436ef14feb8b48b",

@@ -10,19 +10,21 @@
 // GB300 mapping: one CTA per (sequence, head). The state lives in TMEM, transposed: S^T
 // (V x K), lane v = column v of S, as one fp32 copy that the MMAs read as their TMEM-resident
 // A operand (kind::tf32, which reads the operand's upper 19 bits; a CPU emulation of the chunked
-// algorithm gives the same state and output errors as with a round-to-nearest copy). The chunk
-// tiles from the prepare kernel are TMA-loaded SW128 B operands:
+// algorithm gives the same state and output errors as with a round-to-nearest copy). Two state
+// buffers alternate by chunk parity. The chunk tiles from the prepare kernel are TMA-loaded
+// SW128 B operands:
 //   [P | O] = S^T [W; Qt]^T  (one N=128 product: P = S^T W^T, O = S^T Qt^T)  -- on the chain
-//   S^T   *= diag(gam)       (by the chain warps once the product has read S)
+//   S'^T    = S^T diag(gam)  (the chain warps, into the other buffer, while the product reads S)
 //   v_new^T = U^T - P        (written over P in TMEM)
-//   S^T += v_new^T KtT^T                                   -- on the serial chain
-//   O   += v_new^T Aqk^T                                   -- off the chain, issued after
-// The issuing thread starts the next chunk's product as soon as the state update completes;
-// the chain warps decay the state and form v_new while that product's successor is prepared,
-// and copy the entry state out for the backward while the next product reads it. P/v_new and
-// O are double-buffered in TMEM by chunk parity. Eight chain warps share the TMEM lanes (two
-// threads per lane, each on half of the columns); warp 8 streams the tiles with TMA (KtT/Aqk
-// double-buffered) and issues the MMAs from one thread. All waits bounded.
+//   S'^T   += v_new^T KtT^T                                -- on the serial chain
+//   O      += v_new^T Aqk^T                                -- off the chain, issued after
+// The decay (and the backward's copy of the entry state, taken from the same registers)
+// overlaps the product. The issuing thread starts the next chunk's product as soon as the
+// state update completes. P/v_new and O are double-buffered in TMEM by chunk parity; a chunk's
+// output is read out while the next chunk's state update runs, and the product two chunks on
+// waits for that read. Eight chain warps share the TMEM lanes (two threads per lane, each on
+// half of the columns); warp 8 streams the tiles with TMA (KtT/Aqk double-buffered) and issues
+// the MMAs from one thread. All waits bounded.
 //
 // A CTA runs one segment of a sequence's chunks in one of three modes (the segmented chain
 // of common.cuh): in full (from the true entry state, with the output and the backward
@@ -43,8 +45,10 @@ constexpr uint32_t kOffU = 65536;      // 4 panels x [64][32] fp32, no swizzle
 constexpr uint32_t kOffG3 = 98304;     // 2 stages x {KtT 32 KB (2 panels x 128 rows), Aqk 16 KB}
 constexpr uint32_t kG3Stage = 49152;
 constexpr uint32_t kSmemBytes = kOffG3 + 2 * kG3Stage + 1024;
-// TMEM columns: the state, then per chunk parity [P, later v_new | O]
-constexpr uint32_t kTS = 0, kTB = 128;
+// TMEM columns: two state buffers, then per chunk parity [P, later v_new | O]. The state
+// entering chunk j lives in buffer j % 2; the decayed state and the update go to the other.
+constexpr uint32_t kTB = 256;
+__device__ __forceinline__ uint32_t ts(int j) { return uint32_t(j & 1) * 128; }
 __device__ __forceinline__ uint32_t tpv(int j) { return kTB + uint32_t(j & 1) * 128; }
 __device__ __forceinline__ uint32_t tout(int j) { return kTB + uint32_t(j & 1) * 128 + 64; }
 
@@ -52,41 +56,44 @@ __device__ __forceinline__ uint8_t* align1k(uint8_t* p) {
   return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
 }
 
-// Entry state of chunk c (this thread: lane v, state columns [k0, k0+64)) to the backward's
-// save; the state is only read here (the chunk's product may be reading it too).
-__device__ __forceinline__ void chain_save_state(const ChainParams& p, float* h_save, int c, int h, int v, int k0,
-                                                 uint32_t tl) {
-  const size_t tile = size_t(c) * p.H + h;
+// The state entering chunk j (buffer ts(j); this thread: lane v, state columns [k0, k0+64))
+// times chunk c's end decay gam, into buffer ts(j+1), where the chunk's state update then adds
+// k~^T v_new. It runs while the chunk's product reads buffer ts(j). With h_save the entry
+// state also goes to the backward's save from the same registers.
+__device__ __forceinline__ void chain_decay_into(const ChainParams& p, int c, int h, int v, int k0, uint32_t tl,
+                                                 int j, float g0, float* h_save) {
   float s[64];
-  tmem_ld64(tl + kTS + k0, s);
-  tmem_wait_ld_regs(s);
-  float* hs = h_save + tile * kD * kD + size_t(k0) * kD + v;
-#pragma unroll
-  for (int e = 0; e < 64; ++e) hs[size_t(e) * kD] = s[e];
-}
-
-// Decay of the state by chunk c's end decay (gam), in place, once the chunk's product has read
-// the state; the state update then adds k~^T v_new to it.
-__device__ __forceinline__ void chain_decay(const ChainParams& p, int c, int h, int k0, uint32_t tl, float g0) {
-  float s[64];
-  tmem_ld64(tl + kTS + k0, s);
+  tmem_ld64(tl + ts(j) + k0, s);
   tmem_wait_ld_regs(s);
   if (p.kda) {
     const float4* gam = reinterpret_cast<const float4*>(p.gam + (size_t(c) * p.H + h) * kD + k0);
 #pragma unroll
     for (int e = 0; e < 16; ++e) {
       const float4 g4 = gam[e];
-      s[4 * e] *= g4.x;
-      s[4 * e + 1] *= g4.y;
-      s[4 * e + 2] *= g4.z;
-      s[4 * e + 3] *= g4.w;
+      float* x = s + 4 * e;
+      if (h_save) {
+        float* hs = h_save + (size_t(c) * p.H + h) * kD * kD + size_t(k0 + 4 * e) * kD + v;
+        hs[0] = x[0];
+        hs[kD] = x[1];
+        hs[2 * kD] = x[2];
+        hs[3 * kD] = x[3];
+      }
+      x[0] *= g4.x;
+      x[1] *= g4.y;
+      x[2] *= g4.z;
+      x[3] *= g4.w;
     }
   } else {
+    if (h_save) {
+      float* hs = h_save + (size_t(c) * p.H + h) * kD * kD + size_t(k0) * kD + v;
+#pragma unroll
+      for (int e = 0; e < 64; ++e) hs[size_t(e) * kD] = s[e];
+    }
 #pragma unroll
     for (int e = 0; e < 64; ++e) s[e] *= g0;
   }
-  tmem_st32(tl + kTS + k0, s);
-  tmem_st32(tl + kTS + k0 + 32, s + 32);
+  tmem_st32(tl + ts(j + 1) + k0, s);
+  tmem_st32(tl + ts(j + 1) + k0 + 32, s + 32);
 }
 
 }  // namespace
@@ -97,7 +104,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const __grid_constant__ CUtensorMap mU, const ChainParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = align1k(smem_raw);
-  __shared__ uint64_t full1, full2, full3[2], mma1, mma2, mma3, sready, vready;
+  __shared__ uint64_t full1, full2, full3[2], mma1, mma2, mma3, sready, vready, oread;
   __shared__ uint32_t tslot;
   __shared__ int abort_flag;
 
@@ -128,6 +135,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&mma3, 1);
     mbar_init(&sready, kChainThreads);
     mbar_init(&vready, kChainThreads);
+    mbar_init(&oread, kChainThreads);
     fence_mbar_init();
   }
   tc_fence_before();
@@ -174,8 +182,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t tPV = tb + tpv(j), tO = tb + tout(j);
         const uint32_t sKtT = smem_u32(sm + kOffG3 + st * kG3Stage), sAqk = sKtT + 32768;
         if (!mbar_wait(&full1, par, &abort_flag, p.status, kDevTimeoutTma)) break;
+        // the product overwrites the output of chunk j - 2: the chain warps have read it
+        if (outs && p.o && j >= 2 && !mbar_wait(&oread, par, &abort_flag, p.status, kDevTimeoutSync)) break;
         tc_fence_after();
-        for (int s = 0; s < 16; ++s) mma_tf32_ts(tPV, tb + kTS + s * 8, desc_kmajor(sWQ, 16384, s), id_first, s > 0);
+        for (int s = 0; s < 16; ++s) mma_tf32_ts(tPV, tb + ts(j) + s * 8, desc_kmajor(sWQ, 16384, s), id_first, s > 0);
         mma_commit(&mma1);
         // the previous chunk's output product has read its KtT / Aqk stage: refill it two chunks on
         if (j > 0) {
@@ -185,10 +195,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!mbar_wait(&mma1, par, &abort_flag, p.status, kDevTimeoutMma)) break;
         if (j + 1 < nc) load_g1(c + 1);
         if (!mbar_wait(&full3[st], (j >> 1) & 1, &abort_flag, p.status, kDevTimeoutTma)) break;
-        // the chain warps have decayed the state and written v_new
+        // the chain warps have decayed the state into the other buffer and written v_new
         if (!mbar_wait(&vready, par, &abort_flag, p.status, kDevTimeoutSync)) break;
         tc_fence_after();
-        for (int s = 0; s < 8; ++s) mma_tf32_ts(tb + kTS, tPV + s * 8, desc_kmajor(sKtT, 16384, s), id128, true);
+        for (int s = 0; s < 8; ++s) mma_tf32_ts(tb + ts(j + 1), tPV + s * 8, desc_kmajor(sKtT, 16384, s), id128, true);
         mma_commit(&mma2);
         if (outs)
           for (int s = 0; s < 8; ++s) mma_tf32_ts(tO, tPV + s * 8, desc_kmajor(sAqk, 8192, s), id64, true);
@@ -218,8 +228,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int e = 0; e < 64; ++e)
         buf[e] = src ? src[size_t(e) * kD] : (mode == kRunMapM && k0 + e == v ? 1.f : 0.f);
-      tmem_st32(tb + lb + kTS + k0, buf);
-      tmem_st32(tb + lb + kTS + k0 + 32, buf + 32);
+      tmem_st32(tb + lb + ts(0) + k0, buf);
+      tmem_st32(tb + lb + ts(0) + k0 + 32, buf + 32);
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(&sready);
@@ -232,18 +242,43 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     bool alive = true;
     float g_cur = p.kda ? 0.f : p.gam[(size_t(first) * H + h) * kD];
+    // the output of chunk jj: lane pairs (v, v^1) swap halves so each lane stores two adjacent
+    // bf16 of a row (the even lane rows t0..t0+15, the odd lane rows t0+16..t0+31); the chain
+    // warps arrive on oread once the tile is in registers (the product two chunks on rewrites it)
+    auto out_epilogue = [&](int jj, bool signal) {
+      const ChunkEntry ch = p.chunks[first + jj];
+      float r[32];
+      tmem_ld32(tb + lb + tout(jj) + t0, r);
+      tmem_wait_ld_regs(r);
+      if (signal) {
+        tc_fence_before();
+        mbar_arrive(&oread);
+      }
+      const int odd = v & 1;
+      __nv_bfloat162* op = reinterpret_cast<__nv_bfloat162*>(o + (size_t(ch.x + t0 + 16 * odd) * H + h) * kD + (v & ~1));
+#pragma unroll
+      for (int t = 0; t < 16; ++t) {
+        const float mine = odd ? r[16 + t] : r[t];
+        const float give = odd ? r[t] : r[16 + t];
+        const float other = __shfl_xor_sync(0xffffffffu, give, 1);
+        const __nv_bfloat162 pr = odd ? __floats2bfloat162_rn(other, mine) : __floats2bfloat162_rn(mine, other);
+        if (t0 + 16 * odd + t < ch.y) op[size_t(t) * H * kD / 2] = pr;
+      }
+    };
     for (int j = 0; j < nc; ++j) {
       const uint32_t par = j & 1;
       const int c = first + j;
-      const ChunkEntry ch = p.chunks[c];
       const size_t tile = size_t(c) * H + h;
       // next chunk's scalar gate, loaded a chunk ahead of its use
       const float g_next = (j + 1 < nc && !p.kda) ? p.gam[(size_t(c + 1) * H + h) * kD] : 0.f;
+      // the decayed state into the other buffer while this chunk's product reads the state (the
+      // segment's first entry state was saved from the registers that wrote it)
+      chain_decay_into(p, c, h, v, k0, tb + lb, j, g_cur, j > 0 ? h_save : nullptr);
       if (use_u && !mbar_wait(&full2, par, &abort_flag, p.status, kDevTimeoutTma)) { alive = false; break; }
       if (!mbar_wait(&mma1, par, &abort_flag, p.status, kDevTimeoutMma)) { alive = false; break; }
+      // the previous chunk's intra-chunk output product was issued before this product
+      if (o && j > 0 && !mbar_wait(&mma3, par ^ 1u, &abort_flag, p.status, kDevTimeoutMma)) { alive = false; break; }
       tc_fence_after();
-      // the product has read the state: decay it for the state update
-      chain_decay(p, c, h, k0, tb + lb, g_cur);
       {
         float r[32];
         tmem_ld32(tb + lb + tpv(j) + t0, r);
@@ -254,7 +289,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int t = 0; t < 32; ++t) r[t] = to_tf32(u[t] - r[t]);
         tmem_st32(tb + lb + tpv(j) + t0, r);
-        tmem_wait_st();
+        tmem_wait_st();   // the decayed state's stores as well
         tc_fence_before();
         mbar_arrive(&vready);
         if (vnew_save) {
@@ -263,29 +298,18 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int t = 0; t < 32; ++t) vsave[size_t(t) * kD] = r[t];
         }
       }
+      // the previous chunk's output, while this chunk's state update runs
+      if (o && j > 0) out_epilogue(j - 1, true);
       g_cur = g_next;
       if (!mbar_wait(&mma2, par, &abort_flag, p.status, kDevTimeoutMma)) { alive = false; break; }
       tc_fence_after();
-      // the next chunk's entry state, read while its product reads it too
-      if (h_save && j + 1 < nc) chain_save_state(p, h_save, c + 1, h, v, k0, tb + lb);
-      if (o) {
-        if (!mbar_wait(&mma3, par, &abort_flag, p.status, kDevTimeoutMma)) { alive = false; break; }
+    }
+    if (o && alive) {
+      if (mbar_wait(&mma3, (nc - 1) & 1, &abort_flag, p.status, kDevTimeoutMma)) {
         tc_fence_after();
-        float r[32];
-        tmem_ld32(tb + lb + tout(j) + t0, r);
-        tmem_wait_ld_regs(r);
-        // lane pairs (v, v^1) swap halves so each lane stores two adjacent bf16 of a row: the
-        // even lane rows t0..t0+15, the odd lane rows t0+16..t0+31
-        const int odd = v & 1;
-        __nv_bfloat162* op = reinterpret_cast<__nv_bfloat162*>(o + (size_t(ch.x + t0 + 16 * odd) * H + h) * kD + (v & ~1));
-#pragma unroll
-        for (int t = 0; t < 16; ++t) {
-          const float mine = odd ? r[16 + t] : r[t];
-          const float give = odd ? r[t] : r[16 + t];
-          const float other = __shfl_xor_sync(0xffffffffu, give, 1);
-          const __nv_bfloat162 pr = odd ? __floats2bfloat162_rn(other, mine) : __floats2bfloat162_rn(mine, other);
-          if (t0 + 16 * odd + t < ch.y) op[size_t(t) * H * kD / 2] = pr;
-        }
+        out_epilogue(nc - 1, false);
+      } else {
+        alive = false;
       }
     }
     // exit state: the final state, the next segment's entry (pass 0), or the segment's map
@@ -302,7 +326,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (alive && dst) {  // the loop's last mma2 wait covers the final state update
       float s[64];
-      tmem_ld64(tb + lb + kTS + k0, s);
+      tmem_ld64(tb + lb + ts(nc) + k0, s);
       tmem_wait_ld_regs(s);
       const size_t off = size_t(k0) * kD + v;
       if (dst_lo) {
