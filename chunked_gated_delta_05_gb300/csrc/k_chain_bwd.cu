@@ -11,11 +11,14 @@
 // backward); the recurrence above is the exact adjoint of the forward chunk loop.
 //
 // GB300 mapping mirrors the forward chain: one CTA per (sequence, head); dS is held
-// transposed in TMEM (lane v = column v of dS) as an fp32 master copy and a tf32 copy;
-// dO^T and -dv_new^T are TMEM-resident A operands; the chunk tiles (Kt, Aqk^T, Qt^T, W^T,
-// double-buffered) are TMA-loaded SW128 B operands; every product is a 128-lane tf32 MMA.
-// The products that do not depend on dS (Aqk^T dO, Qt^T dO) are issued alongside the chain
-// ones. Eight chain warps, one producer warp; all waits bounded.
+// transposed in TMEM (lane v = column v of dS) in fp32, in two buffers that alternate by chunk
+// step, and the dv_new product reads it there as its A operand (kind::tf32 reads the upper 19
+// bits). While that product runs, the chain warps write gam dS' into the other buffer (and the
+// feature-major kernel's copy of dS'), where the step's two other products accumulate. dO^T is
+// staged in TMEM a step ahead and -dv_new^T written by the chain warps; both are A operands.
+// The chunk tiles (Kt, Aqk^T, Qt^T, W^T, double-buffered) are TMA-loaded SW128 B operands;
+// every product is a 128-lane tf32 MMA. So a step's serial path is the dv_new product, the
+// -dv_new pass and the W^T product. Eight chain warps, one producer warp; all waits bounded.
 //
 // As in the forward chain, a CTA runs one segment (segments counted from the sequence's end)
 // in full, or as the segment's adjoint map: from the identity with dO = 0 (M^T, the products
@@ -35,7 +38,12 @@ constexpr uint32_t kOffAqkT = 32768;                 // [t][i]  2 panels x 64 ro
 constexpr uint32_t kOffQtT = 49152;                  // [k][i]  2 panels x 128 rows  (32 KB)
 constexpr uint32_t kOffWT = 81920;                   // [k][t]  2 panels x 128 rows  (32 KB)
 constexpr uint32_t kSmemBytes = 2 * kStage + 1024;
-constexpr uint32_t kTDM = 0, kTDT = 128, kTDV = 256, kTDN = 320, kTDO = 384;
+// TMEM columns: two dS buffers (the one entering chunk step j is buffer j % 2; the decayed
+// gradient and the step's updates go to the other), dv_new, -dv_new (tf32), and dO^T
+// double-buffered by step parity.
+constexpr uint32_t kTDV = 256, kTDN = 320;
+__device__ __forceinline__ uint32_t tm(int j) { return uint32_t(j & 1) * 128; }
+__device__ __forceinline__ uint32_t tdo(int j) { return 384 + uint32_t(j & 1) * 64; }
 
 __device__ __forceinline__ uint8_t* align1k(uint8_t* p) {
   return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
@@ -55,38 +63,22 @@ __device__ __forceinline__ void load_dO(const RevChainParams& p, int c, int h, i
   }
 }
 
-// dS pass for chunk c (lane v, state columns [k0, k0+64); token columns [t0, t0+32)): write
-// the tf32 copy of dS' (the gradient w.r.t. the state leaving chunk c) and dO^T (prefetched
-// into `d`) as A operands and release the dv_new product (`ready`); then pre-apply the chunk
-// decay to the master copy and release the products that accumulate into it (`mready`), so
-// the decay runs while dv_new is computed; then save dS' (its tf32 copy) for the feature-major
-// backward kernel.
-__device__ __forceinline__ void rev_pass(const RevChainParams& p, float* dh_save, bool use_do, int c, int h,
-                                         int v, int k0, int t0, uint32_t tl, uint64_t* ready, uint64_t* mready,
-                                         const uint32_t* d, float g0) {
+// dS' of chunk c (the gradient w.r.t. the state leaving it; buffer tm(j), which the step's
+// dv_new product reads as it is) times the chunk's decay gam, into buffer tm(j+1), where the
+// step's products then accumulate; this thread: lane v, state columns [k0, k0+64). With dh_save
+// the feature-major backward kernel's copy of dS' (rounded to tf32) is written from the same
+// registers.
+__device__ __forceinline__ void rev_decay_into(const RevChainParams& p, float* dh_save, int c, int h, int v, int k0,
+                                               uint32_t tl, int j, float g0) {
   const size_t tile = size_t(c) * p.H + h;
   float s[64];
-  tmem_ld64(tl + kTDM + k0, s);
+  tmem_ld64(tl + tm(j) + k0, s);
   tmem_wait_ld_regs(s);
+  if (dh_save) {
+    float* ds = dh_save + tile * kD * kD + size_t(k0) * kD + v;
 #pragma unroll
-  for (int half = 0; half < 2; ++half) {
-    float t[32];
-#pragma unroll
-    for (int e = 0; e < 32; ++e) t[e] = to_tf32(s[32 * half + e]);
-    tmem_st32(tl + kTDT + k0 + 32 * half, t);
+    for (int e = 0; e < 64; ++e) ds[size_t(e) * kD] = to_tf32(s[e]);
   }
-  if (use_do) {
-    float df[32];
-#pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      df[2 * i] = __uint_as_float(d[i] << 16);
-      df[2 * i + 1] = __uint_as_float(d[i] & 0xffff0000u);
-    }
-    tmem_st32(tl + kTDO + t0, df);
-  }
-  tmem_wait_st();
-  tc_fence_before();
-  mbar_arrive(ready);
   if (p.kda) {
     const float4* gam = reinterpret_cast<const float4*>(p.gam + tile * kD + k0);
 #pragma unroll
@@ -101,18 +93,20 @@ __device__ __forceinline__ void rev_pass(const RevChainParams& p, float* dh_save
 #pragma unroll
     for (int e = 0; e < 64; ++e) s[e] *= g0;
   }
-  tmem_st32(tl + kTDM + k0, s);
-  tmem_st32(tl + kTDM + k0 + 32, s + 32);
-  tmem_wait_st();
-  tc_fence_before();
-  mbar_arrive(mready);
-  if (!dh_save) return;
-  // re-read the tf32 copy (the MMAs only read it) and save it
-  tmem_ld64(tl + kTDT + k0, s);
-  tmem_wait_ld_regs(s);
-  float* ds = dh_save + tile * kD * kD + size_t(k0) * kD + v;
+  tmem_st32(tl + tm(j + 1) + k0, s);
+  tmem_st32(tl + tm(j + 1) + k0 + 32, s + 32);
+}
+
+// dO^T of the chunk handled at step j (prefetched into `d`: this thread's token columns
+// [t0, t0+32), two bf16 per register) into its TMEM slot tdo(j), a step ahead of its products.
+__device__ __forceinline__ void stage_do(uint32_t tl, int j, int t0, const uint32_t* d) {
+  float df[32];
 #pragma unroll
-  for (int e = 0; e < 64; ++e) ds[size_t(e) * kD] = s[e];
+  for (int i = 0; i < 16; ++i) {
+    df[2 * i] = __uint_as_float(d[i] << 16);
+    df[2 * i + 1] = __uint_as_float(d[i] & 0xffff0000u);
+  }
+  tmem_st32(tl + tdo(j) + t0, df);
 }
 
 }  // namespace
@@ -123,7 +117,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const __grid_constant__ CUtensorMap mdO, const RevChainParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = align1k(smem_raw);
-  __shared__ uint64_t full[2], mma1, mma2, dready, mready, vready;
+  __shared__ uint64_t full[2], mma1, mma2, doready, mready, vready;
   __shared__ uint32_t tslot;
   __shared__ int abort_flag;
 
@@ -151,7 +145,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&full[1], 1);
     mbar_init(&mma1, 1);
     mbar_init(&mma2, 1);
-    mbar_init(&dready, kChainThreads);
+    mbar_init(&doready, kChainThreads);
     mbar_init(&mready, kChainThreads);
     mbar_init(&vready, kChainThreads);
     fence_mbar_init();
@@ -194,23 +188,25 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t par = j & 1;
         const uint32_t base = smem_u32(sm + st * kStage);
         if (!mbar_wait(&full[st], (j >> 1) & 1, &abort_flag, p.status, kDevTimeoutTma)) break;
-        if (!mbar_wait(&dready, par, &abort_flag, p.status, kDevTimeoutSync)) break;
+        // dO^T of this chunk is in its TMEM slot (staged a step ahead); at the first step this
+        // also means the seed gradient is in its buffer
+        if ((use_do || j == 0) && !mbar_wait(&doready, par, &abort_flag, p.status, kDevTimeoutSync)) break;
         tc_fence_after();
-        // dv_new^T = dO^T Aqk + dS'^T Kt^T
+        // dv_new^T = dO^T Aqk + dS'^T Kt^T, with dS' read from its buffer as it is
         if (use_do)
-          for (int s = 0; s < 8; ++s) mma_tf32_ts(tb + kTDV, tb + kTDO + s * 8, desc_kmajor(base + kOffAqkT, 8192, s), id64, s > 0);
+          for (int s = 0; s < 8; ++s) mma_tf32_ts(tb + kTDV, tb + tdo(j) + s * 8, desc_kmajor(base + kOffAqkT, 8192, s), id64, s > 0);
         for (int s = 0; s < 16; ++s)
-          mma_tf32_ts(tb + kTDV, tb + kTDT + s * 8, desc_kmajor(base + kOffKt, 8192, s), id64, use_do || s > 0);
+          mma_tf32_ts(tb + kTDV, tb + tm(j) + s * 8, desc_kmajor(base + kOffKt, 8192, s), id64, use_do || s > 0);
         mma_commit(&mma1);
-        // dS^T += dO^T Qt, once the master copy holds gam dS'^T
+        // dS^T += dO^T Qt, once the other buffer holds gam dS'^T
         if (!mbar_wait(&mready, par, &abort_flag, p.status, kDevTimeoutSync)) break;
         tc_fence_after();
         if (use_do)
-          for (int s = 0; s < 8; ++s) mma_tf32_ts(tb + kTDM, tb + kTDO + s * 8, desc_kmajor(base + kOffQtT, 16384, s), id128, true);
+          for (int s = 0; s < 8; ++s) mma_tf32_ts(tb + tm(j + 1), tb + tdo(j) + s * 8, desc_kmajor(base + kOffQtT, 16384, s), id128, true);
         if (!mbar_wait(&vready, par, &abort_flag, p.status, kDevTimeoutSync)) break;
         tc_fence_after();
         // dS^T += (-dv_new^T) W
-        for (int s = 0; s < 8; ++s) mma_tf32_ts(tb + kTDM, tb + kTDN + s * 8, desc_kmajor(base + kOffWT, 16384, s), id128, true);
+        for (int s = 0; s < 8; ++s) mma_tf32_ts(tb + tm(j + 1), tb + kTDN + s * 8, desc_kmajor(base + kOffWT, 16384, s), id128, true);
         mma_commit(&mma2);
         if (use_do && j + 3 < nc) prefetch_do(c - 3);
         if (!mbar_wait(&mma2, par, &abort_flag, p.status, kDevTimeoutMma)) break;
@@ -234,23 +230,34 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int e = 0; e < 64; ++e)
         buf[e] = src ? src[size_t(e) * kD] : (mode == kRunMapM && k0 + e == v ? 1.f : 0.f);
-      tmem_st32(tl + kTDM + k0, buf);
-      tmem_st32(tl + kTDM + k0 + 32, buf + 32);
+      tmem_st32(tl + tm(0) + k0, buf);
+      tmem_st32(tl + tm(0) + k0 + 32, buf + 32);
       tmem_wait_st();
     }
-    // dO of the chunk after the one being prepared is loaded a whole step ahead of its use
-    uint32_t dnext[16];
-    if (use_do) load_dO(p, last, h, v, t0, dnext);
-    rev_pass(p, dh_save, use_do, last, h, v, k0, t0, tl, &dready, &mready, dnext,
-             p.kda ? 0.f : p.gam[(size_t(last) * H + h) * kD]);
-    if (use_do && nc > 1) load_dO(p, last - 1, h, v, t0, dnext);
     bool alive = true;
+    // dO of the chunk after the one being staged is loaded a whole step ahead of its staging
+    uint32_t dnext[16];
+    if (use_do) {
+      load_dO(p, last, h, v, t0, dnext);
+      stage_do(tl, 0, t0, dnext);
+    }
+    tmem_wait_st();
+    tc_fence_before();
+    mbar_arrive(&doready);   // the seed (and the first chunk's dO^T) are in TMEM
+    if (use_do && nc > 1) load_dO(p, last - 1, h, v, t0, dnext);
+    float g_cur = p.kda ? 0.f : p.gam[(size_t(last) * H + h) * kD];
     for (int j = 0; j < nc; ++j) {
       const int c = last - j;
       const uint32_t par = j & 1;
       const size_t tile = size_t(c) * H + h;
-      // next chunk's scalar gate, loaded early so the dS pass does not wait for it
-      const float gnext = (j + 1 < nc && !p.kda) ? p.gam[(size_t(c - 1) * H + h) * kD] : 0.f;
+      // next chunk's scalar gate, loaded a step ahead of its use
+      const float g_next = (j + 1 < nc && !p.kda) ? p.gam[(size_t(c - 1) * H + h) * kD] : 0.f;
+      // the decayed gradient into the other buffer while the dv_new product reads dS'
+      rev_decay_into(p, dh_save, c, h, v, k0, tl, j, g_cur);
+      g_cur = g_next;
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(&mready);
       if (!mbar_wait(&mma1, par, &abort_flag, p.status, kDevTimeoutMma)) { alive = false; break; }
       tc_fence_after();
       {
@@ -269,12 +276,17 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int t = 0; t < 32; ++t) dv[size_t(t) * kD] = -r[t];
         }
       }
+      // the next chunk's dO^T into the other slot (its last readers, the previous step's
+      // products, completed before that step's final wait)
+      if (use_do && j + 1 < nc) {
+        stage_do(tl, j + 1, t0, dnext);
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(&doready);
+        if (j + 2 < nc) load_dO(p, c - 2, h, v, t0, dnext);
+      }
       if (!mbar_wait(&mma2, par, &abort_flag, p.status, kDevTimeoutMma)) { alive = false; break; }
       tc_fence_after();
-      if (j + 1 < nc) {
-        rev_pass(p, dh_save, use_do, c - 1, h, v, k0, t0, tl, &dready, &mready, dnext, gnext);
-        if (use_do && j + 2 < nc) load_dO(p, c - 2, h, v, t0, dnext);
-      }
     }
     // exit gradient: dh0, the next segment's seed (pass 0), or the segment's map
     float* dst = nullptr;
@@ -290,7 +302,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (alive && dst) {  // the loop's last mma2 wait covers the final update
       float s[64];
-      tmem_ld64(tl + kTDM + k0, s);
+      tmem_ld64(tl + tm(nc) + k0, s);
       tmem_wait_ld_regs(s);
       const size_t off = size_t(k0) * kD + v;
       if (dst_lo) {
