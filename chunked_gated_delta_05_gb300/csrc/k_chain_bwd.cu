@@ -15,10 +15,12 @@
 // step, and the dv_new product reads it there as its A operand (kind::tf32 reads the upper 19
 // bits). While that product runs, the chain warps write gam dS' into the other buffer (and the
 // feature-major kernel's copy of dS'), where the step's two other products accumulate. dO^T is
-// staged in TMEM a step ahead and -dv_new^T written by the chain warps; both are A operands.
-// The chunk tiles (Kt, Aqk^T, Qt^T, W^T, double-buffered) are TMA-loaded SW128 B operands;
-// every product is a 128-lane tf32 MMA. So a step's serial path is the dv_new product, the
-// -dv_new pass and the W^T product. Eight chain warps, one producer warp; all waits bounded.
+// staged in TMEM a step ahead; dv_new^T stays in its accumulator (double-buffered by step) and
+// is the A operand of the W^T product, issued with B negated. The chunk tiles (Kt, Aqk^T,
+// Qt^T, W^T, double-buffered) are TMA-loaded SW128 B operands; every product is a 128-lane
+// tf32 MMA. So a step's serial path is the dv_new product and the W^T product, issued back to
+// back by one thread; the chain warps' decay runs beside the first. Eight chain warps, one
+// producer warp; all waits bounded.
 //
 // As in the forward chain, a CTA runs one segment (segments counted from the sequence's end)
 // in full, or as the segment's adjoint map: from the identity with dO = 0 (M^T, the products
@@ -39,10 +41,10 @@ constexpr uint32_t kOffQtT = 49152;                  // [k][i]  2 panels x 128 r
 constexpr uint32_t kOffWT = 81920;                   // [k][t]  2 panels x 128 rows  (32 KB)
 constexpr uint32_t kSmemBytes = 2 * kStage + 1024;
 // TMEM columns: two dS buffers (the one entering chunk step j is buffer j % 2; the decayed
-// gradient and the step's updates go to the other), dv_new, -dv_new (tf32), and dO^T
+// gradient and the step's updates go to the other), then dv_new and dO^T, each
 // double-buffered by step parity.
-constexpr uint32_t kTDV = 256, kTDN = 320;
 __device__ __forceinline__ uint32_t tm(int j) { return uint32_t(j & 1) * 128; }
+__device__ __forceinline__ uint32_t tdv(int j) { return 256 + uint32_t(j & 1) * 64; }
 __device__ __forceinline__ uint32_t tdo(int j) { return 384 + uint32_t(j & 1) * 64; }
 
 __device__ __forceinline__ uint8_t* align1k(uint8_t* p) {
@@ -117,7 +119,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const __grid_constant__ CUtensorMap mdO, const RevChainParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = align1k(smem_raw);
-  __shared__ uint64_t full[2], mma1, mma2, doready, mready, vready;
+  __shared__ uint64_t full[2], mma1, mma2, doready, mready;
   __shared__ uint32_t tslot;
   __shared__ int abort_flag;
 
@@ -147,7 +149,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&mma2, 1);
     mbar_init(&doready, kChainThreads);
     mbar_init(&mready, kChainThreads);
-    mbar_init(&vready, kChainThreads);
     fence_mbar_init();
   }
   tc_fence_before();
@@ -194,19 +195,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         // dv_new^T = dO^T Aqk + dS'^T Kt^T, with dS' read from its buffer as it is
         if (use_do)
-          for (int s = 0; s < 8; ++s) mma_tf32_ts(tb + kTDV, tb + tdo(j) + s * 8, desc_kmajor(base + kOffAqkT, 8192, s), id64, s > 0);
+          for (int s = 0; s < 8; ++s) mma_tf32_ts(tb + tdv(j), tb + tdo(j) + s * 8, desc_kmajor(base + kOffAqkT, 8192, s), id64, s > 0);
         for (int s = 0; s < 16; ++s)
-          mma_tf32_ts(tb + kTDV, tb + tm(j) + s * 8, desc_kmajor(base + kOffKt, 8192, s), id64, use_do || s > 0);
+          mma_tf32_ts(tb + tdv(j), tb + tm(j) + s * 8, desc_kmajor(base + kOffKt, 8192, s), id64, use_do || s > 0);
         mma_commit(&mma1);
         // dS^T += dO^T Qt, once the other buffer holds gam dS'^T
         if (!mbar_wait(&mready, par, &abort_flag, p.status, kDevTimeoutSync)) break;
         tc_fence_after();
         if (use_do)
           for (int s = 0; s < 8; ++s) mma_tf32_ts(tb + tm(j + 1), tb + tdo(j) + s * 8, desc_kmajor(base + kOffQtT, 16384, s), id128, true);
-        if (!mbar_wait(&vready, par, &abort_flag, p.status, kDevTimeoutSync)) break;
+        if (!mbar_wait(&mma1, par, &abort_flag, p.status, kDevTimeoutMma)) break;
         tc_fence_after();
-        // dS^T += (-dv_new^T) W
-        for (int s = 0; s < 8; ++s) mma_tf32_ts(tb + tm(j + 1), tb + kTDN + s * 8, desc_kmajor(base + kOffWT, 16384, s), id128, true);
+        // dS^T -= dv_new^T W, dv_new read from its accumulator (B negated)
+        for (int s = 0; s < 8; ++s)
+          mma_tf32_ts(tb + tm(j + 1), tb + tdv(j) + s * 8, desc_kmajor(base + kOffWT, 16384, s), id128 | (1u << 14), true);
         mma_commit(&mma2);
         if (use_do && j + 3 < nc) prefetch_do(c - 3);
         if (!mbar_wait(&mma2, par, &abort_flag, p.status, kDevTimeoutMma)) break;
@@ -260,21 +262,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_arrive(&mready);
       if (!mbar_wait(&mma1, par, &abort_flag, p.status, kDevTimeoutMma)) { alive = false; break; }
       tc_fence_after();
-      {
+      if (dvn_save) {
+        // dv_new for the feature-major kernel (rounded to tf32); its buffer is rewritten two
+        // steps on, after this thread's next mready arrival
         float r[32];
-        tmem_ld32(tl + kTDV + t0, r);
+        tmem_ld32(tl + tdv(j) + t0, r);
         tmem_wait_ld_regs(r);
+        float* dv = dvn_save + tile * kTileW + size_t(t0) * kD + v;
 #pragma unroll
-        for (int t = 0; t < 32; ++t) r[t] = -to_tf32(r[t]);
-        tmem_st32(tl + kTDN + t0, r);
-        tmem_wait_st();
-        tc_fence_before();
-        mbar_arrive(&vready);
-        if (dvn_save) {
-          float* dv = dvn_save + tile * kTileW + size_t(t0) * kD + v;
-#pragma unroll
-          for (int t = 0; t < 32; ++t) dv[size_t(t) * kD] = -r[t];
-        }
+        for (int t = 0; t < 32; ++t) dv[size_t(t) * kD] = to_tf32(r[t]);
       }
       // the next chunk's dO^T into the other slot (its last readers, the previous step's
       // products, completed before that step's final wait)
