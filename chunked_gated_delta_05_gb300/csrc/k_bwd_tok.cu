@@ -74,7 +74,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __shared__ uint64_t bar_tma, bar_tma2, bar_mma;
   __shared__ uint32_t tslot;
   __shared__ int abort_flag;
-  __shared__ float s_G[kC], s_G2[kC], s_rq[kC], s_rk[kC], s_b[kC], s_dG[kC], s_db[kC], s_P[kC][kC + 1];
+  __shared__ float s_G[kC], s_G2[kC], s_rq[kC], s_rk[kC], s_b[kC], s_e1[kC], s_dG[kC], s_db[kC], s_P[kC][kC + 1];
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int c = blockIdx.x, h = blockIdx.y + p.hg0, H = p.H;
@@ -131,6 +131,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     s_rq[tid] = ok ? rq : 0.f;
     s_rk[tid] = ok ? rk : 0.f;
     s_b[tid] = ok ? b : 0.f;
+    s_e1[tid] = ok ? b * expf(G) * rk : 0.f;   // the row scale of K1
     s_dG[tid] = 0.f;
     s_db[tid] = 0.f;
   }
@@ -141,12 +142,31 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tl = tb + tmem_lane_base(warp);
   const float Glast = s_G[len - 1];
   const bool tma_ok = mbar_wait(&bar_tma, 0, &abort_flag, p.status, kDevTimeoutTma);
-  // dO as a 64-row tf32 operand [i][v] (rows past the chunk are zero).
+  // dO as a 64-row tf32 operand [i][v] (rows past the chunk are zero): thread row tid / 4,
+  // 32 columns, eight per 16-byte read of the bf16 tile.
   {
-    const int v = tid & 127, t0 = 32 * half;
-#pragma unroll 8
-    for (int e = 0; e < 32; ++e)
-      put32(sm + kR1, kC, t0 + e, v, (t0 + e < len) ? bf16_at(sm + kOffDO, t0 + e, v) : 0.f);
+    const int t = tid >> 2, cq = 32 * (tid & 3);
+    const bool in = t < len;
+#pragma unroll
+    for (int c8 = 0; c8 < 4; ++c8) {
+      const int col = cq + 8 * c8;
+      float f[8];
+      if (in) {
+        const uint4 u = *reinterpret_cast<const uint4*>(sm + kOffDO + sw128_offset(t, col, kC, 2));
+        const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&u);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float2 x = __bfloat1622float2(b2[e]);
+          f[2 * e] = x.x;
+          f[2 * e + 1] = x.y;
+        }
+      } else {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) f[e] = 0.f;
+      }
+      put32x4(sm + kR1, kC, t, col, f[0], f[1], f[2], f[3]);
+      put32x4(sm + kR1, kC, t, col + 4, f[4], f[5], f[6], f[7]);
+    }
   }
   // Rows of q, k, v past the chunk belong to the next document (or are zero): clear them so
   // the exact Gram products below see zeros there.
@@ -182,7 +202,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int c0 = 4 * lane;
 #pragma unroll 2
     for (int j = warp; j < kC; j += 8) {
-      const float s1 = s_b[j] * expf(s_G[j]) * s_rk[j], s2 = s_b[j];
+      const float s1 = s_e1[j], s2 = s_b[j];
       float kf[4], vf[4];
       bf16x4_at(sK, j, c0, kf);
       bf16x4_at(sV, j, c0, vf);
