@@ -17,6 +17,8 @@
 // TMA too (128-row boxes, 128-byte swizzle), so each thread reads its row from shared memory
 // without bank conflicts. Results leave as token-major fp32 rows [t][f] (coalesced: the 128
 // threads of one token row write 512 contiguous bytes).
+// (An L2 prefetch of the next wave's inputs made the whole step slower: with the heads split
+// over two streams it competes with the other group's kernels.)
 #include "common.cuh"
 #include "umma.cuh"
 
@@ -156,18 +158,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int s = 0; s < 16; ++s) mma_tf32_ts(tb + kTP3, tb + kTDH + s * 8, desc_kmajor(sVN, 8192, s), id64, s > 0);
       }
       mma_commit(&bar_mma);
-    }
-    // while the products run: the next wave's CTA finds its inputs in L2
-    int nx, ny;
-    if (next_wave_block(p.sms, &nx, &ny)) {
-      const size_t nt = size_t(nx) * H + ny + p.hg0;
-      prefetch_l2(p.h + nt * kD * kD, 4u * kD * kD);
-      prefetch_l2(p.dh + nt * kD * kD, 4u * kD * kD);
-      prefetch_l2(p.A + nt * kTileAqk, 4u * kTileAqk);
-      for (int pp = 0; pp < 4; ++pp) {
-        prefetch_l2_tile(&mVN, pp * 32, int(nt) * kC);
-        prefetch_l2_tile(&mDVN, pp * 32, int(nt) * kC);
-      }
     }
   }
   __syncwarp();
