@@ -787,7 +787,7 @@ int run_bwd(const gdn_desc_t* d, const gdn_bwd_args_t* a, void* stream, bool kda
       if (rc) return rc;
       {
         TimedLaunch tl_(kKBwdTok, sg);
-        rc = check_cuda(kda ? launch_bwd_tok_kda(M.q, M.k, M.v, M.VN, M.DW, M.DVN, tp, sg)
+        rc = check_cuda(kda ? launch_bwd_tok_kda(M.q, M.k, M.v, M.VN, M.DW, M.DVN, M.dO, tp, sg)
                             : launch_bwd_tok(M.q, M.k, M.v, M.dO, M.VN, M.DW, M.DVN, tp, sg),
                         "token-major backward kernel");
       }

@@ -235,7 +235,7 @@ cudaError_t launch_bwd_tok(const CUtensorMap& mq, const CUtensorMap& mk, const C
                            cudaStream_t s);
 cudaError_t launch_bwd_tok_kda(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
                                const CUtensorMap& mVN, const CUtensorMap& mDW, const CUtensorMap& mDVN,
-                               const BwdTokParams& p, cudaStream_t s);
+                               const CUtensorMap& mdO, const BwdTokParams& p, cudaStream_t s);
 struct GroupSumParams {
   const float *dq32, *dk32;    // [R,H,K]
   __nv_bfloat16 *dq, *dk;      // [R,H/G,K]

@@ -174,7 +174,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     k_bwd_tok_kda(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
                   const __grid_constant__ CUtensorMap mv, const __grid_constant__ CUtensorMap mVN,
                   const __grid_constant__ CUtensorMap mDW, const __grid_constant__ CUtensorMap mDVN,
-                  const BwdTokParams p) {
+                  const __grid_constant__ CUtensorMap mdO, const BwdTokParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = align1k(smem_raw);
   uint8_t* sQ = sm + kOffQ;
@@ -220,7 +220,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tb = tslot;
   const uint32_t tl = tb + tmem_lane_base(warp);
   if (tid == 0) {
-    mbar_expect_tx(&bar_tma, 3u * 16384u + 3u * 32768u);
+    // q, k, v, v_new, dW, dU; the chunk's G tile (bulk copy into R1) and dO (bf16, into the G
+    // area) for the staging below
+    mbar_expect_tx(&bar_tma, 4u * 16384u + 4u * 32768u);
+    bulk_load(sm + kR1, p.Gc + tile * kC * kD, 32768u, &bar_tma);
+    for (int pp = 0; pp < 2; ++pp) tma_load_2d(sm + kOffG + pp * 8192, &mdO, h * kD + 64 * pp, ch.x, &bar_tma);
     for (int pp = 0; pp < 2; ++pp) {
       const int x = h * kD + 64 * pp, xqk = (h / p.qk_group) * kD + 64 * pp;
       tma_load_2d(sQ + pp * 8192, &mq, xqk, ch.x, &bar_tma);
@@ -234,25 +238,25 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
   // G (scaled to log2 units) and dO as a 64-row tf32 operand; rows past the chunk are zero.
+  // Both arrived with the other copies (G in R1, dO in the G area): each thread reads its
+  // values into registers and, once every thread has, writes them to their places.
+  const bool tma_ok = mbar_wait(&bar_tma, 0, &abort_flag, p.status, kDevTimeoutTma);
   {
     const int t0 = 32 * half;
-    const float* gsrc = p.Gc + (tile * kC + t0) * kD + cc;
-    const __nv_bfloat16* src = p.dO + (size_t(ch.x) * H + h) * kD + cc;
+    const float* gt = reinterpret_cast<const float*>(sm + kR1);
     float bg[32], bo[32];
 #pragma unroll
     for (int e = 0; e < 32; ++e) {
-      bg[e] = gsrc[size_t(e) * kD];
-      bo[e] = (t0 + e < len) ? __bfloat162float(src[size_t(t0 + e) * H * kD]) : 0.f;
+      bg[e] = gt[(t0 + e) * kD + cc];
+      bo[e] = (t0 + e < len) ? bf16_at(sm + kOffG, t0 + e, cc) : 0.f;
     }
+    __syncthreads();
 #pragma unroll
     for (int e = 0; e < 32; ++e) {
       sG2[(t0 + e) * kP + cc] = bg[e] * kLog2e;
       put32(sm + kR1, kC, t0 + e, cc, bo[e]);
     }
   }
-  fence_async_smem();
-  __syncthreads();
-  const bool tma_ok = mbar_wait(&bar_tma, 0, &abort_flag, p.status, kDevTimeoutTma);
   if (tid >= len && tid < kC) {
     for (int c16 = 0; c16 < 16; ++c16) {
       const uint32_t off = sw128_offset(tid, c16 * 8, kC, 2);
@@ -513,7 +517,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 cudaError_t launch_bwd_tok_kda(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
                                const CUtensorMap& mVN, const CUtensorMap& mDW, const CUtensorMap& mDVN,
-                               const BwdTokParams& p, cudaStream_t s) {
+                               const CUtensorMap& mdO, const BwdTokParams& p, cudaStream_t s) {
   static bool attr = false;
   if (!attr) {
     cudaError_t e = cudaFuncSetAttribute(k_bwd_tok_kda, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
@@ -521,7 +525,7 @@ cudaError_t launch_bwd_tok_kda(const CUtensorMap& mq, const CUtensorMap& mk, con
     attr = true;
   }
   dim3 grid(p.NC, p.hgn);
-  k_bwd_tok_kda<<<grid, kThreads, kSmemBytes, s>>>(mq, mk, mv, mVN, mDW, mDVN, p);
+  k_bwd_tok_kda<<<grid, kThreads, kSmemBytes, s>>>(mq, mk, mv, mVN, mDW, mDVN, mdO, p);
   return cudaGetLastError();
 }
 
