@@ -190,9 +190,9 @@ struct Layout {
   size_t cu, seqs, chunks, W, U, Qt, KtT, Aqk, gam;               // forward
   size_t Kt, QtT, AqkT, WT, A, Gc, rq, rk, beff;                  // prepare, backward mode
   size_t hs, vns;                                                  // forward chain saves
-  size_t fE, fPhi, fPlo, fB;                                       // forward chain scan (scratch)
+  size_t fE, fPhi, fB;                                       // forward chain scan (scratch)
   size_t dhs, dvns, dQt, dKt, dW, dK1, dV1, dgam;                  // rest part (relative)
-  size_t rE, rPhi, rPlo, rB;                                       // reverse chain scan (rest part)
+  size_t rE, rPhi, rB;                                       // reverse chain scan (rest part)
   size_t dq32, dk32;                                               // grouped q/k: per-value-head dq, dk
   size_t dA_part, ddt_part;                                        // in-kernel gate: parameter partials
   size_t saved_total, rest_total, total;
@@ -234,7 +234,6 @@ Layout make_layout(const Problem& P, bool backward, bool kda = false) {
   const size_t scan_states = L.plan.maxS > 1 ? size_t(P.N) * L.plan.maxS * P.H * kD * kD * 4 : 0;
   L.fE = take(scan_states);
   L.fPhi = take(scan_states);
-  L.fPlo = take(scan_states);
   L.fB = take(scan_states);
   L.saved_total = off;
   off = 0;
@@ -249,7 +248,6 @@ Layout make_layout(const Problem& P, bool backward, bool kda = false) {
     L.dgam = take(4 * tiles * kD);
     L.rE = take(scan_states);
     L.rPhi = take(scan_states);
-    L.rPlo = take(scan_states);
     L.rB = take(scan_states);
     const size_t per_head = P.G > 1 ? size_t(P.R) * P.H * kD * 4 : 0;
     L.dq32 = take(per_head);
@@ -419,14 +417,13 @@ int build_tables(const Problem& P, void* ws, const Layout& L, int* status, cudaS
   return check_cuda(launch_tables(tp, s), "chunk tables");
 }
 
-SegPlan seg_plan(const ScanPlan& sc, char* base, size_t E, size_t Phi, size_t Plo, size_t B) {
+SegPlan seg_plan(const ScanPlan& sc, char* base, size_t E, size_t Phi, size_t B) {
   SegPlan sp{};
   sp.L = sc.L;
   sp.maxS = sc.maxS;
   sp.pass = 0;
   sp.E = reinterpret_cast<float*>(base + E);
   sp.Phi = reinterpret_cast<float*>(base + Phi);
-  sp.Plo = reinterpret_cast<float*>(base + Plo);
   sp.Bm = reinterpret_cast<float*>(base + B);
   return sp;
 }
@@ -507,12 +504,6 @@ class HeadGroups {
 // heads hg0 .. hg0 + hgn - 1.
 int run_compose(const Problem& P, const SeqEntry* seqs, const SegPlan& sp, int* status, int hg0, int hgn,
                 cudaStream_t s) {
-  const uint64_t rows = uint64_t(P.N) * sp.maxS * P.H * kD;
-  CUtensorMap mPhi, mPlo, mB;
-  if (!tile_map(&mPhi, reinterpret_cast<const char*>(sp.Phi), kD, rows, 128, true) ||
-      !tile_map(&mPlo, reinterpret_cast<const char*>(sp.Plo), kD, rows, 128, true) ||
-      !tile_map(&mB, reinterpret_cast<const char*>(sp.Bm), kD, rows, 128, false))
-    return fail(GDN_ECUDA, "cuTensorMapEncodeTiled failed");
   ComposeParams cp{};
   cp.seqs = seqs;
   cp.N = P.N;
@@ -522,7 +513,7 @@ int run_compose(const Problem& P, const SeqEntry* seqs, const SegPlan& sp, int* 
   cp.sp = sp;
   cp.status = status;
   TimedLaunch tl_(kKCompose, s);
-  return check_cuda(launch_compose(mPhi, mPlo, mB, cp, s), "compose kernel");
+  return check_cuda(launch_compose(cp, s), "compose kernel");
 }
 
 // Forward chain: one plain pass, or pass 0, compose, pass 1 of the segmented chain.
@@ -607,7 +598,7 @@ int run_fwd(const gdn_desc_t* d, const gdn_fwd_args_t* a, void* stream, bool kda
     cp.vnew_save = reinterpret_cast<float*>(ws + L.vns);
   }
   cp.status = a->status;
-  cp.sp = seg_plan(L.plan, ws, L.fE, L.fPhi, L.fPlo, L.fB);
+  cp.sp = seg_plan(L.plan, ws, L.fE, L.fPhi, L.fB);
   HeadGroups groups(P, false, s);
   for (int g = 0; g < groups.count(); ++g) {
     const cudaStream_t sg = groups.stream(g);
@@ -693,7 +684,7 @@ int run_bwd(const gdn_desc_t* d, const gdn_bwd_args_t* a, void* stream, bool kda
     cp.h_save = F(L.hs);
     cp.vnew_save = F(L.vns);
     cp.status = a->status;
-    cp.sp = seg_plan(L.plan, sv, L.fE, L.fPhi, L.fPlo, L.fB);
+    cp.sp = seg_plan(L.plan, sv, L.fE, L.fPhi, L.fB);
   }
 
   RevChainParams rp{};
@@ -709,7 +700,7 @@ int run_bwd(const gdn_desc_t* d, const gdn_bwd_args_t* a, void* stream, bool kda
   rp.dh_save = R(L.dhs);
   rp.dvn_save = R(L.dvns);
   rp.status = a->status;
-  rp.sp = seg_plan(L.plan, rs, L.rE, L.rPhi, L.rPlo, L.rB);
+  rp.sp = seg_plan(L.plan, rs, L.rE, L.rPhi, L.rB);
 
   BwdFeatParams fp{};
   fp.chunks = chunks;

@@ -60,8 +60,7 @@ struct SegPlan {
   int maxS;    // most segments of any sequence (1 = plain chain)
   int pass;    // 0 or 1
   float* E;    // [N*maxS*H][128][128] entry state (reverse: exit gradient) of each segment
-  float* Phi;  // [N*maxS*H][128][128] segment map M, tf32 high part
-  float* Plo;  // [N*maxS*H][128][128] segment map M, tf32 low part (M - Phi, rounded)
+  float* Phi;  // [N*maxS*H][128][128] segment map M, transposed (row j = column j of M), fp32
   float* Bm;   // [N*maxS*H][128][128] segment offset B
 };
 
@@ -263,8 +262,7 @@ struct GateGradParams {
   int NC, H;
 };
 cudaError_t launch_gate_grad(const GateGradParams& p, cudaStream_t s);
-cudaError_t launch_compose(const CUtensorMap& mPhi, const CUtensorMap& mPlo, const CUtensorMap& mB,
-                           const ComposeParams& p, cudaStream_t s);
+cudaError_t launch_compose(const ComposeParams& p, cudaStream_t s);
 cudaError_t launch_chain_fwd(const CUtensorMap& mW, const CUtensorMap& mQt, const CUtensorMap& mKtT,
                              const CUtensorMap& mAqk, const CUtensorMap& mU, const ChainParams& p,
                              cudaStream_t s);

@@ -314,13 +314,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     // exit state: the final state, the next segment's entry (pass 0), or the segment's map
     float* dst = nullptr;
-    float* dst_lo = nullptr;
     if (mode == kRunFull) {
       if (seg == ns - 1) dst = p.hT ? p.hT + (size_t(n) * H + h) * kD * kD : nullptr;
       else if (sp.pass == 0) dst = sp.E + ((slot_base + seg + 1) * H + h) * kD * kD;
     } else if (mode == kRunMapM) {
       dst = sp.Phi + ((slot_base + seg) * H + h) * kD * kD;
-      dst_lo = sp.Plo + ((slot_base + seg) * H + h) * kD * kD;
     } else {
       dst = sp.Bm + ((slot_base + seg) * H + h) * kD * kD;
     }
@@ -329,13 +327,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_ld64(tb + lb + ts(nc) + k0, s);
       tmem_wait_ld_regs(s);
       const size_t off = size_t(k0) * kD + v;
-      if (dst_lo) {
+      if (mode == kRunMapM) {
+        // the map transposed: this thread's row v of M^T, columns k0 .. k0+63 (the compose
+        // step reads four rows of M at a time as one 16-byte load)
+        float4* row = reinterpret_cast<float4*>(dst + size_t(v) * kD + k0);
 #pragma unroll
-        for (int e = 0; e < 64; ++e) {
-          const float hi = to_tf32(s[e]);
-          dst[off + size_t(e) * kD] = hi;
-          dst_lo[off + size_t(e) * kD] = to_tf32(s[e] - hi);
-        }
+        for (int e = 0; e < 16; ++e) row[e] = make_float4(s[4 * e], s[4 * e + 1], s[4 * e + 2], s[4 * e + 3]);
       } else {
 #pragma unroll
         for (int e = 0; e < 64; ++e) dst[off + size_t(e) * kD] = s[e];

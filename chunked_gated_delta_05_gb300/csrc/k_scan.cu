@@ -10,170 +10,122 @@
 // Ascend GDN Diff Coverage page). Here the "ranks" are segments of one sequence on one GPU,
 // and the reverse chain's adjoint maps compose the same way.
 //
-// GB300 mapping: one CTA of 128 threads per (sequence, head). E^T lives in TMEM (lane v =
-// column v of E) as two tf32 parts, E_hi + E_lo; M arrives by TMA as its two tf32 parts
-// (K-major SW128 B operands) together with B_s (the next step's copies are issued as soon as
-// the MMAs are done, under the epilogue); the product is accumulated in TMEM on top of B_s^T with three
-// tf32 MMA groups, E_hi M_hi + E_lo M_hi + E_hi M_lo, so the composition keeps fp32 accuracy
-// (split-tf32 products; the dropped E_lo M_lo term is below fp32 rounding). Thread 0 issues
-// the copies and the MMAs. All waits bounded; every exit decision is taken CTA-wide.
+// GB300 mapping: the columns of E are independent, so each (sequence, head) is split over
+// kColBlocks CTAs of kCols columns, and the walk runs on the CUDA cores in fp32 (a 128x128x16
+// product per step and CTA, about a microsecond; the tensor-core version needed three
+// split-tf32 products to keep fp32 accuracy and ran on N*H CTAs only). M_s arrives transposed
+// (row j = column j of M, as the map runs write it) by one bulk copy per step into a double
+// buffer, so the next step's map is in flight while this step computes; the CTA's columns of
+// E stay in shared memory between steps. Thread t computes rows 4 (t / 8) .. +3 and columns
+// 2 (t % 8), +1 of the block. All waits bounded; every exit decision is taken CTA-wide.
 #include "common.cuh"
 #include "umma.cuh"
 
 namespace gdn {
 namespace {
 
-constexpr int kThreads = 128;
-constexpr uint32_t kMapBytes = 65536;        // one 128 x 128 fp32 map part: 4 panels x 128 rows x 128 B
-constexpr uint32_t kOffHi = 0, kOffLo = kMapBytes, kOffB = 2 * kMapBytes;  // B: 4 plain [128][32] panels
-constexpr uint32_t kSmemBytes = 3 * kMapBytes + 1024;
-constexpr uint32_t kTD = 0, kTEH = 128, kTEL = 256;
-
-__device__ __forceinline__ uint8_t* align1k(uint8_t* p) {
-  return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
-}
+constexpr int kThreads = 256;
+constexpr int kCols = 16;                      // columns of E per CTA
+constexpr int kColBlocks = kD / kCols;         // CTAs per (sequence, head)
+constexpr uint32_t kMapBytes = kD * kD * 4;    // one transposed map, [j][k] fp32
+constexpr uint32_t kOffM = 0;                  // two map buffers
+constexpr uint32_t kOffE = 2 * kMapBytes;      // [128][kCols] fp32: the current E block
+constexpr uint32_t kSmemBytes = kOffE + kD * kCols * 4 + 16;
 
 }  // namespace
 
-__global__ void __launch_bounds__(kThreads, 1)
-    k_compose(const __grid_constant__ CUtensorMap mPhi, const __grid_constant__ CUtensorMap mPlo,
-              const __grid_constant__ CUtensorMap mB, const ComposeParams p) {
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* sm = align1k(smem_raw);
-  __shared__ uint64_t full, mma;
-  __shared__ uint32_t tslot;
+__global__ void __launch_bounds__(kThreads, 1) k_compose(const ComposeParams p) {
+  extern __shared__ __align__(16) uint8_t smem_c[];
+  __shared__ uint64_t full[2];
   __shared__ int abort_flag;
 
-  const int tid = threadIdx.x, warp = tid >> 5;
-  const int n = blockIdx.x, h = blockIdx.y + p.hg0, H = p.H;
+  const int tid = threadIdx.x;
+  const int n = blockIdx.x / kColBlocks, cb = blockIdx.x % kColBlocks;
+  const int h = blockIdx.y + p.hg0, H = p.H;
   const SegPlan& sp = p.sp;
   const int ns = (p.seqs[n].y + sp.L - 1) / sp.L;
   if (ns < 3) return;  // nothing between the fully-run first segment and pass 1
   const size_t slot_base = size_t(n) * sp.maxS;
   auto slot = [&](int s) { return (slot_base + s) * H + h; };
-  // copies of step s: both parts of M_s (swizzled K-major B operands) and B_s (plain panels)
-  auto issue = [&](int s) {
-    const int y = int(slot(s)) * kD;
-    mbar_expect_tx(&full, 3 * kMapBytes);
-    for (int pp = 0; pp < 4; ++pp) {
-      tma_load_2d(sm + kOffHi + pp * 16384, &mPhi, pp * 32, y, &full);
-      tma_load_2d(sm + kOffLo + pp * 16384, &mPlo, pp * 32, y, &full);
-      tma_load_2d(sm + kOffB + pp * 16384, &mB, pp * 32, y, &full);
-    }
-  };
+  float* sE = reinterpret_cast<float*>(smem_c + kOffE);
+  const int c0 = cb * kCols;                         // first column of this CTA
+  const int k0 = 4 * (tid >> 3), vp = 2 * (tid & 7);  // this thread's rows and column pair
 
-  if (warp == 0) tmem_alloc(&tslot, 512);
   if (tid == 0) {
     abort_flag = 0;
-    mbar_init(&full, 1);
-    mbar_init(&mma, 1);
+    mbar_init(&full[0], 1);
+    mbar_init(&full[1], 1);
     fence_mbar_init();
+    mbar_expect_tx(&full[0], kMapBytes);
+    bulk_load(smem_c + kOffM, sp.Phi + slot(1) * kD * kD, kMapBytes, &full[0]);
   }
-  tc_fence_before();
+  // E[1] columns c0 .. c0 + kCols - 1 (row j: 16 floats, two threads of a row per 32 bytes)
+  for (int i = tid; i < kD * kCols / 4; i += kThreads) {
+    const int j = i / (kCols / 4), q4 = i % (kCols / 4);
+    reinterpret_cast<float4*>(sE)[i] =
+        *reinterpret_cast<const float4*>(sp.E + slot(1) * kD * kD + size_t(j) * kD + c0 + 4 * q4);
+  }
   __syncthreads();
-  tc_fence_after();
-  const uint32_t tb = tslot;
-  const uint32_t tl = tb + tmem_lane_base(warp);
-  const int v = tid;
-  const uint32_t sHi = smem_u32(sm + kOffHi), sLo = smem_u32(sm + kOffLo);
-  const float* sBm = reinterpret_cast<const float*>(sm + kOffB) + (v >> 5) * 4096 + (v & 31);
-
-  if (tid == 0) {
-    issue(1);
-    // the later maps start their trip to L2 now (the walk is serial)
-    for (int s = 2; s <= ns - 2; ++s) {
-      prefetch_l2(sp.Phi + slot(s) * kD * kD, 4u * kD * kD);
-      prefetch_l2(sp.Plo + slot(s) * kD * kD, 4u * kD * kD);
-      prefetch_l2(sp.Bm + slot(s) * kD * kD, 4u * kD * kD);
-    }
-  }
-  // E[1]^T row v, split into its tf32 parts
-  {
-    const float* src = sp.E + slot(1) * kD * kD + v;
-#pragma unroll 1
-    for (int g = 0; g < 4; g += 2) {
-      float x[64];
-#pragma unroll
-      for (int e = 0; e < 64; ++e) x[e] = src[size_t(32 * g + e) * kD];
-#pragma unroll
-      for (int hh = 0; hh < 2; ++hh) {
-        float hi[32], lo[32];
-#pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          hi[e] = to_tf32(x[32 * hh + e]);
-          lo[e] = to_tf32(x[32 * hh + e] - hi[e]);
-        }
-        tmem_st32(tl + kTEH + 32 * (g + hh), hi);
-        tmem_st32(tl + kTEL + 32 * (g + hh), lo);
-      }
-    }
-  }
-  const uint32_t id = idesc_tf32(128, 128);
 #pragma unroll 1
   for (int s = 1; s <= ns - 2; ++s) {
-    const uint32_t par = (s - 1) & 1;
-    bool ok = mbar_wait(&full, par, &abort_flag, p.status, kDevTimeoutTma);
-    if (ok) {
-      // accumulator <- B_s^T (lane v = column v of B_s), from the staged plain panels
-#pragma unroll 1
-      for (int g = 0; g < 4; ++g) {
-        float b[32];
+    const int buf = (s - 1) & 1;
+    // the offset rows of this step, requested before the map is waited for
+    const float* Bs = sp.Bm + slot(s) * kD * kD + size_t(k0) * kD + c0 + vp;
+    float acc[4][2];
 #pragma unroll
-        for (int e = 0; e < 32; ++e) b[e] = sBm[(32 * g + e) * 32];
-        tmem_st32(tl + kTD + 32 * g, b);
-      }
+    for (int kk = 0; kk < 4; ++kk) {
+      const float2 b = *reinterpret_cast<const float2*>(Bs + size_t(kk) * kD);
+      acc[kk][0] = b.x;
+      acc[kk][1] = b.y;
     }
-    tmem_wait_st();
-    tc_fence_before();
-    if (__syncthreads_or(!ok)) break;
-    if (tid == 0) {
-      tc_fence_after();
-      for (int k = 0; k < 16; ++k) mma_tf32_ts(tb + kTD, tb + kTEH + k * 8, desc_kmajor(sHi, 16384, k), id, true);
-      for (int k = 0; k < 16; ++k) mma_tf32_ts(tb + kTD, tb + kTEL + k * 8, desc_kmajor(sHi, 16384, k), id, true);
-      for (int k = 0; k < 16; ++k) mma_tf32_ts(tb + kTD, tb + kTEH + k * 8, desc_kmajor(sLo, 16384, k), id, true);
-      mma_commit(&mma);
+    const bool ok = mbar_wait(&full[buf], ((s - 1) >> 1) & 1, &abort_flag, p.status, kDevTimeoutTma);
+    if (__syncthreads_or(!ok)) {
+      // the only copy that can be in flight is this step's (the next one is issued after a
+      // successful wait): let it land before the CTA's shared memory goes
+      if (tid == 0) mbar_drain(&full[buf], ((s - 1) >> 1) & 1);
+      break;
     }
-    ok = mbar_wait(&mma, par, &abort_flag, p.status, kDevTimeoutMma);
-    if (__syncthreads_or(!ok)) break;
-    tc_fence_after();
-    // the next step's copies overlap this step's epilogue (the MMAs no longer read the tiles)
-    if (tid == 0 && s + 1 <= ns - 2) issue(s + 1);
-    // E[s+1]^T row v: store it, and split it into the next step's operand
-    {
-      float* dst = sp.E + slot(s + 1) * kD * kD + v;
-#pragma unroll 1
-      for (int g = 0; g < 4; ++g) {
-        float r[32];
-        tmem_ld32(tl + kTD + 32 * g, r);
-        tmem_wait_ld_regs(r);
-        float lo[32];
+    // the next step's map into the other buffer (its last readers finished the previous step)
+    if (tid == 0 && s + 1 <= ns - 2) {
+      mbar_expect_tx(&full[buf ^ 1], kMapBytes);
+      bulk_load(smem_c + kOffM + (buf ^ 1) * kMapBytes, sp.Phi + slot(s + 1) * kD * kD, kMapBytes, &full[buf ^ 1]);
+    }
+    // E[s+1] = M_s E[s] + B_s for rows k0..k0+3, columns vp, vp+1 of the block
+    const float* Mt = reinterpret_cast<const float*>(smem_c + kOffM + buf * kMapBytes);
+#pragma unroll 4
+    for (int j = 0; j < kD; ++j) {
+      const float4 m = *reinterpret_cast<const float4*>(Mt + j * kD + k0);   // M[k0..k0+3][j]
+      const float2 e = *reinterpret_cast<const float2*>(sE + j * kCols + vp);
+      acc[0][0] = fmaf(m.x, e.x, acc[0][0]);
+      acc[0][1] = fmaf(m.x, e.y, acc[0][1]);
+      acc[1][0] = fmaf(m.y, e.x, acc[1][0]);
+      acc[1][1] = fmaf(m.y, e.y, acc[1][1]);
+      acc[2][0] = fmaf(m.z, e.x, acc[2][0]);
+      acc[2][1] = fmaf(m.z, e.y, acc[2][1]);
+      acc[3][0] = fmaf(m.w, e.x, acc[3][0]);
+      acc[3][1] = fmaf(m.w, e.y, acc[3][1]);
+    }
+    __syncthreads();  // every thread has read E[s]
+    float* dst = sp.E + slot(s + 1) * kD * kD + size_t(k0) * kD + c0 + vp;
 #pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          dst[size_t(32 * g + e) * kD] = r[e];
-          const float hi = to_tf32(r[e]);
-          lo[e] = to_tf32(r[e] - hi);
-          r[e] = hi;
-        }
-        tmem_st32(tl + kTEH + 32 * g, r);
-        tmem_st32(tl + kTEL + 32 * g, lo);
-      }
+    for (int kk = 0; kk < 4; ++kk) {
+      const float2 r = make_float2(acc[kk][0], acc[kk][1]);
+      *reinterpret_cast<float2*>(sE + (k0 + kk) * kCols + vp) = r;
+      *reinterpret_cast<float2*>(dst + size_t(kk) * kD) = r;
     }
+    __syncthreads();
   }
-  tc_fence_before();
-  __syncthreads();
-  if (warp == 0) tmem_dealloc(tb, 512);
 }
 
-cudaError_t launch_compose(const CUtensorMap& mPhi, const CUtensorMap& mPlo, const CUtensorMap& mB,
-                           const ComposeParams& p, cudaStream_t s) {
+cudaError_t launch_compose(const ComposeParams& p, cudaStream_t s) {
   static bool attr = false;
   if (!attr) {
     cudaError_t e = cudaFuncSetAttribute(k_compose, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     if (e != cudaSuccess) return e;
     attr = true;
   }
-  dim3 grid(p.N, p.hgn);
-  k_compose<<<grid, kThreads, kSmemBytes, s>>>(mPhi, mPlo, mB, p);
+  dim3 grid(p.N * kColBlocks, p.hgn);
+  k_compose<<<grid, kThreads, kSmemBytes, s>>>(p);
   return cudaGetLastError();
 }
 
