@@ -68,16 +68,16 @@ KERNEL_SOURCES_KDA = {**KERNEL_SOURCES, "prepare": "k_prep_kda.cu", "bwd_tok": "
 # each, all heads in one group). The chunk kernels' traffic is per chunk-head, so the
 # B=1 T=32768 H=16 entries are those bytes x 4 (8192 chunk-heads) and the B=1 T=8192 H=32 KDA
 # entries x 2 (4096); the chains' traffic depends on the segment plan and is not scaled.
-_GDN_T4096 = {"prepare": 615_838_976, "chain_fwd": 612_954_880, "compose": 42_014_464, "chain_bwd": 594_893_824,
-              "bwd_feat": 768_514_304, "bwd_tok": 731_632_896}
-_KDA_T4096 = {"prepare": 748_162_560, "compose": 42_013_696, "chain_bwd": 593_397_504,
-              "bwd_feat": 774_079_488, "bwd_tok": 853_418_240}
-_HASHES = {("prepare", False): "aabf7e6125f0f065", ("bwd_feat", False): "5c86929f2f18a973",
-           ("bwd_tok", False): "40418ce70a38e1a1", ("chain_fwd", False): "806d6bdc6bfaed1f",
-           ("chain_bwd", False): "f2408d66f7b654b9", ("compose", False): "f43302a78ee98062",
-           ("prepare", True): "23c3e57d49b6616a", ("bwd_feat", True): "5c86929f2f18a973",
-           ("bwd_tok", True): "43b6d9807353fc18", ("chain_fwd", True): "2436ef14feb8b48b",
-           ("chain_bwd", True): "f2408d66f7b654b9", ("compose", True): "f43302a78ee98062"}
+_GDN_T4096 = {"prepare": 615_744_512, "chain_fwd": 606_034_688, "compose": 29_376_000,
+              "chain_bwd": 582_142_464, "bwd_feat": 758_795_264, "bwd_tok": 731_686_912}
+_KDA_T4096 = {"prepare": 748_054_784, "chain_fwd": 603_865_344, "compose": 29_396_992,
+              "chain_bwd": 582_913_536, "bwd_feat": 758_413_312, "bwd_tok": 852_842_496}
+_HASHES = {("prepare", False): "1e09286673b20acd", ("prepare", True): "6a74280f2722e6f5",
+           ("chain_fwd", False): "9697ea8042d5a846", ("chain_fwd", True): "9697ea8042d5a846",
+           ("compose", False): "059a56aca0ce6c0f", ("compose", True): "059a56aca0ce6c0f",
+           ("chain_bwd", False): "4adb8bd529345aa8", ("chain_bwd", True): "4adb8bd529345aa8",
+           ("bwd_feat", False): "1bc8ba8a210499f2", ("bwd_feat", True): "1bc8ba8a210499f2",
+           ("bwd_tok", False): "4c78d16e4c465c6b", ("bwd_tok", True): "11fceb34c4af0769"}
 NCU_TRAFFIC_BYTES = {}
 for _k, _v in _GDN_T4096.items():
     NCU_TRAFFIC_BYTES[(_k, "gdn_b2_t4096_h16")] = (_v, _HASHES[(_k, False)])
