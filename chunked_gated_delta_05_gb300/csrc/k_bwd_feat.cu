@@ -80,6 +80,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_load_2d(sm + kOffC + pp * 16384 + 8192, &mDVN, pp * 32, int(tile) * kC, &bar_tma);
     }
     for (int pp = 0; pp < 2; ++pp) tma_load_2d(sm + kOffDO16 + pp * 8192, &mdO, h * kD + 64 * pp, ch.x, &bar_tma);
+    prefetch_l2(p.A + tile * kTileAqk, 4u * kTileAqk);  // read after the first products are issued
   }
   tc_fence_before();
   __syncthreads();
@@ -120,16 +121,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int pp = 0; pp < 4; ++pp)
       tma_load_2d(sm + kOffVN + pp * 8192, &mVN, pp * 32, int(tile) * kC, &bar_tma2);
   }
-  // A^T operand: element (j, i) = A[i][j]; four threads split the 64 rows i of column j = tid % 64.
-  {
-    const int j = tid & 63, i0 = (tid >> 6) * 16;
-    const float* a = p.A + tile * kTileAqk + j;
-    float buf[16];
-#pragma unroll
-    for (int e = 0; e < 16; ++e) buf[e] = a[size_t(i0 + e) * kC];
-#pragma unroll
-    for (int e = 0; e < 16; ++e) *reinterpret_cast<float*>(sm + kOffAT + sw128_offset(j, i0 + e, kC, 4)) = to_tf32(buf[e]);
-  }
   // dO^T operand: element (t, v=f) of the K-major [t][v] tile from the bf16 TMA tile (half hf
   // of the tokens); rows past the chunk (the next document's, or out of range) are zero.
   if (tma_ok) {
@@ -160,6 +151,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       mma_commit(&bar_mma);
     }
   }
+  // A^T operand of the second product group, built while the first products run (A comes
+  // from HBM; nothing before the second group reads it)
+  // element (j, i) = A[i][j]; four threads split the 64 rows i of column j = tid % 64.
+  {
+    const int j = tid & 63, i0 = (tid >> 6) * 16;
+    const float* a = p.A + tile * kTileAqk + j;
+    float buf[16];
+#pragma unroll
+    for (int e = 0; e < 16; ++e) buf[e] = a[size_t(i0 + e) * kC];
+#pragma unroll
+    for (int e = 0; e < 16; ++e) *reinterpret_cast<float*>(sm + kOffAT + sw128_offset(j, i0 + e, kC, 4)) = to_tf32(buf[e]);
+  }
+  fence_async_smem();
   __syncwarp();
   const bool ok = mbar_wait(&bar_mma, 0, &abort_flag, p.status, kDevTimeoutMma);
   tc_fence_after();
