@@ -369,6 +369,7 @@ PrepParams prep_params(const gdn_desc_t* d, const Problem& P, char* sv, const La
   PrepParams pp{};
   pp.chunks = reinterpret_cast<const ChunkEntry*>(sv + L.chunks);
   pp.NC = P.NC;
+  pp.dense_T = P.packed ? 0 : P.T;
   pp.H = P.H;
   pp.g = g;
   pp.beta = static_cast<const __nv_bfloat16*>(beta);
@@ -705,6 +706,7 @@ int run_bwd(const gdn_desc_t* d, const gdn_bwd_args_t* a, void* stream, bool kda
   BwdFeatParams fp{};
   fp.chunks = chunks;
   fp.NC = P.NC;
+  fp.dense_T = P.packed ? 0 : P.T;
   fp.H = P.H;
   fp.kda = kda ? 1 : 0;
   fp.h = F(L.hs);
@@ -720,6 +722,7 @@ int run_bwd(const gdn_desc_t* d, const gdn_bwd_args_t* a, void* stream, bool kda
   BwdTokParams tp{};
   tp.chunks = chunks;
   tp.NC = P.NC;
+  tp.dense_T = P.packed ? 0 : P.T;
   tp.H = P.H;
   tp.scale = P.scale;
   tp.beta_sigmoid = d->use_beta_sigmoid;

@@ -29,6 +29,17 @@ constexpr float kKdaBlockDropMax = 80.f;
 // One chunk of one sequence: {first token row (flattened B*T), valid rows (1..64),
 // sequence index, chunk index within the sequence}.
 using ChunkEntry = int4;
+
+// Chunk c's table entry {first row, rows, sequence, chunk within the sequence}: computed for a
+// dense batch (every sequence dense_T tokens, chunks numbered sequence by sequence), so a CTA
+// can issue its first copies without waiting for the table; loaded for packed documents.
+__device__ __forceinline__ ChunkEntry chunk_entry(const ChunkEntry* chunks, int c, int dense_T) {
+  if (dense_T > 0) {
+    const int ncs = (dense_T + kC - 1) / kC, n = c / ncs, j = c - n * ncs;
+    return make_int4(n * dense_T + j * kC, min(kC, dense_T - j * kC), n, j);
+  }
+  return chunks[c];
+}
 // One sequence: {first chunk index, number of chunks}.
 using SeqEntry = int2;
 
@@ -91,6 +102,7 @@ __host__ __device__ inline bool decode_run(int slot, int pass, int ns, int* seg,
 struct PrepParams {
   const ChunkEntry* chunks;
   int NC, H;
+  int dense_T;                 // tokens per sequence of a dense batch (chunk entries computed), 0 if packed
   int hg0, hgn;                // head group: heads hg0 .. hg0 + hgn - 1 (grid.y = hgn)
   const float* g;              // GDN [R,H]; KDA [R,H,K]
   const __nv_bfloat16* beta;   // [R,H]
@@ -162,6 +174,7 @@ struct UploadParams {
 struct BwdFeatParams {
   const ChunkEntry* chunks;
   int NC, H, kda;
+  int dense_T;                 // tokens per sequence of a dense batch (chunk entries computed), 0 if packed
   int hg0, hgn;                // head group: heads hg0 .. hg0 + hgn - 1 (grid.y = hgn)
   const float* h;              // [NC,H,K,V] state entering each chunk
   const float* dh;             // [NC,H,K,V] gradient w.r.t. the state leaving each chunk
@@ -177,6 +190,7 @@ struct BwdFeatParams {
 struct BwdTokParams {
   const ChunkEntry* chunks;
   int NC, H, kda;
+  int dense_T;                 // tokens per sequence of a dense batch (chunk entries computed), 0 if packed
   int hg0, hgn;                // head group: heads hg0 .. hg0 + hgn - 1 (grid.y = hgn)
   float scale;
   int beta_sigmoid, l2norm;

@@ -61,7 +61,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int c = blockIdx.x, h = blockIdx.y + p.hg0, H = p.H;
   const size_t tile = size_t(c) * H + h;
   const int f = tid & 127, hf = tid >> 7;  // feature (TMEM lane) and column half
-  const ChunkEntry ch = p.chunks[c];  // requested first: the dO load below waits on it
+  const ChunkEntry ch = chunk_entry(p.chunks, c, p.dense_T);  // requested first: the dO load below waits on it
 
   if (warp == 0) tmem_alloc(&tslot, 512);
   if (tid == 0) {

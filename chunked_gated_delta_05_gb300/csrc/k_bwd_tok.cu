@@ -79,7 +79,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int c = blockIdx.x, h = blockIdx.y + p.hg0, H = p.H;
   const size_t tile = size_t(c) * H + h;
-  const ChunkEntry ch = p.chunks[c];
+  const ChunkEntry ch = chunk_entry(p.chunks, c, p.dense_T);
   const int len = ch.y;
   const int wq = warp & 3, half = warp >> 2;   // TMEM lane quadrant; which half of the columns
   const bool owner = lane < 16;                // owns token row rr of every 64-row MMA result

@@ -193,7 +193,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int wq = warp & 3, half = warp >> 2;
   const int c_idx = blockIdx.x, h = blockIdx.y + p.hg0, H = p.H;
   const size_t tile = size_t(c_idx) * H + h;
-  const ChunkEntry ch = p.chunks[c_idx];
+  const ChunkEntry ch = chunk_entry(p.chunks, c_idx, p.dense_T);
   const int len = ch.y;
   const bool owner = lane < 16;
   const int rr = 16 * wq + (lane & 15);

@@ -85,7 +85,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (tid == 0) {
     // the barriers are this thread's alone until the block barrier below: start the loads now
     int4 cb[2];
-    for (int b = 0; b < 2; ++b) cb[b] = 2 * pair + b < p.NC ? p.chunks[2 * pair + b] : make_int4(0, 0, 0, 0);
+    for (int b = 0; b < 2; ++b) cb[b] = 2 * pair + b < p.NC ? chunk_entry(p.chunks, 2 * pair + b, p.dense_T) : make_int4(0, 0, 0, 0);
     abort_flag = 0;
     mbar_init(&bar_tma, 1);
     mbar_init(&bar_mma, 1);

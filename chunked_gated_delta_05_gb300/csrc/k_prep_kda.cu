@@ -86,7 +86,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int hf = tid >> 7;     // which half of the block (rows or columns, per phase)
   const int c_idx = blockIdx.x, h = blockIdx.y + p.hg0, H = p.H;
   const size_t tile = size_t(c_idx) * H + h;
-  const ChunkEntry ch = p.chunks[c_idx];
+  const ChunkEntry ch = chunk_entry(p.chunks, c_idx, p.dense_T);
   const int len = ch.y;
 
   if (warp == 0) tmem_alloc(&tslot, 256);
