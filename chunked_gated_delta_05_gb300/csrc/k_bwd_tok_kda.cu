@@ -43,6 +43,20 @@ __device__ __forceinline__ uint8_t* align1k(uint8_t* p) {
 __device__ __forceinline__ float bf16_at(const uint8_t* tile, int row, int col) {
   return __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(tile + sw128_offset(row, col, kC, 2)));
 }
+// Four consecutive bf16 columns (col % 4 == 0) of a 64-row bf16 tile, as fp32.
+__device__ __forceinline__ void bf16x4_at(const uint8_t* tile, int row, int col, float* f) {
+  const uint2 u = *reinterpret_cast<const uint2*>(tile + sw128_offset(row, col, kC, 2));
+  const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.x));
+  const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.y));
+  f[0] = a.x; f[1] = a.y; f[2] = b.x; f[3] = b.y;
+}
+__device__ __forceinline__ uint2 pack_bf16x4(const float* x) {
+  __nv_bfloat162 a = __floats2bfloat162_rn(x[0], x[1]), b = __floats2bfloat162_rn(x[2], x[3]);
+  uint2 u;
+  u.x = *reinterpret_cast<uint32_t*>(&a);
+  u.y = *reinterpret_cast<uint32_t*>(&b);
+  return u;
+}
 __device__ __forceinline__ void put32(uint8_t* tile, int rows, int row, int col, float x) {
   *reinterpret_cast<float*>(tile + sw128_offset(row, col, rows, 4)) = x;
 }
@@ -458,24 +472,38 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   s_glast[half][cc] = glast_part;
   __syncthreads();
-  // ---- L2-norm backward and writes; dg by reverse cumulative sum per channel
-  for (int t = half; t < len; t += 2) {
-    const float rq = s_rq[t], rk = s_rk[t];
-    const float qh = rq * bf16_at(sQ, t, cc), kh = rk * bf16_at(sK, t, cc);
-    const float dotq = (s_dotq[0][t] + s_dotq[1][t]) + (s_dotq[2][t] + s_dotq[3][t]);
-    const float dotk = (s_dotk[0][t] + s_dotk[1][t]) + (s_dotk[2][t] + s_dotk[3][t]);
-    const float dq = p.l2norm ? rq * (sQacc[t * kD + cc] - qh * dotq) : sQacc[t * kD + cc];
-    const float dk = p.l2norm ? rk * (sKacc[t * kD + cc] - kh * dotk) : sKacc[t * kD + cc];
-    if (p.dq32) {  // per value head, summed over the q/k group later
-      const size_t o = (size_t(ch.x + t) * H + h) * kD + cc;
-      p.dq32[o] = dq;
-      p.dk32[o] = dk;
-    } else {
-      const size_t o = (size_t(ch.x + t) * (H / p.qk_group) + h) * kD + cc;
-      p.dq[o] = __float2bfloat16_rn(dq);
-      p.dk[o] = __float2bfloat16_rn(dk);
+  // ---- L2-norm backward and writes: each warp takes whole token rows, lane l channels
+  // 4l .. 4l+3 (16-byte reads of the accumulators, 8-byte reads of q and k, vector stores)
+  {
+    const int c4 = 4 * lane;
+    for (int t = warp; t < len; t += kThreads / 32) {
+      const float rq = s_rq[t], rk = s_rk[t];
+      const float dotq = (s_dotq[0][t] + s_dotq[1][t]) + (s_dotq[2][t] + s_dotq[3][t]);
+      const float dotk = (s_dotk[0][t] + s_dotk[1][t]) + (s_dotk[2][t] + s_dotk[3][t]);
+      float qv[4], kv[4];
+      bf16x4_at(sQ, t, c4, qv);
+      bf16x4_at(sK, t, c4, kv);
+      const float4 qa = *reinterpret_cast<const float4*>(sQacc + t * kD + c4);
+      const float4 ka = *reinterpret_cast<const float4*>(sKacc + t * kD + c4);
+      const float qac[4] = {qa.x, qa.y, qa.z, qa.w}, kac[4] = {ka.x, ka.y, ka.z, ka.w};
+      float dq[4], dk[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        dq[e] = p.l2norm ? rq * (qac[e] - rq * qv[e] * dotq) : qac[e];
+        dk[e] = p.l2norm ? rk * (kac[e] - rk * kv[e] * dotk) : kac[e];
+      }
+      if (p.dq32) {  // per value head, summed over the q/k group later
+        const size_t o = (size_t(ch.x + t) * H + h) * kD + c4;
+        *reinterpret_cast<float4*>(p.dq32 + o) = make_float4(dq[0], dq[1], dq[2], dq[3]);
+        *reinterpret_cast<float4*>(p.dk32 + o) = make_float4(dk[0], dk[1], dk[2], dk[3]);
+      } else {
+        const size_t o = (size_t(ch.x + t) * (H / p.qk_group) + h) * kD + c4;
+        *reinterpret_cast<uint2*>(p.dq + o) = pack_bf16x4(dq);
+        *reinterpret_cast<uint2*>(p.dk + o) = pack_bf16x4(dk);
+      }
     }
   }
+  // ---- dg by reverse cumulative sum per channel
   if (half == 0) {
     float acc = s_glast[0][cc] + s_glast[1][cc] + exp2f(glc) * dgam_c;
     if (p.gate_act) {
