@@ -198,10 +198,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   __shared__ uint64_t bar_tma, bar_mma;
   __shared__ uint32_t tslot;
   __shared__ int abort_flag;
-  __shared__ float s_rq[kC], s_rk[kC], s_b[kC], s_glast[2][kD];
-  // per-token sums over the channels, one partial per group of 32 channels (warp % 4), added in
-  // a fixed order so that the result does not depend on warp scheduling
-  __shared__ float s_dbp[4][kC], s_dba[4][kC], s_dotq[4][kC], s_dotk[4][kC];
+  __shared__ float s_rq[kC], s_rk[kC], s_b[kC];
+  // per-token sums over the channels: the pair sums' share of dbeta, one partial per group of
+  // 32 channels (warp % 4), added in a fixed order so that the result does not depend on warp
+  // scheduling; the assembly's sums (one warp reduction per token row)
+  __shared__ float s_dbp[4][kC], s_dba[1][kC], s_dotq[1][kC], s_dotk[1][kC];
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int wq = warp & 3, half = warp >> 2;
@@ -250,6 +251,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_load_2d(sm + kR3 + pp * 8192, &mDW, pp * 32, int(tile) * kC, &bar_tma);
       tma_load_2d(sm + kR4 + pp * 8192, &mDVN, pp * 32, int(tile) * kC, &bar_tma);
     }
+    // inputs of the later phases (the inverse, the assembly's gradient tiles): start their
+    // trip from HBM now
+    const size_t rows = tile * kTileW;
+    prefetch_l2(p.A + tile * kTileAqk, 4u * kTileAqk);
+    prefetch_l2(p.dQt + rows, 4u * kTileW);
+    prefetch_l2(p.dKt + rows, 4u * kTileW);
+    prefetch_l2(p.dK1 + rows, 4u * kTileW);
+    prefetch_l2(p.dV1 + rows, 4u * kTileW);
   }
   // G (scaled to log2 units) and dO as a 64-row tf32 operand; rows past the chunk are zero.
   // Both arrived with the other copies (G in R1, dO in the G area): each thread reads its
@@ -408,69 +417,71 @@ __global__ void __launch_bounds__(kThreads, 1)
   for (int b = 0; b < 2; ++b)
     kda_pair_block(2 * half + b, sG2, sK, sQ, s_rk, s_rq, s_b, sD, sN, sKacc, sQacc, sGacc, s_dbp[warp & 3], cc, lane);
   __syncthreads();
-  // ---- per-token assembly (thread: channel cc, rows of parity `half`)
-  float glast_part = 0.f;
+  // ---- per-token assembly: each warp takes whole token rows, lane l channels 4l .. 4l+3.
+  // The row sums over the channels (dbeta, q^ . dq^, k^ . dk^) are one warp reduction each,
+  // in a fixed order; each channel's share of dG_last is summed over the warps below.
   const float glc = sG2[(len - 1) * kP + cc];
-  const size_t rowbase = tile * kTileW;
-  // rows t0 + 2 e, e < 8: the four gradient tiles of eight rows are requested together
-  for (int t0 = half; t0 < len; t0 += 16) {
-    float dqt8[8], dk18[8], dkt8[8], dv18[8];
+  {
+    const int c4 = 4 * lane;
+    const size_t rowbase = tile * kTileW;
+    float glc4[4], glp[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-    for (int e = 0; e < 8; ++e) {  // t0 + 2 e < 64: inside the chunk tile
-      const size_t o = rowbase + size_t(t0 + 2 * e) * kD + cc;
-      dqt8[e] = p.dQt[o];
-      dk18[e] = p.dK1[o];
-      dkt8[e] = p.dKt[o];
-      dv18[e] = p.dV1[o];
-    }
-    // per-row sums over the channels of dbeta, q^ . dq^ and k^ . dk^: 24 values per thread,
-    // reduce-scattered over the warp (each lane group of four ends with three of the sums)
-    float v[24];
+    for (int e = 0; e < 4; ++e) glc4[e] = sG2[(len - 1) * kP + c4 + e];
+    for (int t = warp; t < len; t += kThreads / 32) {
+      const size_t o = rowbase + size_t(t) * kD + c4;
+      const float4 dqt4 = __ldg(reinterpret_cast<const float4*>(p.dQt + o));
+      const float4 dk14 = __ldg(reinterpret_cast<const float4*>(p.dK1 + o));
+      const float4 dkt4 = __ldg(reinterpret_cast<const float4*>(p.dKt + o));
+      const float4 dv14 = __ldg(reinterpret_cast<const float4*>(p.dV1 + o));
+      const float dqt[4] = {dqt4.x, dqt4.y, dqt4.z, dqt4.w}, dk1[4] = {dk14.x, dk14.y, dk14.z, dk14.w};
+      const float dkt[4] = {dkt4.x, dkt4.y, dkt4.z, dkt4.w}, dv1[4] = {dv14.x, dv14.y, dv14.z, dv14.w};
+      float qv[4], kv[4], vv[4];
+      bf16x4_at(sQ, t, c4, qv);
+      bf16x4_at(sK, t, c4, kv);
+      bf16x4_at(sV, t, c4, vv);
+      const float rq = s_rq[t], rk = s_rk[t], bt = s_b[t];
+      float4* qa4 = reinterpret_cast<float4*>(sQacc + t * kD + c4);
+      float4* ka4 = reinterpret_cast<float4*>(sKacc + t * kD + c4);
+      float4* ga4 = reinterpret_cast<float4*>(sGacc + t * kD + c4);
+      const float4 qa = *qa4, ka = *ka4, ga = *ga4;
+      float qacc[4] = {qa.x, qa.y, qa.z, qa.w}, kacc[4] = {ka.x, ka.y, ka.z, ka.w}, gacc[4] = {ga.x, ga.y, ga.z, ga.w};
+      float sdb = 0.f, sq = 0.f, sk = 0.f, dvo[4];
 #pragma unroll
-    for (int e = 0; e < 8; ++e) {
-      const int t = t0 + 2 * e;
-      v[e] = v[8 + e] = v[16 + e] = 0.f;
-      if (t < len) {  // warp-uniform
-        const float dqt = dqt8[e], dk1 = dk18[e], dkt = dkt8[e], dv1 = dv18[e];
-        const float G = sG2[t * kP + cc];
-        const float eG = exp2f(G), eL = exp2f(glc - G);
-        const float qh = s_rq[t] * bf16_at(sQ, t, cc), kh = s_rk[t] * bf16_at(sK, t, cc);
-        const float dqh = sQacc[t * kD + cc] + scale * eG * dqt;
-        const float dkh = sKacc[t * kD + cc] + s_b[t] * eG * dk1 + eL * dkt;
-        sQacc[t * kD + cc] = dqh;
-        sKacc[t * kD + cc] = dkh;
-        sGacc[t * kD + cc] += s_b[t] * eG * dk1 * kh + scale * eG * dqt * qh - eL * dkt * kh;
-        glast_part = fmaf(eL * dkt, kh, glast_part);
-        p.dv[(size_t(ch.x + t) * H + h) * kD + cc] = __float2bfloat16_rn(s_b[t] * dv1);
-        v[e] = eG * dk1 * kh + dv1 * bf16_at(sV, t, cc);
-        v[8 + e] = dqh * qh;
-        v[16 + e] = dkh * kh;
+      for (int e = 0; e < 4; ++e) {
+        const float G = sG2[t * kP + c4 + e];
+        const float eG = exp2f(G), eL = exp2f(glc4[e] - G);
+        const float qh = rq * qv[e], kh = rk * kv[e];
+        const float dqh = qacc[e] + scale * eG * dqt[e];
+        const float dkh = kacc[e] + bt * eG * dk1[e] + eL * dkt[e];
+        qacc[e] = dqh;
+        kacc[e] = dkh;
+        gacc[e] += bt * eG * dk1[e] * kh + scale * eG * dqt[e] * qh - eL * dkt[e] * kh;
+        glp[e] = fmaf(eL * dkt[e], kh, glp[e]);
+        dvo[e] = bt * dv1[e];
+        sdb += eG * dk1[e] * kh + dv1[e] * vv[e];
+        sq += dqh * qh;
+        sk += dkh * kh;
+      }
+      *qa4 = make_float4(qacc[0], qacc[1], qacc[2], qacc[3]);
+      *ka4 = make_float4(kacc[0], kacc[1], kacc[2], kacc[3]);
+      *ga4 = make_float4(gacc[0], gacc[1], gacc[2], gacc[3]);
+      *reinterpret_cast<uint2*>(p.dv + (size_t(ch.x + t) * H + h) * kD + c4) = pack_bf16x4(dvo);
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) {
+        sdb += __shfl_xor_sync(0xffffffffu, sdb, off);
+        sq += __shfl_xor_sync(0xffffffffu, sq, off);
+        sk += __shfl_xor_sync(0xffffffffu, sk, off);
+      }
+      if (lane == 0) {
+        s_dba[0][t] = sdb;
+        s_dotq[0][t] = sq;
+        s_dotk[0][t] = sk;
       }
     }
-    const bool b4 = lane & 16, b3 = lane & 8, b2 = lane & 4;
-    float w[12], u[6], y[3];
+    // the pair sums no longer read dL: its tile holds each warp's dG_last shares [8][128]
 #pragma unroll
-    for (int k = 0; k < 12; ++k)
-      w[k] = (b4 ? v[12 + k] : v[k]) + __shfl_xor_sync(0xffffffffu, b4 ? v[k] : v[12 + k], 16);
-#pragma unroll
-    for (int k = 0; k < 6; ++k)
-      u[k] = (b3 ? w[6 + k] : w[k]) + __shfl_xor_sync(0xffffffffu, b3 ? w[k] : w[6 + k], 8);
-#pragma unroll
-    for (int k = 0; k < 3; ++k) {
-      y[k] = (b2 ? u[3 + k] : u[k]) + __shfl_xor_sync(0xffffffffu, b2 ? u[k] : u[3 + k], 4);
-      y[k] += __shfl_xor_sync(0xffffffffu, y[k], 2);
-      y[k] += __shfl_xor_sync(0xffffffffu, y[k], 1);
-    }
-    if ((lane & 3) == 0) {
-      const int base = (b4 ? 12 : 0) + (b3 ? 6 : 0) + (b2 ? 3 : 0);
-#pragma unroll
-      for (int k = 0; k < 3; ++k) {
-        const int n = base + k, t = t0 + 2 * (n & 7);
-        if (t < len) (n < 8 ? s_dba : (n < 16 ? s_dotq : s_dotk))[warp & 3][t] = y[k];
-      }
-    }
+    for (int e = 0; e < 4; ++e) sD[warp * kD + c4 + e] = glp[e];
   }
-  s_glast[half][cc] = glast_part;
   __syncthreads();
   // ---- L2-norm backward and writes: each warp takes whole token rows, lane l channels
   // 4l .. 4l+3 (16-byte reads of the accumulators, 8-byte reads of q and k, vector stores)
@@ -478,8 +489,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int c4 = 4 * lane;
     for (int t = warp; t < len; t += kThreads / 32) {
       const float rq = s_rq[t], rk = s_rk[t];
-      const float dotq = (s_dotq[0][t] + s_dotq[1][t]) + (s_dotq[2][t] + s_dotq[3][t]);
-      const float dotk = (s_dotk[0][t] + s_dotk[1][t]) + (s_dotk[2][t] + s_dotk[3][t]);
+      const float dotq = s_dotq[0][t], dotk = s_dotk[0][t];
       float qv[4], kv[4];
       bf16x4_at(sQ, t, c4, qv);
       bf16x4_at(sK, t, c4, kv);
@@ -505,7 +515,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   // ---- dg by reverse cumulative sum per channel
   if (half == 0) {
-    float acc = s_glast[0][cc] + s_glast[1][cc] + exp2f(glc) * dgam_c;
+    float acc = exp2f(glc) * dgam_c;
+#pragma unroll
+    for (int w = 0; w < kThreads / 32; ++w) acc += sD[w * kD + cc];   // dG_last shares, in warp order
     if (p.gate_act) {
       // chain rule through the safe gate g = lb sigmoid(z), z = a (x + dt_bias), a = exp(A_log):
       // dx = dg lb s (1 - s) a; the parameter gradients are summed per chunk here and over the
@@ -533,8 +545,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
   if (tid < len) {
-    float db = ((s_dbp[0][tid] + s_dbp[1][tid]) + (s_dbp[2][tid] + s_dbp[3][tid])) +
-               ((s_dba[0][tid] + s_dba[1][tid]) + (s_dba[2][tid] + s_dba[3][tid]));
+    float db = ((s_dbp[0][tid] + s_dbp[1][tid]) + (s_dbp[2][tid] + s_dbp[3][tid])) + s_dba[0][tid];
     if (p.beta_sigmoid) db *= s_b[tid] * (1.f - s_b[tid]);
     p.dbeta[size_t(ch.x + tid) * H + h] = __float2bfloat16_rn(db);
   }
