@@ -302,11 +302,21 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncwarp();
   bool ok = tma_ok && mbar_wait(&bar_mma, 0, &abort_flag, p.status, kDevTimeoutMma);
   tc_fence_after();
-  // ---- K1 = beta r_k exp(G) (.) k and V1 = beta v as 64-row operands [j][c]
-  for (int j = 32 * half; j < 32 * half + 32; ++j) {
-    const float s1 = s_b[j] * s_rk[j];
-    put32(sm + kR1, kC, j, cc, to_tf32(s1 * exp2f(sG2[j * kP + cc]) * bf16_at(sK, j, cc)));
-    put32(sm + kR2, kC, j, cc, to_tf32(s_b[j] * bf16_at(sV, j, cc)));
+  // ---- K1 = beta r_k exp(G) (.) k and V1 = beta v as 64-row operands [j][c]: each warp takes
+  // whole rows, lane l channels 4l .. 4l+3 (one 16-byte chunk of each swizzled row)
+  {
+    const int c4 = 4 * lane;
+    for (int j = warp; j < kC; j += kThreads / 32) {
+      const float s1 = s_b[j] * s_rk[j], s2 = s_b[j];
+      float kv[4], vv[4], k1[4];
+      bf16x4_at(sK, j, c4, kv);
+      bf16x4_at(sV, j, c4, vv);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) k1[e] = to_tf32(s1 * exp2f(sG2[j * kP + c4 + e]) * kv[e]);
+      *reinterpret_cast<float4*>(sm + kR1 + sw128_offset(j, c4, kC, 4)) = make_float4(k1[0], k1[1], k1[2], k1[3]);
+      *reinterpret_cast<float4*>(sm + kR2 + sw128_offset(j, c4, kC, 4)) =
+          make_float4(to_tf32(s2 * vv[0]), to_tf32(s2 * vv[1]), to_tf32(s2 * vv[2]), to_tf32(s2 * vv[3]));
+    }
   }
   fence_async_smem();
   tc_fence_before();
