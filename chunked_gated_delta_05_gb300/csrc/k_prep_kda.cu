@@ -15,7 +15,11 @@
 // For i in block I the first factor is <= 1, and for j < r_I the second one is too; for j in
 // block I it is at most the decay across 15 tokens. One stacked 128-row tf32 operand (keys
 // then queries, each row scaled by its block's reference) times B_I = k^ exp(G_{r_I} - G)
-// (rows j <= 16 I + 15) gives, in four 128-lane MMAs, every row block of both L and Aqk.
+// (rows j <= 16 I + 15, so N = 16 (I + 1)) gives, in four 128-lane MMAs, every row block of
+// both L and Aqk. Row j of B_I splits again at j's own block J: exp(G_{r_I} - G_j) =
+// exp(G_{r_I} - G_{r_J}) exp(G_{r_J} - G_j), a per-channel factor of the block pair (<= 1 for
+// J < I) times the reciprocal of the stacked operand's factor of row j, so each element of the
+// chunk takes two exponentials for all five operands.
 // The unit-lower inverse and the WY products follow the scalar-gate kernel: W's right factor
 // carries the per-channel decay (tf32, thread-written); U uses the raw v tile (bf16); the
 // unit diagonal of A is applied in fp32 from the exact inputs.
@@ -32,8 +36,13 @@ constexpr int kGP = kD + 1;                                // padded row stride 
 constexpr uint32_t kOffQ = 0, kOffK = 16384, kOffV = 32768;  // bf16 [64][128] tiles
 constexpr uint32_t kOffG = 49152;                          // fp32 [64][129]
 constexpr uint32_t kOffAS = 83968;                         // stacked A operand, tf32 [128][128] (64 KB)
-constexpr uint32_t kOffB = 149504;                         // two B_I operands, tf32 [64][128] (2 x 32 KB)
+constexpr uint32_t kOffB = 149504;                         // B_3, B_2, B_0: tf32 [64 / 48 / 16][128]
 constexpr uint32_t kSmemBytes = kOffB + 65536 + 1024;
+// B_I (N = 16 (I + 1) rows) offsets; B_1 borrows the value tile's slot, whose load is issued once
+// the Gram products are done.
+__device__ __forceinline__ uint32_t b_off(int I) {
+  return I == 3 ? kOffB : (I == 2 ? kOffB + 32768 : (I == 1 ? kOffV : kOffB + 57344));
+}
 // Later phases reuse the operand region [kOffAS, kOffB + 64 KB):
 constexpr uint32_t kOffLT = kOffAS;                        // L^T fp32 [64][64]
 constexpr uint32_t kOffX = kOffAS + 16384;                 // inverse columns fp32 [64][64]
@@ -56,6 +65,10 @@ __device__ __forceinline__ float bf16_at(const uint8_t* tile, int row, int col) 
 __device__ __forceinline__ void put32(uint8_t* tile, int rows, int row, int col, float x) {
   *reinterpret_cast<float*>(tile + sw128_offset(row, col, rows, 4)) = x;
 }
+__device__ __forceinline__ void put_tf32x8(uint8_t* tile, int rows, int row, int col, const float* f) {
+  *reinterpret_cast<float4*>(tile + sw128_offset(row, col, rows, 4)) = make_float4(f[0], f[1], f[2], f[3]);
+  *reinterpret_cast<float4*>(tile + sw128_offset(row, col + 4, rows, 4)) = make_float4(f[4], f[5], f[6], f[7]);
+}
 __device__ __forceinline__ void bf16x8_to_f32(const uint4& u, float* f) {
   const __nv_bfloat162* b = reinterpret_cast<const __nv_bfloat162*>(&u);
 #pragma unroll
@@ -77,10 +90,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* sK = sm + kOffK;
   uint8_t* sV = sm + kOffV;
   float* sG = reinterpret_cast<float*>(sm + kOffG);
-  __shared__ uint64_t bar_tma, bar_mma;
+  __shared__ uint64_t bar_tma, bar_v, bar_mma;
   __shared__ uint32_t tslot;
   __shared__ int abort_flag;
   __shared__ float s_rq[kC], s_rk[kC], s_b[kC], s_gl[kD];
+  __shared__ __align__(16) float s_T[6][kD];  // exp(G_{r_I} - G_{r_J}), J < I, at I (I - 1) / 2 + J
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int hf = tid >> 7;     // which half of the block (rows or columns, per phase)
@@ -94,14 +108,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     // the barriers are this thread's alone until the block barrier below: start the loads now
     abort_flag = 0;
     mbar_init(&bar_tma, 1);
+    mbar_init(&bar_v, 1);
     mbar_init(&bar_mma, 1);
     fence_mbar_init();
-    mbar_expect_tx(&bar_tma, 3u * 16384u);
+    mbar_expect_tx(&bar_tma, 2u * 16384u);
     for (int pp = 0; pp < 2; ++pp) {
-      const int x = h * kD + 64 * pp, xqk = (h / p.qk_group) * kD + 64 * pp;
+      const int xqk = (h / p.qk_group) * kD + 64 * pp;
       tma_load_2d(sQ + pp * 8192, &mq, xqk, ch.x, &bar_tma);
       tma_load_2d(sK + pp * 8192, &mk, xqk, ch.x, &bar_tma);
-      tma_load_2d(sV + pp * 8192, &mv, x, ch.x, &bar_tma);
     }
   }
   // Cumulative gate of channel c: each half sums its 32 rows; the second half adds the first
@@ -152,7 +166,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t off = sw128_offset(tid, c16 * 8, kC, 2);
       *reinterpret_cast<uint4*>(sQ + off) = make_uint4(0, 0, 0, 0);
       *reinterpret_cast<uint4*>(sK + off) = make_uint4(0, 0, 0, 0);
-      *reinterpret_cast<uint4*>(sV + off) = make_uint4(0, 0, 0, 0);
     }
   }
   __syncthreads();
@@ -171,6 +184,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         in_range = in_range && fabsf(sG[i * kGP + c] - gr) <= kKdaBlockDropMax;
     }
     if (!in_range && p.status) atomicCAS(p.status, 0, kDevGateRange);
+    for (int pr = hf; pr < 6; pr += 2) {
+      const int I = pr == 0 ? 1 : (pr < 3 ? 2 : 3), J = pr - I * (I - 1) / 2;
+      s_T[pr][c] = __expf(sG[16 * I * kGP + c] - sG[16 * J * kGP + c]);
+    }
   }
   // L2-norm factors: thread pairs (2 p, 2 p + 1) share row p % 64 of q (p < 64) or k, half the
   // columns each (eight per load).
@@ -194,72 +211,68 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (tid < kD) s_gl[tid] = sG[(len - 1) * kGP + tid];
   __syncthreads();
 
-  // Stacked operand: rows 0..63 k^_i, rows 64..127 q^_i, each times exp(G_i - G_{r(i)}); each
-  // thread builds half a row.
+  // One pass builds the stacked operand (rows 0..63 k^_j P_j, rows 64..127 q^_j P_j, with
+  // P_j = exp(G_j - G_{r(j)}) <= 1) and every B_I row of token j: k^_j / P_j for I = J, times
+  // exp(G_{r_I} - G_{r_J}) for I > J. Warp w takes the 16 tokens of block J (w < 4: J = w;
+  // otherwise J = 7 - w, so the two warps of a sub-partition share the B rows evenly) and eight
+  // channel chunks; the two half-warps' chunks sit 16 channels apart (no bank conflicts on G).
   uint8_t* sAS = sm + kOffAS;
   {
-    const int row = tid & 127, i = row & 63;
-    const bool isq = row >= kC;
-    const int rref = i & ~15;
-    const float rs = isq ? s_rq[i] : s_rk[i];
-    const bool vi = i < len;
-    const uint8_t* src = isq ? sQ : sK;
-#pragma unroll 2
-    for (int c16 = 8 * hf; c16 < 8 * hf + 8; ++c16) {
-      float f[8];
-      bf16x8_to_f32(*reinterpret_cast<const uint4*>(src + sw128_offset(i, c16 * 8, kC, 2)), f);
+    const int chh = warp >> 2, J = chh == 0 ? (warp & 3) : 3 - (warp & 3);
+    const int lh = lane >> 4, j = 16 * J + (lane & 15), r = 16 * J;
+    const bool vj = j < len;
+    const float rk = s_rk[j], rq = s_rq[j];
+#pragma unroll 1
+    for (int it = 0; it < 4; ++it) {
+      const int c16 = 8 * chh + (it & 1) + 4 * (it >> 1) + 2 * lh, c0 = 8 * c16;
+      float kf[8], qf[8], kd[8];
+      bf16x8_to_f32(*reinterpret_cast<const uint4*>(sK + sw128_offset(j, c0, kC, 2)), kf);
+      bf16x8_to_f32(*reinterpret_cast<const uint4*>(sQ + sw128_offset(j, c0, kC, 2)), qf);
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
-        const int c = 8 * c16 + e;
-        f[e] = vi ? to_tf32(rs * f[e] * expf(sG[i * kGP + c] - sG[rref * kGP + c])) : 0.f;
+        const float d = sG[j * kGP + c0 + e] - sG[r * kGP + c0 + e];
+        const float P = __expf(d), kr = rk * kf[e];
+        kd[e] = vj ? kr * __expf(-d) : 0.f;
+        kf[e] = vj ? to_tf32(kr * P) : 0.f;
+        qf[e] = vj ? to_tf32(rq * qf[e] * P) : 0.f;
       }
-      *reinterpret_cast<float4*>(sAS + sw128_offset(row, 8 * c16, 128, 4)) = make_float4(f[0], f[1], f[2], f[3]);
-      *reinterpret_cast<float4*>(sAS + sw128_offset(row, 8 * c16 + 4, 128, 4)) = make_float4(f[4], f[5], f[6], f[7]);
+      put_tf32x8(sAS, 2 * kC, j, c0, kf);
+      put_tf32x8(sAS, 2 * kC, kC + j, c0, qf);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) kf[e] = to_tf32(kd[e]);
+      put_tf32x8(sm + b_off(J), 16 * (J + 1), j, c0, kf);
+      for (int I = J + 1; I < 4; ++I) {
+        const float4* t4 = reinterpret_cast<const float4*>(&s_T[I * (I - 1) / 2 + J][c0]);
+        const float4 ta = t4[0], tb4 = t4[1];
+        const float t[8] = {ta.x, ta.y, ta.z, ta.w, tb4.x, tb4.y, tb4.z, tb4.w};
+#pragma unroll
+        for (int e = 0; e < 8; ++e) kf[e] = to_tf32(t[e] * kd[e]);
+        put_tf32x8(sm + b_off(I), 16 * (I + 1), j, c0, kf);
+      }
     }
   }
-  // B_I = k^_j exp(G_{r_I} - G_j) for j <= 16 I + 15 (zero elsewhere), two blocks at a time;
-  // each thread builds half a row.
-  auto build_b = [&](int I0) {
-    const int j = tid & 63, which = (tid >> 6) & 1, I = I0 + which;
-    const int rref = 16 * I;
-    uint8_t* dst = sm + kOffB + which * 32768;
-    const bool vj = j < len && j <= 16 * I + 15;  // a select: the exponent is unbounded elsewhere
-    const float rs = s_rk[j];
-#pragma unroll 2
-    for (int c16 = 8 * hf; c16 < 8 * hf + 8; ++c16) {
-      float f[8];
-      bf16x8_to_f32(*reinterpret_cast<const uint4*>(sK + sw128_offset(j, c16 * 8, kC, 2)), f);
-#pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        const int c = 8 * c16 + e;
-        f[e] = vj ? to_tf32(rs * f[e] * expf(sG[rref * kGP + c] - sG[j * kGP + c])) : 0.f;
-      }
-      *reinterpret_cast<float4*>(dst + sw128_offset(j, 8 * c16, kC, 4)) = make_float4(f[0], f[1], f[2], f[3]);
-      *reinterpret_cast<float4*>(dst + sw128_offset(j, 8 * c16 + 4, kC, 4)) = make_float4(f[4], f[5], f[6], f[7]);
+  fence_async_smem();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (tid == 0) {
+    const uint32_t as = smem_u32(sAS);
+    for (int I = 0; I < 4; ++I) {
+      const uint32_t n = 16 * (I + 1), bs = smem_u32(sm + b_off(I));
+      const uint32_t id_g = idesc_tf32(128, int(n));
+      for (int s = 0; s < 16; ++s)
+        mma_tf32_ss(tb + I * 64, desc_kmajor(as, 16384, s), desc_kmajor(bs, n * 128u, s), id_g, s > 0);
     }
-  };
-  const uint32_t id_g = idesc_tf32(128, 64);
-  uint32_t mma_phase = 0;
-  bool ok = true;
-  for (int I0 = 0; I0 < 4; I0 += 2) {
-    build_b(I0);
-    fence_async_smem();
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    if (tid == 0 && ok) {
-      const uint32_t as = smem_u32(sAS);
-      for (int q = 0; q < 2; ++q) {
-        const uint32_t bs = smem_u32(sm + kOffB + q * 32768);
-        for (int s = 0; s < 16; ++s)
-          mma_tf32_ss(tb + (I0 + q) * 64, desc_kmajor(as, 16384, s), desc_kmajor(bs, 8192, s), id_g, s > 0);
-      }
-      mma_commit(&bar_mma);
-    }
-    __syncwarp();
-    ok = ok && mbar_wait(&bar_mma, mma_phase, &abort_flag, p.status, kDevTimeoutMma);
-    mma_phase ^= 1;
-    tc_fence_after();
+    mma_commit(&bar_mma);
+  }
+  __syncwarp();
+  bool ok = mbar_wait(&bar_mma, 0, &abort_flag, p.status, kDevTimeoutMma);
+  uint32_t mma_phase = 1;
+  tc_fence_after();
+  if (tid == 0 && ok) {
+    // the products have read B_1 out of the value tile's slot: load the values there now
+    mbar_expect_tx(&bar_v, 16384u);
+    for (int pp = 0; pp < 2; ++pp) tma_load_2d(sV + pp * 8192, &mv, h * kD + 64 * pp, ch.x, &bar_v);
   }
   tc_fence_before();
   __syncthreads();
@@ -329,7 +342,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   __syncthreads();
   // WY operands: A1 = (A - I) diag(beta r_k) (tf32), A2 = (A - I) diag(beta) (bf16), both
-  // K-major [i][j]; four threads per column j, 16 rows each.
+  // K-major [i][j]; four threads per column j, 16 rows each. The value tile has landed by now;
+  // its rows past the chunk are cleared first.
+  ok = ok && mbar_wait(&bar_v, 0, &abort_flag, p.status, kDevTimeoutTma);
+  if (ok && tid >= len && tid < kC) {
+    for (int c16 = 0; c16 < 16; ++c16)
+      *reinterpret_cast<uint4*>(sV + sw128_offset(tid, c16 * 8, kC, 2)) = make_uint4(0, 0, 0, 0);
+  }
   {
     const int j = tid & 63, i0 = 16 * (tid >> 6);
     const float s1 = s_b[j] * s_rk[j], s2 = s_b[j];
