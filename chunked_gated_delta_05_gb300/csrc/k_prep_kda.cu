@@ -22,7 +22,9 @@
 // chunk takes two exponentials for all five operands.
 // The unit-lower inverse and the WY products follow the scalar-gate kernel: W's right factor
 // carries the per-channel decay (tf32, thread-written); U uses the raw v tile (bf16); the
-// unit diagonal of A is applied in fp32 from the exact inputs.
+// unit diagonal of A is applied in fp32 from the exact inputs. Exponentials that only feed
+// tf32-rounded operands use the hardware exponential (__expf: a few fp32 ulps, far inside the
+// 2^-11 of tf32); gam, an fp32 output of the state chain, keeps expf.
 #include "common.cuh"
 #include "tri_inverse.cuh"
 #include "umma.cuh"
@@ -51,10 +53,7 @@ constexpr uint32_t kOffA2 = kOffAS + 49152;                // (A - I) diag(beta)
 constexpr uint32_t kOffK1T = kOffB;                        // (k (.) exp(G))^T, tf32 [128][64]
 constexpr int kAP = kC + 1;                                // padded row stride of the Aqk staging
 constexpr uint32_t kOffAqkS = kOffB + 32768;               // Aqk staging fp32 [64][65] (beside K1T)
-constexpr int kWP = kD + 1, kTP = kC + 1;                  // padded strides of the W/U and KtT/QtT staging
-constexpr uint32_t kOffWS = kOffAS, kOffUS = kOffB;        // after the WY products: [64][129] / [128][65]
 static_assert(kOffAqkS + 4 * kC * kAP <= kOffB + 65536, "Aqk staging fits the B region");
-static_assert(4 * kC * kWP <= 65536 && 4 * kD * kTP <= 65536, "W/U and KtT/QtT staging fit their regions");
 
 __device__ __forceinline__ uint8_t* align1k(uint8_t* p) {
   return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
@@ -68,6 +67,10 @@ __device__ __forceinline__ void put32(uint8_t* tile, int rows, int row, int col,
 __device__ __forceinline__ void put_tf32x8(uint8_t* tile, int rows, int row, int col, const float* f) {
   *reinterpret_cast<float4*>(tile + sw128_offset(row, col, rows, 4)) = make_float4(f[0], f[1], f[2], f[3]);
   *reinterpret_cast<float4*>(tile + sw128_offset(row, col + 4, rows, 4)) = make_float4(f[4], f[5], f[6], f[7]);
+}
+__device__ __forceinline__ void st_f32x8(float* dst, const float* f) {
+  reinterpret_cast<float4*>(dst)[0] = make_float4(f[0], f[1], f[2], f[3]);
+  reinterpret_cast<float4*>(dst)[1] = make_float4(f[4], f[5], f[6], f[7]);
 }
 __device__ __forceinline__ void bf16x8_to_f32(const uint4& u, float* f) {
   const __nv_bfloat162* b = reinterpret_cast<const __nv_bfloat162*>(&u);
@@ -313,31 +316,25 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (ok) {
-    float* aqk = p.Aqk + tile * kTileAqk;
-#pragma unroll 4
-    for (int m = 0; m < kC * kC / kThreads; ++m) {
-      const int idx = m * kThreads + tid, r = idx >> 6, col = idx & 63;
-      aqk[idx] = sAqk[r * kAP + col];
-      if (p.AqkT) p.AqkT[tile * kTileAqk + idx] = sAqk[col * kAP + r];  // (r, col) of Aqk^T
-    }
-  }
   float* sX = reinterpret_cast<float*>(sm + kOffX);
   if (hf == 0) {
     // warps 0-3: A = (I + L)^-1, one column per lane pair
     unit_lower_inverse_column(sLT, sX, 16 * warp + (lane & 15), lane >> 4);
   } else {
-    // warps 4-7 meanwhile: K1T = (k (.) exp(G))^T (tf32, K-major [c][j]), row c, 16-byte chunks
-    const int c = tid - 128;
-#pragma unroll 2
-    for (int j4 = 0; j4 < kC; j4 += 4) {
-      float v4[4];
+    // warps 4-7 meanwhile: K1T = (k (.) exp(G))^T (tf32, K-major [c][j]) in the B region, which
+    // the Gram products have released. Thread (token j, chunk group) takes eight channels at a
+    // time from one 16-byte key load; the lanes' consecutive tokens make each transposed store
+    // one line.
+    const int j = lane + 32 * (warp & 1), cg = (warp >> 1) & 1;
+    const bool vj = j < len;
+#pragma unroll 1
+    for (int it = 0; it < 8; ++it) {
+      const int c0 = 8 * (8 * cg + it);
+      float kf[8];
+      bf16x8_to_f32(*reinterpret_cast<const uint4*>(sK + sw128_offset(j, c0, kC, 2)), kf);
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int jj = j4 + e;
-        v4[e] = jj < len ? to_tf32(bf16_at(sK, jj, c) * expf(sG[jj * kGP + c])) : 0.f;
-      }
-      *reinterpret_cast<float4*>(sm + kOffK1T + sw128_offset(c, j4, kD, 4)) = make_float4(v4[0], v4[1], v4[2], v4[3]);
+      for (int e = 0; e < 8; ++e)
+        put32(sm + kOffK1T, kD, c0 + e, j, vj ? to_tf32(kf[e] * __expf(sG[j * kGP + c0 + e])) : 0.f);
     }
   }
   __syncthreads();
@@ -367,101 +364,76 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  // The WY products transposed, so that the accumulator lanes are channels: W^T = K1^T A1^T
+  // (tf32) and U^T = V^T A2^T (bf16, the value tile read MN-major), 128 lanes by 64 tokens.
   if (tid == 0 && ok) {
     const uint32_t a1 = smem_u32(sm + kOffA1), a2 = smem_u32(sm + kOffA2), k1t = smem_u32(sm + kOffK1T);
     const uint32_t v0 = smem_u32(sV);
-    const uint32_t idw = idesc_tf32(64, 128), idu = idesc_bf16(64, 128, false, true);
-    for (int s = 0; s < 8; ++s) mma_tf32_ss(tb, desc_kmajor(a1, 8192, s), desc_kmajor(k1t, 16384, s), idw, s > 0);
-    for (int s = 0; s < 4; ++s) mma_bf16_ss(tb + 128, desc_kmajor(a2, 8192, s), desc_mnmajor_bf16(v0, 8192, s), idu, s > 0);
+    const uint32_t idw = idesc_tf32(128, 64), idu = idesc_bf16(128, 64, true, false);
+    for (int s = 0; s < 8; ++s) mma_tf32_ss(tb, desc_kmajor(k1t, 16384, s), desc_kmajor(a1, 8192, s), idw, s > 0);
+    for (int s = 0; s < 4; ++s) mma_bf16_ss(tb + 128, desc_mnmajor_bf16(v0, 8192, s), desc_kmajor(a2, 8192, s), idu, s > 0);
     mma_commit(&bar_mma);
+  }
+  // Aqk and its transpose leave from their staging (beside K1T, untouched since the Gram
+  // epilogue) while the products run.
+  if (ok) {
+    float* aqk = p.Aqk + tile * kTileAqk;
+#pragma unroll 4
+    for (int m = 0; m < kC * kC / kThreads; ++m) {
+      const int idx = m * kThreads + tid, r = idx >> 6, col = idx & 63;
+      aqk[idx] = sAqk[r * kAP + col];
+      if (p.AqkT) p.AqkT[tile * kTileAqk + idx] = sAqk[col * kAP + r];  // (r, col) of Aqk^T
+    }
   }
   __syncwarp();
   ok = ok && mbar_wait(&bar_mma, mma_phase, &abort_flag, p.status, kDevTimeoutMma);
   tc_fence_after();
-  __syncthreads();  // the operand regions are free from here: W and U are staged over them
-  // W and U rows (64-row MMA results: lane 32*(r/16) + r%16 holds row r), read with the
-  // 16x64b shape so that all 32 lanes work (lane t: row (t >> 2) + 8 (t & 1) of the warp's 16,
-  // columns ((t >> 1) & 1) + 2 e); warps w and w + 4 take two 32-column groups each. Staged
-  // padded [64][129] and written back as whole lines.
-  float* sWs = reinterpret_cast<float*>(sm + kOffWS);
-  float* sUs = reinterpret_cast<float*>(sm + kOffUS);
-  if (ok) {
-    const int r = 16 * (warp & 3) + (lane >> 2) + 8 * (lane & 1);
-    const int cpar = (lane >> 1) & 1;
-    const bool vr = r < len;
-    const float dw = s_b[r] * s_rk[r], du = s_b[r];
-    for (int which = 0; which < 2; ++which) {
-      float* st = which == 0 ? sWs : sUs;
-      for (int q = 2 * hf; q < 2 * hf + 2; ++q) {
-        float x[16];
-        tmem_ld16x64b_x16(tl + which * 128 + 32 * q, x);
-        tmem_wait_ld_regs(x);
-#pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          const int c = 32 * q + cpar + 2 * e;
-          float val = 0.f;
-          if (vr) {
-            val = which == 0 ? to_tf32(fmaf(dw * expf(sG[r * kGP + c]), bf16_at(sK, r, c), x[e]))
-                             : fmaf(du, bf16_at(sV, r, c), x[e]);
-          }
-          st[r * kWP + c] = val;
-        }
-      }
-    }
-  }
-  __syncthreads();
-  if (ok && len > 0) {
-    const int col = tid & 127;
-    float* w = p.W + tile * kTileW;
-    float* u = p.U + tile * kTileW;
-#pragma unroll 4
-    for (int r = 32 * hf; r < 32 * hf + 32; ++r) {
-      w[size_t(r) * kD + col] = sWs[r * kWP + col];
-      u[size_t(r) * kD + col] = sUs[r * kWP + col];
-    }
-    if (p.WT) {  // W^T [c][r]: consecutive threads take consecutive rows r
-      float* wt = p.WT + tile * kTileKtT;
-#pragma unroll 4
-      for (int m = 0; m < kD * kC / kThreads; ++m) {
-        const int idx = m * kThreads + tid, c = idx >> 6, r = idx & 63;
-        wt[idx] = sWs[r * kWP + c];
-      }
-    }
-  }
-  __syncthreads();  // the W / U staging is reused for the transposed gated keys and queries
-  // Per-element outputs: thread (c, half) writes channel c of 32 rows; KtT and QtT are staged
-  // padded [128][65] and leave as whole lines.
-  float* sKT = reinterpret_cast<float*>(sm + kOffWS);
-  float* sQT = reinterpret_cast<float*>(sm + kOffUS);
+  // Per-token outputs: thread (c, hf) takes channel c of the 32 tokens from 32 hf, with the
+  // unit diagonal of A added in fp32: W = A1 K1 + beta r_k exp(G) k and U = A2 v + beta v. W, U,
+  // Qt, Kt and G leave as coalesced rows; W^T, Qt^T and Kt^T as this thread's own row segments.
   {
-    const int c = tid & 127;
+    const int c = tid & 127, t0 = 32 * hf;
     const float glc = s_gl[c];
     if (hf == 0) p.gam[tile * kD + c] = expf(glc);
-    for (int t = 32 * hf; t < 32 * hf + 32; ++t) {
-      const bool vt = t < len;
-      const float G = sG[t * kGP + c];
-      const float qt = vt ? to_tf32(p.scale * s_rq[t] * expf(G) * bf16_at(sQ, t, c)) : 0.f;
-      const float kt = vt ? to_tf32(s_rk[t] * expf(glc - G) * bf16_at(sK, t, c)) : 0.f;
-      p.Qt[tile * kTileW + size_t(t) * kD + c] = qt;
-      sKT[c * kTP + t] = kt;
-      if (p.Kt) p.Kt[tile * kTileW + size_t(t) * kD + c] = kt;
-      sQT[c * kTP + t] = qt;
-      if (p.Gc) p.Gc[(tile * kC + t) * kD + c] = G;
+    float xw[32], xu[32];
+    if (ok) {
+      tmem_ld32(tl + t0, xw);
+      tmem_ld32(tl + 128 + t0, xu);
+      tmem_wait_ld_regs(xw);
+      tmem_wait_ld_regs(xu);
+    } else {
+#pragma unroll
+      for (int i = 0; i < 32; ++i) xw[i] = xu[i] = 0.f;
+    }
+    const size_t tw = tile * kTileW;
+#pragma unroll
+    for (int g8 = 0; g8 < 4; ++g8) {
+      float wv[8], qv[8], kv[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const int t = t0 + 8 * g8 + e;
+        const bool vt = t < len;
+        const float G = sG[t * kGP + c], E = __expf(G), kb = bf16_at(sK, t, c);
+        wv[e] = vt ? to_tf32(fmaf(s_b[t] * s_rk[t] * E, kb, xw[8 * g8 + e])) : 0.f;
+        qv[e] = vt ? to_tf32(p.scale * s_rq[t] * E * bf16_at(sQ, t, c)) : 0.f;
+        kv[e] = vt ? to_tf32(s_rk[t] * __expf(glc - G) * kb) : 0.f;
+        const float u = vt ? fmaf(s_b[t], bf16_at(sV, t, c), xu[8 * g8 + e]) : 0.f;
+        const size_t o = tw + size_t(t) * kD + c;
+        p.W[o] = wv[e];
+        p.U[o] = u;
+        p.Qt[o] = qv[e];
+        if (p.Kt) p.Kt[o] = kv[e];
+        if (p.Gc) p.Gc[(tile * kC + t) * kD + c] = G;
+      }
+      const size_t ot = tile * kTileKtT + size_t(c) * kC + t0 + 8 * g8;
+      if (p.WT) st_f32x8(p.WT + ot, wv);
+      st_f32x8(p.KtT + ot, kv);
+      if (p.QtT) st_f32x8(p.QtT + ot, qv);
     }
     if (tid < kC) {
       if (p.rq) p.rq[tile * kC + tid] = s_rq[tid];
       if (p.rk) p.rk[tile * kC + tid] = s_rk[tid];
       if (p.beff) p.beff[tile * kC + tid] = s_b[tid];
-    }
-  }
-  __syncthreads();
-  {
-    float* ktt = p.KtT + tile * kTileKtT;
-#pragma unroll 4
-    for (int m = 0; m < kD * kC / kThreads; ++m) {
-      const int idx = m * kThreads + tid, c = idx >> 6, t = idx & 63;
-      ktt[idx] = sKT[c * kTP + t];
-      if (p.QtT) p.QtT[tile * kTileKtT + idx] = sQT[c * kTP + t];
     }
   }
   tc_fence_before();
