@@ -285,7 +285,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   // operands A1 = A diag(beta exp(G) r_k) and A2 = A diag(beta), bf16, K-major, 128x128, with
   // the unit diagonal left out (added in fp32 after the MMA).
   {
-    const int cb = warp >> 2, cc = 16 * (warp & 3) + (lane & 15);
+    // The columns of the first 16-row block cost the most; the second chunk takes its blocks in
+    // reverse so that warps w and w + 4 (one SM sub-partition) share the work evenly.
+    const int cb = warp >> 2, cc = 16 * (cb ? 3 - (warp & 3) : (warp & 3)) + (lane & 15);
     unit_lower_inverse_column(sL + cb * (kC * kC), reinterpret_cast<float*>(sQ) + cb * (kC * kC), cc, lane >> 4);
   }
   if (tid == 0) tma_store_wait_read();  // A1 held the staged Aqk tiles
