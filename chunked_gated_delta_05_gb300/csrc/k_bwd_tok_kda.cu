@@ -17,11 +17,11 @@
 //   dbeta_i = sum_c k^_ic X1_ic + sum_c exp(G_ic) dK1_ic k^_ic + sum_c dV1_ic v_ic
 //   dg = reverse cumulative sum of dG over the chunk's tokens, per channel.
 // GB300 mapping: dAqk, dA = [dW | dU][K1 | V1]^T, A^T dA and (A^T dA) A^T are 64-row
-// tcgen05 MMAs (kind::tf32) as in the scalar-gate kernel. The decayed pair sums run on the CUDA
-// cores in fp32, one thread per (channel, pair of 16-row blocks): pairs inside a block take
-// exp(G_ic - G_jc) as a running product of the per-token decays, pairs across blocks factor it
-// through the block's first or last row into two factors of at most 1 (G falls along the
-// chunk), so no exponent is per pair.
+// tcgen05 MMAs (kind::tf32) as in the scalar-gate kernel. The decayed pair sums are tensor-core
+// products too: each pair's decay factors through the reference row of the later token's
+// 16-row block into two bounded per-channel factors (the prepare kernel's Gram factorisation),
+// and two rounds of 128-lane products with the channels on the accumulator lanes give X1, Y1
+// and Z; the CUDA cores apply the row factors and assemble the gradients.
 #include "common.cuh"
 #include "umma.cuh"
 
@@ -35,7 +35,8 @@ constexpr uint32_t kOffQ = 0, kOffK = 16384, kOffV = 32768;  // bf16 [64][128]
 constexpr uint32_t kOffG = 49152;                            // G * log2(e), fp32 [64][129]
 constexpr uint32_t kR1 = 83968, kR2 = 116736, kR3 = 149504, kR4 = 182272;  // 32 KB each
 constexpr uint32_t kSmemBytes = kR4 + 32768 + 1024;
-constexpr uint32_t kTAqk = 0, kTdA = 64, kTX = 128;
+constexpr uint32_t kTAqk = 0, kTdA = 64, kTX = 128;  // 64-row products
+constexpr uint32_t kTXY = 0, kTV = 256;              // pair-sum products (channels on the lanes)
 
 __device__ __forceinline__ uint8_t* align1k(uint8_t* p) {
   return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
@@ -60,127 +61,11 @@ __device__ __forceinline__ uint2 pack_bf16x4(const float* x) {
 __device__ __forceinline__ void put32(uint8_t* tile, int rows, int row, int col, float x) {
   *reinterpret_cast<float*>(tile + sw128_offset(row, col, rows, 4)) = x;
 }
-
-
-// Decayed pair sums of the 16-row block I of the chunk for key channel c: rows i of the block
-// get X1 and Y1, columns j of the block get Z (sums defined in the kernel header; G in log2
-// units). Pairs across blocks factor through the block's reference rows, and since G falls
-// along the chunk both factors are at most 1: for j < 16 I <= i,
-//   exp(G_i - G_j) = exp(G_i - G_r) exp(G_r - G_j),  r = 16 I,
-// and for i > 16 I + 15 >= j,
-//   exp(G_i - G_j) = exp(G_i - G_s) exp(G_s - G_j),  s = 16 I + 15.
-// The 136 pairs inside the block take exp(G_i - G_j) as a running product of the per-token
-// decays (each <= 1), one exponent per row, shared by the three sums.
-// Everything stays in fp32. The block's rows are then written to the dk^ / dq^ / dG
-// accumulators, and k^ . X1 goes to dbeta. One copy of the code serves every block (I is a
-// run-time value), which keeps the kernel's instruction footprint small.
-__device__ __forceinline__ void kda_pair_block(int I, const float* __restrict__ sG2, const uint8_t* __restrict__ sK,
-                                               const uint8_t* __restrict__ sQ, const float* __restrict__ s_rk,
-                                               const float* __restrict__ s_rq, const float* __restrict__ s_b,
-                                               const float* __restrict__ sD, const float* __restrict__ sN,
-                                               float* __restrict__ sKacc, float* __restrict__ sQacc,
-                                               float* __restrict__ sGacc, float* s_db, int c, int lane) {
-  const int r0 = 16 * I;
-  const float R = sG2[r0 * kP + c], S = sG2[(r0 + 15) * kP + c];  // the block's first and last rows
-  float x1[16], y1[16], z[16], kb[16];
-#pragma unroll
-  for (int r = 0; r < 16; ++r) {
-    const int t = r0 + r;
-    kb[r] = s_rk[t] * bf16_at(sK, t, c);
-    x1[r] = 0.f;
-    y1[r] = 0.f;
-    z[r] = 0.f;
-  }
-  {  // rows of the block against the earlier columns, four at a time
-#pragma unroll 1
-    for (int m = 0; m < r0 / 4; ++m) {
-      float P[4];
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int j = 4 * m + e;
-        P[e] = s_rk[j] * bf16_at(sK, j, c) * exp2f(R - sG2[j * kP + c]);
-      }
-#pragma unroll
-      for (int r = 0; r < 16; ++r) {
-        const float4 d = reinterpret_cast<const float4*>(sD + (r0 + r) * kC)[m];
-        const float4 n = reinterpret_cast<const float4*>(sN + (r0 + r) * kC)[m];
-        x1[r] = fmaf(d.x, P[0], fmaf(d.y, P[1], fmaf(d.z, P[2], fmaf(d.w, P[3], x1[r]))));
-        y1[r] = fmaf(n.x, P[0], fmaf(n.y, P[1], fmaf(n.z, P[2], fmaf(n.w, P[3], y1[r]))));
-      }
-    }
-#pragma unroll
-    for (int r = 0; r < 16; ++r) {
-      const float e = exp2f(sG2[(r0 + r) * kP + c] - R);
-      x1[r] *= e;
-      y1[r] *= e;
-    }
-  }
-  {  // later rows against the columns of the block
-#pragma unroll 2
-    for (int i = r0 + 16; i < kC; ++i) {
-      const float u = exp2f(sG2[i * kP + c] - S);
-      const float a = s_b[i] * s_rk[i] * bf16_at(sK, i, c) * u;
-      const float b = s_rq[i] * bf16_at(sQ, i, c) * u;
-      const float4* d4 = reinterpret_cast<const float4*>(sD + i * kC + r0);
-      const float4* n4 = reinterpret_cast<const float4*>(sN + i * kC + r0);
-#pragma unroll
-      for (int m = 0; m < 4; ++m) {
-        const float4 d = d4[m], n = n4[m];
-        z[4 * m] = fmaf(d.x, a, fmaf(n.x, b, z[4 * m]));
-        z[4 * m + 1] = fmaf(d.y, a, fmaf(n.y, b, z[4 * m + 1]));
-        z[4 * m + 2] = fmaf(d.z, a, fmaf(n.z, b, z[4 * m + 2]));
-        z[4 * m + 3] = fmaf(d.w, a, fmaf(n.w, b, z[4 * m + 3]));
-      }
-    }
-#pragma unroll
-    for (int s = 0; s < 16; ++s) z[s] *= exp2f(S - sG2[(r0 + s) * kP + c]);
-  }
-  // Pairs inside the block, i = r0 + r >= j = r0 + s. ex[s] = exp(G_i - G_j) follows the rows
-  // as a running product of the per-token decays exp(G_r - G_{r-1}) <= 1: one exponent per row.
-  float ex[16];
-  float gprev = R;
-#pragma unroll
-  for (int r = 0; r < 16; ++r) {
-    const int i = r0 + r;
-    const float gr = sG2[i * kP + c];
-    if (r > 0) {
-      const float a = exp2f(gr - gprev);
-#pragma unroll
-      for (int s = 0; s < r; ++s) ex[s] *= a;
-    }
-    ex[r] = 1.f;
-    gprev = gr;
-    const float ci = s_b[i] * kb[r], qi = s_rq[i] * bf16_at(sQ, i, c);
-    const float4* d4 = reinterpret_cast<const float4*>(sD + i * kC + r0);
-    const float4* n4 = reinterpret_cast<const float4*>(sN + i * kC + r0);
-#pragma unroll
-    for (int m = 0; m <= r / 4; ++m) {
-      const float4 d = d4[m], n = n4[m];
-      const float dd[4] = {d.x, d.y, d.z, d.w}, nn[4] = {n.x, n.y, n.z, n.w};
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int s = 4 * m + e;
-        if (s <= r) {
-          x1[r] = fmaf(dd[e] * kb[s], ex[s], x1[r]);
-          y1[r] = fmaf(nn[e] * kb[s], ex[s], y1[r]);
-          z[s] = fmaf(fmaf(ci, dd[e], nn[e] * qi), ex[s], z[s]);
-        }
-      }
-    }
-  }
-#pragma unroll
-  for (int r = 0; r < 16; ++r) {
-    const int t = r0 + r;
-    const float bt = s_b[t], qt = s_rq[t] * bf16_at(sQ, t, c);
-    sKacc[t * kD + c] = bt * x1[r] + z[r];
-    sQacc[t * kD + c] = y1[r];
-    sGacc[t * kD + c] = bt * kb[r] * x1[r] + qt * y1[r] - kb[r] * z[r];
-    float part = kb[r] * x1[r];
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) part += __shfl_xor_sync(0xffffffffu, part, off);
-    if (lane == 0) s_db[t] = part;  // this warp's channel group's share (summed in a fixed order later)
-  }
+// Four consecutive fp32 columns (col % 4 == 0: one 16-byte chunk of the swizzled row).
+__device__ __forceinline__ void put32x4(uint8_t* tile, int rows, int row, int col, const float* x) {
+  *reinterpret_cast<float4*>(tile + sw128_offset(row, col, rows, 4)) = make_float4(x[0], x[1], x[2], x[3]);
 }
+
 
 }  // namespace
 
@@ -202,7 +87,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   // per-token sums over the channels: the pair sums' share of dbeta, one partial per group of
   // 32 channels (warp % 4), added in a fixed order so that the result does not depend on warp
   // scheduling; the assembly's sums (one warp reduction per token row)
-  __shared__ float s_dbp[4][kC], s_dba[1][kC], s_dotq[1][kC], s_dotk[1][kC];
+  __shared__ float s_dba[1][kC], s_dotq[1][kC], s_dotk[1][kC];
+  __shared__ __align__(16) float s_glw[kThreads / 32][kD];  // each warp's dG_last shares
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int wq = warp & 3, half = warp >> 2;
@@ -216,7 +102,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int cc = tid & 127;   // channel handled in the CUDA-core phases
   const float dgam_c = p.dgam[tile * kD + cc];  // requested now, used by the last phase
 
-  if (warp == 0) tmem_alloc(&tslot, 256);
+  if (warp == 0) tmem_alloc(&tslot, 512);
   if (tid == 0) {
     abort_flag = 0;
     mbar_init(&bar_tma, 1);
@@ -394,10 +280,25 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncwarp();
   ok = ok && mbar_wait(&bar_mma, 1, &abort_flag, p.status, kDevTimeoutMma);
   tc_fence_after();
-  // ---- stage D = dL (strictly lower) and N = scale dAqk (lower), fp32 [64][64] (every thread
-  // reads the same element at a time, so no padding is needed)
-  float* sD = reinterpret_cast<float*>(sm + kR1);
-  float* sN = sD + kC * kC;
+  // ---- decayed pair sums on the tensor cores. For i in the 16-row block I (reference row
+  // r_I = 16 I) and j <= 16 I + 15, exp(G_ic - G_jc) = P_ic E_I[j][c] with
+  // P_ic = exp(G_ic - G_{r_I,c}) <= 1 and E_I[j][c] = exp(G_{r_I,c} - G_jc), which is <= 1 for
+  // j < r_I and at most the in-block drop for j in block I (the prepare kernel's factorisation).
+  // With D = dL (strictly lower) and N = scale dAqk (lower):
+  //   X1_I = P_I (.) D_I (E_I (.) k^),  Y1_I = P_I (.) N_I (E_I (.) k^)     (rows of block I)
+  //   Z    = sum_{I >= J(j)} E_I (.) V_I,  V_I[j][c] = sum_{i in I} (D_ij beta_i k^_ic + N_ij q^_ic) P_ic
+  // Both products run with the channels on the 128 accumulator lanes (kind::tf32):
+  //   round V: V_I^T = XP_I^T MT_I^T, K = the block's 16 rows for D and 16 for N;
+  //   round X: [X1 | Y1]_I^T (unscaled) = (E_I (.) k^)^T [D_I ; N_I]^T, K = 16 (I + 1) tokens.
+  // The operands: MT [j][k'] and XP^T [c][k'] with k' = 32 I + 16 part + i % 16 (part 0: D and
+  // beta k^ P, part 1: N and q^ P); DN [rho][j], rho = k' (the rows D_I, N_I of block I are
+  // 32 consecutive rows); EK_I^T [c][j]. Rows past the chunk are zero in D, N, k and q.
+  uint8_t* sMT = sm + kR1;                       // [64][128] tf32, four 8 KB panels (one per block)
+  uint8_t* sXP = sm + kR2;                       // [128][128] tf32, four 16 KB panels (R2, R3)
+  auto ek_base = [&](int I) -> uint8_t* {        // EK_I^T [128][16 (I + 1)], 16 KB panels
+    return sm + (I == 3 ? kR2 : (I == 2 ? kR3 : (I == 1 ? kR4 : kR4 + 16384)));
+  };
+  uint8_t* sDN = sm + kR1;                       // [128][64] tf32, two 16 KB panels
   {
     float dl[32], nn[32];
     tmem_ld32(tl + kTX + 32 * half, dl);
@@ -405,27 +306,181 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_wait_ld_regs(dl);
     tmem_wait_ld_regs(nn);
     if (owner) {
-      const int i = rr;
+      const int i = rr, kq = 32 * (i >> 4) + (i & 15);
       const bool vi = i < len;
 #pragma unroll
       for (int jj = 0; jj < 32; ++jj) {
         const int j = 32 * half + jj;
-        const float D = (j < i && vi) ? -dl[jj] : 0.f;
-        sD[i * kC + j] = D;
-        sN[i * kC + j] = (j <= i && vi) ? scale * nn[jj] : 0.f;
+        put32(sMT, kC, j, kq, (j < i && vi) ? to_tf32(-dl[jj]) : 0.f);
+        put32(sMT, kC, j, kq + 16, (j <= i && vi) ? to_tf32(scale * nn[jj]) : 0.f);
       }
     }
   }
+  {
+    // XP^T: thread (channel cc, blocks 2 half and 2 half + 1), four rows per 16-byte store
+    const int c = cc;
+#pragma unroll 1
+    for (int b = 0; b < 2; ++b) {
+      const int I = 2 * half + b, r0 = 16 * I;
+      const float gr = sG2[r0 * kP + c];
+#pragma unroll
+      for (int r4 = 0; r4 < 16; r4 += 4) {
+        float xk[4], xq[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int i = r0 + r4 + e;
+          const float P = exp2f(sG2[i * kP + c] - gr);
+          xk[e] = to_tf32(s_b[i] * s_rk[i] * bf16_at(sK, i, c) * P);
+          xq[e] = to_tf32(s_rq[i] * bf16_at(sQ, i, c) * P);
+        }
+        put32x4(sXP, kD, c, 32 * I + r4, xk);
+        put32x4(sXP, kD, c, 32 * I + 16 + r4, xq);
+      }
+    }
+  }
+  fence_async_smem();
   tc_fence_before();
   __syncthreads();
-  // ---- decayed pair sums on CUDA cores: thread (channel cc, row blocks 2 half and 2 half + 1,
-  // which balances the two halves' work). Rows past the chunk come out zero.
+  tc_fence_after();
+  if (tid == 0 && ok) {
+    const uint32_t id = idesc_tf32(128, 64), xp = smem_u32(sXP), mt = smem_u32(sMT);
+    for (int I = 0; I < 4; ++I)
+      for (int s = 0; s < 4; ++s)
+        mma_tf32_ss(tb + kTV + 64 * I, desc_kmajor(xp + 16384 * I, 16384, s), desc_kmajor(mt + 8192 * I, 8192, s), id, s > 0);
+    mma_commit(&bar_mma);
+  }
+  __syncwarp();
+  ok = ok && mbar_wait(&bar_mma, 0, &abort_flag, p.status, kDevTimeoutMma);
+  tc_fence_after();
+  __syncthreads();  // MT and XP^T are free: DN and EK^T take their places
+  {
+    float dl[32], nn[32];
+    tmem_ld32(tl + kTX + 32 * half, dl);
+    tmem_ld32(tl + kTAqk + 32 * half, nn);
+    tmem_wait_ld_regs(dl);
+    tmem_wait_ld_regs(nn);
+    if (owner) {
+      const int i = rr, rho = 32 * (i >> 4) + (i & 15);
+      const bool vi = i < len;
+#pragma unroll
+      for (int j4 = 0; j4 < 32; j4 += 4) {
+        float d4[4], n4[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int j = 32 * half + j4 + e;
+          d4[e] = (j < i && vi) ? to_tf32(-dl[j4 + e]) : 0.f;
+          n4[e] = (j <= i && vi) ? to_tf32(scale * nn[j4 + e]) : 0.f;
+        }
+        put32x4(sDN, 2 * kC, rho, 32 * half + j4, d4);
+        put32x4(sDN, 2 * kC, rho + 16, 32 * half + j4, n4);
+      }
+    }
+  }
+  {
+    // EK_I^T rows of token block J for every I >= J: thread (channel cc, blocks {0, 3} or
+    // {1, 2}, which balances the halves), four tokens per 16-byte store
+    const int c = cc;
+#pragma unroll 1
+    for (int b = 0; b < 2; ++b) {
+      const int J = half == 0 ? 3 * b : 1 + b, r0 = 16 * J;
+      const float gJ = sG2[r0 * kP + c];
+      float tr[4];
+#pragma unroll
+      for (int I = 0; I < 4; ++I) tr[I] = I > J ? exp2f(sG2[16 * I * kP + c] - gJ) : 1.f;
+#pragma unroll
+      for (int r4 = 0; r4 < 16; r4 += 4) {
+        float kd[4], x[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int j = r0 + r4 + e;
+          kd[e] = s_rk[j] * bf16_at(sK, j, c) * exp2f(gJ - sG2[j * kP + c]);
+        }
+#pragma unroll
+        for (int I = 0; I < 4; ++I) {
+          if (I < J) continue;
+#pragma unroll
+          for (int e = 0; e < 4; ++e) x[e] = to_tf32(tr[I] * kd[e]);
+          put32x4(ek_base(I), kD, c, r0 + r4, x);
+        }
+      }
+    }
+  }
+  fence_async_smem();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (tid == 0 && ok) {
+    const uint32_t id = idesc_tf32(128, 32), dn = smem_u32(sDN);
+    for (int I = 0; I < 4; ++I) {
+      const uint32_t ek = smem_u32(ek_base(I));
+      for (int s = 0; s < 2 * (I + 1); ++s)
+        mma_tf32_ss(tb + kTXY + 32 * I, desc_kmajor(ek, 16384, s), desc_kmajor(dn + 4096 * I, 16384, s), id, s > 0);
+    }
+    mma_commit(&bar_mma);
+  }
+  __syncwarp();
+  ok = ok && mbar_wait(&bar_mma, 1, &abort_flag, p.status, kDevTimeoutMma);
+  tc_fence_after();
+  __syncthreads();  // the EK^T operands are free: the accumulators take their places
+  // Per (token, channel) results into the dk^ / dq^ / dG accumulators and k^ (.) X1 (dbeta's
+  // pair part): thread (channel cc, token blocks {0, 3} or {1, 2}).
+  // dG takes each pair through its row (X1, Y1) and its column (Z) with the same tf32 factors
+  // that entered the products (recomputed bit for bit: XP for the rows, EK for the columns), so
+  // the two sides of every pair cancel exactly over the chunk, as the exact sums do; dk^ and
+  // dq^ take the fp32 factors.
   float* sKacc = reinterpret_cast<float*>(sm + kR2);           // dk^ accumulator [64][128]
   float* sQacc = reinterpret_cast<float*>(sm + kR3);           // dq^ accumulator [64][128]
   float* sGacc = reinterpret_cast<float*>(sm + kR4);           // dG accumulator [64][128]
+  float* sKX = reinterpret_cast<float*>(sm + kR1);             // k^ (.) X1 [64][128] (DN is dead)
+  {
+    const int c = cc;
 #pragma unroll 1
-  for (int b = 0; b < 2; ++b)
-    kda_pair_block(2 * half + b, sG2, sK, sQ, s_rk, s_rq, s_b, sD, sN, sKacc, sQacc, sGacc, s_dbp[warp & 3], cc, lane);
+    for (int b = 0; b < 2; ++b) {
+      const int J = half == 0 ? 3 * b : 1 + b, r0 = 16 * J;
+      const float gJ = sG2[r0 * kP + c];
+      float xy[32], z[16], zg[16], kd[16], ee[16];
+      if (ok) {
+        tmem_ld32(tl + kTXY + 32 * J, xy);
+        tmem_wait_ld_regs(xy);
+      } else {
+#pragma unroll
+        for (int e = 0; e < 32; ++e) xy[e] = 0.f;
+      }
+#pragma unroll
+      for (int r = 0; r < 16; ++r) {
+        const int t = r0 + r;
+        ee[r] = exp2f(gJ - sG2[t * kP + c]);
+        kd[r] = s_rk[t] * bf16_at(sK, t, c) * ee[r];  // E_J (.) k^, as the operand build has it
+        z[r] = 0.f;
+        zg[r] = 0.f;
+      }
+      for (int I = J; I < 4 && ok; ++I) {
+        float v[16];
+        tmem_ld16(tl + kTV + 64 * I + r0, v);
+        tmem_wait_ld_regs(v);
+        const float tr = I > J ? exp2f(sG2[16 * I * kP + c] - gJ) : 1.f;
+#pragma unroll
+        for (int r = 0; r < 16; ++r) {
+          z[r] = fmaf(tr, v[r], z[r]);
+          zg[r] = fmaf(to_tf32(tr * kd[r]), v[r], zg[r]);
+        }
+      }
+#pragma unroll
+      for (int r = 0; r < 16; ++r) {
+        const int t = r0 + r;
+        const float g = sG2[t * kP + c];
+        const float P = exp2f(g - gJ), E = ee[r];
+        const float kb = bf16_at(sK, t, c), qb = bf16_at(sQ, t, c);
+        const float kh = s_rk[t] * kb, bt = s_b[t];
+        const float x1 = P * xy[r], y1 = P * xy[16 + r];
+        const float xk = to_tf32(s_b[t] * s_rk[t] * kb * P), xq = to_tf32(s_rq[t] * qb * P);
+        sKacc[t * kD + c] = bt * x1 + E * z[r];
+        sQacc[t * kD + c] = y1;
+        sGacc[t * kD + c] = xk * xy[r] + xq * xy[16 + r] - zg[r];
+        sKX[t * kD + c] = kh * x1;  // dbeta's pair part, summed over the channels by the assembly
+      }
+    }
+  }
   __syncthreads();
   // ---- per-token assembly: each warp takes whole token rows, lane l channels 4l .. 4l+3.
   // The row sums over the channels (dbeta, q^ . dq^, k^ . dk^) are one warp reduction each,
@@ -455,7 +510,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       float4* ga4 = reinterpret_cast<float4*>(sGacc + t * kD + c4);
       const float4 qa = *qa4, ka = *ka4, ga = *ga4;
       float qacc[4] = {qa.x, qa.y, qa.z, qa.w}, kacc[4] = {ka.x, ka.y, ka.z, ka.w}, gacc[4] = {ga.x, ga.y, ga.z, ga.w};
-      float sdb = 0.f, sq = 0.f, sk = 0.f, dvo[4];
+      const float4 kx = *reinterpret_cast<const float4*>(sKX + t * kD + c4);
+      float sdb = (kx.x + kx.y) + (kx.z + kx.w), sq = 0.f, sk = 0.f, dvo[4];
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         const float G = sG2[t * kP + c4 + e];
@@ -488,9 +544,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         s_dotk[0][t] = sk;
       }
     }
-    // the pair sums no longer read dL: its tile holds each warp's dG_last shares [8][128]
 #pragma unroll
-    for (int e = 0; e < 4; ++e) sD[warp * kD + c4 + e] = glp[e];
+    for (int e = 0; e < 4; ++e) s_glw[warp][c4 + e] = glp[e];
   }
   __syncthreads();
   // ---- L2-norm backward and writes: each warp takes whole token rows, lane l channels
@@ -527,7 +582,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (half == 0) {
     float acc = exp2f(glc) * dgam_c;
 #pragma unroll
-    for (int w = 0; w < kThreads / 32; ++w) acc += sD[w * kD + cc];   // dG_last shares, in warp order
+    for (int w = 0; w < kThreads / 32; ++w) acc += s_glw[w][cc];   // dG_last shares, in warp order
     if (p.gate_act) {
       // chain rule through the safe gate g = lb sigmoid(z), z = a (x + dt_bias), a = exp(A_log):
       // dx = dg lb s (1 - s) a; the parameter gradients are summed per chunk here and over the
@@ -555,13 +610,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
   if (tid < len) {
-    float db = ((s_dbp[0][tid] + s_dbp[1][tid]) + (s_dbp[2][tid] + s_dbp[3][tid])) + s_dba[0][tid];
+    float db = s_dba[0][tid];
     if (p.beta_sigmoid) db *= s_b[tid] * (1.f - s_b[tid]);
     p.dbeta[size_t(ch.x + tid) * H + h] = __float2bfloat16_rn(db);
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == 0) tmem_dealloc(tb, 256);
+  if (warp == 0) tmem_dealloc(tb, 512);
 }
 
 cudaError_t launch_bwd_tok_kda(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
