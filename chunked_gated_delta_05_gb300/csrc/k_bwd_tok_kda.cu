@@ -292,13 +292,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   //   round X: [X1 | Y1]_I^T (unscaled) = (E_I (.) k^)^T [D_I ; N_I]^T, K = 16 (I + 1) tokens.
   // The operands: MT [j][k'] and XP^T [c][k'] with k' = 32 I + 16 part + i % 16 (part 0: D and
   // beta k^ P, part 1: N and q^ P); DN [rho][j], rho = k' (the rows D_I, N_I of block I are
-  // 32 consecutive rows); EK_I^T [c][j]. Rows past the chunk are zero in D, N, k and q.
+  // 32 consecutive rows); EK_I^T [c][j]. Rows past the chunk are zero in D, N, k and q. MT,
+  // XP^T and DN are written in one pass; EK^T replaces MT and XP^T once round V is done.
   uint8_t* sMT = sm + kR1;                       // [64][128] tf32, four 8 KB panels (one per block)
   uint8_t* sXP = sm + kR2;                       // [128][128] tf32, four 16 KB panels (R2, R3)
-  auto ek_base = [&](int I) -> uint8_t* {        // EK_I^T [128][16 (I + 1)], 16 KB panels
-    return sm + (I == 3 ? kR2 : (I == 2 ? kR3 : (I == 1 ? kR4 : kR4 + 16384)));
+  uint8_t* sDN = sm + kR4;                       // [128][64] tf32, two 16 KB panels
+  auto ek_base = [&](int I) -> uint8_t* {        // EK_I^T [128][16 (I + 1)], 16 KB panels, after round V
+    return sm + (I == 3 ? kR1 : (I == 2 ? kR2 : (I == 1 ? kR3 : kR3 + 16384)));
   };
-  uint8_t* sDN = sm + kR1;                       // [128][64] tf32, two 16 KB panels
   {
     float dl[32], nn[32];
     tmem_ld32(tl + kTX + 32 * half, dl);
@@ -309,10 +310,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int i = rr, kq = 32 * (i >> 4) + (i & 15);
       const bool vi = i < len;
 #pragma unroll
-      for (int jj = 0; jj < 32; ++jj) {
-        const int j = 32 * half + jj;
-        put32(sMT, kC, j, kq, (j < i && vi) ? to_tf32(-dl[jj]) : 0.f);
-        put32(sMT, kC, j, kq + 16, (j <= i && vi) ? to_tf32(scale * nn[jj]) : 0.f);
+      for (int j4 = 0; j4 < 32; j4 += 4) {
+        float d4[4], n4[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int j = 32 * half + j4 + e;
+          d4[e] = (j < i && vi) ? to_tf32(-dl[j4 + e]) : 0.f;
+          n4[e] = (j <= i && vi) ? to_tf32(scale * nn[j4 + e]) : 0.f;
+          put32(sMT, kC, j, kq, d4[e]);
+          put32(sMT, kC, j, kq + 16, n4[e]);
+        }
+        put32x4(sDN, 2 * kC, kq, 32 * half + j4, d4);
+        put32x4(sDN, 2 * kC, kq + 16, 32 * half + j4, n4);
       }
     }
   }
@@ -352,30 +361,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncwarp();
   ok = ok && mbar_wait(&bar_mma, 0, &abort_flag, p.status, kDevTimeoutMma);
   tc_fence_after();
-  __syncthreads();  // MT and XP^T are free: DN and EK^T take their places
-  {
-    float dl[32], nn[32];
-    tmem_ld32(tl + kTX + 32 * half, dl);
-    tmem_ld32(tl + kTAqk + 32 * half, nn);
-    tmem_wait_ld_regs(dl);
-    tmem_wait_ld_regs(nn);
-    if (owner) {
-      const int i = rr, rho = 32 * (i >> 4) + (i & 15);
-      const bool vi = i < len;
-#pragma unroll
-      for (int j4 = 0; j4 < 32; j4 += 4) {
-        float d4[4], n4[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int j = 32 * half + j4 + e;
-          d4[e] = (j < i && vi) ? to_tf32(-dl[j4 + e]) : 0.f;
-          n4[e] = (j <= i && vi) ? to_tf32(scale * nn[j4 + e]) : 0.f;
-        }
-        put32x4(sDN, 2 * kC, rho, 32 * half + j4, d4);
-        put32x4(sDN, 2 * kC, rho + 16, 32 * half + j4, n4);
-      }
-    }
-  }
+  __syncthreads();  // MT and XP^T are free: EK^T takes their place
   {
     // EK_I^T rows of token block J for every I >= J: thread (channel cc, blocks {0, 3} or
     // {1, 2}, which balances the halves), four tokens per 16-byte store
