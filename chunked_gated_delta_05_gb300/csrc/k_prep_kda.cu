@@ -178,15 +178,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   // word reports kDevGateRange.
   {
     const int c = tid & 127;
-    bool in_range = true;
-    for (int I = 2 * hf; I < 2 * hf + 2; ++I) {
-      const int r = 16 * I;
-      if (r >= len) break;
+    bool bad = false;  // accumulated without short-circuiting, so the loads all go out at once
+#pragma unroll
+    for (int b = 0; b < 2; ++b) {
+      const int r = 16 * (2 * hf + b);
       const float gr = sG[r * kGP + c];
-      for (int i = r + 1; i < min(r + 16, len); ++i)
-        in_range = in_range && fabsf(sG[i * kGP + c] - gr) <= kKdaBlockDropMax;
+#pragma unroll
+      for (int e = 1; e < 16; ++e)
+        bad |= (r + e < len) & !(fabsf(sG[(r + e) * kGP + c] - gr) <= kKdaBlockDropMax);
     }
-    if (!in_range && p.status) atomicCAS(p.status, 0, kDevGateRange);
+    if (bad && p.status) atomicCAS(p.status, 0, kDevGateRange);
     for (int pr = hf; pr < 6; pr += 2) {
       const int I = pr == 0 ? 1 : (pr < 3 ? 2 : 3), J = pr - I * (I - 1) / 2;
       s_T[pr][c] = __expf(sG[16 * I * kGP + c] - sG[16 * J * kGP + c]);
