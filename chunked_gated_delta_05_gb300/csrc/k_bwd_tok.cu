@@ -362,12 +362,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  // column sums of P
-  if (tid < kC) {
-    float col = 0.f;
-    for (int i = 0; i < kC; ++i) col += s_P[i][tid];
-    s_dG[tid] -= col;
-  }
   // ---- products 4: dq^ part = Nq k^T^T (rows i); dk^ part = E1 k + E2^T k + Nk^T q (rows)
   if (tid == 0 && ok) {
     const uint32_t id = idesc_tf32(64, 128);
@@ -377,6 +371,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int s = 0; s < 8; ++s) mma_tf32_ss(tb + kTRk, desc_kmajor(smem_u32(sE2T), 8192, s), desc_kmajor(kt, 16384, s), id, true);
     for (int s = 0; s < 8; ++s) mma_tf32_ss(tb + kTRk, desc_kmajor(smem_u32(sNkT), 8192, s), desc_kmajor(qt, 16384, s), id, true);
     mma_commit(&bar_mma);
+  }
+  // column sums of P while the products run
+  if (tid < kC) {
+    float col = 0.f;
+#pragma unroll 8
+    for (int i = 0; i < kC; ++i) col += s_P[i][tid];
+    s_dG[tid] -= col;
   }
   __syncwarp();
   ok = ok && mbar_wait(&bar_mma, 0, &abort_flag, p.status, kDevTimeoutMma);

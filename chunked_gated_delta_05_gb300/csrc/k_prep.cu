@@ -157,12 +157,36 @@ __global__ void __launch_bounds__(kThreads, 1)
     part[tid] = ssq;
     part[kThreads + tid] = ssk;
   }
+  tc_fence_before();
   __syncthreads();
+  tc_fence_after();
+  // Gram products: TMEM cols [0,128) = K K^T, [128,256) = Q K^T (pair-stacked). They read only
+  // the raw tiles, so they start here, under the norms and the gate cumsum.
+  if (tid == 0 && !abort_flag) {
+    const uint32_t id = idesc_bf16(128, 128);
+    const uint32_t q0 = smem_u32(sQ), k0 = smem_u32(sK);
+    for (int s = 0; s < 8; ++s) mma_bf16_ss(tb, desc_kmajor(k0, kPanel, s), desc_kmajor(k0, kPanel, s), id, s > 0);
+    for (int s = 0; s < 8; ++s)
+      mma_bf16_ss(tb + 128, desc_kmajor(q0, kPanel, s), desc_kmajor(k0, kPanel, s), id, s > 0);
+    mma_commit(&bar_mma);
+  }
   const float* part = reinterpret_cast<const float*>(sA1);
   const float rq = p.l2norm ? 1.f / sqrtf(part[rt] + part[rt + kRows] + 1e-6f) : 1.f;
   const float rk = p.l2norm ? 1.f / sqrtf(part[kThreads + rt] + part[kThreads + rt + kRows] + 1e-6f) : 1.f;
-  float G = 0.f;
-  for (int j = 0; j <= il; ++j) G += s_g[blk * kC + j];
+  // G = chunk-local cumulative gate of row il: an inclusive scan over the warp's 32 rows plus,
+  // for rows 32..63, the total of rows 0..31 (a warp sum)
+  float G = s_g[rt];
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const float y = __shfl_up_sync(0xffffffffu, G, off);
+    if (lane >= off) G += y;
+  }
+  if (il >= 32) {
+    float base = s_g[blk * kC + lane];
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) base += __shfl_xor_sync(0xffffffffu, base, off);
+    G += base;
+  }
   if (hf == 0) {
     s_rk[rt] = rk;
     s_G2[rt] = G * kLog2e;  // exp(G_i - G_j) = exp2(G2_i - G2_j)
@@ -172,15 +196,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const float Glast2 = len > 0 ? s_G2[blk * kC + len - 1] : 0.f;  // G_last log2(e)
 
-  // Gram products: TMEM cols [0,128) = K K^T, [128,256) = Q K^T (pair-stacked).
-  if (tid == 0 && !abort_flag) {
-    const uint32_t id = idesc_bf16(128, 128);
-    const uint32_t q0 = smem_u32(sQ), k0 = smem_u32(sK);
-    for (int s = 0; s < 8; ++s) mma_bf16_ss(tb, desc_kmajor(k0, kPanel, s), desc_kmajor(k0, kPanel, s), id, s > 0);
-    for (int s = 0; s < 8; ++s)
-      mma_bf16_ss(tb + 128, desc_kmajor(q0, kPanel, s), desc_kmajor(k0, kPanel, s), id, s > 0);
-    mma_commit(&bar_mma);
-  }
 
   // Gated queries and end-decayed keys (state-independent operands of the chunk loop): the
   // row-major Qt and Kt tiles are staged (A1/A2 and L/S0 are free until the inverse) and
