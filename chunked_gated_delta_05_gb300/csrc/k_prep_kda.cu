@@ -270,6 +270,39 @@ __global__ void __launch_bounds__(kThreads, 1)
     mma_commit(&bar_mma);
   }
   __syncwarp();
+  // While the Gram products run: the per-token outputs that need only q, k and G. Thread
+  // (c, hf) takes channel c of the 32 tokens from 32 hf; Qt, Kt and G leave as coalesced rows,
+  // Qt^T and Kt^T as this thread's own row segments.
+  {
+    const int c = tid & 127, t0 = 32 * hf;
+    const float glc = s_gl[c];
+    if (hf == 0) p.gam[tile * kD + c] = expf(glc);
+    const size_t tw = tile * kTileW;
+#pragma unroll 1
+    for (int g8 = 0; g8 < 4; ++g8) {
+      float qv[8], kv[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const int t = t0 + 8 * g8 + e;
+        const bool vt = t < len;
+        const float G = sG[t * kGP + c];
+        qv[e] = vt ? to_tf32(p.scale * s_rq[t] * __expf(G) * bf16_at(sQ, t, c)) : 0.f;
+        kv[e] = vt ? to_tf32(s_rk[t] * __expf(glc - G) * bf16_at(sK, t, c)) : 0.f;
+        const size_t o = tw + size_t(t) * kD + c;
+        p.Qt[o] = qv[e];
+        if (p.Kt) p.Kt[o] = kv[e];
+        if (p.Gc) p.Gc[(tile * kC + t) * kD + c] = G;
+      }
+      const size_t ot = tile * kTileKtT + size_t(c) * kC + t0 + 8 * g8;
+      st_f32x8(p.KtT + ot, kv);
+      if (p.QtT) st_f32x8(p.QtT + ot, qv);
+    }
+    if (tid < kC) {
+      if (p.rq) p.rq[tile * kC + tid] = s_rq[tid];
+      if (p.rk) p.rk[tile * kC + tid] = s_rk[tid];
+      if (p.beff) p.beff[tile * kC + tid] = s_b[tid];
+    }
+  }
   bool ok = mbar_wait(&bar_mma, 0, &abort_flag, p.status, kDevTimeoutMma);
   uint32_t mma_phase = 1;
   tc_fence_after();
@@ -389,13 +422,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncwarp();
   ok = ok && mbar_wait(&bar_mma, mma_phase, &abort_flag, p.status, kDevTimeoutMma);
   tc_fence_after();
-  // Per-token outputs: thread (c, hf) takes channel c of the 32 tokens from 32 hf, with the
-  // unit diagonal of A added in fp32: W = A1 K1 + beta r_k exp(G) k and U = A2 v + beta v. W, U,
-  // Qt, Kt and G leave as coalesced rows; W^T, Qt^T and Kt^T as this thread's own row segments.
+  // W and U rows: thread (c, hf) takes channel c of the 32 tokens from 32 hf, with the unit
+  // diagonal of A added in fp32: W = A1 K1 + beta r_k exp(G) k and U = A2 v + beta v. W and U
+  // leave as coalesced rows, W^T as this thread's own row segments.
   {
     const int c = tid & 127, t0 = 32 * hf;
-    const float glc = s_gl[c];
-    if (hf == 0) p.gam[tile * kD + c] = expf(glc);
     float xw[32], xu[32];
     if (ok) {
       tmem_ld32(tl + t0, xw);
@@ -409,32 +440,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     const size_t tw = tile * kTileW;
 #pragma unroll
     for (int g8 = 0; g8 < 4; ++g8) {
-      float wv[8], qv[8], kv[8];
+      float wv[8];
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
         const int t = t0 + 8 * g8 + e;
         const bool vt = t < len;
-        const float G = sG[t * kGP + c], E = __expf(G), kb = bf16_at(sK, t, c);
-        wv[e] = vt ? to_tf32(fmaf(s_b[t] * s_rk[t] * E, kb, xw[8 * g8 + e])) : 0.f;
-        qv[e] = vt ? to_tf32(p.scale * s_rq[t] * E * bf16_at(sQ, t, c)) : 0.f;
-        kv[e] = vt ? to_tf32(s_rk[t] * __expf(glc - G) * kb) : 0.f;
+        const float E = __expf(sG[t * kGP + c]);
+        wv[e] = vt ? to_tf32(fmaf(s_b[t] * s_rk[t] * E, bf16_at(sK, t, c), xw[8 * g8 + e])) : 0.f;
         const float u = vt ? fmaf(s_b[t], bf16_at(sV, t, c), xu[8 * g8 + e]) : 0.f;
         const size_t o = tw + size_t(t) * kD + c;
         p.W[o] = wv[e];
         p.U[o] = u;
-        p.Qt[o] = qv[e];
-        if (p.Kt) p.Kt[o] = kv[e];
-        if (p.Gc) p.Gc[(tile * kC + t) * kD + c] = G;
       }
-      const size_t ot = tile * kTileKtT + size_t(c) * kC + t0 + 8 * g8;
-      if (p.WT) st_f32x8(p.WT + ot, wv);
-      st_f32x8(p.KtT + ot, kv);
-      if (p.QtT) st_f32x8(p.QtT + ot, qv);
-    }
-    if (tid < kC) {
-      if (p.rq) p.rq[tile * kC + tid] = s_rq[tid];
-      if (p.rk) p.rk[tile * kC + tid] = s_rk[tid];
-      if (p.beff) p.beff[tile * kC + tid] = s_b[tid];
+      if (p.WT) st_f32x8(p.WT + tile * kTileKtT + size_t(c) * kC + t0 + 8 * g8, wv);
     }
   }
   tc_fence_before();
