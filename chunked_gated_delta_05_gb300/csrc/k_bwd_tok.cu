@@ -224,6 +224,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     mma_commit(&bar_mma);
   }
   __syncwarp();
+  // A [i][j] (thread: column j, 16 rows i) is requested now, so that its trip from L2 overlaps
+  // the products
+  float abuf[16];
+  {
+    const float* a = p.A + tile * kTileAqk + (tid & 63);
+    const int i0 = 16 * (tid >> 6);
+#pragma unroll
+    for (int e = 0; e < 16; ++e) abuf[e] = a[size_t(i0 + e) * kC];
+  }
   ok = ok && mbar_wait(&bar_mma, 1, &abort_flag, p.status, kDevTimeoutMma);
   tc_fence_after();
   // ---- dL = -A^T dA A^T: X = A^T dA, then X A^T.
@@ -244,11 +253,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     {
       // A [i][j] read once, coalesced (thread: column j, 16 rows i), into both operands: A^T
       // (row j, four consecutive i per 16-byte chunk) and A (row i, column j)
-      const float* a = p.A + tile * kTileAqk;
       const int j = tid & 63, i0 = 16 * (tid >> 6);
       float buf[16];
 #pragma unroll
-      for (int e = 0; e < 16; ++e) buf[e] = to_tf32(a[size_t(i0 + e) * kC + j]);
+      for (int e = 0; e < 16; ++e) buf[e] = to_tf32(abuf[e]);
 #pragma unroll
       for (int e = 0; e < 16; e += 4) put32x4(sAT, kC, j, i0 + e, buf[e], buf[e + 1], buf[e + 2], buf[e + 3]);
 #pragma unroll
