@@ -68,16 +68,16 @@ KERNEL_SOURCES_KDA = {**KERNEL_SOURCES, "prepare": "k_prep_kda.cu", "bwd_tok": "
 # each, all heads in one group). The chunk kernels' traffic is per chunk-head, so the
 # B=1 T=32768 H=16 entries are those bytes x 4 (8192 chunk-heads) and the B=1 T=8192 H=32 KDA
 # entries x 2 (4096); the chains' traffic depends on the segment plan and is not scaled.
-_GDN_T4096 = {"prepare": 615_744_512, "chain_fwd": 606_034_688, "compose": 29_376_000,
-              "chain_bwd": 582_142_464, "bwd_feat": 758_795_264, "bwd_tok": 731_686_912}
-_KDA_T4096 = {"prepare": 748_054_784, "chain_fwd": 603_865_344, "compose": 29_396_992,
-              "chain_bwd": 582_913_536, "bwd_feat": 758_413_312, "bwd_tok": 852_842_496}
-_HASHES = {("prepare", False): "1e09286673b20acd", ("prepare", True): "6a74280f2722e6f5",
-           ("chain_fwd", False): "9697ea8042d5a846", ("chain_fwd", True): "9697ea8042d5a846",
-           ("compose", False): "059a56aca0ce6c0f", ("compose", True): "059a56aca0ce6c0f",
-           ("chain_bwd", False): "4adb8bd529345aa8", ("chain_bwd", True): "4adb8bd529345aa8",
-           ("bwd_feat", False): "1bc8ba8a210499f2", ("bwd_feat", True): "1bc8ba8a210499f2",
-           ("bwd_tok", False): "4c78d16e4c465c6b", ("bwd_tok", True): "11fceb34c4af0769"}
+_GDN_T4096 = {"prepare": 615_954_176, "chain_fwd": 606_352_640, "compose": 29_380_864,
+              "chain_bwd": 581_913_856, "bwd_feat": 758_830_080, "bwd_tok": 731_342_336}
+_KDA_T4096 = {"prepare": 750_101_504, "chain_fwd": 603_353_344, "compose": 29_376_256,
+              "chain_bwd": 583_386_624, "bwd_feat": 758_095_872, "bwd_tok": 853_983_488}
+_HASHES = {("prepare", False): "ca3d562323200c74", ("prepare", True): "32d8cafd687463b6",
+           ("chain_fwd", False): "6ca5f5c74541d246", ("chain_fwd", True): "6ca5f5c74541d246",
+           ("compose", False): "2a8e76a5313bc45a", ("compose", True): "2a8e76a5313bc45a",
+           ("chain_bwd", False): "b22fa42ebd53fcf1", ("chain_bwd", True): "b22fa42ebd53fcf1",
+           ("bwd_feat", False): "21c2dbfccbb89130", ("bwd_feat", True): "21c2dbfccbb89130",
+           ("bwd_tok", False): "5e572442e06a4f09", ("bwd_tok", True): "dc8c8c7100a014ac"}
 NCU_TRAFFIC_BYTES = {}
 for _k, _v in _GDN_T4096.items():
     NCU_TRAFFIC_BYTES[(_k, "gdn_b2_t4096_h16")] = (_v, _HASHES[(_k, False)])
