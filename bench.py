@@ -108,13 +108,14 @@ def job_throughput(units_per_rank: float, world: int, ms: float) -> float:
 
 def source_hash(kernel: str, per_channel: bool = False):
     """First 16 hex digits of the SHA-256 of the kernel's source file (the per-channel gate's
-    own file where it has one) and the headers every kernel includes (common.cuh, umma.cuh),
-    or None."""
+    own file where it has one) and the headers it includes (common.cuh, umma.cuh, and the
+    inverse's tri_inverse.cuh for the prepare kernels), or None."""
     name = (KERNEL_SOURCES_KDA if per_channel else KERNEL_SOURCES).get(kernel)
     if name is None:
         return None
     h = hashlib.sha256()
-    for part in (name, "common.cuh", "umma.cuh"):
+    parts = (name, "common.cuh", "umma.cuh") + (("tri_inverse.cuh",) if kernel == "prepare" else ())
+    for part in parts:
         try:
             with open(os.path.join(ROOT, "chunked_gated_delta_05_gb300", "csrc", part), "rb") as f:
                 h.update(f.read())

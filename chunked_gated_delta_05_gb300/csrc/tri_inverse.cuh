@@ -12,7 +12,8 @@ namespace gdn {
 // read one column of L as four broadcast float4 loads. Forward substitution by 16-row tiles:
 // y = -L[tile, :16b] X[:16b, c] (the pair's partial sums meet through one shuffle), then both
 // lanes solve the 16x16 diagonal block in registers (x_c = 1, x_r = 0 above the diagonal,
-// x_r = y_r - sum_j L[r][j] x_j below it) and each writes back eight of its rows.
+// x_r = y_r - sum_j L[r][j] x_j below it, applied row by row as each x_j is final) and each
+// writes back eight of its rows.
 __device__ __forceinline__ void unit_lower_inverse_column(const float* __restrict__ LT, float* sX, int c,
                                                           int part) {
   const int c0 = c & ~15;  // warp-uniform: X[j][c] = 0 for j < c is already in sX
@@ -42,18 +43,29 @@ __device__ __forceinline__ void unit_lower_inverse_column(const float* __restric
       }
 #pragma unroll
       for (int e = 0; e < 16; ++e) y[e] += __shfl_xor_sync(0xffffffffu, y[e], 16);
+      // the 16x16 diagonal block, right-looking: row j is final once the rows above it have
+      // been applied, and it then updates the rows below it from one line of L^T (the 16-byte
+      // chunks that hold those rows), so the dependent chain is one FMA per row
 #pragma unroll
-      for (int r = 0; r < 16; ++r) {
-        // two interleaved partial sums halve the dependent FMA chain of the 16x16 solve
-        float acc0 = y[r], acc1 = 0.f;
+      for (int e = 0; e < 16; ++e) x[e] = y[e];
 #pragma unroll
-        for (int j = 0; j < r; ++j) {
-          if (j & 1) acc1 = fmaf(-LT[(r0 + j) * kC + r0 + r], x[j], acc1);
-          else acc0 = fmaf(-LT[(r0 + j) * kC + r0 + r], x[j], acc0);
+      for (int j = 0; j < 16; ++j) {
+        const int R = r0 + j;
+        x[j] = (R < c) ? 0.f : ((R == c) ? 1.f : x[j]);
+        if (j < 15) {
+          const float4* l4 = reinterpret_cast<const float4*>(LT + (r0 + j) * kC + r0);
+          float l[16];
+#pragma unroll
+          for (int q = (j + 1) / 4; q < 4; ++q) {
+            const float4 v = l4[q];
+            l[4 * q] = v.x;
+            l[4 * q + 1] = v.y;
+            l[4 * q + 2] = v.z;
+            l[4 * q + 3] = v.w;
+          }
+#pragma unroll
+          for (int r = j + 1; r < 16; ++r) x[r] = fmaf(-l[r], x[j], x[r]);
         }
-        const float acc = acc0 + acc1;
-        const int R = r0 + r;
-        x[r] = (R < c) ? 0.f : ((R == c) ? 1.f : acc);
       }
     }
 #pragma unroll
