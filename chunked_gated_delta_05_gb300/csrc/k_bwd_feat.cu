@@ -51,7 +51,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                const __grid_constant__ CUtensorMap mDH, const BwdFeatParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = align1k(smem_raw);
-  __shared__ uint64_t bar_tma, bar_tma2, bar_mma;
+  __shared__ uint64_t bar_tma, bar_tma2, bar_mma, bar_mma3;
   __shared__ uint32_t tslot;
   __shared__ int abort_flag;
   __shared__ float s_red[8];
@@ -71,6 +71,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&bar_tma, 1);
     mbar_init(&bar_tma2, 1);
     mbar_init(&bar_mma, 1);
+    mbar_init(&bar_mma3, 1);
     fence_mbar_init();
     mbar_expect_tx(&bar_tma, 2u * 65536u + 32768u + 16384u);
     const int yh = int(tile) * kD;
@@ -138,17 +139,24 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
 
+  // [P1 | P2] (kTP2 = kTP1 + 64) = h [dO ; dv_new]^T from thread 0; P3 = dh' v_new^T from
+  // thread 32 once v_new has landed, with its own barrier, so that everything up to the second
+  // product group proceeds meanwhile
   if (tid == 0) {
     if (tma_ok) {
       tc_fence_after();
-      const uint32_t id64 = idesc_tf32(128, 64), id128 = idesc_tf32(128, 128);
-      const uint32_t sC = smem_u32(sm + kOffC), sVN = smem_u32(sm + kOffVN);
-      // [P1 | P2] (kTP2 = kTP1 + 64) = h [dO ; dv_new]^T, then P3 = dh' v_new^T
+      const uint32_t id128 = idesc_tf32(128, 128), sC = smem_u32(sm + kOffC);
       for (int s = 0; s < 16; ++s) mma_tf32_ts(tb + kTP1, tb + kTH + s * 8, desc_kmajor(sC, 16384, s), id128, s > 0);
+      mma_commit(&bar_mma);
+    }
+  } else if (tid == 32) {
+    if (tma_ok) {
+      tc_fence_after();
+      const uint32_t id64 = idesc_tf32(128, 64), sVN = smem_u32(sm + kOffVN);
       if (mbar_wait(&bar_tma2, 0, &abort_flag, p.status, kDevTimeoutTma)) {
         for (int s = 0; s < 16; ++s) mma_tf32_ts(tb + kTP3, tb + kTDH + s * 8, desc_kmajor(sVN, 8192, s), id64, s > 0);
       }
-      mma_commit(&bar_mma);
+      mma_commit(&bar_mma3);
     }
   }
   // A^T operand of the second product group, built while the first products run (A comes
@@ -177,11 +185,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     float* dq = p.dQt + tile * kTileW + size_t(t0) * kD + f;
 #pragma unroll
     for (int e = 0; e < 32; ++e) dq[size_t(e) * kD] = r[e];
-    tmem_ld32(tl + kTP3 + t0, r);
-    tmem_wait_ld_regs(r);
-    float* dk = p.dKt + tile * kTileW + size_t(t0) * kD + f;
-#pragma unroll
-    for (int e = 0; e < 32; ++e) dk[size_t(e) * kD] = r[e];
     // dW^T = -(h dv_new^T): saved token-major (tf32, an MMA operand later) and written back
     // to TMEM as the A operand of A^T dW.
     tmem_ld32(tl + kTP2 + t0, r);
@@ -193,8 +196,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       dw[size_t(e) * kD] = r[e];
     }
     tmem_st32(tl + kTP2 + t0, r);
-    // dv_new^T row f (lane f = value column f) as the A operand of A^T dv_new (reuses h's
-    // columns), read from the TMA copy of dv_new already in shared memory.
+    // dv_new^T row f (lane f = value column f) as the A operand of A^T dv_new (reuses the first
+    // 64 of h's columns), read from the TMA copy of dv_new already in shared memory.
 #pragma unroll
     for (int e = 0; e < 32; ++e)
       r[e] = to_tf32(*reinterpret_cast<const float*>(sm + kOffC + sw128_offset(kC + t0 + e, f, 2 * kC, 4)));
@@ -207,12 +210,25 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (tid == 0 && ok && !abort_flag) {
     const uint32_t id64 = idesc_tf32(128, 64);
     const uint32_t sAT = smem_u32(sm + kOffAT);
+    // A^T dv_new into h's last 64 columns (dh', P3's operand, may still be being read)
     for (int s = 0; s < 8; ++s) mma_tf32_ts(tb + kTP5, tb + kTP2 + s * 8, desc_kmajor(sAT, 8192, s), id64, s > 0);
-    for (int s = 0; s < 8; ++s) mma_tf32_ts(tb + kTDH, tb + kTH + s * 8, desc_kmajor(sAT, 8192, s), id64, s > 0);
+    for (int s = 0; s < 8; ++s) mma_tf32_ts(tb + kTH + 64, tb + kTH + s * 8, desc_kmajor(sAT, 8192, s), id64, s > 0);
     mma_commit(&bar_mma);
   }
   __syncwarp();
-  const bool ok2 = ok && mbar_wait(&bar_mma, 1, &abort_flag, p.status, kDevTimeoutMma);
+  // dKt = P3, token-major rows, while the second group runs
+  const bool ok3 = ok && mbar_wait(&bar_mma3, 0, &abort_flag, p.status, kDevTimeoutMma);
+  tc_fence_after();
+  if (ok3) {
+    const int t0 = 32 * hf;
+    float r[32];
+    tmem_ld32(tl + kTP3 + t0, r);
+    tmem_wait_ld_regs(r);
+    float* dk = p.dKt + tile * kTileW + size_t(t0) * kD + f;
+#pragma unroll
+    for (int e = 0; e < 32; ++e) dk[size_t(e) * kD] = r[e];
+  }
+  const bool ok2 = ok3 && mbar_wait(&bar_mma, 1, &abort_flag, p.status, kDevTimeoutMma);
   tc_fence_after();
   if (ok2) {
     const int t0 = 32 * hf;
@@ -222,7 +238,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     float* k1 = p.dK1 + tile * kTileW + size_t(t0) * kD + f;
 #pragma unroll
     for (int e = 0; e < 32; ++e) k1[size_t(e) * kD] = r[e];
-    tmem_ld32(tl + kTDH + t0, r);
+    tmem_ld32(tl + kTH + 64 + t0, r);
     tmem_wait_ld_regs(r);
     float* v1 = p.dV1 + tile * kTileW + size_t(t0) * kD + f;
 #pragma unroll
