@@ -142,6 +142,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tl = tb + tmem_lane_base(warp);
   const float Glast = s_G[len - 1];
   const bool tma_ok = mbar_wait(&bar_tma, 0, &abort_flag, p.status, kDevTimeoutTma);
+  // A full chunk has no rows to clear, so its exact Gram products K K^T and Q K^T (raw bf16
+  // tiles) go out now and run under the dO conversion; a ragged chunk issues them with dAqk.
+  const bool early_gram = len == kC;
+  if (tid == 0 && tma_ok && early_gram) {
+    tc_fence_after();
+    const uint32_t id_bf = idesc_bf16(64, 64), q0 = smem_u32(sQ), k0 = smem_u32(sK);
+    for (int s = 0; s < 8; ++s) mma_bf16_ss(tb + kTKK, desc_kmajor(k0, 8192, s), desc_kmajor(k0, 8192, s), id_bf, s > 0);
+    for (int s = 0; s < 8; ++s) mma_bf16_ss(tb + kTQK, desc_kmajor(q0, 8192, s), desc_kmajor(k0, 8192, s), id_bf, s > 0);
+  }
   // dO as a 64-row tf32 operand [i][v] (rows past the chunk are zero): thread row tid / 4,
   // 32 columns, eight per 16-byte read of the bf16 tile.
   {
@@ -189,9 +198,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t r1 = smem_u32(sm + kR1), r2 = smem_u32(sm + kR2);
     const uint32_t q0 = smem_u32(sQ), k0 = smem_u32(sK);
     for (int s = 0; s < 16; ++s) mma_tf32_ss(tb + kTAqk, desc_kmajor(r1, 8192, s), desc_kmajor(r2, 8192, s), id_tf, s > 0);
-    for (int s = 0; s < 8; ++s) mma_bf16_ss(tb + kTKK, desc_kmajor(k0, 8192, s), desc_kmajor(k0, 8192, s), id_bf, s > 0);
-    for (int s = 0; s < 8; ++s) mma_bf16_ss(tb + kTQK, desc_kmajor(q0, 8192, s), desc_kmajor(k0, 8192, s), id_bf, s > 0);
-    mma_commit(&bar_mma);
+    if (!early_gram) {
+      for (int s = 0; s < 8; ++s) mma_bf16_ss(tb + kTKK, desc_kmajor(k0, 8192, s), desc_kmajor(k0, 8192, s), id_bf, s > 0);
+      for (int s = 0; s < 8; ++s) mma_bf16_ss(tb + kTQK, desc_kmajor(q0, 8192, s), desc_kmajor(k0, 8192, s), id_bf, s > 0);
+    }
+    mma_commit(&bar_mma);  // covers the early Gram products too (same issuing thread)
   }
   __syncwarp();
   bool ok = tma_ok && mbar_wait(&bar_mma, 0, &abort_flag, p.status, kDevTimeoutMma);
