@@ -68,16 +68,16 @@ KERNEL_SOURCES_KDA = {**KERNEL_SOURCES, "prepare": "k_prep_kda.cu", "bwd_tok": "
 # each, all heads in one group). The chunk kernels' traffic is per chunk-head, so the
 # B=1 T=32768 H=16 entries are those bytes x 4 (8192 chunk-heads) and the B=1 T=8192 H=32 KDA
 # entries x 2 (4096); the chains' traffic depends on the segment plan and is not scaled.
-_GDN_T4096 = {"prepare": 615_954_176, "chain_fwd": 606_352_640, "compose": 29_380_864,
-              "chain_bwd": 581_913_856, "bwd_feat": 758_830_080, "bwd_tok": 731_342_336}
-_KDA_T4096 = {"prepare": 750_101_504, "chain_fwd": 603_353_344, "compose": 29_376_256,
-              "chain_bwd": 583_386_624, "bwd_feat": 758_095_872, "bwd_tok": 853_983_488}
-_HASHES = {("prepare", False): "ca3d562323200c74", ("prepare", True): "32d8cafd687463b6",
+_GDN_T4096 = {"prepare": 616_121_344, "chain_fwd": 606_150_912, "compose": 29_377_024,
+              "chain_bwd": 582_243_328, "bwd_feat": 758_571_264, "bwd_tok": 731_689_216}
+_KDA_T4096 = {"prepare": 749_943_808, "chain_fwd": 603_621_888, "compose": 29_377_024,
+              "chain_bwd": 583_095_296, "bwd_feat": 758_717_952, "bwd_tok": 853_997_824}
+_HASHES = {("prepare", False): "c2916e6291b1f3fb", ("prepare", True): "c98c767d621466d5",
            ("chain_fwd", False): "6ca5f5c74541d246", ("chain_fwd", True): "6ca5f5c74541d246",
            ("compose", False): "2a8e76a5313bc45a", ("compose", True): "2a8e76a5313bc45a",
            ("chain_bwd", False): "b22fa42ebd53fcf1", ("chain_bwd", True): "b22fa42ebd53fcf1",
-           ("bwd_feat", False): "21c2dbfccbb89130", ("bwd_feat", True): "21c2dbfccbb89130",
-           ("bwd_tok", False): "5e572442e06a4f09", ("bwd_tok", True): "dc8c8c7100a014ac"}
+           ("bwd_feat", False): "caaf82205acec3c6", ("bwd_feat", True): "caaf82205acec3c6",
+           ("bwd_tok", False): "fe3ae544e3105534", ("bwd_tok", True): "dc8c8c7100a014ac"}
 NCU_TRAFFIC_BYTES = {}
 for _k, _v in _GDN_T4096.items():
     NCU_TRAFFIC_BYTES[(_k, "gdn_b2_t4096_h16")] = (_v, _HASHES[(_k, False)])
