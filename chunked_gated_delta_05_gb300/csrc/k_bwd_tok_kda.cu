@@ -87,7 +87,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // per-token sums over the channels: the pair sums' share of dbeta, one partial per group of
   // 32 channels (warp % 4), added in a fixed order so that the result does not depend on warp
   // scheduling; the assembly's sums (one warp reduction per token row)
-  __shared__ float s_dba[1][kC], s_dotq[1][kC], s_dotk[1][kC];
+  __shared__ float s_dba[1][kC];
   __shared__ __align__(16) float s_glw[kThreads / 32][kD];  // each warp's dG_last shares
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -476,9 +476,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
   __syncthreads();
-  // ---- per-token assembly: each warp takes whole token rows, lane l channels 4l .. 4l+3.
-  // The row sums over the channels (dbeta, q^ . dq^, k^ . dk^) are one warp reduction each,
-  // in a fixed order; each channel's share of dG_last is summed over the warps below.
+  // ---- per-token assembly and L2-norm backward: each warp takes whole token rows, lane l
+  // channels 4l .. 4l+3. The row sums over the channels (dbeta, q^ . dq^, k^ . dk^) are one
+  // warp reduction each, in a fixed order, and every lane holds them after it, so the row's dq
+  // and dk follow at once; each channel's share of dG_last is summed over the warps below.
   const float glc = sG2[(len - 1) * kP + cc];
   {
     const int c4 = 4 * lane;
@@ -499,10 +500,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       bf16x4_at(sK, t, c4, kv);
       bf16x4_at(sV, t, c4, vv);
       const float rq = s_rq[t], rk = s_rk[t], bt = s_b[t];
-      float4* qa4 = reinterpret_cast<float4*>(sQacc + t * kD + c4);
-      float4* ka4 = reinterpret_cast<float4*>(sKacc + t * kD + c4);
+      const float4 qa = *reinterpret_cast<const float4*>(sQacc + t * kD + c4);
+      const float4 ka = *reinterpret_cast<const float4*>(sKacc + t * kD + c4);
       float4* ga4 = reinterpret_cast<float4*>(sGacc + t * kD + c4);
-      const float4 qa = *qa4, ka = *ka4, ga = *ga4;
+      const float4 ga = *ga4;
       float qacc[4] = {qa.x, qa.y, qa.z, qa.w}, kacc[4] = {ka.x, ka.y, ka.z, ka.w}, gacc[4] = {ga.x, ga.y, ga.z, ga.w};
       const float4 kx = *reinterpret_cast<const float4*>(sKX + t * kD + c4);
       float sdb = (kx.x + kx.y) + (kx.z + kx.w), sq = 0.f, sk = 0.f, dvo[4];
@@ -522,8 +523,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         sq += dqh * qh;
         sk += dkh * kh;
       }
-      *qa4 = make_float4(qacc[0], qacc[1], qacc[2], qacc[3]);
-      *ka4 = make_float4(kacc[0], kacc[1], kacc[2], kacc[3]);
       *ga4 = make_float4(gacc[0], gacc[1], gacc[2], gacc[3]);
       *reinterpret_cast<uint2*>(p.dv + (size_t(ch.x + t) * H + h) * kD + c4) = pack_bf16x4(dvo);
 #pragma unroll
@@ -532,46 +531,27 @@ __global__ void __launch_bounds__(kThreads, 1)
         sq += __shfl_xor_sync(0xffffffffu, sq, off);
         sk += __shfl_xor_sync(0xffffffffu, sk, off);
       }
-      if (lane == 0) {
-        s_dba[0][t] = sdb;
-        s_dotq[0][t] = sq;
-        s_dotk[0][t] = sk;
+      if (lane == 0) s_dba[0][t] = sdb;
+      float dq[4], dk[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        dq[e] = p.l2norm ? rq * (qacc[e] - rq * qv[e] * sq) : qacc[e];
+        dk[e] = p.l2norm ? rk * (kacc[e] - rk * kv[e] * sk) : kacc[e];
+      }
+      if (p.dq32) {  // per value head, summed over the q/k group later
+        const size_t oq = (size_t(ch.x + t) * H + h) * kD + c4;
+        *reinterpret_cast<float4*>(p.dq32 + oq) = make_float4(dq[0], dq[1], dq[2], dq[3]);
+        *reinterpret_cast<float4*>(p.dk32 + oq) = make_float4(dk[0], dk[1], dk[2], dk[3]);
+      } else {
+        const size_t oq = (size_t(ch.x + t) * (H / p.qk_group) + h) * kD + c4;
+        *reinterpret_cast<uint2*>(p.dq + oq) = pack_bf16x4(dq);
+        *reinterpret_cast<uint2*>(p.dk + oq) = pack_bf16x4(dk);
       }
     }
 #pragma unroll
     for (int e = 0; e < 4; ++e) s_glw[warp][c4 + e] = glp[e];
   }
   __syncthreads();
-  // ---- L2-norm backward and writes: each warp takes whole token rows, lane l channels
-  // 4l .. 4l+3 (16-byte reads of the accumulators, 8-byte reads of q and k, vector stores)
-  {
-    const int c4 = 4 * lane;
-    for (int t = warp; t < len; t += kThreads / 32) {
-      const float rq = s_rq[t], rk = s_rk[t];
-      const float dotq = s_dotq[0][t], dotk = s_dotk[0][t];
-      float qv[4], kv[4];
-      bf16x4_at(sQ, t, c4, qv);
-      bf16x4_at(sK, t, c4, kv);
-      const float4 qa = *reinterpret_cast<const float4*>(sQacc + t * kD + c4);
-      const float4 ka = *reinterpret_cast<const float4*>(sKacc + t * kD + c4);
-      const float qac[4] = {qa.x, qa.y, qa.z, qa.w}, kac[4] = {ka.x, ka.y, ka.z, ka.w};
-      float dq[4], dk[4];
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        dq[e] = p.l2norm ? rq * (qac[e] - rq * qv[e] * dotq) : qac[e];
-        dk[e] = p.l2norm ? rk * (kac[e] - rk * kv[e] * dotk) : kac[e];
-      }
-      if (p.dq32) {  // per value head, summed over the q/k group later
-        const size_t o = (size_t(ch.x + t) * H + h) * kD + c4;
-        *reinterpret_cast<float4*>(p.dq32 + o) = make_float4(dq[0], dq[1], dq[2], dq[3]);
-        *reinterpret_cast<float4*>(p.dk32 + o) = make_float4(dk[0], dk[1], dk[2], dk[3]);
-      } else {
-        const size_t o = (size_t(ch.x + t) * (H / p.qk_group) + h) * kD + c4;
-        *reinterpret_cast<uint2*>(p.dq + o) = pack_bf16x4(dq);
-        *reinterpret_cast<uint2*>(p.dk + o) = pack_bf16x4(dk);
-      }
-    }
-  }
   // ---- dg by reverse cumulative sum per channel
   if (half == 0) {
     float acc = exp2f(glc) * dgam_c;
