@@ -70,14 +70,14 @@ KERNEL_SOURCES_KDA = {**KERNEL_SOURCES, "prepare": "k_prep_kda.cu", "bwd_tok": "
 # entries x 2 (4096); the chains' traffic depends on the segment plan and is not scaled.
 _GDN_T4096 = {"prepare": 616_121_344, "chain_fwd": 606_150_912, "compose": 29_377_024,
               "chain_bwd": 582_243_328, "bwd_feat": 758_571_264, "bwd_tok": 731_689_216}
-_KDA_T4096 = {"prepare": 749_943_808, "chain_fwd": 603_621_888, "compose": 29_377_024,
-              "chain_bwd": 583_095_296, "bwd_feat": 758_717_952, "bwd_tok": 853_997_824}
+_KDA_T4096 = {"prepare": 749_775_616, "chain_fwd": 604_277_504, "compose": 29_376_768,
+              "chain_bwd": 583_158_784, "bwd_feat": 757_906_176, "bwd_tok": 856_912_128}
 _HASHES = {("prepare", False): "c2916e6291b1f3fb", ("prepare", True): "c98c767d621466d5",
            ("chain_fwd", False): "6ca5f5c74541d246", ("chain_fwd", True): "6ca5f5c74541d246",
            ("compose", False): "2a8e76a5313bc45a", ("compose", True): "2a8e76a5313bc45a",
            ("chain_bwd", False): "b22fa42ebd53fcf1", ("chain_bwd", True): "b22fa42ebd53fcf1",
            ("bwd_feat", False): "caaf82205acec3c6", ("bwd_feat", True): "caaf82205acec3c6",
-           ("bwd_tok", False): "fe3ae544e3105534", ("bwd_tok", True): "dc8c8c7100a014ac"}
+           ("bwd_tok", False): "fe3ae544e3105534", ("bwd_tok", True): "ab1c2cd9cbc8111f"}
 NCU_TRAFFIC_BYTES = {}
 for _k, _v in _GDN_T4096.items():
     NCU_TRAFFIC_BYTES[(_k, "gdn_b2_t4096_h16")] = (_v, _HASHES[(_k, False)])
