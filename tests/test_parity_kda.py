@@ -79,3 +79,26 @@ def test_kda_bwd_strong_gates():
     # decays of up to several units per token: the pair sums' block factorisation must stay finite
     check_bwd(synth.custom(1, 192, 2, per_channel=True, beta_logits=True, h0_std=0.02, dht_std=0.01,
                            seed=52, g_scale=2.0))
+
+
+def test_kda_bwd_saved_equals_recompute_and_repeats():
+    """The backward on the forward's saved tiles equals the recomputing backward bit for bit, and
+    a second call returns the same bits: the per-channel kernels reduce in a fixed order (the
+    tensor-core pair sums included), so nothing depends on scheduling."""
+    from chunked_gated_delta_05_gb300 import kda_bwd
+    lens = [130, 7, 300, 64]
+    d = synth.custom(1, sum(lens), 4, per_channel=True, beta_logits=True, h0_std=0.02, dht_std=0.01,
+                     lengths=lens, seed=53)
+    dc = to_cuda(d)
+    kw = dict(initial_state=dc["h0"], cu_seqlens=d["cu_seqlens"])
+    o, hT, saved = kda_fwd(dc["q"], dc["k"], dc["v"], dc["g"], dc["beta"], output_final_state=True,
+                           save=True, **kw)
+    runs = [kda_bwd(dc["q"], dc["k"], dc["v"], dc["g"], dc["beta"], dc["dO"], dht=dc["dht"], saved=saved, **kw),
+            kda_bwd(dc["q"], dc["k"], dc["v"], dc["g"], dc["beta"], dc["dO"], dht=dc["dht"], saved=saved, **kw),
+            kda_bwd(dc["q"], dc["k"], dc["v"], dc["g"], dc["beta"], dc["dO"], dht=dc["dht"], **kw)]
+    torch.cuda.synchronize()
+    for other in runs[1:]:
+        for a, b in zip(runs[0], other):
+            assert (a is None) == (b is None)
+            if a is not None:
+                assert torch.equal(a, b)
