@@ -291,13 +291,21 @@ class Runner:
         self.tokens = w.B * w.T
         self.head_groups = 0  # the library's setting for the timed steps (0: automatic)
 
+    # inputs that only the backward reads (the end-to-end region copies them behind the rest)
+    BWD_ONLY_INPUTS = ("dO", "dht")
+
+    def forward(self, inp):
+        # training forward: saves its chunk intermediates for the backward
+        return self.fwd_fn(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"], initial_state=inp["h0"],
+                           output_final_state=True, status=self.status, save=True, **self.kw)
+
+    def backward(self, inp, saved):
+        return tuple(self.bwd_fn(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"], inp["dO"], dht=inp["dht"],
+                                 initial_state=inp["h0"], status=self.status, saved=saved, **self.kw))
+
     def step(self, inp):
-        # training step: the forward saves its chunk intermediates, the backward consumes them
-        o, hT, saved = self.fwd_fn(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"], initial_state=inp["h0"],
-                                   output_final_state=True, status=self.status, save=True, **self.kw)
-        grads = self.bwd_fn(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"], inp["dO"], dht=inp["dht"],
-                            initial_state=inp["h0"], status=self.status, saved=saved, **self.kw)
-        return (o, hT) + tuple(grads)
+        o, hT, saved = self.forward(inp)
+        return (o, hT) + self.backward(inp, saved)
 
     def check_status(self, where):
         if int(self.status.item()) != 0:
@@ -357,8 +365,11 @@ class Runner:
         """End to end through the public API with host buffers (pinned), every copy inside the
         timed region: step i's inputs go host -> device on a copy stream while step i-1 computes,
         and step i's outputs (every gradient, o and the final state) go device -> host on a second
-        copy stream while step i+1 computes. Two input slots; a slot is refilled only after the
-        step that read it has finished. No copy starts before the region's first event."""
+        copy stream while step i+1 computes. Each step's forward waits only for the inputs it
+        reads; dO and dht, which only the backward reads, are copied behind them and waited for
+        before the backward. o and the final state leave as soon as the forward has written them.
+        Two input slots; a slot is refilled only after the step that read it has finished. No copy
+        starts before the region's first event."""
         torch, dev, stream = self.torch, self.dev, self.stream
         host = self.host
         pinned_in = {k: (v.pin_memory() if isinstance(v, torch.Tensor) else v) for k, v in host.items()}
@@ -381,28 +392,39 @@ class Runner:
             s_in.wait_event(start)
             s_out.wait_event(start)
             last_out = None
-            for i in range(n):
-                sl = i % 2
-                with torch.cuda.stream(s_in):
-                    s_in.wait_event(slot_free[sl])
-                    for k, v in pinned_in.items():
-                        if isinstance(v, torch.Tensor):
-                            slots[sl][k].copy_(v, non_blocking=True)
-                    loaded = torch.cuda.Event()
-                    loaded.record(s_in)
-                stream.wait_event(loaded)
-                outs = self.step(slots[sl])
-                done = torch.cuda.Event()
-                done.record(stream)
-                slot_free[sl] = done
+            def copy_out(ev, srcs, dsts):
                 with torch.cuda.stream(s_out):
-                    s_out.wait_event(done)
-                    for src, dst in zip(outs, pinned_out[sl]):
+                    s_out.wait_event(ev)
+                    for src, dst in zip(srcs, dsts):
                         if src is not None:
                             src.record_stream(s_out)
                             dst.copy_(src, non_blocking=True)
-                    last_out = torch.cuda.Event()
-                    last_out.record(s_out)
+                    e = torch.cuda.Event()
+                    e.record(s_out)
+                return e
+
+            for i in range(n):
+                sl = i % 2
+                loaded = []
+                with torch.cuda.stream(s_in):
+                    s_in.wait_event(slot_free[sl])
+                    for part in (False, True):   # the forward's inputs, then the backward's own
+                        for k, v in pinned_in.items():
+                            if isinstance(v, torch.Tensor) and (k in self.BWD_ONLY_INPUTS) == part:
+                                slots[sl][k].copy_(v, non_blocking=True)
+                        loaded.append(torch.cuda.Event())
+                        loaded[-1].record(s_in)
+                stream.wait_event(loaded[0])
+                o, hT, saved = self.forward(slots[sl])
+                fwd_done = torch.cuda.Event()
+                fwd_done.record(stream)
+                copy_out(fwd_done, (o, hT), pinned_out[sl][:2])
+                stream.wait_event(loaded[1])
+                grads = self.backward(slots[sl], saved)
+                done = torch.cuda.Event()
+                done.record(stream)
+                slot_free[sl] = done
+                last_out = copy_out(done, grads, pinned_out[sl][2:])
             stream.wait_event(last_out)   # the region ends after the last result is on the host
 
         run(2)
