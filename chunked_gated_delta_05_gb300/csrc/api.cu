@@ -227,7 +227,7 @@ Layout make_layout(const Problem& P, bool backward, bool kda = false) {
     L.rq = take(4 * tiles * kC);
     L.rk = take(4 * tiles * kC);
     L.beff = take(4 * tiles * kC);
-    L.hs = take(4 * tiles * kD * kD);
+    L.hs = take(2 * tiles * kD * kD);   // bf16
     L.vns = take(4 * tiles * kTileW);
   }
   L.plan = plan_scan(P);
@@ -238,7 +238,7 @@ Layout make_layout(const Problem& P, bool backward, bool kda = false) {
   L.saved_total = off;
   off = 0;
   if (backward) {
-    L.dhs = take(4 * tiles * kD * kD);
+    L.dhs = take(2 * tiles * kD * kD);  // bf16
     L.dvns = take(4 * tiles * kTileW);
     L.dQt = take(4 * tiles * kTileW);
     L.dKt = take(4 * tiles * kTileW);
@@ -328,13 +328,19 @@ struct TimedLaunch {
 struct Maps {
   CUtensorMap q, k, v, W, Qt, KtT, Aqk, U, Usw;      // forward (Usw: U as a swizzled store target)
   CUtensorMap Kt, AqkT, QtT, WT, VN, DVN, DW, dO;     // backward
-  CUtensorMap Hs, DHs;                               // saved states h, dh' [tile][128][128] (128-row boxes)
+  CUtensorMap Hs, DHs;                               // saved states h, dh' [tile][128][128] bf16 (128-row boxes)
 };
 
 // Row-major fp32 workspace tiles as TMA sources: `cols` per row, boxes of 32 columns.
 bool tile_map(CUtensorMap* m, const char* base, uint64_t cols, uint64_t rows, uint32_t box_rows, bool swz) {
   return make_map(m, base, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, cols, rows, cols * 4, 32, box_rows,
                   swz ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE);
+}
+
+// The bf16 state saves h, dh' [tile][128][128] as TMA sources: 128-row boxes of 64 columns
+// (128 bytes, one 128-byte swizzle panel).
+bool state_map(CUtensorMap* m, const char* base, uint64_t rows) {
+  return make_map(m, base, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, kD, rows, kD * 2, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
 // Whether the layout carries the backward-mode prepare tiles.
@@ -357,8 +363,7 @@ bool bwd_maps(const Problem& P, const char* sv, const char* rs, const Layout& L,
   return tile_map(&M->Kt, sv + L.Kt, kD, r64, 64, true) && tile_map(&M->AqkT, sv + L.AqkT, kC, r64, 64, true) &&
          tile_map(&M->QtT, sv + L.QtT, kC, r128, 128, true) && tile_map(&M->WT, sv + L.WT, kC, r128, 128, true) &&
          tile_map(&M->VN, sv + L.vns, kD, r64, 64, true) && tile_map(&M->DVN, rs + L.dvns, kD, r64, 64, true) &&
-         tile_map(&M->DW, rs + L.dW, kD, r64, 64, true) && tile_map(&M->Hs, sv + L.hs, kD, r128, 128, true) &&
-         tile_map(&M->DHs, rs + L.dhs, kD, r128, 128, true);
+         tile_map(&M->DW, rs + L.dW, kD, r64, 64, true) && state_map(&M->Hs, sv + L.hs, r128) && state_map(&M->DHs, rs + L.dhs, r128);
 }
 
 // Prepare-kernel parameters for a buffer carved by make_layout at `sv` (backward-mode outputs
@@ -595,7 +600,7 @@ int run_fwd(const gdn_desc_t* d, const gdn_fwd_args_t* a, void* stream, bool kda
   cp.hT = d->output_final_state ? a->final_state : nullptr;
   cp.o = static_cast<__nv_bfloat16*>(a->o);
   if (training) {
-    cp.h_save = reinterpret_cast<float*>(ws + L.hs);
+    cp.h_save = reinterpret_cast<__nv_bfloat16*>(ws + L.hs);
     cp.vnew_save = reinterpret_cast<float*>(ws + L.vns);
   }
   cp.status = a->status;
@@ -682,7 +687,7 @@ int run_bwd(const gdn_desc_t* d, const gdn_bwd_args_t* a, void* stream, bool kda
     cp.H = P.H;
     cp.gam = F(L.gam);
     cp.h0 = a->initial_state;
-    cp.h_save = F(L.hs);
+    cp.h_save = reinterpret_cast<__nv_bfloat16*>(sv + L.hs);
     cp.vnew_save = F(L.vns);
     cp.status = a->status;
     cp.sp = seg_plan(L.plan, sv, L.fE, L.fPhi, L.fB);
@@ -698,7 +703,7 @@ int run_bwd(const gdn_desc_t* d, const gdn_bwd_args_t* a, void* stream, bool kda
   rp.dO = static_cast<const __nv_bfloat16*>(a->dO);
   rp.dht = a->dht;
   rp.dh0 = a->dh0;
-  rp.dh_save = R(L.dhs);
+  rp.dh_save = reinterpret_cast<__nv_bfloat16*>(rs + L.dhs);
   rp.dvn_save = R(L.dvns);
   rp.status = a->status;
   rp.sp = seg_plan(L.plan, rs, L.rE, L.rPhi, L.rB);
@@ -709,8 +714,8 @@ int run_bwd(const gdn_desc_t* d, const gdn_bwd_args_t* a, void* stream, bool kda
   fp.dense_T = P.packed ? 0 : P.T;
   fp.H = P.H;
   fp.kda = kda ? 1 : 0;
-  fp.h = F(L.hs);
-  fp.dh = R(L.dhs);
+  fp.h = reinterpret_cast<const __nv_bfloat16*>(sv + L.hs);
+  fp.dh = reinterpret_cast<const __nv_bfloat16*>(rs + L.dhs);
   fp.dO = rp.dO;
   fp.A = F(L.A);
   fp.dvn = R(L.dvns);

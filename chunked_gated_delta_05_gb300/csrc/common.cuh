@@ -54,6 +54,22 @@ constexpr size_t kTileW = size_t(kC) * kD;
 constexpr size_t kTileKtT = size_t(kD) * kC;
 constexpr size_t kTileAqk = size_t(kC) * kC;
 
+// Writes a thread's 64 fp32 values s[e] as bf16 into column v, rows 0..63, of a row-major
+// [rows][kD] bf16 tile at `base` (the state saves of the chain kernels, where lane v holds column
+// v). Lanes v and v ^ 1 (same warp, same rows) swap one value per row pair, so each store writes
+// two adjacent columns: the even lane the even rows, the odd lane the odd rows. Every lane of the
+// warp must take part.
+__device__ __forceinline__ void store_col64_bf16(__nv_bfloat16* base, const float* s, int v) {
+  const int odd = v & 1;
+  __nv_bfloat162* p = reinterpret_cast<__nv_bfloat162*>(base + (v & ~1));
+#pragma unroll
+  for (int e = 0; e < 64; e += 2) {
+    const float other = __shfl_xor_sync(0xffffffffu, odd ? s[e] : s[e + 1], 1);
+    const __nv_bfloat162 pr = odd ? __floats2bfloat162_rn(other, s[e + 1]) : __floats2bfloat162_rn(s[e], other);
+    p[size_t(e + odd) * (kD / 2)] = pr;
+  }
+}
+
 // Segmented chain (chunk-parallel affine state scan). The chunk map of the chain is affine
 // in the state, S_out = M_c S_in + B_c with M_c = diag(gam) - k~^T W and B_c = k~^T U
 // (the affine state summary of the pages' context-parallel GDN path, composed over chunks);
@@ -137,7 +153,7 @@ struct RevChainParams {
   const __nv_bfloat16* dO;     // [R,H,V]
   const float* dht;            // [N,H,K,V] or null
   float* dh0;                  // [N,H,K,V] or null
-  float* dh_save;              // [NC,H,K,V] gradient w.r.t. the state leaving each chunk
+  __nv_bfloat16* dh_save;      // [NC,H,K,V] gradient w.r.t. the state leaving each chunk (bf16)
   float* dvn_save;             // [NC,H,64,V] gradient w.r.t. v_new
   int* status;
 };
@@ -153,7 +169,7 @@ struct ChainParams {
   const float* h0;             // [N,H,K,V] or null
   float* hT;                   // [N,H,K,V] or null
   __nv_bfloat16* o;            // [R,H,V] or null
-  float* h_save;               // [NC,H,K,V] entry state of every chunk, or null
+  __nv_bfloat16* h_save;       // [NC,H,K,V] entry state of every chunk (bf16), or null
   float* vnew_save;            // [NC,H,64,V] or null
   int* status;
 };
@@ -176,8 +192,8 @@ struct BwdFeatParams {
   int NC, H, kda;
   int dense_T;                 // tokens per sequence of a dense batch (chunk entries computed), 0 if packed
   int hg0, hgn;                // head group: heads hg0 .. hg0 + hgn - 1 (grid.y = hgn)
-  const float* h;              // [NC,H,K,V] state entering each chunk
-  const float* dh;             // [NC,H,K,V] gradient w.r.t. the state leaving each chunk
+  const __nv_bfloat16* h;      // [NC,H,K,V] state entering each chunk (bf16; read by TMA)
+  const __nv_bfloat16* dh;     // [NC,H,K,V] gradient w.r.t. the state leaving each chunk (bf16; read by TMA)
   const __nv_bfloat16* dO;     // [R,H,V]
   const float* A;              // [NC,H,64,64]
   const float* dvn;            // [NC,H,64,V]

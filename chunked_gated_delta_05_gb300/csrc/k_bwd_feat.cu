@@ -12,10 +12,11 @@
 //   dgam = sum over v of h (.) dh'   (per key row; summed over keys for the scalar gate)
 // GB300 mapping: one CTA per chunk and head, 256 threads; threads f and f + 128 own feature f
 // (= TMEM lane f) and split its columns in halves. h and dh' rows are loaded by their lane
-// owners and stored to TMEM (tf32) as A operands of kind::tf32 MMAs; dO^T, v_new, dv_new and A^T
-// are SW128 K-major B operands in shared memory (v_new, dv_new by TMA). h and dh' arrive by
-// TMA too (128-row boxes, 128-byte swizzle), so each thread reads its row from shared memory
-// without bank conflicts. Results leave as token-major fp32 rows [t][f] (coalesced: the 128
+// owners and stored to TMEM as A operands of kind::tf32 MMAs (the chains save both in bf16, so
+// the widened values are exact tf32 operands); dO^T, v_new, dv_new and A^T are SW128 K-major B
+// operands in shared memory (v_new, dv_new by TMA). h and dh' arrive by TMA too (128-row boxes
+// of 64 bf16 columns, 128-byte swizzle: a thread's column half is one panel row), so each
+// thread reads its row from shared memory without bank conflicts. Results leave as token-major fp32 rows [t][f] (coalesced: the 128
 // threads of one token row write 512 contiguous bytes).
 // (An L2 prefetch of the next wave's inputs made the whole step slower: with the heads split
 // over two streams it competes with the other group's kernels.)
@@ -31,11 +32,12 @@ constexpr int kThreads = 256;
 // (converted from the bf16 tile), rows 64-127 dv_new (TMA), so h dO^T and h dv_new^T are one
 // N = 128 product.
 constexpr uint32_t kOffC = 0;
-constexpr uint32_t kOffVN = 65536;    // v_new [t][v] (TMA), 4 panels x 64 rows; first dh' panels 2-3
+constexpr uint32_t kOffVN = 65536;    // v_new [t][v] (TMA), 4 panels x 64 rows
 constexpr uint32_t kOffAT = 98304;    // A^T  [j][i] tf32, 2 panels x 64 rows (16 KB)
 constexpr uint32_t kOffDO16 = 114688; // dO   [t][v] bf16 (TMA), 2 panels x 64 rows (16 KB)
-constexpr uint32_t kOffHS = 131072;   // h [f][v], 4 panels x 128 rows (64 KB), then dh' panels 0-1
-constexpr uint32_t kSmemBytes = kOffHS + 98304 + 1024;
+constexpr uint32_t kOffHS = 131072;   // h [f][v] bf16, 2 panels x 128 rows (32 KB)
+constexpr uint32_t kOffDH = kOffHS + 32768;  // dh' [f][v] bf16, 2 panels x 128 rows (32 KB)
+constexpr uint32_t kSmemBytes = kOffDH + 32768 + 1024;
 constexpr uint32_t kTH = 0, kTDH = 128, kTP1 = 256, kTP2 = 320, kTP3 = 384, kTP5 = 448;
 static_assert(kTP2 == kTP1 + 64, "h [dO ; dv_new]^T lands in P1 | P2");
 
@@ -66,21 +68,23 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0) tmem_alloc(&tslot, 512);
   if (tid == 0) {
     // the barriers are this thread's alone until the block barrier below: start the loads now.
-    // First group: h, dh' (dh' panels 2-3 sit in the v_new region until consumed), dv_new, dO.
+    // First group: h, dh', dv_new, dO; v_new (read by the third product only) on its own barrier.
     abort_flag = 0;
     mbar_init(&bar_tma, 1);
     mbar_init(&bar_tma2, 1);
     mbar_init(&bar_mma, 1);
     mbar_init(&bar_mma3, 1);
     fence_mbar_init();
-    mbar_expect_tx(&bar_tma, 2u * 65536u + 32768u + 16384u);
+    mbar_expect_tx(&bar_tma, 2u * 32768u + 32768u + 16384u);
     const int yh = int(tile) * kD;
-    for (int pp = 0; pp < 4; ++pp) {
-      tma_load_2d(sm + kOffHS + pp * 16384, &mH, pp * 32, yh, &bar_tma);
-      tma_load_2d(sm + (pp < 2 ? kOffHS + 65536 + pp * 16384 : kOffVN + (pp - 2) * 16384), &mDH, pp * 32, yh, &bar_tma);
-      tma_load_2d(sm + kOffC + pp * 16384 + 8192, &mDVN, pp * 32, int(tile) * kC, &bar_tma);
+    for (int pp = 0; pp < 2; ++pp) {
+      tma_load_2d(sm + kOffHS + pp * 16384, &mH, pp * 64, yh, &bar_tma);
+      tma_load_2d(sm + kOffDH + pp * 16384, &mDH, pp * 64, yh, &bar_tma);
     }
+    for (int pp = 0; pp < 4; ++pp) tma_load_2d(sm + kOffC + pp * 16384 + 8192, &mDVN, pp * 32, int(tile) * kC, &bar_tma);
     for (int pp = 0; pp < 2; ++pp) tma_load_2d(sm + kOffDO16 + pp * 8192, &mdO, h * kD + 64 * pp, ch.x, &bar_tma);
+    mbar_expect_tx(&bar_tma2, 32768u);
+    for (int pp = 0; pp < 4; ++pp) tma_load_2d(sm + kOffVN + pp * 8192, &mVN, pp * 32, int(tile) * kC, &bar_tma2);
     prefetch_l2(p.A + tile * kTileAqk, 4u * kTileAqk);  // read after the first products are issued
   }
   tc_fence_before();
@@ -88,39 +92,38 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tb = tslot;
   const uint32_t tl = tb + tmem_lane_base(warp);
-  // Half hf of the h and dh' rows f (shared memory -> TMEM as tf32 A operands); dgam partial
-  // sums in fp32. The rows are already tf32 values (the chains save their tf32 copies).
+  // Half hf of the h and dh' rows f (panel hf of each: shared memory -> TMEM as tf32 A
+  // operands, widened exactly from bf16); dgam partial sums in fp32.
   const bool tma_ok = mbar_wait(&bar_tma, 0, &abort_flag, p.status, kDevTimeoutTma);
   float dg = 0.f;
   if (tma_ok) {
-    const uint8_t* dsrc = hf ? sm + kOffVN : sm + kOffHS + 65536;
+    const uint8_t* hrow = sm + kOffHS + hf * 16384;
+    const uint8_t* drow = sm + kOffDH + hf * 16384;
 #pragma unroll
     for (int q = 0; q < 2; ++q) {
       float a[32], b[32];
 #pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        const int col = 64 * hf + 32 * q + 4 * e;
-        const float4 x = *reinterpret_cast<const float4*>(sm + kOffHS + sw128_offset(f, col, 128, 4));
-        const float4 y = *reinterpret_cast<const float4*>(dsrc + sw128_offset(f, col - 64 * hf, 128, 4));
-        const float xs[4] = {x.x, x.y, x.z, x.w}, ys[4] = {y.x, y.y, y.z, y.w};
+      for (int e = 0; e < 4; ++e) {
+        const int col = 32 * q + 8 * e;
+        const uint4 x = *reinterpret_cast<const uint4*>(hrow + sw128_offset(f, col, 128, 2));
+        const uint4 y = *reinterpret_cast<const uint4*>(drow + sw128_offset(f, col, 128, 2));
+        const uint32_t xs[4] = {x.x, x.y, x.z, x.w}, ys[4] = {y.x, y.y, y.z, y.w};
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
-          dg = fmaf(xs[u], ys[u], dg);
-          a[4 * e + u] = xs[u];
-          b[4 * e + u] = ys[u];
+          // two bf16 per word, the lower column in the low half
+          const float x0 = __uint_as_float(xs[u] << 16), x1 = __uint_as_float(xs[u] & 0xffff0000u);
+          const float y0 = __uint_as_float(ys[u] << 16), y1 = __uint_as_float(ys[u] & 0xffff0000u);
+          dg = fmaf(x0, y0, dg);
+          dg = fmaf(x1, y1, dg);
+          a[8 * e + 2 * u] = x0;
+          a[8 * e + 2 * u + 1] = x1;
+          b[8 * e + 2 * u] = y0;
+          b[8 * e + 2 * u + 1] = y1;
         }
       }
       tmem_st32(tl + kTH + 64 * hf + 32 * q, a);
       tmem_st32(tl + kTDH + 64 * hf + 32 * q, b);
     }
-  }
-  // the v_new region is free once every thread has read its dh' rows: load v_new there
-  fence_async_smem();
-  __syncthreads();
-  if (tid == 0 && tma_ok) {
-    mbar_expect_tx(&bar_tma2, 32768u);
-    for (int pp = 0; pp < 4; ++pp)
-      tma_load_2d(sm + kOffVN + pp * 8192, &mVN, pp * 32, int(tile) * kC, &bar_tma2);
   }
   // dO^T operand: element (t, v=f) of the K-major [t][v] tile from the bf16 TMA tile (half hf
   // of the tokens); rows past the chunk (the next document's, or out of range) are zero.
@@ -150,12 +153,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       mma_commit(&bar_mma);
     }
   } else if (tid == 32) {
+    // v_new was requested at the start: its copy lands before the CTA can exit, also when
+    // aborting
+    const bool vn_ok = mbar_wait(&bar_tma2, 0, &abort_flag, p.status, kDevTimeoutTma) || mbar_drain(&bar_tma2, 0);
     if (tma_ok) {
       tc_fence_after();
       const uint32_t id64 = idesc_tf32(128, 64), sVN = smem_u32(sm + kOffVN);
-      if (mbar_wait(&bar_tma2, 0, &abort_flag, p.status, kDevTimeoutTma)) {
+      if (vn_ok && !abort_flag)
         for (int s = 0; s < 16; ++s) mma_tf32_ts(tb + kTP3, tb + kTDH + s * 8, desc_kmajor(sVN, 8192, s), id64, s > 0);
-      }
       mma_commit(&bar_mma3);
     }
   }

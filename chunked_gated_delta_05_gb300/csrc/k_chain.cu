@@ -18,7 +18,7 @@
 //   v_new^T = U^T - P        (written over P in TMEM)
 //   S'^T   += v_new^T KtT^T                                -- on the serial chain
 //   O      += v_new^T Aqk^T                                -- off the chain, issued after
-// The decay (and the backward's copy of the entry state, taken from the same registers)
+// The decay (and the backward's bf16 copy of the entry state, taken from the same registers)
 // overlaps the product. The issuing thread starts the next chunk's product as soon as the
 // state update completes. P/v_new and O are double-buffered in TMEM by chunk parity; a chunk's
 // output is read out while the next chunk's state update runs, and the product two chunks on
@@ -59,36 +59,25 @@ __device__ __forceinline__ uint8_t* align1k(uint8_t* p) {
 // The state entering chunk j (buffer ts(j); this thread: lane v, state columns [k0, k0+64))
 // times chunk c's end decay gam, into buffer ts(j+1), where the chunk's state update then adds
 // k~^T v_new. It runs while the chunk's product reads buffer ts(j). With h_save the entry
-// state also goes to the backward's save from the same registers.
+// state also goes to the backward's save (bf16) from the same registers.
 __device__ __forceinline__ void chain_decay_into(const ChainParams& p, int c, int h, int v, int k0, uint32_t tl,
-                                                 int j, float g0, float* h_save) {
+                                                 int j, float g0, __nv_bfloat16* h_save) {
   float s[64];
   tmem_ld64(tl + ts(j) + k0, s);
   tmem_wait_ld_regs(s);
+  if (h_save) store_col64_bf16(h_save + (size_t(c) * p.H + h) * kD * kD + size_t(k0) * kD, s, v);
   if (p.kda) {
     const float4* gam = reinterpret_cast<const float4*>(p.gam + (size_t(c) * p.H + h) * kD + k0);
 #pragma unroll
     for (int e = 0; e < 16; ++e) {
       const float4 g4 = gam[e];
       float* x = s + 4 * e;
-      if (h_save) {
-        float* hs = h_save + (size_t(c) * p.H + h) * kD * kD + size_t(k0 + 4 * e) * kD + v;
-        hs[0] = x[0];
-        hs[kD] = x[1];
-        hs[2 * kD] = x[2];
-        hs[3 * kD] = x[3];
-      }
       x[0] *= g4.x;
       x[1] *= g4.y;
       x[2] *= g4.z;
       x[3] *= g4.w;
     }
   } else {
-    if (h_save) {
-      float* hs = h_save + (size_t(c) * p.H + h) * kD * kD + size_t(k0) * kD + v;
-#pragma unroll
-      for (int e = 0; e < 64; ++e) hs[size_t(e) * kD] = s[e];
-    }
 #pragma unroll
     for (int e = 0; e < 64; ++e) s[e] *= g0;
   }
@@ -215,7 +204,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float* sU = reinterpret_cast<const float*>(sm + kOffU);
     const int k0 = 64 * half;  // state columns handled by this thread
     const int t0 = 32 * half;  // token columns handled by this thread
-    float* h_save = outs ? p.h_save : nullptr;
+    __nv_bfloat16* h_save = outs ? p.h_save : nullptr;
     float* vnew_save = outs ? p.vnew_save : nullptr;
     __nv_bfloat16* o = outs ? p.o : nullptr;
     {
@@ -235,9 +224,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_arrive(&sready);
       if (h_save) {
         // the entry state of the first chunk, from the registers (identical to what was stored)
-        float* hs = h_save + (size_t(first) * H + h) * kD * kD + size_t(k0) * kD + v;
-#pragma unroll
-        for (int e = 0; e < 64; ++e) hs[size_t(e) * kD] = buf[e];
+        store_col64_bf16(h_save + (size_t(first) * H + h) * kD * kD + size_t(k0) * kD, buf, v);
       }
     }
     bool alive = true;

@@ -68,19 +68,14 @@ __device__ __forceinline__ void load_dO(const RevChainParams& p, int c, int h, i
 // dS' of chunk c (the gradient w.r.t. the state leaving it; buffer tm(j), which the step's
 // dv_new product reads as it is) times the chunk's decay gam, into buffer tm(j+1), where the
 // step's products then accumulate; this thread: lane v, state columns [k0, k0+64). With dh_save
-// the feature-major backward kernel's copy of dS' (rounded to tf32) is written from the same
-// registers.
-__device__ __forceinline__ void rev_decay_into(const RevChainParams& p, float* dh_save, int c, int h, int v, int k0,
+// the feature-major backward kernel's copy of dS' (bf16) is written from the same registers.
+__device__ __forceinline__ void rev_decay_into(const RevChainParams& p, __nv_bfloat16* dh_save, int c, int h, int v, int k0,
                                                uint32_t tl, int j, float g0) {
   const size_t tile = size_t(c) * p.H + h;
   float s[64];
   tmem_ld64(tl + tm(j) + k0, s);
   tmem_wait_ld_regs(s);
-  if (dh_save) {
-    float* ds = dh_save + tile * kD * kD + size_t(k0) * kD + v;
-#pragma unroll
-    for (int e = 0; e < 64; ++e) ds[size_t(e) * kD] = to_tf32(s[e]);
-  }
+  if (dh_save) store_col64_bf16(dh_save + tile * kD * kD + size_t(k0) * kD, s, v);
   if (p.kda) {
     const float4* gam = reinterpret_cast<const float4*>(p.gam + tile * kD + k0);
 #pragma unroll
@@ -219,7 +214,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int v = tid & 127, half = tid >> 7;
     const uint32_t tl = tb + tmem_lane_base(warp);
     const int k0 = 64 * half, t0 = 32 * half;
-    float* dh_save = outs ? p.dh_save : nullptr;
+    __nv_bfloat16* dh_save = outs ? p.dh_save : nullptr;
     float* dvn_save = outs ? p.dvn_save : nullptr;
     {
       // seed: dht, a composed segment seed, the identity (map M) or zero

@@ -28,7 +28,9 @@
  *
  * Dtypes. q, k, v, o, beta, dq, dk, dv, dbeta, dO: bf16 (passed as uint16 bit patterns).
  * g, dg, states, dht, dh0: fp32. Arithmetic: fp32 accumulation; tensor-core operands bf16
- * where they are exact input values, tf32 (round-to-nearest) elsewhere.
+ * where they are exact input values, tf32 (round-to-nearest) elsewhere, except the per-chunk
+ * copies of the state and of its gradient that the backward's feature-major products read,
+ * which are kept in bf16 (round-to-nearest).
  *
  * Ownership. Every pointer in the argument structs is a DEVICE pointer owned by the caller,
  * except cu_seqlens (HOST). The library never allocates or frees memory: the caller passes a
