@@ -240,10 +240,10 @@ Layout make_layout(const Problem& P, bool backward, bool kda = false) {
   if (backward) {
     L.dhs = take(2 * tiles * kD * kD);  // bf16
     L.dvns = take(4 * tiles * kTileW);
-    L.dQt = take(4 * tiles * kTileW);
-    L.dKt = take(4 * tiles * kTileW);
+    L.dQt = take(2 * tiles * kTileW);   // bf16
+    L.dKt = take(2 * tiles * kTileW);   // bf16
     L.dW = take(4 * tiles * kTileW);
-    L.dK1 = take(4 * tiles * kTileW);
+    L.dK1 = take(2 * tiles * kTileW);   // bf16
     L.dV1 = take(4 * tiles * kTileW);
     L.dgam = take(4 * tiles * kD);
     L.rE = take(scan_states);
@@ -667,6 +667,7 @@ int run_bwd(const gdn_desc_t* d, const gdn_bwd_args_t* a, void* stream, bool kda
     return fail(GDN_ECUDA, "cuTensorMapEncodeTiled failed");
   auto F = [&](size_t off) { return reinterpret_cast<float*>(sv + off); };
   auto R = [&](size_t off) { return reinterpret_cast<float*>(rs + off); };
+  auto H16 = [&](size_t off) { return reinterpret_cast<__nv_bfloat16*>(rs + off); };
   const ChunkEntry* chunks = reinterpret_cast<const ChunkEntry*>(sv + L.chunks);
   PrepParams pp{};
   ChainParams cp{};
@@ -719,7 +720,7 @@ int run_bwd(const gdn_desc_t* d, const gdn_bwd_args_t* a, void* stream, bool kda
   fp.dO = rp.dO;
   fp.A = F(L.A);
   fp.dvn = R(L.dvns);
-  fp.dQt = R(L.dQt); fp.dKt = R(L.dKt); fp.dW = R(L.dW); fp.dK1 = R(L.dK1); fp.dV1 = R(L.dV1);
+  fp.dQt = H16(L.dQt); fp.dKt = H16(L.dKt); fp.dW = R(L.dW); fp.dK1 = H16(L.dK1); fp.dV1 = R(L.dV1);
   fp.dgam = R(L.dgam);
   fp.sms = sm_count();
   fp.status = a->status;
@@ -735,7 +736,7 @@ int run_bwd(const gdn_desc_t* d, const gdn_bwd_args_t* a, void* stream, bool kda
   tp.dO = rp.dO;
   tp.A = F(L.A);
   tp.Gc = F(L.Gc); tp.rq = F(L.rq); tp.rk = F(L.rk); tp.beff = F(L.beff);
-  tp.dQt = R(L.dQt); tp.dKt = R(L.dKt); tp.dK1 = R(L.dK1); tp.dV1 = R(L.dV1);
+  tp.dQt = H16(L.dQt); tp.dKt = H16(L.dKt); tp.dK1 = H16(L.dK1); tp.dV1 = R(L.dV1);
   tp.gam = F(L.gam); tp.dgam = R(L.dgam);
   tp.dq = static_cast<__nv_bfloat16*>(a->dq);
   tp.dk = static_cast<__nv_bfloat16*>(a->dk);

@@ -54,20 +54,28 @@ constexpr size_t kTileW = size_t(kC) * kD;
 constexpr size_t kTileKtT = size_t(kD) * kC;
 constexpr size_t kTileAqk = size_t(kC) * kC;
 
-// Writes a thread's 64 fp32 values s[e] as bf16 into column v, rows 0..63, of a row-major
-// [rows][kD] bf16 tile at `base` (the state saves of the chain kernels, where lane v holds column
-// v). Lanes v and v ^ 1 (same warp, same rows) swap one value per row pair, so each store writes
-// two adjacent columns: the even lane the even rows, the odd lane the odd rows. Every lane of the
-// warp must take part.
-__device__ __forceinline__ void store_col64_bf16(__nv_bfloat16* base, const float* s, int v) {
+// Writes a thread's N fp32 values s[e] as bf16 into column v, rows 0..N-1, of a row-major
+// [rows][kD] bf16 tile at `base` (the chain kernels' state saves and the feature-major backward's
+// token-major results, where lane v holds column v). Lanes v and v ^ 1 (same warp, same rows)
+// swap one value per row pair, so each store writes two adjacent columns: the even lane the even
+// rows, the odd lane the odd rows. Every lane of the warp must take part.
+template <int N>
+__device__ __forceinline__ void store_col_bf16(__nv_bfloat16* base, const float* s, int v) {
   const int odd = v & 1;
   __nv_bfloat162* p = reinterpret_cast<__nv_bfloat162*>(base + (v & ~1));
 #pragma unroll
-  for (int e = 0; e < 64; e += 2) {
+  for (int e = 0; e < N; e += 2) {
     const float other = __shfl_xor_sync(0xffffffffu, odd ? s[e] : s[e + 1], 1);
     const __nv_bfloat162 pr = odd ? __floats2bfloat162_rn(other, s[e + 1]) : __floats2bfloat162_rn(s[e], other);
     p[size_t(e + odd) * (kD / 2)] = pr;
   }
+}
+
+// Four consecutive bf16 (8 bytes, 8-byte aligned) of read-only memory as fp32.
+__device__ __forceinline__ float4 ldg_bf16x4(const __nv_bfloat16* src) {
+  const uint2 u = __ldg(reinterpret_cast<const uint2*>(src));
+  return make_float4(__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xffff0000u),
+                     __uint_as_float(u.y << 16), __uint_as_float(u.y & 0xffff0000u));
 }
 
 // Segmented chain (chunk-parallel affine state scan). The chunk map of the chain is affine
@@ -197,7 +205,8 @@ struct BwdFeatParams {
   const __nv_bfloat16* dO;     // [R,H,V]
   const float* A;              // [NC,H,64,64]
   const float* dvn;            // [NC,H,64,V]
-  float *dQt, *dKt, *dW, *dK1, *dV1;  // [NC,H,64,128] token-major
+  __nv_bfloat16 *dQt, *dKt, *dK1;    // [NC,H,64,128] token-major, bf16
+  float *dW, *dV1;                    // [NC,H,64,128] token-major
   float* dgam;                 // [NC,H,128] (GDN: entry 0)
   int sms;                     // SM count (the distance to the next wave's CTA for prefetching)
   int* status;
@@ -213,7 +222,8 @@ struct BwdTokParams {
   const __nv_bfloat16* dO;     // [R,H,V]
   const float* A;              // [NC,H,64,64]
   const float *Gc, *rq, *rk, *beff;   // per token [NC,H,64]
-  const float *dQt, *dKt, *dK1, *dV1; // [NC,H,64,128]
+  const __nv_bfloat16 *dQt, *dKt, *dK1;  // [NC,H,64,128] token-major, bf16
+  const float* dV1;                      // [NC,H,64,128] token-major
   const float *gam, *dgam;     // [NC,H,128]
   __nv_bfloat16 *dq, *dk, *dv, *dbeta;
   float* dg;

@@ -17,7 +17,9 @@
 // operands in shared memory (v_new, dv_new by TMA). h and dh' arrive by TMA too (128-row boxes
 // of 64 bf16 columns, 128-byte swizzle: a thread's column half is one panel row), so each
 // thread reads its row from shared memory without bank conflicts. Results leave as token-major fp32 rows [t][f] (coalesced: the 128
-// threads of one token row write 512 contiguous bytes).
+// threads of one token row write 512 contiguous bytes; dQt, dKt and dK1, which only the
+// token-major backward's CUDA-core assembly reads, are bf16: 256 bytes per row, each store two
+// adjacent columns).
 // (An L2 prefetch of the next wave's inputs made the whole step slower: with the heads split
 // over two streams it competes with the other group's kernels.)
 #include "common.cuh"
@@ -187,9 +189,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // dQt and dKt: token-major rows
     tmem_ld32(tl + kTP1 + t0, r);
     tmem_wait_ld_regs(r);
-    float* dq = p.dQt + tile * kTileW + size_t(t0) * kD + f;
-#pragma unroll
-    for (int e = 0; e < 32; ++e) dq[size_t(e) * kD] = r[e];
+    store_col_bf16<32>(p.dQt + tile * kTileW + size_t(t0) * kD, r, f);
     // dW^T = -(h dv_new^T): saved token-major (tf32, an MMA operand later) and written back
     // to TMEM as the A operand of A^T dW.
     tmem_ld32(tl + kTP2 + t0, r);
@@ -229,9 +229,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     float r[32];
     tmem_ld32(tl + kTP3 + t0, r);
     tmem_wait_ld_regs(r);
-    float* dk = p.dKt + tile * kTileW + size_t(t0) * kD + f;
-#pragma unroll
-    for (int e = 0; e < 32; ++e) dk[size_t(e) * kD] = r[e];
+    store_col_bf16<32>(p.dKt + tile * kTileW + size_t(t0) * kD, r, f);
   }
   const bool ok2 = ok3 && mbar_wait(&bar_mma, 1, &abort_flag, p.status, kDevTimeoutMma);
   tc_fence_after();
@@ -240,9 +238,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     float r[32];
     tmem_ld32(tl + kTP5 + t0, r);
     tmem_wait_ld_regs(r);
-    float* k1 = p.dK1 + tile * kTileW + size_t(t0) * kD + f;
-#pragma unroll
-    for (int e = 0; e < 32; ++e) k1[size_t(e) * kD] = r[e];
+    store_col_bf16<32>(p.dK1 + tile * kTileW + size_t(t0) * kD, r, f);
     tmem_ld32(tl + kTH + 64 + t0, r);
     tmem_wait_ld_regs(r);
     float* v1 = p.dV1 + tile * kTileW + size_t(t0) * kD + f;

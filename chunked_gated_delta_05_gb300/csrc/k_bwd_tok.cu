@@ -116,9 +116,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     // inputs of the later phases: start their trip from HBM now
     const size_t rows = tile * kTileW;
     prefetch_l2(p.A + tile * kTileAqk, 4u * kTileAqk);
-    prefetch_l2(p.dQt + rows, 4u * kTileW);
-    prefetch_l2(p.dKt + rows, 4u * kTileW);
-    prefetch_l2(p.dK1 + rows, 4u * kTileW);
+    prefetch_l2(p.dQt + rows, 2u * kTileW);
+    prefetch_l2(p.dKt + rows, 2u * kTileW);
+    prefetch_l2(p.dK1 + rows, 2u * kTileW);
     prefetch_l2(p.dV1 + rows, 4u * kTileW);
   }
   if (tid < kC) {
@@ -404,7 +404,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   // ---- per-token assembly. Owner threads stage their rows of the two last products from
   // TMEM into padded shared rows; then each warp takes whole token rows (lane l: columns
-  // 4l..4l+3) with coalesced float4 loads of the fp32 intermediates and shuffle-reduced dots.
+  // 4l..4l+3) with coalesced loads of the intermediates (dV1 fp32; dQt, dKt, dK1 bf16) and
+  // shuffle-reduced dots.
   constexpr int kPad = 132;                                  // padded row stride (floats)
   float* sRq = reinterpret_cast<float*>(sm + kR1);           // [64][132]
   float* sRk = sRq + kC * kPad;                              // [64][132]
@@ -467,6 +468,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         f[4 * m] = x.x; f[4 * m + 1] = x.y; f[4 * m + 2] = x.z; f[4 * m + 3] = x.w;
       }
     };
+    auto load16h = [&](const __nv_bfloat16* src, bool v, float* f) {   // bf16 tiles, read-only
+#pragma unroll
+      for (int m = 0; m < 4; ++m) {
+        const float4 x = v ? ldg_bf16x4(src + 32 * m) : make_float4(0.f, 0.f, 0.f, 0.f);
+        f[4 * m] = x.x; f[4 * m + 1] = x.y; f[4 * m + 2] = x.z; f[4 * m + 3] = x.w;
+      }
+    };
     auto smem16 = [&](const float* src, float* f) {
 #pragma unroll
       for (int m = 0; m < 4; ++m) {
@@ -481,9 +489,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int tt = valid ? t : 0;
       const size_t ro = rowbase + size_t(tt) * kD + d0;
       float dqt[16], k1v[16], ktv[16], v1v[16];
-      load16(p.dQt + ro, valid, dqt);
-      load16(p.dK1 + ro, valid, k1v);
-      load16(p.dKt + ro, valid, ktv);
+      load16h(p.dQt + ro, valid, dqt);
+      load16h(p.dK1 + ro, valid, k1v);
+      load16h(p.dKt + ro, valid, ktv);
       load16(p.dV1 + ro, valid, v1v);
       const float Gt = s_G[tt], rqt = s_rq[tt], rkt = s_rk[tt], bt = s_b[tt];
       const float eG = expf(Gt), eL = expf(Glast - Gt);

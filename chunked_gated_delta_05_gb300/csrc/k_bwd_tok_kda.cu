@@ -141,9 +141,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     // trip from HBM now
     const size_t rows = tile * kTileW;
     prefetch_l2(p.A + tile * kTileAqk, 4u * kTileAqk);
-    prefetch_l2(p.dQt + rows, 4u * kTileW);
-    prefetch_l2(p.dKt + rows, 4u * kTileW);
-    prefetch_l2(p.dK1 + rows, 4u * kTileW);
+    prefetch_l2(p.dQt + rows, 2u * kTileW);
+    prefetch_l2(p.dKt + rows, 2u * kTileW);
+    prefetch_l2(p.dK1 + rows, 2u * kTileW);
     prefetch_l2(p.dV1 + rows, 4u * kTileW);
   }
   // G (scaled to log2 units) and dO as a 64-row tf32 operand; rows past the chunk are zero.
@@ -489,9 +489,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int e = 0; e < 4; ++e) glc4[e] = sG2[(len - 1) * kP + c4 + e];
     for (int t = warp; t < len; t += kThreads / 32) {
       const size_t o = rowbase + size_t(t) * kD + c4;
-      const float4 dqt4 = __ldg(reinterpret_cast<const float4*>(p.dQt + o));
-      const float4 dk14 = __ldg(reinterpret_cast<const float4*>(p.dK1 + o));
-      const float4 dkt4 = __ldg(reinterpret_cast<const float4*>(p.dKt + o));
+      const float4 dqt4 = ldg_bf16x4(p.dQt + o);
+      const float4 dk14 = ldg_bf16x4(p.dK1 + o);
+      const float4 dkt4 = ldg_bf16x4(p.dKt + o);
       const float4 dv14 = __ldg(reinterpret_cast<const float4*>(p.dV1 + o));
       const float dqt[4] = {dqt4.x, dqt4.y, dqt4.z, dqt4.w}, dk1[4] = {dk14.x, dk14.y, dk14.z, dk14.w};
       const float dkt[4] = {dkt4.x, dkt4.y, dkt4.z, dkt4.w}, dv1[4] = {dv14.x, dv14.y, dv14.z, dv14.w};

@@ -65,7 +65,7 @@ __device__ __forceinline__ void chain_decay_into(const ChainParams& p, int c, in
   float s[64];
   tmem_ld64(tl + ts(j) + k0, s);
   tmem_wait_ld_regs(s);
-  if (h_save) store_col64_bf16(h_save + (size_t(c) * p.H + h) * kD * kD + size_t(k0) * kD, s, v);
+  if (h_save) store_col_bf16<64>(h_save + (size_t(c) * p.H + h) * kD * kD + size_t(k0) * kD, s, v);
   if (p.kda) {
     const float4* gam = reinterpret_cast<const float4*>(p.gam + (size_t(c) * p.H + h) * kD + k0);
 #pragma unroll
@@ -224,7 +224,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_arrive(&sready);
       if (h_save) {
         // the entry state of the first chunk, from the registers (identical to what was stored)
-        store_col64_bf16(h_save + (size_t(first) * H + h) * kD * kD + size_t(k0) * kD, buf, v);
+        store_col_bf16<64>(h_save + (size_t(first) * H + h) * kD * kD + size_t(k0) * kD, buf, v);
       }
     }
     bool alive = true;

@@ -75,7 +75,7 @@ __device__ __forceinline__ void rev_decay_into(const RevChainParams& p, __nv_bfl
   float s[64];
   tmem_ld64(tl + tm(j) + k0, s);
   tmem_wait_ld_regs(s);
-  if (dh_save) store_col64_bf16(dh_save + tile * kD * kD + size_t(k0) * kD, s, v);
+  if (dh_save) store_col_bf16<64>(dh_save + tile * kD * kD + size_t(k0) * kD, s, v);
   if (p.kda) {
     const float4* gam = reinterpret_cast<const float4*>(p.gam + tile * kD + k0);
 #pragma unroll
