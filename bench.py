@@ -68,16 +68,16 @@ KERNEL_SOURCES_KDA = {**KERNEL_SOURCES, "prepare": "k_prep_kda.cu", "bwd_tok": "
 # each, all heads in one group). The chunk kernels' traffic is per chunk-head, so the
 # B=1 T=32768 H=16 entries are those bytes x 4 (8192 chunk-heads) and the B=1 T=8192 H=32 KDA
 # entries x 2 (4096); the chains' traffic depends on the segment plan and is not scaled.
-_GDN_T4096 = {"prepare": 616_121_344, "chain_fwd": 606_150_912, "compose": 29_377_024,
-              "chain_bwd": 582_243_328, "bwd_feat": 758_571_264, "bwd_tok": 731_689_216}
-_KDA_T4096 = {"prepare": 749_775_616, "chain_fwd": 604_277_504, "compose": 29_376_768,
-              "chain_bwd": 583_158_784, "bwd_feat": 757_906_176, "bwd_tok": 856_912_128}
-_HASHES = {("prepare", False): "c2916e6291b1f3fb", ("prepare", True): "c98c767d621466d5",
-           ("chain_fwd", False): "6ca5f5c74541d246", ("chain_fwd", True): "6ca5f5c74541d246",
-           ("compose", False): "2a8e76a5313bc45a", ("compose", True): "2a8e76a5313bc45a",
-           ("chain_bwd", False): "b22fa42ebd53fcf1", ("chain_bwd", True): "b22fa42ebd53fcf1",
-           ("bwd_feat", False): "caaf82205acec3c6", ("bwd_feat", True): "caaf82205acec3c6",
-           ("bwd_tok", False): "fe3ae544e3105534", ("bwd_tok", True): "ab1c2cd9cbc8111f"}
+_GDN_T4096 = {"prepare": 615_656_448, "chain_fwd": 548_957_184, "compose": 29_377_280,
+              "chain_bwd": 532_263_680, "bwd_feat": 527_159_040, "bwd_tok": 624_750_080}
+_KDA_T4096 = {"prepare": 749_953_280, "chain_fwd": 548_404_736, "compose": 29_380_352,
+              "chain_bwd": 533_579_520, "bwd_feat": 528_061_696, "bwd_tok": 750_161_408}
+_HASHES = {("prepare", False): "8c60c78a984d722d", ("prepare", True): "45ce61eefff8b141",
+           ("chain_fwd", False): "b67d2f0c67e5583f", ("chain_fwd", True): "b67d2f0c67e5583f",
+           ("compose", False): "63934c6fea906ff7", ("compose", True): "63934c6fea906ff7",
+           ("chain_bwd", False): "a56ac1d8c8c4bd41", ("chain_bwd", True): "a56ac1d8c8c4bd41",
+           ("bwd_feat", False): "33817ed548065fd7", ("bwd_feat", True): "33817ed548065fd7",
+           ("bwd_tok", False): "2cd204b4af6bc3cf", ("bwd_tok", True): "2e736338f16a5432"}
 NCU_TRAFFIC_BYTES = {}
 for _k, _v in _GDN_T4096.items():
     NCU_TRAFFIC_BYTES[(_k, "gdn_b2_t4096_h16")] = (_v, _HASHES[(_k, False)])
