@@ -432,11 +432,38 @@ class Runner:
         per_step = self.timed_regions(steps, min_seconds, run)
         self.check_status("during the end-to-end region")
         ms = statistics.median(per_step)
+
+        # The same copies with no compute: one step's inputs in and outputs out, concurrently on
+        # the two copy streams (the host link's floor for this region's per-step time).
+        def copies_only():
+            start = torch.cuda.Event(enable_timing=True)
+            end = torch.cuda.Event(enable_timing=True)
+            start.record(stream)
+            evs = []
+            for s, pairs in ((s_in, [(slots[0][k], v) for k, v in pinned_in.items() if isinstance(v, torch.Tensor)]),
+                             (s_out, [(dst, src) for src, dst in zip(outs_dev, pinned_out[0]) if src is not None])):
+                s.wait_event(start)
+                with torch.cuda.stream(s):
+                    for dst, src in pairs:
+                        dst.copy_(src, non_blocking=True)
+                    evs.append(torch.cuda.Event())
+                    evs[-1].record(s)
+            for ev in evs:
+                stream.wait_event(ev)
+            end.record(stream)
+            torch.cuda.synchronize(dev)
+            return start.elapsed_time(end)
+
+        copies_only()
+        copy_ms = statistics.median([copies_only() for _ in range(5)])
         return {"value": job_throughput(self.tokens, self.world, ms), "unit": "tokens/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": ms,
                 "repeats": len(per_step),
                 "copies": "pinned host buffers; inputs of step i+1 and outputs of step i-1 copied on two "
-                          "streams while step i computes"}
+                          "streams while step i computes",
+                "copies_only_ms_per_step": copy_ms,
+                "copies_only": "one step's host-to-device and device-to-host copies alone, both directions "
+                               "at once, no compute: the host link's floor for ms_per_step"}
 
 
 def roofline_of(runner, per_kernel, steps, peaks, peak_src):
