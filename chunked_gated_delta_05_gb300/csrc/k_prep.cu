@@ -72,7 +72,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __shared__ uint64_t bar_tma, bar_mma;
   __shared__ uint32_t tslot;
   __shared__ int abort_flag;
-  __shared__ float s_g[kRows], s_b[kRows], s_rk[kRows], s_G2[kRows];  // s_G2 = G log2(e)
+  __shared__ float s_g[kRows], s_rk[kRows], s_G2[kRows];  // s_G2 = G log2(e)
   __shared__ int4 s_chunk[2];
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -134,7 +134,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   if (hf == 0) {
     s_g[rt] = gi;
-    s_b[rt] = bi;
   }
   mbar_wait(&bar_tma, 0, &abort_flag, p.status, kDevTimeoutTma);
 
