@@ -29,7 +29,9 @@
 // A CTA runs one segment of a sequence's chunks in one of three modes (the segmented chain
 // of common.cuh): in full (from the true entry state, with the output and the backward
 // saves), or as the segment's affine map, from the identity with U = 0 (M) or from zero
-// (B), with no outputs and the output products, Qt and Aqk left out.
+// (B), with no outputs and the output products, Qt and Aqk left out. In M mode v_new = -P,
+// so the state update reads P from its accumulator with B negated (as the reverse chain
+// reads dv_new), and the chain warps' v_new pass leaves the serial path.
 #include "common.cuh"
 #include "umma.cuh"
 
@@ -93,7 +95,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const __grid_constant__ CUtensorMap mU, const ChainParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = align1k(smem_raw);
-  __shared__ uint64_t full1, full2, full3[2], mma1, mma2, mma3, sready, vready, oread;
+  __shared__ uint64_t full1, full1b, full2, full3[2], mma1, mma2, mma3, sready, vready, oread;
   __shared__ uint32_t tslot;
   __shared__ int abort_flag;
 
@@ -116,6 +118,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (tid == 0) {
     abort_flag = 0;
     mbar_init(&full1, 1);
+    mbar_init(&full1b, 1);
     mbar_init(&full2, 1);
     mbar_init(&full3[0], 1);
     mbar_init(&full3[1], 1);
@@ -157,12 +160,25 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (outs) tma_load_2d(base + 32768 + pp * 8192, &mAqk, pp * 32, (c * H + h) * kC, &full3[st]);
         }
       };
-      load_g1(first);
+      // M mode: W double-buffered in the rows Qt takes in full mode (full1 for even steps,
+      // full1b for odd ones), so each W copy has two steps to land
+      auto load_w = [&](int c, int b) {
+        uint64_t* bar = b ? &full1b : &full1;
+        mbar_expect_tx(bar, 32768u);
+        for (int pp = 0; pp < 4; ++pp) tma_load_2d(sm + kOffWQ + pp * 16384 + b * 8192, &mW, pp * 32, (c * H + h) * kC, bar);
+      };
+      if (mode == kRunMapM) {
+        load_w(first, 0);
+        if (nc > 1) load_w(first + 1, 1);
+      } else {
+        load_g1(first);
+      }
       if (use_u) load_g2(first);
       load_g3(first, 0);
       if (nc > 1) load_g3(first + 1, 1);
       const uint32_t id64 = idesc_tf32(128, 64), id128 = idesc_tf32(128, 128);
       const uint32_t id_first = outs ? id128 : id64;  // [P | O] or P alone
+      const uint32_t id128_negb = id128 | (1u << 14);   // B negated
       // the chain warps have written the entry state
       bool alive = mbar_wait(&sready, 0, &abort_flag, p.status, kDevTimeoutSync);
       for (int j = 0; j < nc && alive; ++j) {
@@ -170,6 +186,31 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int c = first + j, st = j & 1;
         const uint32_t tPV = tb + tpv(j), tO = tb + tout(j);
         const uint32_t sKtT = smem_u32(sm + kOffG3 + st * kG3Stage), sAqk = sKtT + 32768;
+        if (mode == kRunMapM) {
+          if (!mbar_wait(par ? &full1b : &full1, (j >> 1) & 1, &abort_flag, p.status, kDevTimeoutTma)) break;
+          // U = 0, so v_new = -P: the update reads the product's accumulator itself, with B
+          // negated, issued right behind it (the MMAs run in issue order), as the reverse chain
+          // does; the chain warps only decay the state
+          tc_fence_after();
+          for (int s = 0; s < 16; ++s)
+            mma_tf32_ts(tPV, tb + ts(j) + s * 8, desc_kmajor(sWQ + par * 8192, 16384, s), id64, s > 0);
+          mma_commit(&mma1);
+          if (j > 0) {
+            if (!mbar_wait(&mma3, par ^ 1u, &abort_flag, p.status, kDevTimeoutMma)) break;
+            if (j + 1 < nc) load_g3(c + 1, st ^ 1);
+          }
+          if (!mbar_wait(&full3[st], (j >> 1) & 1, &abort_flag, p.status, kDevTimeoutTma)) break;
+          if (!mbar_wait(&vready, par, &abort_flag, p.status, kDevTimeoutSync)) break;
+          tc_fence_after();
+          for (int s = 0; s < 8; ++s) mma_tf32_ts(tb + ts(j + 1), tPV + s * 8, desc_kmajor(sKtT, 16384, s), id128_negb, true);
+          mma_commit(&mma2);
+          mma_commit(&mma3);
+          // the product has read this buffer's W: the tile two chunks on may replace it
+          if (!mbar_wait(&mma1, par, &abort_flag, p.status, kDevTimeoutMma)) break;
+          if (j + 2 < nc) load_w(c + 2, par);
+          if (!mbar_wait(&mma2, par, &abort_flag, p.status, kDevTimeoutMma)) break;
+          continue;
+        }
         if (!mbar_wait(&full1, par, &abort_flag, p.status, kDevTimeoutTma)) break;
         // the product overwrites the output of chunk j - 2: the chain warps have read it
         if (outs && p.o && j >= 2 && !mbar_wait(&oread, par, &abort_flag, p.status, kDevTimeoutSync)) break;
@@ -261,6 +302,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       // the decayed state into the other buffer while this chunk's product reads the state (the
       // segment's first entry state was saved from the registers that wrote it)
       chain_decay_into(p, c, h, v, k0, tb + lb, j, g_cur, j > 0 ? h_save : nullptr);
+      if (mode == kRunMapM) {
+        // the update negates P itself: signal the decayed state only
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(&vready);
+        g_cur = g_next;
+        if (!mbar_wait(&mma2, par, &abort_flag, p.status, kDevTimeoutMma)) { alive = false; break; }
+        tc_fence_after();
+        continue;
+      }
       if (use_u && !mbar_wait(&full2, par, &abort_flag, p.status, kDevTimeoutTma)) { alive = false; break; }
       if (!mbar_wait(&mma1, par, &abort_flag, p.status, kDevTimeoutMma)) { alive = false; break; }
       // the previous chunk's intra-chunk output product was issued before this product
