@@ -68,12 +68,12 @@ KERNEL_SOURCES_KDA = {**KERNEL_SOURCES, "prepare": "k_prep_kda.cu", "bwd_tok": "
 # each, all heads in one group). The chunk kernels' traffic is per chunk-head, so the
 # B=1 T=32768 H=16 entries are those bytes x 4 (8192 chunk-heads) and the B=1 T=8192 H=32 KDA
 # entries x 2 (4096); the chains' traffic depends on the segment plan and is not scaled.
-_GDN_T4096 = {"prepare": 615_266_304, "chain_fwd": 548_717_056, "compose": 29_376_000,
-              "chain_bwd": 531_900_672, "bwd_feat": 526_976_768, "bwd_tok": 624_670_720}
-_KDA_T4096 = {"prepare": 749_953_280, "chain_fwd": 548_404_736, "compose": 29_380_352,
-              "chain_bwd": 533_579_520, "bwd_feat": 528_061_696, "bwd_tok": 750_161_408}
+_GDN_T4096 = {"prepare": 615_627_776, "chain_fwd": 545_890_048, "compose": 29_377_280,
+              "chain_bwd": 532_660_736, "bwd_feat": 527_221_504, "bwd_tok": 624_840_448}
+_KDA_T4096 = {"prepare": 750_086_912, "chain_fwd": 546_662_144, "compose": 29_376_768,
+              "chain_bwd": 533_866_240, "bwd_feat": 528_282_624, "bwd_tok": 750_107_392}
 _HASHES = {("prepare", False): "1e22db98a14704fb", ("prepare", True): "45ce61eefff8b141",
-           ("chain_fwd", False): "b67d2f0c67e5583f", ("chain_fwd", True): "b67d2f0c67e5583f",
+           ("chain_fwd", False): "e1bc39a93d6f554d", ("chain_fwd", True): "e1bc39a93d6f554d",
            ("compose", False): "63934c6fea906ff7", ("compose", True): "63934c6fea906ff7",
            ("chain_bwd", False): "a56ac1d8c8c4bd41", ("chain_bwd", True): "a56ac1d8c8c4bd41",
            ("bwd_feat", False): "33817ed548065fd7", ("bwd_feat", True): "33817ed548065fd7",
