@@ -90,6 +90,11 @@ __device__ __forceinline__ float4 ldg_bf16x4(const __nv_bfloat16* src) {
 // chunk count (maxS == 1) is the plain serial chain.
 enum RunMode : int { kRunFull = 0, kRunMapM = 1, kRunMapB = 2 };
 
+// Grids: the chain kernels launch (runs, heads of the group); the chunk kernels (prepare and
+// the two backward kernels) launch one flat dimension of chunk x heads with the head fastest,
+// so the CTAs in flight read whole token rows of the [T, H, 128] inputs and neighbouring
+// per-(chunk, head) tiles.
+
 struct SegPlan {
   int L;       // chunks per segment
   int maxS;    // most segments of any sequence (1 = plain chain)
@@ -127,7 +132,7 @@ struct PrepParams {
   const ChunkEntry* chunks;
   int NC, H;
   int dense_T;                 // tokens per sequence of a dense batch (chunk entries computed), 0 if packed
-  int hg0, hgn;                // head group: heads hg0 .. hg0 + hgn - 1 (grid.y = hgn)
+  int hg0, hgn;                // head group: heads hg0 .. hg0 + hgn - 1
   const float* g;              // GDN [R,H]; KDA [R,H,K]
   const __nv_bfloat16* beta;   // [R,H]
   float scale;
@@ -154,7 +159,7 @@ struct RevChainParams {
   const SeqEntry* seqs;
   const ChunkEntry* chunks;
   int N, H;
-  int hg0, hgn;                // head group: heads hg0 .. hg0 + hgn - 1 (grid.y = hgn)
+  int hg0, hgn;                // head group: heads hg0 .. hg0 + hgn - 1
   int kda;
   SegPlan sp;
   const float* gam;            // [NC,H,128]
@@ -170,7 +175,7 @@ struct ChainParams {
   const SeqEntry* seqs;
   const ChunkEntry* chunks;
   int N, H;
-  int hg0, hgn;                // head group: heads hg0 .. hg0 + hgn - 1 (grid.y = hgn)
+  int hg0, hgn;                // head group: heads hg0 .. hg0 + hgn - 1
   int kda;
   SegPlan sp;
   const float* gam;
@@ -199,7 +204,7 @@ struct BwdFeatParams {
   const ChunkEntry* chunks;
   int NC, H, kda;
   int dense_T;                 // tokens per sequence of a dense batch (chunk entries computed), 0 if packed
-  int hg0, hgn;                // head group: heads hg0 .. hg0 + hgn - 1 (grid.y = hgn)
+  int hg0, hgn;                // head group: heads hg0 .. hg0 + hgn - 1
   const __nv_bfloat16* h;      // [NC,H,K,V] state entering each chunk (bf16; read by TMA)
   const __nv_bfloat16* dh;     // [NC,H,K,V] gradient w.r.t. the state leaving each chunk (bf16; read by TMA)
   const __nv_bfloat16* dO;     // [R,H,V]
@@ -216,7 +221,7 @@ struct BwdTokParams {
   const ChunkEntry* chunks;
   int NC, H, kda;
   int dense_T;                 // tokens per sequence of a dense batch (chunk entries computed), 0 if packed
-  int hg0, hgn;                // head group: heads hg0 .. hg0 + hgn - 1 (grid.y = hgn)
+  int hg0, hgn;                // head group: heads hg0 .. hg0 + hgn - 1
   float scale;
   int beta_sigmoid, l2norm;
   const __nv_bfloat16* dO;     // [R,H,V]
@@ -286,7 +291,7 @@ struct GroupSumParams {
 struct ComposeParams {
   const SeqEntry* seqs;
   int N, H;
-  int hg0, hgn;                // head group: heads hg0 .. hg0 + hgn - 1 (grid.y = hgn)
+  int hg0, hgn;                // head group: heads hg0 .. hg0 + hgn - 1
   SegPlan sp;
   int* status;
 };

@@ -62,7 +62,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   __shared__ float s_dg[kThreads];
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int c = blockIdx.x, h = blockIdx.y + p.hg0, H = p.H;
+  // heads fastest: the CTAs in flight share token rows of dO and neighbouring tiles
+  const int c = int(blockIdx.x / p.hgn), h = int(blockIdx.x % p.hgn) + p.hg0, H = p.H;
   const size_t tile = size_t(c) * H + h;
   const int f = tid & 127, hf = tid >> 7;  // feature (TMEM lane) and column half
   const ChunkEntry ch = chunk_entry(p.chunks, c, p.dense_T);  // requested first: the dO load below waits on it
@@ -274,7 +275,7 @@ cudaError_t launch_bwd_feat(const CUtensorMap& mVN, const CUtensorMap& mDVN, con
     if (e != cudaSuccess) return e;
     attr = true;
   }
-  dim3 grid(p.NC, p.hgn);
+  dim3 grid(unsigned(p.NC) * unsigned(p.hgn));
   k_bwd_feat<<<grid, kThreads, kSmemBytes, s>>>(mVN, mDVN, mdO, mH, mDH, p);
   return cudaGetLastError();
 }

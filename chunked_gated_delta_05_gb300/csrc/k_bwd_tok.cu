@@ -77,7 +77,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   __shared__ float s_G[kC], s_G2[kC], s_rq[kC], s_rk[kC], s_b[kC], s_e1[kC], s_dG[kC], s_db[kC], s_P[kC][kC + 1];
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int c = blockIdx.x, h = blockIdx.y + p.hg0, H = p.H;
+  // heads fastest: the CTAs in flight share token rows of the inputs and gradients
+  const int c = int(blockIdx.x / p.hgn), h = int(blockIdx.x % p.hgn) + p.hg0, H = p.H;
   const size_t tile = size_t(c) * H + h;
   const ChunkEntry ch = chunk_entry(p.chunks, c, p.dense_T);
   const int len = ch.y;
@@ -622,7 +623,7 @@ cudaError_t launch_bwd_tok(const CUtensorMap& mq, const CUtensorMap& mk, const C
     if (e != cudaSuccess) return e;
     attr = true;
   }
-  dim3 grid(p.NC, p.hgn);
+  dim3 grid(unsigned(p.NC) * unsigned(p.hgn));
   k_bwd_tok<<<grid, kThreads, kSmemBytes, s>>>(mq, mk, mv, mdO, mVN, mDW, mDVN, p);
   return cudaGetLastError();
 }

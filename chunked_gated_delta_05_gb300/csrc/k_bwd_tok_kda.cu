@@ -92,7 +92,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int wq = warp & 3, half = warp >> 2;
-  const int c_idx = blockIdx.x, h = blockIdx.y + p.hg0, H = p.H;
+  // heads fastest: the CTAs in flight share token rows of the inputs and gradients
+  const int c_idx = int(blockIdx.x / p.hgn), h = int(blockIdx.x % p.hgn) + p.hg0, H = p.H;
   const size_t tile = size_t(c_idx) * H + h;
   const ChunkEntry ch = chunk_entry(p.chunks, c_idx, p.dense_T);
   const int len = ch.y;
@@ -602,7 +603,7 @@ cudaError_t launch_bwd_tok_kda(const CUtensorMap& mq, const CUtensorMap& mk, con
     if (e != cudaSuccess) return e;
     attr = true;
   }
-  dim3 grid(p.NC, p.hgn);
+  dim3 grid(unsigned(p.NC) * unsigned(p.hgn));
   k_bwd_tok_kda<<<grid, kThreads, kSmemBytes, s>>>(mq, mk, mv, mVN, mDW, mDVN, mdO, p);
   return cudaGetLastError();
 }

@@ -76,7 +76,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   __shared__ int4 s_chunk[2];
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int h = blockIdx.y + p.hg0, pair = blockIdx.x, H = p.H;
+  // heads fastest: the CTAs in flight share token rows of q, k, v and neighbouring tiles
+  const int h = int(blockIdx.x % p.hgn) + p.hg0, pair = int(blockIdx.x / p.hgn), H = p.H;
   // Row of the stacked tile (= TMEM lane) and column half of this thread.
   const int rt = tid & (kRows - 1), hf = tid >> 7;
   const int blk = rt >> 6, il = rt & 63;
@@ -406,7 +407,7 @@ cudaError_t launch_prep_gdn(const CUtensorMap& mq, const CUtensorMap& mk, const 
     if (e != cudaSuccess) return e;
     attr = true;
   }
-  dim3 grid((p.NC + 1) / 2, p.hgn);
+  dim3 grid(unsigned((p.NC + 1) / 2) * unsigned(p.hgn));
   k_prep_gdn<<<grid, kThreads, kSmemBytes, s>>>(mq, mk, mv, mQt, mKt, mAqk, mW, mU, p);
   return cudaGetLastError();
 }
