@@ -68,16 +68,16 @@ KERNEL_SOURCES_KDA = {**KERNEL_SOURCES, "prepare": "k_prep_kda.cu", "bwd_tok": "
 # each, all heads in one group). The chunk kernels' traffic is per chunk-head, so the
 # B=1 T=32768 H=16 entries are those bytes x 4 (8192 chunk-heads) and the B=1 T=8192 H=32 KDA
 # entries x 2 (4096); the chains' traffic depends on the segment plan and is not scaled.
-_GDN_T4096 = {"prepare": 615_627_776, "chain_fwd": 545_890_048, "compose": 29_377_280,
-              "chain_bwd": 532_660_736, "bwd_feat": 527_221_504, "bwd_tok": 624_840_448}
-_KDA_T4096 = {"prepare": 750_086_912, "chain_fwd": 546_662_144, "compose": 29_376_768,
-              "chain_bwd": 533_866_240, "bwd_feat": 528_282_624, "bwd_tok": 750_107_392}
-_HASHES = {("prepare", False): "1e22db98a14704fb", ("prepare", True): "45ce61eefff8b141",
-           ("chain_fwd", False): "e1bc39a93d6f554d", ("chain_fwd", True): "e1bc39a93d6f554d",
-           ("compose", False): "63934c6fea906ff7", ("compose", True): "63934c6fea906ff7",
-           ("chain_bwd", False): "a56ac1d8c8c4bd41", ("chain_bwd", True): "a56ac1d8c8c4bd41",
-           ("bwd_feat", False): "33817ed548065fd7", ("bwd_feat", True): "33817ed548065fd7",
-           ("bwd_tok", False): "2cd204b4af6bc3cf", ("bwd_tok", True): "2e736338f16a5432"}
+_GDN_T4096 = {"prepare": 611_470_336, "chain_fwd": 545_798_400, "compose": 29_376_000,
+              "chain_bwd": 532_253_440, "bwd_feat": 526_161_920, "bwd_tok": 623_438_592}
+_KDA_T4096 = {"prepare": 748_809_984, "chain_fwd": 548_044_800, "compose": 29_377_024,
+              "chain_bwd": 533_810_176, "bwd_feat": 526_905_344, "bwd_tok": 749_082_368}
+_HASHES = {("prepare", False): "9f4bd99a328245fe", ("prepare", True): "ef796d48524c2ad1",
+           ("chain_fwd", False): "ede9cdea014a4770", ("chain_fwd", True): "ede9cdea014a4770",
+           ("compose", False): "aee154a000cfde9f", ("compose", True): "aee154a000cfde9f",
+           ("chain_bwd", False): "9a792f73725d839b", ("chain_bwd", True): "9a792f73725d839b",
+           ("bwd_feat", False): "ca6dc5d5b6a21f11", ("bwd_feat", True): "ca6dc5d5b6a21f11",
+           ("bwd_tok", False): "e3d84be8a81a7d84", ("bwd_tok", True): "674c8996578b69be"}
 NCU_TRAFFIC_BYTES = {}
 for _k, _v in _GDN_T4096.items():
     NCU_TRAFFIC_BYTES[(_k, "gdn_b2_t4096_h16")] = (_v, _HASHES[(_k, False)])
